@@ -1,0 +1,321 @@
+"""CPU oracle for the block-diffusion denoising step (test infrastructure).
+
+This package is test infrastructure.  Only the tests, the smoke check and the
+CPU-baseline leg of the benchmark may import it; the device library never does.
+It wraps the plain double-precision C++ restatement in ``dg_oracle.cpp`` with
+ctypes and numpy marshalling.  The shared library is compiled on first use
+with the host C++ compiler (it builds the same on x86-64 and aarch64).
+"""
+from __future__ import annotations
+
+import ctypes as ct
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "dg_oracle.cpp")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD, "libdg_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle library (g++, -O2, no fast-math, no FP contraction)."""
+    os.makedirs(_BUILD, exist_ok=True)
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+        tmp = _LIB_PATH + f".{os.getpid()}.tmp"
+        cmd = ["g++", "-O2", "-std=c++17", "-fPIC", "-shared", "-pthread", "-ffp-contract=off",
+               "-fno-fast-math", _SRC, "-o", tmp]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+class Dims(ct.Structure):
+    _fields_ = [("V", ct.c_int32), ("d", ct.c_int32), ("C", ct.c_int32), ("B", ct.c_int32),
+                ("Hq", ct.c_int32), ("Hkv", ct.c_int32), ("hd", ct.c_int32), ("F", ct.c_int32),
+                ("P", ct.c_int32), ("cap", ct.c_int32), ("rope_base", ct.c_double),
+                ("rms_eps", ct.c_double), ("mirror_bf16", ct.c_int32)]
+
+
+_F = ct.POINTER(ct.c_float)
+_D = ct.POINTER(ct.c_double)
+_I = ct.POINTER(ct.c_int32)
+_U8 = ct.POINTER(ct.c_uint8)
+
+
+class StepIn(ct.Structure):
+    _fields_ = [("E", _F), ("Wq", _F), ("Wk", _F), ("Wv", _F), ("Wo", _F), ("W1", _F), ("W2", _F),
+                ("Kc", _F), ("Vc", _F), ("x", _I), ("z", _F), ("alpha", _F), ("prev_argmax", _I),
+                ("tau", ct.c_double), ("b", ct.c_double), ("stop_H", ct.c_double),
+                ("seed", ct.c_uint64), ("step", ct.c_int32), ("block", ct.c_int32)]
+
+
+class StepOut(ct.Structure):
+    _fields_ = [("a", _D), ("q", _D), ("k", _D), ("v", _D), ("o", _D), ("h", _D), ("logits", _D),
+                ("H", _D), ("m", _D), ("Z", _D), ("top2gap", _D), ("argmax", _I), ("accept", _U8),
+                ("cum", _D), ("rank", _I), ("renoise_tok", _I), ("sample_tok", _I),
+                ("gumbel_gap", _D), ("tokens_out", _I), ("u", _D), ("g", _D), ("z_out", _D),
+                ("n_acc", _I), ("meanH", _D), ("stop", _I)]
+
+
+def lib():
+    global _lib
+    with _lock:
+        if _lib is None:
+            L = ct.CDLL(build())
+            L.or_philox4x64_10.argtypes = [ct.POINTER(ct.c_uint64), ct.POINTER(ct.c_uint64),
+                                           ct.POINTER(ct.c_uint64)]
+            L.or_philox_word.argtypes = [ct.c_uint64, ct.c_int32, ct.c_int32, ct.c_int32, ct.c_int32,
+                                         ct.c_int64, ct.c_int32]
+            L.or_philox_word.restype = ct.c_uint64
+            L.or_uniform_token.argtypes = [ct.c_uint64, ct.c_int32]
+            L.or_uniform_token.restype = ct.c_int32
+            L.or_gumbel.argtypes = [ct.c_uint64]
+            L.or_gumbel.restype = ct.c_float
+            L.or_gumbel_argmax.argtypes = [_D, ct.c_int64, ct.c_uint64, ct.c_int32, ct.c_int32,
+                                           ct.c_int32, ct.c_int32, _D]
+            L.or_gumbel_argmax.restype = ct.c_int32
+            L.or_gumbel_argmax_many.argtypes = [_D, ct.c_int64, ct.c_uint64, ct.c_int32, _I]
+            L.or_uniform_many.argtypes = [ct.c_int32, ct.c_uint64, ct.c_int32, _I]
+            L.or_gumbel_many.argtypes = [ct.c_uint64, ct.c_int64, _F]
+            L.or_canvas_init.argtypes = [_I, ct.c_int32, ct.c_int32, ct.c_int32, ct.c_uint64, ct.c_int32]
+            L.or_rmsnorm.argtypes = [_D, ct.c_int32, ct.c_double, _D]
+            L.or_rope.argtypes = [_D, ct.c_int32, ct.c_double, ct.c_double]
+            L.or_gelu.argtypes = [ct.c_double]
+            L.or_gelu.restype = ct.c_double
+            L.or_row_stats.argtypes = [_D, ct.c_int64, ct.c_double, _D, _D, _D, _I, _D]
+            L.or_accept.argtypes = [_D, ct.c_int32, ct.c_double, _U8, _D, _I]
+            L.or_accept.restype = ct.c_int32
+            L.or_attend_row.argtypes = [_D, _F, _F, ct.c_int64, _D, _D, ct.c_int64, ct.c_int32, _D]
+            L.or_denoise_step.argtypes = [ct.POINTER(Dims), ct.POINTER(StepIn), ct.POINTER(StepOut),
+                                          _I, ct.c_int32, ct.c_int32]
+            L.or_denoise_canvas.argtypes = [ct.POINTER(Dims)] + [_F] * 9 + [
+                _I, _F, _F, ct.c_int32, ct.c_double, ct.c_double, ct.c_double, ct.c_double,
+                ct.c_uint64, ct.c_int32, _I, _I, _I, _I, ct.c_int32]
+            L.or_commit.argtypes = [ct.POINTER(Dims), _F, _F, _F, _I, _F, _F, ct.c_int32]
+            L.or_round_bf16.argtypes = [ct.c_double]
+            L.or_round_bf16.restype = ct.c_double
+            _lib = L
+    return _lib
+
+
+def _p(a, ctype):
+    if a is None:
+        return None
+    return a.ctypes.data_as(ctype)
+
+
+def _f32(a):
+    return np.ascontiguousarray(np.asarray(a, dtype=np.float32))
+
+
+def _i32(a):
+    return np.ascontiguousarray(np.asarray(a, dtype=np.int32))
+
+
+def default_threads() -> int:
+    return max(1, os.cpu_count() or 1)
+
+
+# ----------------------------------------------------------------- scalars --
+def philox4x64_10(ctr, key):
+    c = np.ascontiguousarray(np.asarray(ctr, dtype=np.uint64))
+    k = np.ascontiguousarray(np.asarray(key, dtype=np.uint64))
+    out = np.zeros(4, dtype=np.uint64)
+    lib().or_philox4x64_10(_p(c, ct.POINTER(ct.c_uint64)), _p(k, ct.POINTER(ct.c_uint64)),
+                           _p(out, ct.POINTER(ct.c_uint64)))
+    return out
+
+
+def philox_word(seed, block, step, batch, pos, v, stream) -> int:
+    return int(lib().or_philox_word(seed, block, step, batch, pos, v, stream))
+
+
+def uniform_token(w: int, V: int) -> int:
+    return int(lib().or_uniform_token(w, V))
+
+
+def gumbel(w: int) -> float:
+    return float(lib().or_gumbel(w))
+
+
+def gumbel_argmax(s, seed, block=0, step=0, batch=0, pos=0):
+    s = np.ascontiguousarray(np.asarray(s, dtype=np.float64))
+    gap = ct.c_double()
+    i = lib().or_gumbel_argmax(_p(s, _D), s.size, seed, block, step, batch, pos, ct.byref(gap))
+    return int(i), gap.value
+
+
+def gumbel_argmax_many(s, seed, npos):
+    s = np.ascontiguousarray(np.asarray(s, dtype=np.float64))
+    out = np.zeros(npos, dtype=np.int32)
+    lib().or_gumbel_argmax_many(_p(s, _D), s.size, seed, npos, _p(out, _I))
+    return out
+
+
+def uniform_many(V, seed, npos):
+    out = np.zeros(npos, dtype=np.int32)
+    lib().or_uniform_many(V, seed, npos, _p(out, _I))
+    return out
+
+
+def gumbel_many(seed, n):
+    out = np.zeros(n, dtype=np.float32)
+    lib().or_gumbel_many(seed, n, _p(out, _F))
+    return out
+
+
+def round_bf16(x: float) -> float:
+    return float(lib().or_round_bf16(x))
+
+
+def canvas_init(B, C, V, seed, block=0):
+    t = np.zeros((B, C), dtype=np.int32)
+    lib().or_canvas_init(_p(t, _I), B, C, V, seed, block)
+    return t
+
+
+# ---------------------------------------------------------- small pieces ----
+def rmsnorm(x, eps=1e-6):
+    x = np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+    y = np.zeros_like(x)
+    lib().or_rmsnorm(_p(x, _D), x.size, eps, _p(y, _D))
+    return y
+
+
+def rope(x, pos, base=10000.0):
+    y = np.ascontiguousarray(np.array(x, dtype=np.float64))
+    lib().or_rope(_p(y, _D), y.size, float(pos), float(base))
+    return y
+
+
+def gelu(x: float) -> float:
+    return float(lib().or_gelu(float(x)))
+
+
+def row_stats(logits, tau):
+    l = np.ascontiguousarray(np.asarray(logits, dtype=np.float64))
+    H, m, Z, g = (ct.c_double(), ct.c_double(), ct.c_double(), ct.c_double())
+    am = ct.c_int32()
+    lib().or_row_stats(_p(l, _D), l.size, float(tau), ct.byref(H), ct.byref(m), ct.byref(Z),
+                       ct.byref(am), ct.byref(g))
+    return dict(H=H.value, m=m.value, Z=Z.value, argmax=am.value, top2gap=g.value)
+
+
+def accept(H, b):
+    Hh = np.ascontiguousarray(np.asarray(H, dtype=np.float64))
+    C = Hh.size
+    acc = np.zeros(C, dtype=np.uint8)
+    cum = np.zeros(C, dtype=np.float64)
+    rank = np.zeros(C, dtype=np.int32)
+    n = lib().or_accept(_p(Hh, _D), C, float(b), _p(acc, _U8), _p(cum, _D), _p(rank, _I))
+    return dict(n=int(n), accept=acc.astype(bool), cum=cum, rank=rank)
+
+
+def attend_row(q, Kp, Vp, Kc, Vc):
+    q = np.ascontiguousarray(np.asarray(q, dtype=np.float64))
+    hd = q.size
+    Kp = _f32(Kp).reshape(-1, hd)
+    Vp = _f32(Vp).reshape(-1, hd)
+    Kc = np.ascontiguousarray(np.asarray(Kc, dtype=np.float64)).reshape(-1, hd)
+    Vc = np.ascontiguousarray(np.asarray(Vc, dtype=np.float64)).reshape(-1, hd)
+    o = np.zeros(hd, dtype=np.float64)
+    lib().or_attend_row(_p(q, _D), _p(Kp, _F), _p(Vp, _F), Kp.shape[0], _p(Kc, _D), _p(Vc, _D),
+                        Kc.shape[0], hd, _p(o, _D))
+    return o
+
+
+# ------------------------------------------------------------- the step -----
+def _dims(dims, mirror_bf16: bool, P=None):
+    return Dims(V=dims.V, d=dims.d, C=dims.C, B=dims.B, Hq=dims.Hq, Hkv=dims.Hkv, hd=dims.hd,
+                F=dims.F, P=dims.P if P is None else P, cap=dims.cap, rope_base=dims.rope_base,
+                rms_eps=dims.rms_eps, mirror_bf16=1 if mirror_bf16 else 0)
+
+
+_WANT_ALL = ("a", "q", "k", "v", "o", "h", "logits", "H", "m", "Z", "top2gap", "argmax", "accept",
+             "cum", "rank", "renoise_tok", "sample_tok", "gumbel_gap", "tokens_out", "u", "g",
+             "z_out", "n_acc", "meanH", "stop")
+
+
+def denoise_step(dims, w, x, z, alpha, tau, b, seed, step, block=0, prev_argmax=None,
+                 stop_H=0.005, mirror_bf16=True, rows=None, want=None, nthreads=None):
+    """Run one oracle denoising step.
+
+    dims: an object with V, d, C, B, Hq, Hkv, hd, F, P, cap, rope_base, rms_eps.
+    w: dict of float32 numpy arrays E, Wq, Wk, Wv, Wo, W1, W2, Kc, Vc.
+    x [B, C] int32, z [B, C, d] float32, alpha [B, C] float32.
+    rows: optional list of global rows (b * C + i) for the vocabulary stages.
+    want: names of outputs to return (default: everything except logits).
+    """
+    B, C, d, V, F = dims.B, dims.C, dims.d, dims.V, dims.F
+    M, nq, nkv = B * C, dims.Hq * dims.hd, dims.Hkv * dims.hd
+    if want is None:
+        want = tuple(n for n in _WANT_ALL if n != "logits")
+    shapes = dict(a=(M, d), q=(M, nq), k=(M, nkv), v=(M, nkv), o=(M, nq), h=(M, d), logits=(M, V),
+                  H=(M,), m=(M,), Z=(M,), top2gap=(M,), argmax=(M,), accept=(M,), cum=(M,),
+                  rank=(M,), renoise_tok=(M,), sample_tok=(M,), gumbel_gap=(M,), tokens_out=(M,),
+                  u=(M, d), g=(M, F), z_out=(M, d), n_acc=(B,), meanH=(B,), stop=(B,))
+    types = dict(argmax=np.int32, accept=np.uint8, rank=np.int32, renoise_tok=np.int32,
+                 sample_tok=np.int32, tokens_out=np.int32, n_acc=np.int32, stop=np.int32)
+    outs = {}
+    so = StepOut()
+    ctmap = {np.float64: _D, np.int32: _I, np.uint8: _U8}
+    for n in want:
+        t = types.get(n, np.float64)
+        arr = np.zeros(shapes[n], dtype=t)
+        outs[n] = arr
+        setattr(so, n, _p(arr, ctmap[t]))
+    keep = [_f32(w[k]) for k in ("E", "Wq", "Wk", "Wv", "Wo", "W1", "W2", "Kc", "Vc")]
+    xx, zz, aa = _i32(x), _f32(z), _f32(alpha)
+    pa = _i32(prev_argmax) if prev_argmax is not None else None
+    si = StepIn(*[_p(a, _F) for a in keep], _p(xx, _I), _p(zz, _F), _p(aa, _F),
+                _p(pa, _I) if pa is not None else None, float(tau), float(b), float(stop_H),
+                int(seed), int(step), int(block))
+    rr = _i32(rows) if rows is not None else None
+    D = _dims(dims, mirror_bf16)
+    rc = lib().or_denoise_step(ct.byref(D), ct.byref(si), ct.byref(so),
+                               _p(rr, _I) if rr is not None else None,
+                               0 if rr is None else rr.size, nthreads or default_threads())
+    if rc != 0:
+        raise ValueError("oracle denoise_step: bad arguments")
+    if "accept" in outs:
+        outs["accept"] = outs["accept"].astype(bool)
+    return outs
+
+
+def denoise_canvas(dims, w, x0, alpha, seed, N=48, tau0=0.8, tau1=0.4, b=0.1, stop_H=0.005,
+                   block=0, z0=None, mirror_bf16=True, nthreads=None):
+    B, C, d = dims.B, dims.C, dims.d
+    x = _i32(x0).copy().reshape(B, C)
+    z = _f32(np.zeros((B, C, d)) if z0 is None else z0).copy()
+    al = _f32(alpha)
+    keep = [_f32(w[k]) for k in ("E", "Wq", "Wk", "Wv", "Wo", "W1", "W2", "Kc", "Vc")]
+    steps = np.zeros(B, dtype=np.int32)
+    conv = np.zeros(B, dtype=np.int32)
+    acc = np.zeros((B, N), dtype=np.int32)
+    xhat = np.zeros((B, C), dtype=np.int32)
+    D = _dims(dims, mirror_bf16)
+    rc = lib().or_denoise_canvas(ct.byref(D), *[_p(a, _F) for a in keep], _p(x, _I), _p(z, _F),
+                                 _p(al, _F), N, tau0, tau1, b, stop_H, int(seed), int(block),
+                                 _p(steps, _I), _p(conv, _I), _p(acc, _I), _p(xhat, _I),
+                                 nthreads or default_threads())
+    if rc != 0:
+        raise ValueError("oracle denoise_canvas: bad arguments")
+    return dict(tokens=x, z=z, steps_taken=steps, converged=conv, accepted=acc, xhat0=xhat)
+
+
+def commit(dims, E, Wk, Wv, tokens, Kc, Vc, P, mirror_bf16=True, nthreads=None):
+    """Append the re-encoded K/V of `tokens` [B, C] at rows P..P+C-1; returns new (Kc, Vc)."""
+    Kc = _f32(Kc).copy()
+    Vc = _f32(Vc).copy()
+    D = _dims(dims, mirror_bf16, P=P)
+    rc = lib().or_commit(ct.byref(D), _p(_f32(E), _F), _p(_f32(Wk), _F), _p(_f32(Wv), _F),
+                         _p(_i32(tokens), _I), _p(Kc, _F), _p(Vc, _F), nthreads or default_threads())
+    if rc != 0:
+        raise ValueError("oracle commit: cache capacity exceeded")
+    return Kc, Vc

@@ -1,0 +1,467 @@
+"""Pins of the CPU oracle against what the pages and the mathematics fix.
+
+Each test checks the oracle against something other than itself: published
+known answers, closed forms, invariants, library routines that the operation
+reduces to in a special case, or brute force on tiny inputs.
+"""
+import itertools
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from block_diffusion_text_gb300 import synth
+
+pytestmark = pytest.mark.filterwarnings("ignore::DeprecationWarning")
+
+
+# --------------------------------------------------------------- Philox -----
+def _kat(golden_dir):
+    rows = []
+    with open(os.path.join(golden_dir, "philox4x64_10_kat.txt")) as f:
+        for line in f:
+            if line.startswith("#") or not line.strip():
+                continue
+            w = [int(t, 16) for t in line.split()]
+            rows.append((w[0:4], w[4:6], w[6:10]))
+    return rows
+
+
+def test_philox_known_answers(golden_dir):
+    rows = _kat(golden_dir)
+    assert len(rows) == 3
+    for ctr, key, want in rows:
+        got = [int(x) for x in oracle.philox4x64_10(ctr, key)]
+        assert got == want
+
+
+def test_philox_matches_numpy():
+    # numpy's Philox (4x64, 10 rounds) bumps its 256-bit counter before each
+    # block, so the block of counter c is produced from state c - 1.
+    rng = np.random.default_rng(123)
+    for _ in range(200):
+        ctr = [int(x) for x in rng.integers(0, 2**64, size=4, dtype=np.uint64)]
+        key = [int(x) for x in rng.integers(0, 2**64, size=2, dtype=np.uint64)]
+        c = (sum(w << (64 * i) for i, w in enumerate(ctr)) - 1) % (1 << 256)
+        cw = np.array([(c >> (64 * i)) & (2**64 - 1) for i in range(4)], dtype=np.uint64)
+        want = np.random.Philox(key=np.array(key, dtype=np.uint64), counter=cw).random_raw(4)
+        got = oracle.philox4x64_10(ctr, key)
+        assert [int(x) for x in got] == [int(x) for x in want]
+
+
+def test_philox_word_streams_differ():
+    a = oracle.philox_word(5, 0, 3, 0, 7, 0, 0)
+    b = oracle.philox_word(5, 0, 3, 0, 7, 0, 1)
+    c = oracle.philox_word(5, 0, 4, 0, 7, 0, 1)
+    d = oracle.philox_word(5, 1, 3, 0, 7, 0, 1)
+    assert len({a, b, c, d}) == 4
+    # four consecutive vocabulary indices share one Philox block
+    blk = oracle.philox4x64_10([1, 7, (0 << 32) | 3, (0 << 32) | 0], [5, 0])
+    for v in range(4, 8):
+        assert oracle.philox_word(5, 0, 3, 0, 7, v, 0) == int(blk[v & 3])
+
+
+# ------------------------------------------------------- uniform tokens -----
+def test_uniform_token_exact_high_word():
+    rng = np.random.default_rng(1)
+    for _ in range(1000):
+        w = int(rng.integers(0, 2**64, dtype=np.uint64))
+        V = int(rng.integers(1, 2**31 - 1))
+        assert oracle.uniform_token(w, V) == (w * V) >> 64
+    assert oracle.uniform_token(2**64 - 1, 262144) == 262143
+    assert oracle.uniform_token(0, 262144) == 0
+
+
+def test_uniform_tokens_chi_square():
+    from scipy import stats
+    V, n = 512, 400_000
+    t = oracle.uniform_many(V, 11, n)
+    assert t.min() >= 0 and t.max() < V
+    counts = np.bincount(t, minlength=V)
+    chi2 = ((counts - n / V) ** 2 / (n / V)).sum()
+    p = stats.chi2.sf(chi2, V - 1)
+    assert p > 1e-4, (chi2, p)
+
+
+def test_canvas_init_in_range_and_seeded():
+    a = oracle.canvas_init(2, 64, 1000, seed=3, block=0)
+    b = oracle.canvas_init(2, 64, 1000, seed=3, block=1)
+    assert a.min() >= 0 and a.max() < 1000
+    assert not np.array_equal(a, b)
+    assert np.array_equal(a, oracle.canvas_init(2, 64, 1000, seed=3, block=0))
+
+
+# ---------------------------------------------------------------- Gumbel ----
+def test_gumbel_moments():
+    g = oracle.gumbel_many(3, 1_000_000).astype(np.float64)
+    assert np.isfinite(g).all()
+    assert abs(g.mean() - 0.5772156649) < 5e-3          # Euler-Mascheroni constant
+    assert abs(g.var() - math.pi ** 2 / 6) < 2e-2
+    assert g.min() >= -2.82 and g.max() <= 16.7
+
+
+def test_gumbel_max_law():
+    # argmax(s + G) is distributed as softmax(s) (the Gumbel-max trick).
+    from scipy import stats
+    s = np.array([0.0, 1.0, -0.5, 2.0, 0.3, -1.0, 1.5, 0.7])
+    n = 200_000
+    t = oracle.gumbel_argmax_many(s, 9, n)
+    p = np.exp(s - s.max())
+    p /= p.sum()
+    counts = np.bincount(t, minlength=s.size)
+    chi2 = ((counts - n * p) ** 2 / (n * p)).sum()
+    assert stats.chi2.sf(chi2, s.size - 1) > 1e-4, (counts, n * p)
+
+
+def test_gumbel_argmax_of_one_hot_row():
+    s = np.full(1000, -1e4)
+    s[417] = 0.0
+    i, gap = oracle.gumbel_argmax(s, seed=1, pos=3)
+    assert i == 417 and gap > 1e3
+
+
+# ---------------------------------------------------------- bf16 rounding ---
+def test_round_bf16_matches_torch():
+    rng = np.random.default_rng(0)
+    x = np.concatenate([rng.standard_normal(5000).astype(np.float32),
+                        (rng.standard_normal(1000) * 1e-30).astype(np.float32),
+                        (rng.standard_normal(1000) * 1e30).astype(np.float32)])
+    want = torch.from_numpy(x).to(torch.bfloat16).to(torch.float64).numpy()
+    got = np.array([oracle.round_bf16(float(v)) for v in x])
+    assert np.array_equal(got, want)
+    # ties go to even
+    assert oracle.round_bf16(1.0 + 2 ** -8) == 1.0
+    assert oracle.round_bf16(1.0 + 3 * 2 ** -8) == 1.0 + 2 ** -6
+
+
+# ------------------------------------------------------------- RMSNorm ------
+def test_rmsnorm_unit_rms_and_scale_invariance():
+    rng = np.random.default_rng(2)
+    x = rng.standard_normal(1024) * 3.0
+    y = oracle.rmsnorm(x, 1e-6)
+    ms = np.mean(x * x)
+    assert abs(np.sqrt(np.mean(y * y)) - np.sqrt(ms / (ms + 1e-6))) < 1e-12
+    y2 = oracle.rmsnorm(5.0 * x, 0.0)
+    assert np.allclose(y2, oracle.rmsnorm(x, 0.0), rtol=1e-13, atol=0)
+    ref = torch.nn.functional.rms_norm(torch.from_numpy(x), (1024,), eps=1e-6).numpy()
+    assert np.allclose(y, ref, rtol=1e-12, atol=1e-14)
+
+
+# ---------------------------------------------------------------- RoPE ------
+def test_rope_complex_form_and_norm():
+    rng = np.random.default_rng(3)
+    hd = 32
+    x = rng.standard_normal(hd)
+    pos = 123.0
+    y = oracle.rope(x, pos, 10000.0)
+    # complex form: (x_j + i x_{j+hd/2}) * exp(i pos base^(-2j/hd))
+    zc = (x[: hd // 2] + 1j * x[hd // 2:]) * np.exp(1j * pos * 10000.0 ** (-2.0 * np.arange(hd // 2) / hd))
+    assert np.allclose(y, np.concatenate([zc.real, zc.imag]), rtol=0, atol=1e-12)
+    assert abs(np.linalg.norm(y) - np.linalg.norm(x)) < 1e-12
+    assert np.array_equal(oracle.rope(x, 0.0, 10000.0), x)
+
+
+def test_rope_relative_position():
+    rng = np.random.default_rng(4)
+    q, k = rng.standard_normal(64), rng.standard_normal(64)
+    d1 = oracle.rope(q, 1000.0, 10000.0) @ oracle.rope(k, 990.0, 10000.0)
+    d2 = oracle.rope(q, 20.0, 10000.0) @ oracle.rope(k, 10.0, 10000.0)
+    assert abs(d1 - d2) < 1e-10
+
+
+# ---------------------------------------------------------------- GELU ------
+def test_gelu_matches_torch():
+    xs = np.linspace(-6, 6, 241)
+    want = torch.nn.functional.gelu(torch.from_numpy(xs), approximate="none").numpy()
+    got = np.array([oracle.gelu(v) for v in xs])
+    assert np.allclose(got, want, rtol=1e-14, atol=1e-15)
+
+
+# ------------------------------------------------------------- entropy ------
+def test_entropy_uniform_row_is_log_v():
+    for V in (512, 32768):
+        st = oracle.row_stats(np.full(V, 0.37), 0.8)
+        assert abs(st["H"] - math.log(V)) < 1e-12
+        assert st["argmax"] == 0
+
+
+def test_entropy_two_level_closed_form():
+    V, tau = 512, 0.8
+    for a in (0.5, 3.0, 20.0, 80.0):
+        l = np.zeros(V)
+        l[7] = a * tau  # s = l / tau puts one logit at a and V-1 at 0
+        Z = math.exp(a) + V - 1
+        want = math.log(Z) - a * math.exp(a) / Z
+        st = oracle.row_stats(l, tau)
+        assert abs(st["H"] - want) < 1e-12
+        assert st["argmax"] == 7
+
+
+def test_entropy_matches_scipy_and_bounds():
+    from scipy import special, stats
+    rng = np.random.default_rng(5)
+    for tau in (0.8, 0.4):
+        l = rng.standard_normal(4096) * 4.0
+        st = oracle.row_stats(l, tau)
+        p = special.softmax(l / tau)
+        assert abs(st["H"] - stats.entropy(p)) < 1e-10
+        assert 0.0 <= st["H"] <= math.log(l.size)
+        assert st["argmax"] == int(np.argmax(l))
+        assert abs(st["m"] - l.max() / tau) < 1e-12
+        # temperature enters only through l / tau
+        st2 = oracle.row_stats(l / tau, 1.0)
+        assert abs(st2["H"] - st["H"]) < 1e-12
+
+
+# ---------------------------------------------------------- acceptance ------
+def test_accept_bruteforce_max_cardinality():
+    # Accepting the smallest entropies first maximises how many positions fit
+    # in the budget; brute force over every subset confirms the count, and the
+    # accepted set is the sorted prefix of that size.
+    rng = np.random.default_rng(6)
+    for trial in range(300):
+        C = int(rng.integers(1, 11))
+        H = rng.exponential(0.04, size=C)
+        if trial % 5 == 0:
+            H[rng.integers(0, C)] = H[rng.integers(0, C)]  # ties
+        b = 0.1
+        best = 0
+        for r in range(C + 1):
+            for S in itertools.combinations(range(C), r):
+                if sum(H[list(S)]) <= b + 1e-15:
+                    best = max(best, r)
+        res = oracle.accept(H, b)
+        assert res["n"] == best
+        order = sorted(range(C), key=lambda i: (H[i], i))
+        assert set(np.nonzero(res["accept"])[0]) == set(order[: res["n"]])
+        if res["n"] < C:
+            assert H[res["accept"]].sum() + H[order[res["n"]]] > b
+
+
+def test_accept_edge_cases():
+    assert oracle.accept([0.2, 0.3, math.log(512)], 0.1)["n"] == 0          # H_min > b
+    assert oracle.accept([0.01, 0.02, 0.03], 0.1)["n"] == 3                 # sum <= b
+    r = oracle.accept([0.05, 0.05], 0.1)                                    # sum == b
+    assert r["n"] == 2
+    r = oracle.accept([0.06, 0.06, 0.06], 0.1)                              # equal, ties by index
+    assert list(r["accept"]) == [True, False, False]
+    r = oracle.accept(np.full(16, math.log(512)), 0.1)                      # uniform rows
+    assert r["n"] == 0
+
+
+# ---------------------------------------------------------- attention -------
+def test_attention_matches_sdpa():
+    rng = np.random.default_rng(7)
+    hd = 16
+    for P, C in ((8, 4), (0, 5), (33, 1)):
+        q = rng.standard_normal(hd)
+        Kp, Vp = rng.standard_normal((P, hd)), rng.standard_normal((P, hd))
+        Kc, Vc = rng.standard_normal((C, hd)), rng.standard_normal((C, hd))
+        Kp32, Vp32 = Kp.astype(np.float32), Vp.astype(np.float32)
+        o = oracle.attend_row(q, Kp32, Vp32, Kc, Vc)
+        K = torch.from_numpy(np.concatenate([Kp32.astype(np.float64), Kc]))
+        Vv = torch.from_numpy(np.concatenate([Vp32.astype(np.float64), Vc]))
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            torch.from_numpy(q)[None, None, None], K[None, None], Vv[None, None])[0, 0, 0].numpy()
+        assert np.allclose(o, ref, rtol=1e-12, atol=1e-12)
+
+
+# ------------------------------------------------------ the whole step ------
+TINY = synth.workload("tiny_v512_c16")[0]
+
+
+def _tiny_inputs(dtype=torch.float32, alpha=None, seed=0, dims=TINY):
+    w = synth.to_numpy_f32(synth.make_weights(dims, seed, dtype=dtype))
+    x, z, a = synth.make_canvas(dims, seed, dtype=dtype)
+    if alpha is not None:
+        a = torch.full_like(a, alpha)
+    return w, x.numpy(), z.to(torch.float32).numpy(), a.numpy()
+
+
+def _torch_forward(dims, w, x, z, mirror):
+    """Independent float64 composition of library routines for a1..a4."""
+    f = lambda k: torch.from_numpy(w[k]).double()
+    rb = (lambda t: t.to(torch.bfloat16).double()) if mirror else (lambda t: t)
+    B, C, d, Hq, Hkv, hd, P = dims.B, dims.C, dims.d, dims.Hq, dims.Hkv, dims.hd, dims.P
+    e = f("E")[torch.from_numpy(x).long()] + torch.from_numpy(z).double()
+    a = rb(torch.nn.functional.rms_norm(e, (d,), eps=dims.rms_eps))
+    q = (a @ f("Wq").T).view(B, C, Hq, hd).transpose(1, 2)
+    k = (a @ f("Wk").T).view(B, C, Hkv, hd).transpose(1, 2)
+    v = rb((a @ f("Wv").T).view(B, C, Hkv, hd).transpose(1, 2))
+    pos = torch.arange(P, P + C, dtype=torch.float64)
+    ang = pos[:, None] * dims.rope_base ** (-2.0 * torch.arange(hd // 2, dtype=torch.float64) / hd)
+    rot = torch.polar(torch.ones_like(ang), ang)
+
+    def rope(t):
+        c = torch.complex(t[..., : hd // 2], t[..., hd // 2:]) * rot
+        return torch.cat([c.real, c.imag], -1)
+
+    q, k = rb(rope(q)), rb(rope(k))
+    Kall = torch.cat([f("Kc")[:, :, :P], k], 2)
+    Vall = torch.cat([f("Vc")[:, :, :P], v], 2)
+    rep = Hq // Hkv
+    o = torch.nn.functional.scaled_dot_product_attention(
+        q, Kall.repeat_interleave(rep, 1), Vall.repeat_interleave(rep, 1))
+    o = rb(o.transpose(1, 2).reshape(B, C, Hq * hd))
+    h = rb(a + o @ f("Wo").T)
+    return a.reshape(B * C, d), o.reshape(B * C, -1), h.reshape(B * C, d)
+
+
+@pytest.mark.parametrize("mirror", [False, True])
+def test_step_forward_matches_library_composition(mirror):
+    dtype = torch.bfloat16 if mirror else torch.float32
+    w, x, z, a = _tiny_inputs(dtype)
+    out = oracle.denoise_step(TINY, w, x, z, a, tau=0.8, b=0.1, seed=0, step=0,
+                              mirror_bf16=mirror, want=("a", "o", "h"), nthreads=2)
+    ra, ro, rh = _torch_forward(TINY, w, x, z, mirror)
+    tol = 1e-10 if not mirror else 1e-2  # bf16 mirrors may flip one ulp at a rounding edge
+    assert np.allclose(out["a"], ra.numpy(), rtol=0, atol=tol)
+    assert np.allclose(out["o"], ro.numpy(), rtol=0, atol=tol)
+    assert np.allclose(out["h"], rh.numpy(), rtol=0, atol=tol * 4)
+    if mirror:
+        assert np.mean(np.abs(out["h"] - rh.numpy()) > 0) < 0.01
+
+
+def test_step_vocab_stages_match_library_composition():
+    from scipy import special, stats
+    w, x, z, a = _tiny_inputs(torch.float32, seed=1)
+    tau = 0.6
+    out = oracle.denoise_step(TINY, w, x, z, a, tau=tau, b=0.1, seed=4, step=2, mirror_bf16=False,
+                              want=("h", "logits", "H", "argmax", "u", "g", "z_out"), nthreads=2)
+    h = out["h"]
+    l = a.reshape(-1, 1) * (h @ w["E"].astype(np.float64).T) / math.sqrt(TINY.d)
+    assert np.allclose(out["logits"], l, rtol=1e-12, atol=1e-12)
+    p = special.softmax(l / tau, axis=1)
+    assert np.allclose(out["H"], stats.entropy(p, axis=1), atol=1e-10)
+    assert np.array_equal(out["argmax"], np.argmax(l, axis=1))
+    u = p @ w["E"].astype(np.float64)
+    assert np.allclose(out["u"], u, atol=1e-12)
+    g = torch.nn.functional.gelu(torch.from_numpy(u) @ torch.from_numpy(w["W1"]).double().T).numpy()
+    assert np.allclose(out["g"], g, atol=1e-12)
+    assert np.allclose(out["z_out"], g @ w["W2"].astype(np.float64).T, atol=1e-12)
+
+
+def test_step_sampler_invariants():
+    w, x, z, a = _tiny_inputs(torch.bfloat16, seed=2)
+    out = oracle.denoise_step(TINY, w, x, z, a, tau=0.8, b=0.1, seed=9, step=3, nthreads=2)
+    H, acc = out["H"], out["accept"]
+    order = sorted(range(TINY.C), key=lambda i: (H[i], i))
+    n = int(out["n_acc"][0])
+    assert n == acc.sum()
+    assert set(np.nonzero(acc)[0]) == set(order[:n])
+    assert H[acc].sum() <= 0.1
+    if n < TINY.C:
+        assert H[acc].sum() + H[order[n]] > 0.1
+    for i in range(TINY.C):
+        want = out["sample_tok"][i] if acc[i] else out["renoise_tok"][i]
+        assert out["tokens_out"][i] == want
+        assert out["renoise_tok"][i] == oracle.uniform_token(
+            oracle.philox_word(9, 0, 3, 0, i, 0, 1), TINY.V)
+    assert abs(out["meanH"][0] - H.mean()) < 1e-12
+
+
+def test_step_uniform_logits_accept_nothing():
+    # alpha -> 0 makes every logit row uniform: H = log V > b, nothing accepted.
+    w, x, z, a = _tiny_inputs(torch.float32, alpha=1e-12)
+    out = oracle.denoise_step(TINY, w, x, z, a, tau=0.8, b=0.1, seed=0, step=0, mirror_bf16=False)
+    assert np.allclose(out["H"], math.log(TINY.V), atol=1e-9)
+    assert out["n_acc"][0] == 0 and not out["accept"].any()
+    assert abs(out["meanH"][0] - math.log(TINY.V)) < 1e-9
+    # and u is the mean embedding row
+    assert np.allclose(out["u"], w["E"].astype(np.float64).mean(0)[None], atol=1e-9)
+
+
+def test_step_one_hot_p0_gives_embedding_row():
+    # very sharp logits make p0 one-hot, so p0 . E is the row of E at the argmax.
+    w, x, z, a = _tiny_inputs(torch.float32, alpha=1e5)
+    out = oracle.denoise_step(TINY, w, x, z, a, tau=0.4, b=0.1, seed=0, step=0, mirror_bf16=False)
+    E = w["E"].astype(np.float64)
+    assert np.allclose(out["u"], E[out["argmax"]], rtol=0, atol=1e-6)
+    assert np.all(out["H"] < 1e-6)
+    # every position fits in the budget and samples its argmax
+    assert out["accept"].all()
+    assert np.array_equal(out["tokens_out"], out["argmax"])
+
+
+def test_rows_mode_agrees_with_full_mode():
+    w, x, z, a = _tiny_inputs(torch.bfloat16, seed=3)
+    full = oracle.denoise_step(TINY, w, x, z, a, tau=0.7, b=0.1, seed=1, step=1, nthreads=3)
+    rows = [0, 5, 15]
+    part = oracle.denoise_step(TINY, w, x, z, a, tau=0.7, b=0.1, seed=1, step=1, rows=rows,
+                               want=("H", "argmax", "sample_tok", "z_out"), nthreads=1)
+    for r in rows:
+        assert part["H"][r] == full["H"][r]
+        assert part["argmax"][r] == full["argmax"][r]
+        assert part["sample_tok"][r] == full["sample_tok"][r]
+        assert np.array_equal(part["z_out"][r], full["z_out"][r])
+
+
+def test_thread_count_bit_identical():
+    w, x, z, a = _tiny_inputs(torch.bfloat16, seed=4)
+    r1 = oracle.denoise_step(TINY, w, x, z, a, tau=0.8, b=0.1, seed=2, step=0, nthreads=1)
+    r4 = oracle.denoise_step(TINY, w, x, z, a, tau=0.8, b=0.1, seed=2, step=0, nthreads=4)
+    for k in r1:
+        assert np.array_equal(r1[k], r4[k]), k
+
+
+# -------------------------------------------------------- loop and commit ---
+def test_loop_sharp_alpha_stops_at_step_one(golden_dir):
+    # With alpha = 64 every row is confident: all positions are accepted, the
+    # argmax repeats, mean entropy is below the threshold, and the stop test
+    # fires at the first step where it can (step index 1).
+    w, x, z, a = _tiny_inputs(torch.bfloat16, alpha=64.0, seed=5)
+    r = oracle.denoise_canvas(TINY, w, x, a, seed=5, N=48)
+    assert r["converged"][0] == 1
+    assert r["steps_taken"][0] == 2
+    assert r["accepted"][0, 0] == TINY.C and r["accepted"][0, 2] == -1
+
+
+def test_loop_matches_manual_steps_with_linear_anneal(golden_dir):
+    table = {}
+    with open(os.path.join(golden_dir, "sampler_table2.txt")) as f:
+        for line in f:
+            if line.strip() and not line.startswith("#"):
+                k, v = line.split()
+                table[k] = float(v)
+    N = 4
+    tau0, tau1 = table["tau_start"], table["tau_end"]
+    w, x, z, a = _tiny_inputs(torch.bfloat16, seed=6)
+    loop = oracle.denoise_canvas(TINY, w, x, a, seed=8, N=N, tau0=tau0, tau1=tau1,
+                                 b=table["entropy_budget"], stop_H=table["stop_mean_entropy"])
+    taus = [tau0 + (tau1 - tau0) * s / (N - 1) for s in range(N)]
+    assert taus[0] == 0.8 and abs(taus[-1] - 0.4) < 1e-15
+    xx, zz, prev = x.copy(), z.copy(), None
+    for s in range(N):
+        o = oracle.denoise_step(TINY, w, xx, zz, a, tau=taus[s], b=0.1, seed=8, step=s,
+                                prev_argmax=prev)
+        xx = o["tokens_out"].reshape(x.shape)
+        zz = o["z_out"].astype(np.float32).reshape(z.shape)
+        prev = o["argmax"].reshape(x.shape)
+        assert loop["accepted"][0, s] == o["n_acc"][0]
+    assert loop["steps_taken"][0] == N and loop["converged"][0] == 0
+    assert np.array_equal(loop["tokens"], xx)
+    assert np.array_equal(loop["xhat0"], prev)
+
+
+def test_commit_appends_reencoded_kv():
+    dims = synth.Dims(V=512, d=64, C=16, B=2, Hq=2, Hkv=1, hd=32, F=128, P=32, cap=64)
+    w = synth.to_numpy_f32(synth.make_weights(dims, 3, dtype=torch.float32))
+    toks = np.random.default_rng(0).integers(0, 512, size=(2, 16)).astype(np.int32)
+    Kc, Vc = oracle.commit(dims, w["E"], w["Wk"], w["Wv"], toks, w["Kc"], w["Vc"], P=32,
+                           mirror_bf16=False)
+    assert np.array_equal(Kc[:, :, :32], w["Kc"][:, :, :32])
+    assert np.all(Kc[:, :, 48:] == 0)
+    a = torch.nn.functional.rms_norm(torch.from_numpy(w["E"]).double()[torch.from_numpy(toks).long()],
+                                     (64,), eps=1e-6)
+    k = (a @ torch.from_numpy(w["Wk"]).double().T).numpy()
+    v = (a @ torch.from_numpy(w["Wv"]).double().T).numpy()
+    for bb in range(2):
+        for i in range(16):
+            kr = oracle.rope(k[bb, i], 32 + i, 10000.0)
+            assert np.allclose(Kc[bb, 0, 32 + i], kr, atol=1e-6)
+            assert np.allclose(Vc[bb, 0, 32 + i], v[bb, i], atol=1e-6)
+    with pytest.raises(ValueError):
+        oracle.commit(dims, w["E"], w["Wk"], w["Wv"], toks, w["Kc"], w["Vc"], P=60)
