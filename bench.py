@@ -1,0 +1,432 @@
+#!/usr/bin/env python
+"""Denoise steps/s of one uniform-state denoising step over a 256-token canvas
+(V = 262144, d = 2816, prefix 8192, 16 q / 8 kv heads) on one GB300, with the
+roofline of its dominant kernel.
+
+One timed "step" is one pass of the whole hot path over the canvas: embedding +
+RMSNorm, q/k/v + RoPE, attention over prefix + canvas, output projection, LM
+head with softmax statistics, entropy-bounded accept / renoise with the stop
+test, p0 . E with Gumbel-max sampling, and the self-conditioning FFW.  The
+temperature follows the 48-step schedule (step s uses tau_{s mod 48}); the
+canvas state carries over from step to step as in the real loop.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs an independent replica on its own GPU
+(no data-path collective); the value is the steps of all ranks divided by the
+slowest rank's time.  --impl reference times the CPU oracle on the host cores
+instead (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from block_diffusion_text_gb300 import synth  # noqa: E402
+
+METRIC = "denoise steps/s (C=256, V=262144)"
+UNIT = "denoise steps/s"
+DEFAULT_WORKLOAD = "loop_v262k_c256_p8k"
+
+
+def _args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=("ours", "reference"))
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1 and not torch.distributed.is_initialized():
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        torch.distributed.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def _barrier(world):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def _max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    dev = "cuda" if torch.distributed.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return dict(hbm=float(p["hbm_gbs"]), tc=float(p["bf16_tflops"]),
+                    tc_sustained=float(p.get("bf16_tflops_sustained", p["bf16_tflops"])), src="measured")
+    except Exception:
+        return dict(hbm=6800.0, tc=1900.0, tc_sustained=1700.0, src="fallback")
+
+
+# ---------------------------------------------------------------- clocks --
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.samples = []
+        self.proc = None
+        try:
+            uuid = "GPU-" + str(torch.cuda.get_device_properties(device_index).uuid)
+        except Exception:
+            uuid = str(device_index)
+        self.cmd = ["nvidia-smi", f"--id={uuid}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                    "-lms", "200"]
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(self.cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 8:
+                self.samples.append(parts)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(s[0]) for s in self.samples if num(s[0]) is not None]
+        mx = [num(s[1]) for s in self.samples if num(s[1]) is not None]
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        reasons = sorted({n for s in self.samples for n, v in zip(names, s[4:8]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(self.samples)}
+
+
+# ------------------------------------------------------- algorithmic work --
+def kernel_work(d: synth.Dims):
+    """Algorithmic FLOPs and HBM bytes per launch of the dominant kernels."""
+    M, V, D = d.B * d.C, d.V, d.d
+    NT = math.ceil(V / 256)
+    T = d.P + d.C
+    lm_flops = 2.0 * M * V * D
+    lm_bytes = 2.0 * V * D + 2.0 * M * D + 2.0 * M * V + 20.0 * NT * M + 4.0 * M
+    sc_flops = 2.0 * M * V * D
+    sc_bytes = 2.0 * V * D + 2.0 * M * V + 4.0 * NT * M
+    at_flops = 4.0 * d.B * d.Hq * d.C * T * d.hd
+    at_bytes = 2.0 * 2 * d.B * d.Hkv * T * d.hd + 2.0 * 2 * M * d.Hq * d.hd
+    return {"lmhead": (lm_flops, lm_bytes), "selfcond": (sc_flops, sc_bytes), "attn": (at_flops, at_bytes)}
+
+
+def _traffic(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, if it still matches the source."""
+    try:
+        import hashlib
+        with open(os.path.join(ROOT, "profiles", "ncu_traffic.json")) as f:
+            t = json.load(f)
+        e = t.get(kernel)
+        if not e:
+            return None
+        src = os.path.join(ROOT, e["source"])
+        with open(src, "rb") as f:
+            if hashlib.sha256(f.read()).hexdigest() != e["source_sha256"]:
+                return None
+        return float(e["bytes_per_launch_full_size"])
+    except Exception:
+        return None
+
+
+# ------------------------------------------------------------ CPU oracle --
+def oracle_sample(dims, w_np, x, z, a, nthreads):
+    """Time the oracle on a bounded sample of one step; returns (steps/s estimate, detail)."""
+    import numpy as np
+    import oracle
+    rows = list(range(min(nthreads, dims.B * dims.C)))
+    t0 = time.perf_counter()
+    oracle.denoise_step(dims, w_np, x, z, a, tau=0.8, b=0.1, seed=0, step=0, rows=[],
+                        want=("H",), nthreads=nthreads)
+    t_front = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    oracle.denoise_step(dims, w_np, x, z, a, tau=0.8, b=0.1, seed=0, step=0, rows=rows,
+                        want=("H", "z_out"), nthreads=nthreads)
+    t_all = time.perf_counter() - t0
+    per_rows = max(t_all - t_front, 1e-9)
+    t_step = t_front + per_rows * (dims.B * dims.C) / len(rows)
+    del np
+    return 1.0 / t_step, dict(t_front_s=round(t_front, 3), t_rows_s=round(per_rows, 3), rows=len(rows),
+                              t_step_est_s=round(t_step, 2))
+
+
+def _oracle_inputs_from(w, x, z, a):
+    wn = synth.to_numpy_f32(w)
+    return wn, x.cpu().numpy(), z.float().cpu().numpy(), a.cpu().numpy()
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    dims, seed = synth.workload(args.workload)
+    nthreads = os.cpu_count() or 1
+    w = synth.make_weights(dims, seed, device="cpu")
+    x, z, a = synth.make_canvas(dims, seed, device="cpu")
+    wn, xn, zn, an = _oracle_inputs_from(w, x, z, a)
+    del w
+    import oracle
+    rows = list(range(min(nthreads, dims.M)))
+    t0 = time.perf_counter()
+    oracle.denoise_step(dims, wn, xn, zn, an, tau=0.8, b=0.1, seed=seed, step=0, rows=[], want=("H",),
+                        nthreads=nthreads)
+    t_front = time.perf_counter() - t0
+    ests = []
+    taus = [0.8 + (0.4 - 0.8) * s / 47 for s in range(48)]
+    for s in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        oracle.denoise_step(dims, wn, xn, zn, an, tau=taus[s % 48], b=0.1, seed=seed, step=s % 48, rows=rows,
+                            want=("H", "z_out"), nthreads=nthreads)
+        t = time.perf_counter() - t0
+        if s >= args.warmup:
+            ests.append(t_front + max(t - t_front, 1e-9) * dims.M / len(rows))
+    t_step = statistics.mean(ests)
+    value = 1.0 / t_step
+    sample = (f"per step: the oracle's attention front (a..h) for all {dims.M} rows once, then the "
+              f"vocabulary stages for {len(rows)} of {dims.M} rows, scaled to the full canvas")
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": t_step * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "impl": "reference",
+            "config": _config(dims, args.workload),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": nthreads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def _config(dims, name):
+    return {"workload": name, "V": dims.V, "d": dims.d, "C": dims.C, "B": dims.B, "P": dims.P,
+            "Hq": dims.Hq, "Hkv": dims.Hkv, "hd": dims.hd, "F": dims.F, "tau": "0.8->0.4 over 48 steps",
+            "b": 0.1, "l2": f"inputs larger than L2 (E alone is {2 * dims.V * dims.d / 1e9:.2f} GB)"}
+
+
+# ------------------------------------------------------------- our path ---
+def run_ours(args, world, rank, local):
+    from block_diffusion_text_gb300 import dg
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    dims, seed = synth.workload(args.workload)
+    w = synth.make_weights(dims, seed, device=dev)
+    x, z, a = synth.make_canvas(dims, seed, device=dev)
+    x0, z0 = x.clone(), z.clone()
+    model = dg.Model(dims, w)
+    canvas = dg.Canvas(x, z, a)
+    taus = dg.tau_schedule(48)
+    outbuf = None
+    slots = dg.PROF_SLOTS
+    timed_slots = ("attn", "lmhead", "selfcond")
+
+    def step(s, events=None):
+        nonlocal outbuf
+        outbuf = dg.denoise_step(model, canvas, tau=taus[s % 48], b=0.1, seed=seed, step=s % 48,
+                                 out=outbuf, events=events)
+
+    stream = torch.cuda.current_stream()
+    for s in range(args.warmup):
+        step(s)
+    torch.cuda.synchronize()
+    if model.status() != 0:
+        raise RuntimeError("device status word set during warm-up")
+
+    # per-kernel events of the timed steps (recorded once so that the handles exist)
+    ev = []
+    for _ in range(args.steps):
+        row = [None] * (2 * len(slots))
+        for name in timed_slots:
+            k = slots.index(name)
+            for e in (0, 1):
+                t = torch.cuda.Event(enable_timing=True)
+                t.record(stream)
+                row[2 * k + e] = t
+        ev.append(row)
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(local)
+    _barrier(world)
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for s in range(args.steps):
+        step(args.warmup + s, events=ev[s])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    _barrier(world)
+    clk = clocks.stop()
+    elapsed_ms = t0.elapsed_time(t1)
+    if model.status() != 0:
+        raise RuntimeError("device status word set during the timed steps")
+    per_kernel = {}
+    for name in timed_slots:
+        k = slots.index(name)
+        per_kernel[name] = statistics.mean(ev[s][2 * k].elapsed_time(ev[s][2 * k + 1]) for s in range(args.steps))
+    max_ms = _max_over_ranks(elapsed_ms, world)
+    value = world * args.steps / (max_ms / 1e3)
+
+    # end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        hx = x0.cpu().pin_memory()
+        hz = z0.cpu().pin_memory()
+        ha = a.cpu().pin_memory()
+        ox = torch.empty_like(hx).pin_memory()
+        oz = torch.empty_like(hz).pin_memory()
+        oh = torch.empty(dims.B, dims.C, dtype=torch.float32).pin_memory()
+        oa = torch.empty(dims.B, dims.C, dtype=torch.uint8).pin_memory()
+        h2d = hx.numel() * 4 + hz.numel() * 2 + ha.numel() * 4
+        d2h = ox.numel() * 4 + oz.numel() * 2 + oh.numel() * 4 + oa.numel()
+        ksteps = min(args.steps, 50)
+
+        def e2e_step(s):
+            canvas.tokens.copy_(hx, non_blocking=True)
+            canvas.z.copy_(hz, non_blocking=True)
+            canvas.alpha.copy_(ha, non_blocking=True)
+            out = dg.denoise_step(model, canvas, tau=taus[s % 48], b=0.1, seed=seed, step=s % 48, out=outbuf)
+            ox.copy_(canvas.tokens, non_blocking=True)
+            oz.copy_(canvas.z, non_blocking=True)
+            oh.copy_(out["entropy"], non_blocking=True)
+            oa.copy_(out["accept"], non_blocking=True)
+            torch.cuda.current_stream().synchronize()
+            hx.copy_(ox)
+            hz.copy_(oz)
+
+        for s in range(3):
+            e2e_step(s)
+        _barrier(world)
+        torch.cuda.synchronize()
+        tt = time.perf_counter()
+        for s in range(ksteps):
+            e2e_step(s)
+        torch.cuda.synchronize()
+        e_s = _max_over_ranks(time.perf_counter() - tt, world)
+        e2e = {"value": world * ksteps / e_s, "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "steps": ksteps}
+
+    # roofline of the dominant kernel
+    peaks = _peaks()
+    work = kernel_work(dims)
+    dominant = max(("lmhead", "selfcond"), key=lambda k: per_kernel[k])
+    rl = {}
+    for name in timed_slots:
+        fl, by = work[name]
+        sec = per_kernel[name] / 1e3
+        t_tc = fl / (peaks["tc_sustained"] * 1e12)
+        t_hbm = by / (peaks["hbm"] * 1e9)
+        bound = "tensor" if t_tc >= t_hbm else "hbm"
+        if bound == "tensor":
+            ach, peak, unit = fl / sec / 1e12, peaks["tc_sustained"], "TFLOP/s"
+        else:
+            ach, peak, unit = by / sec / 1e9, peaks["hbm"], "GB/s"
+        rl[name] = {"bound": bound, "achieved": ach, "peak": peak, "unit": unit, "frac": ach / peak,
+                    "traffic": _traffic(name), "ms": per_kernel[name],
+                    "tflops": fl / sec / 1e12, "gbs": by / sec / 1e9,
+                    "peak_note": ("of measured" if peaks["src"] == "measured" else "of fallback")
+                    + (" sustained bf16" if bound == "tensor" else " HBM copy")}
+    dom = rl[dominant]
+
+    launches_per_step = 11
+    from block_diffusion_text_gb300.dg import load  # noqa: F401
+    ns = _attn_splits(dims)
+    if ns > 1:
+        launches_per_step += 1
+
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": max_ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": _config(dims, args.workload),
+            "canvas_tokens_per_s": value * dims.B * dims.C,
+            "roofline": {"bound": dom["bound"], "achieved": dom["achieved"], "peak": dom["peak"],
+                         "unit": dom["unit"], "frac": dom["frac"], "traffic": dom["traffic"],
+                         "kernel": dominant, "peak_note": dom["peak_note"]},
+            "kernels": rl,
+            "clocks": clk,
+            "e2e": e2e,
+            "gpu_launches": launches_per_step * args.steps}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        try:
+            nthreads = os.cpu_count() or 1
+            wn, xn, zn, an = _oracle_inputs_from(w, x0, z0, a)
+            v, det = oracle_sample(dims, wn, xn, zn, an, nthreads)
+            line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": nthreads, "kind": "oracle",
+                                    "sample": (f"a..h for all {dims.M} rows, vocabulary stages for "
+                                               f"{det['rows']} rows, scaled to one step"), **det}
+        except Exception as e:  # the baseline is reported, not required
+            line["cpu_baseline"] = {"value": None, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+                                    "sample": f"failed: {e!r}"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def _attn_splits(dims):
+    units = math.ceil(dims.C / 64) * dims.B * dims.Hq
+    T = dims.P + dims.C
+    ns = min(math.ceil(3 * 152 / units), math.ceil(T / 256), 64)
+    ns = max(ns, 1)
+    kps = math.ceil(math.ceil(T / ns) / 64) * 64
+    return math.ceil(T / kps)
+
+
+def main():
+    args = _args()
+    world, rank, local = _dist()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_ours(args, world, rank, local)
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,278 @@
+// Bidirectional grouped-query attention of the canvas queries over the
+// static prefix cache followed by the canvas keys, with no mask
+// ("DiffusionGemma" docs chapter, attention-mask list: the current canvas is
+// a full bidirectional matrix and it reads the prompt / finished-block KV
+// cache; "DiffusionGemma explained", denoising mode).
+//
+// Flash-style: each CTA owns 64 query rows of one (canvas, query head) and one
+// contiguous chunk of the key sequence; K/V blocks of 64 keys are streamed
+// through shared memory with cp.async double buffering, scores and P.V use
+// the warp-level MMA, the softmax is online in base 2.  Scores use bf16 q, k;
+// the probabilities enter P.V as f16 (V re-encoded from bf16 to f16, exact in
+// the f16 range), which keeps their rounding 8x below bf16's.  With several
+// chunks per row the CTAs write unnormalised partials that a combine kernel
+// merges with their (max, sum).
+#include <cfloat>
+
+#include "dg_common.cuh"
+#include "dg_internal.h"
+
+namespace dg {
+
+template <int HD>
+DG_DEV int swz(int r, int c) {
+  if constexpr (HD >= 64) return c ^ (r & 7);
+  else return c ^ ((r >> 1) & 3);
+}
+
+template <int HD>
+__global__ void __launch_bounds__(128)
+    attn_kernel(AttnArgs a, int nqt, int nsplit, int kps, float scale_log2, StopCtl ctl) {
+  if (all_stopped(ctl.stop_at, ctl.B, ctl.step)) return;
+  constexpr int CH = HD / 8;  // 16-byte chunks per row
+  extern __shared__ uint8_t smem_raw[];
+  __nv_bfloat16* sQ = reinterpret_cast<__nv_bfloat16*>(smem_raw);
+  __nv_bfloat16* sK = sQ + kAttnRows * HD;  // [2][64][HD]
+  __nv_bfloat16* sV = sK + 2 * kAttnKeys * HD;
+
+  const int split = blockIdx.x / nqt, qt = blockIdx.x % nqt;
+  const int b = blockIdx.y / a.Hq, h = blockIdx.y % a.Hq;
+  const int g = h / (a.Hq / a.Hkv);
+  const int T = a.P + a.C;
+  const int k_begin = split * kps;
+  const int k_end = min(T, k_begin + kps);
+  const int q0 = qt * kAttnRows;
+  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+
+  const __nv_bfloat16* Q = reinterpret_cast<const __nv_bfloat16*>(a.q) + ((size_t)b * a.Hq + h) * a.C * HD;
+  const __nv_bfloat16* Kp = reinterpret_cast<const __nv_bfloat16*>(a.Kp) + ((size_t)b * a.Hkv + g) * a.cap * HD;
+  const __nv_bfloat16* Vp = reinterpret_cast<const __nv_bfloat16*>(a.Vp) + ((size_t)b * a.Hkv + g) * a.cap * HD;
+  const __nv_bfloat16* Kc = reinterpret_cast<const __nv_bfloat16*>(a.kc) + ((size_t)b * a.Hkv + g) * a.C * HD;
+  const __nv_bfloat16* Vc = reinterpret_cast<const __nv_bfloat16*>(a.vc) + ((size_t)b * a.Hkv + g) * a.C * HD;
+
+  for (int idx = tid; idx < kAttnRows * CH; idx += 128) {
+    const int r = idx / CH, c = idx % CH;
+    const bool ok = q0 + r < a.C;
+    cp_async16(sQ + r * HD + swz<HD>(r, c) * 8, Q + (size_t)(ok ? q0 + r : 0) * HD + c * 8, ok);
+  }
+  cp_async_commit();
+
+  auto load_kv = [&](int blk, int buf) {
+    const int kb0 = k_begin + blk * kAttnKeys;
+    for (int idx = tid; idx < kAttnKeys * CH; idx += 128) {
+      const int r = idx / CH, c = idx % CH;
+      const int j = kb0 + r;
+      const bool ok = j < k_end;
+      const __nv_bfloat16 *ks, *vs;
+      if (!ok) {
+        ks = Kc;
+        vs = Vc;
+      } else if (j < a.P) {
+        ks = Kp + (size_t)j * HD;
+        vs = Vp + (size_t)j * HD;
+      } else {
+        ks = Kc + (size_t)(j - a.P) * HD;
+        vs = Vc + (size_t)(j - a.P) * HD;
+      }
+      const int so = buf * kAttnKeys * HD + r * HD + swz<HD>(r, c) * 8;
+      cp_async16(sK + so, ks + c * 8, ok);
+      cp_async16(sV + so, vs + c * 8, ok);
+    }
+    cp_async_commit();
+  };
+
+  const int nblk = (k_end - k_begin + kAttnKeys - 1) / kAttnKeys;
+  load_kv(0, 0);
+  cp_async_wait<1>();
+  __syncthreads();
+
+  uint32_t qa[HD / 16][4];
+#pragma unroll
+  for (int ks = 0; ks < HD / 16; ++ks) {
+    const int mat = lane / 8;
+    const int r = warp * 16 + (mat % 2) * 8 + lane % 8;
+    const int c = ks * 2 + mat / 2;
+    ldmatrix_x4(qa[ks], sQ + r * HD + swz<HD>(r, c) * 8);
+  }
+
+  float o[HD / 8][4];
+#pragma unroll
+  for (int n = 0; n < HD / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+  float m_run[2] = {-FLT_MAX, -FLT_MAX}, l_run[2] = {0.f, 0.f};
+  const int tq = lane % 4;
+
+  for (int blk = 0; blk < nblk; ++blk) {
+    const int buf = blk & 1;
+    if (blk + 1 < nblk) load_kv(blk + 1, buf ^ 1);
+    else cp_async_commit();
+    cp_async_wait<1>();
+    __syncthreads();
+    const __nv_bfloat16* cK = sK + buf * kAttnKeys * HD;
+    const __nv_bfloat16* cV = sV + buf * kAttnKeys * HD;
+
+    float s[8][4];
+#pragma unroll
+    for (int n = 0; n < 8; ++n) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < HD / 16; ++ks) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        uint32_t kb[4];
+        const int mat = lane / 8;
+        const int key = j * 16 + (mat / 2) * 8 + lane % 8;
+        const int c = ks * 2 + (mat % 2);
+        ldmatrix_x4(kb, cK + key * HD + swz<HD>(key, c) * 8);
+        mma_bf16_16816(s[2 * j], qa[ks], kb[0], kb[1]);
+        mma_bf16_16816(s[2 * j + 1], qa[ks], kb[2], kb[3]);
+      }
+    }
+    // Keys past the chunk end do not exist.
+    const int kbase = k_begin + blk * kAttnKeys;
+#pragma unroll
+    for (int n = 0; n < 8; ++n) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int key = kbase + n * 8 + 2 * tq + (e & 1);
+        s[n][e] = key < k_end ? s[n][e] * scale_log2 : -FLT_MAX;
+      }
+    }
+#pragma unroll
+    for (int hr = 0; hr < 2; ++hr) {
+      float mx = -FLT_MAX;
+#pragma unroll
+      for (int n = 0; n < 8; ++n) mx = fmaxf(mx, fmaxf(s[n][2 * hr], s[n][2 * hr + 1]));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+      const float m_new = fmaxf(m_run[hr], mx);
+      const float corr = exp2f(m_run[hr] - m_new);
+      float rs = 0.f;
+#pragma unroll
+      for (int n = 0; n < 8; ++n) {
+        s[n][2 * hr] = exp2f(s[n][2 * hr] - m_new);
+        s[n][2 * hr + 1] = exp2f(s[n][2 * hr + 1] - m_new);
+        rs += s[n][2 * hr] + s[n][2 * hr + 1];
+      }
+      l_run[hr] = l_run[hr] * corr + rs;
+      m_run[hr] = m_new;
+#pragma unroll
+      for (int n = 0; n < HD / 8; ++n) {
+        o[n][2 * hr] *= corr;
+        o[n][2 * hr + 1] *= corr;
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      uint32_t pa[4] = {pack_f16(s[2 * j][0], s[2 * j][1]), pack_f16(s[2 * j][2], s[2 * j][3]),
+                        pack_f16(s[2 * j + 1][0], s[2 * j + 1][1]),
+                        pack_f16(s[2 * j + 1][2], s[2 * j + 1][3])};
+#pragma unroll
+      for (int dn = 0; dn < HD / 16; ++dn) {
+        uint32_t vb[4];
+        const int mat = lane / 8;
+        const int key = j * 16 + (mat % 2) * 8 + lane % 8;
+        const int c = dn * 2 + mat / 2;
+        ldmatrix_x4_trans(vb, cV + key * HD + swz<HD>(key, c) * 8);
+        mma_f16_16816(o[2 * dn], pa, bf16x2_to_f16x2(vb[0]), bf16x2_to_f16x2(vb[1]));
+        mma_f16_16816(o[2 * dn + 1], pa, bf16x2_to_f16x2(vb[2]), bf16x2_to_f16x2(vb[3]));
+      }
+    }
+    __syncthreads();
+  }
+
+#pragma unroll
+  for (int hr = 0; hr < 2; ++hr) {
+    l_run[hr] += __shfl_xor_sync(0xffffffffu, l_run[hr], 1);
+    l_run[hr] += __shfl_xor_sync(0xffffffffu, l_run[hr], 2);
+  }
+  const int gq = lane / 4;
+#pragma unroll
+  for (int hr = 0; hr < 2; ++hr) {
+    const int i = q0 + warp * 16 + gq + hr * 8;
+    if (i >= a.C) continue;
+    if (nsplit == 1) {
+      const float inv = 1.0f / l_run[hr];
+      __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(a.o) +
+                           ((size_t)b * a.C + i) * ((size_t)a.Hq * HD) + (size_t)h * HD;
+#pragma unroll
+      for (int n = 0; n < HD / 8; ++n)
+        *reinterpret_cast<uint32_t*>(dst + n * 8 + 2 * tq) =
+            pack_bf16(o[n][2 * hr] * inv, o[n][2 * hr + 1] * inv);
+    } else {
+      const size_t rowid = (((size_t)split * a.B + b) * a.Hq + h) * a.C + i;
+      float* dst = a.opart + rowid * HD;
+#pragma unroll
+      for (int n = 0; n < HD / 8; ++n)
+        *reinterpret_cast<float2*>(dst + n * 8 + 2 * tq) = make_float2(o[n][2 * hr], o[n][2 * hr + 1]);
+      if (tq == 0) *reinterpret_cast<float2*>(a.ml + rowid * 2) = make_float2(m_run[hr], l_run[hr]);
+    }
+  }
+}
+
+// Merge of the per-chunk partials of one (canvas, head, query row).
+__global__ void attn_combine_kernel(AttnArgs a, int nsplit, StopCtl ctl) {
+  if (all_stopped(ctl.stop_at, ctl.B, ctl.step)) return;
+  const int hd = a.hd;
+  const size_t row = blockIdx.x;  // ((b * Hq + h) * C + i)
+  const int i = (int)(row % a.C);
+  const int bh = (int)(row / a.C);
+  const int b = bh / a.Hq, h = bh % a.Hq;
+  const size_t stride = (size_t)a.B * a.Hq * a.C;
+  float m = -FLT_MAX;
+  for (int s = 0; s < nsplit; ++s) m = fmaxf(m, a.ml[(s * stride + row) * 2]);
+  float l = 0.f;
+  for (int s = 0; s < nsplit; ++s) l += a.ml[(s * stride + row) * 2 + 1] * exp2f(a.ml[(s * stride + row) * 2] - m);
+  const float inv = 1.0f / l;
+  for (int t = threadIdx.x; t < hd; t += blockDim.x) {
+    float acc = 0.f;
+    for (int s = 0; s < nsplit; ++s)
+      acc += a.opart[(s * stride + row) * hd + t] * exp2f(a.ml[(s * stride + row) * 2] - m);
+    reinterpret_cast<__nv_bfloat16*>(a.o)[((size_t)b * a.C + i) * ((size_t)a.Hq * hd) + (size_t)h * hd + t] =
+        __float2bfloat16_rn(acc * inv);
+  }
+}
+
+void attn_split(const dg_dims& D, int T, int* nsplit, int* keys_per_split) {
+  const int nqt = cdiv(D.C, kAttnRows);
+  const int units = nqt * D.B * D.Hq;
+  int target = cdiv(3 * kTargetCtas, units);
+  int ns = target < cdiv(T, 256) ? target : cdiv(T, 256);
+  if (ns > kMaxAttnSplits) ns = kMaxAttnSplits;
+  if (ns < 1) ns = 1;
+  int kps = cdiv(cdiv(T, ns), kAttnKeys) * kAttnKeys;
+  *keys_per_split = kps;
+  *nsplit = cdiv(T, kps);
+}
+
+template <int HD>
+static cudaError_t attn_impl(const AttnArgs& a, StopCtl ctl, cudaStream_t st) {
+  dg_dims D{};
+  D.C = a.C;
+  D.B = a.B;
+  D.Hq = a.Hq;
+  const int T = a.P + a.C;
+  int ns, kps;
+  attn_split(D, T, &ns, &kps);
+  const int nqt = cdiv(a.C, kAttnRows);
+  const size_t smem = (size_t)(kAttnRows + 4 * kAttnKeys) * HD * 2;
+  auto kern = attn_kernel<HD>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  const float scale_log2 = 1.4426950408889634f / sqrtf((float)HD);
+  dim3 grid(nqt * ns, a.B * a.Hq);
+  kern<<<grid, 128, smem, st>>>(a, nqt, ns, kps, scale_log2, ctl);
+  e = cudaGetLastError();
+  if (e != cudaSuccess || ns == 1) return e;
+  attn_combine_kernel<<<a.B * a.Hq * a.C, HD, 0, st>>>(a, ns, ctl);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_attention(const AttnArgs& a, StopCtl ctl, cudaStream_t st) {
+  switch (a.hd) {
+    case 32: return attn_impl<32>(a, ctl, st);
+    case 64: return attn_impl<64>(a, ctl, st);
+    case 128: return attn_impl<128>(a, ctl, st);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace dg

@@ -1,0 +1,740 @@
+// Tensor-core (tcgen05 + TMA + mbarrier) GEMM engine of libdg and the fused
+// kernels built on it:
+//   * gemm_kernel: D = A B^T with A [M][K], B [N][K] (or [K][N]) bf16, fp32
+//     accumulation in TMEM, warp-specialised (TMA producer warp, MMA warp,
+//     four epilogue warps), persistent over output tiles with a
+//     double-buffered TMEM accumulator.  Epilogues: fp32 store (diagnostics),
+//     bf16 store with residual / GELU (output projection, FFW), RoPE
+//     projections (q, k, v), and the LM head statistics epilogue.
+//   * selfcond_kernel: u = p0 . E where the p0 tiles are rebuilt in shared
+//     memory from the stored exp(s - m_tile) tiles and E is the MN-major B
+//     operand, plus the Gumbel-max search of accepted positions.
+#include <cfloat>
+
+#include "dg_common.cuh"
+#include "dg_internal.h"
+
+namespace dg {
+
+constexpr int kBM = 128;  // rows per MMA (one TMEM lane per row)
+constexpr int kBK = 64;   // bf16 elements per 128-byte swizzled row
+constexpr int kGemmThreads = 192;
+
+DG_DEV uint8_t* align1024(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+// If a role gave up (timeout), sleep long enough for copies and MMAs it may
+// have left in flight to land before the CTA releases TMEM and exits.
+DG_DEV void drain_if_aborted(volatile int* abort) {
+  if (*abort) {
+    uint64_t t0 = globaltimer();
+    while (globaltimer() - t0 < 2000000ull) __nanosleep(1000);
+  }
+}
+
+// ================================================================ epilogues
+struct EpiF32 {
+  float* out;
+  int ldo;
+  template <int BN, class LD>
+  DG_DEV void tile(int row, bool ok, int n0, int N, LD& ld) const {
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+      float v[32];
+      ld(c, v);
+      if (!ok) continue;
+      int col0 = n0 + c * 32;
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (col0 + j < N) out[(size_t)row * ldo + col0 + j] = v[j];
+    }
+  }
+};
+
+struct EpiBF16 {
+  __nv_bfloat16* out;
+  int ldo;
+  const __nv_bfloat16* resid;
+  int ldr;
+  int gelu;
+  int C;
+  StopCtl ctl;
+  template <int BN, class LD>
+  DG_DEV void tile(int row, bool ok, int n0, int N, LD& ld) const {
+    const bool active = ok && canvas_active(ctl.stop_at, row / C, ctl.step);
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+      float v[32];
+      ld(c, v);
+      if (!active) continue;
+      const int col0 = n0 + c * 32;
+      if (resid) {
+#pragma unroll
+        for (int j = 0; j < 32; j += 8) {
+          if (col0 + j + 8 <= N) {
+            uint4 r = *reinterpret_cast<const uint4*>(resid + (size_t)row * ldr + col0 + j);
+            const __nv_bfloat16* rb = reinterpret_cast<const __nv_bfloat16*>(&r);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) v[j + e] += __bfloat162float(rb[e]);
+          }
+        }
+      }
+      if (gelu) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = 0.5f * v[j] * (1.0f + erff(v[j] * 0.70710678118654752f));
+      }
+      if (col0 + 32 <= N) {
+        uint4* dst = reinterpret_cast<uint4*>(out + (size_t)row * ldo + col0);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          uint4 w;
+          w.x = pack_bf16(v[8 * j + 0], v[8 * j + 1]);
+          w.y = pack_bf16(v[8 * j + 2], v[8 * j + 3]);
+          w.z = pack_bf16(v[8 * j + 4], v[8 * j + 5]);
+          w.w = pack_bf16(v[8 * j + 6], v[8 * j + 7]);
+          dst[j] = w;
+        }
+      } else {
+        for (int j = 0; j < 32; ++j)
+          if (col0 + j < N) out[(size_t)row * ldo + col0 + j] = __float2bfloat16_rn(v[j]);
+      }
+    }
+  }
+};
+
+// q, k, v projections with RoPE on q and k.  One 128-column tile covers
+// 128 / HD whole heads, so both halves of every rotated pair are in the
+// thread's registers.
+template <int HD>
+struct EpiQKV {
+  __nv_bfloat16 *q, *k, *v;
+  const float2* rope;  // [C][HD/2] (cos, sin) of positions P + i
+  int C, Hq, Hkv, nq, nkv, kv_rows, kv_row0;
+  template <int BN, class LD>
+  DG_DEV void tile(int row, bool ok, int n0, int N, LD& ld) const {
+    static_assert(BN % HD == 0, "tile must hold whole heads");
+    float x[BN];
+#pragma unroll
+    for (int c = 0; c < BN / 32; ++c) {
+      float t[32];
+      ld(c, t);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) x[c * 32 + j] = t[j];
+    }
+    if (!ok) return;
+    const int b = row / C, i = row % C;
+#pragma unroll
+    for (int hh = 0; hh < BN / HD; ++hh) {
+      const int col0 = n0 + hh * HD;
+      if (col0 >= N) break;
+      const bool is_q = col0 < nq;
+      const bool is_k = !is_q && col0 < nq + nkv;
+      float* xv = x + hh * HD;
+      if (is_q || is_k) {
+        const float2* cs = rope + (size_t)i * (HD / 2);
+#pragma unroll
+        for (int j = 0; j < HD / 2; ++j) {
+          float2 r = cs[j];
+          float a0 = xv[j], a1 = xv[j + HD / 2];
+          xv[j] = a0 * r.x - a1 * r.y;
+          xv[j + HD / 2] = a0 * r.y + a1 * r.x;
+        }
+      }
+      __nv_bfloat16* dst;
+      if (is_q) {
+        dst = q + (((size_t)b * Hq + col0 / HD) * C + i) * HD;
+      } else {
+        const int head = (col0 - nq - (is_k ? 0 : nkv)) / HD;
+        dst = (is_k ? k : v) + (((size_t)b * Hkv + head) * kv_rows + kv_row0 + i) * HD;
+      }
+      uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+      for (int j = 0; j < HD / 8; ++j) {
+        uint4 w;
+        w.x = pack_bf16(xv[8 * j + 0], xv[8 * j + 1]);
+        w.y = pack_bf16(xv[8 * j + 2], xv[8 * j + 3]);
+        w.z = pack_bf16(xv[8 * j + 4], xv[8 * j + 5]);
+        w.w = pack_bf16(xv[8 * j + 6], xv[8 * j + 7]);
+        d4[j] = w;
+      }
+    }
+  }
+};
+
+// LM head: l = alpha h.E / sqrt d, s = l / tau.  Per (row, 256-column tile):
+// m_t = max s (kept in log2 units), exp(s - m_t) stored as bf16 for the
+// self-conditioning pass, l_t = sum exp(s - m_t), S_t = sum exp(s - m_t)
+// (s - m_t) log2 e, and the argmax of h.E (lowest column on ties).
+struct EpiLM {
+  const float* alpha;
+  float coef2;  // log2(e) / (sqrt(d) tau)
+  float inv_sqrt_d;
+  __nv_bfloat16* pt;
+  float *pm, *pl, *pS, *pvmax;
+  int* pidx;
+  float* logits;
+  int M, V;
+  template <int BN, class LD>
+  DG_DEV void tile(int row, bool ok, int n0, int N, LD& ld) const {
+    const float al = ok ? __ldg(alpha + row) : 1.0f;
+    const float c2 = al * coef2;
+    float vmax = -FLT_MAX;
+    int imax = n0;
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+      float v[32];
+      ld(c, v);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const int col = n0 + c * 32 + j;
+        if (col < N && v[j] > vmax) {
+          vmax = v[j];
+          imax = col;
+        }
+      }
+    }
+    const float m2 = vmax * c2;
+    float l = 0.f, S = 0.f;
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+      float v[32];
+      ld(c, v);
+      const int col0 = n0 + c * 32;
+      uint32_t pk[16];
+#pragma unroll
+      for (int j = 0; j < 32; j += 2) {
+        const float t0 = fmaf(v[j], c2, -m2), t1 = fmaf(v[j + 1], c2, -m2);
+        const float p0 = (col0 + j < N) ? exp2f(t0) : 0.f;
+        const float p1 = (col0 + j + 1 < N) ? exp2f(t1) : 0.f;
+        l += p0 + p1;
+        S = fmaf(p0, t0, fmaf(p1, t1, S));
+        pk[j / 2] = pack_bf16(p0, p1);
+      }
+      if (ok) {
+        if (col0 + 32 <= N) {
+          uint4* dst = reinterpret_cast<uint4*>(pt + (size_t)row * V + col0);
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            dst[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+        } else {
+          const __nv_bfloat16* pb = reinterpret_cast<const __nv_bfloat16*>(pk);
+          for (int j = 0; j < 32; ++j)
+            if (col0 + j < N) pt[(size_t)row * V + col0 + j] = pb[j];
+        }
+        if (logits) {
+          const float cl = al * inv_sqrt_d;
+          for (int j = 0; j < 32; ++j)
+            if (col0 + j < N) logits[(size_t)row * V + col0 + j] = v[j] * cl;
+        }
+      }
+    }
+    if (ok) {
+      const size_t o = (size_t)(n0 / BN) * M + row;
+      pm[o] = m2;
+      pl[o] = l;
+      pS[o] = S;
+      pvmax[o] = vmax;
+      pidx[o] = imax;
+    }
+  }
+};
+
+// ============================================================ GEMM kernel
+template <int BN, int STAGES, bool B_MN>
+struct GemmLayout {
+  static constexpr int kA = kBM * kBK * 2;
+  static constexpr int kB = BN * kBK * 2;
+  static constexpr int kStage = kA + kB;
+  static constexpr int kBar = STAGES * kStage;
+  static constexpr int kSmem = kBar + 256 + 1024;
+};
+
+// B rows [0, nb0) come from mB0, [nb0, nb0 + nb1) from mB1, the rest from mB2
+// (used to run the q, k, v projections as one GEMM over three weights).  A
+// K-major B tile is loaded as BN / b_sub boxes of b_sub rows, each from the
+// map that holds its rows (b_sub divides nb0 and nb1).
+template <int BN, int STAGES, bool B_MN, class Epi>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap mA, const __grid_constant__ CUtensorMap mB0,
+                const __grid_constant__ CUtensorMap mB1, const __grid_constant__ CUtensorMap mB2,
+                int nb0, int nb1, int b_sub, int M, int N, int K, uint32_t b_lbo, uint32_t b_sbo,
+                Epi epi, int* status, StopCtl ctl) {
+  using L = GemmLayout<BN, STAGES, B_MN>;
+  if (all_stopped(ctl.stop_at, ctl.B, ctl.step)) return;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kBar);
+  uint64_t* empty = full + STAGES;
+  uint64_t* tfull = empty + STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+  volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int num_m = (M + kBM - 1) / kBM, num_n = (N + BN - 1) / BN;
+  const int num_tiles = num_m * num_n;
+  const int nk = (K + kBK - 1) / kBK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 128);
+    }
+    *abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, 2 * BN);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      tma_prefetch(&mA);
+      tma_prefetch(&mB0);
+      int stage = 0;
+      uint32_t phase = 0;
+      bool alive = true;
+      for (int tile = blockIdx.x; tile < num_tiles && alive; tile += gridDim.x) {
+        const int m0 = (tile % num_m) * kBM, n0 = (tile / num_m) * BN;
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1, status, abort)) {
+            alive = false;
+            break;
+          }
+          uint8_t* sa = smem + stage * L::kStage;
+          uint8_t* sb = sa + L::kA;
+          mbar_arrive_expect_tx(&full[stage], L::kStage);
+          tma_load_2d(sa, &mA, &full[stage], kb * kBK, m0);
+          if (!B_MN) {
+            for (int r = 0; r < BN; r += b_sub) {
+              const int n = n0 + r;
+              const CUtensorMap* mb = &mB0;
+              int nb = n;
+              if (n >= nb0 + nb1) {
+                mb = &mB2;
+                nb = n - nb0 - nb1;
+              } else if (n >= nb0) {
+                mb = &mB1;
+                nb = n - nb0;
+              }
+              tma_load_2d(sb + r * 128, mb, &full[stage], kb * kBK, nb);
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < BN / 64; ++j)
+              tma_load_2d(sb + j * (kBK * 128), &mB0, &full[stage], n0 + 64 * j, kb * kBK);
+          }
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    constexpr uint32_t idesc = idesc_bf16(kBM, BN, B_MN);
+    int stage = 0;
+    uint32_t phase = 0;
+    bool alive = true;
+    int it = 0;
+    for (int tile = blockIdx.x; tile < num_tiles && alive; tile += gridDim.x, ++it) {
+      const int acc = it & 1;
+      const uint32_t aph = (it >> 1) & 1;
+      if (!mbar_wait(&tempty[acc], aph ^ 1, status, abort)) break;
+      tc_fence_after();
+      const uint32_t dt = tmem + acc * BN;
+      for (int kb = 0; kb < nk; ++kb) {
+        if (!mbar_wait(&full[stage], phase, status, abort)) {
+          alive = false;
+          break;
+        }
+        tc_fence_after();
+        if (lane == 0) {
+          const uint32_t sa = smem_u32(smem + stage * L::kStage);
+          const uint32_t sb = sa + L::kA;
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk) {
+            const uint64_t ad = sdesc_sw128(sa + kk * 32, 16, 1024);
+            const uint64_t bd = B_MN ? sdesc_sw128(sb + kk * 2048, b_lbo, b_sbo)
+                                     : sdesc_sw128(sb + kk * 32, 16, 1024);
+            umma_bf16(dt, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+          }
+          umma_commit(&empty[stage]);
+        }
+        __syncwarp();
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+      if (alive && lane == 0) umma_commit(&tfull[acc]);
+      __syncwarp();
+    }
+  } else {
+    const int q = warp & 3;  // TMEM lane quarter this warp may read
+    const int r_local = q * 32 + lane;
+    int it = 0;
+    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++it) {
+      const int acc = it & 1;
+      const uint32_t aph = (it >> 1) & 1;
+      if (!mbar_wait(&tfull[acc], aph, status, abort)) break;
+      tc_fence_after();
+      const int m0 = (tile % num_m) * kBM, n0 = (tile / num_m) * BN;
+      const int row = m0 + r_local;
+      const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
+      auto ld = [&](int c, float(&v)[32]) { tmem_ld32(tb + c * 32, v); };
+      epi.template tile<BN>(row, row < M, n0, N, ld);
+      tc_fence_before();
+      mbar_arrive(&tempty[acc]);
+    }
+  }
+  __syncthreads();
+  drain_if_aborted(abort);
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 2 * BN);
+  }
+}
+
+// ====================================================== host-side helpers
+static int num_sms() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = kTargetCtas;
+  }
+  return n;
+}
+
+bool make_tmap_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
+                  uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer) {
+  typedef CUresult (*EncodeFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                               const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                               const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                               CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+  static EncodeFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult qr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &qr) != cudaSuccess ||
+        qr != cudaDriverEntryPointSuccess || !p)
+      return false;
+    fn = reinterpret_cast<EncodeFn>(p);
+  }
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                  box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// K-major operand X [rows][K]: box of 64 K-elements x box_rows rows.
+static bool tmap_kmajor(CUtensorMap* m, const void* X, int rows, int K, int box_rows) {
+  return make_tmap_2d(m, X, (uint64_t)K, (uint64_t)rows, (uint64_t)K * 2, kBK, (uint32_t)box_rows);
+}
+// MN-major operand X [K][N]: box of 64 N-elements x 64 K-rows.
+static bool tmap_mnmajor(CUtensorMap* m, const void* X, int K, int N) {
+  return make_tmap_2d(m, X, (uint64_t)N, (uint64_t)K, (uint64_t)N * 2, 64, kBK);
+}
+
+template <int BN, int STAGES, bool B_MN, class Epi>
+static cudaError_t run_gemm(const CUtensorMap& mA, const CUtensorMap& mB0, const CUtensorMap& mB1,
+                            const CUtensorMap& mB2, int nb0, int nb1, int b_sub, int M, int N, int K,
+                            uint32_t lbo, uint32_t sbo, const Epi& epi, int* status, StopCtl ctl,
+                            cudaStream_t st) {
+  using L = GemmLayout<BN, STAGES, B_MN>;
+  auto kern = gemm_kernel<BN, STAGES, B_MN, Epi>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmem);
+  if (e != cudaSuccess) return e;
+  const int tiles = cdiv(M, kBM) * cdiv(N, BN);
+  const int grid = tiles < num_sms() ? tiles : num_sms();
+  kern<<<grid, kGemmThreads, L::kSmem, st>>>(mA, mB0, mB1, mB2, nb0, nb1, b_sub, M, N, K, lbo, sbo,
+                                             epi, status, ctl);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_debug_gemm(const void* A, const void* Bm, float* D, int M, int N, int K,
+                              int b_mn_major, int* status, cudaStream_t st) {
+  CUtensorMap mA, mB;
+  EpiF32 epi{D, N};
+  StopCtl ctl{nullptr, 0, 0};
+  if (!tmap_kmajor(&mA, A, M, K, kBM)) return cudaErrorInvalidValue;
+  if (b_mn_major == 0) {
+    if (!tmap_kmajor(&mB, Bm, N, K, 256)) return cudaErrorInvalidValue;
+    return run_gemm<256, 4, false>(mA, mB, mB, mB, N, 0, 256, M, N, K, 0, 0, epi, status, ctl, st);
+  }
+  if (!tmap_mnmajor(&mB, Bm, K, N)) return cudaErrorInvalidValue;
+  // 1: LBO = distance between 64-column blocks along N, SBO = between 8-row
+  // groups along K (the layout the self-conditioning kernel uses); 2: swapped.
+  const uint32_t lbo = b_mn_major == 1 ? kBK * 128 : 1024;
+  const uint32_t sbo = b_mn_major == 1 ? 1024 : kBK * 128;
+  return run_gemm<256, 4, true>(mA, mB, mB, mB, N, 0, 64, M, N, K, lbo, sbo, epi, status, ctl, st);
+}
+
+cudaError_t launch_gemm_bf16(const void* A, const void* W, void* out, int ldo, const void* resid,
+                             int ldr, int gelu, int M, int N, int K, int C, StopCtl ctl,
+                             int* status, cudaStream_t st) {
+  CUtensorMap mA, mB;
+  if (!tmap_kmajor(&mA, A, M, K, kBM) || !tmap_kmajor(&mB, W, N, K, 128)) return cudaErrorInvalidValue;
+  EpiBF16 epi{reinterpret_cast<__nv_bfloat16*>(out), ldo,
+              reinterpret_cast<const __nv_bfloat16*>(resid), ldr, gelu, C, ctl};
+  return run_gemm<128, 4, false>(mA, mB, mB, mB, N, 0, 128, M, N, K, 0, 0, epi, status, ctl, st);
+}
+
+template <int HD>
+static cudaError_t qkv_impl(const CUtensorMap& mA, const CUtensorMap& m0, const CUtensorMap& m1,
+                            const CUtensorMap& m2, int nb0, int nb1, int M, int N, int K,
+                            const EpiQKV<HD>& epi, int* status, StopCtl ctl, cudaStream_t st) {
+  return run_gemm<128, 4, false>(mA, m0, m1, m2, nb0, nb1, HD, M, N, K, 0, 0, epi, status, ctl, st);
+}
+
+cudaError_t launch_qkv(const void* a, const void* Wq, const void* Wk, const void* Wv, void* q,
+                       void* k, void* v, int kv_rows, int kv_row0, const float2* rope,
+                       const dg_dims& D, StopCtl ctl, int* status, cudaStream_t st) {
+  const int M = D.B * D.C, nq = Wq ? D.Hq * D.hd : 0, nkv = D.Hkv * D.hd;
+  CUtensorMap mA, mq, mk, mv;
+  if (!tmap_kmajor(&mA, a, M, D.d, kBM)) return cudaErrorInvalidValue;
+  // boxes of one head (hd rows) so that a tile may span the q / k / v weights
+  if (!tmap_kmajor(&mk, Wk, nkv, D.d, D.hd) || !tmap_kmajor(&mv, Wv, nkv, D.d, D.hd))
+    return cudaErrorInvalidValue;
+  if (Wq && !tmap_kmajor(&mq, Wq, nq, D.d, D.hd)) return cudaErrorInvalidValue;
+  const int N = nq + 2 * nkv;
+  auto bf = [](void* p) { return reinterpret_cast<__nv_bfloat16*>(p); };
+  const CUtensorMap& m0 = Wq ? mq : mk;
+  const CUtensorMap& m1 = Wq ? mk : mv;
+  const CUtensorMap& m2 = mv;
+  const int nb0 = Wq ? nq : nkv, nb1 = Wq ? nkv : nkv;
+  switch (D.hd) {
+    case 32: {
+      EpiQKV<32> e{bf(q), bf(k), bf(v), rope, D.C, D.Hq, D.Hkv, nq, nkv, kv_rows, kv_row0};
+      return qkv_impl<32>(mA, m0, m1, m2, nb0, nb1, M, N, D.d, e, status, ctl, st);
+    }
+    case 64: {
+      EpiQKV<64> e{bf(q), bf(k), bf(v), rope, D.C, D.Hq, D.Hkv, nq, nkv, kv_rows, kv_row0};
+      return qkv_impl<64>(mA, m0, m1, m2, nb0, nb1, M, N, D.d, e, status, ctl, st);
+    }
+    case 128: {
+      EpiQKV<128> e{bf(q), bf(k), bf(v), rope, D.C, D.Hq, D.Hkv, nq, nkv, kv_rows, kv_row0};
+      return qkv_impl<128>(mA, m0, m1, m2, nb0, nb1, M, N, D.d, e, status, ctl, st);
+    }
+  }
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_lmhead(const LmArgs& a, StopCtl ctl, int* status, cudaStream_t st) {
+  CUtensorMap mA, mB;
+  if (!tmap_kmajor(&mA, a.h, a.M, a.d, kBM) || !tmap_kmajor(&mB, a.E, a.V, a.d, kLmBN))
+    return cudaErrorInvalidValue;
+  EpiLM epi{a.alpha, a.coef2, a.inv_sqrt_d, reinterpret_cast<__nv_bfloat16*>(a.pt), a.pm, a.pl,
+            a.pS, a.pvmax, a.pidx, a.logits, a.M, a.V};
+  return run_gemm<kLmBN, 4, false>(mA, mB, mB, mB, a.V, 0, kLmBN, a.M, a.V, a.d, 0, 0, epi, status, ctl,
+                                   st);
+}
+
+// ====================================================== self-conditioning
+constexpr int kScStages = 3;
+struct ScLayout {
+  static constexpr int kA = 2 * kBM * kBK * 2;  // 256 rows of p0, 32 KB
+  static constexpr int kB = kBK * kScBN * 2;    // 64 vocabulary rows x 256 columns of E, 32 KB
+  static constexpr int kStage = kA + kB;
+  static constexpr int kBar = kScStages * kStage;
+  static constexpr int kSmem = kBar + 256 + 1024;
+};
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    selfcond_kernel(const __grid_constant__ CUtensorMap mP, const __grid_constant__ CUtensorMap mE,
+                    ScArgs a, int n_tiles, int m_pairs, int* status, StopCtl ctl) {
+  if (all_stopped(ctl.stop_at, ctl.B, ctl.step)) return;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + ScLayout::kBar);
+  uint64_t* ready = full + kScStages;
+  uint64_t* empty = ready + kScStages;
+  uint64_t* tfull = empty + kScStages;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tfull + 1);
+  volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int nt = blockIdx.x % n_tiles;
+  const int rest = blockIdx.x / n_tiles;
+  const int mp = rest % m_pairs;
+  const int split = rest / m_pairs;
+  const int nkb = (a.V + kBK - 1) / kBK;
+  const int kb0 = (int)((int64_t)split * nkb / a.nsplit);
+  const int kb1 = (int)((int64_t)(split + 1) * nkb / a.nsplit);
+  const int m0 = mp * 2 * kBM, n0 = nt * kScBN;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kScStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&ready[s], 128);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(tfull, 1);
+    *abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      tma_prefetch(&mP);
+      tma_prefetch(&mE);
+      int stage = 0;
+      uint32_t phase = 0;
+      for (int kb = kb0; kb < kb1; ++kb) {
+        if (!mbar_wait(&empty[stage], phase ^ 1, status, abort)) break;
+        uint8_t* sa = smem + stage * ScLayout::kStage;
+        uint8_t* sb = sa + ScLayout::kA;
+        mbar_arrive_expect_tx(&full[stage], ScLayout::kStage);
+        tma_load_2d(sa, &mP, &full[stage], kb * kBK, m0);
+        tma_load_2d(sa + kBM * kBK * 2, &mP, &full[stage], kb * kBK, m0 + kBM);
+#pragma unroll
+        for (int j = 0; j < kScBN / 64; ++j)
+          tma_load_2d(sb + j * (kBK * 128), &mE, &full[stage], n0 + 64 * j, kb * kBK);
+        if (++stage == kScStages) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+    }
+  } else if (warp == 1) {
+    constexpr uint32_t idesc = idesc_bf16(kBM, kScBN, true);
+    int stage = 0;
+    uint32_t phase = 0;
+    bool alive = true;
+    for (int kb = kb0; kb < kb1; ++kb) {
+      if (!mbar_wait(&ready[stage], phase, status, abort)) {
+        alive = false;
+        break;
+      }
+      tc_fence_after();
+      if (lane == 0) {
+        const uint32_t sa = smem_u32(smem + stage * ScLayout::kStage);
+        const uint32_t sb = sa + ScLayout::kA;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk) {
+            const uint64_t ad = sdesc_sw128(sa + h * (kBM * kBK * 2) + kk * 32, 16, 1024);
+            const uint64_t bd = sdesc_sw128(sb + kk * 2048, kBK * 128, 1024);
+            umma_bf16(tmem + h * kScBN, ad, bd, idesc, (kb != kb0 || kk != 0) ? 1u : 0u);
+          }
+        }
+        umma_commit(&empty[stage]);
+      }
+      __syncwarp();
+      if (++stage == kScStages) {
+        stage = 0;
+        phase ^= 1;
+      }
+    }
+    if (alive && lane == 0) umma_commit(tfull);
+    __syncwarp();
+  } else {
+    // Transform warps: rebuild p0 = exp(s - m_tile) * exp(m_tile - m) / l in
+    // place, thread t owning row t of each 128-row half.
+    const int t = threadIdx.x - 64;
+    const int rows[2] = {m0 + t, m0 + kBM + t};
+    float f[2] = {0.f, 0.f};
+    int cur_vt = -1;
+    int stage = 0;
+    uint32_t phase = 0;
+    for (int kb = kb0; kb < kb1; ++kb) {
+      if (!mbar_wait(&full[stage], phase, status, abort)) break;
+      const int vt = (kb * kBK) / kLmBN;
+      if (vt != cur_vt) {
+        cur_vt = vt;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) f[h] = rows[h] < a.M ? a.fscale[(size_t)vt * a.M + rows[h]] : 0.f;
+      }
+      uint8_t* sa = smem + stage * ScLayout::kStage;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint4* rowp = reinterpret_cast<uint4*>(sa + h * (kBM * kBK * 2) + t * 128);
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          uint4 x = rowp[c];
+          const __nv_bfloat16* xb = reinterpret_cast<const __nv_bfloat16*>(&x);
+          uint4 y;
+          y.x = pack_bf16(__bfloat162float(xb[0]) * f[h], __bfloat162float(xb[1]) * f[h]);
+          y.y = pack_bf16(__bfloat162float(xb[2]) * f[h], __bfloat162float(xb[3]) * f[h]);
+          y.z = pack_bf16(__bfloat162float(xb[4]) * f[h], __bfloat162float(xb[5]) * f[h]);
+          y.w = pack_bf16(__bfloat162float(xb[6]) * f[h], __bfloat162float(xb[7]) * f[h]);
+          rowp[c] = y;
+        }
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(&ready[stage]);
+      if (++stage == kScStages) {
+        stage = 0;
+        phase ^= 1;
+      }
+    }
+    // Epilogue: the split's partial u tile, TMEM lane = row within the half.
+    if (mbar_wait(tfull, 0, status, abort)) {
+      tc_fence_after();
+      const int q = warp & 3;
+      const int rl = q * 32 + lane;
+#pragma unroll 1
+      for (int h = 0; h < 2; ++h) {
+        const int row = m0 + h * kBM + rl;
+        const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(h * kScBN);
+#pragma unroll 1
+        for (int c = 0; c < kScBN / 32; ++c) {
+          float v[32];
+          tmem_ld32(tb + c * 32, v);
+          const int col0 = n0 + c * 32;
+          if (row < a.M && col0 < a.d) {
+            float4* dst = reinterpret_cast<float4*>(a.upart + ((size_t)split * a.M + row) * a.d + col0);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) dst[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+          }
+        }
+      }
+    }
+  }
+  __syncthreads();
+  drain_if_aborted(abort);
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+cudaError_t launch_selfcond(const ScArgs& a, StopCtl ctl, int* status, cudaStream_t st) {
+  CUtensorMap mP, mE;
+  if (!tmap_kmajor(&mP, a.pt, a.M, a.V, kBM) || !tmap_mnmajor(&mE, a.E, a.V, a.d))
+    return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(selfcond_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       ScLayout::kSmem);
+  if (e != cudaSuccess) return e;
+  const int n_tiles = cdiv(a.d, kScBN), m_pairs = cdiv(a.M, 2 * kBM);
+  const int grid = n_tiles * m_pairs * a.nsplit;
+  selfcond_kernel<<<grid, kGemmThreads, ScLayout::kSmem, st>>>(mP, mE, a, n_tiles, m_pairs, status, ctl);
+  return cudaGetLastError();
+}
+
+}  // namespace dg

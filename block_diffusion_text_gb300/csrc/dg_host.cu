@@ -1,0 +1,417 @@
+// C-ABI entry points of libdg: argument validation, workspace layout and the
+// ordered launch of the kernels of one denoising step, the annealed loop and
+// the block commit.  Nothing here computes on the host.
+#include <climits>
+#include <cmath>
+#include <cstring>
+
+#include "dg_internal.h"
+
+using namespace dg;
+
+namespace {
+
+// Status word used by the diagnostics entry point (module memory).
+__device__ int g_debug_status;
+
+bool dims_ok(const dg_dims* D) {
+  if (!D) return false;
+  if (D->V <= 0 || D->d <= 0 || D->C <= 0 || D->B <= 0 || D->Hq <= 0 || D->Hkv <= 0 || D->hd <= 0 ||
+      D->F <= 0)
+    return false;
+  if (D->Hq % D->Hkv != 0) return false;
+  if (!(D->rope_base > 0.f) || !(D->rms_eps >= 0.f)) return false;
+  return true;
+}
+
+dg_status dims_supported(const dg_dims* D) {
+  if (!dims_ok(D)) return DG_ERR_ARG;
+  if (D->V % 8 != 0 || D->d % 64 != 0 || D->d > 16384 || D->F % 64 != 0) return DG_ERR_SHAPE;
+  if (D->hd != 32 && D->hd != 64 && D->hd != 128) return DG_ERR_SHAPE;
+  if (D->C > 1024) return DG_ERR_SHAPE;
+  if ((int64_t)D->B * D->C > (1 << 20) || (int64_t)D->V > (1 << 30)) return DG_ERR_SHAPE;
+  return DG_OK;
+}
+
+template <class T>
+T* at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(reinterpret_cast<uint8_t*>(ws) + off);
+}
+
+dg_status cuda_status(cudaError_t e) { return e == cudaSuccess ? DG_OK : DG_ERR_CUDA; }
+
+#define DG_TRY(expr)                         \
+  do {                                       \
+    cudaError_t _e = (expr);                 \
+    if (_e != cudaSuccess) return DG_ERR_CUDA; \
+  } while (0)
+
+struct StepCtx {
+  const dg_model* model;
+  const dg_kv_cache* cache;
+  dg_canvas* canvas;
+  void* ws;
+  WsLayout L;
+  cudaStream_t st;
+};
+
+dg_status check_model(const dg_model* m) {
+  if (!m) return DG_ERR_ARG;
+  dg_status s = dims_supported(&m->dims);
+  if (s) return s;
+  if (!m->E || !m->Wq || !m->Wk || !m->Wv || !m->Wo || !m->W1 || !m->W2) return DG_ERR_ARG;
+  return DG_OK;
+}
+
+dg_status check_ws(const dg_dims& D, int32_t cap, void* ws, size_t ws_bytes, WsLayout* L) {
+  if (!ws) return DG_ERR_ARG;
+  if (reinterpret_cast<uintptr_t>(ws) % 256 != 0) return DG_ERR_WORKSPACE;
+  if (!ws_layout(D, cap, L)) return DG_ERR_SHAPE;
+  if (ws_bytes < L->total) return DG_ERR_WORKSPACE;
+  return DG_OK;
+}
+
+struct Prof {
+  void* const* ev;
+  cudaStream_t st;
+  cudaError_t mark(int slot, int end) const {
+    if (!ev || !ev[2 * slot + end]) return cudaSuccess;
+    return cudaEventRecord(reinterpret_cast<cudaEvent_t>(ev[2 * slot + end]), st);
+  }
+};
+
+// All kernels of one denoising step, in order, on ctx.st.
+dg_status enqueue_step(const StepCtx& c, float tau, float b, float stop_H, uint64_t seed, int step,
+                       int block, const dg_step_out* out, int* accepted_log, int N) {
+  const dg_dims& D = c.model->dims;
+  const WsLayout& L = c.L;
+  void* ws = c.ws;
+  const int M = D.B * D.C, NT = cdiv(D.V, kLmBN), P = c.cache->len;
+  int* status = at<int>(ws, L.status);
+  int* stop_at = at<int>(ws, L.stop_at);
+  StopCtl ctl{stop_at, D.B, step};
+  float2* rope = at<float2>(ws, L.rope);
+  const Prof pf{out ? out->events : nullptr, c.st};
+
+  DG_TRY(pf.mark(DG_PROF_EMBED, 0));
+  DG_TRY(launch_embed_rmsnorm(c.canvas->tokens, c.model->E, c.canvas->z, at<void>(ws, L.a), rope, D, M,
+                              P, ctl, c.st));
+  DG_TRY(pf.mark(DG_PROF_EMBED, 1));
+  DG_TRY(pf.mark(DG_PROF_QKV, 0));
+  DG_TRY(launch_qkv(at<void>(ws, L.a), c.model->Wq, c.model->Wk, c.model->Wv, at<void>(ws, L.q),
+                    at<void>(ws, L.kc), at<void>(ws, L.vc), D.C, 0, rope, D, ctl, status, c.st));
+  DG_TRY(pf.mark(DG_PROF_QKV, 1));
+  AttnArgs aa{at<void>(ws, L.q), c.cache->K, c.cache->V, at<void>(ws, L.kc), at<void>(ws, L.vc),
+              at<void>(ws, L.o), at<float>(ws, L.attn_o), at<float>(ws, L.attn_ml), D.B, D.C, D.Hq,
+              D.Hkv, D.hd, P, c.cache->cap};
+  DG_TRY(pf.mark(DG_PROF_ATTN, 0));
+  DG_TRY(launch_attention(aa, ctl, c.st));
+  DG_TRY(pf.mark(DG_PROF_ATTN, 1));
+  DG_TRY(pf.mark(DG_PROF_OPROJ, 0));
+  DG_TRY(launch_gemm_bf16(at<void>(ws, L.o), c.model->Wo, at<void>(ws, L.h), D.d, at<void>(ws, L.a), D.d,
+                          0, M, D.d, D.Hq * D.hd, D.C, ctl, status, c.st));
+  DG_TRY(pf.mark(DG_PROF_OPROJ, 1));
+  LmArgs lm{};
+  lm.h = at<void>(ws, L.h);
+  lm.E = c.model->E;
+  lm.alpha = c.canvas->alpha;
+  lm.coef2 = (float)(1.4426950408889634 / (std::sqrt((double)D.d) * (double)tau));
+  lm.inv_sqrt_d = (float)(1.0 / std::sqrt((double)D.d));
+  lm.pt = at<void>(ws, L.pt);
+  lm.pm = at<float>(ws, L.pm);
+  lm.pl = at<float>(ws, L.pl);
+  lm.pS = at<float>(ws, L.pS);
+  lm.pvmax = at<float>(ws, L.pvmax);
+  lm.pidx = at<int>(ws, L.pidx);
+  lm.logits = (out && out->debug) ? out->debug->logits : nullptr;
+  lm.M = M;
+  lm.V = D.V;
+  lm.d = D.d;
+  DG_TRY(pf.mark(DG_PROF_LMHEAD, 0));
+  DG_TRY(launch_lmhead(lm, ctl, status, c.st));
+  DG_TRY(pf.mark(DG_PROF_LMHEAD, 1));
+  StatsArgs sa{at<float>(ws, L.pm), at<float>(ws, L.pl), at<float>(ws, L.pS), at<float>(ws, L.pvmax),
+               at<int>(ws, L.pidx), NT, M, at<double>(ws, L.Hd), at<float>(ws, L.lsum),
+               at<float>(ws, L.fscale), at<int>(ws, L.amax), out ? out->entropy : nullptr,
+               out ? out->argmax : nullptr};
+  DG_TRY(pf.mark(DG_PROF_STATS, 0));
+  DG_TRY(launch_stats(sa, ctl, c.st));
+  DG_TRY(pf.mark(DG_PROF_STATS, 1));
+  SamplerArgs sp{};
+  sp.Hd = at<double>(ws, L.Hd);
+  sp.amax = at<int>(ws, L.amax);
+  sp.prev_argmax = c.canvas->prev_argmax;
+  sp.tokens = c.canvas->tokens;
+  sp.acc = at<uint8_t>(ws, L.acc);
+  sp.acc_out = out ? out->accept : nullptr;
+  sp.n_acc = out ? out->n_acc : nullptr;
+  sp.mean_H = out ? out->mean_H : nullptr;
+  sp.stop = out ? out->stop : nullptr;
+  sp.stop_at = stop_at;
+  sp.B = D.B;
+  sp.C = D.C;
+  sp.V = D.V;
+  sp.b = b;
+  sp.stop_H = stop_H;
+  sp.seed = seed;
+  sp.block = block;
+  sp.step = step;
+  sp.accepted_log = accepted_log;
+  sp.N = N;
+  DG_TRY(pf.mark(DG_PROF_SAMPLER, 0));
+  DG_TRY(launch_sampler(sp, c.st));
+  DG_TRY(pf.mark(DG_PROF_SAMPLER, 1));
+  ScArgs sc{};
+  sc.pt = at<void>(ws, L.pt);
+  sc.E = c.model->E;
+  sc.fscale = at<float>(ws, L.fscale);
+  sc.upart = at<float>(ws, L.upart);
+  sc.M = M;
+  sc.V = D.V;
+  sc.d = D.d;
+  sc.nsplit = selfcond_splits(D);
+  DG_TRY(pf.mark(DG_PROF_SELFCOND, 0));
+  DG_TRY(launch_selfcond(sc, ctl, status, c.st));
+  DG_TRY(pf.mark(DG_PROF_SELFCOND, 1));
+  GumbelArgs gu{};
+  gu.pt = at<void>(ws, L.pt);
+  gu.fscale = at<float>(ws, L.fscale);
+  gu.amax = at<int>(ws, L.amax);
+  gu.acc = at<uint8_t>(ws, L.acc);
+  gu.gbest = at<float>(ws, L.gbest);
+  gu.gidx = at<int>(ws, L.gidx);
+  gu.M = M;
+  gu.V = D.V;
+  gu.C = D.C;
+  gu.seed = seed;
+  gu.block = block;
+  gu.step = step;
+  DG_TRY(pf.mark(DG_PROF_GUMBEL, 0));
+  DG_TRY(launch_gumbel(gu, ctl, c.st));
+  DG_TRY(pf.mark(DG_PROF_GUMBEL, 1));
+  ReduceArgs ra{at<float>(ws, L.upart), at<float>(ws, L.gbest), at<int>(ws, L.gidx), at<uint8_t>(ws, L.acc),
+                at<void>(ws, L.u), c.canvas->tokens, M, D.d, D.C, sc.nsplit, cdiv(D.V, kGumbelChunk)};
+  DG_TRY(pf.mark(DG_PROF_REDUCE, 0));
+  DG_TRY(launch_reduce(ra, ctl, c.st));
+  DG_TRY(pf.mark(DG_PROF_REDUCE, 1));
+  DG_TRY(pf.mark(DG_PROF_FFW1, 0));
+  DG_TRY(launch_gemm_bf16(at<void>(ws, L.u), c.model->W1, at<void>(ws, L.g), D.F, nullptr, 0, 1, M, D.F,
+                          D.d, D.C, ctl, status, c.st));
+  DG_TRY(pf.mark(DG_PROF_FFW1, 1));
+  DG_TRY(pf.mark(DG_PROF_FFW2, 0));
+  DG_TRY(launch_gemm_bf16(at<void>(ws, L.g), c.model->W2, c.canvas->z, D.d, nullptr, 0, 0, M, D.d, D.F,
+                          D.C, ctl, status, c.st));
+  DG_TRY(pf.mark(DG_PROF_FFW2, 1));
+  if (out && out->debug) {
+    const dg_step_debug* g = out->debug;
+    const size_t bf = 2;
+    struct {
+      void* dst;
+      size_t off, bytes;
+    } cp[] = {{g->a, L.a, bf * M * D.d},
+              {g->q, L.q, bf * M * D.Hq * D.hd},
+              {g->k, L.kc, bf * M * D.Hkv * D.hd},
+              {g->v, L.vc, bf * M * D.Hkv * D.hd},
+              {g->o, L.o, bf * M * D.Hq * D.hd},
+              {g->h, L.h, bf * M * D.d},
+              {g->u, L.u, bf * M * D.d},
+              {g->g, L.g, bf * M * D.F}};
+    for (auto& e : cp)
+      if (e.dst) DG_TRY(cudaMemcpyAsync(e.dst, at<void>(ws, e.off), e.bytes, cudaMemcpyDeviceToDevice, c.st));
+  }
+  return DG_OK;
+}
+
+dg_status check_cache(const dg_dims& D, const dg_kv_cache* cache) {
+  if (!cache || !cache->K || !cache->V) return DG_ERR_ARG;
+  if (cache->cap < 0 || cache->len < 0 || cache->len > cache->cap) return DG_ERR_ARG;
+  (void)D;
+  return DG_OK;
+}
+
+dg_status check_canvas(const dg_canvas* cv) {
+  if (!cv || !cv->tokens || !cv->z || !cv->alpha || !cv->prev_argmax) return DG_ERR_ARG;
+  return DG_OK;
+}
+
+}  // namespace
+
+namespace dg {
+
+int selfcond_splits(const dg_dims& D) {
+  const int n_tiles = cdiv(D.d, kScBN), m_pairs = cdiv((int64_t)D.B * D.C, 256);
+  int ns = kTargetCtas / (n_tiles * m_pairs);
+  const int nkb = cdiv(D.V, 64);
+  if (ns > nkb) ns = nkb;
+  if (ns > 64) ns = 64;
+  if (ns < 1) ns = 1;
+  return ns;
+}
+
+bool ws_layout(const dg_dims& D, int32_t cap, WsLayout* L) {
+  if (cap < 0) return false;
+  const size_t M = (size_t)D.B * D.C, NT = (size_t)cdiv(D.V, kLmBN);
+  int ns_attn, kps;
+  attn_split(D, cap + D.C, &ns_attn, &kps);
+  // room for the largest split count any prefix length up to cap can use
+  {
+    const int nqt = cdiv(D.C, kAttnRows);
+    int target = cdiv(3 * kTargetCtas, nqt * D.B * D.Hq);
+    if (target > kMaxAttnSplits) target = kMaxAttnSplits;
+    if (ns_attn < target) ns_attn = target;
+  }
+  const size_t S = (size_t)selfcond_splits(D);
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    size_t o = off;
+    off = align_up(off + (bytes ? bytes : 1), 256);
+    return o;
+  };
+  L->status = take(256);
+  L->stop_at = take(4 * D.B);
+  L->rope = take(8 * (size_t)D.C * (D.hd / 2));
+  L->a = take(2 * M * D.d);
+  L->q = take(2 * M * D.Hq * D.hd);
+  L->kc = take(2 * M * D.Hkv * D.hd);
+  L->vc = take(2 * M * D.Hkv * D.hd);
+  L->o = take(2 * M * D.Hq * D.hd);
+  L->h = take(2 * M * D.d);
+  L->attn_o = take(4 * (size_t)ns_attn * M * D.Hq * D.hd);
+  L->attn_ml = take(8 * (size_t)ns_attn * M * D.Hq);
+  L->pt = take(2 * M * (size_t)D.V);
+  L->pm = take(4 * NT * M);
+  L->pl = take(4 * NT * M);
+  L->pS = take(4 * NT * M);
+  L->pvmax = take(4 * NT * M);
+  L->pidx = take(4 * NT * M);
+  L->Hd = take(8 * M);
+  L->lsum = take(4 * M);
+  L->fscale = take(4 * NT * M);
+  L->amax = take(4 * M);
+  L->acc = take(M);
+  L->upart = take(4 * S * M * D.d);
+  const size_t NC = (size_t)cdiv(D.V, kGumbelChunk);
+  L->gbest = take(4 * NC * M);
+  L->gidx = take(4 * NC * M);
+  L->u = take(2 * M * D.d);
+  L->g = take(2 * M * D.F);
+  L->total = off;
+  return true;
+}
+
+}  // namespace dg
+
+extern "C" {
+
+const char* dg_status_string(dg_status s) {
+  switch (s) {
+    case DG_OK: return "ok";
+    case DG_ERR_ARG: return "invalid argument";
+    case DG_ERR_SHAPE: return "unsupported shape";
+    case DG_ERR_CAPACITY: return "cache capacity exceeded";
+    case DG_ERR_WORKSPACE: return "workspace too small or misaligned";
+    case DG_ERR_CUDA: return "CUDA error";
+    case DG_ERR_TIMEOUT: return "device wait timed out";
+  }
+  return "unknown status";
+}
+
+dg_status dg_workspace_size(const dg_dims* dims, int32_t cap, size_t* bytes) {
+  if (!bytes) return DG_ERR_ARG;
+  dg_status s = dims_supported(dims);
+  if (s) return s;
+  if (cap < 0) return DG_ERR_ARG;
+  WsLayout L;
+  if (!ws_layout(*dims, cap, &L)) return DG_ERR_SHAPE;
+  *bytes = L.total;
+  return DG_OK;
+}
+
+dg_status dg_read_status(const void* ws, int32_t* status, void* stream) {
+  if (!ws || !status) return DG_ERR_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  DG_TRY(cudaMemcpyAsync(status, ws, 4, cudaMemcpyDeviceToHost, st));
+  DG_TRY(cudaStreamSynchronize(st));
+  return DG_OK;
+}
+
+dg_status dg_canvas_init(int32_t* tokens, int32_t B, int32_t C, int32_t V, uint64_t seed,
+                         int32_t block, void* stream) {
+  if (!tokens || B <= 0 || C <= 0 || V <= 0) return DG_ERR_ARG;
+  return cuda_status(launch_canvas_init(tokens, B, C, V, seed, block, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+dg_status dg_denoise_step(const dg_model* model, const dg_kv_cache* cache, dg_canvas* canvas,
+                          float tau, float b, uint64_t seed, int32_t step, int32_t block, void* ws,
+                          size_t ws_bytes, dg_step_out* out, void* stream) {
+  dg_status s = check_model(model);
+  if (s) return s;
+  if ((s = check_cache(model->dims, cache)) || (s = check_canvas(canvas))) return s;
+  if (!(tau > 0.f) || !(b >= 0.f) || step < 0 || block < 0) return DG_ERR_ARG;
+  StepCtx c{model, cache, canvas, ws, {}, reinterpret_cast<cudaStream_t>(stream)};
+  if ((s = check_ws(model->dims, cache->cap, ws, ws_bytes, &c.L))) return s;
+  // A lone step treats every canvas as still denoising.
+  DG_TRY(cudaMemsetAsync(at<void>(ws, c.L.stop_at), 0x7f, 4 * (size_t)model->dims.B, c.st));
+  return enqueue_step(c, tau, b, 0.005f, seed, step, block, out, nullptr, 0);
+}
+
+dg_status dg_denoise_canvas(const dg_model* model, const dg_kv_cache* cache, dg_canvas* canvas,
+                            const dg_sched* sched, uint64_t seed, int32_t block, void* ws,
+                            size_t ws_bytes, dg_canvas_result* result, void* stream) {
+  dg_status s = check_model(model);
+  if (s) return s;
+  if ((s = check_cache(model->dims, cache)) || (s = check_canvas(canvas))) return s;
+  if (!sched || sched->N <= 0 || sched->N > 4096 || !(sched->tau0 > 0.f) || !(sched->tau1 > 0.f) ||
+      !(sched->b >= 0.f) || block < 0)
+    return DG_ERR_ARG;
+  if (!result || !result->steps_taken || !result->converged || !result->accepted || !result->xhat0)
+    return DG_ERR_ARG;
+  StepCtx c{model, cache, canvas, ws, {}, reinterpret_cast<cudaStream_t>(stream)};
+  if ((s = check_ws(model->dims, cache->cap, ws, ws_bytes, &c.L))) return s;
+  const dg_dims& D = model->dims;
+  DG_TRY(cudaMemsetAsync(at<void>(ws, c.L.stop_at), 0x7f, 4 * (size_t)D.B, c.st));
+  DG_TRY(cudaMemsetAsync(result->accepted, 0xff, 4 * (size_t)D.B * sched->N, c.st));
+  const int N = sched->N;
+  for (int step = 0; step < N; ++step) {
+    const double frac = N > 1 ? (double)step / (double)(N - 1) : 0.0;
+    const float tau = (float)((double)sched->tau0 + ((double)sched->tau1 - (double)sched->tau0) * frac);
+    s = enqueue_step(c, tau, sched->b, sched->stop_H, seed, step, block, nullptr, result->accepted, N);
+    if (s) return s;
+  }
+  return cuda_status(launch_loop_finish(at<int>(ws, c.L.stop_at), D.B, N, result->steps_taken,
+                                        result->converged, canvas->prev_argmax, result->xhat0, D.C, c.st));
+}
+
+dg_status dg_commit_block(const dg_model* model, dg_kv_cache* cache, const int32_t* tokens, void* ws,
+                          size_t ws_bytes, void* stream) {
+  dg_status s = check_model(model);
+  if (s) return s;
+  if ((s = check_cache(model->dims, cache))) return s;
+  if (!tokens) return DG_ERR_ARG;
+  const dg_dims& D = model->dims;
+  WsLayout L;
+  if ((s = check_ws(D, cache->cap, ws, ws_bytes, &L))) return s;
+  if ((int64_t)cache->len + D.C > cache->cap) return DG_ERR_CAPACITY;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  StopCtl none{nullptr, 0, 0};
+  float2* rope = at<float2>(ws, L.rope);
+  DG_TRY(launch_embed_rmsnorm(tokens, model->E, nullptr, at<void>(ws, L.a), rope, D, D.B * D.C, cache->len,
+                              none, st));
+  DG_TRY(launch_qkv(at<void>(ws, L.a), nullptr, model->Wk, model->Wv, nullptr, cache->K, cache->V,
+                    cache->cap, cache->len, rope, D, none, at<int>(ws, L.status), st));
+  cache->len += D.C;
+  return DG_OK;
+}
+
+dg_status dg_debug_gemm(const void* A, const void* Bm, float* D, int32_t M, int32_t N, int32_t K,
+                        int32_t b_mn_major, void* stream) {
+  if (!A || !Bm || !D || M <= 0 || N <= 0 || K <= 0 || b_mn_major < 0 || b_mn_major > 2)
+    return DG_ERR_ARG;
+  if (K % 8 != 0 || N % 8 != 0) return DG_ERR_SHAPE;
+  int* status = nullptr;
+  DG_TRY(cudaGetSymbolAddress(reinterpret_cast<void**>(&status), g_debug_status));
+  return cuda_status(launch_debug_gemm(A, Bm, D, M, N, K, b_mn_major, status,
+                                       reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,169 @@
+// Internal declarations shared by the translation units of libdg.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/dg.h"
+
+namespace dg {
+
+// Tuning constant: CTAs the split-K / split-KV grids aim for (one wave on the
+// 152 SMs of a GB300).  Kernels are correct for any SM count.
+constexpr int kTargetCtas = 152;
+constexpr int kLmBN = 256;     // vocabulary columns per LM-head tile
+constexpr int kScBN = 256;     // model columns per self-conditioning tile
+constexpr int kAttnRows = 64;  // query rows per attention CTA
+constexpr int kAttnKeys = 64;  // keys per attention block
+constexpr int kMaxAttnSplits = 64;
+
+inline int cdiv(int64_t a, int64_t b) { return (int)((a + b - 1) / b); }
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Split of the key sequence [prefix ; canvas] of length T into chunks for the
+// attention grid; returns the number of splits and the keys per split.
+void attn_split(const dg_dims& D, int T, int* nsplit, int* keys_per_split);
+// Split of the vocabulary (the contraction of p0 . E) between CTAs.
+int selfcond_splits(const dg_dims& D);
+
+// Byte offsets of every buffer in the caller's workspace.
+struct WsLayout {
+  size_t status, stop_at, rope;
+  size_t a, q, kc, vc, o, h;
+  size_t attn_o, attn_ml;
+  size_t pt;
+  size_t pm, pl, pS, pvmax, pidx;
+  size_t Hd, lsum, fscale, amax, acc;
+  size_t upart, gbest, gidx;
+  size_t u, g;
+  size_t total;
+};
+bool ws_layout(const dg_dims& D, int32_t cap, WsLayout* L);
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point.
+bool make_tmap_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
+                  uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer);
+
+// ------------------------------------------------------------- launchers --
+struct StopCtl {
+  const int* stop_at;  // int32 [B] or nullptr
+  int B;
+  int step;
+};
+
+// D fp32 [M][N] = A[M][K] B^T (diagnostics).
+cudaError_t launch_debug_gemm(const void* A, const void* Bm, float* D, int M, int N, int K,
+                              int b_mn_major, int* status, cudaStream_t st);
+// out bf16 [M][N] (row pitch ldo) = act(A[M][K] W[N][K]^T (+ resid)); rows of
+// stopped canvases (row / C) are left untouched when ctl.stop_at is set.
+cudaError_t launch_gemm_bf16(const void* A, const void* W, void* out, int ldo, const void* resid,
+                             int ldr, int gelu, int M, int N, int K, int C, StopCtl ctl,
+                             int* status, cudaStream_t st);
+// Projections of a [M][d]: q (RoPE) to [B][Hq][C][hd], k (RoPE) and v to
+// [B][Hkv][kv_rows][hd] at row kv_row0 + i.  With Wq == nullptr only k, v.
+cudaError_t launch_qkv(const void* a, const void* Wq, const void* Wk, const void* Wv, void* q,
+                       void* k, void* v, int kv_rows, int kv_row0, const float2* rope,
+                       const dg_dims& D, StopCtl ctl, int* status, cudaStream_t st);
+// LM head with the statistics epilogue.
+struct LmArgs {
+  const void* h;       // bf16 [M][d]
+  const void* E;       // bf16 [V][d]
+  const float* alpha;  // [M]
+  float coef2;         // log2(e) / (sqrt(d) tau)
+  float inv_sqrt_d;
+  void* pt;            // bf16 [M][V]  exp(s - m_tile)
+  float *pm, *pl, *pS, *pvmax;
+  int* pidx;           // [NT][M]
+  float* logits;       // optional fp32 [M][V]
+  int M, V, d;
+};
+cudaError_t launch_lmhead(const LmArgs& a, StopCtl ctl, int* status, cudaStream_t st);
+// Self-conditioning contraction u = p0 . E (split over the vocabulary).
+struct ScArgs {
+  const void* pt;        // bf16 [M][V]
+  const void* E;         // bf16 [V][d]
+  const float* fscale;   // [NT][M]  exp(m_tile - m) / l
+  float* upart;          // [S][M][d]
+  int M, V, d, nsplit;
+};
+cudaError_t launch_selfcond(const ScArgs& a, StopCtl ctl, int* status, cudaStream_t st);
+// Gumbel-max search of the accepted rows over vocabulary chunks.
+constexpr int kGumbelChunk = 8192;
+struct GumbelArgs {
+  const void* pt;        // bf16 [M][V]
+  const float* fscale;   // [NT][M]
+  const int* amax;       // [M]
+  const uint8_t* acc;    // [M]
+  float* gbest;          // [NC][M]
+  int* gidx;             // [NC][M]
+  int M, V, C;
+  uint64_t seed;
+  int block, step;
+};
+cudaError_t launch_gumbel(const GumbelArgs& a, StopCtl ctl, cudaStream_t st);
+
+// Attention over [prefix ; canvas] (legacy warp MMA path).
+struct AttnArgs {
+  const void* q;            // bf16 [B][Hq][C][hd]
+  const void *Kp, *Vp;      // bf16 [B][Hkv][cap][hd]
+  const void *kc, *vc;      // bf16 [B][Hkv][C][hd]
+  void* o;                  // bf16 [B*C][Hq*hd]
+  float* opart;             // fp32 [S][B][Hq][C][hd]
+  float* ml;                // fp32 [S][B][Hq][C][2]
+  int B, C, Hq, Hkv, hd, P, cap;
+};
+cudaError_t launch_attention(const AttnArgs& a, StopCtl ctl, cudaStream_t st);
+
+// Misc kernels.
+cudaError_t launch_embed_rmsnorm(const int32_t* tokens, const void* E, const void* z, void* a,
+                                 float2* rope, const dg_dims& D, int rows, int P, StopCtl ctl,
+                                 cudaStream_t st);
+struct StatsArgs {
+  const float *pm, *pl, *pS, *pvmax;
+  const int* pidx;
+  int NT, M;
+  double* Hd;            // [M]
+  float* lsum;           // [M]
+  float* fscale;         // [NT][M]
+  int* amax;             // [M]
+  float* entropy;        // optional out [M]
+  int* argmax_out;       // optional out [M]
+};
+cudaError_t launch_stats(const StatsArgs& a, StopCtl ctl, cudaStream_t st);
+struct SamplerArgs {
+  const double* Hd;      // [B][C]
+  const int* amax;       // [B][C]
+  int* prev_argmax;      // [B][C]
+  int* tokens;           // [B][C]
+  uint8_t* acc;          // [B][C] (workspace copy)
+  uint8_t* acc_out;      // optional
+  int* n_acc;            // optional [B]
+  float* mean_H;         // optional [B]
+  int* stop;             // optional [B]
+  int* stop_at;          // [B] (workspace)
+  int B, C, V;
+  float b, stop_H;
+  uint64_t seed;
+  int block, step;
+  int* accepted_log;     // optional [B][N] for the loop
+  int N;
+};
+cudaError_t launch_sampler(const SamplerArgs& a, cudaStream_t st);
+struct ReduceArgs {
+  const float* upart;    // [S][M][d]
+  const float* gbest;    // [NC][M]
+  const int* gidx;       // [NC][M]
+  const uint8_t* acc;
+  void* u;               // bf16 [M][d]
+  int* tokens;           // [M]
+  int M, d, C, nsplit, nchunks;
+};
+cudaError_t launch_reduce(const ReduceArgs& a, StopCtl ctl, cudaStream_t st);
+cudaError_t launch_canvas_init(int32_t* tokens, int B, int C, int V, uint64_t seed, int block,
+                               cudaStream_t st);
+cudaError_t launch_loop_finish(const int* stop_at, int B, int N, int* steps_taken, int* converged,
+                               const int* prev_argmax, int* xhat0, int C, cudaStream_t st);
+
+}  // namespace dg

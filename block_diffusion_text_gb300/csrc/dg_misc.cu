@@ -1,0 +1,442 @@
+// Memory-bound kernels of the denoising step: embedding + RMSNorm, the merge
+// of the LM-head tile statistics, the entropy-bounded sampler, the reduction
+// of the self-conditioning partials, canvas initialisation and the loop
+// bookkeeping.
+#include <cfloat>
+#include <climits>
+
+#include "dg_common.cuh"
+#include "dg_internal.h"
+
+namespace dg {
+
+// ------------------------------------------------------- embed + RMSNorm --
+// a = RMSNorm(E[x] + z) with no learned gain ("DiffusionGemma" docs chapter,
+// data-flow pseudocode: embed(canvas) + self_conditioning(prev); technical
+// report summary, step 3).  Row blocks 0..C-1 also fill the RoPE table of
+// positions P + i in double precision.
+constexpr int kEmbThreads = 256;
+constexpr int kEmbMaxChunks = 8;  // d <= 8 * 8 * 256
+
+__global__ void __launch_bounds__(kEmbThreads)
+    embed_rmsnorm_kernel(const int32_t* tokens, const __nv_bfloat16* E, const __nv_bfloat16* z,
+                         __nv_bfloat16* a, float2* rope, int d, float eps, int C, int P, int hd,
+                         float rope_base, StopCtl ctl) {
+  if (all_stopped(ctl.stop_at, ctl.B, ctl.step)) return;
+  const int row = blockIdx.x;
+  const int tok = tokens[row];
+  const int nch = d / 8;
+  const uint4* e4 = reinterpret_cast<const uint4*>(E + (size_t)tok * d);
+  const uint4* z4 = z ? reinterpret_cast<const uint4*>(z + (size_t)row * d) : nullptr;
+  float x[kEmbMaxChunks][8];
+  float ss = 0.f;
+#pragma unroll
+  for (int k = 0; k < kEmbMaxChunks; ++k) {
+    const int c = threadIdx.x + k * kEmbThreads;
+    if (c < nch) {
+      uint4 ev = e4[c];
+      const __nv_bfloat16* eb = reinterpret_cast<const __nv_bfloat16*>(&ev);
+      uint4 zv = z4 ? z4[c] : make_uint4(0, 0, 0, 0);
+      const __nv_bfloat16* zb = reinterpret_cast<const __nv_bfloat16*>(&zv);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        x[k][e] = __bfloat162float(eb[e]) + __bfloat162float(zb[e]);
+        ss = fmaf(x[k][e], x[k][e], ss);
+      }
+    }
+  }
+  __shared__ float red[kEmbThreads / 32];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  if (threadIdx.x % 32 == 0) red[threadIdx.x / 32] = ss;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    float t = threadIdx.x < kEmbThreads / 32 ? red[threadIdx.x] : 0.f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+    if (threadIdx.x == 0) red[0] = t;
+  }
+  __syncthreads();
+  const float r = 1.0f / sqrtf(red[0] / (float)d + eps);
+  uint4* a4 = reinterpret_cast<uint4*>(a + (size_t)row * d);
+#pragma unroll
+  for (int k = 0; k < kEmbMaxChunks; ++k) {
+    const int c = threadIdx.x + k * kEmbThreads;
+    if (c < nch) {
+      uint4 w;
+      w.x = pack_bf16(x[k][0] * r, x[k][1] * r);
+      w.y = pack_bf16(x[k][2] * r, x[k][3] * r);
+      w.z = pack_bf16(x[k][4] * r, x[k][5] * r);
+      w.w = pack_bf16(x[k][6] * r, x[k][7] * r);
+      a4[c] = w;
+    }
+  }
+  if (rope && row < C) {
+    for (int j = threadIdx.x; j < hd / 2; j += kEmbThreads) {
+      const double theta = pow((double)rope_base, -2.0 * j / hd);
+      const double ang = (double)(P + row) * theta;
+      double sn, cs;
+      sincos(ang, &sn, &cs);
+      rope[(size_t)row * (hd / 2) + j] = make_float2((float)cs, (float)sn);
+    }
+  }
+}
+
+cudaError_t launch_embed_rmsnorm(const int32_t* tokens, const void* E, const void* z, void* a,
+                                 float2* rope, const dg_dims& D, int rows, int P, StopCtl ctl,
+                                 cudaStream_t st) {
+  embed_rmsnorm_kernel<<<rows, kEmbThreads, 0, st>>>(
+      tokens, reinterpret_cast<const __nv_bfloat16*>(E), reinterpret_cast<const __nv_bfloat16*>(z),
+      reinterpret_cast<__nv_bfloat16*>(a), rope, D.d, D.rms_eps, D.C, P, D.hd, D.rope_base, ctl);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------- tile statistics --
+// Merge of the per-tile (max, sum, weighted sum, argmax) of each row into the
+// tempered-softmax entropy H = ln Z - S / Z, the argmax, Z, and the factors
+// exp(m_t - m) / Z that turn a stored tile exp(s - m_t) into p0.  One CTA per
+// row; tile weights in float, sums in double.
+constexpr int kStatsThreads = 256;
+
+template <class T, class Op>
+DG_DEV T block_reduce(T v, Op op, T* sh) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = op(v, __shfl_xor_sync(0xffffffffu, v, o));
+  if (threadIdx.x % 32 == 0) sh[threadIdx.x / 32] = v;
+  __syncthreads();
+  T r = sh[0];
+  for (int w = 1; w < (int)(blockDim.x / 32); ++w) r = op(r, sh[w]);
+  __syncthreads();
+  return r;
+}
+
+__global__ void __launch_bounds__(kStatsThreads) stats_kernel(StatsArgs a, StopCtl ctl) {
+  if (all_stopped(ctl.stop_at, ctl.B, ctl.step)) return;
+  const int row = blockIdx.x;
+  __shared__ float shf[kStatsThreads / 32];
+  __shared__ double shd[kStatsThreads / 32];
+  __shared__ float shv[kStatsThreads / 32];
+  __shared__ int shi[kStatsThreads / 32];
+  float mx = -FLT_MAX, vbest = -FLT_MAX;
+  int ibest = INT_MAX;
+  for (int t = threadIdx.x; t < a.NT; t += blockDim.x) {
+    const size_t o = (size_t)t * a.M + row;
+    mx = fmaxf(mx, a.pm[o]);
+    const float v = a.pvmax[o];
+    const int i = a.pidx[o];
+    if (v > vbest || (v == vbest && i < ibest)) {
+      vbest = v;
+      ibest = i;
+    }
+  }
+  const float M2 = block_reduce(mx, [](float x, float y) { return fmaxf(x, y); }, shf);
+  // argmax: (value, lowest index) over the block
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float v2 = __shfl_xor_sync(0xffffffffu, vbest, o);
+    const int i2 = __shfl_xor_sync(0xffffffffu, ibest, o);
+    if (v2 > vbest || (v2 == vbest && i2 < ibest)) {
+      vbest = v2;
+      ibest = i2;
+    }
+  }
+  if (threadIdx.x % 32 == 0) {
+    shv[threadIdx.x / 32] = vbest;
+    shi[threadIdx.x / 32] = ibest;
+  }
+  double l = 0.0, S = 0.0;
+  for (int t = threadIdx.x; t < a.NT; t += blockDim.x) {
+    const size_t o = (size_t)t * a.M + row;
+    const float dm = a.pm[o] - M2;
+    const double w = (double)exp2f(dm);
+    l += w * (double)a.pl[o];
+    S += w * ((double)a.pS[o] + (double)a.pl[o] * (double)dm);
+  }
+  const double Z = block_reduce(l, [](double x, double y) { return x + y; }, shd);
+  const double St = block_reduce(S, [](double x, double y) { return x + y; }, shd);
+  const float invZ = (float)(1.0 / Z);
+  for (int t = threadIdx.x; t < a.NT; t += blockDim.x) {
+    const size_t o = (size_t)t * a.M + row;
+    a.fscale[o] = exp2f(a.pm[o] - M2) * invZ;
+  }
+  if (threadIdx.x == 0) {
+    float vb = -FLT_MAX;
+    int ib = INT_MAX;
+    for (int w = 0; w < (int)(blockDim.x / 32); ++w) {
+      if (shv[w] > vb || (shv[w] == vb && shi[w] < ib)) {
+        vb = shv[w];
+        ib = shi[w];
+      }
+    }
+    const double H = log(Z) - 0.69314718055994531 * St / Z;
+    a.Hd[row] = H;
+    a.lsum[row] = (float)Z;
+    a.amax[row] = ib;
+    if (a.entropy) a.entropy[row] = (float)H;
+    if (a.argmax_out) a.argmax_out[row] = ib;
+  }
+}
+
+cudaError_t launch_stats(const StatsArgs& a, StopCtl ctl, cudaStream_t st) {
+  stats_kernel<<<a.M, kStatsThreads, 0, st>>>(a, ctl);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------ Gumbel-max --
+// Sample of an accepted position: argmax_v (log p0_v + G_v) with G_v the
+// Gumbel noise of Philox stream 0 keyed by (seed, block, step, canvas,
+// position, v), lowest index on ties (technical report summary, step 3:
+// accepted positions take their predicted token; the Gumbel-max form of that
+// draw is this library's reading).  The score of the argmax position is a
+// lower bound of the maximum, so an entry can only win where
+// log p0_v > score(argmax) - max G; the largest Gumbel draw is 16.636
+// (U = 1 - 2^-24), and the test uses 16.65.  One CTA per (row, 8192-entry
+// chunk); rows that were not accepted return at once.
+constexpr int kGumbelThreads = 256;
+constexpr float kGumbelMaxDraw = 16.65f;
+
+__global__ void __launch_bounds__(kGumbelThreads) gumbel_kernel(GumbelArgs a, StopCtl ctl) {
+  const int row = blockIdx.y;
+  const int chunk = blockIdx.x;
+  if (!a.acc[row] || !canvas_active(ctl.stop_at, row / a.C, ctl.step)) return;
+  const __nv_bfloat16* pt = reinterpret_cast<const __nv_bfloat16*>(a.pt) + (size_t)row * a.V;
+  const int canvas = row / a.C, pos = row % a.C;
+  // seed score at the argmax
+  const int am = a.amax[row];
+  const float pam = __bfloat162float(pt[am]) * a.fscale[(size_t)(am / kLmBN) * a.M + row];
+  uint64_t w[4];
+  philox_block(w, a.seed, a.block, a.step, canvas, pos, am >> 2, 0);
+  const float best0 = logf(pam) + gumbel_from_word(w[am & 3]);
+  const float thr = expf(best0 - kGumbelMaxDraw);
+  float best = -FLT_MAX;
+  int bidx = INT_MAX;
+  const int v_begin = chunk * kGumbelChunk;
+  const int v_end = min(a.V, v_begin + kGumbelChunk);
+  for (int v0 = v_begin + threadIdx.x * 8; v0 < v_end; v0 += kGumbelThreads * 8) {
+    const float f = a.fscale[(size_t)(v0 / kLmBN) * a.M + row];
+    uint4 x = *reinterpret_cast<const uint4*>(pt + v0);
+    const __nv_bfloat16* xb = reinterpret_cast<const __nv_bfloat16*>(&x);
+    float p[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) p[e] = __bfloat162float(xb[e]) * f;
+#pragma unroll
+    for (int g4 = 0; g4 < 2; ++g4) {
+      bool any = false;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) any |= p[g4 * 4 + e] >= thr && v0 + g4 * 4 + e < v_end;
+      if (!any) continue;
+      philox_block(w, a.seed, a.block, a.step, canvas, pos, (v0 + g4 * 4) >> 2, 0);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int v = v0 + g4 * 4 + e;
+        const float pv = p[g4 * 4 + e];
+        if (pv >= thr && v < v_end && pv > 0.f) {
+          const float sc = logf(pv) + gumbel_from_word(w[e]);
+          if (sc > best) {
+            best = sc;
+            bidx = v;
+          }
+        }
+      }
+    }
+  }
+  // (score, lowest index) over the block
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float b2 = __shfl_xor_sync(0xffffffffu, best, o);
+    const int i2 = __shfl_xor_sync(0xffffffffu, bidx, o);
+    if (b2 > best || (b2 == best && i2 < bidx)) {
+      best = b2;
+      bidx = i2;
+    }
+  }
+  __shared__ float sb[kGumbelThreads / 32];
+  __shared__ int si[kGumbelThreads / 32];
+  if (threadIdx.x % 32 == 0) {
+    sb[threadIdx.x / 32] = best;
+    si[threadIdx.x / 32] = bidx;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int k = 1; k < kGumbelThreads / 32; ++k) {
+      if (sb[k] > best || (sb[k] == best && si[k] < bidx)) {
+        best = sb[k];
+        bidx = si[k];
+      }
+    }
+    a.gbest[(size_t)chunk * a.M + row] = best;
+    a.gidx[(size_t)chunk * a.M + row] = bidx;
+  }
+}
+
+cudaError_t launch_gumbel(const GumbelArgs& a, StopCtl ctl, cudaStream_t st) {
+  dim3 grid(cdiv(a.V, kGumbelChunk), a.M);
+  gumbel_kernel<<<grid, kGumbelThreads, 0, st>>>(a, ctl);
+  return cudaGetLastError();
+}
+
+// --------------------------------------------------------------- sampler --
+// Entropy-bounded acceptance ("DiffusionGemma Technical Report" summary,
+// method step 3): positions sorted by ascending entropy (ties by position),
+// the longest prefix whose cumulative entropy is <= b is accepted, every other
+// position is renoised to a uniform random token (Philox stream 1).  Also the
+// mean entropy, the accepted count and the adaptive-stop test of step 4
+// (mean entropy <= stop_H and the argmax equal to the previous step's).
+// One CTA per canvas, one thread per (padded) position.
+__global__ void __launch_bounds__(1024) sampler_kernel(SamplerArgs a, int npow2) {
+  const int b = blockIdx.x;
+  const int i = threadIdx.x;
+  const bool active = a.stop_at[b] >= a.step;
+  // Every canvas skips its work once it has stopped.
+  if (!active) return;
+  __shared__ double key[1024];
+  __shared__ int idx[1024];
+  __shared__ double cum[1024];
+  __shared__ int flags[2];
+  const int base = b * a.C;
+  key[i] = i < a.C ? a.Hd[base + i] : DBL_MAX;
+  idx[i] = i;
+  if (i == 0) {
+    flags[0] = 0;  // accepted count
+    flags[1] = 1;  // argmax unchanged everywhere
+  }
+  __syncthreads();
+  // Bitonic sort of (key, idx) ascending.
+  for (int k = 2; k <= npow2; k <<= 1) {
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      const int p = i ^ j;
+      if (p > i) {
+        const bool up = (i & k) == 0;
+        const double ki = key[i], kp = key[p];
+        const int ii = idx[i], ip = idx[p];
+        const bool gt = (ki > kp) || (ki == kp && ii > ip);
+        if (gt == up) {
+          key[i] = kp;
+          key[p] = ki;
+          idx[i] = ip;
+          idx[p] = ii;
+        }
+      }
+      __syncthreads();
+    }
+  }
+  // Inclusive prefix sum of the sorted entropies (double), Hillis-Steele.
+  cum[i] = i < a.C ? key[i] : 0.0;
+  __syncthreads();
+  for (int off = 1; off < npow2; off <<= 1) {
+    const double v = i >= off ? cum[i - off] : 0.0;
+    __syncthreads();
+    cum[i] += v;
+    __syncthreads();
+  }
+  if (i < a.C) {
+    const int pos = idx[i];
+    const bool acc = cum[i] <= (double)a.b;
+    a.acc[base + pos] = acc ? 1 : 0;
+    if (a.acc_out) a.acc_out[base + pos] = acc ? 1 : 0;
+    if (acc) atomicAdd(&flags[0], 1);
+    if (!acc) {
+      uint64_t w[4];
+      philox_block(w, a.seed, a.block, a.step, b, pos, 0, 1);
+      a.tokens[base + pos] = uniform_token(w[0], a.V);
+    }
+    const int am = a.amax[base + i];
+    if (a.step < 1 || a.prev_argmax[base + i] != am) atomicAnd(&flags[1], 0);
+  }
+  __syncthreads();
+  if (i < a.C) a.prev_argmax[base + i] = a.amax[base + i];
+  if (i == 0) {
+    const double meanH = cum[a.C - 1] / (double)a.C;
+    const int stop = (a.step >= 1 && flags[1] && meanH <= (double)a.stop_H) ? 1 : 0;
+    if (a.n_acc) a.n_acc[b] = flags[0];
+    if (a.mean_H) a.mean_H[b] = (float)meanH;
+    if (a.stop) a.stop[b] = stop;
+    if (a.accepted_log) a.accepted_log[(size_t)b * a.N + a.step] = flags[0];
+    if (stop) a.stop_at[b] = a.step;
+  }
+}
+
+cudaError_t launch_sampler(const SamplerArgs& a, cudaStream_t st) {
+  int np = 32;
+  while (np < a.C) np <<= 1;
+  sampler_kernel<<<a.B, np, 0, st>>>(a, np);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------ self-conditioning reduce --
+// u = sum of the per-split partials of p0 . E (bf16 out), and the Gumbel-max
+// token of accepted positions = the best (score, lowest index) over chunks.
+__global__ void __launch_bounds__(256) reduce_kernel(ReduceArgs a, StopCtl ctl) {
+  if (all_stopped(ctl.stop_at, ctl.B, ctl.step)) return;
+  const int row = blockIdx.x;
+  const int n4 = a.d / 4;
+  const size_t sstride = (size_t)a.M * a.d;
+  for (int c = threadIdx.x; c < n4; c += blockDim.x) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s = 0; s < a.nsplit; ++s) {
+      const float4 v = *reinterpret_cast<const float4*>(a.upart + s * sstride + (size_t)row * a.d + 4 * c);
+      acc.x += v.x;
+      acc.y += v.y;
+      acc.z += v.z;
+      acc.w += v.w;
+    }
+    uint2 w;
+    w.x = pack_bf16(acc.x, acc.y);
+    w.y = pack_bf16(acc.z, acc.w);
+    *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(a.u) + (size_t)row * a.d + 4 * c) = w;
+  }
+  if (threadIdx.x == 0 && a.acc[row] && canvas_active(ctl.stop_at, row / a.C, ctl.step)) {
+    float best = -FLT_MAX;
+    int bi = INT_MAX;
+    for (int s = 0; s < a.nchunks; ++s) {
+      const float v = a.gbest[(size_t)s * a.M + row];
+      const int i = a.gidx[(size_t)s * a.M + row];
+      if (v > best || (v == best && i < bi)) {
+        best = v;
+        bi = i;
+      }
+    }
+    a.tokens[row] = bi;
+  }
+}
+
+cudaError_t launch_reduce(const ReduceArgs& a, StopCtl ctl, cudaStream_t st) {
+  reduce_kernel<<<a.M, 256, 0, st>>>(a, ctl);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------- canvas + loop ----
+__global__ void canvas_init_kernel(int32_t* tokens, int B, int C, int V, uint64_t seed, int block) {
+  const int t = blockIdx.x * blockDim.x + threadIdx.x;
+  if (t >= B * C) return;
+  uint64_t w[4];
+  philox_block(w, seed, block, 0, t / C, t % C, 0, 2);
+  tokens[t] = uniform_token(w[0], V);
+}
+
+cudaError_t launch_canvas_init(int32_t* tokens, int B, int C, int V, uint64_t seed, int block,
+                               cudaStream_t st) {
+  canvas_init_kernel<<<cdiv(B * C, 256), 256, 0, st>>>(tokens, B, C, V, seed, block);
+  return cudaGetLastError();
+}
+
+__global__ void loop_finish_kernel(const int* stop_at, int B, int N, int* steps_taken, int* converged,
+                                   const int* prev_argmax, int* xhat0, int C) {
+  const int t = blockIdx.x * blockDim.x + threadIdx.x;
+  if (t < B) {
+    const int s = stop_at[t];
+    const bool conv = s < N;
+    if (steps_taken) steps_taken[t] = conv ? s + 1 : N;
+    if (converged) converged[t] = conv ? 1 : 0;
+  }
+  if (t < B * C && xhat0) xhat0[t] = prev_argmax[t];
+}
+
+cudaError_t launch_loop_finish(const int* stop_at, int B, int N, int* steps_taken, int* converged,
+                               const int* prev_argmax, int* xhat0, int C, cudaStream_t st) {
+  loop_finish_kernel<<<cdiv(B * C > B ? B * C : B, 256), 256, 0, st>>>(stop_at, B, N, steps_taken,
+                                                                         converged, prev_argmax, xhat0, C);
+  return cudaGetLastError();
+}
+
+}  // namespace dg

@@ -1,0 +1,273 @@
+"""Python binding of libdg (ctypes).
+
+Argument marshalling only: every step of the path runs in the CUDA kernels of
+libdg.  PyTorch supplies device memory and the current stream.  The binding
+fails loudly if the library has not been built (there is no CPU fallback).
+The functions ``dg_*`` of the C ABI are reachable as ``lib().dg_*``; the
+helpers below take torch tensors.
+"""
+from __future__ import annotations
+
+import ctypes as ct
+import math
+import os
+import threading
+from dataclasses import dataclass
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libdg.so")
+_lock = threading.Lock()
+_lib = None
+
+DG_OK, DG_ERR_ARG, DG_ERR_SHAPE, DG_ERR_CAPACITY, DG_ERR_WORKSPACE, DG_ERR_CUDA, DG_ERR_TIMEOUT = range(7)
+
+# Every function the C header declares (checked by the tests).
+EXPORTS = ("dg_status_string", "dg_workspace_size", "dg_read_status", "dg_canvas_init",
+           "dg_denoise_step", "dg_denoise_canvas", "dg_commit_block", "dg_debug_gemm")
+
+
+class DgError(RuntimeError):
+    def __init__(self, code, what):
+        super().__init__(f"{what}: {status_string(code)} ({code})")
+        self.code = code
+
+
+class dg_dims(ct.Structure):
+    _fields_ = [("V", ct.c_int32), ("d", ct.c_int32), ("C", ct.c_int32), ("B", ct.c_int32),
+                ("Hq", ct.c_int32), ("Hkv", ct.c_int32), ("hd", ct.c_int32), ("F", ct.c_int32),
+                ("rope_base", ct.c_float), ("rms_eps", ct.c_float)]
+
+
+class dg_model(ct.Structure):
+    _fields_ = [("dims", dg_dims)] + [(n, ct.c_void_p) for n in ("E", "Wq", "Wk", "Wv", "Wo", "W1", "W2")]
+
+
+class dg_kv_cache(ct.Structure):
+    _fields_ = [("K", ct.c_void_p), ("V", ct.c_void_p), ("cap", ct.c_int32), ("len", ct.c_int32)]
+
+
+class dg_canvas(ct.Structure):
+    _fields_ = [("tokens", ct.c_void_p), ("z", ct.c_void_p), ("alpha", ct.c_void_p),
+                ("prev_argmax", ct.c_void_p)]
+
+
+class dg_step_debug(ct.Structure):
+    _fields_ = [(n, ct.c_void_p) for n in ("a", "q", "k", "v", "o", "h", "u", "g", "logits")]
+
+
+class dg_step_out(ct.Structure):
+    _fields_ = [(n, ct.c_void_p) for n in ("entropy", "argmax", "accept", "n_acc", "mean_H", "stop")] + [
+        ("debug", ct.POINTER(dg_step_debug)), ("events", ct.POINTER(ct.c_void_p))]
+
+
+# Kernel slots of one step (dg_step_out.events), in launch order.
+PROF_SLOTS = ("embed", "qkv", "attn", "oproj", "lmhead", "stats", "sampler", "selfcond", "gumbel",
+              "reduce", "ffw1", "ffw2")
+
+
+class dg_sched(ct.Structure):
+    _fields_ = [("tau0", ct.c_float), ("tau1", ct.c_float), ("N", ct.c_int32), ("b", ct.c_float),
+                ("stop_H", ct.c_float)]
+
+
+class dg_canvas_result(ct.Structure):
+    _fields_ = [(n, ct.c_void_p) for n in ("steps_taken", "converged", "accepted", "xhat0")]
+
+
+def load():
+    """Load libdg.so; raises if it is missing (build it with __graft_entry__.build())."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"libdg is not built ({LIB_PATH} missing); run __graft_entry__.build()")
+            L = ct.CDLL(LIB_PATH)
+            L.dg_status_string.restype = ct.c_char_p
+            L.dg_status_string.argtypes = [ct.c_int32]
+            for name in EXPORTS[1:]:
+                getattr(L, name).restype = ct.c_int32
+            L.dg_workspace_size.argtypes = [ct.POINTER(dg_dims), ct.c_int32, ct.POINTER(ct.c_size_t)]
+            L.dg_read_status.argtypes = [ct.c_void_p, ct.POINTER(ct.c_int32), ct.c_void_p]
+            L.dg_canvas_init.argtypes = [ct.c_void_p, ct.c_int32, ct.c_int32, ct.c_int32, ct.c_uint64,
+                                         ct.c_int32, ct.c_void_p]
+            L.dg_denoise_step.argtypes = [ct.POINTER(dg_model), ct.POINTER(dg_kv_cache),
+                                          ct.POINTER(dg_canvas), ct.c_float, ct.c_float, ct.c_uint64,
+                                          ct.c_int32, ct.c_int32, ct.c_void_p, ct.c_size_t,
+                                          ct.POINTER(dg_step_out), ct.c_void_p]
+            L.dg_denoise_canvas.argtypes = [ct.POINTER(dg_model), ct.POINTER(dg_kv_cache),
+                                            ct.POINTER(dg_canvas), ct.POINTER(dg_sched), ct.c_uint64,
+                                            ct.c_int32, ct.c_void_p, ct.c_size_t,
+                                            ct.POINTER(dg_canvas_result), ct.c_void_p]
+            L.dg_commit_block.argtypes = [ct.POINTER(dg_model), ct.POINTER(dg_kv_cache), ct.c_void_p,
+                                          ct.c_void_p, ct.c_size_t, ct.c_void_p]
+            L.dg_debug_gemm.argtypes = [ct.c_void_p, ct.c_void_p, ct.c_void_p, ct.c_int32, ct.c_int32,
+                                        ct.c_int32, ct.c_int32, ct.c_void_p]
+            _lib = L
+    return _lib
+
+
+lib = load
+
+
+def status_string(code: int) -> str:
+    try:
+        return load().dg_status_string(code).decode()
+    except Exception:  # library missing while formatting an error
+        return "status"
+
+
+def _check(code, what):
+    if code != DG_OK:
+        raise DgError(code, what)
+
+
+def _ptr(t):
+    return None if t is None else ct.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ct.c_void_p(s.cuda_stream)
+
+
+def make_dims(d) -> dg_dims:
+    return dg_dims(V=d.V, d=d.d, C=d.C, B=d.B, Hq=d.Hq, Hkv=d.Hkv, hd=d.hd, F=d.F,
+                   rope_base=d.rope_base, rms_eps=d.rms_eps)
+
+
+def workspace_size(dims, cap: int) -> int:
+    n = ct.c_size_t()
+    _check(load().dg_workspace_size(ct.byref(make_dims(dims)), int(cap), ct.byref(n)), "dg_workspace_size")
+    return n.value
+
+
+class Model:
+    """Weights (bf16 device tensors, [out][in]) and the prefix cache of a batch of canvases."""
+
+    def __init__(self, dims, w: dict, cache_len: int | None = None):
+        self.dims = dims
+        self.w = w
+        self.K, self.V = w["Kc"], w["Vc"]
+        self.cap = self.K.shape[2]
+        self.len = dims.P if cache_len is None else cache_len
+        self.s = dg_model(make_dims(dims), *[ct.c_void_p(w[k].data_ptr()) for k in
+                                             ("E", "Wq", "Wk", "Wv", "Wo", "W1", "W2")])
+        self.ws_bytes = workspace_size(dims, self.cap)
+        # zero-initialised: the first word is the device status word
+        self.ws = torch.zeros(self.ws_bytes + 256, dtype=torch.uint8, device=self.K.device)
+        off = (-self.ws.data_ptr()) % 256
+        self.ws_ptr = ct.c_void_p(self.ws.data_ptr() + off)
+
+    def cache(self) -> dg_kv_cache:
+        return dg_kv_cache(ct.c_void_p(self.K.data_ptr()), ct.c_void_p(self.V.data_ptr()), self.cap, self.len)
+
+    def status(self) -> int:
+        st = ct.c_int32()
+        _check(load().dg_read_status(self.ws_ptr, ct.byref(st), _stream()), "dg_read_status")
+        return st.value
+
+
+@dataclass
+class Canvas:
+    tokens: torch.Tensor          # int32 [B, C]
+    z: torch.Tensor               # bf16 [B, C, d]
+    alpha: torch.Tensor           # fp32 [B, C]
+    prev_argmax: torch.Tensor | None = None
+
+    def __post_init__(self):
+        if self.prev_argmax is None:
+            self.prev_argmax = torch.zeros_like(self.tokens)
+
+    def struct(self) -> dg_canvas:
+        return dg_canvas(_ptr(self.tokens), _ptr(self.z), _ptr(self.alpha), _ptr(self.prev_argmax))
+
+
+def denoise_step(model: Model, canvas: Canvas, tau: float, b: float, seed: int, step: int, block: int = 0,
+                 debug: bool = False, stream=None, events=None, out=None) -> dict:
+    """One denoising step (dg_denoise_step); updates canvas in place, returns outputs.
+
+    events: optional list of 2 * len(PROF_SLOTS) recorded torch.cuda.Event (per-kernel timing).
+    out: optional dict of preallocated output tensors (as returned by a previous call).
+    """
+    d = model.dims
+    dev = canvas.tokens.device
+    M = d.B * d.C
+    if out is None:
+        out = dict(entropy=torch.empty(d.B, d.C, dtype=torch.float32, device=dev),
+                   argmax=torch.empty(d.B, d.C, dtype=torch.int32, device=dev),
+                   accept=torch.empty(d.B, d.C, dtype=torch.uint8, device=dev),
+                   n_acc=torch.empty(d.B, dtype=torch.int32, device=dev),
+                   mean_H=torch.empty(d.B, dtype=torch.float32, device=dev),
+                   stop=torch.empty(d.B, dtype=torch.int32, device=dev))
+    so = dg_step_out(*[_ptr(out[k]) for k in ("entropy", "argmax", "accept", "n_acc", "mean_H", "stop")])
+    if events is not None:
+        arr = (ct.c_void_p * len(events))(*[ct.c_void_p(e.cuda_event if e is not None else 0) for e in events])
+        so.events = ct.cast(arr, ct.POINTER(ct.c_void_p))
+    dbg = None
+    if debug:
+        bf = dict(dtype=torch.bfloat16, device=dev)
+        dbg_t = dict(a=torch.empty(M, d.d, **bf), q=torch.empty(d.B, d.Hq, d.C, d.hd, **bf),
+                     k=torch.empty(d.B, d.Hkv, d.C, d.hd, **bf), v=torch.empty(d.B, d.Hkv, d.C, d.hd, **bf),
+                     o=torch.empty(M, d.Hq * d.hd, **bf), h=torch.empty(M, d.d, **bf),
+                     u=torch.empty(M, d.d, **bf), g=torch.empty(M, d.F, **bf),
+                     logits=torch.empty(M, d.V, dtype=torch.float32, device=dev))
+        dbg = dg_step_debug(*[_ptr(dbg_t[k]) for k in ("a", "q", "k", "v", "o", "h", "u", "g", "logits")])
+        so.debug = ct.pointer(dbg)
+        out["debug"] = dbg_t
+    cs = canvas.struct()
+    cache = model.cache()
+    rc = load().dg_denoise_step(ct.byref(model.s), ct.byref(cache), ct.byref(cs), float(tau), float(b),
+                                int(seed), int(step), int(block), model.ws_ptr, model.ws_bytes,
+                                ct.byref(so), _stream(stream))
+    _check(rc, "dg_denoise_step")
+    return out
+
+
+def tau_schedule(N=48, tau0=0.8, tau1=0.4):
+    return [tau0 + (tau1 - tau0) * s / (N - 1) if N > 1 else tau0 for s in range(N)]
+
+
+def denoise_canvas(model: Model, canvas: Canvas, seed: int, block: int = 0, N: int = 48, tau0: float = 0.8,
+                   tau1: float = 0.4, b: float = 0.1, stop_H: float = 0.005, stream=None) -> dict:
+    """The annealed loop (dg_denoise_canvas); returns device tensors of the result."""
+    d = model.dims
+    dev = canvas.tokens.device
+    res = dict(steps_taken=torch.empty(d.B, dtype=torch.int32, device=dev),
+               converged=torch.empty(d.B, dtype=torch.int32, device=dev),
+               accepted=torch.empty(d.B, N, dtype=torch.int32, device=dev),
+               xhat0=torch.empty(d.B, d.C, dtype=torch.int32, device=dev))
+    rs = dg_canvas_result(*[_ptr(res[k]) for k in ("steps_taken", "converged", "accepted", "xhat0")])
+    sched = dg_sched(tau0, tau1, N, b, stop_H)
+    cs = canvas.struct()
+    cache = model.cache()
+    rc = load().dg_denoise_canvas(ct.byref(model.s), ct.byref(cache), ct.byref(cs), ct.byref(sched), int(seed),
+                                  int(block), model.ws_ptr, model.ws_bytes, ct.byref(rs), _stream(stream))
+    _check(rc, "dg_denoise_canvas")
+    return res
+
+
+def commit_block(model: Model, tokens: torch.Tensor, stream=None) -> None:
+    """Append the re-encoded K/V of tokens [B, C] to the cache (dg_commit_block)."""
+    cache = model.cache()
+    rc = load().dg_commit_block(ct.byref(model.s), ct.byref(cache), _ptr(tokens), model.ws_ptr,
+                                model.ws_bytes, _stream(stream))
+    _check(rc, "dg_commit_block")
+    model.len = cache.len
+
+
+def canvas_init(B, C, V, seed, block=0, device="cuda", stream=None) -> torch.Tensor:
+    t = torch.empty(B, C, dtype=torch.int32, device=device)
+    _check(load().dg_canvas_init(_ptr(t), B, C, V, int(seed), int(block), _stream(stream)), "dg_canvas_init")
+    return t
+
+
+def debug_gemm(A: torch.Tensor, Bm: torch.Tensor, b_mn_major: int = 0, stream=None) -> torch.Tensor:
+    """fp32 A B^T on the tensor-core engine; B is [N][K] (b_mn_major=0) or [K][N] (1 or 2)."""
+    M, K = A.shape
+    N = Bm.shape[0] if b_mn_major == 0 else Bm.shape[1]
+    D = torch.empty(M, N, dtype=torch.float32, device=A.device)
+    _check(load().dg_debug_gemm(_ptr(A), _ptr(Bm), _ptr(D), M, N, K, b_mn_major, _stream(stream)),
+           "dg_debug_gemm")
+    return D

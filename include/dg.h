@@ -1,0 +1,244 @@
+/*
+ * dg.h -- C ABI of the GB300 block-diffusion denoising library (libdg.so).
+ *
+ * The library computes the hot path of a DiffusionGemma-style uniform-state
+ * text diffusion decoder on one GPU: denoising steps over a C-token canvas that
+ * reads a static prefix KV cache, the annealed loop of such steps, and the
+ * commit of a finished block into the cache.
+ *
+ * Sources of the operations (page title, then section):
+ *   [TR]   "DiffusionGemma Technical Report" summary page: "Method step
+ *          details" (inference steps 1-5) and the reproduction paragraph that
+ *          lists the sampler hyper-parameters of the report's Table 2.
+ *   [EXP]  "DiffusionGemma explained" (Gemma docs): "Uniform State Diffusion",
+ *          "Architecture: incremental prefill and denoising",
+ *          "Self-conditioning", "Multi-canvas sampling".
+ *   [CH12] "DiffusionGemma" chapter of the diffusion docs: the KV-cache timing
+ *          list, the attention-mask list and the data-flow pseudocode.
+ * The model is a one-layer synthetic stand-in: RMSNorm of embedding plus
+ * self-conditioning, one GQA attention layer with RoPE, a tied LM head with a
+ * per-position logit sharpness alpha, and a two-matrix FFW for
+ * self-conditioning.
+ *
+ * Conventions for every entry point:
+ *  - All tensors are caller-owned DEVICE buffers unless stated otherwise; the
+ *    library never allocates device memory and keeps no per-model state.
+ *  - bf16 tensors are IEEE bfloat16, row-major, densely packed.  Weight
+ *    matrices are stored [out][in] (the row of W that produces output n is
+ *    contiguous), so y = x W^T.
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  Every
+ *    call only enqueues work on `stream` and returns; the exceptions are said.
+ *  - Arguments are validated before anything is enqueued: on any error code no
+ *    device memory has been written.
+ *  - The workspace `ws` (size from dg_workspace_size, 256-byte aligned) holds
+ *    intermediates between calls of one step; its first 4 bytes are a device
+ *    status word that kernels set to DG_ERR_TIMEOUT if a bounded wait inside a
+ *    kernel ran out (read it with dg_read_status); zero the workspace (or at
+ *    least that word) before its first use.  Calls sharing one workspace must
+ *    not overlap on the GPU.
+ */
+#ifndef DG_H
+#define DG_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define DG_API __attribute__((visibility("default")))
+#else
+#define DG_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int32_t dg_status;
+enum {
+  DG_OK = 0,
+  DG_ERR_ARG = 1,        /* null pointer, non-positive size, inconsistent dims */
+  DG_ERR_SHAPE = 2,      /* a size the kernels do not support (see dg_dims) */
+  DG_ERR_CAPACITY = 3,   /* commit would write past the cache capacity */
+  DG_ERR_WORKSPACE = 4,  /* workspace too small or misaligned */
+  DG_ERR_CUDA = 5,       /* a CUDA runtime call or kernel launch failed */
+  DG_ERR_TIMEOUT = 6     /* a bounded device-side wait ran out (status word) */
+};
+
+/* Model and canvas sizes.
+ *   V    vocabulary size (multiple of 8)
+ *   d    model width (multiple of 64, <= 16384)
+ *   C    canvas length (1..1024); B canvases are processed together
+ *   Hq   query heads, Hkv key/value heads (Hq % Hkv == 0, grouped-query)
+ *   hd   head dim: 32, 64 or 128
+ *   F    self-conditioning FFW hidden width (multiple of 64)
+ *   rope_base  RoPE base (10000); rms_eps  RMSNorm epsilon (1e-6)          */
+typedef struct dg_dims {
+  int32_t V, d, C, B, Hq, Hkv, hd, F;
+  float rope_base, rms_eps;
+} dg_dims;
+
+/* Weights (device, bf16):
+ *   E  [V][d]        tied token embedding and LM head
+ *   Wq [Hq*hd][d], Wk [Hkv*hd][d], Wv [Hkv*hd][d], Wo [d][Hq*hd]
+ *   W1 [F][d], W2 [d][F]                                                    */
+typedef struct dg_model {
+  dg_dims dims;
+  const void *E, *Wq, *Wk, *Wv, *Wo, *W1, *W2;
+} dg_model;
+
+/* Static prefix KV cache ([CH12] "prompt / finished output block -> causal
+ * encoder prefill -> written to the KV cache"; [EXP] incremental prefill).
+ * K, V: bf16 [B][Hkv][cap][hd]; rows 0..len-1 of every (canvas, head) are
+ * valid, keys already rotated by RoPE at their absolute positions.  `len` is
+ * a host value: every canvas of the batch has the same prefix length.      */
+typedef struct dg_kv_cache {
+  void *K, *V;
+  int32_t cap;
+  int32_t len;
+} dg_kv_cache;
+
+/* Canvas state of B canvases ([TR] steps 2-3):
+ *   tokens       int32 [B][C]   x_t on entry, x_{t+1} on return
+ *   z            bf16 [B][C][d] self-conditioning z_t on entry, z_{t+1} on return
+ *   alpha        fp32 [B][C]    per-position logit sharpness (> 0)
+ *   prev_argmax  int32 [B][C]   argmax of the previous step on entry (read only
+ *                               when step >= 1), this step's argmax on return */
+typedef struct dg_canvas {
+  int32_t* tokens;
+  void* z;
+  const float* alpha;
+  int32_t* prev_argmax;
+} dg_canvas;
+
+/* Optional copies of the intermediates of one step, for checking (every
+ * pointer may be NULL).  Device buffers:
+ *   a, h [B*C][d]; q [B][Hq][C][hd]; k, v [B][Hkv][C][hd]; o [B*C][Hq*hd];
+ *   u [B*C][d]; g [B*C][F]  (bf16)      logits fp32 [B*C][V] (l = alpha h.E / sqrt d) */
+typedef struct dg_step_debug {
+  void *a, *q, *k, *v, *o, *h, *u, *g;
+  float* logits;
+} dg_step_debug;
+
+/* Kernel slots of a step, in launch order, for dg_step_out.events. */
+enum {
+  DG_PROF_EMBED = 0,     /* embedding + self-conditioning + RMSNorm   */
+  DG_PROF_QKV = 1,       /* q, k, v projections with RoPE             */
+  DG_PROF_ATTN = 2,      /* attention over prefix + canvas (+ merge)  */
+  DG_PROF_OPROJ = 3,     /* output projection + residual              */
+  DG_PROF_LMHEAD = 4,    /* LM head with softmax statistics           */
+  DG_PROF_STATS = 5,     /* merge of the statistics: entropy, argmax  */
+  DG_PROF_SAMPLER = 6,   /* sort, cumulative entropy, accept, renoise */
+  DG_PROF_SELFCOND = 7,  /* p0 . E on the tensor cores                */
+  DG_PROF_GUMBEL = 8,    /* Gumbel-max search of accepted positions   */
+  DG_PROF_REDUCE = 9,    /* reduction of p0 . E, sampled tokens        */
+  DG_PROF_FFW1 = 10,     /* GELU(W1 u)                                */
+  DG_PROF_FFW2 = 11,     /* z = W2 g                                  */
+  DG_PROF_NUM = 12
+};
+
+/* Per-step outputs (device; any pointer may be NULL except where noted):
+ *   entropy  fp32 [B][C]  entropy of softmax(l / tau) in nats
+ *   argmax   int32 [B][C] argmax_v l (lowest index on ties)
+ *   accept   uint8 [B][C] 1 where the position was accepted
+ *   n_acc    int32 [B]    accepted positions per canvas
+ *   mean_H   fp32 [B]     mean entropy of the canvas
+ *   stop     int32 [B]    1 when the adaptive stop test fired at this step
+ *   debug    host pointer to a dg_step_debug, or NULL
+ *   events   host array of 2 * DG_PROF_NUM cudaEvent_t (caller-created), or
+ *            NULL: events[2k] / events[2k+1] are recorded on `stream` just
+ *            before / after the kernels of slot k (for per-kernel timing);
+ *            NULL entries are skipped                                       */
+typedef struct dg_step_out {
+  float* entropy;
+  int32_t* argmax;
+  uint8_t* accept;
+  int32_t* n_acc;
+  float* mean_H;
+  int32_t* stop;
+  const dg_step_debug* debug;
+  void* const* events;
+} dg_step_out;
+
+/* Sampler schedule ([TR] step 3 and Table 2): tau_s = tau0 + (tau1 - tau0) *
+ * s / (N - 1) for s = 0..N-1; entropy budget b; stop when the mean entropy of
+ * the canvas is <= stop_H and the argmax equals the previous step's.  Defaults
+ * 0.8, 0.4, 48, 0.1, 0.005.                                                 */
+typedef struct dg_sched {
+  float tau0, tau1;
+  int32_t N;
+  float b, stop_H;
+} dg_sched;
+
+/* Result of the denoising loop (device buffers):
+ *   steps_taken int32 [B]; converged int32 [B] (1 = stopped early);
+ *   accepted int32 [B][N] (accepted count per step, -1 after the canvas stopped);
+ *   xhat0 int32 [B][C] (argmax of the canvas's last step: the block to commit) */
+typedef struct dg_canvas_result {
+  int32_t* steps_taken;
+  int32_t* converged;
+  int32_t* accepted;
+  int32_t* xhat0;
+} dg_canvas_result;
+
+/* Human-readable name of a status code (static string). */
+DG_API const char* dg_status_string(dg_status s);
+
+/* Bytes of workspace needed for `dims` with a prefix cache of up to `cap`
+ * rows.  Returns DG_ERR_ARG / DG_ERR_SHAPE for unsupported dims.             */
+DG_API dg_status dg_workspace_size(const dg_dims* dims, int32_t cap, size_t* bytes);
+
+/* Copies the device status word of `ws` to *status (synchronises `stream`). */
+DG_API dg_status dg_read_status(const void* ws, int32_t* status, void* stream);
+
+/* Initial canvas, [TR] step 2: tokens[b][i] uniform over [0, V) from the
+ * Philox stream of (seed, block, canvas b, position i); also the uniform
+ * token law used for renoising ([EXP] "Uniform State Diffusion").           */
+DG_API dg_status dg_canvas_init(int32_t* tokens, int32_t B, int32_t C, int32_t V, uint64_t seed,
+                         int32_t block, void* stream);
+
+/* One denoising step over B canvases, [TR] step 3 (with the stop test of
+ * step 4):
+ *   a = RMSNorm(E[x_t] + z_t); q, k = RoPE(a Wq^T, a Wk^T) at positions
+ *   len + i, v = a Wv^T; o = softmax(q [K_pre ; k]^T / sqrt hd) [V_pre ; v]
+ *   (no mask: canvas queries see every canvas key and the whole prefix);
+ *   h = a + o Wo^T; l = alpha h E^T / sqrt d; p0 = softmax(l / tau);
+ *   positions sorted by ascending entropy are accepted while the cumulative
+ *   entropy stays <= b; accepted positions take the Gumbel-max sample of
+ *   l / tau, all others a uniform random token; z_{t+1} = W2 GELU(W1 (p0 E)).
+ * Random draws are Philox4x64-10 keyed by (seed, block, step, canvas,
+ * position).  The cache is read only.  Canvas state is updated in place.    */
+DG_API dg_status dg_denoise_step(const dg_model* model, const dg_kv_cache* cache, dg_canvas* canvas,
+                          float tau, float b, uint64_t seed, int32_t step, int32_t block,
+                          void* ws, size_t ws_bytes, dg_step_out* out, void* stream);
+
+/* The annealed denoising loop of one block, [TR] steps 3-4: up to sched->N
+ * steps with the linear temperature schedule; each canvas stops on its own
+ * when its stop test fires and is left unchanged afterwards; work for steps
+ * after every canvas stopped is skipped on the device.  Enqueues everything
+ * without synchronising.  canvas->tokens/z must hold the initial canvas
+ * (dg_canvas_init, z = 0).                                                 */
+DG_API dg_status dg_denoise_canvas(const dg_model* model, const dg_kv_cache* cache, dg_canvas* canvas,
+                            const dg_sched* sched, uint64_t seed, int32_t block, void* ws,
+                            size_t ws_bytes, dg_canvas_result* result, void* stream);
+
+/* Commit of a finished block, [TR] step 5 and [CH12] KV-cache timing: the
+ * tokens int32 [B][C] are re-encoded by the encoder path (RMSNorm(E[x]), no
+ * self-conditioning) and their keys (RoPE at positions len..len+C-1) and
+ * values are written to cache rows len..len+C-1; then cache->len += C.
+ * DG_ERR_CAPACITY (nothing written) if len + C > cap.                       */
+DG_API dg_status dg_commit_block(const dg_model* model, dg_kv_cache* cache, const int32_t* tokens,
+                          void* ws, size_t ws_bytes, void* stream);
+
+/* Diagnostics of the tensor-core GEMM engine, used by the tests to check it
+ * in isolation (not a step of the method).  D fp32 [M][N] = A B^T with
+ * A bf16 [M][K], and B bf16 [N][K] when b_mn_major == 0, or B bf16 [K][N]
+ * when b_mn_major == 1 (the layout of E in the self-conditioning contraction).
+ * K, N multiples of 8.                                                        */
+DG_API dg_status dg_debug_gemm(const void* A, const void* Bm, float* D, int32_t M, int32_t N, int32_t K,
+                        int32_t b_mn_major, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DG_H */

@@ -277,10 +277,13 @@ def denoise_step(dims, w, x, z, alpha, tau, b, seed, step, block=0, prev_argmax=
                 _p(pa, _I) if pa is not None else None, float(tau), float(b), float(stop_H),
                 int(seed), int(step), int(block))
     rr = _i32(rows) if rows is not None else None
+    nrows = 0 if rr is None else rr.size
+    if rr is not None and rr.size == 0:
+        rr = np.zeros(1, dtype=np.int32)  # non-null pointer: front stages only
     D = _dims(dims, mirror_bf16)
     rc = lib().or_denoise_step(ct.byref(D), ct.byref(si), ct.byref(so),
                                _p(rr, _I) if rr is not None else None,
-                               0 if rr is None else rr.size, nthreads or default_threads())
+                               nrows, nthreads or default_threads())
     if rc != 0:
         raise ValueError("oracle denoise_step: bad arguments")
     if "accept" in outs:

@@ -1,0 +1,108 @@
+"""One denoising step through the C ABI against the CPU oracle on the same seeded inputs."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from block_diffusion_text_gb300 import synth
+
+from parity import (Collect, bf16_to_np, check_argmax, check_close_bf16, check_entropy, check_logits,
+                    check_rel_l2, check_sampler)
+
+pytestmark = pytest.mark.gpu
+
+RAGGED = synth.Dims(V=1000, d=128, C=40, B=3, Hq=4, Hkv=2, hd=64, F=192, P=100, cap=160)
+
+
+def _setup(dims, seed, alpha=None):
+    from block_diffusion_text_gb300 import dg
+    w = synth.make_weights(dims, seed, device="cpu")
+    x, z, a = synth.make_canvas(dims, seed, device="cpu")
+    if alpha is not None:
+        a = torch.full_like(a, alpha)
+    model = dg.Model(dims, {k: v.cuda() for k, v in w.items()})
+    canvas = dg.Canvas(x.cuda(), z.cuda(), a.cuda())
+    return w, x, z, a, model, canvas
+
+
+def _run_and_compare(dims, seed, tau=0.8, b=0.1, step=0, alpha=None, z_in=None, prev=None):
+    from block_diffusion_text_gb300 import dg
+    w, x, z, a, model, canvas = _setup(dims, seed, alpha)
+    if z_in is not None:
+        z = z_in
+        canvas.z.copy_(z.cuda())
+    if prev is not None:
+        canvas.prev_argmax.copy_(torch.as_tensor(prev).cuda())
+    out = dg.denoise_step(model, canvas, tau=tau, b=b, seed=seed, step=step, debug=True)
+    torch.cuda.synchronize()
+    assert model.status() == 0
+    wn = synth.to_numpy_f32(w)
+    ref = oracle.denoise_step(dims, wn, x.numpy(), z.float().numpy(), a.numpy(), tau=tau, b=b, seed=seed,
+                              step=step, prev_argmax=prev,
+                              want=("a", "q", "k", "v", "o", "h", "logits", "H", "m", "Z", "top2gap",
+                                    "argmax", "accept", "cum", "rank", "renoise_tok", "sample_tok",
+                                    "gumbel_gap", "tokens_out", "u", "g", "z_out", "n_acc", "meanH",
+                                    "stop"))
+    dbg = out["debug"]
+    B, C, Hq, Hkv, hd = dims.B, dims.C, dims.Hq, dims.Hkv, dims.hd
+    ck = Collect()
+    ck(check_close_bf16, "a", bf16_to_np(dbg["a"]), ref["a"])
+    q = bf16_to_np(dbg["q"]).reshape(B, Hq, C, hd).transpose(0, 2, 1, 3).reshape(B * C, Hq * hd)
+    ck(check_close_bf16, "q", q, ref["q"])
+    k = bf16_to_np(dbg["k"]).reshape(B, Hkv, C, hd).transpose(0, 2, 1, 3).reshape(B * C, Hkv * hd)
+    ck(check_close_bf16, "k", k, ref["k"])
+    v = bf16_to_np(dbg["v"]).reshape(B, Hkv, C, hd).transpose(0, 2, 1, 3).reshape(B * C, Hkv * hd)
+    ck(check_close_bf16, "v", v, ref["v"])
+    ck(check_close_bf16, "o", bf16_to_np(dbg["o"]), ref["o"])
+    ck(check_close_bf16, "h", bf16_to_np(dbg["h"]), ref["h"])
+    ck(check_logits, dbg["logits"].cpu().numpy(), ref["logits"])
+    ck(check_entropy, out["entropy"].cpu().numpy().reshape(-1), ref["H"])
+    scale = np.max(np.abs(ref["logits"]), axis=1)
+    n_am = ck(check_argmax, out["argmax"].cpu().numpy(), ref["argmax"], ref["top2gap"], scale)
+    stats = ck(check_sampler, out["accept"].cpu().numpy(), canvas.tokens.cpu().numpy(), ref, b, C)
+    # u, g, z: the stated relative-L2 tolerance (a chain of three bf16 roundings)
+    ck(check_rel_l2, "u", bf16_to_np(dbg["u"]), ref["u"])
+    ck(check_rel_l2, "g", bf16_to_np(dbg["g"]), ref["g"])
+    zz = bf16_to_np(canvas.z).reshape(B * C, dims.d)
+    ck(check_rel_l2, "z", zz, ref["z_out"])
+    # per-canvas scalars
+    def scalars():
+        if stats and stats["boundary_excused"] == 0:
+            assert np.array_equal(out["n_acc"].cpu().numpy(), ref["n_acc"]), (out["n_acc"], ref["n_acc"])
+        assert np.allclose(out["mean_H"].cpu().numpy(), ref["meanH"], atol=1e-3), "mean_H"
+        if n_am == 0:
+            assert np.array_equal(out["stop"].cpu().numpy(), ref["stop"]), "stop"
+            assert np.array_equal(canvas.prev_argmax.cpu().numpy().reshape(-1), ref["argmax"]), "prev"
+    ck(scalars)
+    print(dims, "stats", stats, "n_acc", out["n_acc"].cpu().numpy(), ref["n_acc"])
+    ck.done()
+    return out, ref, stats
+
+
+def test_tiny_step():
+    dims, seed = synth.workload("tiny_v512_c16")
+    _run_and_compare(dims, seed)
+
+
+def test_tiny_step_sharp_alpha_accepts_all():
+    dims, seed = synth.workload("tiny_v512_c16")
+    out, ref, stats = _run_and_compare(dims, seed, alpha=64.0, tau=0.4)
+    assert stats["accepted"] == dims.C
+
+
+def test_ragged_step_later_step_with_z():
+    # several canvases, a vocabulary that leaves a partial tile, M not a multiple of 128
+    seed = 11
+    g = torch.Generator().manual_seed(5)
+    z = (torch.randn(RAGGED.B, RAGGED.C, RAGGED.d, generator=g) * 0.02).to(torch.bfloat16)
+    prev = np.random.default_rng(1).integers(0, RAGGED.V, size=(RAGGED.B, RAGGED.C)).astype(np.int32)
+    _run_and_compare(RAGGED, seed, tau=0.55, step=3, z_in=z, prev=prev)
+
+
+@pytest.mark.slow
+def test_single_step_v32k():
+    dims, seed = synth.workload("step_v32k_c256_p2k")
+    out, ref, stats = _run_and_compare(dims, seed)
+    print("accepted", stats)
