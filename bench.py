@@ -168,10 +168,11 @@ def _traffic(kernel: str):
         e = t.get(kernel)
         if not e:
             return None
-        src = os.path.join(ROOT, e["source"])
-        with open(src, "rb") as f:
-            if hashlib.sha256(f.read()).hexdigest() != e["source_sha256"]:
-                return None
+        srcs = {e["source"]: e["source_sha256"], **e.get("also", {})}
+        for rel, sha in srcs.items():
+            with open(os.path.join(ROOT, rel), "rb") as f:
+                if hashlib.sha256(f.read()).hexdigest() != sha:
+                    return None
         return float(e["bytes_per_launch_full_size"])
     except Exception:
         return None

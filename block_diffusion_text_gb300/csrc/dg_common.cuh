@@ -55,10 +55,14 @@ DG_DEV bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // recording the timeout in *status and raising *abort) if the wait ran out or
 // another role of the CTA already gave up.
 DG_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, int* status, volatile int* abort) {
-  if (mbar_try_wait(bar, parity)) return true;
-  uint64_t t0 = globaltimer();
-  while (true) {
+#pragma unroll 1
+  for (int i = 0; i < 256; ++i)
     if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 64; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
     if (*abort) return false;
     if (globaltimer() - t0 > kWaitLimitNs) {
       atomicExch(status, kStatusTimeout);

@@ -656,34 +656,46 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   } else {
     // Transform warps: rebuild p0 = exp(s - m_tile) * exp(m_tile - m) / l in
     // place, thread t owning row t of each 128-row half.
+    // Row t occupies bytes [128 t, 128 t + 128) of its 128-row box; the 128-byte
+    // swizzle permutes its eight 16-byte chunks by (t mod 8), so walking the
+    // physical chunks (c xor t) keeps the eight threads of each quarter-warp
+    // on distinct banks.  Each row's scale factor is fetched one tile ahead.
     const int t = threadIdx.x - 64;
     const int rows[2] = {m0 + t, m0 + kBM + t};
-    float f[2] = {0.f, 0.f};
-    int cur_vt = -1;
+    auto fetch = [&](int vt, int h) -> float {
+      const size_t o = (size_t)vt * a.M + rows[h];
+      return (rows[h] < a.M && vt * kLmBN < a.V) ? a.fscale[o] : 0.f;
+    };
+    int cur_vt = (kb0 * kBK) / kLmBN;
+    float f[2] = {fetch(cur_vt, 0), fetch(cur_vt, 1)};
+    float fn[2] = {fetch(cur_vt + 1, 0), fetch(cur_vt + 1, 1)};
     int stage = 0;
     uint32_t phase = 0;
     for (int kb = kb0; kb < kb1; ++kb) {
-      if (!mbar_wait(&full[stage], phase, status, abort)) break;
       const int vt = (kb * kBK) / kLmBN;
       if (vt != cur_vt) {
         cur_vt = vt;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) f[h] = rows[h] < a.M ? a.fscale[(size_t)vt * a.M + rows[h]] : 0.f;
+        f[0] = fn[0];
+        f[1] = fn[1];
+        fn[0] = fetch(vt + 1, 0);
+        fn[1] = fetch(vt + 1, 1);
       }
+      if (!mbar_wait(&full[stage], phase, status, abort)) break;
       uint8_t* sa = smem + stage * ScLayout::kStage;
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         uint4* rowp = reinterpret_cast<uint4*>(sa + h * (kBM * kBK * 2) + t * 128);
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
-          uint4 x = rowp[c];
+          const int pc = c ^ (t & 7);
+          uint4 x = rowp[pc];
           const __nv_bfloat16* xb = reinterpret_cast<const __nv_bfloat16*>(&x);
           uint4 y;
           y.x = pack_bf16(__bfloat162float(xb[0]) * f[h], __bfloat162float(xb[1]) * f[h]);
           y.y = pack_bf16(__bfloat162float(xb[2]) * f[h], __bfloat162float(xb[3]) * f[h]);
           y.z = pack_bf16(__bfloat162float(xb[4]) * f[h], __bfloat162float(xb[5]) * f[h]);
           y.w = pack_bf16(__bfloat162float(xb[6]) * f[h], __bfloat162float(xb[7]) * f[h]);
-          rowp[c] = y;
+          rowp[pc] = y;
         }
       }
       fence_proxy_async_smem();

@@ -271,3 +271,4 @@ def debug_gemm(A: torch.Tensor, Bm: torch.Tensor, b_mn_major: int = 0, stream=No
     _check(load().dg_debug_gemm(_ptr(A), _ptr(Bm), _ptr(D), M, N, K, b_mn_major, _stream(stream)),
            "dg_debug_gemm")
     return D
+

@@ -1,0 +1,142 @@
+"""The C-ABI library without a GPU: it loads, exports every declared symbol, and
+rejects bad arguments with the documented codes before touching the device.
+Device pointers passed here are never dereferenced: every call takes an error
+path that returns before any CUDA call."""
+import ctypes as ct
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def dg():
+    import __graft_entry__ as g
+    from block_diffusion_text_gb300 import dg as _dg
+    if not os.path.exists(_dg.LIB_PATH):
+        g.build_cuda()
+    _dg.load()
+    return _dg
+
+
+def _declared():
+    with open(os.path.join(ROOT, "include", "dg.h")) as f:
+        text = f.read()
+    return sorted(set(re.findall(r"DG_API[^;(]*?\b(dg_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    names = _declared()
+    for n in ("dg_denoise_step", "dg_denoise_canvas", "dg_commit_block", "dg_workspace_size"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(dg):
+    lib = ct.CDLL(dg.LIB_PATH)
+    for n in _declared():
+        assert hasattr(lib, n), n
+    assert set(_declared()) == set(dg.EXPORTS)
+
+
+def test_status_strings(dg):
+    L = dg.load()
+    seen = {L.dg_status_string(c).decode() for c in range(7)}
+    assert len(seen) == 7
+    assert L.dg_status_string(99).decode() == "unknown status"
+
+
+def _dims(**kw):
+    from block_diffusion_text_gb300 import synth
+    d = synth.workload("step_v32k_c256_p2k")[0]
+    from dataclasses import replace
+    return replace(d, **kw)
+
+
+def test_workspace_size_validates_dims(dg):
+    L = dg.load()
+    n = ct.c_size_t()
+    assert L.dg_workspace_size(ct.byref(dg.make_dims(_dims())), 2048, ct.byref(n)) == dg.DG_OK
+    assert n.value > 2 * 256 * 32768  # holds at least the exp(s - m) tiles
+    bad = [(dict(V=1001), dg.DG_ERR_SHAPE), (dict(hd=96), dg.DG_ERR_SHAPE), (dict(Hq=6, Hkv=4), dg.DG_ERR_ARG),
+           (dict(C=2048), dg.DG_ERR_SHAPE), (dict(d=1000), dg.DG_ERR_SHAPE), (dict(F=100), dg.DG_ERR_SHAPE),
+           (dict(B=0), dg.DG_ERR_ARG)]
+    for kw, code in bad:
+        assert L.dg_workspace_size(ct.byref(dg.make_dims(_dims(**kw))), 2048, ct.byref(n)) == code, kw
+    assert L.dg_workspace_size(None, 2048, ct.byref(n)) == dg.DG_ERR_ARG
+    assert L.dg_workspace_size(ct.byref(dg.make_dims(_dims())), -1, ct.byref(n)) == dg.DG_ERR_ARG
+    # grows with the cache capacity (attention partials are sized for it)
+    n2 = ct.c_size_t()
+    L.dg_workspace_size(ct.byref(dg.make_dims(_dims())), 131072, ct.byref(n2))
+    assert n2.value >= n.value
+
+
+FAKE = 1 << 20  # a non-null address that is never dereferenced on these paths
+
+
+def _structs(dg, dims, ws_bytes=None, cap=2048, length=2048):
+    m = dg.dg_model(dg.make_dims(dims), *[ct.c_void_p(FAKE)] * 7)
+    c = dg.dg_kv_cache(ct.c_void_p(FAKE), ct.c_void_p(FAKE), cap, length)
+    cv = dg.dg_canvas(*[ct.c_void_p(FAKE)] * 4)
+    L = dg.load()
+    n = ct.c_size_t()
+    L.dg_workspace_size(ct.byref(dg.make_dims(dims)), cap, ct.byref(n))
+    return m, c, cv, n.value if ws_bytes is None else ws_bytes
+
+
+def test_step_argument_errors(dg):
+    L = dg.load()
+    dims = _dims()
+    m, c, cv, wsb = _structs(dg, dims)
+    ws = ct.c_void_p(1 << 30)
+    call = lambda m_, c_, cv_, tau, ws_, wsb_: L.dg_denoise_step(
+        m_, c_, cv_, tau, 0.1, 1, 0, 0, ws_, wsb_, None, None)
+    assert call(None, ct.byref(c), ct.byref(cv), 0.8, ws, wsb) == dg.DG_ERR_ARG
+    assert call(ct.byref(m), None, ct.byref(cv), 0.8, ws, wsb) == dg.DG_ERR_ARG
+    assert call(ct.byref(m), ct.byref(c), None, 0.8, ws, wsb) == dg.DG_ERR_ARG
+    assert call(ct.byref(m), ct.byref(c), ct.byref(cv), 0.0, ws, wsb) == dg.DG_ERR_ARG
+    assert call(ct.byref(m), ct.byref(c), ct.byref(cv), 0.8, ws, wsb - 1) == dg.DG_ERR_WORKSPACE
+    assert call(ct.byref(m), ct.byref(c), ct.byref(cv), 0.8, ct.c_void_p((1 << 30) + 8), wsb) == \
+        dg.DG_ERR_WORKSPACE
+    assert call(ct.byref(m), ct.byref(c), ct.byref(cv), 0.8, None, wsb) == dg.DG_ERR_ARG
+    c_bad = dg.dg_kv_cache(ct.c_void_p(FAKE), ct.c_void_p(FAKE), 100, 200)   # len > cap
+    assert call(ct.byref(m), ct.byref(c_bad), ct.byref(cv), 0.8, ws, wsb) == dg.DG_ERR_ARG
+    m_null = dg.dg_model(dg.make_dims(dims), *([ct.c_void_p(FAKE)] * 6 + [None]))
+    assert call(ct.byref(m_null), ct.byref(c), ct.byref(cv), 0.8, ws, wsb) == dg.DG_ERR_ARG
+
+
+def test_canvas_loop_argument_errors(dg):
+    L = dg.load()
+    dims = _dims()
+    m, c, cv, wsb = _structs(dg, dims)
+    ws = ct.c_void_p(1 << 30)
+    res = dg.dg_canvas_result(*[ct.c_void_p(FAKE)] * 4)
+    for sched in (dg.dg_sched(0.8, 0.4, 0, 0.1, 0.005), dg.dg_sched(0.0, 0.4, 48, 0.1, 0.005),
+                  dg.dg_sched(0.8, 0.4, 48, -1.0, 0.005)):
+        assert L.dg_denoise_canvas(ct.byref(m), ct.byref(c), ct.byref(cv), ct.byref(sched), 1, 0, ws, wsb,
+                                   ct.byref(res), None) == dg.DG_ERR_ARG
+    good = dg.dg_sched(0.8, 0.4, 48, 0.1, 0.005)
+    assert L.dg_denoise_canvas(ct.byref(m), ct.byref(c), ct.byref(cv), ct.byref(good), 1, 0, ws, wsb,
+                               None, None) == dg.DG_ERR_ARG
+
+
+def test_commit_capacity_is_checked_before_any_write(dg):
+    L = dg.load()
+    dims = _dims()
+    m, c, cv, wsb = _structs(dg, dims, cap=2100, length=2048)  # 2048 + 256 > 2100
+    ws = ct.c_void_p(1 << 30)
+    assert L.dg_commit_block(ct.byref(m), ct.byref(c), ct.c_void_p(FAKE), ws, wsb, None) == dg.DG_ERR_CAPACITY
+    assert c.len == 2048
+    assert L.dg_commit_block(ct.byref(m), ct.byref(c), None, ws, wsb, None) == dg.DG_ERR_ARG
+
+
+def test_small_entry_points_validate(dg):
+    L = dg.load()
+    assert L.dg_canvas_init(None, 1, 16, 512, 0, 0, None) == dg.DG_ERR_ARG
+    assert L.dg_canvas_init(ct.c_void_p(FAKE), 1, 0, 512, 0, 0, None) == dg.DG_ERR_ARG
+    st = ct.c_int32()
+    assert L.dg_read_status(None, ct.byref(st), None) == dg.DG_ERR_ARG
+    assert L.dg_debug_gemm(None, None, None, 1, 8, 8, 0, None) == dg.DG_ERR_ARG
+    assert L.dg_debug_gemm(ct.c_void_p(FAKE), ct.c_void_p(FAKE), ct.c_void_p(FAKE), 4, 12, 8, 0, None) == \
+        dg.DG_ERR_SHAPE
