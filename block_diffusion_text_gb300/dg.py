@@ -25,7 +25,8 @@ DG_OK, DG_ERR_ARG, DG_ERR_SHAPE, DG_ERR_CAPACITY, DG_ERR_WORKSPACE, DG_ERR_CUDA,
 
 # Every function the C header declares (checked by the tests).
 EXPORTS = ("dg_status_string", "dg_workspace_size", "dg_read_status", "dg_canvas_init",
-           "dg_denoise_step", "dg_denoise_canvas", "dg_commit_block", "dg_debug_gemm")
+           "dg_denoise_step", "dg_denoise_canvas", "dg_commit_block", "dg_debug_gemm",
+           "dg_attention_noalloc")
 
 
 class DgError(RuntimeError):
@@ -104,6 +105,9 @@ def load():
                                           ct.c_void_p, ct.c_size_t, ct.c_void_p]
             L.dg_debug_gemm.argtypes = [ct.c_void_p, ct.c_void_p, ct.c_void_p, ct.c_int32, ct.c_int32,
                                         ct.c_int32, ct.c_int32, ct.c_void_p]
+            L.dg_attention_noalloc.argtypes = [ct.c_void_p, ct.c_void_p, ct.c_void_p, ct.c_int32, ct.c_int32,
+                                               ct.c_void_p, ct.c_void_p, ct.c_void_p, ct.c_int32, ct.c_int32,
+                                               ct.c_int32, ct.c_int32, ct.c_int32, ct.c_void_p]
             _lib = L
     return _lib
 
@@ -272,3 +276,14 @@ def debug_gemm(A: torch.Tensor, Bm: torch.Tensor, b_mn_major: int = 0, stream=No
            "dg_debug_gemm")
     return D
 
+
+def attention_noalloc(q, K, V, cache_len, k, v, o=None, stream=None) -> torch.Tensor:
+    """Step attention with the library's static scratch (dg_attention_noalloc), for callers
+    that cannot allocate device memory; q [B,Hq,C,hd], K/V [B,Hkv,cap,hd], k/v [B,Hkv,C,hd]."""
+    B, Hq, C, hd = q.shape
+    Hkv, cap = K.shape[1], K.shape[2]
+    if o is None:
+        o = torch.empty(B * C, Hq * hd, dtype=q.dtype, device=q.device)
+    _check(load().dg_attention_noalloc(_ptr(q), _ptr(K), _ptr(V), cap, int(cache_len), _ptr(k), _ptr(v), _ptr(o),
+                                       B, C, Hq, Hkv, hd, _stream(stream)), "dg_attention_noalloc")
+    return o

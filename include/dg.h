@@ -229,6 +229,24 @@ DG_API dg_status dg_denoise_canvas(const dg_model* model, const dg_kv_cache* cac
 DG_API dg_status dg_commit_block(const dg_model* model, dg_kv_cache* cache, const int32_t* tokens,
                           void* ws, size_t ws_bytes, void* stream);
 
+/* Attention of the denoising step (the bidirectional attention inside
+ * dg_denoise_step) for callers that cannot allocate device memory, e.g. a
+ * process whose device memory is fully pre-reserved by another framework's
+ * caching allocator, or embedding code that is only handed fixed buffers.
+ * The pages describe no such entry point; it has no counterpart there.
+ *   q  bf16 [B][Hq][C][hd] (RoPE applied); K, V bf16 [B][Hkv][cap][hd] prefix
+ *   cache with rows 0..len-1 valid; k, v bf16 [B][Hkv][C][hd] canvas keys and
+ *   values; o bf16 [B*C][Hq*hd] output (caller-owned).
+ * Its scratch is a 16 MiB static device array inside the library (held on
+ * every GPU that loads it until exit), so no workspace is passed and nothing
+ * is allocated.  DG_ERR_WORKSPACE (nothing launched) if the scratch this size
+ * needs exceeds 16 MiB, e.g. 16 query heads over 8192 prefix keys.  The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) and should come before any stream capture.  All
+ * calls share the array: calls that overlap on the GPU race.              */
+DG_API dg_status dg_attention_noalloc(const void* q, const void* K, const void* V, int32_t cap,
+                                      int32_t len, const void* k, const void* v, void* o, int32_t B,
+                                      int32_t C, int32_t Hq, int32_t Hkv, int32_t hd, void* stream);
+
 /* Diagnostics of the tensor-core GEMM engine, used by the tests to check it
  * in isolation (not a step of the method).  D fp32 [M][N] = A B^T with
  * A bf16 [M][K], and B bf16 [N][K] when b_mn_major == 0, or B bf16 [K][N]

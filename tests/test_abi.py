@@ -140,3 +140,9 @@ def test_small_entry_points_validate(dg):
     assert L.dg_debug_gemm(None, None, None, 1, 8, 8, 0, None) == dg.DG_ERR_ARG
     assert L.dg_debug_gemm(ct.c_void_p(FAKE), ct.c_void_p(FAKE), ct.c_void_p(FAKE), 4, 12, 8, 0, None) == \
         dg.DG_ERR_SHAPE
+    f = ct.c_void_p(FAKE)
+    assert L.dg_attention_noalloc(f, f, f, 100, 50, f, f, f, 1, 16, 2, 1, 96, None) == dg.DG_ERR_SHAPE
+    assert L.dg_attention_noalloc(f, f, f, 100, 200, f, f, f, 1, 16, 2, 1, 32, None) == dg.DG_ERR_ARG
+    assert L.dg_attention_noalloc(None, f, f, 100, 50, f, f, f, 1, 16, 2, 1, 32, None) == dg.DG_ERR_ARG
+    # 16 query heads over 8192 prefix keys need more than the static scratch
+    assert L.dg_attention_noalloc(f, f, f, 8192, 8192, f, f, f, 1, 256, 16, 8, 128, None) == dg.DG_ERR_WORKSPACE
