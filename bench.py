@@ -263,7 +263,7 @@ def run_ours(args, world, rank, local):
     taus = dg.tau_schedule(48)
     outbuf = None
     slots = dg.PROF_SLOTS
-    timed_slots = ("attn", "lmhead", "selfcond")
+    timed_slots = slots
 
     def step(s, events=None):
         nonlocal outbuf
@@ -358,7 +358,7 @@ def run_ours(args, world, rank, local):
     work = kernel_work(dims)
     dominant = max(("lmhead", "selfcond"), key=lambda k: per_kernel[k])
     rl = {}
-    for name in timed_slots:
+    for name in ("attn", "lmhead", "selfcond"):
         fl, by = work[name]
         sec = per_kernel[name] / 1e3
         t_tc = fl / (peaks["tc_sustained"] * 1e12)
@@ -375,8 +375,7 @@ def run_ours(args, world, rank, local):
                     + (" sustained bf16" if bound == "tensor" else " HBM copy")}
     dom = rl[dominant]
 
-    launches_per_step = 11
-    from block_diffusion_text_gb300.dg import load  # noqa: F401
+    launches_per_step = len(dg.PROF_SLOTS)
     ns = _attn_splits(dims)
     if ns > 1:
         launches_per_step += 1
@@ -390,6 +389,7 @@ def run_ours(args, world, rank, local):
                          "unit": dom["unit"], "frac": dom["frac"], "traffic": dom["traffic"],
                          "kernel": dominant, "peak_note": dom["peak_note"]},
             "kernels": rl,
+            "kernel_ms": {k: round(v, 5) for k, v in per_kernel.items()},
             "clocks": clk,
             "e2e": e2e,
             "gpu_launches": launches_per_step * args.steps}
@@ -409,11 +409,16 @@ def run_ours(args, world, rank, local):
 
 
 def _attn_splits(dims):
-    units = math.ceil(dims.C / 64) * dims.B * dims.Hq
+    """Key splits of the attention launch (mirrors the library's choice; used to count launches)."""
     T = dims.P + dims.C
-    ns = min(math.ceil(3 * 152 / units), math.ceil(T / 256), 64)
+    if dims.hd == 128 and dims.P % 64 == 0:
+        units = math.ceil(dims.Hq // dims.Hkv * dims.C / 128) * dims.B * dims.Hkv
+        ns, blk = min(152 // units, math.ceil(T / 256), 64), 64
+    else:
+        units = math.ceil(dims.C / 64) * dims.B * dims.Hq
+        ns, blk = min(math.ceil(3 * 152 / units), math.ceil(T / 256), 64), 64
     ns = max(ns, 1)
-    kps = math.ceil(math.ceil(T / ns) / 64) * 64
+    kps = math.ceil(math.ceil(T / ns) / blk) * blk
     return math.ceil(T / kps)
 
 

@@ -8,8 +8,8 @@
 // contiguous chunk of the key sequence; K/V blocks of 64 keys are streamed
 // through shared memory with cp.async double buffering, scores and P.V use
 // the warp-level MMA, the softmax is online in base 2.  Scores use bf16 q, k;
-// the probabilities enter P.V as f16 (V re-encoded from bf16 to f16, exact in
-// the f16 range), which keeps their rounding 8x below bf16's.  With several
+// the probabilities enter P.V as two f16 parts P_hi + P_lo (V re-encoded from
+// bf16 to f16, exact in the f16 range), i.e. to ~2^-22.  With several
 // chunks per row the CTAs write unnormalised partials that a combine kernel
 // merges with their (max, sum).
 #include <cfloat>
@@ -162,9 +162,15 @@ __global__ void __launch_bounds__(128)
     }
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      uint32_t pa[4] = {pack_f16(s[2 * j][0], s[2 * j][1]), pack_f16(s[2 * j][2], s[2 * j][3]),
-                        pack_f16(s[2 * j + 1][0], s[2 * j + 1][1]),
-                        pack_f16(s[2 * j + 1][2], s[2 * j + 1][3])};
+      const float pv[8] = {s[2 * j][0], s[2 * j][1], s[2 * j][2], s[2 * j][3],
+                           s[2 * j + 1][0], s[2 * j + 1][1], s[2 * j + 1][2], s[2 * j + 1][3]};
+      uint32_t pa[4], pl[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        pa[e] = pack_f16(pv[2 * e], pv[2 * e + 1]);
+        const __half2 hh = *reinterpret_cast<const __half2*>(&pa[e]);
+        pl[e] = pack_f16(pv[2 * e] - __low2float(hh), pv[2 * e + 1] - __high2float(hh));
+      }
 #pragma unroll
       for (int dn = 0; dn < HD / 16; ++dn) {
         uint32_t vb[4];
@@ -172,8 +178,12 @@ __global__ void __launch_bounds__(128)
         const int key = j * 16 + (mat % 2) * 8 + lane % 8;
         const int c = dn * 2 + mat / 2;
         ldmatrix_x4_trans(vb, cV + key * HD + swz<HD>(key, c) * 8);
-        mma_f16_16816(o[2 * dn], pa, bf16x2_to_f16x2(vb[0]), bf16x2_to_f16x2(vb[1]));
-        mma_f16_16816(o[2 * dn + 1], pa, bf16x2_to_f16x2(vb[2]), bf16x2_to_f16x2(vb[3]));
+        const uint32_t v0 = bf16x2_to_f16x2(vb[0]), v1 = bf16x2_to_f16x2(vb[1]);
+        const uint32_t v2 = bf16x2_to_f16x2(vb[2]), v3 = bf16x2_to_f16x2(vb[3]);
+        mma_f16_16816(o[2 * dn], pa, v0, v1);
+        mma_f16_16816(o[2 * dn], pl, v0, v1);
+        mma_f16_16816(o[2 * dn + 1], pa, v2, v3);
+        mma_f16_16816(o[2 * dn + 1], pl, v2, v3);
       }
     }
     __syncthreads();
@@ -231,7 +241,7 @@ __global__ void attn_combine_kernel(AttnArgs a, int nsplit, StopCtl ctl) {
   }
 }
 
-void attn_split(const dg_dims& D, int T, int* nsplit, int* keys_per_split) {
+void attn_split_mma(const dg_dims& D, int T, int* nsplit, int* keys_per_split) {
   const int nqt = cdiv(D.C, kAttnRows);
   const int units = nqt * D.B * D.Hq;
   int target = cdiv(3 * kTargetCtas, units);
@@ -243,15 +253,35 @@ void attn_split(const dg_dims& D, int T, int* nsplit, int* keys_per_split) {
   *nsplit = cdiv(T, kps);
 }
 
+void attn_split(const dg_dims& D, int T, int P, int* nsplit, int* keys_per_split) {
+  if (attn_use_tc(D, P)) attn_split_tc(D, T, nsplit, keys_per_split);
+  else attn_split_mma(D, T, nsplit, keys_per_split);
+}
+
+int attn_max_splits(const dg_dims& D, int T) {
+  int ns1, ns2, k;
+  attn_split_mma(D, T, &ns1, &k);
+  attn_split_tc(D, T, &ns2, &k);
+  // the split count of either kernel grows with T, so T = cap + C bounds every prefix length
+  return ns1 > ns2 ? ns1 : ns2;
+}
+
+cudaError_t launch_attention_combine(const AttnArgs& a, int nsplit, StopCtl ctl, cudaStream_t st) {
+  attn_combine_kernel<<<a.B * a.Hq * a.C, a.hd, 0, st>>>(a, nsplit, ctl);
+  return cudaGetLastError();
+}
+
 template <int HD>
 static cudaError_t attn_impl(const AttnArgs& a, StopCtl ctl, cudaStream_t st) {
   dg_dims D{};
   D.C = a.C;
   D.B = a.B;
   D.Hq = a.Hq;
+  D.Hkv = a.Hkv;
+  D.hd = a.hd;
   const int T = a.P + a.C;
   int ns, kps;
-  attn_split(D, T, &ns, &kps);
+  attn_split_mma(D, T, &ns, &kps);
   const int nqt = cdiv(a.C, kAttnRows);
   const size_t smem = (size_t)(kAttnRows + 4 * kAttnKeys) * HD * 2;
   auto kern = attn_kernel<HD>;
@@ -262,11 +292,13 @@ static cudaError_t attn_impl(const AttnArgs& a, StopCtl ctl, cudaStream_t st) {
   kern<<<grid, 128, smem, st>>>(a, nqt, ns, kps, scale_log2, ctl);
   e = cudaGetLastError();
   if (e != cudaSuccess || ns == 1) return e;
-  attn_combine_kernel<<<a.B * a.Hq * a.C, HD, 0, st>>>(a, ns, ctl);
-  return cudaGetLastError();
+  return launch_attention_combine(a, ns, ctl, st);
 }
 
-cudaError_t launch_attention(const AttnArgs& a, StopCtl ctl, cudaStream_t st) {
+cudaError_t launch_attention(const AttnArgs& a, StopCtl ctl, int* status, cudaStream_t st) {
+  dg_dims D{};
+  D.hd = a.hd;
+  if (attn_use_tc(D, a.P)) return launch_attention_tc(a, ctl, status, st);
   switch (a.hd) {
     case 32: return attn_impl<32>(a, ctl, st);
     case 64: return attn_impl<64>(a, ctl, st);

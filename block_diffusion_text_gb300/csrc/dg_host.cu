@@ -105,7 +105,7 @@ dg_status enqueue_step(const StepCtx& c, float tau, float b, float stop_H, uint6
               at<void>(ws, L.o), at<float>(ws, L.attn_o), at<float>(ws, L.attn_ml), D.B, D.C, D.Hq,
               D.Hkv, D.hd, P, c.cache->cap};
   DG_TRY(pf.mark(DG_PROF_ATTN, 0));
-  DG_TRY(launch_attention(aa, ctl, c.st));
+  DG_TRY(launch_attention(aa, ctl, status, c.st));
   DG_TRY(pf.mark(DG_PROF_ATTN, 1));
   DG_TRY(pf.mark(DG_PROF_OPROJ, 0));
   DG_TRY(launch_gemm_bf16(at<void>(ws, L.o), c.model->Wo, at<void>(ws, L.h), D.d, at<void>(ws, L.a), D.d,
@@ -251,15 +251,8 @@ int selfcond_splits(const dg_dims& D) {
 bool ws_layout(const dg_dims& D, int32_t cap, WsLayout* L) {
   if (cap < 0) return false;
   const size_t M = (size_t)D.B * D.C, NT = (size_t)cdiv(D.V, kLmBN);
-  int ns_attn, kps;
-  attn_split(D, cap + D.C, &ns_attn, &kps);
   // room for the largest split count any prefix length up to cap can use
-  {
-    const int nqt = cdiv(D.C, kAttnRows);
-    int target = cdiv(3 * kTargetCtas, nqt * D.B * D.Hq);
-    if (target > kMaxAttnSplits) target = kMaxAttnSplits;
-    if (ns_attn < target) ns_attn = target;
-  }
+  const int ns_attn = attn_max_splits(D, cap + D.C);
   const size_t S = (size_t)selfcond_splits(D);
   size_t off = 0;
   auto take = [&](size_t bytes) {

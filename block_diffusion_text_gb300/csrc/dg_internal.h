@@ -22,9 +22,13 @@ constexpr int kMaxAttnSplits = 64;
 inline int cdiv(int64_t a, int64_t b) { return (int)((a + b - 1) / b); }
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Split of the key sequence [prefix ; canvas] of length T into chunks for the
-// attention grid; returns the number of splits and the keys per split.
-void attn_split(const dg_dims& D, int T, int* nsplit, int* keys_per_split);
+// Split of the key sequence [prefix ; canvas] of length T (prefix P) into
+// chunks for the attention grid; returns the number of splits and the keys per
+// split.  Head dim 128 with P a multiple of 64 takes the tensor-core kernel,
+// other shapes the warp-MMA kernel; attn_max_splits bounds both for any P <= cap.
+bool attn_use_tc(const dg_dims& D, int P);
+void attn_split(const dg_dims& D, int T, int P, int* nsplit, int* keys_per_split);
+int attn_max_splits(const dg_dims& D, int T);
 // Split of the vocabulary (the contraction of p0 . E) between CTAs.
 int selfcond_splits(const dg_dims& D);
 
@@ -104,7 +108,7 @@ struct GumbelArgs {
 };
 cudaError_t launch_gumbel(const GumbelArgs& a, StopCtl ctl, cudaStream_t st);
 
-// Attention over [prefix ; canvas] (legacy warp MMA path).
+// Attention over [prefix ; canvas].
 struct AttnArgs {
   const void* q;            // bf16 [B][Hq][C][hd]
   const void *Kp, *Vp;      // bf16 [B][Hkv][cap][hd]
@@ -114,7 +118,11 @@ struct AttnArgs {
   float* ml;                // fp32 [S][B][Hq][C][2]
   int B, C, Hq, Hkv, hd, P, cap;
 };
-cudaError_t launch_attention(const AttnArgs& a, StopCtl ctl, cudaStream_t st);
+cudaError_t launch_attention(const AttnArgs& a, StopCtl ctl, int* status, cudaStream_t st);
+cudaError_t launch_attention_tc(const AttnArgs& a, StopCtl ctl, int* status, cudaStream_t st);
+cudaError_t launch_attention_combine(const AttnArgs& a, int nsplit, StopCtl ctl, cudaStream_t st);
+void attn_split_tc(const dg_dims& D, int T, int* nsplit, int* keys_per_split);
+void attn_split_mma(const dg_dims& D, int T, int* nsplit, int* keys_per_split);
 
 // Misc kernels.
 cudaError_t launch_embed_rmsnorm(const int32_t* tokens, const void* E, const void* z, void* a,

@@ -22,6 +22,9 @@ namespace {
 constexpr size_t kScratchBytes = size_t(16) << 20;
 __device__ __align__(256) unsigned char g_attn_scratch[kScratchBytes];
 
+// Status word for the bounded waits of the attention kernels (not read back).
+__device__ int g_noalloc_status;
+
 constexpr int kMaxDevices = 64;
 std::mutex g_setup_mutex;
 unsigned char* g_scratch_ptr[kMaxDevices] = {};
@@ -56,8 +59,10 @@ extern "C" dg_status dg_attention_noalloc(const void* q, const void* K, const vo
   D.B = B;
   D.C = C;
   D.Hq = Hq;
+  D.Hkv = Hkv;
+  D.hd = hd;
   int ns = 1, kps = 0;
-  dg::attn_split(D, len + C, &ns, &kps);
+  dg::attn_split(D, len + C, len, &ns, &kps);
   const size_t rows = (size_t)B * Hq * C;
   const size_t part_bytes = dg::align_up((size_t)ns * rows * hd * 4, 256);
   const size_t need = ns > 1 ? part_bytes + (size_t)ns * rows * 8 : 0;
@@ -68,6 +73,10 @@ extern "C" dg_status dg_attention_noalloc(const void* q, const void* K, const vo
   dg::AttnArgs a{q, K, V, k, v, o, reinterpret_cast<float*>(scratch),
                  reinterpret_cast<float*>(scratch + part_bytes), B, C, Hq, Hkv, hd, len, cap};
   dg::StopCtl none{nullptr, 0, 0};
-  return dg::launch_attention(a, none, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? DG_OK
-                                                                                               : DG_ERR_CUDA;
+  int* status = nullptr;
+  if (cudaGetSymbolAddress(reinterpret_cast<void**>(&status), g_noalloc_status) != cudaSuccess)
+    return DG_ERR_CUDA;
+  return dg::launch_attention(a, none, status, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? DG_OK
+             : DG_ERR_CUDA;
 }

@@ -14,6 +14,9 @@ from parity import (Collect, bf16_to_np, check_argmax, check_close_bf16, check_e
 pytestmark = pytest.mark.gpu
 
 RAGGED = synth.Dims(V=1000, d=128, C=40, B=3, Hq=4, Hkv=2, hd=64, F=192, P=100, cap=160)
+# head dim 128 with a prefix that is a multiple of 64: the tensor-core attention kernel, with a partial
+# canvas key block (C = 40) and a 3-head group whose 300 query rows leave a partial second Q block
+RAGGED_TC = synth.Dims(V=1000, d=128, C=100, B=2, Hq=6, Hkv=2, hd=128, F=192, P=192, cap=256)
 
 
 def _setup(dims, seed, alpha=None):
@@ -99,6 +102,18 @@ def test_ragged_step_later_step_with_z():
     z = (torch.randn(RAGGED.B, RAGGED.C, RAGGED.d, generator=g) * 0.02).to(torch.bfloat16)
     prev = np.random.default_rng(1).integers(0, RAGGED.V, size=(RAGGED.B, RAGGED.C)).astype(np.int32)
     _run_and_compare(RAGGED, seed, tau=0.55, step=3, z_in=z, prev=prev)
+
+
+def test_ragged_step_tensor_core_attention():
+    seed = 12
+    g = torch.Generator().manual_seed(6)
+    z = (torch.randn(RAGGED_TC.B, RAGGED_TC.C, RAGGED_TC.d, generator=g) * 0.02).to(torch.bfloat16)
+    _run_and_compare(RAGGED_TC, seed, tau=0.7, step=2, z_in=z)
+
+
+def test_tensor_core_attention_canvas_tail():
+    dims = synth.Dims(V=512, d=64, C=40, B=1, Hq=2, Hkv=2, hd=128, F=64, P=64, cap=64)
+    _run_and_compare(dims, 13)
 
 
 @pytest.mark.slow

@@ -46,19 +46,20 @@ def test_attention_noalloc_matches_step_attention_twice():
 
 
 def test_attention_noalloc_rejects_sizes_beyond_its_scratch():
-    """16 query heads over an 8192-key prefix need 16 MiB + 256 KiB of partials: rejected before
-    any launch.  Every buffer is allocated at its full size all the same."""
+    """Two canvases of 8 heads over an 8190-key prefix (not a multiple of 64, so the warp-MMA kernel
+    with 8 key splits) need 17.0 MB of partials: rejected before any launch.  Every buffer is
+    allocated at its full size all the same."""
     from block_diffusion_text_gb300 import dg
     L = dg.load()
-    B, C, Hq, Hkv, hd, P = 1, 256, 16, 8, 128, 8192
+    B, C, Hq, Hkv, hd, P = 2, 256, 8, 8, 128, 8190
     bf = dict(dtype=torch.bfloat16, device="cuda")
     q = torch.zeros(B, Hq, C, hd, **bf)
-    K = torch.zeros(B, Hkv, P, hd, **bf)
+    K = torch.zeros(B, Hkv, P + 2, hd, **bf)
     V = torch.zeros_like(K)
     k = torch.zeros(B, Hkv, C, hd, **bf)
     v = torch.zeros_like(k)
     o = torch.zeros(B * C, Hq * hd, **bf)
-    rc = _call(L, q, K, V, P, P, k, v, o, B, C, Hq, Hkv, hd)
+    rc = _call(L, q, K, V, P + 2, P, k, v, o, B, C, Hq, Hkv, hd)
     assert rc == dg.DG_ERR_WORKSPACE
     torch.cuda.synchronize()
     assert torch.count_nonzero(o).item() == 0
