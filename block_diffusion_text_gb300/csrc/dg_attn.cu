@@ -285,7 +285,7 @@ static cudaError_t attn_impl(const AttnArgs& a, StopCtl ctl, cudaStream_t st) {
   const int nqt = cdiv(a.C, kAttnRows);
   const size_t smem = (size_t)(kAttnRows + 4 * kAttnKeys) * HD * 2;
   auto kern = attn_kernel<HD>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = set_smem_once<attn_kernel<HD>>((int)smem);
   if (e != cudaSuccess) return e;
   const float scale_log2 = 1.4426950408889634f / sqrtf((float)HD);
   dim3 grid(nqt * ns, a.B * a.Hq);

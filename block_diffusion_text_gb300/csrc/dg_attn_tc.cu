@@ -403,8 +403,7 @@ cudaError_t launch_attention_tc(const AttnArgs& a, StopCtl ctl, int* status, cud
       !make_tmap_2d(&mKc, a.kc, kTcHD, (uint64_t)a.B * a.Hkv * a.C, kTcHD * 2, 64, kTcKeys) ||
       !make_tmap_2d(&mVc, a.vc, kTcHD, (uint64_t)a.B * a.Hkv * a.C, kTcHD * 2, 64, kTcKeys))
     return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       TcLayout::kSmem);
+  cudaError_t e = set_smem_once<attn_tc_kernel>(TcLayout::kSmem);
   if (e != cudaSuccess) return e;
   const float scale_log2 = 1.4426950408889634f / sqrtf((float)kTcHD);
   dim3 grid(nqt * ns, a.B * a.Hkv);

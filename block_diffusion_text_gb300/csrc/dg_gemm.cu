@@ -460,7 +460,7 @@ static cudaError_t run_gemm(const CUtensorMap& mA, const CUtensorMap& mB0, const
                             cudaStream_t st) {
   using L = GemmLayout<BN, STAGES, B_MN>;
   auto kern = gemm_kernel<BN, STAGES, B_MN, Epi>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmem);
+  cudaError_t e = set_smem_once<gemm_kernel<BN, STAGES, B_MN, Epi>>(L::kSmem);
   if (e != cudaSuccess) return e;
   const int tiles = cdiv(M, kBM) * cdiv(N, BN);
   const int grid = tiles < num_sms() ? tiles : num_sms();
@@ -740,8 +740,7 @@ cudaError_t launch_selfcond(const ScArgs& a, StopCtl ctl, int* status, cudaStrea
   CUtensorMap mP, mE;
   if (!tmap_kmajor(&mP, a.pt, a.M, a.V, kBM) || !tmap_mnmajor(&mE, a.E, a.V, a.d))
     return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(selfcond_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       ScLayout::kSmem);
+  cudaError_t e = set_smem_once<selfcond_kernel>(ScLayout::kSmem);
   if (e != cudaSuccess) return e;
   const int n_tiles = cdiv(a.d, kScBN), m_pairs = cdiv(a.M, 2 * kBM);
   const int grid = n_tiles * m_pairs * a.nsplit;

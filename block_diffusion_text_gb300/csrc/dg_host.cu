@@ -74,9 +74,12 @@ dg_status check_ws(const dg_dims& D, int32_t cap, void* ws, size_t ws_bytes, WsL
 struct Prof {
   void* const* ev;
   cudaStream_t st;
+  // External record: inside a stream capture it becomes an event-record node of
+  // the graph (timing each replay); outside a capture it is a plain record.
   cudaError_t mark(int slot, int end) const {
     if (!ev || !ev[2 * slot + end]) return cudaSuccess;
-    return cudaEventRecord(reinterpret_cast<cudaEvent_t>(ev[2 * slot + end]), st);
+    return cudaEventRecordWithFlags(reinterpret_cast<cudaEvent_t>(ev[2 * slot + end]), st,
+                                    cudaEventRecordExternal);
   }
 };
 

@@ -46,6 +46,15 @@ struct WsLayout {
 };
 bool ws_layout(const dg_dims& D, int32_t cap, WsLayout* L);
 
+// Opt a kernel in to more than 48 KB of dynamic shared memory, once per
+// kernel (the value is fixed per kernel), so that enqueueing a step makes no
+// attribute calls and can be captured into a CUDA graph.
+template <auto Kernel>
+cudaError_t set_smem_once(int bytes) {
+  static cudaError_t result = cudaFuncSetAttribute(Kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  return result;
+}
+
 // cuTensorMapEncodeTiled through the runtime's driver entry point.
 bool make_tmap_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
                   uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer);

@@ -147,7 +147,8 @@ enum {
  *   events   host array of 2 * DG_PROF_NUM cudaEvent_t (caller-created), or
  *            NULL: events[2k] / events[2k+1] are recorded on `stream` just
  *            before / after the kernels of slot k (for per-kernel timing);
- *            NULL entries are skipped                                       */
+ *            NULL entries are skipped.  Records are external, so a step
+ *            captured into a CUDA graph records them at every replay.       */
 typedef struct dg_step_out {
   float* entropy;
   int32_t* argmax;

@@ -200,3 +200,30 @@ def test_full_size_sampled_rows(name):
             ck.errors.append(f"canvas {b}: n_acc")
     print(name, "accepted per canvas", out["n_acc"].cpu().tolist())
     ck.done()
+
+
+def test_steps_captured_in_a_cuda_graph_match_eager_steps():
+    from block_diffusion_text_gb300 import dg
+    dims, seed = synth.workload("step_v32k_c256_p2k")
+    w, x, z, a, model = _model(dims, seed)
+    taus = dg.tau_schedule(48)
+    eager = dg.Canvas(x.cuda(), z.cuda(), a.cuda())
+    out = None
+    for s in range(3):
+        out = dg.denoise_step(model, eager, tau=taus[s], b=0.1, seed=seed, step=s, out=out)
+    torch.cuda.synchronize()
+    graphed = dg.Canvas(x.cuda(), z.cuda(), a.cuda())
+    out2 = dg.denoise_step(model, dg.Canvas(x.cuda(), z.cuda(), a.cuda()), tau=0.8, b=0.1, seed=seed, step=0)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream()
+    cap.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.graph(g, stream=cap):
+        for s in range(3):
+            dg.denoise_step(model, graphed, tau=taus[s], b=0.1, seed=seed, step=s, out=out2)
+    g.replay()
+    torch.cuda.synchronize()
+    assert model.status() == 0
+    assert torch.equal(graphed.tokens, eager.tokens)
+    assert torch.equal(graphed.z, eager.z)
+    assert torch.equal(out2["entropy"], out["entropy"])
