@@ -6,9 +6,9 @@
 //     double-buffered TMEM accumulator.  Epilogues: fp32 store (diagnostics),
 //     bf16 store with residual / GELU (output projection, FFW), RoPE
 //     projections (q, k, v), and the LM head statistics epilogue.
-//   * selfcond_kernel: u = p0 . E where the p0 tiles are rebuilt in shared
-//     memory from the stored exp(s - m_tile) tiles and E is the MN-major B
-//     operand, plus the Gumbel-max search of accepted positions.
+//   * selfcond_kernel: u = p0 . E with p0 (bf16, rescaled in place after the
+//     LM head) as the A operand and E as the MN-major B operand, split over
+//     the vocabulary.
 #include <cfloat>
 
 #include "dg_common.cuh"
@@ -563,13 +563,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + ScLayout::kBar);
-  uint64_t* ready = full + kScStages;
-  uint64_t* empty = ready + kScStages;
+  uint64_t* empty = full + kScStages;
   uint64_t* tfull = empty + kScStages;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tfull + 1);
   volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  // adjacent CTAs share the vocabulary split (the same p0 rows, through L2)
   const int nt = blockIdx.x % n_tiles;
   const int rest = blockIdx.x / n_tiles;
   const int mp = rest % m_pairs;
@@ -582,7 +582,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < kScStages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&ready[s], 128);
       mbar_init(&empty[s], 1);
     }
     mbar_init(tfull, 1);
@@ -626,7 +625,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     uint32_t phase = 0;
     bool alive = true;
     for (int kb = kb0; kb < kb1; ++kb) {
-      if (!mbar_wait(&ready[stage], phase, status, abort)) {
+      if (!mbar_wait(&full[stage], phase, status, abort)) {
         alive = false;
         break;
       }
@@ -654,57 +653,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     if (alive && lane == 0) umma_commit(tfull);
     __syncwarp();
   } else {
-    // Transform warps: rebuild p0 = exp(s - m_tile) * exp(m_tile - m) / l in
-    // place, thread t owning row t of each 128-row half.
-    // Row t occupies bytes [128 t, 128 t + 128) of its 128-row box; the 128-byte
-    // swizzle permutes its eight 16-byte chunks by (t mod 8), so walking the
-    // physical chunks (c xor t) keeps the eight threads of each quarter-warp
-    // on distinct banks.  Each row's scale factor is fetched one tile ahead.
-    const int t = threadIdx.x - 64;
-    const int rows[2] = {m0 + t, m0 + kBM + t};
-    auto fetch = [&](int vt, int h) -> float {
-      const size_t o = (size_t)vt * a.M + rows[h];
-      return (rows[h] < a.M && vt * kLmBN < a.V) ? a.fscale[o] : 0.f;
-    };
-    int cur_vt = (kb0 * kBK) / kLmBN;
-    float f[2] = {fetch(cur_vt, 0), fetch(cur_vt, 1)};
-    float fn[2] = {fetch(cur_vt + 1, 0), fetch(cur_vt + 1, 1)};
-    int stage = 0;
-    uint32_t phase = 0;
-    for (int kb = kb0; kb < kb1; ++kb) {
-      const int vt = (kb * kBK) / kLmBN;
-      if (vt != cur_vt) {
-        cur_vt = vt;
-        f[0] = fn[0];
-        f[1] = fn[1];
-        fn[0] = fetch(vt + 1, 0);
-        fn[1] = fetch(vt + 1, 1);
-      }
-      if (!mbar_wait(&full[stage], phase, status, abort)) break;
-      uint8_t* sa = smem + stage * ScLayout::kStage;
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint4* rowp = reinterpret_cast<uint4*>(sa + h * (kBM * kBK * 2) + t * 128);
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const int pc = c ^ (t & 7);
-          uint4 x = rowp[pc];
-          const __nv_bfloat16* xb = reinterpret_cast<const __nv_bfloat16*>(&x);
-          uint4 y;
-          y.x = pack_bf16(__bfloat162float(xb[0]) * f[h], __bfloat162float(xb[1]) * f[h]);
-          y.y = pack_bf16(__bfloat162float(xb[2]) * f[h], __bfloat162float(xb[3]) * f[h]);
-          y.z = pack_bf16(__bfloat162float(xb[4]) * f[h], __bfloat162float(xb[5]) * f[h]);
-          y.w = pack_bf16(__bfloat162float(xb[6]) * f[h], __bfloat162float(xb[7]) * f[h]);
-          rowp[pc] = y;
-        }
-      }
-      fence_proxy_async_smem();
-      mbar_arrive(&ready[stage]);
-      if (++stage == kScStages) {
-        stage = 0;
-        phase ^= 1;
-      }
-    }
     // Epilogue: the split's partial u tile, TMEM lane = row within the half.
     if (mbar_wait(tfull, 0, status, abort)) {
       tc_fence_after();

@@ -164,10 +164,25 @@ dg_status enqueue_step(const StepCtx& c, float tau, float b, float stop_H, uint6
   DG_TRY(pf.mark(DG_PROF_SAMPLER, 0));
   DG_TRY(launch_sampler(sp, c.st));
   DG_TRY(pf.mark(DG_PROF_SAMPLER, 1));
+  P0Args p0{};
+  p0.pt = at<void>(ws, L.pt);
+  p0.fscale = at<float>(ws, L.fscale);
+  p0.lsum = at<float>(ws, L.lsum);
+  p0.acc = at<uint8_t>(ws, L.acc);
+  p0.gbest = at<float>(ws, L.gbest);
+  p0.gidx = at<int>(ws, L.gidx);
+  p0.M = M;
+  p0.V = D.V;
+  p0.C = D.C;
+  p0.seed = seed;
+  p0.block = block;
+  p0.step = step;
+  DG_TRY(pf.mark(DG_PROF_P0, 0));
+  DG_TRY(launch_p0_gumbel(p0, ctl, c.st));
+  DG_TRY(pf.mark(DG_PROF_P0, 1));
   ScArgs sc{};
   sc.pt = at<void>(ws, L.pt);
   sc.E = c.model->E;
-  sc.fscale = at<float>(ws, L.fscale);
   sc.upart = at<float>(ws, L.upart);
   sc.M = M;
   sc.V = D.V;
@@ -176,22 +191,6 @@ dg_status enqueue_step(const StepCtx& c, float tau, float b, float stop_H, uint6
   DG_TRY(pf.mark(DG_PROF_SELFCOND, 0));
   DG_TRY(launch_selfcond(sc, ctl, status, c.st));
   DG_TRY(pf.mark(DG_PROF_SELFCOND, 1));
-  GumbelArgs gu{};
-  gu.pt = at<void>(ws, L.pt);
-  gu.fscale = at<float>(ws, L.fscale);
-  gu.amax = at<int>(ws, L.amax);
-  gu.acc = at<uint8_t>(ws, L.acc);
-  gu.gbest = at<float>(ws, L.gbest);
-  gu.gidx = at<int>(ws, L.gidx);
-  gu.M = M;
-  gu.V = D.V;
-  gu.C = D.C;
-  gu.seed = seed;
-  gu.block = block;
-  gu.step = step;
-  DG_TRY(pf.mark(DG_PROF_GUMBEL, 0));
-  DG_TRY(launch_gumbel(gu, ctl, c.st));
-  DG_TRY(pf.mark(DG_PROF_GUMBEL, 1));
   ReduceArgs ra{at<float>(ws, L.upart), at<float>(ws, L.gbest), at<int>(ws, L.gidx), at<uint8_t>(ws, L.acc),
                 at<void>(ws, L.u), c.canvas->tokens, M, D.d, D.C, sc.nsplit, cdiv(D.V, kGumbelChunk)};
   DG_TRY(pf.mark(DG_PROF_REDUCE, 0));

@@ -95,19 +95,19 @@ struct LmArgs {
 cudaError_t launch_lmhead(const LmArgs& a, StopCtl ctl, int* status, cudaStream_t st);
 // Self-conditioning contraction u = p0 . E (split over the vocabulary).
 struct ScArgs {
-  const void* pt;        // bf16 [M][V]
+  const void* pt;        // bf16 [M][V]: p0
   const void* E;         // bf16 [V][d]
-  const float* fscale;   // [NT][M]  exp(m_tile - m) / l
   float* upart;          // [S][M][d]
   int M, V, d, nsplit;
 };
 cudaError_t launch_selfcond(const ScArgs& a, StopCtl ctl, int* status, cudaStream_t st);
-// Gumbel-max search of the accepted rows over vocabulary chunks.
+// The stored tiles become p0 in place, and the Gumbel-max search of the
+// accepted rows runs over vocabulary chunks in the same pass.
 constexpr int kGumbelChunk = 8192;
-struct GumbelArgs {
-  const void* pt;        // bf16 [M][V]
+struct P0Args {
+  void* pt;              // bf16 [M][V]: exp(s - m_tile) in, p0 out
   const float* fscale;   // [NT][M]
-  const int* amax;       // [M]
+  const float* lsum;     // [M]  Z
   const uint8_t* acc;    // [M]
   float* gbest;          // [NC][M]
   int* gidx;             // [NC][M]
@@ -115,7 +115,7 @@ struct GumbelArgs {
   uint64_t seed;
   int block, step;
 };
-cudaError_t launch_gumbel(const GumbelArgs& a, StopCtl ctl, cudaStream_t st);
+cudaError_t launch_p0_gumbel(const P0Args& a, StopCtl ctl, cudaStream_t st);
 
 // Attention over [prefix ; canvas].
 struct AttnArgs {

@@ -182,64 +182,73 @@ cudaError_t launch_stats(const StatsArgs& a, StopCtl ctl, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-// ------------------------------------------------------------ Gumbel-max --
-// Sample of an accepted position: argmax_v (log p0_v + G_v) with G_v the
-// Gumbel noise of Philox stream 0 keyed by (seed, block, step, canvas,
-// position, v), lowest index on ties (technical report summary, step 3:
-// accepted positions take their predicted token; the Gumbel-max form of that
-// draw is this library's reading).  The score of the argmax position is a
-// lower bound of the maximum, so an entry can only win where
-// log p0_v > score(argmax) - max G; the largest Gumbel draw is 16.636
-// (U = 1 - 2^-24), and the test uses 16.65.  One CTA per (row, 8192-entry
-// chunk); rows that were not accepted return at once.
-constexpr int kGumbelThreads = 256;
-constexpr float kGumbelMaxDraw = 16.65f;
+// ------------------------------------------- p0 and Gumbel-max sampling --
+// One pass over the stored tiles exp(s - m_t): each becomes p0 =
+// exp(s - m_t) * exp(m_t - m) / Z in place (the A operand of the
+// self-conditioning contraction), and for the accepted rows the sample
+// argmax_v (log p0_v + G_v) is searched, G_v the Gumbel noise of Philox
+// stream 0 keyed by (seed, block, step, canvas, position, v), lowest index on
+// ties (technical report summary, step 3: accepted positions take their
+// predicted token; the Gumbel-max form of that draw is this library's
+// reading).  The argmax token's perturbed score is at least
+// log(1 / Z) - 2.81 (its p0 is 1/Z up to bf16 rounding, and G >= -2.81),
+// and the largest draw is 16.64, so entries with
+// log p0 < log(1/Z) - 2.81 - 16.64 - 0.02 can never win and skip the draw.
+// One CTA per (row, 8192-entry chunk).
+constexpr int kP0Threads = 256;
+constexpr float kGumbelMinDraw = -2.8136f;  // -log(-log((0.5) / 2^23))
+constexpr float kGumbelMaxDraw = 16.6355f;  // -log(-log(1 - 2^-24))
 
-__global__ void __launch_bounds__(kGumbelThreads) gumbel_kernel(GumbelArgs a, StopCtl ctl) {
+__global__ void __launch_bounds__(kP0Threads) p0_gumbel_kernel(P0Args a, StopCtl ctl) {
+  if (all_stopped(ctl.stop_at, ctl.B, ctl.step)) return;
   const int row = blockIdx.y;
   const int chunk = blockIdx.x;
-  if (!a.acc[row] || !canvas_active(ctl.stop_at, row / a.C, ctl.step)) return;
-  const __nv_bfloat16* pt = reinterpret_cast<const __nv_bfloat16*>(a.pt) + (size_t)row * a.V;
+  __nv_bfloat16* pt = reinterpret_cast<__nv_bfloat16*>(a.pt) + (size_t)row * a.V;
+  const bool gum = a.acc[row] && canvas_active(ctl.stop_at, row / a.C, ctl.step);
   const int canvas = row / a.C, pos = row % a.C;
-  // seed score at the argmax
-  const int am = a.amax[row];
-  const float pam = __bfloat162float(pt[am]) * a.fscale[(size_t)(am / kLmBN) * a.M + row];
-  uint64_t w[4];
-  philox_block(w, a.seed, a.block, a.step, canvas, pos, am >> 2, 0);
-  const float best0 = logf(pam) + gumbel_from_word(w[am & 3]);
-  const float thr = expf(best0 - kGumbelMaxDraw);
+  // p0 threshold below which no entry can win the Gumbel-max search
+  const float thr = expf(-logf(a.lsum[row]) + kGumbelMinDraw - kGumbelMaxDraw - 0.02f);
   float best = -FLT_MAX;
   int bidx = INT_MAX;
   const int v_begin = chunk * kGumbelChunk;
   const int v_end = min(a.V, v_begin + kGumbelChunk);
-  for (int v0 = v_begin + threadIdx.x * 8; v0 < v_end; v0 += kGumbelThreads * 8) {
+  for (int v0 = v_begin + threadIdx.x * 8; v0 < v_end; v0 += kP0Threads * 8) {
     const float f = a.fscale[(size_t)(v0 / kLmBN) * a.M + row];
-    uint4 x = *reinterpret_cast<const uint4*>(pt + v0);
+    uint4* p4 = reinterpret_cast<uint4*>(pt + v0);
+    uint4 x = *p4;
     const __nv_bfloat16* xb = reinterpret_cast<const __nv_bfloat16*>(&x);
     float p[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e) p[e] = __bfloat162float(xb[e]) * f;
+    uint4 y;
+    y.x = pack_bf16(p[0], p[1]);
+    y.y = pack_bf16(p[2], p[3]);
+    y.z = pack_bf16(p[4], p[5]);
+    y.w = pack_bf16(p[6], p[7]);
+    *p4 = y;
+    if (!gum) continue;
 #pragma unroll
     for (int g4 = 0; g4 < 2; ++g4) {
       bool any = false;
 #pragma unroll
-      for (int e = 0; e < 4; ++e) any |= p[g4 * 4 + e] >= thr && v0 + g4 * 4 + e < v_end;
+      for (int e = 0; e < 4; ++e) any |= p[g4 * 4 + e] >= thr;
       if (!any) continue;
+      uint64_t w[4];
       philox_block(w, a.seed, a.block, a.step, canvas, pos, (v0 + g4 * 4) >> 2, 0);
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const int v = v0 + g4 * 4 + e;
         const float pv = p[g4 * 4 + e];
-        if (pv >= thr && v < v_end && pv > 0.f) {
+        if (pv >= thr && pv > 0.f) {
           const float sc = logf(pv) + gumbel_from_word(w[e]);
           if (sc > best) {
             best = sc;
-            bidx = v;
+            bidx = v0 + g4 * 4 + e;
           }
         }
       }
     }
   }
+  if (!gum) return;  // uniform over the CTA
   // (score, lowest index) over the block
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
@@ -250,15 +259,15 @@ __global__ void __launch_bounds__(kGumbelThreads) gumbel_kernel(GumbelArgs a, St
       bidx = i2;
     }
   }
-  __shared__ float sb[kGumbelThreads / 32];
-  __shared__ int si[kGumbelThreads / 32];
+  __shared__ float sb[kP0Threads / 32];
+  __shared__ int si[kP0Threads / 32];
   if (threadIdx.x % 32 == 0) {
     sb[threadIdx.x / 32] = best;
     si[threadIdx.x / 32] = bidx;
   }
   __syncthreads();
   if (threadIdx.x == 0) {
-    for (int k = 1; k < kGumbelThreads / 32; ++k) {
+    for (int k = 1; k < kP0Threads / 32; ++k) {
       if (sb[k] > best || (sb[k] == best && si[k] < bidx)) {
         best = sb[k];
         bidx = si[k];
@@ -269,9 +278,9 @@ __global__ void __launch_bounds__(kGumbelThreads) gumbel_kernel(GumbelArgs a, St
   }
 }
 
-cudaError_t launch_gumbel(const GumbelArgs& a, StopCtl ctl, cudaStream_t st) {
+cudaError_t launch_p0_gumbel(const P0Args& a, StopCtl ctl, cudaStream_t st) {
   dim3 grid(cdiv(a.V, kGumbelChunk), a.M);
-  gumbel_kernel<<<grid, kGumbelThreads, 0, st>>>(a, ctl);
+  p0_gumbel_kernel<<<grid, kP0Threads, 0, st>>>(a, ctl);
   return cudaGetLastError();
 }
 

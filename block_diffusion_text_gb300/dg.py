@@ -64,7 +64,7 @@ class dg_step_out(ct.Structure):
 
 
 # Kernel slots of one step (dg_step_out.events), in launch order.
-PROF_SLOTS = ("embed", "qkv", "attn", "oproj", "lmhead", "stats", "sampler", "selfcond", "gumbel",
+PROF_SLOTS = ("embed", "qkv", "attn", "oproj", "lmhead", "stats", "sampler", "p0", "selfcond",
               "reduce", "ffw1", "ffw2")
 
 
