@@ -38,7 +38,7 @@ struct EpiF32 {
   float* out;
   int ldo;
   template <int BN, class LD>
-  DG_DEV void tile(int row, bool ok, int n0, int N, LD& ld) const {
+  DG_DEV void tile(int row, bool ok, int n0, int N, LD& ld, int /*split*/) const {
 #pragma unroll 1
     for (int c = 0; c < BN / 32; ++c) {
       float v[32];
@@ -52,6 +52,31 @@ struct EpiF32 {
   }
 };
 
+// Split-K partial: the fp32 tile of one K-split, reduced by splitk_*_kernel.
+struct EpiPartial {
+  float* part;  // [ksplit][M][N]
+  int M, N;
+  template <int BN, class LD>
+  DG_DEV void tile(int row, bool ok, int n0, int N_, LD& ld, int split) const {
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+      float v[32];
+      ld(c, v);
+      const int col0 = n0 + c * 32;
+      if (!ok || col0 >= N) continue;
+      float* dst = part + ((size_t)split * M + row) * N + col0;
+      if (col0 + 32 <= N) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          reinterpret_cast<float4*>(dst)[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+      } else {
+        for (int j = 0; j < 32; ++j)
+          if (col0 + j < N) dst[j] = v[j];
+      }
+    }
+  }
+};
+
 struct EpiBF16 {
   __nv_bfloat16* out;
   int ldo;
@@ -61,7 +86,7 @@ struct EpiBF16 {
   int C;
   StopCtl ctl;
   template <int BN, class LD>
-  DG_DEV void tile(int row, bool ok, int n0, int N, LD& ld) const {
+  DG_DEV void tile(int row, bool ok, int n0, int N, LD& ld, int /*split*/) const {
     const bool active = ok && canvas_active(ctl.stop_at, row / C, ctl.step);
 #pragma unroll 1
     for (int c = 0; c < BN / 32; ++c) {
@@ -112,7 +137,7 @@ struct EpiQKV {
   const float2* rope;  // [C][HD/2] (cos, sin) of positions P + i
   int C, Hq, Hkv, nq, nkv, kv_rows, kv_row0;
   template <int BN, class LD>
-  DG_DEV void tile(int row, bool ok, int n0, int N, LD& ld) const {
+  DG_DEV void tile(int row, bool ok, int n0, int N, LD& ld, int /*split*/) const {
     static_assert(BN % HD == 0, "tile must hold whole heads");
     float x[BN];
 #pragma unroll
@@ -176,7 +201,7 @@ struct EpiLM {
   float* logits;
   int M, V;
   template <int BN, class LD>
-  DG_DEV void tile(int row, bool ok, int n0, int N, LD& ld) const {
+  DG_DEV void tile(int row, bool ok, int n0, int N, LD& ld, int /*split*/) const {
     const float al = ok ? __ldg(alpha + row) : 1.0f;
     const float c2 = al * coef2;
     float vmax = -FLT_MAX;
@@ -258,8 +283,8 @@ template <int BN, int STAGES, bool B_MN, class Epi>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap mA, const __grid_constant__ CUtensorMap mB0,
                 const __grid_constant__ CUtensorMap mB1, const __grid_constant__ CUtensorMap mB2,
-                int nb0, int nb1, int b_sub, int M, int N, int K, uint32_t b_lbo, uint32_t b_sbo,
-                Epi epi, int* status, StopCtl ctl) {
+                int nb0, int nb1, int b_sub, int M, int N, int K, int ksplit, uint32_t b_lbo,
+                uint32_t b_sbo, Epi epi, int* status, StopCtl ctl) {
   using L = GemmLayout<BN, STAGES, B_MN>;
   if (all_stopped(ctl.stop_at, ctl.B, ctl.step)) return;
   extern __shared__ uint8_t smem_raw[];
@@ -273,8 +298,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int num_m = (M + kBM - 1) / kBM, num_n = (N + BN - 1) / BN;
-  const int num_tiles = num_m * num_n;
-  const int nk = (K + kBK - 1) / kBK;
+  const int num_mn = num_m * num_n;
+  const int num_tiles = num_mn * ksplit;  // tile t: split t / num_mn, (m, n) from t % num_mn
+  const int nk_all = (K + kBK - 1) / kBK;
+  auto krange = [&](int tile, int& kb_lo, int& kb_hi) {
+    const int sp = tile / num_mn;
+    kb_lo = (int)((int64_t)sp * nk_all / ksplit);
+    kb_hi = (int)((int64_t)(sp + 1) * nk_all / ksplit);
+  };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -305,8 +336,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       uint32_t phase = 0;
       bool alive = true;
       for (int tile = blockIdx.x; tile < num_tiles && alive; tile += gridDim.x) {
-        const int m0 = (tile % num_m) * kBM, n0 = (tile / num_m) * BN;
-        for (int kb = 0; kb < nk; ++kb) {
+        const int tmn = tile % num_mn;
+        const int m0 = (tmn % num_m) * kBM, n0 = (tmn / num_m) * BN;
+        int kb_lo, kb_hi;
+        krange(tile, kb_lo, kb_hi);
+        for (int kb = kb_lo; kb < kb_hi; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1, status, abort)) {
             alive = false;
             break;
@@ -353,7 +387,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       if (!mbar_wait(&tempty[acc], aph ^ 1, status, abort)) break;
       tc_fence_after();
       const uint32_t dt = tmem + acc * BN;
-      for (int kb = 0; kb < nk; ++kb) {
+      int kb_lo, kb_hi;
+      krange(tile, kb_lo, kb_hi);
+      for (int kb = kb_lo; kb < kb_hi; ++kb) {
         if (!mbar_wait(&full[stage], phase, status, abort)) {
           alive = false;
           break;
@@ -367,7 +403,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             const uint64_t ad = sdesc_sw128(sa + kk * 32, 16, 1024);
             const uint64_t bd = B_MN ? sdesc_sw128(sb + kk * 2048, b_lbo, b_sbo)
                                      : sdesc_sw128(sb + kk * 32, 16, 1024);
-            umma_bf16(dt, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+            umma_bf16(dt, ad, bd, idesc, (kb != kb_lo || kk != 0) ? 1u : 0u);
           }
           umma_commit(&empty[stage]);
         }
@@ -389,11 +425,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const uint32_t aph = (it >> 1) & 1;
       if (!mbar_wait(&tfull[acc], aph, status, abort)) break;
       tc_fence_after();
-      const int m0 = (tile % num_m) * kBM, n0 = (tile / num_m) * BN;
+      const int tmn = tile % num_mn;
+      const int m0 = (tmn % num_m) * kBM, n0 = (tmn / num_m) * BN;
       const int row = m0 + r_local;
       const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
       auto ld = [&](int c, float(&v)[32]) { tmem_ld32(tb + c * 32, v); };
-      epi.template tile<BN>(row, row < M, n0, N, ld);
+      epi.template tile<BN>(row, row < M, n0, N, ld, tile / num_mn);
       tc_fence_before();
       mbar_arrive(&tempty[acc]);
     }
@@ -457,15 +494,15 @@ template <int BN, int STAGES, bool B_MN, class Epi>
 static cudaError_t run_gemm(const CUtensorMap& mA, const CUtensorMap& mB0, const CUtensorMap& mB1,
                             const CUtensorMap& mB2, int nb0, int nb1, int b_sub, int M, int N, int K,
                             uint32_t lbo, uint32_t sbo, const Epi& epi, int* status, StopCtl ctl,
-                            cudaStream_t st) {
+                            cudaStream_t st, int ksplit = 1) {
   using L = GemmLayout<BN, STAGES, B_MN>;
   auto kern = gemm_kernel<BN, STAGES, B_MN, Epi>;
   cudaError_t e = set_smem_once<gemm_kernel<BN, STAGES, B_MN, Epi>>(L::kSmem);
   if (e != cudaSuccess) return e;
-  const int tiles = cdiv(M, kBM) * cdiv(N, BN);
+  const int tiles = cdiv(M, kBM) * cdiv(N, BN) * ksplit;
   const int grid = tiles < num_sms() ? tiles : num_sms();
-  kern<<<grid, kGemmThreads, L::kSmem, st>>>(mA, mB0, mB1, mB2, nb0, nb1, b_sub, M, N, K, lbo, sbo,
-                                             epi, status, ctl);
+  kern<<<grid, kGemmThreads, L::kSmem, st>>>(mA, mB0, mB1, mB2, nb0, nb1, b_sub, M, N, K, ksplit, lbo,
+                                             sbo, epi, status, ctl);
   return cudaGetLastError();
 }
 
@@ -487,11 +524,106 @@ cudaError_t launch_debug_gemm(const void* A, const void* Bm, float* D, int M, in
   return run_gemm<256, 4, true>(mA, mB, mB, mB, N, 0, 64, M, N, K, lbo, sbo, epi, status, ctl, st);
 }
 
+int gemm_ksplit(int M, int N, int K) {
+  const int tiles = cdiv(M, kBM) * cdiv(N, 128);
+  const int nk = cdiv(K, kBK);
+  int ks = kTargetCtas / tiles;
+  if (ks > nk / 2) ks = nk / 2;
+  if (ks > 16) ks = 16;
+  return ks < 1 ? 1 : ks;
+}
+
+// Sum of the K-split partials of one row segment of 8 columns, then the
+// residual / GELU epilogue of the small GEMMs, bf16 out.
+__global__ void __launch_bounds__(256)
+    splitk_bf16_kernel(const float* part, int ksplit, int M, int N, __nv_bfloat16* out, int ldo,
+                       const __nv_bfloat16* resid, int ldr, int gelu, int C, StopCtl ctl) {
+  if (all_stopped(ctl.stop_at, ctl.B, ctl.step)) return;
+  const int row = blockIdx.y;
+  const int c8 = (blockIdx.x * blockDim.x + threadIdx.x) * 8;
+  if (c8 >= N || !canvas_active(ctl.stop_at, row / C, ctl.step)) return;
+  float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  for (int sp = 0; sp < ksplit; ++sp) {
+    const float4* src = reinterpret_cast<const float4*>(part + ((size_t)sp * M + row) * N + c8);
+    const float4 x = src[0], y = src[1];
+    v[0] += x.x; v[1] += x.y; v[2] += x.z; v[3] += x.w;
+    v[4] += y.x; v[5] += y.y; v[6] += y.z; v[7] += y.w;
+  }
+  if (resid) {
+    uint4 r = *reinterpret_cast<const uint4*>(resid + (size_t)row * ldr + c8);
+    const __nv_bfloat16* rb = reinterpret_cast<const __nv_bfloat16*>(&r);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) v[e] += __bfloat162float(rb[e]);
+  }
+  if (gelu) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) v[e] = 0.5f * v[e] * (1.0f + erff(v[e] * 0.70710678118654752f));
+  }
+  uint4 w;
+  w.x = pack_bf16(v[0], v[1]);
+  w.y = pack_bf16(v[2], v[3]);
+  w.z = pack_bf16(v[4], v[5]);
+  w.w = pack_bf16(v[6], v[7]);
+  *reinterpret_cast<uint4*>(out + (size_t)row * ldo + c8) = w;
+}
+
+// Sum of the K-split partials of the q / k / v projections; RoPE on the
+// (j, j + hd/2) pairs of q and k.  Thread = (row, head, j < hd/2).
+struct QkvOut {
+  __nv_bfloat16 *q, *k, *v;
+  const float2* rope;
+  int C, Hq, Hkv, nq, nkv, kv_rows, kv_row0, hd;
+};
+__global__ void __launch_bounds__(256)
+    splitk_qkv_kernel(const float* part, int ksplit, int M, int N, QkvOut o, StopCtl ctl) {
+  if (all_stopped(ctl.stop_at, ctl.B, ctl.step)) return;
+  const int row = blockIdx.y;
+  const int pidx = blockIdx.x * blockDim.x + threadIdx.x;
+  const int half = o.hd / 2;
+  if (pidx >= N / 2) return;
+  const int head = pidx / half, j = pidx % half;
+  const int col0 = head * o.hd + j, col1 = col0 + half;
+  float x0 = 0.f, x1 = 0.f;
+  for (int sp = 0; sp < ksplit; ++sp) {
+    const float* src = part + ((size_t)sp * M + row) * N;
+    x0 += src[col0];
+    x1 += src[col1];
+  }
+  const int b = row / o.C, i = row % o.C;
+  const bool is_q = col0 < o.nq;
+  const bool is_k = !is_q && col0 < o.nq + o.nkv;
+  if (is_q || is_k) {
+    const float2 r = o.rope[(size_t)i * half + j];
+    const float a0 = x0, a1 = x1;
+    x0 = a0 * r.x - a1 * r.y;
+    x1 = a0 * r.y + a1 * r.x;
+  }
+  __nv_bfloat16* dst;
+  if (is_q) {
+    dst = o.q + (((size_t)b * o.Hq + col0 / o.hd) * o.C + i) * o.hd;
+  } else {
+    const int hh = (col0 - o.nq - (is_k ? 0 : o.nkv)) / o.hd;
+    dst = (is_k ? o.k : o.v) + (((size_t)b * o.Hkv + hh) * o.kv_rows + o.kv_row0 + i) * o.hd;
+  }
+  dst[j] = __float2bfloat16_rn(x0);
+  dst[j + half] = __float2bfloat16_rn(x1);
+}
+
 cudaError_t launch_gemm_bf16(const void* A, const void* W, void* out, int ldo, const void* resid,
                              int ldr, int gelu, int M, int N, int K, int C, StopCtl ctl,
-                             int* status, cudaStream_t st) {
+                             int* status, float* part, size_t part_elems, cudaStream_t st) {
   CUtensorMap mA, mB;
   if (!tmap_kmajor(&mA, A, M, K, kBM) || !tmap_kmajor(&mB, W, N, K, 128)) return cudaErrorInvalidValue;
+  const int ks = gemm_ksplit(M, N, K);
+  if (ks > 1 && part && (size_t)ks * M * N <= part_elems && N % 8 == 0) {
+    EpiPartial ep{part, M, N};
+    cudaError_t e = run_gemm<128, 4, false>(mA, mB, mB, mB, N, 0, 128, M, N, K, 0, 0, ep, status, ctl, st, ks);
+    if (e != cudaSuccess) return e;
+    dim3 grid(cdiv(N / 8, 256), M);
+    splitk_bf16_kernel<<<grid, 256, 0, st>>>(part, ks, M, N, reinterpret_cast<__nv_bfloat16*>(out), ldo,
+                                             reinterpret_cast<const __nv_bfloat16*>(resid), ldr, gelu, C, ctl);
+    return cudaGetLastError();
+  }
   EpiBF16 epi{reinterpret_cast<__nv_bfloat16*>(out), ldo,
               reinterpret_cast<const __nv_bfloat16*>(resid), ldr, gelu, C, ctl};
   return run_gemm<128, 4, false>(mA, mB, mB, mB, N, 0, 128, M, N, K, 0, 0, epi, status, ctl, st);
@@ -506,7 +638,8 @@ static cudaError_t qkv_impl(const CUtensorMap& mA, const CUtensorMap& m0, const 
 
 cudaError_t launch_qkv(const void* a, const void* Wq, const void* Wk, const void* Wv, void* q,
                        void* k, void* v, int kv_rows, int kv_row0, const float2* rope,
-                       const dg_dims& D, StopCtl ctl, int* status, cudaStream_t st) {
+                       const dg_dims& D, StopCtl ctl, int* status, float* part, size_t part_elems,
+                       cudaStream_t st) {
   const int M = D.B * D.C, nq = Wq ? D.Hq * D.hd : 0, nkv = D.Hkv * D.hd;
   CUtensorMap mA, mq, mk, mv;
   if (!tmap_kmajor(&mA, a, M, D.d, kBM)) return cudaErrorInvalidValue;
@@ -520,6 +653,17 @@ cudaError_t launch_qkv(const void* a, const void* Wq, const void* Wk, const void
   const CUtensorMap& m1 = Wq ? mk : mv;
   const CUtensorMap& m2 = mv;
   const int nb0 = Wq ? nq : nkv, nb1 = Wq ? nkv : nkv;
+  const int ks = gemm_ksplit(M, N, D.d);
+  if (ks > 1 && part && (size_t)ks * M * N <= part_elems) {
+    EpiPartial ep{part, M, N};
+    cudaError_t e =
+        run_gemm<128, 4, false>(mA, m0, m1, m2, nb0, nb1, D.hd, M, N, D.d, 0, 0, ep, status, ctl, st, ks);
+    if (e != cudaSuccess) return e;
+    QkvOut o{bf(q), bf(k), bf(v), rope, D.C, D.Hq, D.Hkv, nq, nkv, kv_rows, kv_row0, D.hd};
+    dim3 grid(cdiv(N / 2, 256), M);
+    splitk_qkv_kernel<<<grid, 256, 0, st>>>(part, ks, M, N, o, ctl);
+    return cudaGetLastError();
+  }
   switch (D.hd) {
     case 32: {
       EpiQKV<32> e{bf(q), bf(k), bf(v), rope, D.C, D.Hq, D.Hkv, nq, nkv, kv_rows, kv_row0};

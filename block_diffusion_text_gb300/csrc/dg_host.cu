@@ -102,7 +102,8 @@ dg_status enqueue_step(const StepCtx& c, float tau, float b, float stop_H, uint6
   DG_TRY(pf.mark(DG_PROF_EMBED, 1));
   DG_TRY(pf.mark(DG_PROF_QKV, 0));
   DG_TRY(launch_qkv(at<void>(ws, L.a), c.model->Wq, c.model->Wk, c.model->Wv, at<void>(ws, L.q),
-                    at<void>(ws, L.kc), at<void>(ws, L.vc), D.C, 0, rope, D, ctl, status, c.st));
+                    at<void>(ws, L.kc), at<void>(ws, L.vc), D.C, 0, rope, D, ctl, status,
+                    at<float>(ws, L.gpart), L.gpart_elems, c.st));
   DG_TRY(pf.mark(DG_PROF_QKV, 1));
   AttnArgs aa{at<void>(ws, L.q), c.cache->K, c.cache->V, at<void>(ws, L.kc), at<void>(ws, L.vc),
               at<void>(ws, L.o), at<float>(ws, L.attn_o), at<float>(ws, L.attn_ml), D.B, D.C, D.Hq,
@@ -112,7 +113,8 @@ dg_status enqueue_step(const StepCtx& c, float tau, float b, float stop_H, uint6
   DG_TRY(pf.mark(DG_PROF_ATTN, 1));
   DG_TRY(pf.mark(DG_PROF_OPROJ, 0));
   DG_TRY(launch_gemm_bf16(at<void>(ws, L.o), c.model->Wo, at<void>(ws, L.h), D.d, at<void>(ws, L.a), D.d,
-                          0, M, D.d, D.Hq * D.hd, D.C, ctl, status, c.st));
+                          0, M, D.d, D.Hq * D.hd, D.C, ctl, status, at<float>(ws, L.gpart), L.gpart_elems,
+                          c.st));
   DG_TRY(pf.mark(DG_PROF_OPROJ, 1));
   LmArgs lm{};
   lm.h = at<void>(ws, L.h);
@@ -198,11 +200,11 @@ dg_status enqueue_step(const StepCtx& c, float tau, float b, float stop_H, uint6
   DG_TRY(pf.mark(DG_PROF_REDUCE, 1));
   DG_TRY(pf.mark(DG_PROF_FFW1, 0));
   DG_TRY(launch_gemm_bf16(at<void>(ws, L.u), c.model->W1, at<void>(ws, L.g), D.F, nullptr, 0, 1, M, D.F,
-                          D.d, D.C, ctl, status, c.st));
+                          D.d, D.C, ctl, status, at<float>(ws, L.gpart), L.gpart_elems, c.st));
   DG_TRY(pf.mark(DG_PROF_FFW1, 1));
   DG_TRY(pf.mark(DG_PROF_FFW2, 0));
   DG_TRY(launch_gemm_bf16(at<void>(ws, L.g), c.model->W2, c.canvas->z, D.d, nullptr, 0, 0, M, D.d, D.F,
-                          D.C, ctl, status, c.st));
+                          D.C, ctl, status, at<float>(ws, L.gpart), L.gpart_elems, c.st));
   DG_TRY(pf.mark(DG_PROF_FFW2, 1));
   if (out && out->debug) {
     const dg_step_debug* g = out->debug;
@@ -288,6 +290,17 @@ bool ws_layout(const dg_dims& D, int32_t cap, WsLayout* L) {
   const size_t NC = (size_t)cdiv(D.V, kGumbelChunk);
   L->gbest = take(4 * NC * M);
   L->gidx = take(4 * NC * M);
+  {
+    const int nq = D.Hq * D.hd, nkv = D.Hkv * D.hd;
+    const int shapes[5][2] = {{nq + 2 * nkv, D.d}, {D.d, nq}, {D.F, D.d}, {D.d, D.F}, {2 * nkv, D.d}};
+    size_t most = 0;
+    for (auto& sh : shapes) {
+      const size_t e = (size_t)gemm_ksplit((int)M, sh[0], sh[1]) * M * sh[0];
+      if (e > most) most = e;
+    }
+    L->gpart_elems = most;
+    L->gpart = take(4 * most);
+  }
   L->u = take(2 * M * D.d);
   L->g = take(2 * M * D.F);
   L->total = off;
@@ -393,7 +406,8 @@ dg_status dg_commit_block(const dg_model* model, dg_kv_cache* cache, const int32
   DG_TRY(launch_embed_rmsnorm(tokens, model->E, nullptr, at<void>(ws, L.a), rope, D, D.B * D.C, cache->len,
                               none, st));
   DG_TRY(launch_qkv(at<void>(ws, L.a), nullptr, model->Wk, model->Wv, nullptr, cache->K, cache->V,
-                    cache->cap, cache->len, rope, D, none, at<int>(ws, L.status), st));
+                    cache->cap, cache->len, rope, D, none, at<int>(ws, L.status), at<float>(ws, L.gpart),
+                    L.gpart_elems, st));
   cache->len += D.C;
   return DG_OK;
 }

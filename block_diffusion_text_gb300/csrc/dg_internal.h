@@ -41,6 +41,7 @@ struct WsLayout {
   size_t pm, pl, pS, pvmax, pidx;
   size_t Hd, lsum, fscale, amax, acc;
   size_t upart, gbest, gidx;
+  size_t gpart, gpart_elems;  // split-K partials of the small GEMMs
   size_t u, g;
   size_t total;
 };
@@ -71,14 +72,18 @@ cudaError_t launch_debug_gemm(const void* A, const void* Bm, float* D, int M, in
                               int b_mn_major, int* status, cudaStream_t st);
 // out bf16 [M][N] (row pitch ldo) = act(A[M][K] W[N][K]^T (+ resid)); rows of
 // stopped canvases (row / C) are left untouched when ctl.stop_at is set.
+// Small GEMMs that would leave SMs idle are split over K into `part`
+// (fp32, ksplit x M x N, at most part_elems) and reduced by a fused epilogue.
+int gemm_ksplit(int M, int N, int K);
 cudaError_t launch_gemm_bf16(const void* A, const void* W, void* out, int ldo, const void* resid,
                              int ldr, int gelu, int M, int N, int K, int C, StopCtl ctl,
-                             int* status, cudaStream_t st);
+                             int* status, float* part, size_t part_elems, cudaStream_t st);
 // Projections of a [M][d]: q (RoPE) to [B][Hq][C][hd], k (RoPE) and v to
 // [B][Hkv][kv_rows][hd] at row kv_row0 + i.  With Wq == nullptr only k, v.
 cudaError_t launch_qkv(const void* a, const void* Wq, const void* Wk, const void* Wv, void* q,
                        void* k, void* v, int kv_rows, int kv_row0, const float2* rope,
-                       const dg_dims& D, StopCtl ctl, int* status, cudaStream_t st);
+                       const dg_dims& D, StopCtl ctl, int* status, float* part, size_t part_elems,
+                       cudaStream_t st);
 // LM head with the statistics epilogue.
 struct LmArgs {
   const void* h;       // bf16 [M][d]

@@ -195,7 +195,7 @@ cudaError_t launch_stats(const StatsArgs& a, StopCtl ctl, cudaStream_t st) {
 // and the largest draw is 16.64, so entries with
 // log p0 < log(1/Z) - 2.81 - 16.64 - 0.02 can never win and skip the draw.
 // One CTA per (row, 8192-entry chunk).
-constexpr int kP0Threads = 256;
+constexpr int kP0Threads = kGumbelChunk / 32;
 constexpr float kGumbelMinDraw = -2.8136f;  // -log(-log((0.5) / 2^23))
 constexpr float kGumbelMaxDraw = 16.6355f;  // -log(-log(1 - 2^-24))
 
@@ -210,39 +210,49 @@ __global__ void __launch_bounds__(kP0Threads) p0_gumbel_kernel(P0Args a, StopCtl
   const float thr = expf(-logf(a.lsum[row]) + kGumbelMinDraw - kGumbelMaxDraw - 0.02f);
   float best = -FLT_MAX;
   int bidx = INT_MAX;
-  const int v_begin = chunk * kGumbelChunk;
-  const int v_end = min(a.V, v_begin + kGumbelChunk);
-  for (int v0 = v_begin + threadIdx.x * 8; v0 < v_end; v0 += kP0Threads * 8) {
+  // 32 contiguous entries per thread (inside one 256-column tile): four 16-byte
+  // loads in flight, one scale factor.
+  const int v0 = chunk * kGumbelChunk + threadIdx.x * 32;
+  if (v0 < a.V) {
+    const int nvec = min(4, (a.V - v0) / 8);  // V is a multiple of 8
     const float f = a.fscale[(size_t)(v0 / kLmBN) * a.M + row];
     uint4* p4 = reinterpret_cast<uint4*>(pt + v0);
-    uint4 x = *p4;
-    const __nv_bfloat16* xb = reinterpret_cast<const __nv_bfloat16*>(&x);
-    float p[8];
+    uint4 x[4];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) p[e] = __bfloat162float(xb[e]) * f;
-    uint4 y;
-    y.x = pack_bf16(p[0], p[1]);
-    y.y = pack_bf16(p[2], p[3]);
-    y.z = pack_bf16(p[4], p[5]);
-    y.w = pack_bf16(p[6], p[7]);
-    *p4 = y;
-    if (!gum) continue;
+    for (int q = 0; q < 4; ++q)
+      if (q < nvec) x[q] = p4[q];
 #pragma unroll
-    for (int g4 = 0; g4 < 2; ++g4) {
-      bool any = false;
+    for (int q = 0; q < 4; ++q) {
+      if (q >= nvec) break;
+      const __nv_bfloat16* xb = reinterpret_cast<const __nv_bfloat16*>(&x[q]);
+      float p[8];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) any |= p[g4 * 4 + e] >= thr;
-      if (!any) continue;
-      uint64_t w[4];
-      philox_block(w, a.seed, a.block, a.step, canvas, pos, (v0 + g4 * 4) >> 2, 0);
+      for (int e = 0; e < 8; ++e) p[e] = __bfloat162float(xb[e]) * f;
+      uint4 y;
+      y.x = pack_bf16(p[0], p[1]);
+      y.y = pack_bf16(p[2], p[3]);
+      y.z = pack_bf16(p[4], p[5]);
+      y.w = pack_bf16(p[6], p[7]);
+      p4[q] = y;
+      if (!gum) continue;
+      const int vq = v0 + q * 8;
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float pv = p[g4 * 4 + e];
-        if (pv >= thr && pv > 0.f) {
-          const float sc = logf(pv) + gumbel_from_word(w[e]);
-          if (sc > best) {
-            best = sc;
-            bidx = v0 + g4 * 4 + e;
+      for (int g4 = 0; g4 < 2; ++g4) {
+        bool any = false;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) any |= p[g4 * 4 + e] >= thr;
+        if (!any) continue;
+        uint64_t w[4];
+        philox_block(w, a.seed, a.block, a.step, canvas, pos, (vq + g4 * 4) >> 2, 0);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float pv = p[g4 * 4 + e];
+          if (pv >= thr && pv > 0.f) {
+            const float sc = logf(pv) + gumbel_from_word(w[e]);
+            if (sc > best) {
+              best = sc;
+              bidx = vq + g4 * 4 + e;
+            }
           }
         }
       }
