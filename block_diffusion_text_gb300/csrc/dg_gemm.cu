@@ -6,9 +6,10 @@
 //     double-buffered TMEM accumulator.  Epilogues: fp32 store (diagnostics),
 //     bf16 store with residual / GELU (output projection, FFW), RoPE
 //     projections (q, k, v), and the LM head statistics epilogue.
-//   * selfcond_kernel: u = p0 . E with p0 (bf16, rescaled in place after the
-//     LM head) as the A operand and E as the MN-major B operand, split over
-//     the vocabulary.
+//   * gemm_pair_kernel: the same engine on CTA pairs (M = 256 MMAs over two
+//     SMs), for the two vocabulary-sized products: the LM head and the
+//     self-conditioning contraction u = p0 . E (p0 rescaled in place after
+//     the LM head, E as the MN-major B operand, split over the vocabulary).
 #include <cfloat>
 
 #include "dg_common.cuh"
@@ -506,6 +507,255 @@ static cudaError_t run_gemm(const CUtensorMap& mA, const CUtensorMap& mB0, const
   return cudaGetLastError();
 }
 
+// ============================================================ pair GEMM
+// The same product on CTA pairs: a cluster of two CTAs computes an output
+// tile of 256 rows x BN columns with M = 256 MMAs (cta_group::2).  Each CTA
+// loads its 128 rows of A and its half (BN / 2 columns) of B, so a B tile is
+// fetched once per pair and each SM's shared memory holds and serves a third
+// less operand data per MMA than with two independent M = 128 tiles.  The
+// leader (rank 0) waits for both CTAs' copies on its own `full` barrier
+// (each copy signals it across the pair) and issues the MMAs; its commits
+// arrive on the `empty` / `tfull` barriers of both CTAs.  Each CTA's four
+// epilogue warps drain its own TMEM rows and arrive on the leader's `tempty`.
+// Persistent over tiles (split, n, m-pair), one tile sequence per cluster.
+template <int BN, int STAGES, bool B_MN>
+struct PairLayout {
+  static constexpr int kA = kBM * kBK * 2;         // this CTA's 128 rows of A
+  static constexpr int kB = (BN / 2) * kBK * 2;    // this CTA's half of the B tile
+  static constexpr int kStage = kA + kB;
+  static constexpr int kBar = STAGES * kStage;
+  static constexpr int kSmem = kBar + 256 + 1024;
+};
+
+template <int BN, int STAGES, bool B_MN, class Epi>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    gemm_pair_kernel(const __grid_constant__ CUtensorMap mA, const __grid_constant__ CUtensorMap mB, int M,
+                     int N, int K, int ksplit, Epi epi, int* status, StopCtl ctl) {
+  using L = PairLayout<BN, STAGES, B_MN>;
+  static_assert(!B_MN || (BN / 2) % 64 == 0, "MN-major B halves are whole 64-column blocks");
+  if (all_stopped(ctl.stop_at, ctl.B, ctl.step)) return;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kBar);
+  uint64_t* empty = full + STAGES;
+  uint64_t* tfull = empty + STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+  volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  const int cid = (int)cluster_id_x(), ncl = (int)num_clusters_x();
+  const int num_mp = (M + 2 * kBM - 1) / (2 * kBM), num_n = (N + BN - 1) / BN;
+  const int num_mn = num_mp * num_n;
+  const int num_tiles = num_mn * ksplit;  // tile t: split t / num_mn, m-pair and n from t % num_mn
+  const int nk_all = (K + kBK - 1) / kBK;
+  auto coords = [&](int tile, int& m0, int& n0, int& kb_lo, int& kb_hi) {
+    const int sp = tile / num_mn, tmn = tile % num_mn;
+    m0 = (tmn % num_mp) * 2 * kBM;
+    n0 = (tmn / num_mp) * BN;
+    kb_lo = (int)((int64_t)sp * nk_all / ksplit);
+    kb_hi = (int)((int64_t)(sp + 1) * nk_all / ksplit);
+  };
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 8);  // four epilogue warps in each CTA
+    }
+    *abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(tmem_slot, 2 * BN);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  cluster_sync();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      tma_prefetch(&mA);
+      tma_prefetch(&mB);
+      int stage = 0;
+      uint32_t phase = 0;
+      bool alive = true;
+      for (int tile = cid; tile < num_tiles && alive; tile += ncl) {
+        int m0, n0, kb_lo, kb_hi;
+        coords(tile, m0, n0, kb_lo, kb_hi);
+        const int arow = m0 + (int)rank * kBM, bcol = n0 + (int)rank * (BN / 2);
+        for (int kb = kb_lo; kb < kb_hi; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1, status, abort)) {
+            alive = false;
+            break;
+          }
+          uint8_t* sa = smem + stage * L::kStage;
+          uint8_t* sb = sa + L::kA;
+          if (leader) mbar_arrive_expect_tx(&full[stage], 2 * L::kStage);
+          const uint32_t bar = cluster_addr(&full[stage], 0);
+          tma_load_2d_pair(sa, &mA, bar, kb * kBK, arow);
+          if (!B_MN) {
+            tma_load_2d_pair(sb, &mB, bar, kb * kBK, bcol);
+          } else {
+#pragma unroll
+            for (int j = 0; j < BN / 128; ++j)
+              tma_load_2d_pair(sb + j * (kBK * 128), &mB, bar, bcol + 64 * j, kb * kBK);
+          }
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      // Wait until the leader's MMAs released every stage, so that no commit
+      // is still on its way to this CTA's barriers when it exits.
+      for (int i = 0; i < STAGES && alive; ++i) {
+        if (!mbar_wait(&empty[stage], phase ^ 1, status, abort)) break;
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (leader) {
+      constexpr uint32_t idesc = idesc_bf16(2 * kBM, BN, B_MN);
+      int stage = 0;
+      uint32_t phase = 0;
+      bool alive = true;
+      int it = 0;
+      for (int tile = cid; tile < num_tiles && alive; tile += ncl, ++it) {
+        const int acc = it & 1;
+        const uint32_t aph = (it >> 1) & 1;
+        if (!mbar_wait(&tempty[acc], aph ^ 1, status, abort)) break;
+        tc_fence_after();
+        const uint32_t dt = tmem + acc * BN;
+        int m0, n0, kb_lo, kb_hi;
+        coords(tile, m0, n0, kb_lo, kb_hi);
+        for (int kb = kb_lo; kb < kb_hi; ++kb) {
+          if (!mbar_wait(&full[stage], phase, status, abort)) {
+            alive = false;
+            break;
+          }
+          tc_fence_after();
+          if (lane == 0) {
+            const uint32_t sa = smem_u32(smem + stage * L::kStage);
+            const uint32_t sb = sa + L::kA;
+#pragma unroll
+            for (int kk = 0; kk < kBK / 16; ++kk) {
+              const uint64_t ad = sdesc_sw128(sa + kk * 32, 16, 1024);
+              const uint64_t bd = B_MN ? sdesc_sw128(sb + kk * 2048, kBK * 128, 1024)
+                                       : sdesc_sw128(sb + kk * 32, 16, 1024);
+              umma_bf16_pair(dt, ad, bd, idesc, (kb != kb_lo || kk != 0) ? 1u : 0u);
+            }
+            umma_commit_pair(&empty[stage]);
+          }
+          __syncwarp();
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (alive && lane == 0) umma_commit_pair(&tfull[acc]);
+        __syncwarp();
+      }
+    }
+  } else {
+    const int q = warp & 3;  // TMEM lane quarter this warp may read
+    const int r_local = q * 32 + lane;
+    int it = 0;
+    for (int tile = cid; tile < num_tiles; tile += ncl, ++it) {
+      const int acc = it & 1;
+      const uint32_t aph = (it >> 1) & 1;
+      if (!mbar_wait(&tfull[acc], aph, status, abort)) break;
+      tc_fence_after();
+      int m0, n0, kb_lo, kb_hi;
+      coords(tile, m0, n0, kb_lo, kb_hi);
+      const int row = m0 + (int)rank * kBM + r_local;
+      const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
+      auto ld = [&](int c, float(&v)[32]) { tmem_ld32(tb + c * 32, v); };
+      epi.template tile<BN>(row, row < M, n0, N, ld, tile / num_mn);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(cluster_addr(&tempty[acc], 0));
+    }
+  }
+  __syncwarp();
+  drain_if_aborted(abort);
+  tc_fence_before();
+  cluster_sync();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem, 2 * BN);
+  }
+}
+
+// Clusters of two that can be resident at once with this kernel's shared
+// memory (SMs per GPC may be odd, so it can be below half the SM count).
+template <auto Kernel>
+static int max_pair_clusters(int smem) {
+  static int n = -1;
+  if (n < 0) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * (kTargetCtas / 2), 1, 1);
+    cfg.blockDim = dim3(kGemmThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int c = 0;
+    if (cudaOccupancyMaxActiveClusters(&c, Kernel, &cfg) != cudaSuccess || c <= 0) {
+      cudaGetLastError();
+      c = 0;
+    }
+    n = c;
+  }
+  return n;
+}
+
+// Clusters a pair GEMM of this many tiles may use (0 if none can launch).
+template <int BN, int STAGES, bool B_MN, class Epi>
+static int pair_clusters() {
+  using L = PairLayout<BN, STAGES, B_MN>;
+  if (set_smem_once<gemm_pair_kernel<BN, STAGES, B_MN, Epi>>(L::kSmem) != cudaSuccess) return 0;
+  return max_pair_clusters<gemm_pair_kernel<BN, STAGES, B_MN, Epi>>(L::kSmem);
+}
+
+template <int BN, int STAGES, bool B_MN, class Epi>
+static cudaError_t run_gemm_pair(const CUtensorMap& mA, const CUtensorMap& mB, int M, int N, int K, int ksplit,
+                                 const Epi& epi, int* status, StopCtl ctl, cudaStream_t st) {
+  using L = PairLayout<BN, STAGES, B_MN>;
+  const int maxc = pair_clusters<BN, STAGES, B_MN, Epi>();
+  if (maxc <= 0) return cudaErrorInvalidConfiguration;
+  const int tiles = cdiv(M, 2 * kBM) * cdiv(N, BN) * ksplit;
+  const int ncl = tiles < maxc ? tiles : maxc;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * ncl, 1, 1);
+  cfg.blockDim = dim3(kGemmThreads, 1, 1);
+  cfg.dynamicSmemBytes = L::kSmem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, gemm_pair_kernel<BN, STAGES, B_MN, Epi>, mA, mB, M, N, K, ksplit, epi, status,
+                            ctl);
+}
+
 cudaError_t launch_debug_gemm(const void* A, const void* Bm, float* D, int M, int N, int K,
                               int b_mn_major, int* status, cudaStream_t st) {
   CUtensorMap mA, mB;
@@ -516,7 +766,14 @@ cudaError_t launch_debug_gemm(const void* A, const void* Bm, float* D, int M, in
     if (!tmap_kmajor(&mB, Bm, N, K, 256)) return cudaErrorInvalidValue;
     return run_gemm<256, 4, false>(mA, mB, mB, mB, N, 0, 256, M, N, K, 0, 0, epi, status, ctl, st);
   }
+  if (b_mn_major == 3) {  // CTA-pair engine, B [N][K]
+    if (!tmap_kmajor(&mB, Bm, N, K, 128)) return cudaErrorInvalidValue;
+    return run_gemm_pair<256, 6, false>(mA, mB, M, N, K, 1, epi, status, ctl, st);
+  }
   if (!tmap_mnmajor(&mB, Bm, K, N)) return cudaErrorInvalidValue;
+  if (b_mn_major == 4) {  // CTA-pair engine, B [K][N]
+    return run_gemm_pair<256, 6, true>(mA, mB, M, N, K, 1, epi, status, ctl, st);
+  }
   // 1: LBO = distance between 64-column blocks along N, SBO = between 8-row
   // groups along K (the layout the self-conditioning kernel uses); 2: swapped.
   const uint32_t lbo = b_mn_major == 1 ? kBK * 128 : 1024;
@@ -682,162 +939,35 @@ cudaError_t launch_qkv(const void* a, const void* Wq, const void* Wk, const void
 }
 
 cudaError_t launch_lmhead(const LmArgs& a, StopCtl ctl, int* status, cudaStream_t st) {
-  CUtensorMap mA, mB;
-  if (!tmap_kmajor(&mA, a.h, a.M, a.d, kBM) || !tmap_kmajor(&mB, a.E, a.V, a.d, kLmBN))
+  CUtensorMap mA, mB;  // B boxes: half a vocabulary tile (one CTA of a pair)
+  if (!tmap_kmajor(&mA, a.h, a.M, a.d, kBM) || !tmap_kmajor(&mB, a.E, a.V, a.d, kLmBN / 2))
     return cudaErrorInvalidValue;
   EpiLM epi{a.alpha, a.coef2, a.inv_sqrt_d, reinterpret_cast<__nv_bfloat16*>(a.pt), a.pm, a.pl,
             a.pS, a.pvmax, a.pidx, a.logits, a.M, a.V};
-  return run_gemm<kLmBN, 4, false>(mA, mB, mB, mB, a.V, 0, kLmBN, a.M, a.V, a.d, 0, 0, epi, status, ctl,
-                                   st);
+  return run_gemm_pair<kLmBN, 6, false>(mA, mB, a.M, a.V, a.d, 1, epi, status, ctl, st);
 }
 
 // ====================================================== self-conditioning
-constexpr int kScStages = 3;
-struct ScLayout {
-  static constexpr int kA = 2 * kBM * kBK * 2;  // 256 rows of p0, 32 KB
-  static constexpr int kB = kBK * kScBN * 2;    // 64 vocabulary rows x 256 columns of E, 32 KB
-  static constexpr int kStage = kA + kB;
-  static constexpr int kBar = kScStages * kStage;
-  static constexpr int kSmem = kBar + 256 + 1024;
-};
-__global__ void __launch_bounds__(kGemmThreads, 1)
-    selfcond_kernel(const __grid_constant__ CUtensorMap mP, const __grid_constant__ CUtensorMap mE,
-                    ScArgs a, int n_tiles, int m_pairs, int* status, StopCtl ctl) {
-  if (all_stopped(ctl.stop_at, ctl.B, ctl.step)) return;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = align1024(smem_raw);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + ScLayout::kBar);
-  uint64_t* empty = full + kScStages;
-  uint64_t* tfull = empty + kScStages;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tfull + 1);
-  volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
-
-  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  // adjacent CTAs share the vocabulary split (the same p0 rows, through L2)
-  const int nt = blockIdx.x % n_tiles;
-  const int rest = blockIdx.x / n_tiles;
-  const int mp = rest % m_pairs;
-  const int split = rest / m_pairs;
-  const int nkb = (a.V + kBK - 1) / kBK;
-  const int kb0 = (int)((int64_t)split * nkb / a.nsplit);
-  const int kb1 = (int)((int64_t)(split + 1) * nkb / a.nsplit);
-  const int m0 = mp * 2 * kBM, n0 = nt * kScBN;
-
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < kScStages; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
-    }
-    mbar_init(tfull, 1);
-    *abort = 0;
-    fence_mbar_init();
-  }
-  if (warp == 1) {
-    tmem_alloc(tmem_slot, 512);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
-
-  if (warp == 0) {
-    if (lane == 0) {
-      tma_prefetch(&mP);
-      tma_prefetch(&mE);
-      int stage = 0;
-      uint32_t phase = 0;
-      for (int kb = kb0; kb < kb1; ++kb) {
-        if (!mbar_wait(&empty[stage], phase ^ 1, status, abort)) break;
-        uint8_t* sa = smem + stage * ScLayout::kStage;
-        uint8_t* sb = sa + ScLayout::kA;
-        mbar_arrive_expect_tx(&full[stage], ScLayout::kStage);
-        tma_load_2d(sa, &mP, &full[stage], kb * kBK, m0);
-        tma_load_2d(sa + kBM * kBK * 2, &mP, &full[stage], kb * kBK, m0 + kBM);
-#pragma unroll
-        for (int j = 0; j < kScBN / 64; ++j)
-          tma_load_2d(sb + j * (kBK * 128), &mE, &full[stage], n0 + 64 * j, kb * kBK);
-        if (++stage == kScStages) {
-          stage = 0;
-          phase ^= 1;
-        }
-      }
-    }
-  } else if (warp == 1) {
-    constexpr uint32_t idesc = idesc_bf16(kBM, kScBN, true);
-    int stage = 0;
-    uint32_t phase = 0;
-    bool alive = true;
-    for (int kb = kb0; kb < kb1; ++kb) {
-      if (!mbar_wait(&full[stage], phase, status, abort)) {
-        alive = false;
-        break;
-      }
-      tc_fence_after();
-      if (lane == 0) {
-        const uint32_t sa = smem_u32(smem + stage * ScLayout::kStage);
-        const uint32_t sb = sa + ScLayout::kA;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-#pragma unroll
-          for (int kk = 0; kk < kBK / 16; ++kk) {
-            const uint64_t ad = sdesc_sw128(sa + h * (kBM * kBK * 2) + kk * 32, 16, 1024);
-            const uint64_t bd = sdesc_sw128(sb + kk * 2048, kBK * 128, 1024);
-            umma_bf16(tmem + h * kScBN, ad, bd, idesc, (kb != kb0 || kk != 0) ? 1u : 0u);
-          }
-        }
-        umma_commit(&empty[stage]);
-      }
-      __syncwarp();
-      if (++stage == kScStages) {
-        stage = 0;
-        phase ^= 1;
-      }
-    }
-    if (alive && lane == 0) umma_commit(tfull);
-    __syncwarp();
-  } else {
-    // Epilogue: the split's partial u tile, TMEM lane = row within the half.
-    if (mbar_wait(tfull, 0, status, abort)) {
-      tc_fence_after();
-      const int q = warp & 3;
-      const int rl = q * 32 + lane;
-#pragma unroll 1
-      for (int h = 0; h < 2; ++h) {
-        const int row = m0 + h * kBM + rl;
-        const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(h * kScBN);
-#pragma unroll 1
-        for (int c = 0; c < kScBN / 32; ++c) {
-          float v[32];
-          tmem_ld32(tb + c * 32, v);
-          const int col0 = n0 + c * 32;
-          if (row < a.M && col0 < a.d) {
-            float4* dst = reinterpret_cast<float4*>(a.upart + ((size_t)split * a.M + row) * a.d + col0);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) dst[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-          }
-        }
-      }
-    }
-  }
-  __syncthreads();
-  drain_if_aborted(abort);
-  if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc(tmem, 512);
-  }
+// u_split = p0[:, vocabulary split] . E[vocabulary split, :] on CTA pairs:
+// A = p0 [M][V] (K-major over the vocabulary), B = E [V][d] (MN-major), fp32
+// partials [split][M][d] summed by reduce_kernel.  Consecutive clusters take
+// the d-tiles of one split, so the p0 columns they share are read from HBM
+// once and from L2 after.
+int selfcond_active_splits(const dg_dims& D) {
+  const int bound = selfcond_splits(D);
+  const int tiles = cdiv(D.d, kScBN) * cdiv(D.B * D.C, 2 * kBM);
+  const int maxc = pair_clusters<kScBN, 6, true, EpiPartial>();
+  int ns = maxc / tiles;
+  if (ns > bound) ns = bound;
+  return ns < 1 ? 1 : ns;
 }
 
 cudaError_t launch_selfcond(const ScArgs& a, StopCtl ctl, int* status, cudaStream_t st) {
   CUtensorMap mP, mE;
   if (!tmap_kmajor(&mP, a.pt, a.M, a.V, kBM) || !tmap_mnmajor(&mE, a.E, a.V, a.d))
     return cudaErrorInvalidValue;
-  cudaError_t e = set_smem_once<selfcond_kernel>(ScLayout::kSmem);
-  if (e != cudaSuccess) return e;
-  const int n_tiles = cdiv(a.d, kScBN), m_pairs = cdiv(a.M, 2 * kBM);
-  const int grid = n_tiles * m_pairs * a.nsplit;
-  selfcond_kernel<<<grid, kGemmThreads, ScLayout::kSmem, st>>>(mP, mE, a, n_tiles, m_pairs, status, ctl);
-  return cudaGetLastError();
+  EpiPartial ep{a.upart, a.M, a.d};
+  return run_gemm_pair<kScBN, 6, true>(mP, mE, a.M, a.d, a.V, a.nsplit, ep, status, ctl, st);
 }
 
 }  // namespace dg

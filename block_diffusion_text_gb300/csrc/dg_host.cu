@@ -189,7 +189,7 @@ dg_status enqueue_step(const StepCtx& c, float tau, float b, float stop_H, uint6
   sc.M = M;
   sc.V = D.V;
   sc.d = D.d;
-  sc.nsplit = selfcond_splits(D);
+  sc.nsplit = selfcond_active_splits(D);
   DG_TRY(pf.mark(DG_PROF_SELFCOND, 0));
   DG_TRY(launch_selfcond(sc, ctl, status, c.st));
   DG_TRY(pf.mark(DG_PROF_SELFCOND, 1));
@@ -244,7 +244,7 @@ namespace dg {
 
 int selfcond_splits(const dg_dims& D) {
   const int n_tiles = cdiv(D.d, kScBN), m_pairs = cdiv((int64_t)D.B * D.C, 256);
-  int ns = kTargetCtas / (n_tiles * m_pairs);
+  int ns = (kTargetCtas / 2) / (n_tiles * m_pairs);  // one CTA pair per (split, tile)
   const int nkb = cdiv(D.V, 64);
   if (ns > nkb) ns = nkb;
   if (ns > 64) ns = 64;
@@ -414,7 +414,7 @@ dg_status dg_commit_block(const dg_model* model, dg_kv_cache* cache, const int32
 
 dg_status dg_debug_gemm(const void* A, const void* Bm, float* D, int32_t M, int32_t N, int32_t K,
                         int32_t b_mn_major, void* stream) {
-  if (!A || !Bm || !D || M <= 0 || N <= 0 || K <= 0 || b_mn_major < 0 || b_mn_major > 2)
+  if (!A || !Bm || !D || M <= 0 || N <= 0 || K <= 0 || b_mn_major < 0 || b_mn_major > 4)
     return DG_ERR_ARG;
   if (K % 8 != 0 || N % 8 != 0) return DG_ERR_SHAPE;
   int* status = nullptr;

@@ -29,8 +29,6 @@ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 bool attn_use_tc(const dg_dims& D, int P);
 void attn_split(const dg_dims& D, int T, int P, int* nsplit, int* keys_per_split);
 int attn_max_splits(const dg_dims& D, int T);
-// Split of the vocabulary (the contraction of p0 . E) between CTAs.
-int selfcond_splits(const dg_dims& D);
 
 // Byte offsets of every buffer in the caller's workspace.
 struct WsLayout {
@@ -106,6 +104,11 @@ struct ScArgs {
   int M, V, d, nsplit;
 };
 cudaError_t launch_selfcond(const ScArgs& a, StopCtl ctl, int* status, cudaStream_t st);
+// Vocabulary splits of the self-conditioning contraction: selfcond_splits is
+// the bound the workspace is sized for, selfcond_active_splits what a launch
+// on the current device uses (at most the bound).
+int selfcond_splits(const dg_dims& D);
+int selfcond_active_splits(const dg_dims& D);
 // The stored tiles become p0 in place, and the Gumbel-max search of the
 // accepted rows runs over vocabulary chunks in the same pass.
 constexpr int kGumbelChunk = 8192;

@@ -254,7 +254,9 @@ DG_API dg_status dg_attention_noalloc(const void* q, const void* K, const void* 
  * in isolation (not a step of the method).  D fp32 [M][N] = A B^T with
  * A bf16 [M][K], and B bf16 [N][K] when b_mn_major == 0, or B bf16 [K][N]
  * when b_mn_major == 1 (the layout of E in the self-conditioning contraction).
- * K, N multiples of 8.                                                        */
+ * b_mn_major == 3 / 4 run the same products (B [N][K] / B [K][N]) on the
+ * CTA-pair engine (M = 256 MMAs over two SMs) that the LM head and the
+ * self-conditioning contraction use.  K, N multiples of 8.                     */
 DG_API dg_status dg_debug_gemm(const void* A, const void* Bm, float* D, int32_t M, int32_t N, int32_t K,
                         int32_t b_mn_major, void* stream);
 

@@ -6,20 +6,34 @@ pytestmark = pytest.mark.gpu
 
 
 def _ref(A, B, mn):
-    Bk = B.double() if mn == 0 else B.double().T
+    Bk = B.double() if mn in (0, 3) else B.double().T
     return A.double() @ Bk.T
 
 
 @pytest.mark.parametrize("M,N,K", [(256, 512, 1024), (128, 256, 64), (200, 136, 200), (16, 64, 64),
                                    (300, 1000, 2816)])
-@pytest.mark.parametrize("mn", [0, 1])
+@pytest.mark.parametrize("mn", [0, 1, 3])
 def test_gemm_matches_matmul(M, N, K, mn):
     from block_diffusion_text_gb300 import dg
     g = torch.Generator(device="cuda").manual_seed(M * 7 + N)
     A = torch.randn(M, K, device="cuda", generator=g).to(torch.bfloat16)
-    B = torch.randn((N, K) if mn == 0 else (K, N), device="cuda", generator=g).to(torch.bfloat16)
+    B = torch.randn((N, K) if mn in (0, 3) else (K, N), device="cuda", generator=g).to(torch.bfloat16)
     D = dg.debug_gemm(A, B, mn)
     torch.cuda.synchronize()
     ref = _ref(A, B, mn)
+    err = (D.double() - ref).abs().max().item() / ref.abs().max().item()
+    assert err < 1e-5, err
+
+
+@pytest.mark.parametrize("M,N,K", [(256, 512, 1024), (16, 64, 64), (300, 2816, 256), (512, 200, 640)])
+def test_pair_gemm_mn_major_b(M, N, K):
+    """The CTA-pair engine with B [K][N] (each CTA holds 128 of the 256 columns of a tile)."""
+    from block_diffusion_text_gb300 import dg
+    g = torch.Generator(device="cuda").manual_seed(M + 3 * N)
+    A = torch.randn(M, K, device="cuda", generator=g).to(torch.bfloat16)
+    B = torch.randn(K, N, device="cuda", generator=g).to(torch.bfloat16)
+    D = dg.debug_gemm(A, B, 4)
+    torch.cuda.synchronize()
+    ref = _ref(A, B, 4)
     err = (D.double() - ref).abs().max().item() / ref.abs().max().item()
     assert err < 1e-5, err
