@@ -103,7 +103,8 @@ class ClockSampler:
         except Exception:
             uuid = str(device_index)
         self.cmd = ["nvidia-smi", f"--id={uuid}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                    "-lms", "200"]
+                    "-lms", "20"]
+        self.window = None
 
     def start(self):
         try:
@@ -117,7 +118,11 @@ class ClockSampler:
         for line in self.proc.stdout:
             parts = [p.strip() for p in line.split(",")]
             if len(parts) >= 8:
-                self.samples.append(parts)
+                self.samples.append((time.time(), parts))
+
+    def mark(self, t0, t1):
+        """Host-clock bounds of the timed region; only samples inside it are reported."""
+        self.window = (t0, t1)
 
     def stop(self):
         if self.proc is None:
@@ -128,8 +133,15 @@ class ClockSampler:
         except Exception:
             self.proc.kill()
         self.thread.join(timeout=2)
+        if self.window is not None:
+            inside = [p for t, p in self.samples if self.window[0] <= t <= self.window[1] + 0.025]
+        else:
+            inside = [p for _, p in self.samples]
+        n_all = len(self.samples)
+        self.samples = inside
         if not self.samples:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0,
+                    "samples_total": n_all}
 
         def num(x):
             try:
@@ -140,8 +152,10 @@ class ClockSampler:
         mx = [num(s[1]) for s in self.samples if num(s[1]) is not None]
         names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
         reasons = sorted({n for s in self.samples for n, v in zip(names, s[4:8]) if v.lower() == "active"})
+        pw = [num(s[2]) for s in self.samples if num(s[2]) is not None]
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": reasons, "samples": len(self.samples)}
+                "sm_mhz_min": min(sm) if sm else None, "power_w_max": max(pw) if pw else None,
+                "reasons": reasons, "samples": len(self.samples), "window": "timed region only"}
 
 
 # ------------------------------------------------------- algorithmic work --
@@ -330,10 +344,12 @@ def run_ours(args, world, rank, local):
     time.sleep(0.3)
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
+    h0 = time.time()
     t0.record(stream)
     graph.replay()
     t1.record(stream)
     torch.cuda.synchronize()
+    clocks.mark(h0, time.time())
     _barrier(world)
     clk = clocks.stop()
     elapsed_ms = t0.elapsed_time(t1)
@@ -472,9 +488,9 @@ def _kernel_nodes(graph):
 def _attn_splits(dims):
     """Key splits of the attention launch (mirrors the library's choice; used to count launches)."""
     T = dims.P + dims.C
-    if dims.hd == 128 and dims.P % 64 == 0:
-        units = math.ceil(dims.Hq // dims.Hkv * dims.C / 128) * dims.B * dims.Hkv
-        ns, blk = min(152 // units, math.ceil(T / 256), 64), 64
+    if dims.hd == 128 and dims.P % 128 == 0:
+        units = math.ceil(math.ceil(dims.Hq // dims.Hkv * dims.C / 128) / 2) * dims.B * dims.Hkv
+        ns, blk = min(152 // units, math.ceil(T / 256), 64), 128
     else:
         units = math.ceil(dims.C / 64) * dims.B * dims.Hq
         ns, blk = min(math.ceil(3 * 152 / units), math.ceil(T / 256), 64), 64

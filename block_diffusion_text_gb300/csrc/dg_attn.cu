@@ -28,6 +28,7 @@ DG_DEV int swz(int r, int c) {
 template <int HD>
 __global__ void __launch_bounds__(128)
     attn_kernel(AttnArgs a, int nqt, int nsplit, int kps, float scale_log2, StopCtl ctl) {
+  pdl_wait();
   if (all_stopped(ctl.stop_at, ctl.B, ctl.step)) return;
   constexpr int CH = HD / 8;  // 16-byte chunks per row
   extern __shared__ uint8_t smem_raw[];
@@ -220,6 +221,7 @@ __global__ void __launch_bounds__(128)
 
 // Merge of the per-chunk partials of one (canvas, head, query row).
 __global__ void attn_combine_kernel(AttnArgs a, int nsplit, StopCtl ctl) {
+  pdl_wait();
   if (all_stopped(ctl.stop_at, ctl.B, ctl.step)) return;
   const int hd = a.hd;
   const size_t row = blockIdx.x;  // ((b * Hq + h) * C + i)
@@ -267,8 +269,7 @@ int attn_max_splits(const dg_dims& D, int T) {
 }
 
 cudaError_t launch_attention_combine(const AttnArgs& a, int nsplit, StopCtl ctl, cudaStream_t st) {
-  attn_combine_kernel<<<a.B * a.Hq * a.C, a.hd, 0, st>>>(a, nsplit, ctl);
-  return cudaGetLastError();
+  return launch_pdl(attn_combine_kernel, dim3(a.B * a.Hq * a.C), dim3(a.hd), 0, st, a, nsplit, ctl);
 }
 
 template <int HD>
@@ -289,8 +290,7 @@ static cudaError_t attn_impl(const AttnArgs& a, StopCtl ctl, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   const float scale_log2 = 1.4426950408889634f / sqrtf((float)HD);
   dim3 grid(nqt * ns, a.B * a.Hq);
-  kern<<<grid, 128, smem, st>>>(a, nqt, ns, kps, scale_log2, ctl);
-  e = cudaGetLastError();
+  e = launch_pdl(kern, grid, dim3(128), smem, st, a, nqt, ns, kps, scale_log2, ctl);
   if (e != cudaSuccess || ns == 1) return e;
   return launch_attention_combine(a, ns, ctl, st);
 }

@@ -29,6 +29,15 @@ DG_DEV uint64_t globaltimer() {
   return t;
 }
 
+// ---------------------------------------------- programmatic launches ----
+// Every kernel of the library begins with pdl_wait(): wait until the kernel
+// before it in the stream has completed and its writes are visible (a no-op
+// when launched without programmatic serialisation).  No kernel triggers its
+// dependents early: CTAs of the next kernel parked on the SMs while this one
+// runs cost more than the launch latency they hide (measured), so the next
+// launch begins as this kernel's CTAs retire.
+DG_DEV void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ------------------------------------------------------------- mbarrier ----
 DG_DEV void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
@@ -70,6 +79,13 @@ DG_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, int* status, volatile int*
       return false;
     }
   }
+}
+
+// The same wait taken by a whole warp that goes on to warp-collective
+// tcgen05 loads / stores: every lane gets the same answer, so the warp never
+// splits between a lane that gave up and one that carries on.
+DG_DEV bool mbar_wait_warp(uint64_t* bar, uint32_t parity, int* status, volatile int* abort) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, status, abort));
 }
 
 // ------------------------------------------------------------------ TMA ----
@@ -132,6 +148,16 @@ DG_DEV void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t 
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accum)
       : "memory");
 }
+// D[tmem] (+)= A[tmem] * B[smem], bf16 inputs, fp32 accumulation: A (M = 128
+// rows, one per TMEM lane) is read from TMEM, two bf16 of consecutive K per
+// 32-bit column, so one K = 16 step spans 8 columns.
+DG_DEV void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc, uint32_t accum) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accum)
+      : "memory");
+}
 // Arrive on `bar` once all previously issued MMAs of this thread completed.
 DG_DEV void umma_commit(uint64_t* bar) {
   asm volatile(
@@ -159,6 +185,42 @@ DG_DEV void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   tmem_wait_ld();
 #pragma unroll
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// tmem_ld32 without the wait: several loads may be in flight; complete them
+// with tmem_wait_ld() before reading v.
+DG_DEV void tmem_ld32_async(uint32_t taddr, float (&v)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3]), "=f"(v[4]), "=f"(v[5]), "=f"(v[6]),
+        "=f"(v[7]), "=f"(v[8]), "=f"(v[9]), "=f"(v[10]), "=f"(v[11]), "=f"(v[12]), "=f"(v[13]),
+        "=f"(v[14]), "=f"(v[15]), "=f"(v[16]), "=f"(v[17]), "=f"(v[18]), "=f"(v[19]),
+        "=f"(v[20]), "=f"(v[21]), "=f"(v[22]), "=f"(v[23]), "=f"(v[24]), "=f"(v[25]),
+        "=f"(v[26]), "=f"(v[27]), "=f"(v[28]), "=f"(v[29]), "=f"(v[30]), "=f"(v[31])
+      : "r"(taddr)
+      : "memory");
+}
+// Warp-collective load of 16 consecutive 32-bit columns per lane (waits).
+DG_DEV void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+        "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+      : "r"(taddr)
+      : "memory");
+  tmem_wait_ld();
+}
+// Warp-collective store of 16 consecutive 32-bit columns per lane.
+DG_DEV void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
+      "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+      : "memory");
 }
 
 // Warp-collective store of 32 consecutive 32-bit columns per lane (inverse of

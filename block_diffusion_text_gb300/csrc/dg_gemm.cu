@@ -286,6 +286,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 const __grid_constant__ CUtensorMap mB1, const __grid_constant__ CUtensorMap mB2,
                 int nb0, int nb1, int b_sub, int M, int N, int K, int ksplit, uint32_t b_lbo,
                 uint32_t b_sbo, Epi epi, int* status, StopCtl ctl) {
+  pdl_wait();
   using L = GemmLayout<BN, STAGES, B_MN>;
   if (all_stopped(ctl.stop_at, ctl.B, ctl.step)) return;
   extern __shared__ uint8_t smem_raw[];
@@ -377,26 +378,26 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
     }
   } else if (warp == 1) {
-    constexpr uint32_t idesc = idesc_bf16(kBM, BN, B_MN);
-    int stage = 0;
-    uint32_t phase = 0;
-    bool alive = true;
-    int it = 0;
-    for (int tile = blockIdx.x; tile < num_tiles && alive; tile += gridDim.x, ++it) {
-      const int acc = it & 1;
-      const uint32_t aph = (it >> 1) & 1;
-      if (!mbar_wait(&tempty[acc], aph ^ 1, status, abort)) break;
-      tc_fence_after();
-      const uint32_t dt = tmem + acc * BN;
-      int kb_lo, kb_hi;
-      krange(tile, kb_lo, kb_hi);
-      for (int kb = kb_lo; kb < kb_hi; ++kb) {
-        if (!mbar_wait(&full[stage], phase, status, abort)) {
-          alive = false;
-          break;
-        }
+    if (lane == 0) {  // one thread waits and issues; the MMAs need no other lane
+      constexpr uint32_t idesc = idesc_bf16(kBM, BN, B_MN);
+      int stage = 0;
+      uint32_t phase = 0;
+      bool alive = true;
+      int it = 0;
+      for (int tile = blockIdx.x; tile < num_tiles && alive; tile += gridDim.x, ++it) {
+        const int acc = it & 1;
+        const uint32_t aph = (it >> 1) & 1;
+        if (!mbar_wait(&tempty[acc], aph ^ 1, status, abort)) break;
         tc_fence_after();
-        if (lane == 0) {
+        const uint32_t dt = tmem + acc * BN;
+        int kb_lo, kb_hi;
+        krange(tile, kb_lo, kb_hi);
+        for (int kb = kb_lo; kb < kb_hi; ++kb) {
+          if (!mbar_wait(&full[stage], phase, status, abort)) {
+            alive = false;
+            break;
+          }
+          tc_fence_after();
           const uint32_t sa = smem_u32(smem + stage * L::kStage);
           const uint32_t sb = sa + L::kA;
 #pragma unroll
@@ -407,16 +408,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             umma_bf16(dt, ad, bd, idesc, (kb != kb_lo || kk != 0) ? 1u : 0u);
           }
           umma_commit(&empty[stage]);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
         }
-        __syncwarp();
-        if (++stage == STAGES) {
-          stage = 0;
-          phase ^= 1;
-        }
+        if (alive) umma_commit(&tfull[acc]);
       }
-      if (alive && lane == 0) umma_commit(&tfull[acc]);
-      __syncwarp();
     }
+    __syncwarp();
   } else {
     const int q = warp & 3;  // TMEM lane quarter this warp may read
     const int r_local = q * 32 + lane;
@@ -424,7 +424,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++it) {
       const int acc = it & 1;
       const uint32_t aph = (it >> 1) & 1;
-      if (!mbar_wait(&tfull[acc], aph, status, abort)) break;
+      if (!mbar_wait_warp(&tfull[acc], aph, status, abort)) break;
       tc_fence_after();
       const int tmn = tile % num_mn;
       const int m0 = (tmn % num_m) * kBM, n0 = (tmn / num_m) * BN;
@@ -502,9 +502,8 @@ static cudaError_t run_gemm(const CUtensorMap& mA, const CUtensorMap& mB0, const
   if (e != cudaSuccess) return e;
   const int tiles = cdiv(M, kBM) * cdiv(N, BN) * ksplit;
   const int grid = tiles < num_sms() ? tiles : num_sms();
-  kern<<<grid, kGemmThreads, L::kSmem, st>>>(mA, mB0, mB1, mB2, nb0, nb1, b_sub, M, N, K, ksplit, lbo,
-                                             sbo, epi, status, ctl);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(grid), dim3(kGemmThreads), L::kSmem, st, mA, mB0, mB1, mB2, nb0, nb1, b_sub, M,
+                    N, K, ksplit, lbo, sbo, epi, status, ctl);
 }
 
 // ============================================================ pair GEMM
@@ -531,6 +530,7 @@ template <int BN, int STAGES, bool B_MN, class Epi>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap mA, const __grid_constant__ CUtensorMap mB, int M,
                      int N, int K, int ksplit, Epi epi, int* status, StopCtl ctl) {
+  pdl_wait();
   using L = PairLayout<BN, STAGES, B_MN>;
   static_assert(!B_MN || (BN / 2) % 64 == 0, "MN-major B halves are whole 64-column blocks");
   if (all_stopped(ctl.stop_at, ctl.B, ctl.step)) return;
@@ -625,7 +625,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
     }
   } else if (warp == 1) {
-    if (leader) {
+    if (leader && lane == 0) {  // one thread of the leader waits and issues for the pair
       constexpr uint32_t idesc = idesc_bf16(2 * kBM, BN, B_MN);
       int stage = 0;
       uint32_t phase = 0;
@@ -645,28 +645,25 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             break;
           }
           tc_fence_after();
-          if (lane == 0) {
-            const uint32_t sa = smem_u32(smem + stage * L::kStage);
-            const uint32_t sb = sa + L::kA;
+          const uint32_t sa = smem_u32(smem + stage * L::kStage);
+          const uint32_t sb = sa + L::kA;
 #pragma unroll
-            for (int kk = 0; kk < kBK / 16; ++kk) {
-              const uint64_t ad = sdesc_sw128(sa + kk * 32, 16, 1024);
-              const uint64_t bd = B_MN ? sdesc_sw128(sb + kk * 2048, kBK * 128, 1024)
-                                       : sdesc_sw128(sb + kk * 32, 16, 1024);
-              umma_bf16_pair(dt, ad, bd, idesc, (kb != kb_lo || kk != 0) ? 1u : 0u);
-            }
-            umma_commit_pair(&empty[stage]);
+          for (int kk = 0; kk < kBK / 16; ++kk) {
+            const uint64_t ad = sdesc_sw128(sa + kk * 32, 16, 1024);
+            const uint64_t bd = B_MN ? sdesc_sw128(sb + kk * 2048, kBK * 128, 1024)
+                                     : sdesc_sw128(sb + kk * 32, 16, 1024);
+            umma_bf16_pair(dt, ad, bd, idesc, (kb != kb_lo || kk != 0) ? 1u : 0u);
           }
-          __syncwarp();
+          umma_commit_pair(&empty[stage]);
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1;
           }
         }
-        if (alive && lane == 0) umma_commit_pair(&tfull[acc]);
-        __syncwarp();
+        if (alive) umma_commit_pair(&tfull[acc]);
       }
     }
+    __syncwarp();
   } else {
     const int q = warp & 3;  // TMEM lane quarter this warp may read
     const int r_local = q * 32 + lane;
@@ -674,7 +671,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     for (int tile = cid; tile < num_tiles; tile += ncl, ++it) {
       const int acc = it & 1;
       const uint32_t aph = (it >> 1) & 1;
-      if (!mbar_wait(&tfull[acc], aph, status, abort)) break;
+      if (!mbar_wait_warp(&tfull[acc], aph, status, abort)) break;
       tc_fence_after();
       int m0, n0, kb_lo, kb_hi;
       coords(tile, m0, n0, kb_lo, kb_hi);
@@ -745,13 +742,15 @@ static cudaError_t run_gemm_pair(const CUtensorMap& mA, const CUtensorMap& mB, i
   cfg.blockDim = dim3(kGemmThreads, 1, 1);
   cfg.dynamicSmemBytes = L::kSmem;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = kProgrammaticLaunch;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, gemm_pair_kernel<BN, STAGES, B_MN, Epi>, mA, mB, M, N, K, ksplit, epi, status,
                             ctl);
 }
@@ -795,6 +794,7 @@ int gemm_ksplit(int M, int N, int K) {
 __global__ void __launch_bounds__(256)
     splitk_bf16_kernel(const float* part, int ksplit, int M, int N, __nv_bfloat16* out, int ldo,
                        const __nv_bfloat16* resid, int ldr, int gelu, int C, StopCtl ctl) {
+  pdl_wait();
   if (all_stopped(ctl.stop_at, ctl.B, ctl.step)) return;
   const int row = blockIdx.y;
   const int c8 = (blockIdx.x * blockDim.x + threadIdx.x) * 8;
@@ -833,6 +833,7 @@ struct QkvOut {
 };
 __global__ void __launch_bounds__(256)
     splitk_qkv_kernel(const float* part, int ksplit, int M, int N, QkvOut o, StopCtl ctl) {
+  pdl_wait();
   if (all_stopped(ctl.stop_at, ctl.B, ctl.step)) return;
   const int row = blockIdx.y;
   const int pidx = blockIdx.x * blockDim.x + threadIdx.x;
@@ -877,9 +878,9 @@ cudaError_t launch_gemm_bf16(const void* A, const void* W, void* out, int ldo, c
     cudaError_t e = run_gemm<128, 4, false>(mA, mB, mB, mB, N, 0, 128, M, N, K, 0, 0, ep, status, ctl, st, ks);
     if (e != cudaSuccess) return e;
     dim3 grid(cdiv(N / 8, 256), M);
-    splitk_bf16_kernel<<<grid, 256, 0, st>>>(part, ks, M, N, reinterpret_cast<__nv_bfloat16*>(out), ldo,
-                                             reinterpret_cast<const __nv_bfloat16*>(resid), ldr, gelu, C, ctl);
-    return cudaGetLastError();
+    return launch_pdl(splitk_bf16_kernel, grid, dim3(256), 0, st, (const float*)part, ks, M, N,
+                      reinterpret_cast<__nv_bfloat16*>(out), ldo, reinterpret_cast<const __nv_bfloat16*>(resid),
+                      ldr, gelu, C, ctl);
   }
   EpiBF16 epi{reinterpret_cast<__nv_bfloat16*>(out), ldo,
               reinterpret_cast<const __nv_bfloat16*>(resid), ldr, gelu, C, ctl};
@@ -918,8 +919,7 @@ cudaError_t launch_qkv(const void* a, const void* Wq, const void* Wk, const void
     if (e != cudaSuccess) return e;
     QkvOut o{bf(q), bf(k), bf(v), rope, D.C, D.Hq, D.Hkv, nq, nkv, kv_rows, kv_row0, D.hd};
     dim3 grid(cdiv(N / 2, 256), M);
-    splitk_qkv_kernel<<<grid, 256, 0, st>>>(part, ks, M, N, o, ctl);
-    return cudaGetLastError();
+    return launch_pdl(splitk_qkv_kernel, grid, dim3(256), 0, st, (const float*)part, ks, M, N, o, ctl);
   }
   switch (D.hd) {
     case 32: {

@@ -24,7 +24,7 @@ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Split of the key sequence [prefix ; canvas] of length T (prefix P) into
 // chunks for the attention grid; returns the number of splits and the keys per
-// split.  Head dim 128 with P a multiple of 64 takes the tensor-core kernel,
+// split.  Head dim 128 with P a multiple of 128 takes the tensor-core kernel,
 // other shapes the warp-MMA kernel; attn_max_splits bounds both for any P <= cap.
 bool attn_use_tc(const dg_dims& D, int P);
 void attn_split(const dg_dims& D, int T, int P, int* nsplit, int* keys_per_split);
@@ -44,6 +44,27 @@ struct WsLayout {
   size_t total;
 };
 bool ws_layout(const dg_dims& D, int32_t cap, WsLayout* L);
+
+constexpr int kProgrammaticLaunch = 1;
+
+// Launch with programmatic stream serialisation: the launch may begin while
+// the kernel before it in the stream is still retiring (each kernel opens
+// with griddepcontrol.wait, so none reads its inputs early).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = kProgrammaticLaunch;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
 
 // Opt a kernel in to more than 48 KB of dynamic shared memory, once per
 // kernel (the value is fixed per kernel), so that enqueueing a step makes no

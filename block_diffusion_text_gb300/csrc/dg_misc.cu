@@ -22,6 +22,7 @@ __global__ void __launch_bounds__(kEmbThreads)
     embed_rmsnorm_kernel(const int32_t* tokens, const __nv_bfloat16* E, const __nv_bfloat16* z,
                          __nv_bfloat16* a, float2* rope, int d, float eps, int C, int P, int hd,
                          float rope_base, StopCtl ctl) {
+  pdl_wait();
   if (all_stopped(ctl.stop_at, ctl.B, ctl.step)) return;
   const int row = blockIdx.x;
   const int tok = tokens[row];
@@ -85,10 +86,9 @@ __global__ void __launch_bounds__(kEmbThreads)
 cudaError_t launch_embed_rmsnorm(const int32_t* tokens, const void* E, const void* z, void* a,
                                  float2* rope, const dg_dims& D, int rows, int P, StopCtl ctl,
                                  cudaStream_t st) {
-  embed_rmsnorm_kernel<<<rows, kEmbThreads, 0, st>>>(
-      tokens, reinterpret_cast<const __nv_bfloat16*>(E), reinterpret_cast<const __nv_bfloat16*>(z),
-      reinterpret_cast<__nv_bfloat16*>(a), rope, D.d, D.rms_eps, D.C, P, D.hd, D.rope_base, ctl);
-  return cudaGetLastError();
+  return launch_pdl(embed_rmsnorm_kernel, dim3(rows), dim3(kEmbThreads), 0, st, tokens,
+                    reinterpret_cast<const __nv_bfloat16*>(E), reinterpret_cast<const __nv_bfloat16*>(z),
+                    reinterpret_cast<__nv_bfloat16*>(a), rope, D.d, D.rms_eps, D.C, P, D.hd, D.rope_base, ctl);
 }
 
 // ------------------------------------------------------- tile statistics --
@@ -111,6 +111,7 @@ DG_DEV T block_reduce(T v, Op op, T* sh) {
 }
 
 __global__ void __launch_bounds__(kStatsThreads) stats_kernel(StatsArgs a, StopCtl ctl) {
+  pdl_wait();
   if (all_stopped(ctl.stop_at, ctl.B, ctl.step)) return;
   const int row = blockIdx.x;
   __shared__ float shf[kStatsThreads / 32];
@@ -178,8 +179,7 @@ __global__ void __launch_bounds__(kStatsThreads) stats_kernel(StatsArgs a, StopC
 }
 
 cudaError_t launch_stats(const StatsArgs& a, StopCtl ctl, cudaStream_t st) {
-  stats_kernel<<<a.M, kStatsThreads, 0, st>>>(a, ctl);
-  return cudaGetLastError();
+  return launch_pdl(stats_kernel, dim3(a.M), dim3(kStatsThreads), 0, st, a, ctl);
 }
 
 // ------------------------------------------- p0 and Gumbel-max sampling --
@@ -200,6 +200,7 @@ constexpr float kGumbelMinDraw = -2.8136f;  // -log(-log((0.5) / 2^23))
 constexpr float kGumbelMaxDraw = 16.6355f;  // -log(-log(1 - 2^-24))
 
 __global__ void __launch_bounds__(kP0Threads) p0_gumbel_kernel(P0Args a, StopCtl ctl) {
+  pdl_wait();
   if (all_stopped(ctl.stop_at, ctl.B, ctl.step)) return;
   const int row = blockIdx.y;
   const int chunk = blockIdx.x;
@@ -290,8 +291,7 @@ __global__ void __launch_bounds__(kP0Threads) p0_gumbel_kernel(P0Args a, StopCtl
 
 cudaError_t launch_p0_gumbel(const P0Args& a, StopCtl ctl, cudaStream_t st) {
   dim3 grid(cdiv(a.V, kGumbelChunk), a.M);
-  p0_gumbel_kernel<<<grid, kP0Threads, 0, st>>>(a, ctl);
-  return cudaGetLastError();
+  return launch_pdl(p0_gumbel_kernel, grid, dim3(kP0Threads), 0, st, a, ctl);
 }
 
 // --------------------------------------------------------------- sampler --
@@ -303,6 +303,7 @@ cudaError_t launch_p0_gumbel(const P0Args& a, StopCtl ctl, cudaStream_t st) {
 // (mean entropy <= stop_H and the argmax equal to the previous step's).
 // One CTA per canvas, one thread per (padded) position.
 __global__ void __launch_bounds__(1024) sampler_kernel(SamplerArgs a, int npow2) {
+  pdl_wait();
   const int b = blockIdx.x;
   const int i = threadIdx.x;
   const bool active = a.stop_at[b] >= a.step;
@@ -378,14 +379,14 @@ __global__ void __launch_bounds__(1024) sampler_kernel(SamplerArgs a, int npow2)
 cudaError_t launch_sampler(const SamplerArgs& a, cudaStream_t st) {
   int np = 32;
   while (np < a.C) np <<= 1;
-  sampler_kernel<<<a.B, np, 0, st>>>(a, np);
-  return cudaGetLastError();
+  return launch_pdl(sampler_kernel, dim3(a.B), dim3(np), 0, st, a, np);
 }
 
 // ------------------------------------------------ self-conditioning reduce --
 // u = sum of the per-split partials of p0 . E (bf16 out), and the Gumbel-max
 // token of accepted positions = the best (score, lowest index) over chunks.
 __global__ void __launch_bounds__(256) reduce_kernel(ReduceArgs a, StopCtl ctl) {
+  pdl_wait();
   if (all_stopped(ctl.stop_at, ctl.B, ctl.step)) return;
   const int row = blockIdx.x;
   const int n4 = a.d / 4;
@@ -420,12 +421,12 @@ __global__ void __launch_bounds__(256) reduce_kernel(ReduceArgs a, StopCtl ctl) 
 }
 
 cudaError_t launch_reduce(const ReduceArgs& a, StopCtl ctl, cudaStream_t st) {
-  reduce_kernel<<<a.M, 256, 0, st>>>(a, ctl);
-  return cudaGetLastError();
+  return launch_pdl(reduce_kernel, dim3(a.M), dim3(256), 0, st, a, ctl);
 }
 
 // ------------------------------------------------------- canvas + loop ----
 __global__ void canvas_init_kernel(int32_t* tokens, int B, int C, int V, uint64_t seed, int block) {
+  pdl_wait();
   const int t = blockIdx.x * blockDim.x + threadIdx.x;
   if (t >= B * C) return;
   uint64_t w[4];
@@ -435,12 +436,12 @@ __global__ void canvas_init_kernel(int32_t* tokens, int B, int C, int V, uint64_
 
 cudaError_t launch_canvas_init(int32_t* tokens, int B, int C, int V, uint64_t seed, int block,
                                cudaStream_t st) {
-  canvas_init_kernel<<<cdiv(B * C, 256), 256, 0, st>>>(tokens, B, C, V, seed, block);
-  return cudaGetLastError();
+  return launch_pdl(canvas_init_kernel, dim3(cdiv(B * C, 256)), dim3(256), 0, st, tokens, B, C, V, seed, block);
 }
 
 __global__ void loop_finish_kernel(const int* stop_at, int B, int N, int* steps_taken, int* converged,
                                    const int* prev_argmax, int* xhat0, int C) {
+  pdl_wait();
   const int t = blockIdx.x * blockDim.x + threadIdx.x;
   if (t < B) {
     const int s = stop_at[t];
@@ -453,9 +454,8 @@ __global__ void loop_finish_kernel(const int* stop_at, int B, int N, int* steps_
 
 cudaError_t launch_loop_finish(const int* stop_at, int B, int N, int* steps_taken, int* converged,
                                const int* prev_argmax, int* xhat0, int C, cudaStream_t st) {
-  loop_finish_kernel<<<cdiv(B * C > B ? B * C : B, 256), 256, 0, st>>>(stop_at, B, N, steps_taken,
-                                                                         converged, prev_argmax, xhat0, C);
-  return cudaGetLastError();
+  return launch_pdl(loop_finish_kernel, dim3(cdiv(B * C > B ? B * C : B, 256)), dim3(256), 0, st, stop_at, B, N,
+                    steps_taken, converged, prev_argmax, xhat0, C);
 }
 
 }  // namespace dg

@@ -242,7 +242,7 @@ DG_API dg_status dg_commit_block(const dg_model* model, dg_kv_cache* cache, cons
  * every GPU that loads it until exit), so no workspace is passed and nothing
  * is allocated.  DG_ERR_WORKSPACE (nothing launched) if the scratch this size
  * needs exceeds 16 MiB, e.g. 2 canvases of 8 heads over 8190 prefix keys (a
- * prefix that is not a multiple of 64 takes the warp-MMA kernel, which splits
+ * prefix that is not a multiple of 128 takes the warp-MMA kernel, which splits
  * the keys more finely).  The first call on a device looks up the array's device address
  * (cudaGetSymbolAddress) and should come before any stream capture.  All
  * calls share the array: calls that overlap on the GPU race.              */

@@ -14,9 +14,10 @@ from parity import (Collect, bf16_to_np, check_argmax, check_close_bf16, check_e
 pytestmark = pytest.mark.gpu
 
 RAGGED = synth.Dims(V=1000, d=128, C=40, B=3, Hq=4, Hkv=2, hd=64, F=192, P=100, cap=160)
-# head dim 128 with a prefix that is a multiple of 64: the tensor-core attention kernel, with a partial
-# canvas key block (C = 40) and a 3-head group whose 300 query rows leave a partial second Q block
-RAGGED_TC = synth.Dims(V=1000, d=128, C=100, B=2, Hq=6, Hkv=2, hd=128, F=192, P=192, cap=256)
+# head dim 128 with a prefix that is a multiple of 128: the tensor-core attention kernel, with a partial
+# canvas key block (C = 100) and a 3-head group whose 300 query rows leave a partial third Q tile and an
+# empty fourth one (Q tiles go in pairs)
+RAGGED_TC = synth.Dims(V=1000, d=128, C=100, B=2, Hq=6, Hkv=2, hd=128, F=192, P=256, cap=256)
 
 
 def _setup(dims, seed, alpha=None):
@@ -112,7 +113,7 @@ def test_ragged_step_tensor_core_attention():
 
 
 def test_tensor_core_attention_canvas_tail():
-    dims = synth.Dims(V=512, d=64, C=40, B=1, Hq=2, Hkv=2, hd=128, F=64, P=64, cap=64)
+    dims = synth.Dims(V=512, d=64, C=40, B=1, Hq=2, Hkv=2, hd=128, F=64, P=128, cap=128)
     _run_and_compare(dims, 13)
 
 

@@ -46,7 +46,7 @@ def test_attention_noalloc_matches_step_attention_twice():
 
 
 def test_attention_noalloc_rejects_sizes_beyond_its_scratch():
-    """Two canvases of 8 heads over an 8190-key prefix (not a multiple of 64, so the warp-MMA kernel
+    """Two canvases of 8 heads over an 8190-key prefix (not a multiple of 128, so the warp-MMA kernel
     with 8 key splits) need 17.0 MB of partials: rejected before any launch.  Every buffer is
     allocated at its full size all the same."""
     from block_diffusion_text_gb300 import dg
