@@ -305,8 +305,12 @@ DG_DEV uint32_t cluster_addr(const void* p, uint32_t rank) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
   return r;
 }
+// Arrive on an mbarrier of either CTA of the pair (default .release.cta
+// semantics: the callers signal completed tcgen05 stores or loads, ordered by
+// tcgen05.wait and tcgen05.fence::before_thread_sync; a cluster-scope
+// release would add a memory barrier to every call).
 DG_DEV void mbar_arrive_cluster(uint32_t caddr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(caddr) : "memory");
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(caddr) : "memory");
 }
 // 2-D tiled copy into this CTA's shared memory whose completion is counted on
 // an mbarrier of either CTA of the pair (cluster address).

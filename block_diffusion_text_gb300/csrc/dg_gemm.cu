@@ -256,7 +256,7 @@ struct EpiLM {
       }
     }
     if (ok) {
-      const size_t o = (size_t)(n0 / BN) * M + row;
+      const size_t o = (size_t)row * ((V + BN - 1) / BN) + n0 / BN;  // [row][tile]
       pm[o] = m2;
       pl[o] = l;
       pS[o] = S;

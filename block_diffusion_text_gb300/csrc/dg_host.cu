@@ -84,8 +84,10 @@ struct Prof {
 };
 
 // All kernels of one denoising step, in order, on ctx.st.
+// fill_rope: (re)compute the RoPE table of positions P + i; a canvas loop
+// fills it at its first step only (P is fixed for the loop).
 dg_status enqueue_step(const StepCtx& c, float tau, float b, float stop_H, uint64_t seed, int step,
-                       int block, const dg_step_out* out, int* accepted_log, int N) {
+                       int block, const dg_step_out* out, int* accepted_log, int N, bool fill_rope) {
   const dg_dims& D = c.model->dims;
   const WsLayout& L = c.L;
   void* ws = c.ws;
@@ -97,7 +99,8 @@ dg_status enqueue_step(const StepCtx& c, float tau, float b, float stop_H, uint6
   const Prof pf{out ? out->events : nullptr, c.st};
 
   DG_TRY(pf.mark(DG_PROF_EMBED, 0));
-  DG_TRY(launch_embed_rmsnorm(c.canvas->tokens, c.model->E, c.canvas->z, at<void>(ws, L.a), rope, D, M,
+  DG_TRY(launch_embed_rmsnorm(c.canvas->tokens, c.model->E, c.canvas->z, at<void>(ws, L.a),
+                              fill_rope ? rope : nullptr, D, M,
                               P, ctl, c.st));
   DG_TRY(pf.mark(DG_PROF_EMBED, 1));
   DG_TRY(pf.mark(DG_PROF_QKV, 0));
@@ -360,7 +363,7 @@ dg_status dg_denoise_step(const dg_model* model, const dg_kv_cache* cache, dg_ca
   if ((s = check_ws(model->dims, cache->cap, ws, ws_bytes, &c.L))) return s;
   // A lone step treats every canvas as still denoising.
   DG_TRY(cudaMemsetAsync(at<void>(ws, c.L.stop_at), 0x7f, 4 * (size_t)model->dims.B, c.st));
-  return enqueue_step(c, tau, b, 0.005f, seed, step, block, out, nullptr, 0);
+  return enqueue_step(c, tau, b, 0.005f, seed, step, block, out, nullptr, 0, true);
 }
 
 dg_status dg_denoise_canvas(const dg_model* model, const dg_kv_cache* cache, dg_canvas* canvas,
@@ -383,7 +386,8 @@ dg_status dg_denoise_canvas(const dg_model* model, const dg_kv_cache* cache, dg_
   for (int step = 0; step < N; ++step) {
     const double frac = N > 1 ? (double)step / (double)(N - 1) : 0.0;
     const float tau = (float)((double)sched->tau0 + ((double)sched->tau1 - (double)sched->tau0) * frac);
-    s = enqueue_step(c, tau, sched->b, sched->stop_H, seed, step, block, nullptr, result->accepted, N);
+    s = enqueue_step(c, tau, sched->b, sched->stop_H, seed, step, block, nullptr, result->accepted, N,
+                     step == 0);
     if (s) return s;
   }
   return cuda_status(launch_loop_finish(at<int>(ws, c.L.stop_at), D.B, N, result->steps_taken,

@@ -112,7 +112,7 @@ struct LmArgs {
   float inv_sqrt_d;
   void* pt;            // bf16 [M][V]  exp(s - m_tile)
   float *pm, *pl, *pS, *pvmax;
-  int* pidx;           // [NT][M]
+  int* pidx;           // [M][NT] (with pm, pl, pS, pvmax)
   float* logits;       // optional fp32 [M][V]
   int M, V, d;
 };
@@ -135,7 +135,7 @@ int selfcond_active_splits(const dg_dims& D);
 constexpr int kGumbelChunk = 8192;
 struct P0Args {
   void* pt;              // bf16 [M][V]: exp(s - m_tile) in, p0 out
-  const float* fscale;   // [NT][M]
+  const float* fscale;   // [M][NT]
   const float* lsum;     // [M]  Z
   const uint8_t* acc;    // [M]
   float* gbest;          // [NC][M]
@@ -172,7 +172,7 @@ struct StatsArgs {
   int NT, M;
   double* Hd;            // [M]
   float* lsum;           // [M]
-  float* fscale;         // [NT][M]
+  float* fscale;         // [M][NT]
   int* amax;             // [M]
   float* entropy;        // optional out [M]
   int* argmax_out;       // optional out [M]

@@ -94,92 +94,90 @@ cudaError_t launch_embed_rmsnorm(const int32_t* tokens, const void* E, const voi
 // ------------------------------------------------------- tile statistics --
 // Merge of the per-tile (max, sum, weighted sum, argmax) of each row into the
 // tempered-softmax entropy H = ln Z - S / Z, the argmax, Z, and the factors
-// exp(m_t - m) / Z that turn a stored tile exp(s - m_t) into p0.  One CTA per
-// row; tile weights in float, sums in double.
+// exp(m_t - m) / Z that turn a stored tile exp(s - m_t) into p0.  The tile
+// statistics are laid out [row][tile]; each row is taken by `wpr` warps of a
+// CTA (all eight for long rows, one for short ones), which read it with
+// coalesced loads.  Tile weights in float, sums in double.
 constexpr int kStatsThreads = 256;
+constexpr int kStatsWarps = kStatsThreads / 32;
 
+// Reduction over the wpr warps of each row (warps r*wpr .. r*wpr + wpr - 1).
 template <class T, class Op>
-DG_DEV T block_reduce(T v, Op op, T* sh) {
+DG_DEV T rows_reduce(T v, Op op, T* sh, int wpr) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = op(v, __shfl_xor_sync(0xffffffffu, v, o));
-  if (threadIdx.x % 32 == 0) sh[threadIdx.x / 32] = v;
+  const int warp = threadIdx.x / 32;
+  if (threadIdx.x % 32 == 0) sh[warp] = v;
   __syncthreads();
-  T r = sh[0];
-  for (int w = 1; w < (int)(blockDim.x / 32); ++w) r = op(r, sh[w]);
+  const int w0 = warp / wpr * wpr;
+  T r = sh[w0];
+  for (int w = 1; w < wpr; ++w) r = op(r, sh[w0 + w]);
   __syncthreads();
   return r;
 }
 
-__global__ void __launch_bounds__(kStatsThreads) stats_kernel(StatsArgs a, StopCtl ctl) {
+__global__ void __launch_bounds__(kStatsThreads) stats_kernel(StatsArgs a, int wpr, StopCtl ctl) {
   pdl_wait();
   if (all_stopped(ctl.stop_at, ctl.B, ctl.step)) return;
-  const int row = blockIdx.x;
-  __shared__ float shf[kStatsThreads / 32];
-  __shared__ double shd[kStatsThreads / 32];
-  __shared__ float shv[kStatsThreads / 32];
-  __shared__ int shi[kStatsThreads / 32];
+  const int warp = threadIdx.x / 32;
+  const int row = blockIdx.x * (kStatsWarps / wpr) + warp / wpr;
+  const bool ok = row < a.M;
+  const int t0 = (warp % wpr) * 32 + threadIdx.x % 32, tstep = wpr * 32;
+  const size_t base = (size_t)(ok ? row : 0) * a.NT;
+  __shared__ float shf[kStatsWarps];
+  __shared__ double shd[kStatsWarps];
+  __shared__ int shi[kStatsWarps];
   float mx = -FLT_MAX, vbest = -FLT_MAX;
   int ibest = INT_MAX;
-  for (int t = threadIdx.x; t < a.NT; t += blockDim.x) {
-    const size_t o = (size_t)t * a.M + row;
-    mx = fmaxf(mx, a.pm[o]);
-    const float v = a.pvmax[o];
-    const int i = a.pidx[o];
-    if (v > vbest || (v == vbest && i < ibest)) {
-      vbest = v;
-      ibest = i;
-    }
-  }
-  const float M2 = block_reduce(mx, [](float x, float y) { return fmaxf(x, y); }, shf);
-  // argmax: (value, lowest index) over the block
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float v2 = __shfl_xor_sync(0xffffffffu, vbest, o);
-    const int i2 = __shfl_xor_sync(0xffffffffu, ibest, o);
-    if (v2 > vbest || (v2 == vbest && i2 < ibest)) {
-      vbest = v2;
-      ibest = i2;
-    }
-  }
-  if (threadIdx.x % 32 == 0) {
-    shv[threadIdx.x / 32] = vbest;
-    shi[threadIdx.x / 32] = ibest;
-  }
-  double l = 0.0, S = 0.0;
-  for (int t = threadIdx.x; t < a.NT; t += blockDim.x) {
-    const size_t o = (size_t)t * a.M + row;
-    const float dm = a.pm[o] - M2;
-    const double w = (double)exp2f(dm);
-    l += w * (double)a.pl[o];
-    S += w * ((double)a.pS[o] + (double)a.pl[o] * (double)dm);
-  }
-  const double Z = block_reduce(l, [](double x, double y) { return x + y; }, shd);
-  const double St = block_reduce(S, [](double x, double y) { return x + y; }, shd);
-  const float invZ = (float)(1.0 / Z);
-  for (int t = threadIdx.x; t < a.NT; t += blockDim.x) {
-    const size_t o = (size_t)t * a.M + row;
-    a.fscale[o] = exp2f(a.pm[o] - M2) * invZ;
-  }
-  if (threadIdx.x == 0) {
-    float vb = -FLT_MAX;
-    int ib = INT_MAX;
-    for (int w = 0; w < (int)(blockDim.x / 32); ++w) {
-      if (shv[w] > vb || (shv[w] == vb && shi[w] < ib)) {
-        vb = shv[w];
-        ib = shi[w];
+  if (ok) {
+#pragma unroll 4
+    for (int t = t0; t < a.NT; t += tstep) {
+      mx = fmaxf(mx, a.pm[base + t]);
+      const float v = a.pvmax[base + t];
+      const int i = a.pidx[base + t];
+      if (v > vbest || (v == vbest && i < ibest)) {
+        vbest = v;
+        ibest = i;
       }
     }
+  }
+  const float M2 = rows_reduce(mx, [](float x, float y) { return fmaxf(x, y); }, shf, wpr);
+  // argmax: the largest value, lowest index among the threads that hold it
+  const float vrow = rows_reduce(vbest, [](float x, float y) { return fmaxf(x, y); }, shf, wpr);
+  const int irow =
+      rows_reduce(vbest == vrow ? ibest : INT_MAX, [](int x, int y) { return x < y ? x : y; }, shi, wpr);
+  double l = 0.0, S = 0.0;
+  if (ok) {
+#pragma unroll 4
+    for (int t = t0; t < a.NT; t += tstep) {
+      const float dm = a.pm[base + t] - M2;
+      const double w = (double)exp2f(dm);
+      const double pl = (double)a.pl[base + t];
+      l += w * pl;
+      S += w * ((double)a.pS[base + t] + pl * (double)dm);
+    }
+  }
+  const double Z = rows_reduce(l, [](double x, double y) { return x + y; }, shd, wpr);
+  const double St = rows_reduce(S, [](double x, double y) { return x + y; }, shd, wpr);
+  if (!ok) return;
+  const float invZ = (float)(1.0 / Z);
+  for (int t = t0; t < a.NT; t += tstep) a.fscale[base + t] = exp2f(a.pm[base + t] - M2) * invZ;
+  if (t0 == 0) {
     const double H = log(Z) - 0.69314718055994531 * St / Z;
     a.Hd[row] = H;
     a.lsum[row] = (float)Z;
-    a.amax[row] = ib;
+    a.amax[row] = irow;
     if (a.entropy) a.entropy[row] = (float)H;
-    if (a.argmax_out) a.argmax_out[row] = ib;
+    if (a.argmax_out) a.argmax_out[row] = irow;
   }
 }
 
 cudaError_t launch_stats(const StatsArgs& a, StopCtl ctl, cudaStream_t st) {
-  return launch_pdl(stats_kernel, dim3(a.M), dim3(kStatsThreads), 0, st, a, ctl);
+  // warps per row: about 4 tiles per thread, one to eight warps
+  int wpr = 1;
+  while (wpr < kStatsWarps && wpr * 32 * 4 < a.NT) wpr *= 2;
+  const int rows_per_cta = kStatsWarps / wpr;
+  return launch_pdl(stats_kernel, dim3(cdiv(a.M, rows_per_cta)), dim3(kStatsThreads), 0, st, a, wpr, ctl);
 }
 
 // ------------------------------------------- p0 and Gumbel-max sampling --
@@ -216,7 +214,7 @@ __global__ void __launch_bounds__(kP0Threads) p0_gumbel_kernel(P0Args a, StopCtl
   const int v0 = chunk * kGumbelChunk + threadIdx.x * 32;
   if (v0 < a.V) {
     const int nvec = min(4, (a.V - v0) / 8);  // V is a multiple of 8
-    const float f = a.fscale[(size_t)(v0 / kLmBN) * a.M + row];
+    const float f = a.fscale[(size_t)row * ((a.V + kLmBN - 1) / kLmBN) + v0 / kLmBN];
     uint4* p4 = reinterpret_cast<uint4*>(pt + v0);
     uint4 x[4];
 #pragma unroll
