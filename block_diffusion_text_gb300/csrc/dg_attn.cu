@@ -219,28 +219,69 @@ __global__ void __launch_bounds__(128)
   }
 }
 
-// Merge of the per-chunk partials of one (canvas, head, query row).
-__global__ void attn_combine_kernel(AttnArgs a, int nsplit, StopCtl ctl) {
+// Merge of the per-chunk partials: one warp per (canvas, head, query row),
+// eight rows per CTA.  Lane s holds the (max, sum) of chunks s and s + 32; the
+// head dim is split over the lanes (HD / 32 consecutive floats each).
+constexpr int kCombineRows = 8;
+
+template <int HD>
+__global__ void __launch_bounds__(32 * kCombineRows) attn_combine_kernel(AttnArgs a, int nsplit, StopCtl ctl) {
   pdl_wait();
   if (all_stopped(ctl.stop_at, ctl.B, ctl.step)) return;
-  const int hd = a.hd;
-  const size_t row = blockIdx.x;  // ((b * Hq + h) * C + i)
+  constexpr int VEC = HD / 32;
+  const int lane = threadIdx.x % 32;
+  const size_t nrows = (size_t)a.B * a.Hq * a.C;
+  const size_t row = (size_t)blockIdx.x * kCombineRows + threadIdx.x / 32;  // ((b * Hq + h) * C + i)
+  if (row >= nrows) return;
+  float m[2], l[2];
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const int s = lane + 32 * k;
+    const float2 v = s < nsplit ? *reinterpret_cast<const float2*>(a.ml + (s * nrows + row) * 2)
+                                : make_float2(-FLT_MAX, 0.f);
+    m[k] = v.x;
+    l[k] = v.y;
+  }
+  float M = fmaxf(m[0], m[1]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  float w[2], L = 0.f;
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    w[k] = lane + 32 * k < nsplit ? exp2f(m[k] - M) : 0.f;
+    L += w[k] * l[k];
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+  float acc[VEC];
+#pragma unroll
+  for (int e = 0; e < VEC; ++e) acc[e] = 0.f;
+#pragma unroll 4
+  for (int s = 0; s < nsplit; ++s) {
+    const float ws = __shfl_sync(0xffffffffu, w[s / 32], s % 32);
+    const float* src = a.opart + (s * nrows + row) * HD + lane * VEC;
+    if constexpr (VEC == 4) {
+      const float4 v = *reinterpret_cast<const float4*>(src);
+      acc[0] += v.x * ws;
+      acc[1] += v.y * ws;
+      acc[2] += v.z * ws;
+      acc[3] += v.w * ws;
+    } else if constexpr (VEC == 2) {
+      const float2 v = *reinterpret_cast<const float2*>(src);
+      acc[0] += v.x * ws;
+      acc[1] += v.y * ws;
+    } else {
+      acc[0] += src[0] * ws;
+    }
+  }
+  const float inv = 1.0f / L;
   const int i = (int)(row % a.C);
   const int bh = (int)(row / a.C);
   const int b = bh / a.Hq, h = bh % a.Hq;
-  const size_t stride = (size_t)a.B * a.Hq * a.C;
-  float m = -FLT_MAX;
-  for (int s = 0; s < nsplit; ++s) m = fmaxf(m, a.ml[(s * stride + row) * 2]);
-  float l = 0.f;
-  for (int s = 0; s < nsplit; ++s) l += a.ml[(s * stride + row) * 2 + 1] * exp2f(a.ml[(s * stride + row) * 2] - m);
-  const float inv = 1.0f / l;
-  for (int t = threadIdx.x; t < hd; t += blockDim.x) {
-    float acc = 0.f;
-    for (int s = 0; s < nsplit; ++s)
-      acc += a.opart[(s * stride + row) * hd + t] * exp2f(a.ml[(s * stride + row) * 2] - m);
-    reinterpret_cast<__nv_bfloat16*>(a.o)[((size_t)b * a.C + i) * ((size_t)a.Hq * hd) + (size_t)h * hd + t] =
-        __float2bfloat16_rn(acc * inv);
-  }
+  __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(a.o) + ((size_t)b * a.C + i) * ((size_t)a.Hq * HD) +
+                       (size_t)h * HD + lane * VEC;
+#pragma unroll
+  for (int e = 0; e < VEC; ++e) dst[e] = __float2bfloat16_rn(acc[e] * inv);
 }
 
 void attn_split_mma(const dg_dims& D, int T, int* nsplit, int* keys_per_split) {
@@ -269,7 +310,14 @@ int attn_max_splits(const dg_dims& D, int T) {
 }
 
 cudaError_t launch_attention_combine(const AttnArgs& a, int nsplit, StopCtl ctl, cudaStream_t st) {
-  return launch_pdl(attn_combine_kernel, dim3(a.B * a.Hq * a.C), dim3(a.hd), 0, st, a, nsplit, ctl);
+  if (nsplit > 64) return cudaErrorInvalidValue;
+  const dim3 grid(cdiv((int64_t)a.B * a.Hq * a.C, kCombineRows)), block(32 * kCombineRows);
+  switch (a.hd) {
+    case 32: return launch_pdl(attn_combine_kernel<32>, grid, block, 0, st, a, nsplit, ctl);
+    case 64: return launch_pdl(attn_combine_kernel<64>, grid, block, 0, st, a, nsplit, ctl);
+    case 128: return launch_pdl(attn_combine_kernel<128>, grid, block, 0, st, a, nsplit, ctl);
+  }
+  return cudaErrorInvalidValue;
 }
 
 template <int HD>

@@ -227,14 +227,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       float mx;
       {
-        float t32[32];
+        // 3-input maxima into four running values (two keys each per step)
+        static_assert(kTcKeys % 8 == 0, "key block");
+        float r4[4] = {sv[0], sv[1], sv[2], sv[3]};
 #pragma unroll
-        for (int c = 0; c < 32; ++c) t32[c] = fmaxf(fmaxf(sv[c], sv[c + 32]), fmaxf(sv[c + 64], sv[c + 96]));
+        for (int c = 4; c + 8 <= kTcKeys; c += 8) {
 #pragma unroll
-        for (int w = 16; w > 0; w >>= 1)
+          for (int k = 0; k < 4; ++k) r4[k] = fmax3(r4[k], sv[c + 2 * k], sv[c + 2 * k + 1]);
+        }
 #pragma unroll
-          for (int c = 0; c < w; ++c) t32[c] = fmaxf(t32[c], t32[c + w]);
-        mx = t32[0] * scale_log2;  // scale_log2 > 0
+        for (int k = 0; k < 4; ++k) r4[k] = fmaxf(r4[k], sv[kTcKeys - 4 + k]);
+        mx = fmaxf(fmaxf(r4[0], r4[1]), fmaxf(r4[2], r4[3])) * scale_log2;  // scale_log2 > 0
       }
       if (j == 0) {
         m_run = mx;
@@ -259,18 +262,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
         }
       }
-      const float nm = -m_run;
-      float rs[4] = {0.f, 0.f, 0.f, 0.f};
+      // p = 2^(s * scale - m) two keys at a time (paired fp32 FMA / add / sub)
+      const uint64_t scale2 = f2_pack(scale_log2, scale_log2), nm2 = f2_pack(-m_run, -m_run);
+      uint64_t rs2[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
 #pragma unroll
       for (int c = 0; c < kTcKeys / 32; ++c) {  // 32 keys: 16 columns of P_hi and of P_lo
         uint32_t hw[16], lw[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          const float p0 = ex2(fmaf(sv[32 * c + 2 * e], scale_log2, nm));
-          const float p1 = ex2(fmaf(sv[32 * c + 2 * e + 1], scale_log2, nm));
-          rs[e & 3] += p0 + p1;
+          float t0, t1;
+          f2_unpack(f2_fma(f2_pack(sv[32 * c + 2 * e], sv[32 * c + 2 * e + 1]), scale2, nm2), t0, t1);
+          const float p0 = ex2(t0), p1 = ex2(t1);
+          const uint64_t p2 = f2_pack(p0, p1);
+          rs2[e & 1] = f2_add(rs2[e & 1], p2);
           hw[e] = pack_bf16(p0, p1);
-          lw[e] = pack_bf16(p0 - __uint_as_float(hw[e] << 16), p1 - __uint_as_float(hw[e] & 0xffff0000u));
+          float l0, l1;
+          f2_unpack(f2_sub(p2, f2_pack(__uint_as_float(hw[e] << 16), __uint_as_float(hw[e] & 0xffff0000u))), l0, l1);
+          lw[e] = pack_bf16(l0, l1);
         }
         tmem_st16(tS + 16 * c, hw);
         tmem_st16(tS + kTcKeys / 2 + 16 * c, lw);
@@ -280,7 +288,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           mbar_arrive(&pready[2 * t + c / 2]);
         }
       }
-      l_run += (rs[0] + rs[1]) + (rs[2] + rs[3]);
+      {
+        float a0, a1, b0, b1;
+        f2_unpack(rs2[0], a0, a1);
+        f2_unpack(rs2[1], b0, b1);
+        l_run += (a0 + a1) + (b0 + b1);
+      }
     }
     if (ok && nblk > 0 && mbar_wait_warp(&pvdone[t], (nblk - 1) & 1, status, abort)) {
       tc_fence_after();
