@@ -872,6 +872,17 @@ cudaError_t launch_gemm_bf16(const void* A, const void* W, void* out, int ldo, c
                              int* status, float* part, size_t part_elems, cudaStream_t st) {
   CUtensorMap mA, mB;
   if (!tmap_kmajor(&mA, A, M, K, kBM) || !tmap_kmajor(&mB, W, N, K, 128)) return cudaErrorInvalidValue;
+  EpiBF16 epi{reinterpret_cast<__nv_bfloat16*>(out), ldo,
+              reinterpret_cast<const __nv_bfloat16*>(resid), ldr, gelu, C, ctl};
+  // When 64-column tiles fit in one wave and the K loop is short, they run
+  // unsplit (no partials, no reduce launch), which measured faster; otherwise
+  // 128-column tiles, split over K when too few to fill the GPU.
+  const int tiles64 = cdiv(M, kBM) * (N / 64);
+  if (N % 64 == 0 && tiles64 <= kTargetCtas && (K <= 1024 || (tiles64 >= 64 && K <= 2048))) {
+    CUtensorMap mB64;
+    if (!tmap_kmajor(&mB64, W, N, K, 64)) return cudaErrorInvalidValue;
+    return run_gemm<64, 6, false>(mA, mB64, mB64, mB64, N, 0, 64, M, N, K, 0, 0, epi, status, ctl, st);
+  }
   const int ks = gemm_ksplit(M, N, K);
   if (ks > 1 && part && (size_t)ks * M * N <= part_elems && N % 8 == 0) {
     EpiPartial ep{part, M, N};
@@ -882,8 +893,6 @@ cudaError_t launch_gemm_bf16(const void* A, const void* W, void* out, int ldo, c
                       reinterpret_cast<__nv_bfloat16*>(out), ldo, reinterpret_cast<const __nv_bfloat16*>(resid),
                       ldr, gelu, C, ctl);
   }
-  EpiBF16 epi{reinterpret_cast<__nv_bfloat16*>(out), ldo,
-              reinterpret_cast<const __nv_bfloat16*>(resid), ldr, gelu, C, ctl};
   return run_gemm<128, 4, false>(mA, mB, mB, mB, N, 0, 128, M, N, K, 0, 0, epi, status, ctl, st);
 }
 

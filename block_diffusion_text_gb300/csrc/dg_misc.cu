@@ -209,49 +209,53 @@ __global__ void __launch_bounds__(kP0Threads) p0_gumbel_kernel(P0Args a, StopCtl
   const float thr = expf(-logf(a.lsum[row]) + kGumbelMinDraw - kGumbelMaxDraw - 0.02f);
   float best = -FLT_MAX;
   int bidx = INT_MAX;
-  // 32 contiguous entries per thread (inside one 256-column tile): four 16-byte
-  // loads in flight, one scale factor.
-  const int v0 = chunk * kGumbelChunk + threadIdx.x * 32;
-  if (v0 < a.V) {
-    const int nvec = min(4, (a.V - v0) / 8);  // V is a multiple of 8
-    const float f = a.fscale[(size_t)row * ((a.V + kLmBN - 1) / kLmBN) + v0 / kLmBN];
-    uint4* p4 = reinterpret_cast<uint4*>(pt + v0);
-    uint4 x[4];
+  // Each warp takes 1024 contiguous entries (2 KB); load q of lane l is the
+  // 16-byte chunk q * 32 + l, so a warp's load covers 512 contiguous bytes and
+  // all 32 chunks of a load lie in one 256-column tile (one scale factor).
+  const int wbase = chunk * kGumbelChunk + (threadIdx.x / 32) * 1024;
+  const int lane = threadIdx.x % 32;
+  const size_t fbase = (size_t)row * ((a.V + kLmBN - 1) / kLmBN);
+  uint4 x[4];
+  float f[4];
 #pragma unroll
-    for (int q = 0; q < 4; ++q)
-      if (q < nvec) x[q] = p4[q];
+  for (int q = 0; q < 4; ++q) {
+    const int v = wbase + (q * 32 + lane) * 8;
+    if (v < a.V) {  // V is a multiple of 8
+      x[q] = *reinterpret_cast<const uint4*>(pt + v);
+      f[q] = a.fscale[fbase + (wbase + q * 256) / kLmBN];
+    }
+  }
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      if (q >= nvec) break;
-      const __nv_bfloat16* xb = reinterpret_cast<const __nv_bfloat16*>(&x[q]);
-      float p[8];
+  for (int q = 0; q < 4; ++q) {
+    const int vq = wbase + (q * 32 + lane) * 8;
+    if (vq >= a.V) break;
+    const __nv_bfloat16* xb = reinterpret_cast<const __nv_bfloat16*>(&x[q]);
+    float p[8];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) p[e] = __bfloat162float(xb[e]) * f;
-      uint4 y;
-      y.x = pack_bf16(p[0], p[1]);
-      y.y = pack_bf16(p[2], p[3]);
-      y.z = pack_bf16(p[4], p[5]);
-      y.w = pack_bf16(p[6], p[7]);
-      p4[q] = y;
-      if (!gum) continue;
-      const int vq = v0 + q * 8;
+    for (int e = 0; e < 8; ++e) p[e] = __bfloat162float(xb[e]) * f[q];
+    uint4 y;
+    y.x = pack_bf16(p[0], p[1]);
+    y.y = pack_bf16(p[2], p[3]);
+    y.z = pack_bf16(p[4], p[5]);
+    y.w = pack_bf16(p[6], p[7]);
+    *reinterpret_cast<uint4*>(pt + vq) = y;
+    if (!gum) continue;
 #pragma unroll
-      for (int g4 = 0; g4 < 2; ++g4) {
-        bool any = false;
+    for (int g4 = 0; g4 < 2; ++g4) {
+      bool any = false;
 #pragma unroll
-        for (int e = 0; e < 4; ++e) any |= p[g4 * 4 + e] >= thr;
-        if (!any) continue;
-        uint64_t w[4];
-        philox_block(w, a.seed, a.block, a.step, canvas, pos, (vq + g4 * 4) >> 2, 0);
+      for (int e = 0; e < 4; ++e) any |= p[g4 * 4 + e] >= thr;
+      if (!any) continue;
+      uint64_t w[4];
+      philox_block(w, a.seed, a.block, a.step, canvas, pos, (vq + g4 * 4) >> 2, 0);
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float pv = p[g4 * 4 + e];
-          if (pv >= thr && pv > 0.f) {
-            const float sc = logf(pv) + gumbel_from_word(w[e]);
-            if (sc > best) {
-              best = sc;
-              bidx = vq + g4 * 4 + e;
-            }
+      for (int e = 0; e < 4; ++e) {
+        const float pv = p[g4 * 4 + e];
+        if (pv >= thr && pv > 0.f) {
+          const float sc = logf(pv) + gumbel_from_word(w[e]);
+          if (sc > best) {
+            best = sc;
+            bidx = vq + g4 * 4 + e;
           }
         }
       }
