@@ -162,7 +162,7 @@ class ClockSampler:
 def kernel_work(d: synth.Dims):
     """Algorithmic FLOPs and HBM bytes per launch of the dominant kernels."""
     M, V, D = d.B * d.C, d.V, d.d
-    NT = math.ceil(V / 256)
+    NT = math.ceil(V / 128)  # softmax-statistics groups of 128 columns
     T = d.P + d.C
     lm_flops = 2.0 * M * V * D
     lm_bytes = 2.0 * V * D + 2.0 * M * D + 2.0 * M * V + 20.0 * NT * M + 4.0 * M

@@ -201,67 +201,76 @@ struct EpiLM {
   int* pidx;
   float* logits;
   int M, V;
+  // Statistics per group of kStatCols columns, so that a tile may be 128 or
+  // 256 columns wide.
   template <int BN, class LD>
   DG_DEV void tile(int row, bool ok, int n0, int N, LD& ld, int /*split*/) const {
+    static_assert(BN % kStatCols == 0, "a tile holds whole statistics groups");
     const float al = ok ? __ldg(alpha + row) : 1.0f;
     const float c2 = al * coef2;
-    float vmax = -FLT_MAX;
-    int imax = n0;
+    const int NT = (V + kStatCols - 1) / kStatCols;
 #pragma unroll 1
-    for (int c = 0; c < BN / 32; ++c) {
-      float v[32];
-      ld(c, v);
+    for (int g = 0; g < BN / kStatCols; ++g) {
+      const int g0 = n0 + g * kStatCols;
+      if (g0 >= N) break;  // uniform over the warp
+      float vmax = -FLT_MAX;
+      int imax = g0;
+#pragma unroll 1
+      for (int c = 0; c < kStatCols / 32; ++c) {
+        float v[32];
+        ld(g * (kStatCols / 32) + c, v);
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const int col = n0 + c * 32 + j;
-        if (col < N && v[j] > vmax) {
-          vmax = v[j];
-          imax = col;
+        for (int j = 0; j < 32; ++j) {
+          const int col = g0 + c * 32 + j;
+          if (col < N && v[j] > vmax) {
+            vmax = v[j];
+            imax = col;
+          }
         }
       }
-    }
-    const float m2 = vmax * c2;
-    float l = 0.f, S = 0.f;
+      const float m2 = vmax * c2;
+      float l = 0.f, S = 0.f;
 #pragma unroll 1
-    for (int c = 0; c < BN / 32; ++c) {
-      float v[32];
-      ld(c, v);
-      const int col0 = n0 + c * 32;
-      uint32_t pk[16];
+      for (int c = 0; c < kStatCols / 32; ++c) {
+        float v[32];
+        ld(g * (kStatCols / 32) + c, v);
+        const int col0 = g0 + c * 32;
+        uint32_t pk[16];
 #pragma unroll
-      for (int j = 0; j < 32; j += 2) {
-        const float t0 = fmaf(v[j], c2, -m2), t1 = fmaf(v[j + 1], c2, -m2);
-        const float p0 = (col0 + j < N) ? exp2f(t0) : 0.f;
-        const float p1 = (col0 + j + 1 < N) ? exp2f(t1) : 0.f;
-        l += p0 + p1;
-        S = fmaf(p0, t0, fmaf(p1, t1, S));
-        pk[j / 2] = pack_bf16(p0, p1);
+        for (int j = 0; j < 32; j += 2) {
+          const float t0 = fmaf(v[j], c2, -m2), t1 = fmaf(v[j + 1], c2, -m2);
+          const float p0 = (col0 + j < N) ? exp2f(t0) : 0.f;
+          const float p1 = (col0 + j + 1 < N) ? exp2f(t1) : 0.f;
+          l += p0 + p1;
+          S = fmaf(p0, t0, fmaf(p1, t1, S));
+          pk[j / 2] = pack_bf16(p0, p1);
+        }
+        if (ok) {
+          if (col0 + 32 <= N) {
+            uint4* dst = reinterpret_cast<uint4*>(pt + (size_t)row * V + col0);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              dst[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+          } else {
+            const __nv_bfloat16* pb = reinterpret_cast<const __nv_bfloat16*>(pk);
+            for (int j = 0; j < 32; ++j)
+              if (col0 + j < N) pt[(size_t)row * V + col0 + j] = pb[j];
+          }
+          if (logits) {
+            const float cl = al * inv_sqrt_d;
+            for (int j = 0; j < 32; ++j)
+              if (col0 + j < N) logits[(size_t)row * V + col0 + j] = v[j] * cl;
+          }
+        }
       }
       if (ok) {
-        if (col0 + 32 <= N) {
-          uint4* dst = reinterpret_cast<uint4*>(pt + (size_t)row * V + col0);
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-            dst[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
-        } else {
-          const __nv_bfloat16* pb = reinterpret_cast<const __nv_bfloat16*>(pk);
-          for (int j = 0; j < 32; ++j)
-            if (col0 + j < N) pt[(size_t)row * V + col0 + j] = pb[j];
-        }
-        if (logits) {
-          const float cl = al * inv_sqrt_d;
-          for (int j = 0; j < 32; ++j)
-            if (col0 + j < N) logits[(size_t)row * V + col0 + j] = v[j] * cl;
-        }
+        const size_t o = (size_t)row * NT + g0 / kStatCols;  // [row][group]
+        pm[o] = m2;
+        pl[o] = l;
+        pS[o] = S;
+        pvmax[o] = vmax;
+        pidx[o] = imax;
       }
-    }
-    if (ok) {
-      const size_t o = (size_t)row * ((V + BN - 1) / BN) + n0 / BN;  // [row][tile]
-      pm[o] = m2;
-      pl[o] = l;
-      pS[o] = S;
-      pvmax[o] = vmax;
-      pidx[o] = imax;
     }
   }
 };
@@ -526,13 +535,18 @@ struct PairLayout {
   static constexpr int kSmem = kBar + 256 + 1024;
 };
 
-template <int BN, int STAGES, bool B_MN, class Epi>
+// TAIL: when the last round of tiles would leave clusters idle (fewer
+// remaining tiles than clusters), those tiles are cut into two halves of BN / 2
+// columns (loaded through mBh, boxes of BN / 4 rows), so the round is shorter.
+template <int BN, int STAGES, bool B_MN, class Epi, bool TAIL = false>
 __global__ void __launch_bounds__(kGemmThreads, 1)
-    gemm_pair_kernel(const __grid_constant__ CUtensorMap mA, const __grid_constant__ CUtensorMap mB, int M,
-                     int N, int K, int ksplit, Epi epi, int* status, StopCtl ctl) {
+    gemm_pair_kernel(const __grid_constant__ CUtensorMap mA, const __grid_constant__ CUtensorMap mB,
+                     const __grid_constant__ CUtensorMap mBh, int M, int N, int K, int ksplit, Epi epi,
+                     int* status, StopCtl ctl) {
   pdl_wait();
   using L = PairLayout<BN, STAGES, B_MN>;
   static_assert(!B_MN || (BN / 2) % 64 == 0, "MN-major B halves are whole 64-column blocks");
+  static_assert(!TAIL || !B_MN, "half tiles are loaded K-major");
   if (all_stopped(ctl.stop_at, ctl.B, ctl.step)) return;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
@@ -549,12 +563,23 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const int cid = (int)cluster_id_x(), ncl = (int)num_clusters_x();
   const int num_mp = (M + 2 * kBM - 1) / (2 * kBM), num_n = (N + BN - 1) / BN;
   const int num_mn = num_mp * num_n;
-  const int num_tiles = num_mn * ksplit;  // tile t: split t / num_mn, m-pair and n from t % num_mn
+  const int num_full = num_mn * ksplit;  // tile t: split t / num_mn, m-pair and n from t % num_mn
   const int nk_all = (K + kBK - 1) / kBK;
-  auto coords = [&](int tile, int& m0, int& n0, int& kb_lo, int& kb_hi) {
+  // work items: full tiles, then (TAIL) the last round's tiles as two halves each
+  const int n_whole = num_full / ncl * ncl, n_rest = num_full - n_whole;
+  const bool halves = TAIL && ksplit == 1 && n_rest > 0 && 2 * n_rest <= ncl;
+  const int num_tiles = halves ? n_whole + 2 * n_rest : num_full;
+  auto coords = [&](int item, int& m0, int& n0, int& kb_lo, int& kb_hi, int& width) {
+    int tile = item, sub = 0;
+    width = BN;
+    if (halves && item >= n_whole) {
+      tile = n_whole + (item - n_whole) / 2;
+      sub = (item - n_whole) & 1;
+      width = BN / 2;
+    }
     const int sp = tile / num_mn, tmn = tile % num_mn;
     m0 = (tmn % num_mp) * 2 * kBM;
-    n0 = (tmn / num_mp) * BN;
+    n0 = (tmn / num_mp) * BN + sub * (BN / 2);
     kb_lo = (int)((int64_t)sp * nk_all / ksplit);
     kb_hi = (int)((int64_t)(sp + 1) * nk_all / ksplit);
   };
@@ -588,9 +613,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       uint32_t phase = 0;
       bool alive = true;
       for (int tile = cid; tile < num_tiles && alive; tile += ncl) {
-        int m0, n0, kb_lo, kb_hi;
-        coords(tile, m0, n0, kb_lo, kb_hi);
-        const int arow = m0 + (int)rank * kBM, bcol = n0 + (int)rank * (BN / 2);
+        int m0, n0, kb_lo, kb_hi, width;
+        coords(tile, m0, n0, kb_lo, kb_hi, width);
+        const int arow = m0 + (int)rank * kBM, bcol = n0 + (int)rank * (width / 2);
         for (int kb = kb_lo; kb < kb_hi; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1, status, abort)) {
             alive = false;
@@ -598,11 +623,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
           uint8_t* sa = smem + stage * L::kStage;
           uint8_t* sb = sa + L::kA;
-          if (leader) mbar_arrive_expect_tx(&full[stage], 2 * L::kStage);
+          if (leader) mbar_arrive_expect_tx(&full[stage], 2 * (L::kA + (width / 2) * kBK * 2));
           const uint32_t bar = cluster_addr(&full[stage], 0);
           tma_load_2d_pair(sa, &mA, bar, kb * kBK, arow);
           if (!B_MN) {
-            tma_load_2d_pair(sb, &mB, bar, kb * kBK, bcol);
+            tma_load_2d_pair(sb, width == BN ? &mB : &mBh, bar, kb * kBK, bcol);
           } else {
 #pragma unroll
             for (int j = 0; j < BN / 128; ++j)
@@ -626,7 +651,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
   } else if (warp == 1) {
     if (leader && lane == 0) {  // one thread of the leader waits and issues for the pair
-      constexpr uint32_t idesc = idesc_bf16(2 * kBM, BN, B_MN);
+      constexpr uint32_t idesc_full = idesc_bf16(2 * kBM, BN, B_MN);
+      constexpr uint32_t idesc_half = idesc_bf16(2 * kBM, BN / 2, B_MN);
       int stage = 0;
       uint32_t phase = 0;
       bool alive = true;
@@ -637,8 +663,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         if (!mbar_wait(&tempty[acc], aph ^ 1, status, abort)) break;
         tc_fence_after();
         const uint32_t dt = tmem + acc * BN;
-        int m0, n0, kb_lo, kb_hi;
-        coords(tile, m0, n0, kb_lo, kb_hi);
+        int m0, n0, kb_lo, kb_hi, width;
+        coords(tile, m0, n0, kb_lo, kb_hi, width);
+        const uint32_t idesc = width == BN ? idesc_full : idesc_half;
         for (int kb = kb_lo; kb < kb_hi; ++kb) {
           if (!mbar_wait(&full[stage], phase, status, abort)) {
             alive = false;
@@ -673,12 +700,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const uint32_t aph = (it >> 1) & 1;
       if (!mbar_wait_warp(&tfull[acc], aph, status, abort)) break;
       tc_fence_after();
-      int m0, n0, kb_lo, kb_hi;
-      coords(tile, m0, n0, kb_lo, kb_hi);
+      int m0, n0, kb_lo, kb_hi, width;
+      coords(tile, m0, n0, kb_lo, kb_hi, width);
       const int row = m0 + (int)rank * kBM + r_local;
       const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
       auto ld = [&](int c, float(&v)[32]) { tmem_ld32(tb + c * 32, v); };
-      epi.template tile<BN>(row, row < M, n0, N, ld, tile / num_mn);
+      if (!TAIL || width == BN)
+        epi.template tile<BN>(row, row < M, n0, N, ld, tile / num_mn);
+      else
+        epi.template tile<BN / 2>(row, row < M, n0, N, ld, 0);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(cluster_addr(&tempty[acc], 0));
@@ -722,18 +752,19 @@ static int max_pair_clusters(int smem) {
 }
 
 // Clusters a pair GEMM of this many tiles may use (0 if none can launch).
-template <int BN, int STAGES, bool B_MN, class Epi>
+template <int BN, int STAGES, bool B_MN, class Epi, bool TAIL = false>
 static int pair_clusters() {
   using L = PairLayout<BN, STAGES, B_MN>;
-  if (set_smem_once<gemm_pair_kernel<BN, STAGES, B_MN, Epi>>(L::kSmem) != cudaSuccess) return 0;
-  return max_pair_clusters<gemm_pair_kernel<BN, STAGES, B_MN, Epi>>(L::kSmem);
+  if (set_smem_once<gemm_pair_kernel<BN, STAGES, B_MN, Epi, TAIL>>(L::kSmem) != cudaSuccess) return 0;
+  return max_pair_clusters<gemm_pair_kernel<BN, STAGES, B_MN, Epi, TAIL>>(L::kSmem);
 }
 
-template <int BN, int STAGES, bool B_MN, class Epi>
-static cudaError_t run_gemm_pair(const CUtensorMap& mA, const CUtensorMap& mB, int M, int N, int K, int ksplit,
-                                 const Epi& epi, int* status, StopCtl ctl, cudaStream_t st) {
+template <int BN, int STAGES, bool B_MN, class Epi, bool TAIL = false>
+static cudaError_t run_gemm_pair(const CUtensorMap& mA, const CUtensorMap& mB, const CUtensorMap& mBh, int M,
+                                 int N, int K, int ksplit, const Epi& epi, int* status, StopCtl ctl,
+                                 cudaStream_t st) {
   using L = PairLayout<BN, STAGES, B_MN>;
-  const int maxc = pair_clusters<BN, STAGES, B_MN, Epi>();
+  const int maxc = pair_clusters<BN, STAGES, B_MN, Epi, TAIL>();
   if (maxc <= 0) return cudaErrorInvalidConfiguration;
   const int tiles = cdiv(M, 2 * kBM) * cdiv(N, BN) * ksplit;
   const int ncl = tiles < maxc ? tiles : maxc;
@@ -751,8 +782,8 @@ static cudaError_t run_gemm_pair(const CUtensorMap& mA, const CUtensorMap& mB, i
   attr[1].val.programmaticStreamSerializationAllowed = kProgrammaticLaunch;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, gemm_pair_kernel<BN, STAGES, B_MN, Epi>, mA, mB, M, N, K, ksplit, epi, status,
-                            ctl);
+  return cudaLaunchKernelEx(&cfg, gemm_pair_kernel<BN, STAGES, B_MN, Epi, TAIL>, mA, mB, mBh, M, N, K, ksplit, epi,
+                            status, ctl);
 }
 
 cudaError_t launch_debug_gemm(const void* A, const void* Bm, float* D, int M, int N, int K,
@@ -767,11 +798,11 @@ cudaError_t launch_debug_gemm(const void* A, const void* Bm, float* D, int M, in
   }
   if (b_mn_major == 3) {  // CTA-pair engine, B [N][K]
     if (!tmap_kmajor(&mB, Bm, N, K, 128)) return cudaErrorInvalidValue;
-    return run_gemm_pair<256, 6, false>(mA, mB, M, N, K, 1, epi, status, ctl, st);
+    return run_gemm_pair<256, 6, false>(mA, mB, mB, M, N, K, 1, epi, status, ctl, st);
   }
   if (!tmap_mnmajor(&mB, Bm, K, N)) return cudaErrorInvalidValue;
   if (b_mn_major == 4) {  // CTA-pair engine, B [K][N]
-    return run_gemm_pair<256, 6, true>(mA, mB, M, N, K, 1, epi, status, ctl, st);
+    return run_gemm_pair<256, 6, true>(mA, mB, mB, M, N, K, 1, epi, status, ctl, st);
   }
   // 1: LBO = distance between 64-column blocks along N, SBO = between 8-row
   // groups along K (the layout the self-conditioning kernel uses); 2: swapped.
@@ -948,12 +979,13 @@ cudaError_t launch_qkv(const void* a, const void* Wq, const void* Wk, const void
 }
 
 cudaError_t launch_lmhead(const LmArgs& a, StopCtl ctl, int* status, cudaStream_t st) {
-  CUtensorMap mA, mB;  // B boxes: half a vocabulary tile (one CTA of a pair)
-  if (!tmap_kmajor(&mA, a.h, a.M, a.d, kBM) || !tmap_kmajor(&mB, a.E, a.V, a.d, kLmBN / 2))
+  CUtensorMap mA, mB, mBh;  // B boxes: half a vocabulary tile (one CTA of a pair), or half of a half tile
+  if (!tmap_kmajor(&mA, a.h, a.M, a.d, kBM) || !tmap_kmajor(&mB, a.E, a.V, a.d, kLmBN / 2) ||
+      !tmap_kmajor(&mBh, a.E, a.V, a.d, kLmBN / 4))
     return cudaErrorInvalidValue;
   EpiLM epi{a.alpha, a.coef2, a.inv_sqrt_d, reinterpret_cast<__nv_bfloat16*>(a.pt), a.pm, a.pl,
             a.pS, a.pvmax, a.pidx, a.logits, a.M, a.V};
-  return run_gemm_pair<kLmBN, 6, false>(mA, mB, a.M, a.V, a.d, 1, epi, status, ctl, st);
+  return run_gemm_pair<kLmBN, 6, false, EpiLM, true>(mA, mB, mBh, a.M, a.V, a.d, 1, epi, status, ctl, st);
 }
 
 // ====================================================== self-conditioning
@@ -976,7 +1008,7 @@ cudaError_t launch_selfcond(const ScArgs& a, StopCtl ctl, int* status, cudaStrea
   if (!tmap_kmajor(&mP, a.pt, a.M, a.V, kBM) || !tmap_mnmajor(&mE, a.E, a.V, a.d))
     return cudaErrorInvalidValue;
   EpiPartial ep{a.upart, a.M, a.d};
-  return run_gemm_pair<kScBN, 6, true>(mP, mE, a.M, a.d, a.V, a.nsplit, ep, status, ctl, st);
+  return run_gemm_pair<kScBN, 6, true>(mP, mE, mE, a.M, a.d, a.V, a.nsplit, ep, status, ctl, st);
 }
 
 }  // namespace dg

@@ -91,7 +91,7 @@ dg_status enqueue_step(const StepCtx& c, float tau, float b, float stop_H, uint6
   const dg_dims& D = c.model->dims;
   const WsLayout& L = c.L;
   void* ws = c.ws;
-  const int M = D.B * D.C, NT = cdiv(D.V, kLmBN), P = c.cache->len;
+  const int M = D.B * D.C, NT = cdiv(D.V, kStatCols), P = c.cache->len;
   int* status = at<int>(ws, L.status);
   int* stop_at = at<int>(ws, L.stop_at);
   StopCtl ctl{stop_at, D.B, step};
@@ -140,7 +140,7 @@ dg_status enqueue_step(const StepCtx& c, float tau, float b, float stop_H, uint6
   DG_TRY(pf.mark(DG_PROF_LMHEAD, 1));
   StatsArgs sa{at<float>(ws, L.pm), at<float>(ws, L.pl), at<float>(ws, L.pS), at<float>(ws, L.pvmax),
                at<int>(ws, L.pidx), NT, M, at<double>(ws, L.Hd), at<float>(ws, L.lsum),
-               at<float>(ws, L.fscale), at<int>(ws, L.amax), out ? out->entropy : nullptr,
+               at<float>(ws, L.rowmax), at<int>(ws, L.amax), out ? out->entropy : nullptr,
                out ? out->argmax : nullptr};
   DG_TRY(pf.mark(DG_PROF_STATS, 0));
   DG_TRY(launch_stats(sa, ctl, c.st));
@@ -171,7 +171,8 @@ dg_status enqueue_step(const StepCtx& c, float tau, float b, float stop_H, uint6
   DG_TRY(pf.mark(DG_PROF_SAMPLER, 1));
   P0Args p0{};
   p0.pt = at<void>(ws, L.pt);
-  p0.fscale = at<float>(ws, L.fscale);
+  p0.pm = at<float>(ws, L.pm);
+  p0.rowmax = at<float>(ws, L.rowmax);
   p0.lsum = at<float>(ws, L.lsum);
   p0.acc = at<uint8_t>(ws, L.acc);
   p0.gbest = at<float>(ws, L.gbest);
@@ -257,7 +258,7 @@ int selfcond_splits(const dg_dims& D) {
 
 bool ws_layout(const dg_dims& D, int32_t cap, WsLayout* L) {
   if (cap < 0) return false;
-  const size_t M = (size_t)D.B * D.C, NT = (size_t)cdiv(D.V, kLmBN);
+  const size_t M = (size_t)D.B * D.C, NT = (size_t)cdiv(D.V, kStatCols);
   // room for the largest split count any prefix length up to cap can use
   const int ns_attn = attn_max_splits(D, cap + D.C);
   const size_t S = (size_t)selfcond_splits(D);
@@ -286,7 +287,7 @@ bool ws_layout(const dg_dims& D, int32_t cap, WsLayout* L) {
   L->pidx = take(4 * NT * M);
   L->Hd = take(8 * M);
   L->lsum = take(4 * M);
-  L->fscale = take(4 * NT * M);
+  L->rowmax = take(4 * M);
   L->amax = take(4 * M);
   L->acc = take(M);
   L->upart = take(4 * S * M * D.d);

@@ -14,6 +14,7 @@ namespace dg {
 // 152 SMs of a GB300).  Kernels are correct for any SM count.
 constexpr int kTargetCtas = 152;
 constexpr int kLmBN = 256;     // vocabulary columns per LM-head tile
+constexpr int kStatCols = 128; // vocabulary columns per softmax-statistics group
 constexpr int kScBN = 256;     // model columns per self-conditioning tile
 constexpr int kAttnRows = 64;  // query rows per attention CTA
 constexpr int kAttnKeys = 64;  // keys per attention block
@@ -37,7 +38,7 @@ struct WsLayout {
   size_t attn_o, attn_ml;
   size_t pt;
   size_t pm, pl, pS, pvmax, pidx;
-  size_t Hd, lsum, fscale, amax, acc;
+  size_t Hd, lsum, rowmax, amax, acc;
   size_t upart, gbest, gidx;
   size_t gpart, gpart_elems;  // split-K partials of the small GEMMs
   size_t u, g;
@@ -135,7 +136,8 @@ int selfcond_active_splits(const dg_dims& D);
 constexpr int kGumbelChunk = 8192;
 struct P0Args {
   void* pt;              // bf16 [M][V]: exp(s - m_tile) in, p0 out
-  const float* fscale;   // [M][NT]
+  const float* pm;       // [M][NT]  group maxima m_g (log2 units)
+  const float* rowmax;   // [M]  row maximum m (log2 units)
   const float* lsum;     // [M]  Z
   const uint8_t* acc;    // [M]
   float* gbest;          // [NC][M]
@@ -171,8 +173,8 @@ struct StatsArgs {
   const int* pidx;
   int NT, M;
   double* Hd;            // [M]
-  float* lsum;           // [M]
-  float* fscale;         // [M][NT]
+  float* lsum;           // [M]  Z
+  float* rowmax;         // [M]  m (log2 units)
   int* amax;             // [M]
   float* entropy;        // optional out [M]
   int* argmax_out;       // optional out [M]

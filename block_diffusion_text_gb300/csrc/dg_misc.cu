@@ -92,14 +92,44 @@ cudaError_t launch_embed_rmsnorm(const int32_t* tokens, const void* E, const voi
 }
 
 // ------------------------------------------------------- tile statistics --
-// Merge of the per-tile (max, sum, weighted sum, argmax) of each row into the
-// tempered-softmax entropy H = ln Z - S / Z, the argmax, Z, and the factors
-// exp(m_t - m) / Z that turn a stored tile exp(s - m_t) into p0.  The tile
-// statistics are laid out [row][tile]; each row is taken by `wpr` warps of a
-// CTA (all eight for long rows, one for short ones), which read it with
-// coalesced loads.  Tile weights in float, sums in double.
+// Merge of the per-group (max, sum, weighted sum, argmax) of each row into the
+// tempered-softmax entropy H = ln Z - S / Z, the argmax, the row maximum m and
+// Z (a stored group exp(s - m_g) becomes p0 with the factor exp(m_g - m) / Z).
+// The group statistics are laid out [row][group]; each row is taken by `wpr`
+// warps of a CTA (all eight for long rows, one for short ones), which read it
+// once with coalesced loads, merging online: running maximum R, with
+// L = sum 2^(m_g - R) l_g and Q = sum 2^(m_g - R) (S_g + l_g (m_g - R)),
+// rescaled when R grows.  Sums in fp32 (two accumulators per thread); the
+// entropy is formed in double.
 constexpr int kStatsThreads = 256;
 constexpr int kStatsWarps = kStatsThreads / 32;
+
+struct RowSum {
+  float R, L, Q;
+};
+DG_DEV RowSum merge_rowsum(RowSum a, RowSum b) {
+  if (b.L == 0.f) return a;
+  if (a.L == 0.f) return b;
+  const float R = fmaxf(a.R, b.R);
+  const float da = a.R - R, db = b.R - R;
+  const float wa = exp2f(da), wb = exp2f(db);
+  return {R, wa * a.L + wb * b.L, wa * fmaf(da, a.L, a.Q) + wb * fmaf(db, b.L, b.Q)};
+}
+DG_DEV void add_group(RowSum& acc, float mt, float lt, float St) {
+  if (mt > acc.R) {  // the running maximum grows: rescale what was summed
+    if (acc.L != 0.f) {
+      const float d = acc.R - mt;
+      const float w = exp2f(d);
+      acc.Q = w * fmaf(d, acc.L, acc.Q);
+      acc.L *= w;
+    }
+    acc.R = mt;
+  }
+  const float dm = mt - acc.R;
+  const float w = exp2f(dm);
+  acc.L = fmaf(w, lt, acc.L);
+  acc.Q = fmaf(w, fmaf(lt, dm, St), acc.Q);
+}
 
 // Reduction over the wpr warps of each row (warps r*wpr .. r*wpr + wpr - 1).
 template <class T, class Op>
@@ -115,6 +145,10 @@ DG_DEV T rows_reduce(T v, Op op, T* sh, int wpr) {
   __syncthreads();
   return r;
 }
+DG_DEV RowSum shfl_rowsum(RowSum v, int o) {
+  return {__shfl_xor_sync(0xffffffffu, v.R, o), __shfl_xor_sync(0xffffffffu, v.L, o),
+          __shfl_xor_sync(0xffffffffu, v.Q, o)};
+}
 
 __global__ void __launch_bounds__(kStatsThreads) stats_kernel(StatsArgs a, int wpr, StopCtl ctl) {
   pdl_wait();
@@ -125,55 +159,58 @@ __global__ void __launch_bounds__(kStatsThreads) stats_kernel(StatsArgs a, int w
   const int t0 = (warp % wpr) * 32 + threadIdx.x % 32, tstep = wpr * 32;
   const size_t base = (size_t)(ok ? row : 0) * a.NT;
   __shared__ float shf[kStatsWarps];
-  __shared__ double shd[kStatsWarps];
   __shared__ int shi[kStatsWarps];
-  float mx = -FLT_MAX, vbest = -FLT_MAX;
+  __shared__ RowSum shr[kStatsWarps];
+  RowSum acc{-FLT_MAX, 0.f, 0.f}, acc2{-FLT_MAX, 0.f, 0.f};
+  float vbest = -FLT_MAX;
   int ibest = INT_MAX;
   if (ok) {
-#pragma unroll 4
-    for (int t = t0; t < a.NT; t += tstep) {
-      mx = fmaxf(mx, a.pm[base + t]);
-      const float v = a.pvmax[base + t];
-      const int i = a.pidx[base + t];
-      if (v > vbest || (v == vbest && i < ibest)) {
-        vbest = v;
-        ibest = i;
+#pragma unroll 2
+    for (int t = t0; t < a.NT; t += 2 * tstep) {
+      const int t2 = t + tstep;
+      const bool has2 = t2 < a.NT;
+      const float m1 = a.pm[base + t], l1 = a.pl[base + t], S1 = a.pS[base + t], v1 = a.pvmax[base + t];
+      const int i1 = a.pidx[base + t];
+      const float m2 = has2 ? a.pm[base + t2] : -FLT_MAX, l2 = has2 ? a.pl[base + t2] : 0.f;
+      const float S2 = has2 ? a.pS[base + t2] : 0.f, v2 = has2 ? a.pvmax[base + t2] : -FLT_MAX;
+      const int i2 = has2 ? a.pidx[base + t2] : INT_MAX;
+      if (v1 > vbest || (v1 == vbest && i1 < ibest)) {
+        vbest = v1;
+        ibest = i1;
       }
+      if (v2 > vbest || (v2 == vbest && i2 < ibest)) {
+        vbest = v2;
+        ibest = i2;
+      }
+      add_group(acc, m1, l1, S1);
+      if (has2) add_group(acc2, m2, l2, S2);
     }
   }
-  const float M2 = rows_reduce(mx, [](float x, float y) { return fmaxf(x, y); }, shf, wpr);
-  // argmax: the largest value, lowest index among the threads that hold it
+  acc = merge_rowsum(acc, acc2);
+  // per row: the merged sums, and the argmax (largest value, lowest index)
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc = merge_rowsum(acc, shfl_rowsum(acc, o));
+  if (threadIdx.x % 32 == 0) shr[warp] = acc;
+  __syncthreads();
+  const int w0 = warp / wpr * wpr;
+  RowSum tot = shr[w0];
+  for (int w = 1; w < wpr; ++w) tot = merge_rowsum(tot, shr[w0 + w]);
   const float vrow = rows_reduce(vbest, [](float x, float y) { return fmaxf(x, y); }, shf, wpr);
   const int irow =
       rows_reduce(vbest == vrow ? ibest : INT_MAX, [](int x, int y) { return x < y ? x : y; }, shi, wpr);
-  double l = 0.0, S = 0.0;
-  if (ok) {
-#pragma unroll 4
-    for (int t = t0; t < a.NT; t += tstep) {
-      const float dm = a.pm[base + t] - M2;
-      const double w = (double)exp2f(dm);
-      const double pl = (double)a.pl[base + t];
-      l += w * pl;
-      S += w * ((double)a.pS[base + t] + pl * (double)dm);
-    }
-  }
-  const double Z = rows_reduce(l, [](double x, double y) { return x + y; }, shd, wpr);
-  const double St = rows_reduce(S, [](double x, double y) { return x + y; }, shd, wpr);
-  if (!ok) return;
-  const float invZ = (float)(1.0 / Z);
-  for (int t = t0; t < a.NT; t += tstep) a.fscale[base + t] = exp2f(a.pm[base + t] - M2) * invZ;
-  if (t0 == 0) {
-    const double H = log(Z) - 0.69314718055994531 * St / Z;
-    a.Hd[row] = H;
-    a.lsum[row] = (float)Z;
-    a.amax[row] = irow;
-    if (a.entropy) a.entropy[row] = (float)H;
-    if (a.argmax_out) a.argmax_out[row] = irow;
-  }
+  if (!ok || t0 != 0) return;
+  const double Z = (double)tot.L;
+  const double H = log(Z) - 0.69314718055994531 * (double)tot.Q / Z;
+  a.Hd[row] = H;
+  a.lsum[row] = (float)Z;
+  a.rowmax[row] = tot.R;
+  a.amax[row] = irow;
+  if (a.entropy) a.entropy[row] = (float)H;
+  if (a.argmax_out) a.argmax_out[row] = irow;
 }
 
 cudaError_t launch_stats(const StatsArgs& a, StopCtl ctl, cudaStream_t st) {
-  // warps per row: about 4 tiles per thread, one to eight warps
+  // warps per row: about 4 groups per thread, one to eight warps
   int wpr = 1;
   while (wpr < kStatsWarps && wpr * 32 * 4 < a.NT) wpr *= 2;
   const int rows_per_cta = kStatsWarps / wpr;
@@ -210,11 +247,12 @@ __global__ void __launch_bounds__(kP0Threads) p0_gumbel_kernel(P0Args a, StopCtl
   float best = -FLT_MAX;
   int bidx = INT_MAX;
   // Each warp takes 1024 contiguous entries (2 KB); load q of lane l is the
-  // 16-byte chunk q * 32 + l, so a warp's load covers 512 contiguous bytes and
-  // all 32 chunks of a load lie in one 256-column tile (one scale factor).
+  // 16-byte chunk q * 32 + l, so a warp's load covers 512 contiguous bytes
+  // (two statistics groups of 128 columns, one scale factor each).
   const int wbase = chunk * kGumbelChunk + (threadIdx.x / 32) * 1024;
   const int lane = threadIdx.x % 32;
-  const size_t fbase = (size_t)row * ((a.V + kLmBN - 1) / kLmBN);
+  const size_t fbase = (size_t)row * ((a.V + kStatCols - 1) / kStatCols);
+  const float mrow = a.rowmax[row], invZ = 1.0f / a.lsum[row];
   uint4 x[4];
   float f[4];
 #pragma unroll
@@ -222,9 +260,11 @@ __global__ void __launch_bounds__(kP0Threads) p0_gumbel_kernel(P0Args a, StopCtl
     const int v = wbase + (q * 32 + lane) * 8;
     if (v < a.V) {  // V is a multiple of 8
       x[q] = *reinterpret_cast<const uint4*>(pt + v);
-      f[q] = a.fscale[fbase + (wbase + q * 256) / kLmBN];
+      f[q] = a.pm[fbase + v / kStatCols];
     }
   }
+#pragma unroll
+  for (int q = 0; q < 4; ++q) f[q] = exp2f(f[q] - mrow) * invZ;  // exp(m_g - m) / Z
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     const int vq = wbase + (q * 32 + lane) * 8;
