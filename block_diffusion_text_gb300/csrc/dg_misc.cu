@@ -5,6 +5,8 @@
 #include <cfloat>
 #include <climits>
 
+#include <cmath>
+
 #include "dg_common.cuh"
 #include "dg_internal.h"
 
@@ -18,10 +20,15 @@ namespace dg {
 constexpr int kEmbThreads = 256;
 constexpr int kEmbMaxChunks = 8;  // d <= 8 * 8 * 256
 
+// RoPE frequencies theta_j = base^(-2j / hd), computed on the host in double.
+struct RopeTheta {
+  double th[64];  // hd / 2 <= 64
+};
+
 __global__ void __launch_bounds__(kEmbThreads)
     embed_rmsnorm_kernel(const int32_t* tokens, const __nv_bfloat16* E, const __nv_bfloat16* z,
                          __nv_bfloat16* a, float2* rope, int d, float eps, int C, int P, int hd,
-                         float rope_base, StopCtl ctl) {
+                         RopeTheta theta, StopCtl ctl) {
   pdl_wait();
   if (all_stopped(ctl.stop_at, ctl.B, ctl.step)) return;
   const int row = blockIdx.x;
@@ -73,12 +80,15 @@ __global__ void __launch_bounds__(kEmbThreads)
     }
   }
   if (rope && row < C) {
+    // angle (P + i) theta_j reduced modulo 2 pi in double (a few operations on
+    // the slow FP64 units), then sine and cosine in float of |r| <= pi
     for (int j = threadIdx.x; j < hd / 2; j += kEmbThreads) {
-      const double theta = pow((double)rope_base, -2.0 * j / hd);
-      const double ang = (double)(P + row) * theta;
-      double sn, cs;
-      sincos(ang, &sn, &cs);
-      rope[(size_t)row * (hd / 2) + j] = make_float2((float)cs, (float)sn);
+      const double ang = (double)(P + row) * theta.th[j];
+      const double k = rint(ang * 0.15915494309189535);  // 1 / (2 pi)
+      const double r = fma(-k, 6.283185307179586, ang);
+      float sn, cs;
+      sincosf((float)r, &sn, &cs);
+      rope[(size_t)row * (hd / 2) + j] = make_float2(cs, sn);
     }
   }
 }
@@ -86,9 +96,11 @@ __global__ void __launch_bounds__(kEmbThreads)
 cudaError_t launch_embed_rmsnorm(const int32_t* tokens, const void* E, const void* z, void* a,
                                  float2* rope, const dg_dims& D, int rows, int P, StopCtl ctl,
                                  cudaStream_t st) {
+  RopeTheta th{};
+  for (int j = 0; j < D.hd / 2 && j < 64; ++j) th.th[j] = std::pow((double)D.rope_base, -2.0 * j / D.hd);
   return launch_pdl(embed_rmsnorm_kernel, dim3(rows), dim3(kEmbThreads), 0, st, tokens,
                     reinterpret_cast<const __nv_bfloat16*>(E), reinterpret_cast<const __nv_bfloat16*>(z),
-                    reinterpret_cast<__nv_bfloat16*>(a), rope, D.d, D.rms_eps, D.C, P, D.hd, D.rope_base, ctl);
+                    reinterpret_cast<__nv_bfloat16*>(a), rope, D.d, D.rms_eps, D.C, P, D.hd, th, ctl);
 }
 
 // ------------------------------------------------------- tile statistics --
@@ -343,7 +355,15 @@ cudaError_t launch_p0_gumbel(const P0Args& a, StopCtl ctl, cudaStream_t st) {
 // position is renoised to a uniform random token (Philox stream 1).  Also the
 // mean entropy, the accepted count and the adaptive-stop test of step 4
 // (mean entropy <= stop_H and the argmax equal to the previous step's).
-// One CTA per canvas, one thread per (padded) position.
+// One CTA per canvas, one thread per (padded) position.  The sort is by rank:
+// each position counts the positions ordered before it (entropy as an
+// order-preserving integer key, ties by position), then the entropies are
+// placed in rank order and summed with a warp-shuffle scan.
+DG_DEV uint64_t order_key(double h) {
+  const uint64_t b = (uint64_t)__double_as_longlong(h);
+  return (b >> 63) ? ~b : (b | 0x8000000000000000ull);  // unsigned order = numeric order
+}
+
 __global__ void __launch_bounds__(1024) sampler_kernel(SamplerArgs a, int npow2) {
   pdl_wait();
   const int b = blockIdx.x;
@@ -351,46 +371,56 @@ __global__ void __launch_bounds__(1024) sampler_kernel(SamplerArgs a, int npow2)
   const bool active = a.stop_at[b] >= a.step;
   // Every canvas skips its work once it has stopped.
   if (!active) return;
-  __shared__ double key[1024];
+  __shared__ uint64_t key[1024];
   __shared__ int idx[1024];
   __shared__ double cum[1024];
+  __shared__ double wsum[32];
   __shared__ int flags[2];
   const int base = b * a.C;
-  key[i] = i < a.C ? a.Hd[base + i] : DBL_MAX;
-  idx[i] = i;
+  const double h = i < a.C ? a.Hd[base + i] : 0.0;
+  const uint64_t ki = order_key(h);
+  if (i < a.C) key[i] = ki;
   if (i == 0) {
     flags[0] = 0;  // accepted count
     flags[1] = 1;  // argmax unchanged everywhere
   }
   __syncthreads();
-  // Bitonic sort of (key, idx) ascending.
-  for (int k = 2; k <= npow2; k <<= 1) {
-    for (int j = k >> 1; j > 0; j >>= 1) {
-      const int p = i ^ j;
-      if (p > i) {
-        const bool up = (i & k) == 0;
-        const double ki = key[i], kp = key[p];
-        const int ii = idx[i], ip = idx[p];
-        const bool gt = (ki > kp) || (ki == kp && ii > ip);
-        if (gt == up) {
-          key[i] = kp;
-          key[p] = ki;
-          idx[i] = ip;
-          idx[p] = ii;
-        }
-      }
-      __syncthreads();
+  // rank of position i in (entropy, position) order
+  int rank = 0;
+  if (i < a.C) {
+#pragma unroll 8
+    for (int j = 0; j < a.C; ++j) {
+      const uint64_t kj = key[j];
+      rank += (kj < ki || (kj == ki && j < i)) ? 1 : 0;
     }
+    idx[rank] = i;
+    cum[rank] = h;
   }
-  // Inclusive prefix sum of the sorted entropies (double), Hillis-Steele.
-  cum[i] = i < a.C ? key[i] : 0.0;
   __syncthreads();
-  for (int off = 1; off < npow2; off <<= 1) {
-    const double v = i >= off ? cum[i - off] : 0.0;
-    __syncthreads();
-    cum[i] += v;
-    __syncthreads();
+  // inclusive prefix sum of the sorted entropies (double): warp scan, then
+  // the warps' totals
+  double v = i < a.C ? cum[i] : 0.0;
+  const int lane = i & 31, w = i >> 5;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const double u = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += u;
   }
+  if (lane == 31) wsum[w] = v;
+  __syncthreads();
+  if (w == 0) {
+    double t = lane < (npow2 + 31) / 32 ? wsum[lane] : 0.0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const double u = __shfl_up_sync(0xffffffffu, t, o);
+      if (lane >= o) t += u;
+    }
+    wsum[lane] = t;  // inclusive totals of warps 0..lane
+  }
+  __syncthreads();
+  if (w > 0) v += wsum[w - 1];
+  if (i < a.C) cum[i] = v;
+  __syncthreads();
   if (i < a.C) {
     const int pos = idx[i];
     const bool acc = cum[i] <= (double)a.b;
@@ -398,9 +428,9 @@ __global__ void __launch_bounds__(1024) sampler_kernel(SamplerArgs a, int npow2)
     if (a.acc_out) a.acc_out[base + pos] = acc ? 1 : 0;
     if (acc) atomicAdd(&flags[0], 1);
     if (!acc) {
-      uint64_t w[4];
-      philox_block(w, a.seed, a.block, a.step, b, pos, 0, 1);
-      a.tokens[base + pos] = uniform_token(w[0], a.V);
+      uint64_t pw[4];
+      philox_block(pw, a.seed, a.block, a.step, b, pos, 0, 1);
+      a.tokens[base + pos] = uniform_token(pw[0], a.V);
     }
     const int am = a.amax[base + i];
     if (a.step < 1 || a.prev_argmax[base + i] != am) atomicAnd(&flags[1], 0);
