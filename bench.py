@@ -364,32 +364,34 @@ def run_ours(args, world, rank, local):
     max_ms = _max_over_ranks(elapsed_ms, world)
     value = world * args.steps / (max_ms / 1e3)
 
-    # end to end through the public API with host buffers
+    # end to end through the public API with host buffers: the step's inputs
+    # (tokens, z, alpha) go up from pinned host memory and its results (tokens,
+    # z, entropy, accept mask) come back, each as one contiguous copy; two host
+    # buffers alternate, so a step's results are the next step's inputs.
     e2e = None
     if not args.no_e2e:
-        hx = x0.cpu().pin_memory()
-        hz = z0.cpu().pin_memory()
-        ha = a.cpu().pin_memory()
-        ox = torch.empty_like(hx).pin_memory()
-        oz = torch.empty_like(hz).pin_memory()
-        oh = torch.empty(dims.B, dims.C, dtype=torch.float32).pin_memory()
-        oa = torch.empty(dims.B, dims.C, dtype=torch.uint8).pin_memory()
-        h2d = hx.numel() * 4 + hz.numel() * 2 + ha.numel() * 4
-        d2h = ox.numel() * 4 + oz.numel() * 2 + oh.numel() * 4 + oa.numel()
+        io_dev, io_host, views = _e2e_buffers(dims, dev)
+        tok_d, z_d, a_d, ent_d, acc_d = views(io_dev)
+        tok_d.copy_(x0)
+        z_d.copy_(z0)
+        a_d.copy_(a)
+        io_host[0].copy_(io_dev)
+        io_host[1].copy_(io_dev)
+        e_canvas = dg.Canvas(tok_d, z_d, a_d)
+        e_out = dict(entropy=ent_d, accept=acc_d, argmax=torch.empty_like(tok_d),
+                     n_acc=torch.empty(dims.B, dtype=torch.int32, device=dev),
+                     mean_H=torch.empty(dims.B, dtype=torch.float32, device=dev),
+                     stop=torch.empty(dims.B, dtype=torch.int32, device=dev))
+        n_in = _e2e_input_bytes(dims)
+        h2d, d2h = n_in, io_dev.numel()
         ksteps = min(args.steps, 50)
 
         def e2e_step(s):
-            canvas.tokens.copy_(hx, non_blocking=True)
-            canvas.z.copy_(hz, non_blocking=True)
-            canvas.alpha.copy_(ha, non_blocking=True)
-            out = dg.denoise_step(model, canvas, tau=taus[s % 48], b=0.1, seed=seed, step=s % 48, out=outbuf)
-            ox.copy_(canvas.tokens, non_blocking=True)
-            oz.copy_(canvas.z, non_blocking=True)
-            oh.copy_(out["entropy"], non_blocking=True)
-            oa.copy_(out["accept"], non_blocking=True)
+            src, dst = io_host[s % 2], io_host[(s + 1) % 2]
+            io_dev[:n_in].copy_(src[:n_in], non_blocking=True)
+            dg.denoise_step(model, e_canvas, tau=taus[s % 48], b=0.1, seed=seed, step=s % 48, out=e_out)
+            dst.copy_(io_dev, non_blocking=True)
             torch.cuda.current_stream().synchronize()
-            hx.copy_(ox)
-            hz.copy_(oz)
 
         for s in range(3):
             e2e_step(s)
@@ -460,6 +462,36 @@ def run_ours(args, world, rank, local):
                                     "sample": f"failed: {e!r}"}
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+def _e2e_offsets(dims):
+    """Byte offsets of tokens, z, alpha, entropy, accept in the e2e I/O block (256-byte aligned)."""
+    M = dims.B * dims.C
+    sizes = (4 * M, 2 * M * dims.d, 4 * M, 4 * M, M)
+    offs, o = [], 0
+    for n in sizes:
+        offs.append(o)
+        o = (o + n + 255) // 256 * 256
+    return offs, sizes, o
+
+
+def _e2e_input_bytes(dims):
+    offs, sizes, _ = _e2e_offsets(dims)
+    return offs[2] + sizes[2]  # tokens, z, alpha
+
+
+def _e2e_buffers(dims, dev):
+    offs, sizes, total = _e2e_offsets(dims)
+    io_dev = torch.zeros(total, dtype=torch.uint8, device=dev)
+    io_host = [torch.zeros(total, dtype=torch.uint8).pin_memory() for _ in range(2)]
+    M = dims.B * dims.C
+
+    def views(buf):
+        v = lambda k, dt: buf[offs[k]:offs[k] + sizes[k]].view(dt)
+        return (v(0, torch.int32).view(dims.B, dims.C), v(1, torch.bfloat16).view(dims.B, dims.C, dims.d),
+                v(2, torch.float32).view(dims.B, dims.C), v(3, torch.float32).view(dims.B, dims.C),
+                v(4, torch.uint8).view(dims.B, dims.C))
+    return io_dev, io_host, views
 
 
 def _kernel_nodes(graph):

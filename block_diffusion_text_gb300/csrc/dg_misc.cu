@@ -463,24 +463,45 @@ __global__ void __launch_bounds__(256) reduce_kernel(ReduceArgs a, StopCtl ctl) 
   const int row = blockIdx.x;
   const int n4 = a.d / 4;
   const size_t sstride = (size_t)a.M * a.d;
+  const float* src = a.upart + (size_t)row * a.d;
   for (int c = threadIdx.x; c < n4; c += blockDim.x) {
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int s = 0; s < a.nsplit; ++s) {
-      const float4 v = *reinterpret_cast<const float4*>(a.upart + s * sstride + (size_t)row * a.d + 4 * c);
-      acc.x += v.x;
-      acc.y += v.y;
-      acc.z += v.z;
-      acc.w += v.w;
+    // four splits at a time: independent loads in flight
+    float4 acc[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+    int s = 0;
+    for (; s + 4 <= a.nsplit; s += 4) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float4 v = *reinterpret_cast<const float4*>(src + (s + k) * sstride + 4 * c);
+        acc[k].x += v.x;
+        acc[k].y += v.y;
+        acc[k].z += v.z;
+        acc[k].w += v.w;
+      }
     }
+    for (; s < a.nsplit; ++s) {
+      const float4 v = *reinterpret_cast<const float4*>(src + s * sstride + 4 * c);
+      acc[0].x += v.x;
+      acc[0].y += v.y;
+      acc[0].z += v.z;
+      acc[0].w += v.w;
+    }
+    const float x = (acc[0].x + acc[1].x) + (acc[2].x + acc[3].x);
+    const float y = (acc[0].y + acc[1].y) + (acc[2].y + acc[3].y);
+    const float z = (acc[0].z + acc[1].z) + (acc[2].z + acc[3].z);
+    const float t = (acc[0].w + acc[1].w) + (acc[2].w + acc[3].w);
     uint2 w;
-    w.x = pack_bf16(acc.x, acc.y);
-    w.y = pack_bf16(acc.z, acc.w);
+    w.x = pack_bf16(x, y);
+    w.y = pack_bf16(z, t);
     *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(a.u) + (size_t)row * a.d + 4 * c) = w;
   }
-  if (threadIdx.x == 0 && a.acc[row] && canvas_active(ctl.stop_at, row / a.C, ctl.step)) {
+  // sampled token of an accepted row: the best (score, lowest index) over the
+  // chunks, one warp
+  if (threadIdx.x < 32 && a.acc[row] && canvas_active(ctl.stop_at, row / a.C, ctl.step)) {
     float best = -FLT_MAX;
     int bi = INT_MAX;
-    for (int s = 0; s < a.nchunks; ++s) {
+    for (int s = threadIdx.x; s < a.nchunks; s += 32) {
       const float v = a.gbest[(size_t)s * a.M + row];
       const int i = a.gidx[(size_t)s * a.M + row];
       if (v > best || (v == best && i < bi)) {
@@ -488,7 +509,16 @@ __global__ void __launch_bounds__(256) reduce_kernel(ReduceArgs a, StopCtl ctl) 
         bi = i;
       }
     }
-    a.tokens[row] = bi;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float b2 = __shfl_xor_sync(0xffffffffu, best, o);
+      const int i2 = __shfl_xor_sync(0xffffffffu, bi, o);
+      if (b2 > best || (b2 == best && i2 < bi)) {
+        best = b2;
+        bi = i2;
+      }
+    }
+    if (threadIdx.x == 0) a.tokens[row] = bi;
   }
 }
 
