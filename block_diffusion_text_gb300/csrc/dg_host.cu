@@ -428,4 +428,16 @@ dg_status dg_debug_gemm(const void* A, const void* Bm, float* D, int32_t M, int3
                                        reinterpret_cast<cudaStream_t>(stream)));
 }
 
+dg_status dg_debug_wait_timeout(int32_t* status, void* stream) {
+  if (!status) return DG_ERR_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  int* word = nullptr;
+  DG_TRY(cudaGetSymbolAddress(reinterpret_cast<void**>(&word), g_debug_status));
+  DG_TRY(cudaMemsetAsync(word, 0, sizeof(int), st));
+  DG_TRY(launch_wait_timeout(word, st));
+  DG_TRY(cudaMemcpyAsync(status, word, sizeof(int), cudaMemcpyDeviceToHost, st));
+  DG_TRY(cudaStreamSynchronize(st));
+  return DG_OK;
+}
+
 }  // extern "C"

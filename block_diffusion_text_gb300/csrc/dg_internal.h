@@ -209,6 +209,7 @@ struct ReduceArgs {
   int M, d, C, nsplit, nchunks;
 };
 cudaError_t launch_reduce(const ReduceArgs& a, StopCtl ctl, cudaStream_t st);
+cudaError_t launch_wait_timeout(int* status, cudaStream_t st);
 cudaError_t launch_canvas_init(int32_t* tokens, int B, int C, int V, uint64_t seed, int block,
                                cudaStream_t st);
 cudaError_t launch_loop_finish(const int* stop_at, int B, int N, int* steps_taken, int* converged,

@@ -526,6 +526,28 @@ cudaError_t launch_reduce(const ReduceArgs& a, StopCtl ctl, cudaStream_t st) {
   return launch_pdl(reduce_kernel, dim3(a.M), dim3(256), 0, st, a, ctl);
 }
 
+// ------------------------------------------------- bounded-wait diagnostics --
+// One thread waits on an mbarrier phase that nothing completes.  The bounded
+// wait gives up after its limit, records DG_ERR_TIMEOUT in *status and the
+// kernel returns: the path every pipeline takes when a copy or MMA it waits
+// for never lands.
+__global__ void wait_timeout_kernel(int* status) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) mbar_wait(&bar, 0, status, &abort_flag);
+}
+
+cudaError_t launch_wait_timeout(int* status, cudaStream_t st) {
+  wait_timeout_kernel<<<1, 32, 0, st>>>(status);
+  return cudaGetLastError();
+}
+
 // ------------------------------------------------------- canvas + loop ----
 __global__ void canvas_init_kernel(int32_t* tokens, int B, int C, int V, uint64_t seed, int block) {
   pdl_wait();

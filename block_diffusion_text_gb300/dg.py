@@ -26,7 +26,7 @@ DG_OK, DG_ERR_ARG, DG_ERR_SHAPE, DG_ERR_CAPACITY, DG_ERR_WORKSPACE, DG_ERR_CUDA,
 # Every function the C header declares (checked by the tests).
 EXPORTS = ("dg_status_string", "dg_workspace_size", "dg_read_status", "dg_canvas_init",
            "dg_denoise_step", "dg_denoise_canvas", "dg_commit_block", "dg_debug_gemm",
-           "dg_attention_noalloc")
+           "dg_attention_noalloc", "dg_debug_wait_timeout")
 
 
 class DgError(RuntimeError):
@@ -103,6 +103,7 @@ def load():
                                             ct.POINTER(dg_canvas_result), ct.c_void_p]
             L.dg_commit_block.argtypes = [ct.POINTER(dg_model), ct.POINTER(dg_kv_cache), ct.c_void_p,
                                           ct.c_void_p, ct.c_size_t, ct.c_void_p]
+            L.dg_debug_wait_timeout.argtypes = [ct.POINTER(ct.c_int32), ct.c_void_p]
             L.dg_debug_gemm.argtypes = [ct.c_void_p, ct.c_void_p, ct.c_void_p, ct.c_int32, ct.c_int32,
                                         ct.c_int32, ct.c_int32, ct.c_void_p]
             L.dg_attention_noalloc.argtypes = [ct.c_void_p, ct.c_void_p, ct.c_void_p, ct.c_int32, ct.c_int32,
@@ -276,6 +277,13 @@ def debug_gemm(A: torch.Tensor, Bm: torch.Tensor, b_mn_major: int = 0, stream=No
     _check(load().dg_debug_gemm(_ptr(A), _ptr(Bm), _ptr(D), M, N, K, b_mn_major, _stream(stream)),
            "dg_debug_gemm")
     return D
+
+
+def debug_wait_timeout(stream=None) -> int:
+    """Run the never-satisfied bounded wait (dg_debug_wait_timeout); returns the status word it left."""
+    st = ct.c_int32(-1)
+    _check(load().dg_debug_wait_timeout(ct.byref(st), _stream(stream)), "dg_debug_wait_timeout")
+    return st.value
 
 
 def attention_noalloc(q, K, V, cache_len, k, v, o=None, stream=None) -> torch.Tensor:

@@ -257,6 +257,14 @@ DG_API dg_status dg_attention_noalloc(const void* q, const void* K, const void* 
  * b_mn_major == 3 / 4 run the same products (B [N][K] / B [K][N]) on the
  * CTA-pair engine (M = 256 MMAs over two SMs) that the LM head and the
  * self-conditioning contraction use.  K, N multiples of 8.                     */
+/* Diagnostics of the bounded device waits (not a step of the method): runs
+ * one kernel whose mbarrier wait is never satisfied.  The wait gives up after
+ * its limit (2 s), records DG_ERR_TIMEOUT in a library status word, and the
+ * kernel returns; *status receives that word (synchronises `stream`), so a
+ * caller sees DG_ERR_TIMEOUT and the context stays usable.  The tests use it
+ * to check that path without a device fault.                                  */
+DG_API dg_status dg_debug_wait_timeout(int32_t* status, void* stream);
+
 DG_API dg_status dg_debug_gemm(const void* A, const void* Bm, float* D, int32_t M, int32_t N, int32_t K,
                         int32_t b_mn_major, void* stream);
 

@@ -138,6 +138,7 @@ def test_small_entry_points_validate(dg):
     st = ct.c_int32()
     assert L.dg_read_status(None, ct.byref(st), None) == dg.DG_ERR_ARG
     assert L.dg_debug_gemm(None, None, None, 1, 8, 8, 0, None) == dg.DG_ERR_ARG
+    assert L.dg_debug_wait_timeout(None, None) == dg.DG_ERR_ARG
     assert L.dg_debug_gemm(ct.c_void_p(FAKE), ct.c_void_p(FAKE), ct.c_void_p(FAKE), 4, 12, 8, 0, None) == \
         dg.DG_ERR_SHAPE
     f = ct.c_void_p(FAKE)
