@@ -166,7 +166,11 @@ class Model:
         self.ws_ptr = ct.c_void_p(self.ws.data_ptr() + off)
 
     def cache(self) -> dg_kv_cache:
-        return dg_kv_cache(ct.c_void_p(self.K.data_ptr()), ct.c_void_p(self.V.data_ptr()), self.cap, self.len)
+        key = (self.K.data_ptr(), self.V.data_ptr(), self.cap, self.len)
+        if getattr(self, "_cache_key", None) != key:
+            self._cache_s = dg_kv_cache(ct.c_void_p(key[0]), ct.c_void_p(key[1]), self.cap, self.len)
+            self._cache_key = key
+        return self._cache_s
 
     def status(self) -> int:
         st = ct.c_int32()
@@ -186,7 +190,14 @@ class Canvas:
             self.prev_argmax = torch.zeros_like(self.tokens)
 
     def struct(self) -> dg_canvas:
-        return dg_canvas(_ptr(self.tokens), _ptr(self.z), _ptr(self.alpha), _ptr(self.prev_argmax))
+        key = (self.tokens.data_ptr(), self.z.data_ptr(), self.alpha.data_ptr(), self.prev_argmax.data_ptr())
+        if getattr(self, "_key", None) != key:
+            self._s = dg_canvas(*[ct.c_void_p(p) for p in key])
+            self._key = key
+        return self._s
+
+
+_STEP_OUT_CACHE: dict = {}
 
 
 def denoise_step(model: Model, canvas: Canvas, tau: float, b: float, seed: int, step: int, block: int = 0,
@@ -206,7 +217,14 @@ def denoise_step(model: Model, canvas: Canvas, tau: float, b: float, seed: int, 
                    n_acc=torch.empty(d.B, dtype=torch.int32, device=dev),
                    mean_H=torch.empty(d.B, dtype=torch.float32, device=dev),
                    stop=torch.empty(d.B, dtype=torch.int32, device=dev))
-    so = dg_step_out(*[_ptr(out[k]) for k in ("entropy", "argmax", "accept", "n_acc", "mean_H", "stop")])
+    keys = ("entropy", "argmax", "accept", "n_acc", "mean_H", "stop")
+    ptrs = tuple(out[k].data_ptr() for k in keys)
+    so = _STEP_OUT_CACHE.get(ptrs) if events is None and not debug else None
+    if so is None:
+        so = dg_step_out(*[ct.c_void_p(p) for p in ptrs])
+        if events is None and not debug:
+            _STEP_OUT_CACHE.clear()  # one entry: the output set of the latest plain call
+            _STEP_OUT_CACHE[ptrs] = so
     if events is not None:
         arr = (ct.c_void_p * len(events))(*[ct.c_void_p(e.cuda_event if e is not None else 0) for e in events])
         so.events = ct.cast(arr, ct.POINTER(ct.c_void_p))
