@@ -175,6 +175,7 @@ dg_status enqueue_step(const StepCtx& c, float tau, float b, float stop_H, uint6
   p0.rowmax = at<float>(ws, L.rowmax);
   p0.lsum = at<float>(ws, L.lsum);
   p0.acc = at<uint8_t>(ws, L.acc);
+  p0.amax = at<int>(ws, L.amax);
   p0.gbest = at<float>(ws, L.gbest);
   p0.gidx = at<int>(ws, L.gidx);
   p0.M = M;

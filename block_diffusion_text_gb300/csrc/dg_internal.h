@@ -140,6 +140,7 @@ struct P0Args {
   const float* rowmax;   // [M]  row maximum m (log2 units)
   const float* lsum;     // [M]  Z
   const uint8_t* acc;    // [M]
+  const int* amax;       // [M]  argmax of the logits (lowest index on ties)
   float* gbest;          // [NC][M]
   int* gidx;             // [NC][M]
   int M, V, C;

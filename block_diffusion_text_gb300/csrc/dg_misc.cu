@@ -237,13 +237,12 @@ cudaError_t launch_stats(const StatsArgs& a, StopCtl ctl, cudaStream_t st) {
 // stream 0 keyed by (seed, block, step, canvas, position, v), lowest index on
 // ties (technical report summary, step 3: accepted positions take their
 // predicted token; the Gumbel-max form of that draw is this library's
-// reading).  The argmax token's perturbed score is at least
-// log(1 / Z) - 2.81 (its p0 is 1/Z up to bf16 rounding, and G >= -2.81),
-// and the largest draw is 16.64, so entries with
-// log p0 < log(1/Z) - 2.81 - 16.64 - 0.02 can never win and skip the draw.
+// reading).  The argmax token's p0 is exactly 1/Z (its stored value is 2^0
+// and its scale factor 1/Z), so its perturbed score S_a = log(1/Z) + G_a is
+// computed first; the largest draw is 16.64, so entries with
+// log p0 < S_a - 16.64 - 0.02 can never win and skip the draw.
 // One CTA per (row, 8192-entry chunk).
 constexpr int kP0Threads = kGumbelChunk / 32;
-constexpr float kGumbelMinDraw = -2.8136f;  // -log(-log((0.5) / 2^23))
 constexpr float kGumbelMaxDraw = 16.6355f;  // -log(-log(1 - 2^-24))
 
 __global__ void __launch_bounds__(kP0Threads) p0_gumbel_kernel(P0Args a, StopCtl ctl) {
@@ -254,8 +253,7 @@ __global__ void __launch_bounds__(kP0Threads) p0_gumbel_kernel(P0Args a, StopCtl
   __nv_bfloat16* pt = reinterpret_cast<__nv_bfloat16*>(a.pt) + (size_t)row * a.V;
   const bool gum = a.acc[row] && canvas_active(ctl.stop_at, row / a.C, ctl.step);
   const int canvas = row / a.C, pos = row % a.C;
-  // p0 threshold below which no entry can win the Gumbel-max search
-  const float thr = expf(-logf(a.lsum[row]) + kGumbelMinDraw - kGumbelMaxDraw - 0.02f);
+  const float mrow = a.rowmax[row], invZ = 1.0f / a.lsum[row];
   float best = -FLT_MAX;
   int bidx = INT_MAX;
   // Each warp takes 1024 contiguous entries (2 KB); load q of lane l is the
@@ -264,7 +262,6 @@ __global__ void __launch_bounds__(kP0Threads) p0_gumbel_kernel(P0Args a, StopCtl
   const int wbase = chunk * kGumbelChunk + (threadIdx.x / 32) * 1024;
   const int lane = threadIdx.x % 32;
   const size_t fbase = (size_t)row * ((a.V + kStatCols - 1) / kStatCols);
-  const float mrow = a.rowmax[row], invZ = 1.0f / a.lsum[row];
   uint4 x[4];
   float f[4];
 #pragma unroll
@@ -277,6 +274,19 @@ __global__ void __launch_bounds__(kP0Threads) p0_gumbel_kernel(P0Args a, StopCtl
   }
 #pragma unroll
   for (int q = 0; q < 4; ++q) f[q] = exp2f(f[q] - mrow) * invZ;  // exp(m_g - m) / Z
+  // p0 threshold below which no entry can win the Gumbel-max search: the
+  // argmax token's p0 is exactly 1/Z (its stored tile value is 2^0), so its
+  // perturbed score S_a is known, and an entry beats it only if
+  // log p0 + (largest draw) >= S_a.
+  float thr = 0.f;
+  if (gum) {
+    const int va = a.amax[row];
+    uint64_t wa[4];
+    philox_block(wa, a.seed, a.block, a.step, canvas, pos, va >> 2, 0);
+    const float sa = logf(invZ) + gumbel_from_word(wa[va & 3]);
+    thr = expf(sa - kGumbelMaxDraw - 0.02f);
+  }
+
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     const int vq = wbase + (q * 32 + lane) * 8;
