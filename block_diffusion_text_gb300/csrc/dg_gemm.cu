@@ -985,7 +985,7 @@ cudaError_t launch_lmhead(const LmArgs& a, StopCtl ctl, int* status, cudaStream_
     return cudaErrorInvalidValue;
   EpiLM epi{a.alpha, a.coef2, a.inv_sqrt_d, reinterpret_cast<__nv_bfloat16*>(a.pt), a.pm, a.pl,
             a.pS, a.pvmax, a.pidx, a.logits, a.M, a.V};
-  return run_gemm_pair<kLmBN, 6, false, EpiLM, true>(mA, mB, mBh, a.M, a.V, a.d, 1, epi, status, ctl, st);
+  return run_gemm_pair<kLmBN, 7, false, EpiLM, true>(mA, mB, mBh, a.M, a.V, a.d, 1, epi, status, ctl, st);
 }
 
 // ====================================================== self-conditioning
@@ -997,7 +997,7 @@ cudaError_t launch_lmhead(const LmArgs& a, StopCtl ctl, int* status, cudaStream_
 int selfcond_active_splits(const dg_dims& D) {
   const int bound = selfcond_splits(D);
   const int tiles = cdiv(D.d, kScBN) * cdiv(D.B * D.C, 2 * kBM);
-  const int maxc = pair_clusters<kScBN, 6, true, EpiPartial>();
+  const int maxc = pair_clusters<kScBN, 7, true, EpiPartial>();
   int ns = maxc / tiles;
   if (ns > bound) ns = bound;
   return ns < 1 ? 1 : ns;
@@ -1008,7 +1008,7 @@ cudaError_t launch_selfcond(const ScArgs& a, StopCtl ctl, int* status, cudaStrea
   if (!tmap_kmajor(&mP, a.pt, a.M, a.V, kBM) || !tmap_mnmajor(&mE, a.E, a.V, a.d))
     return cudaErrorInvalidValue;
   EpiPartial ep{a.upart, a.M, a.d};
-  return run_gemm_pair<kScBN, 6, true>(mP, mE, mE, a.M, a.d, a.V, a.nsplit, ep, status, ctl, st);
+  return run_gemm_pair<kScBN, 7, true>(mP, mE, mE, a.M, a.d, a.V, a.nsplit, ep, status, ctl, st);
 }
 
 }  // namespace dg
