@@ -14,6 +14,7 @@
 namespace dg {
 
 constexpr int kStatusTimeout = 6;  // DG_ERR_TIMEOUT
+constexpr int kStatusValue = 7;    // DG_ERR_VALUE
 // Upper bound of any spin on an mbarrier (ns of %globaltimer).  A healthy
 // pipeline never waits more than microseconds; past this the kernel records
 // DG_ERR_TIMEOUT in the status word and winds down instead of hanging.

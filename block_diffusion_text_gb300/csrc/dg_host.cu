@@ -101,7 +101,7 @@ dg_status enqueue_step(const StepCtx& c, float tau, float b, float stop_H, uint6
   DG_TRY(pf.mark(DG_PROF_EMBED, 0));
   DG_TRY(launch_embed_rmsnorm(c.canvas->tokens, c.model->E, c.canvas->z, at<void>(ws, L.a),
                               fill_rope ? rope : nullptr, D, M,
-                              P, ctl, c.st));
+                              P, ctl, status, c.st));
   DG_TRY(pf.mark(DG_PROF_EMBED, 1));
   DG_TRY(pf.mark(DG_PROF_QKV, 0));
   DG_TRY(launch_qkv(at<void>(ws, L.a), c.model->Wq, c.model->Wk, c.model->Wv, at<void>(ws, L.q),
@@ -199,7 +199,8 @@ dg_status enqueue_step(const StepCtx& c, float tau, float b, float stop_H, uint6
   DG_TRY(launch_selfcond(sc, ctl, status, c.st));
   DG_TRY(pf.mark(DG_PROF_SELFCOND, 1));
   ReduceArgs ra{at<float>(ws, L.upart), at<float>(ws, L.gbest), at<int>(ws, L.gidx), at<uint8_t>(ws, L.acc),
-                at<void>(ws, L.u), c.canvas->tokens, M, D.d, D.C, sc.nsplit, cdiv(D.V, kGumbelChunk)};
+                at<void>(ws, L.u), c.canvas->tokens, status, M, D.d, D.C, D.V, sc.nsplit,
+                cdiv(D.V, kGumbelChunk)};
   DG_TRY(pf.mark(DG_PROF_REDUCE, 0));
   DG_TRY(launch_reduce(ra, ctl, c.st));
   DG_TRY(pf.mark(DG_PROF_REDUCE, 1));
@@ -325,6 +326,7 @@ const char* dg_status_string(dg_status s) {
     case DG_ERR_WORKSPACE: return "workspace too small or misaligned";
     case DG_ERR_CUDA: return "CUDA error";
     case DG_ERR_TIMEOUT: return "device wait timed out";
+    case DG_ERR_VALUE: return "device value check failed (token out of range or non-finite probabilities)";
   }
   return "unknown status";
 }
@@ -410,7 +412,7 @@ dg_status dg_commit_block(const dg_model* model, dg_kv_cache* cache, const int32
   StopCtl none{nullptr, 0, 0};
   float2* rope = at<float2>(ws, L.rope);
   DG_TRY(launch_embed_rmsnorm(tokens, model->E, nullptr, at<void>(ws, L.a), rope, D, D.B * D.C, cache->len,
-                              none, st));
+                              none, at<int>(ws, L.status), st));
   DG_TRY(launch_qkv(at<void>(ws, L.a), nullptr, model->Wk, model->Wv, nullptr, cache->K, cache->V,
                     cache->cap, cache->len, rope, D, none, at<int>(ws, L.status), at<float>(ws, L.gpart),
                     L.gpart_elems, st));

@@ -166,9 +166,10 @@ void attn_split_tc(const dg_dims& D, int T, int* nsplit, int* keys_per_split);
 void attn_split_mma(const dg_dims& D, int T, int* nsplit, int* keys_per_split);
 
 // Misc kernels.
+// A token outside [0, V) is embedded as token 0 and sets DG_ERR_VALUE in *status.
 cudaError_t launch_embed_rmsnorm(const int32_t* tokens, const void* E, const void* z, void* a,
                                  float2* rope, const dg_dims& D, int rows, int P, StopCtl ctl,
-                                 cudaStream_t st);
+                                 int* status, cudaStream_t st);
 struct StatsArgs {
   const float *pm, *pl, *pS, *pvmax;
   const int* pidx;
@@ -200,6 +201,7 @@ struct SamplerArgs {
   int N;
 };
 cudaError_t launch_sampler(const SamplerArgs& a, cudaStream_t st);
+
 struct ReduceArgs {
   const float* upart;    // [S][M][d]
   const float* gbest;    // [NC][M]
@@ -207,7 +209,8 @@ struct ReduceArgs {
   const uint8_t* acc;
   void* u;               // bf16 [M][d]
   int* tokens;           // [M]
-  int M, d, C, nsplit, nchunks;
+  int* status;           // DG_ERR_VALUE if an accepted row has no finite Gumbel score
+  int M, d, C, V, nsplit, nchunks;
 };
 cudaError_t launch_reduce(const ReduceArgs& a, StopCtl ctl, cudaStream_t st);
 cudaError_t launch_wait_timeout(int* status, cudaStream_t st);

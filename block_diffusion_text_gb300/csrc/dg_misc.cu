@@ -20,6 +20,38 @@ namespace dg {
 constexpr int kEmbThreads = 256;
 constexpr int kEmbMaxChunks = 8;  // d <= 8 * 8 * 256
 
+// The sum of squares is kept as an unevaluated pair of floats (error-free
+// products and sums), the scale r = 1 / sqrt(mean + eps) is formed once per
+// row as a float pair (~2^-44), and each x r is rounded to bf16 from a float
+// pair: a is the correctly rounded bf16 of x r, the value the definition
+// gives, so its rounding does not depend on the order of the sum.  (FP64
+// division and square root are slow on this part; nothing here uses them.)
+DG_DEV void two_sum(float a, float b, float& s, float& e) {
+  s = a + b;
+  const float bb = s - a;
+  e = (a - (s - bb)) + (b - bb);
+}
+DG_DEV void pair_add(float& hi, float& lo, float bhi, float blo) {  // (hi, lo) += (bhi, blo)
+  float s, e;
+  two_sum(hi, bhi, s, e);
+  e += lo + blo;
+  hi = s + e;
+  lo = e - (hi - s);
+}
+// bf16 of hi + lo, round to nearest even: the midpoint between the two bf16
+// neighbours of hi has hi's exponent, so hi - mid is exact and the sign of
+// (hi - mid) + lo is that of the exact difference.
+DG_DEV uint32_t bf16_of_pair(float hi, float lo) {
+  const uint32_t bits = __float_as_uint(hi);
+  const uint32_t t = bits >> 16;  // sign, exponent, 7 mantissa bits
+  if ((bits & 0x7f800000u) == 0x7f800000u) return t | ((bits & 0xffffu) ? 0x40u : 0u);  // inf, nan
+  const float mid = __uint_as_float((t << 16) | 0x8000u);
+  const float dlt = (hi - mid) + lo;
+  bool up = (bits >> 31) ? (dlt < 0.f) : (dlt > 0.f);  // magnitude above the midpoint
+  if (dlt == 0.f) up = (t & 1u) != 0;
+  return t + (up ? 1u : 0u);
+}
+
 // RoPE frequencies theta_j = base^(-2j / hd), computed on the host in double.
 struct RopeTheta {
   double th[64];  // hd / 2 <= 64
@@ -27,17 +59,21 @@ struct RopeTheta {
 
 __global__ void __launch_bounds__(kEmbThreads)
     embed_rmsnorm_kernel(const int32_t* tokens, const __nv_bfloat16* E, const __nv_bfloat16* z,
-                         __nv_bfloat16* a, float2* rope, int d, float eps, int C, int P, int hd,
-                         RopeTheta theta, StopCtl ctl) {
+                         __nv_bfloat16* a, float2* rope, int d, int V, float eps, int C, int P, int hd,
+                         RopeTheta theta, StopCtl ctl, int* status) {
   pdl_wait();
   if (all_stopped(ctl.stop_at, ctl.B, ctl.step)) return;
   const int row = blockIdx.x;
-  const int tok = tokens[row];
+  int tok = tokens[row];
+  if (tok < 0 || tok >= V) {  // never gather outside E: record the bad token, embed token 0
+    if (threadIdx.x == 0) atomicExch(status, kStatusValue);
+    tok = 0;
+  }
   const int nch = d / 8;
   const uint4* e4 = reinterpret_cast<const uint4*>(E + (size_t)tok * d);
   const uint4* z4 = z ? reinterpret_cast<const uint4*>(z + (size_t)row * d) : nullptr;
   float x[kEmbMaxChunks][8];
-  float ss = 0.f;
+  float sh = 0.f, sl = 0.f;  // sum of squares as a float pair
 #pragma unroll
   for (int k = 0; k < kEmbMaxChunks; ++k) {
     const int c = threadIdx.x + k * kEmbThreads;
@@ -49,33 +85,54 @@ __global__ void __launch_bounds__(kEmbThreads)
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         x[k][e] = __bfloat162float(eb[e]) + __bfloat162float(zb[e]);
-        ss = fmaf(x[k][e], x[k][e], ss);
+        const float p = x[k][e] * x[k][e];
+        pair_add(sh, sl, p, fmaf(x[k][e], x[k][e], -p));
       }
     }
   }
-  __shared__ float red[kEmbThreads / 32];
+  __shared__ float red[2][kEmbThreads / 32];
+  __shared__ float rs[2];
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-  if (threadIdx.x % 32 == 0) red[threadIdx.x / 32] = ss;
-  __syncthreads();
-  if (threadIdx.x < 32) {
-    float t = threadIdx.x < kEmbThreads / 32 ? red[threadIdx.x] : 0.f;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
-    if (threadIdx.x == 0) red[0] = t;
+  for (int o = 16; o > 0; o >>= 1)
+    pair_add(sh, sl, __shfl_xor_sync(0xffffffffu, sh, o), __shfl_xor_sync(0xffffffffu, sl, o));
+  if (threadIdx.x % 32 == 0) {
+    red[0][threadIdx.x / 32] = sh;
+    red[1][threadIdx.x / 32] = sl;
   }
   __syncthreads();
-  const float r = 1.0f / sqrtf(red[0] / (float)d + eps);
+  if (threadIdx.x == 0) {
+    float th = red[0][0], tl = red[1][0];
+    for (int w = 1; w < kEmbThreads / 32; ++w) pair_add(th, tl, red[0][w], red[1][w]);
+    // m = sum / d + eps as a float pair (the remainder of a correctly rounded
+    // quotient is exact under fma)
+    const float fd = (float)d;
+    float mh = th / fd;
+    float ml = (fmaf(-mh, fd, th) + tl) / fd;
+    pair_add(mh, ml, eps, 0.f);
+    // r = 1 / sqrt(m): rsqrtf, then one Newton step whose residual 1 - m r0^2
+    // is formed from exact products (its relative error squares: ~2^-44)
+    const float r0 = rsqrtf(mh);
+    const float t = r0 * r0, te = fmaf(r0, r0, -t);
+    const float p = mh * t, pe = fmaf(mh, t, -p);
+    const float e = ((1.0f - p) - pe) - fmaf(mh, te, ml * t);
+    two_sum(r0, 0.5f * r0 * e, rs[0], rs[1]);
+  }
+  __syncthreads();
+  const float rh = rs[0], rl = rs[1];
+  auto scaled = [&](float v) {  // bf16 of v r from the float pair v rh + v rl
+    const float ph = v * rh;
+    return bf16_of_pair(ph, fmaf(v, rl, fmaf(v, rh, -ph)));
+  };
   uint4* a4 = reinterpret_cast<uint4*>(a + (size_t)row * d);
 #pragma unroll
   for (int k = 0; k < kEmbMaxChunks; ++k) {
     const int c = threadIdx.x + k * kEmbThreads;
     if (c < nch) {
       uint4 w;
-      w.x = pack_bf16(x[k][0] * r, x[k][1] * r);
-      w.y = pack_bf16(x[k][2] * r, x[k][3] * r);
-      w.z = pack_bf16(x[k][4] * r, x[k][5] * r);
-      w.w = pack_bf16(x[k][6] * r, x[k][7] * r);
+      w.x = scaled(x[k][0]) | (scaled(x[k][1]) << 16);
+      w.y = scaled(x[k][2]) | (scaled(x[k][3]) << 16);
+      w.z = scaled(x[k][4]) | (scaled(x[k][5]) << 16);
+      w.w = scaled(x[k][6]) | (scaled(x[k][7]) << 16);
       a4[c] = w;
     }
   }
@@ -95,12 +152,13 @@ __global__ void __launch_bounds__(kEmbThreads)
 
 cudaError_t launch_embed_rmsnorm(const int32_t* tokens, const void* E, const void* z, void* a,
                                  float2* rope, const dg_dims& D, int rows, int P, StopCtl ctl,
-                                 cudaStream_t st) {
+                                 int* status, cudaStream_t st) {
   RopeTheta th{};
   for (int j = 0; j < D.hd / 2 && j < 64; ++j) th.th[j] = std::pow((double)D.rope_base, -2.0 * j / D.hd);
   return launch_pdl(embed_rmsnorm_kernel, dim3(rows), dim3(kEmbThreads), 0, st, tokens,
                     reinterpret_cast<const __nv_bfloat16*>(E), reinterpret_cast<const __nv_bfloat16*>(z),
-                    reinterpret_cast<__nv_bfloat16*>(a), rope, D.d, D.rms_eps, D.C, P, D.hd, th, ctl);
+                    reinterpret_cast<__nv_bfloat16*>(a), rope, D.d, D.V, D.rms_eps, D.C, P, D.hd, th, ctl,
+                    status);
 }
 
 // ------------------------------------------------------- tile statistics --
@@ -528,7 +586,13 @@ __global__ void __launch_bounds__(256) reduce_kernel(ReduceArgs a, StopCtl ctl) 
         bi = i2;
       }
     }
-    if (threadIdx.x == 0) a.tokens[row] = bi;
+    // no candidate only when the probabilities are not finite: keep the token
+    if (threadIdx.x == 0) {
+      if (bi >= 0 && bi < a.V)
+        a.tokens[row] = bi;
+      else
+        atomicExch(a.status, kStatusValue);
+    }
   }
 }
 

@@ -21,7 +21,7 @@ LIB_PATH = os.path.join(_HERE, "_build", "libdg.so")
 _lock = threading.Lock()
 _lib = None
 
-DG_OK, DG_ERR_ARG, DG_ERR_SHAPE, DG_ERR_CAPACITY, DG_ERR_WORKSPACE, DG_ERR_CUDA, DG_ERR_TIMEOUT = range(7)
+DG_OK, DG_ERR_ARG, DG_ERR_SHAPE, DG_ERR_CAPACITY, DG_ERR_WORKSPACE, DG_ERR_CUDA, DG_ERR_TIMEOUT, DG_ERR_VALUE = range(8)
 
 # Every function the C header declares (checked by the tests).
 EXPORTS = ("dg_status_string", "dg_workspace_size", "dg_read_status", "dg_canvas_init",

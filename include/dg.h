@@ -33,7 +33,8 @@
  *  - The workspace `ws` (size from dg_workspace_size, 256-byte aligned) holds
  *    intermediates between calls of one step; its first 4 bytes are a device
  *    status word that kernels set to DG_ERR_TIMEOUT if a bounded wait inside a
- *    kernel ran out (read it with dg_read_status); zero the workspace (or at
+ *    kernel ran out, or to DG_ERR_VALUE if a device-side value check failed
+ *    (read it with dg_read_status); zero the workspace (or at
  *    least that word) before its first use.  Calls sharing one workspace must
  *    not overlap on the GPU.
  */
@@ -61,7 +62,11 @@ enum {
   DG_ERR_CAPACITY = 3,   /* commit would write past the cache capacity */
   DG_ERR_WORKSPACE = 4,  /* workspace too small or misaligned */
   DG_ERR_CUDA = 5,       /* a CUDA runtime call or kernel launch failed */
-  DG_ERR_TIMEOUT = 6     /* a bounded device-side wait ran out (status word) */
+  DG_ERR_TIMEOUT = 6,    /* a bounded device-side wait ran out (status word) */
+  DG_ERR_VALUE = 7       /* a device-side value check failed (status word): a canvas
+                            token outside [0, V) reached the embedding (embedded as
+                            token 0), or an accepted row had no finite Gumbel score
+                            (non-finite probabilities; the row kept its token) */
 };
 
 /* Model and canvas sizes.

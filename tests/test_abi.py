@@ -42,8 +42,8 @@ def test_library_exports_every_declared_symbol(dg):
 
 def test_status_strings(dg):
     L = dg.load()
-    seen = {L.dg_status_string(c).decode() for c in range(7)}
-    assert len(seen) == 7
+    seen = {L.dg_status_string(c).decode() for c in range(8)}
+    assert len(seen) == 8
     assert L.dg_status_string(99).decode() == "unknown status"
 
 

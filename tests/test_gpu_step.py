@@ -31,7 +31,17 @@ def _setup(dims, seed, alpha=None):
     return w, x, z, a, model, canvas
 
 
-def _run_and_compare(dims, seed, tau=0.8, b=0.1, step=0, alpha=None, z_in=None, prev=None):
+def _entropy_given_device_h(dims, w, alpha, h_dev, tau):
+    """The oracle's tempered-softmax entropy of logits formed from the device's own h."""
+    import oracle
+    E = np.asarray(w["E"], np.float64)
+    al = np.asarray(alpha, np.float64).reshape(-1)
+    logits = al[:, None] * (np.asarray(h_dev, np.float64) @ E.T) / math.sqrt(dims.d)
+    return np.array([oracle.row_stats(r, tau)["H"] for r in logits])
+
+
+def _run_and_compare(dims, seed, tau=0.8, b=0.1, step=0, alpha=None, z_in=None, prev=None,
+                     entropy_given_h=False):
     from block_diffusion_text_gb300 import dg
     w, x, z, a, model, canvas = _setup(dims, seed, alpha)
     if z_in is not None:
@@ -52,7 +62,11 @@ def _run_and_compare(dims, seed, tau=0.8, b=0.1, step=0, alpha=None, z_in=None, 
     dbg = out["debug"]
     B, C, Hq, Hkv, hd = dims.B, dims.C, dims.Hq, dims.Hkv, dims.hd
     ck = Collect()
-    ck(check_close_bf16, "a", bf16_to_np(dbg["a"]), ref["a"])
+    # a = RMSNorm(E[x] + z) is the correctly rounded bf16 of its definition on both sides
+    def a_exact():
+        n = int((bf16_to_np(dbg["a"]) != ref["a"]).sum())
+        assert n == 0, f"a: {n} elements differ from the oracle"
+    ck(a_exact)
     q = bf16_to_np(dbg["q"]).reshape(B, Hq, C, hd).transpose(0, 2, 1, 3).reshape(B * C, Hq * hd)
     ck(check_close_bf16, "q", q, ref["q"])
     k = bf16_to_np(dbg["k"]).reshape(B, Hkv, C, hd).transpose(0, 2, 1, 3).reshape(B * C, Hkv * hd)
@@ -62,7 +76,11 @@ def _run_and_compare(dims, seed, tau=0.8, b=0.1, step=0, alpha=None, z_in=None, 
     ck(check_close_bf16, "o", bf16_to_np(dbg["o"]), ref["o"])
     ck(check_close_bf16, "h", bf16_to_np(dbg["h"]), ref["h"])
     ck(check_logits, dbg["logits"].cpu().numpy(), ref["logits"])
-    ck(check_entropy, out["entropy"].cpu().numpy().reshape(-1), ref["H"])
+    if entropy_given_h:
+        ck(check_entropy, out["entropy"].cpu().numpy().reshape(-1),
+           _entropy_given_device_h(dims, synth.to_numpy_f32(w), a.numpy(), bf16_to_np(dbg["h"]), tau))
+    else:
+        ck(check_entropy, out["entropy"].cpu().numpy().reshape(-1), ref["H"])
     scale = np.max(np.abs(ref["logits"]), axis=1)
     n_am = ck(check_argmax, out["argmax"].cpu().numpy(), ref["argmax"], ref["top2gap"], scale)
     stats = ck(check_sampler, out["accept"].cpu().numpy(), canvas.tokens.cpu().numpy(), ref, b, C)
@@ -110,6 +128,16 @@ def test_ragged_step_tensor_core_attention():
     g = torch.Generator().manual_seed(6)
     z = (torch.randn(RAGGED_TC.B, RAGGED_TC.C, RAGGED_TC.d, generator=g) * 0.02).to(torch.bfloat16)
     _run_and_compare(RAGGED_TC, seed, tau=0.7, step=2, z_in=z)
+
+
+def test_long_canvas_entropy_given_h():
+    # 600 rows of a d = 128 model with sharp alpha: a few q / k / v elements round to the other bf16
+    # neighbour than the oracle's (fp32 against exact accumulation), which moves h by an ulp in a few
+    # places and the end-to-end entropy by up to ~1.4e-3 nats; every other quantity is compared end to
+    # end, and the entropy against the oracle's statistics of the device's own h (the LM head and the
+    # statistics merge, to 1e-3)
+    dims = synth.Dims(V=1000, d=128, C=300, B=2, Hq=4, Hkv=2, hd=64, F=192, P=64, cap=64)
+    _run_and_compare(dims, 14, tau=0.6, entropy_given_h=True)
 
 
 def test_tensor_core_attention_canvas_tail():
