@@ -144,6 +144,51 @@ def test_commit_matches_oracle_and_checks_capacity():
     assert torch.equal(model.K[:, :, :dims.P + dims.C], before[:, :, :dims.P + dims.C])
 
 
+def _check_sampled_rows(ck, dims, wn, x0, z0, alpha, prev, out, canvas, seed, step, tau, block=0):
+    """One device step against the oracle run from the same state (tokens x0, z0, previous argmax,
+    the prefix cache in wn): sampled rows for the vocabulary-sized stages, the acceptance invariants
+    on every row of the device's own entropies."""
+    M = dims.M
+    rows = sorted({0, 1, M // 3, M // 2 + 7, M - 1})
+    ref = oracle.denoise_step(dims, wn, x0, z0, alpha, tau=tau, b=0.1, seed=seed, step=step, block=block,
+                              prev_argmax=prev, rows=rows,
+                              want=("h", "H", "argmax", "top2gap", "sample_tok", "gumbel_gap", "renoise_tok",
+                                    "z_out"))
+    H = out["entropy"].cpu().numpy().reshape(-1)
+    am = out["argmax"].cpu().numpy().reshape(-1)
+    acc = out["accept"].cpu().numpy().reshape(-1).astype(bool)
+    tok = canvas.tokens.cpu().numpy().reshape(-1)
+    tag = f"step {step}"
+    ck(check_close_bf16, f"h ({tag})", bf16_to_np(out["debug"]["h"])[rows], ref["h"][rows])
+    ck(check_entropy, H[rows], ref["H"][rows])
+    zz = bf16_to_np(canvas.z).reshape(M, dims.d)
+    ck(check_rel_l2, f"z ({tag})", zz[rows], ref["z_out"][rows])
+    logits = out["debug"]["logits"][rows].cpu().numpy()
+    for j, r in enumerate(rows):
+        if am[r] != ref["argmax"][r] and ref["top2gap"][r] >= 1e-4 * np.abs(logits[j]).max():
+            ck.errors.append(f"{tag}: argmax row {r}")
+        if acc[r]:
+            if tok[r] != ref["sample_tok"][r] and ref["gumbel_gap"][r] >= GUMBEL_GAP_TOL:
+                ck.errors.append(f"{tag}: sample row {r}")
+        elif tok[r] != ref["renoise_tok"][r]:
+            ck.errors.append(f"{tag}: renoise row {r}")
+    # acceptance invariants on the device's own entropies, per canvas
+    for b in range(dims.B):
+        Hb = H[b * dims.C:(b + 1) * dims.C].astype(np.float64)
+        ab = acc[b * dims.C:(b + 1) * dims.C]
+        order = np.lexsort((np.arange(dims.C), Hb))
+        n = int(ab.sum())
+        if set(np.nonzero(ab)[0]) != set(order[:n]):
+            ck.errors.append(f"{tag}, canvas {b}: accepted set is not a sorted prefix")
+        if Hb[ab].sum() > 0.1 + 1e-6:
+            ck.errors.append(f"{tag}, canvas {b}: accepted entropy {Hb[ab].sum()} > b")
+        if n < dims.C and Hb[ab].sum() + Hb[order[n]] <= 0.1 - 1e-6:
+            ck.errors.append(f"{tag}, canvas {b}: prefix not maximal")
+        if n != int(out["n_acc"][b]):
+            ck.errors.append(f"{tag}, canvas {b}: n_acc")
+    return out["n_acc"].cpu().tolist()
+
+
 @pytest.mark.slow
 @pytest.mark.parametrize("name", ["loop_v262k_c256_p8k", "prefix_p131k_v32k_c256", "blocks_b8_v32k_p4k"])
 def test_full_size_sampled_rows(name):
@@ -159,46 +204,83 @@ def test_full_size_sampled_rows(name):
     out = dg.denoise_step(model, canvas, tau=0.8, b=0.1, seed=seed, step=0, debug=True)
     torch.cuda.synchronize()
     assert model.status() == 0
-    M = dims.M
-    rows = sorted({0, 1, M // 3, M // 2 + 7, M - 1})
-    wn = synth.to_numpy_f32(w)
-    ref = oracle.denoise_step(dims, wn, x0.cpu().numpy(), z0.float().cpu().numpy(), a.cpu().numpy(), tau=0.8,
-                              b=0.1, seed=seed, step=0, rows=rows,
-                              want=("h", "H", "argmax", "top2gap", "sample_tok", "gumbel_gap", "renoise_tok",
-                                    "z_out"))
     ck = Collect()
-    H = out["entropy"].cpu().numpy().reshape(-1)
-    am = out["argmax"].cpu().numpy().reshape(-1)
-    acc = out["accept"].cpu().numpy().reshape(-1).astype(bool)
-    tok = canvas.tokens.cpu().numpy().reshape(-1)
-    ck(check_close_bf16, "h", bf16_to_np(out["debug"]["h"])[rows], ref["h"][rows])
-    ck(check_entropy, H[rows], ref["H"][rows])
-    zz = bf16_to_np(canvas.z).reshape(M, dims.d)
-    ck(check_rel_l2, "z", zz[rows], ref["z_out"][rows])
-    logits = out["debug"]["logits"][rows].cpu().numpy()
-    for j, r in enumerate(rows):
-        if am[r] != ref["argmax"][r] and ref["top2gap"][r] >= 1e-4 * np.abs(logits[j]).max():
-            ck.errors.append(f"argmax row {r}")
-        if acc[r]:
-            if tok[r] != ref["sample_tok"][r] and ref["gumbel_gap"][r] >= GUMBEL_GAP_TOL:
-                ck.errors.append(f"sample row {r}")
-        elif tok[r] != ref["renoise_tok"][r]:
-            ck.errors.append(f"renoise row {r}")
-    # acceptance invariants on the device's own entropies, per canvas
-    for b in range(dims.B):
-        Hb = H[b * dims.C:(b + 1) * dims.C].astype(np.float64)
-        ab = acc[b * dims.C:(b + 1) * dims.C]
-        order = np.lexsort((np.arange(dims.C), Hb))
-        n = int(ab.sum())
-        if set(np.nonzero(ab)[0]) != set(order[:n]):
-            ck.errors.append(f"canvas {b}: accepted set is not a sorted prefix")
-        if Hb[ab].sum() > 0.1 + 1e-6:
-            ck.errors.append(f"canvas {b}: accepted entropy {Hb[ab].sum()} > b")
-        if n < dims.C and Hb[ab].sum() + Hb[order[n]] <= 0.1 - 1e-6:
-            ck.errors.append(f"canvas {b}: prefix not maximal")
-        if n != int(out["n_acc"][b]):
-            ck.errors.append(f"canvas {b}: n_acc")
-    print(name, "accepted per canvas", out["n_acc"].cpu().tolist())
+    n_acc = _check_sampled_rows(ck, dims, synth.to_numpy_f32(w), x0.cpu().numpy(), z0.float().cpu().numpy(),
+                                a.cpu().numpy(), None, out, canvas, seed, 0, 0.8)
+    print(name, "accepted per canvas", n_acc)
+    ck.done()
+
+
+@pytest.mark.slow
+def test_full_size_loop_teacher_forced():
+    """The 48-step annealed loop at V = 262144, C = 256, P = 8192: steps 0, 1, 24 and 47 checked
+    against the oracle run from the device's own state before that step (free-running
+    trajectories may part after an excused mismatch, so they are not compared)."""
+    from block_diffusion_text_gb300 import dg
+    dims, seed = synth.workload("loop_v262k_c256_p8k")
+    N = 48
+    dev = torch.device("cuda")
+    w = synth.make_weights(dims, seed, device=dev)
+    x, z, a = synth.make_canvas(dims, seed, device=dev)
+    model = dg.Model(dims, w)
+    canvas = dg.Canvas(x, z, a)
+    wn = synth.to_numpy_f32(w)
+    taus = dg.tau_schedule(N)
+    ck = Collect()
+    log = []
+    for s in range(N):
+        check = s in (0, 1, N // 2, N - 1)
+        if check:
+            x0 = canvas.tokens.cpu().numpy().copy()
+            z0 = canvas.z.float().cpu().numpy().copy()
+            prev = canvas.prev_argmax.cpu().numpy().copy() if s > 0 else None
+        out = dg.denoise_step(model, canvas, tau=taus[s], b=0.1, seed=seed, step=s, debug=check)
+        if check:
+            torch.cuda.synchronize()
+            assert model.status() == 0
+            log.append((s, _check_sampled_rows(ck, dims, wn, x0, z0, a.cpu().numpy(), prev, out, canvas, seed,
+                                               s, taus[s])))
+    print("accepted per checked step", log)
+    ck.done()
+
+
+@pytest.mark.slow
+def test_full_size_blocks_commit_teacher_forced():
+    """8 canvases at V = 32768: block 0 runs the annealed loop (adaptive stop), its x0 is committed
+    (checked against the oracle's re-encode of the same tokens), and step 0 of block 1 on the
+    committed cache is checked against the oracle given that cache."""
+    import dataclasses
+    from block_diffusion_text_gb300 import dg
+    dims, seed = synth.workload("blocks_b8_v32k_p4k")
+    dev = torch.device("cuda")
+    w = synth.make_weights(dims, seed, device=dev)
+    x, z, a = synth.make_canvas(dims, seed, device=dev)
+    model = dg.Model(dims, w)
+    wn = synth.to_numpy_f32(w)
+    canvas = dg.Canvas(dg.canvas_init(dims.B, dims.C, dims.V, seed, 0), z.clone(), a)
+    res = dg.denoise_canvas(model, canvas, seed=seed, block=0, N=48)
+    xhat0 = res["xhat0"].clone()
+    dg.commit_block(model, xhat0)
+    torch.cuda.synchronize()
+    assert model.status() == 0 and model.len == dims.P + dims.C
+    Kr, Vr = oracle.commit(dims, wn["E"], wn["Wk"], wn["Wv"], xhat0.cpu().numpy(), wn["Kc"], wn["Vc"], P=dims.P)
+    K, V = bf16_to_np(model.K), bf16_to_np(model.V)
+    sl = slice(dims.P, dims.P + dims.C)
+    assert np.array_equal(K[:, :, :dims.P], Kr[:, :, :dims.P])
+    ck = Collect()
+    ck(check_close_bf16, "committed k", K[:, :, sl], Kr[:, :, sl])
+    ck(check_close_bf16, "committed v", V[:, :, sl], Vr[:, :, sl])
+    # block 1, step 0, on the device's committed cache
+    d1 = dataclasses.replace(dims, P=dims.P + dims.C)
+    w1 = dict(wn, Kc=K, Vc=V)
+    c1 = dg.Canvas(dg.canvas_init(dims.B, dims.C, dims.V, seed, 1), torch.zeros_like(z), a)
+    x0 = c1.tokens.cpu().numpy().copy()
+    out = dg.denoise_step(model, c1, tau=0.8, b=0.1, seed=seed, step=0, block=1, debug=True)
+    torch.cuda.synchronize()
+    assert model.status() == 0
+    n_acc = _check_sampled_rows(ck, d1, w1, x0, np.zeros((dims.B, dims.C, dims.d), np.float32),
+                                a.cpu().numpy(), None, out, c1, seed, 0, 0.8, block=1)
+    print("block 0 steps", res["steps_taken"].cpu().tolist(), "block 1 step 0 accepted", n_acc)
     ck.done()
 
 
