@@ -423,95 +423,125 @@ cudaError_t launch_p0_gumbel(const P0Args& a, StopCtl ctl, cudaStream_t st) {
 // position is renoised to a uniform random token (Philox stream 1).  Also the
 // mean entropy, the accepted count and the adaptive-stop test of step 4
 // (mean entropy <= stop_H and the argmax equal to the previous step's).
-// One CTA per canvas, one thread per (padded) position.  The sort is by rank:
-// each position counts the positions ordered before it (entropy as an
-// order-preserving integer key, ties by position), then the entropies are
-// placed in rank order and summed with a warp-shuffle scan.
+// One CTA per canvas, one thread per (padded) position:
+//  - every global load and the Philox draw of the thread's own position are
+//    issued first, so their latency overlaps the sort;
+//  - (entropy as an order-preserving integer key, position) pairs are sorted
+//    by a bitonic network: strides below 32 by warp shuffles, the others
+//    through shared memory;
+//  - the sorted entropies are summed in fixed point (units of 2^-44, exact
+//    integer sums, so the result does not depend on the order of additions;
+//    it differs from a double sum by < 1e-10);
+//  - counts and the all-unchanged test are block ballots.
 DG_DEV uint64_t order_key(double h) {
   const uint64_t b = (uint64_t)__double_as_longlong(h);
   return (b >> 63) ? ~b : (b | 0x8000000000000000ull);  // unsigned order = numeric order
 }
+constexpr double kFixScale = 17592186044416.0;  // 2^44
+DG_DEV long long fixed_entropy(double h) {
+  // |H| <= 32 for any finite entropy of V <= 2^31 tokens; anything else (not
+  // finite) counts as 32 nats: never accepted, and 1024 of them cannot overflow
+  return (h > -32.0 && h < 32.0) ? __double2ll_rn(h * kFixScale) : (long long)(32.0 * kFixScale);
+}
+DG_DEV bool sorts_before(uint64_t ka, int ia, uint64_t kb, int ib) { return ka < kb || (ka == kb && ia < ib); }
 
 __global__ void __launch_bounds__(1024) sampler_kernel(SamplerArgs a, int npow2) {
   pdl_wait();
   const int b = blockIdx.x;
-  const int i = threadIdx.x;
-  const bool active = a.stop_at[b] >= a.step;
+  const int t = threadIdx.x;
   // Every canvas skips its work once it has stopped.
-  if (!active) return;
-  __shared__ uint64_t key[1024];
-  __shared__ int idx[1024];
-  __shared__ double cum[1024];
-  __shared__ double wsum[32];
-  __shared__ int flags[2];
+  if (a.stop_at[b] < a.step) return;
+  __shared__ uint64_t sk[1024];
+  __shared__ int si[1024];
+  __shared__ long long sf[1024];
+  __shared__ int stok[1024];
+  __shared__ long long wsum[32];
+  __shared__ long long total;
   const int base = b * a.C;
-  const double h = i < a.C ? a.Hd[base + i] : 0.0;
-  const uint64_t ki = order_key(h);
-  if (i < a.C) key[i] = ki;
-  if (i == 0) {
-    flags[0] = 0;  // accepted count
-    flags[1] = 1;  // argmax unchanged everywhere
+  const bool valid = t < a.C;
+  // own position: entropy, argmax, previous argmax, renoise token
+  double h = 0.0;
+  int am = 0, prev = 0;
+  if (valid) {
+    h = a.Hd[base + t];
+    am = a.amax[base + t];
+    prev = a.prev_argmax[base + t];
+    uint64_t pw[4];
+    philox_block(pw, a.seed, a.block, a.step, b, t, 0, 1);
+    stok[t] = uniform_token(pw[0], a.V);
+    sf[t] = fixed_entropy(h);
   }
-  __syncthreads();
-  // rank of position i in (entropy, position) order
-  int rank = 0;
-  if (i < a.C) {
-#pragma unroll 8
-    for (int j = 0; j < a.C; ++j) {
-      const uint64_t kj = key[j];
-      rank += (kj < ki || (kj == ki && j < i)) ? 1 : 0;
+  const bool unchanged = !valid || (a.step >= 1 && prev == am);
+  if (valid) a.prev_argmax[base + t] = am;
+  uint64_t k = valid ? order_key(h) : ~0ull;
+  int ix = t;
+  const int all_unchanged = __syncthreads_and(unchanged);  // also publishes stok, sf
+  // bitonic sort of (k, ix) ascending: thread t ends with the element of rank t
+  for (int size = 2; size <= npow2; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      uint64_t ko;
+      int io;
+      if (stride >= 32) {
+        sk[t] = k;
+        si[t] = ix;
+        __syncthreads();
+        ko = sk[t ^ stride];
+        io = si[t ^ stride];
+        __syncthreads();
+      } else {
+        ko = __shfl_xor_sync(0xffffffffu, k, stride);
+        io = __shfl_xor_sync(0xffffffffu, ix, stride);
+      }
+      // the lower index of a pair keeps the smaller element in an ascending
+      // block (the larger in a descending one), the upper index the other
+      const bool keep_min = ((t & stride) == 0) == ((t & size) == 0);
+      const bool other_first = sorts_before(ko, io, k, ix);
+      if (keep_min == other_first) {
+        k = ko;
+        ix = io;
+      }
     }
-    idx[rank] = i;
-    cum[rank] = h;
   }
-  __syncthreads();
-  // inclusive prefix sum of the sorted entropies (double): warp scan, then
-  // the warps' totals
-  double v = i < a.C ? cum[i] : 0.0;
-  const int lane = i & 31, w = i >> 5;
+  // inclusive prefix sums of the sorted entropies (padding adds 0)
+  const long long f = ix < a.C ? sf[ix] : 0ll;
+  long long v = f;
+  const int lane = t & 31, w = t >> 5;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const double u = __shfl_up_sync(0xffffffffu, v, o);
+    const long long u = __shfl_up_sync(0xffffffffu, v, o);
     if (lane >= o) v += u;
   }
   if (lane == 31) wsum[w] = v;
   __syncthreads();
   if (w == 0) {
-    double t = lane < (npow2 + 31) / 32 ? wsum[lane] : 0.0;
+    long long s = lane < (npow2 + 31) / 32 ? wsum[lane] : 0ll;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const double u = __shfl_up_sync(0xffffffffu, t, o);
-      if (lane >= o) t += u;
+      const long long u = __shfl_up_sync(0xffffffffu, s, o);
+      if (lane >= o) s += u;
     }
-    wsum[lane] = t;  // inclusive totals of warps 0..lane
+    wsum[lane] = s;  // inclusive totals of warps 0..lane
   }
   __syncthreads();
   if (w > 0) v += wsum[w - 1];
-  if (i < a.C) cum[i] = v;
-  __syncthreads();
-  if (i < a.C) {
-    const int pos = idx[i];
-    const bool acc = cum[i] <= (double)a.b;
+  if (t == a.C - 1) total = v;
+  // accept the sorted prefix with cumulative entropy <= b
+  const long long bfix = (long long)floor((double)a.b * kFixScale);
+  const bool acc = t < a.C && v <= bfix;
+  if (t < a.C) {
+    const int pos = ix;
     a.acc[base + pos] = acc ? 1 : 0;
     if (a.acc_out) a.acc_out[base + pos] = acc ? 1 : 0;
-    if (acc) atomicAdd(&flags[0], 1);
-    if (!acc) {
-      uint64_t pw[4];
-      philox_block(pw, a.seed, a.block, a.step, b, pos, 0, 1);
-      a.tokens[base + pos] = uniform_token(pw[0], a.V);
-    }
-    const int am = a.amax[base + i];
-    if (a.step < 1 || a.prev_argmax[base + i] != am) atomicAnd(&flags[1], 0);
+    if (!acc) a.tokens[base + pos] = stok[pos];
   }
-  __syncthreads();
-  if (i < a.C) a.prev_argmax[base + i] = a.amax[base + i];
-  if (i == 0) {
-    const double meanH = cum[a.C - 1] / (double)a.C;
-    const int stop = (a.step >= 1 && flags[1] && meanH <= (double)a.stop_H) ? 1 : 0;
-    if (a.n_acc) a.n_acc[b] = flags[0];
+  const int n_acc = __syncthreads_count(acc);  // also publishes total
+  if (t == 0) {
+    const double meanH = (double)total / kFixScale / (double)a.C;
+    const int stop = (a.step >= 1 && all_unchanged && meanH <= (double)a.stop_H) ? 1 : 0;
+    if (a.n_acc) a.n_acc[b] = n_acc;
     if (a.mean_H) a.mean_H[b] = (float)meanH;
     if (a.stop) a.stop[b] = stop;
-    if (a.accepted_log) a.accepted_log[(size_t)b * a.N + a.step] = flags[0];
+    if (a.accepted_log) a.accepted_log[(size_t)b * a.N + a.step] = n_acc;
     if (stop) a.stop_at[b] = a.step;
   }
 }
