@@ -47,6 +47,37 @@ def test_loop_sharp_alpha_converges_at_step_one():
     assert np.array_equal(res["xhat0"].cpu().numpy(), ref["xhat0"])
 
 
+def test_loop_canvases_stop_independently():
+    """Three canvases in one batch: the sharp first and last stop at step 1 (adaptive stop), the
+    middle one runs every step.  Stopped canvases are left untouched by the later steps (their
+    tokens, z and x0 equal the oracle's frozen state) while the batch goes on."""
+    from block_diffusion_text_gb300 import dg
+    dims = synth.Dims(V=512, d=64, C=16, B=3, Hq=2, Hkv=1, hd=32, F=128, P=32)
+    N = 6
+    w, x, z, a, model = _model(dims, 8)
+    a[0] = 64.0
+    a[2] = 64.0
+    canvas = dg.Canvas(x.cuda(), z.cuda(), a.cuda())
+    res = dg.denoise_canvas(model, canvas, seed=8, N=N)
+    torch.cuda.synchronize()
+    assert model.status() == 0
+    ref = oracle.denoise_canvas(dims, synth.to_numpy_f32(w), x.numpy(), a.numpy(), seed=8, N=N)
+    steps = res["steps_taken"].cpu().numpy()
+    assert steps.tolist() == ref["steps_taken"].tolist()
+    assert res["converged"].cpu().tolist() == ref["converged"].tolist()
+    assert steps[0] == steps[2] == 2 and steps[1] > 2  # the batch outlives its stopped canvases
+    acc = res["accepted"].cpu().numpy()
+    tok = canvas.tokens.cpu().numpy()
+    zz = bf16_to_np(canvas.z).reshape(dims.B, dims.C, dims.d)
+    for b in (0, 2):
+        assert np.array_equal(acc[b], ref["accepted"][b]), b
+        assert (acc[b, 2:] == -1).all()
+        assert np.array_equal(res["xhat0"][b].cpu().numpy(), ref["xhat0"][b])
+        assert np.array_equal(tok[b], ref["tokens"][b])
+        assert check_rel_l2(f"z canvas {b}", zz[b], ref["z"][b]) <= 1e-2
+    assert (acc[1] >= 0).all()
+
+
 def _step_by_step(dims, seed, N, alpha=None):
     """GPU and oracle loops side by side, each from its own state; returns per-step agreement."""
     from block_diffusion_text_gb300 import dg
