@@ -50,6 +50,7 @@ def _args():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-loop", action="store_true")
     return ap.parse_args()
 
 
@@ -159,18 +160,45 @@ class ClockSampler:
 
 
 # ------------------------------------------------------- algorithmic work --
-def kernel_work(d: synth.Dims):
-    """Algorithmic FLOPs and HBM bytes per launch of the dominant kernels."""
+def stage_work(d: synth.Dims):
+    """Algorithmic FLOPs and HBM bytes per step of each stage: what the method must compute and
+    move (weights and E read once, the stage's own inputs and outputs), not what a kernel happens
+    to store for itself (the exp(s - m) tiles, split partials, statistics).  Every stage of the
+    step is listed, so their sum of roofline times is the step's roofline."""
     M, V, D = d.B * d.C, d.V, d.d
-    NT = math.ceil(V / 128)  # softmax-statistics groups of 128 columns
+    nq, nkv = d.Hq * d.hd, d.Hkv * d.hd
     T = d.P + d.C
-    lm_flops = 2.0 * M * V * D
-    lm_bytes = 2.0 * V * D + 2.0 * M * D + 2.0 * M * V + 20.0 * NT * M + 4.0 * M
-    sc_flops = 2.0 * M * V * D
-    sc_bytes = 2.0 * V * D + 2.0 * M * V + 4.0 * NT * M
-    at_flops = 4.0 * d.B * d.Hq * d.C * T * d.hd
-    at_bytes = 2.0 * 2 * d.B * d.Hkv * T * d.hd + 2.0 * 2 * M * d.Hq * d.hd
-    return {"lmhead": (lm_flops, lm_bytes), "selfcond": (sc_flops, sc_bytes), "attn": (at_flops, at_bytes)}
+    bf = 2.0
+    w = {}
+    w["embed"] = (0.0, bf * M * D * 3 + 4.0 * M)                       # E rows, z, a
+    w["qkv"] = (2.0 * M * D * (nq + 2 * nkv), bf * D * (nq + 2 * nkv) + bf * M * D + bf * M * (nq + 2 * nkv))
+    w["attn"] = (4.0 * d.B * d.Hq * d.C * T * d.hd, bf * 2 * d.B * d.Hkv * T * d.hd + bf * 2 * M * nq)
+    w["oproj"] = (2.0 * M * nq * D, bf * nq * D + bf * M * nq + bf * 2 * M * D)
+    w["lmhead"] = (2.0 * M * V * D, bf * V * D + bf * M * D + 4.0 * M)  # E + h (+ alpha)
+    w["selfcond"] = (2.0 * M * V * D, bf * V * D + bf * M * D)          # E + u
+    w["ffw"] = (4.0 * M * D * d.F, bf * 2 * D * d.F + bf * 2 * M * D + bf * M * d.F)
+    w["sampler"] = (0.0, 4.0 * M * 4)                                   # entropy, argmax, tokens, accept
+    return w
+
+
+def kernel_work(d: synth.Dims):
+    """(FLOPs, algorithmic bytes) per launch of the timed kernel slots."""
+    w = stage_work(d)
+    return {"lmhead": w["lmhead"], "selfcond": w["selfcond"], "attn": w["attn"]}
+
+
+def step_roofline(d: synth.Dims, peaks):
+    """T_roof = sum over stages of max(FLOPs / tensor peak, bytes / HBM peak), with E read once per
+    step for the two vocabulary products together (their bytes are counted once).  Sustained bf16
+    tensor peak: the step runs back to back."""
+    w = stage_work(d)
+    w = dict(w)
+    fl = w["lmhead"][0] + w["selfcond"][0]
+    w["vocab"] = (fl, 2.0 * d.V * d.d + 2.0 * 2 * d.M * d.d + 4.0 * d.M)
+    del w["lmhead"], w["selfcond"]
+    tc, bw = peaks["tc_sustained"] * 1e12, peaks["hbm"] * 1e9
+    per = {k: max(f / tc, b / bw) for k, (f, b) in w.items()}
+    return sum(per.values()), per
 
 
 def _traffic(kernel: str):
@@ -193,24 +221,13 @@ def _traffic(kernel: str):
 
 
 # ------------------------------------------------------------ CPU oracle --
-def oracle_sample(dims, w_np, x, z, a, nthreads):
-    """Time the oracle on a bounded sample of one step; returns (steps/s estimate, detail)."""
-    import numpy as np
+def oracle_full_step(dims, w_np, x, z, a, nthreads, tau=0.8, step=0, seed=0):
+    """Seconds of one full oracle step (every stage, every row) on `nthreads` host threads."""
     import oracle
-    rows = list(range(min(nthreads, dims.B * dims.C)))
     t0 = time.perf_counter()
-    oracle.denoise_step(dims, w_np, x, z, a, tau=0.8, b=0.1, seed=0, step=0, rows=[],
-                        want=("H",), nthreads=nthreads)
-    t_front = time.perf_counter() - t0
-    t0 = time.perf_counter()
-    oracle.denoise_step(dims, w_np, x, z, a, tau=0.8, b=0.1, seed=0, step=0, rows=rows,
-                        want=("H", "z_out"), nthreads=nthreads)
-    t_all = time.perf_counter() - t0
-    per_rows = max(t_all - t_front, 1e-9)
-    t_step = t_front + per_rows * (dims.B * dims.C) / len(rows)
-    del np
-    return 1.0 / t_step, dict(t_front_s=round(t_front, 3), t_rows_s=round(per_rows, 3), rows=len(rows),
-                              t_step_est_s=round(t_step, 2))
+    oracle.denoise_step(dims, w_np, x, z, a, tau=tau, b=0.1, seed=seed, step=step,
+                        want=("H", "tokens_out", "z_out", "n_acc"), nthreads=nthreads)
+    return time.perf_counter() - t0
 
 
 def _oracle_inputs_from(w, x, z, a):
@@ -219,40 +236,37 @@ def _oracle_inputs_from(w, x, z, a):
 
 
 def run_reference(args, world, rank):
+    """The oracle as it stands, on the host cores.  Each timed step is one full oracle step (every
+    stage for every row of the canvas); the warm-up steps run the oracle's front stages (a..h) only,
+    since the oracle has no state that a full warm-up step would prepare."""
     if rank != 0:
         return
+    import oracle
     dims, seed = synth.workload(args.workload)
     nthreads = os.cpu_count() or 1
     w = synth.make_weights(dims, seed, device="cpu")
     x, z, a = synth.make_canvas(dims, seed, device="cpu")
     wn, xn, zn, an = _oracle_inputs_from(w, x, z, a)
     del w
-    import oracle
-    rows = list(range(min(nthreads, dims.M)))
-    t0 = time.perf_counter()
-    oracle.denoise_step(dims, wn, xn, zn, an, tau=0.8, b=0.1, seed=seed, step=0, rows=[], want=("H",),
-                        nthreads=nthreads)
-    t_front = time.perf_counter() - t0
-    ests = []
-    taus = [0.8 + (0.4 - 0.8) * s / 47 for s in range(48)]
-    for s in range(args.warmup + args.steps):
-        t0 = time.perf_counter()
-        oracle.denoise_step(dims, wn, xn, zn, an, tau=taus[s % 48], b=0.1, seed=seed, step=s % 48, rows=rows,
-                            want=("H", "z_out"), nthreads=nthreads)
-        t = time.perf_counter() - t0
-        if s >= args.warmup:
-            ests.append(t_front + max(t - t_front, 1e-9) * dims.M / len(rows))
-    t_step = statistics.mean(ests)
-    value = 1.0 / t_step
-    sample = (f"per step: the oracle's attention front (a..h) for all {dims.M} rows once, then the "
-              f"vocabulary stages for {len(rows)} of {dims.M} rows, scaled to the full canvas")
+    taus = oracle.tau_schedule(48, 0.8, 0.4)
+    for s in range(args.warmup):
+        oracle.denoise_step(dims, wn, xn, zn, an, tau=taus[s % 48], b=0.1, seed=seed, step=s % 48, rows=[],
+                            want=("h",), nthreads=nthreads)
+    times = []
+    t_all = time.perf_counter()
+    for s in range(args.steps):
+        times.append(oracle_full_step(dims, wn, xn, zn, an, nthreads, tau=taus[s % 48], step=s % 48, seed=seed))
+    t_all = time.perf_counter() - t_all
+    value = args.steps / t_all
+    sample = (f"each timed step is one full oracle step: all {dims.M} rows through every stage "
+              f"(front, LM head, sampler, p0.E, FFW); warm-up steps run the front stages only")
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": t_step * 1e3, "higher_is_better": True,
+            "warmup": args.warmup, "ms_per_step": t_all / args.steps * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "impl": "reference",
             "config": _config(dims, args.workload),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": nthreads, "kind": "oracle",
-                             "sample": sample},
+                             "sample": sample, "step_s": [round(t, 3) for t in times]},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -405,27 +419,75 @@ def run_ours(args, world, rank, local):
         e2e = {"value": world * ksteps / e_s, "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "steps": ksteps}
 
-    # roofline of the dominant kernel
+    # rooflines: per kernel against both bounds (algorithmic work), and the whole step
     peaks = _peaks()
     work = kernel_work(dims)
-    dominant = max(("lmhead", "selfcond"), key=lambda k: per_kernel[k])
     rl = {}
-    for name in ("attn", "lmhead", "selfcond"):
-        fl, by = work[name]
+    for name, (fl, by) in work.items():
+        if name not in per_kernel:
+            continue
         sec = per_kernel[name] / 1e3
         t_tc = fl / (peaks["tc_sustained"] * 1e12)
         t_hbm = by / (peaks["hbm"] * 1e9)
         bound = "tensor" if t_tc >= t_hbm else "hbm"
+        tc_frac = fl / sec / 1e12 / peaks["tc_sustained"]
+        hbm_frac = by / sec / 1e9 / peaks["hbm"]
         if bound == "tensor":
-            ach, peak, unit = fl / sec / 1e12, peaks["tc_sustained"], "TFLOP/s"
+            ach, peak, unit, frac = fl / sec / 1e12, peaks["tc_sustained"], "TFLOP/s", tc_frac
         else:
-            ach, peak, unit = by / sec / 1e9, peaks["hbm"], "GB/s"
-        rl[name] = {"bound": bound, "achieved": ach, "peak": peak, "unit": unit, "frac": ach / peak,
+            ach, peak, unit, frac = by / sec / 1e9, peaks["hbm"], "GB/s", hbm_frac
+        rl[name] = {"bound": bound, "achieved": ach, "peak": peak, "unit": unit, "frac": frac,
                     "traffic": _traffic(name), "ms": per_kernel[name],
                     "tflops": fl / sec / 1e12, "gbs": by / sec / 1e9,
+                    "tensor_frac": tc_frac, "hbm_frac": hbm_frac,
+                    "algorithmic": {"flop": fl, "bytes": by},
                     "peak_note": ("of measured" if peaks["src"] == "measured" else "of fallback")
                     + (" sustained bf16" if bound == "tensor" else " HBM copy")}
+    dominant = max(rl, key=lambda k: rl[k]["ms"])
     dom = rl[dominant]
+    t_roof, t_stage = step_roofline(dims, peaks)
+    step_s = max_ms / args.steps / 1e3
+    step_rl = {"t_roof_ms": t_roof * 1e3, "steps_per_s_roof": 1.0 / t_roof, "frac": t_roof / step_s,
+               "canvas_tokens_per_s_roof": dims.M / t_roof, "canvas_tokens_frac": t_roof / step_s,
+               "stage_roof_ms": {k: round(v * 1e3, 4) for k, v in t_stage.items()},
+               "note": "sum over stages of max(FLOPs / sustained bf16 peak, algorithmic bytes / HBM peak); "
+                       "E read once per step for both vocabulary products"}
+
+    # the annealed loop itself (dg_denoise_canvas, up to 48 steps with adaptive stop) from the
+    # benchmark's initial canvas, and the commit of its result
+    loop = None
+    if rank == 0 and not args.no_loop:
+        lc = dg.Canvas(x0.clone(), z0.clone(), a)
+        torch.cuda.synchronize()
+        tl = time.perf_counter()
+        res = dg.denoise_canvas(model, lc, seed=seed, N=48)
+        torch.cuda.synchronize()
+        tl = time.perf_counter() - tl
+        acc = res["accepted"].cpu().numpy()
+        taken = res["steps_taken"].cpu().tolist()
+        per_step = [int(v) for v in acc[0] if v >= 0]
+        loop = {"steps_taken": taken, "converged": res["converged"].cpu().tolist(),
+                "accepted_per_step": per_step,
+                "mean_accepted_per_step": float(sum(per_step) / max(len(per_step), 1)),
+                "ms": tl * 1e3, "steps_per_s": sum(taken) / tl,
+                "note": "one dg_denoise_canvas call, host clock (the loop reads its 4-byte stop count "
+                        "every 4 steps)"}
+        if model.status() != 0:
+            raise RuntimeError("device status word set during the loop")
+        # commit of the loop's x0 at position P (into rows P..P+C-1 of a cache with room for it)
+        Kx = torch.zeros(dims.B, dims.Hkv, dims.P + dims.C, dims.hd, dtype=torch.bfloat16, device=dev)
+        Vx = torch.zeros_like(Kx)
+        xh = res["xhat0"]
+        for _ in range(3):
+            dg.commit_block(model, xh, cache=(Kx, Vx, dims.P))
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        c0.record(stream)
+        for _ in range(20):
+            dg.commit_block(model, xh, cache=(Kx, Vx, dims.P))
+        c1.record(stream)
+        torch.cuda.synchronize()
+        loop["commit_ms"] = c0.elapsed_time(c1) / 20
+        del Kx, Vx
 
     if graph_kernels is not None:
         gpu_launches, launch_src = graph_kernels, "kernel nodes of the timed CUDA graph"
@@ -440,7 +502,10 @@ def run_ours(args, world, rank, local):
             "canvas_tokens_per_s": value * dims.B * dims.C,
             "roofline": {"bound": dom["bound"], "achieved": dom["achieved"], "peak": dom["peak"],
                          "unit": dom["unit"], "frac": dom["frac"], "traffic": dom["traffic"],
-                         "kernel": dominant, "peak_note": dom["peak_note"]},
+                         "kernel": dominant, "peak_note": dom["peak_note"],
+                         "tensor_frac": dom["tensor_frac"], "hbm_frac": dom["hbm_frac"]},
+            "step_roofline": step_rl,
+            "loop": loop,
             "kernels": rl,
             "kernel_ms": {k: round(v, 5) for k, v in per_kernel.items()},
             "timing": "K steps captured in one CUDA graph, CUDA events around its replay; per-kernel "
@@ -453,10 +518,10 @@ def run_ours(args, world, rank, local):
         try:
             nthreads = os.cpu_count() or 1
             wn, xn, zn, an = _oracle_inputs_from(w, x0, z0, a)
-            v, det = oracle_sample(dims, wn, xn, zn, an, nthreads)
-            line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": nthreads, "kind": "oracle",
-                                    "sample": (f"a..h for all {dims.M} rows, vocabulary stages for "
-                                               f"{det['rows']} rows, scaled to one step"), **det}
+            t = oracle_full_step(dims, wn, xn, zn, an, nthreads, seed=seed)
+            line["cpu_baseline"] = {"value": 1.0 / t, "unit": UNIT, "cores": nthreads, "kind": "oracle",
+                                    "sample": f"one full oracle step: all {dims.M} rows through every stage",
+                                    "step_s": round(t, 3)}
         except Exception as e:  # the baseline is reported, not required
             line["cpu_baseline"] = {"value": None, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
                                     "sample": f"failed: {e!r}"}

@@ -156,6 +156,7 @@ dg_status enqueue_step(const StepCtx& c, float tau, float b, float stop_H, uint6
   sp.mean_H = out ? out->mean_H : nullptr;
   sp.stop = out ? out->stop : nullptr;
   sp.stop_at = stop_at;
+  sp.n_stopped = at<int>(ws, L.status) + 1;
   sp.B = D.B;
   sp.C = D.C;
   sp.V = D.V;
@@ -242,6 +243,13 @@ dg_status check_cache(const dg_dims& D, const dg_kv_cache* cache) {
 dg_status check_canvas(const dg_canvas* cv) {
   if (!cv || !cv->tokens || !cv->z || !cv->alpha || !cv->prev_argmax) return DG_ERR_ARG;
   return DG_OK;
+}
+
+// Linear temperature anneal of [TR] step 3 / Table 2: tau0 at step 0, tau1 at
+// step N - 1, in double, rounded once to float.
+float tau_at(const dg_sched& sc, int step) {
+  const double frac = sc.N > 1 ? (double)step / (double)(sc.N - 1) : 0.0;
+  return (float)((double)sc.tau0 + ((double)sc.tau1 - (double)sc.tau0) * frac);
 }
 
 }  // namespace
@@ -342,6 +350,14 @@ dg_status dg_workspace_size(const dg_dims* dims, int32_t cap, size_t* bytes) {
   return DG_OK;
 }
 
+dg_status dg_tau(const dg_sched* sched, int32_t step, float* tau) {
+  if (!sched || !tau || sched->N <= 0 || step < 0 || step >= sched->N || !(sched->tau0 > 0.f) ||
+      !(sched->tau1 > 0.f))
+    return DG_ERR_ARG;
+  *tau = tau_at(*sched, step);
+  return DG_OK;
+}
+
 dg_status dg_read_status(const void* ws, int32_t* status, void* stream) {
   if (!ws || !status) return DG_ERR_ARG;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
@@ -384,15 +400,30 @@ dg_status dg_denoise_canvas(const dg_model* model, const dg_kv_cache* cache, dg_
   StepCtx c{model, cache, canvas, ws, {}, reinterpret_cast<cudaStream_t>(stream)};
   if ((s = check_ws(model->dims, cache->cap, ws, ws_bytes, &c.L))) return s;
   const dg_dims& D = model->dims;
+  int* n_stopped = at<int>(ws, c.L.status) + 1;
   DG_TRY(cudaMemsetAsync(at<void>(ws, c.L.stop_at), 0x7f, 4 * (size_t)D.B, c.st));
+  DG_TRY(cudaMemsetAsync(n_stopped, 0, sizeof(int), c.st));
   DG_TRY(cudaMemsetAsync(result->accepted, 0xff, 4 * (size_t)D.B * sched->N, c.st));
+  // Outside a stream capture the loop reads the count of stopped canvases
+  // (4 bytes; the stream is synchronised) after step 1, the first step at
+  // which the stop test can fire, and every kLoopCheck steps after, and
+  // enqueues nothing more once every canvas has stopped.  Under capture it
+  // enqueues all N steps; their kernels exit at once after every canvas stopped.
+  constexpr int kLoopCheck = 4;
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  DG_TRY(cudaStreamIsCapturing(c.st, &cap));
+  const bool check = cap == cudaStreamCaptureStatusNone;
   const int N = sched->N;
   for (int step = 0; step < N; ++step) {
-    const double frac = N > 1 ? (double)step / (double)(N - 1) : 0.0;
-    const float tau = (float)((double)sched->tau0 + ((double)sched->tau1 - (double)sched->tau0) * frac);
-    s = enqueue_step(c, tau, sched->b, sched->stop_H, seed, step, block, nullptr, result->accepted, N,
-                     step == 0);
+    s = enqueue_step(c, tau_at(*sched, step), sched->b, sched->stop_H, seed, step, block, nullptr,
+                     result->accepted, N, step == 0);
     if (s) return s;
+    if (check && step + 1 < N && step % kLoopCheck == 1) {
+      int stopped = 0;
+      DG_TRY(cudaMemcpyAsync(&stopped, n_stopped, sizeof(int), cudaMemcpyDeviceToHost, c.st));
+      DG_TRY(cudaStreamSynchronize(c.st));
+      if (stopped >= D.B) break;
+    }
   }
   return cuda_status(launch_loop_finish(at<int>(ws, c.L.stop_at), D.B, N, result->steps_taken,
                                         result->converged, canvas->prev_argmax, result->xhat0, D.C, c.st));

@@ -193,6 +193,7 @@ struct SamplerArgs {
   float* mean_H;         // optional [B]
   int* stop;             // optional [B]
   int* stop_at;          // [B] (workspace)
+  int* n_stopped;        // canvases whose stop test fired (workspace), or nullptr
   int B, C, V;
   float b, stop_H;
   uint64_t seed;

@@ -542,7 +542,10 @@ __global__ void __launch_bounds__(1024) sampler_kernel(SamplerArgs a, int npow2)
     if (a.mean_H) a.mean_H[b] = (float)meanH;
     if (a.stop) a.stop[b] = stop;
     if (a.accepted_log) a.accepted_log[(size_t)b * a.N + a.step] = n_acc;
-    if (stop) a.stop_at[b] = a.step;
+    if (stop) {
+      a.stop_at[b] = a.step;
+      if (a.n_stopped) atomicAdd(a.n_stopped, 1);
+    }
   }
 }
 

@@ -5,14 +5,18 @@
 // allocator, or embedding code that is only handed fixed buffers and must not
 // allocate (a cudaMalloc can also synchronise the device).  For them,
 // dg_attention_noalloc runs the split-key attention of the denoising step
-// with its scratch (the per-split partial outputs and their max / sum) in a
-// static device array of this file instead of a caller workspace.
+// with its scratch (a status word, the per-split partial outputs and their
+// max / sum) in a static device array of this file instead of a caller
+// workspace.
 //
 // The array is 16 MiB.  Every GPU that loads the library holds it until the
 // process exits.  All calls share it and it keeps the contents of the last
-// call; every split writes its whole partial tile before the merge reads it,
-// so nothing in it needs to start at zero.  Calls that overlap on the GPU
-// (different streams, or different host threads on one device) race on it.
+// call.  Only the status word must start at zero: each call clears it on the
+// stream before its kernels run; every split writes its whole partial tile
+// before the merge reads it, so the partials need no clearing.  Calls that
+// overlap on the GPU (different streams, or different host threads on one
+// device) race on it.
+#include <climits>
 #include <mutex>
 
 #include "dg_internal.h"
@@ -20,10 +24,8 @@
 namespace {
 
 constexpr size_t kScratchBytes = size_t(16) << 20;
+constexpr size_t kStatusBytes = 256;  // the status word, padded to keep the partials aligned
 __device__ __align__(256) unsigned char g_attn_scratch[kScratchBytes];
-
-// Status word for the bounded waits of the attention kernels (not read back).
-__device__ int g_noalloc_status;
 
 constexpr int kMaxDevices = 64;
 std::mutex g_setup_mutex;
@@ -31,7 +33,9 @@ unsigned char* g_scratch_ptr[kMaxDevices] = {};
 
 // Device address of the static array on the current device.  The first call
 // on a device looks it up with cudaGetSymbolAddress (with that device
-// current); later calls reuse it.
+// current); later calls reuse it.  The cached address belongs to the device's
+// primary context: a caller that destroys that context (cudaDeviceReset) must
+// not call these entry points again in the same process.
 dg_status scratch_on_current_device(unsigned char** out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return DG_ERR_CUDA;
@@ -54,7 +58,11 @@ extern "C" dg_status dg_attention_noalloc(const void* q, const void* K, const vo
   if (B <= 0 || C <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || cap < 0 || len < 0 || len > cap)
     return DG_ERR_ARG;
   if (hd != 32 && hd != 64 && hd != 128) return DG_ERR_SHAPE;
-  if (C > 1024) return DG_ERR_SHAPE;
+  // the same bounds the denoising step applies to its dims, and the grid's
+  // second dimension (one row per canvas and head)
+  if (C > 1024 || (int64_t)B * C > (1 << 20) || (int64_t)B * Hq > 65535) return DG_ERR_SHAPE;
+  const int64_t T = (int64_t)len + C;
+  if (T > INT32_MAX / 2) return DG_ERR_SHAPE;
   dg_dims D{};
   D.B = B;
   D.C = C;
@@ -62,21 +70,32 @@ extern "C" dg_status dg_attention_noalloc(const void* q, const void* K, const vo
   D.Hkv = Hkv;
   D.hd = hd;
   int ns = 1, kps = 0;
-  dg::attn_split(D, len + C, len, &ns, &kps);
+  dg::attn_split(D, (int)T, len, &ns, &kps);
   const size_t rows = (size_t)B * Hq * C;
   const size_t part_bytes = dg::align_up((size_t)ns * rows * hd * 4, 256);
   const size_t need = ns > 1 ? part_bytes + (size_t)ns * rows * 8 : 0;
-  if (need > kScratchBytes) return DG_ERR_WORKSPACE;  // larger than the static scratch
+  if (need > kScratchBytes - kStatusBytes) return DG_ERR_WORKSPACE;  // larger than the static scratch
   unsigned char* scratch = nullptr;
   dg_status s = scratch_on_current_device(&scratch);
   if (s != DG_OK) return s;
-  dg::AttnArgs a{q, K, V, k, v, o, reinterpret_cast<float*>(scratch),
-                 reinterpret_cast<float*>(scratch + part_bytes), B, C, Hq, Hkv, hd, len, cap};
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  int* status = reinterpret_cast<int*>(scratch);
+  unsigned char* parts = scratch + kStatusBytes;
+  if (cudaMemsetAsync(status, 0, sizeof(int), st) != cudaSuccess) return DG_ERR_CUDA;
+  dg::AttnArgs a{q, K, V, k, v, o, reinterpret_cast<float*>(parts),
+                 reinterpret_cast<float*>(parts + part_bytes), B, C, Hq, Hkv, hd, len, cap};
   dg::StopCtl none{nullptr, 0, 0};
-  int* status = nullptr;
-  if (cudaGetSymbolAddress(reinterpret_cast<void**>(&status), g_noalloc_status) != cudaSuccess)
+  return dg::launch_attention(a, none, status, st) == cudaSuccess ? DG_OK : DG_ERR_CUDA;
+}
+
+extern "C" dg_status dg_attention_noalloc_status(int32_t* status, void* stream) {
+  if (!status) return DG_ERR_ARG;
+  unsigned char* scratch = nullptr;
+  dg_status s = scratch_on_current_device(&scratch);
+  if (s != DG_OK) return s;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(status, scratch, sizeof(int32_t), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+      cudaStreamSynchronize(st) != cudaSuccess)
     return DG_ERR_CUDA;
-  return dg::launch_attention(a, none, status, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
-             ? DG_OK
-             : DG_ERR_CUDA;
+  return DG_OK;
 }

@@ -24,9 +24,9 @@ _lib = None
 DG_OK, DG_ERR_ARG, DG_ERR_SHAPE, DG_ERR_CAPACITY, DG_ERR_WORKSPACE, DG_ERR_CUDA, DG_ERR_TIMEOUT, DG_ERR_VALUE = range(8)
 
 # Every function the C header declares (checked by the tests).
-EXPORTS = ("dg_status_string", "dg_workspace_size", "dg_read_status", "dg_canvas_init",
+EXPORTS = ("dg_status_string", "dg_workspace_size", "dg_read_status", "dg_tau", "dg_canvas_init",
            "dg_denoise_step", "dg_denoise_canvas", "dg_commit_block", "dg_debug_gemm",
-           "dg_attention_noalloc", "dg_debug_wait_timeout")
+           "dg_attention_noalloc", "dg_attention_noalloc_status", "dg_debug_wait_timeout")
 
 
 class DgError(RuntimeError):
@@ -91,6 +91,8 @@ def load():
                 getattr(L, name).restype = ct.c_int32
             L.dg_workspace_size.argtypes = [ct.POINTER(dg_dims), ct.c_int32, ct.POINTER(ct.c_size_t)]
             L.dg_read_status.argtypes = [ct.c_void_p, ct.POINTER(ct.c_int32), ct.c_void_p]
+            L.dg_tau.argtypes = [ct.POINTER(dg_sched), ct.c_int32, ct.POINTER(ct.c_float)]
+            L.dg_attention_noalloc_status.argtypes = [ct.POINTER(ct.c_int32), ct.c_void_p]
             L.dg_canvas_init.argtypes = [ct.c_void_p, ct.c_int32, ct.c_int32, ct.c_int32, ct.c_uint64,
                                          ct.c_int32, ct.c_void_p]
             L.dg_denoise_step.argtypes = [ct.POINTER(dg_model), ct.POINTER(dg_kv_cache),
@@ -248,8 +250,16 @@ def denoise_step(model: Model, canvas: Canvas, tau: float, b: float, seed: int, 
     return out
 
 
+def tau(step: int, N: int = 48, tau0: float = 0.8, tau1: float = 0.4) -> float:
+    """Temperature of step `step` of the annealed schedule, as the library computes it (dg_tau)."""
+    t = ct.c_float()
+    _check(load().dg_tau(ct.byref(dg_sched(tau0, tau1, N, 0.1, 0.005)), int(step), ct.byref(t)), "dg_tau")
+    return t.value
+
+
 def tau_schedule(N=48, tau0=0.8, tau1=0.4):
-    return [tau0 + (tau1 - tau0) * s / (N - 1) if N > 1 else tau0 for s in range(N)]
+    """Temperatures of steps 0..N-1 (dg_tau for each step)."""
+    return [tau(s, N, tau0, tau1) for s in range(N)]
 
 
 def denoise_canvas(model: Model, canvas: Canvas, seed: int, block: int = 0, N: int = 48, tau0: float = 0.8,
@@ -271,13 +281,22 @@ def denoise_canvas(model: Model, canvas: Canvas, seed: int, block: int = 0, N: i
     return res
 
 
-def commit_block(model: Model, tokens: torch.Tensor, stream=None) -> None:
-    """Append the re-encoded K/V of tokens [B, C] to the cache (dg_commit_block)."""
-    cache = model.cache()
-    rc = load().dg_commit_block(ct.byref(model.s), ct.byref(cache), _ptr(tokens), model.ws_ptr,
+def commit_block(model: Model, tokens: torch.Tensor, stream=None, cache=None) -> int:
+    """Append the re-encoded K/V of tokens [B, C] to the cache (dg_commit_block).
+
+    cache: optional (K, V, len) of another cache with the model's layout ([B, Hkv, cap, hd] bf16);
+    by default the model's own cache, whose length is advanced.  Returns the new length."""
+    if cache is None:
+        cs = model.cache()
+    else:
+        K, V, n = cache
+        cs = dg_kv_cache(ct.c_void_p(K.data_ptr()), ct.c_void_p(V.data_ptr()), K.shape[2], int(n))
+    rc = load().dg_commit_block(ct.byref(model.s), ct.byref(cs), _ptr(tokens), model.ws_ptr,
                                 model.ws_bytes, _stream(stream))
     _check(rc, "dg_commit_block")
-    model.len = cache.len
+    if cache is None:
+        model.len = cs.len
+    return cs.len
 
 
 def canvas_init(B, C, V, seed, block=0, device="cuda", stream=None) -> torch.Tensor:
@@ -314,3 +333,10 @@ def attention_noalloc(q, K, V, cache_len, k, v, o=None, stream=None) -> torch.Te
     _check(load().dg_attention_noalloc(_ptr(q), _ptr(K), _ptr(V), cap, int(cache_len), _ptr(k), _ptr(v), _ptr(o),
                                        B, C, Hq, Hkv, hd, _stream(stream)), "dg_attention_noalloc")
     return o
+
+
+def attention_noalloc_status(stream=None) -> int:
+    """Status word of the last attention_noalloc call on this device (synchronises the stream)."""
+    st = ct.c_int32(-1)
+    _check(load().dg_attention_noalloc_status(ct.byref(st), _stream(stream)), "dg_attention_noalloc_status")
+    return st.value

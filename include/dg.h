@@ -175,6 +175,13 @@ typedef struct dg_sched {
   float b, stop_H;
 } dg_sched;
 
+/* Temperature of step `step` (0 <= step < N) of the schedule: tau0 + (tau1 -
+ * tau0) * step / (N - 1), evaluated in double and rounded to float (tau0 when
+ * N == 1).  dg_denoise_canvas uses exactly this value at each step; callers
+ * that run the loop step by step take theirs from here.  DG_ERR_ARG for a
+ * null pointer, N <= 0, a step outside [0, N) or a non-positive tau.       */
+DG_API dg_status dg_tau(const dg_sched* sched, int32_t step, float* tau);
+
 /* Result of the denoising loop (device buffers):
  *   steps_taken int32 [B]; converged int32 [B] (1 = stopped early);
  *   accepted int32 [B][N] (accepted count per step, -1 after the canvas stopped);
@@ -218,11 +225,16 @@ DG_API dg_status dg_denoise_step(const dg_model* model, const dg_kv_cache* cache
                           void* ws, size_t ws_bytes, dg_step_out* out, void* stream);
 
 /* The annealed denoising loop of one block, [TR] steps 3-4: up to sched->N
- * steps with the linear temperature schedule; each canvas stops on its own
- * when its stop test fires and is left unchanged afterwards; work for steps
- * after every canvas stopped is skipped on the device.  Enqueues everything
- * without synchronising.  canvas->tokens/z must hold the initial canvas
- * (dg_canvas_init, z = 0).                                                 */
+ * steps with the linear temperature schedule (dg_tau); each canvas stops on
+ * its own when its stop test fires and is left unchanged afterwards.
+ * Stopping: when `stream` is not being captured into a CUDA graph, the call
+ * reads a 4-byte count of stopped canvases from the workspace after step 1
+ * (the first step at which the stop test can fire) and every 4 steps after,
+ * synchronising `stream` for each read, and enqueues no further step once
+ * every canvas has stopped.  Under stream capture it enqueues all N steps
+ * without synchronising; their kernels return at once after every canvas
+ * stopped.  canvas->tokens/z must hold the initial canvas (dg_canvas_init,
+ * z = 0).                                                                  */
 DG_API dg_status dg_denoise_canvas(const dg_model* model, const dg_kv_cache* cache, dg_canvas* canvas,
                             const dg_sched* sched, uint64_t seed, int32_t block, void* ws,
                             size_t ws_bytes, dg_canvas_result* result, void* stream);
@@ -248,12 +260,24 @@ DG_API dg_status dg_commit_block(const dg_model* model, dg_kv_cache* cache, cons
  * is allocated.  DG_ERR_WORKSPACE (nothing launched) if the scratch this size
  * needs exceeds 16 MiB, e.g. 2 canvases of 8 heads over 8190 prefix keys (a
  * prefix that is not a multiple of 128 takes the warp-MMA kernel, which splits
- * the keys more finely).  The first call on a device looks up the array's device address
+ * the keys more finely).  DG_ERR_SHAPE (nothing launched) for sizes the step
+ * rejects as well: C > 1024, B*C > 2^20, B*Hq > 65535, len + C > 2^30.
+ * The first call on a device looks up the array's device address
  * (cudaGetSymbolAddress) and should come before any stream capture.  All
- * calls share the array: calls that overlap on the GPU race.              */
+ * calls share the array: calls that overlap on the GPU race.
+ * Failure of a bounded device wait: the array holds a status word that each
+ * call clears on `stream` before its kernels run; a wait that runs out sets it
+ * to DG_ERR_TIMEOUT and leaves `o` unwritten.  The call itself only enqueues
+ * work, so it returns DG_OK in that case: read the word with
+ * dg_attention_noalloc_status after the call.                              */
 DG_API dg_status dg_attention_noalloc(const void* q, const void* K, const void* V, int32_t cap,
                                       int32_t len, const void* k, const void* v, void* o, int32_t B,
                                       int32_t C, int32_t Hq, int32_t Hkv, int32_t hd, void* stream);
+
+/* Status word of the last dg_attention_noalloc call on the current device:
+ * synchronises `stream` and copies the word to *status (DG_OK, or
+ * DG_ERR_TIMEOUT if a bounded wait of that call ran out).  Allocates nothing.  */
+DG_API dg_status dg_attention_noalloc_status(int32_t* status, void* stream);
 
 /* Diagnostics of the tensor-core GEMM engine, used by the tests to check it
  * in isolation (not a step of the method).  D fp32 [M][N] = A B^T with

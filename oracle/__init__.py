@@ -75,6 +75,8 @@ def lib():
             L.or_philox_word.restype = ct.c_uint64
             L.or_uniform_token.argtypes = [ct.c_uint64, ct.c_int32]
             L.or_uniform_token.restype = ct.c_int32
+            L.or_tau.argtypes = [ct.c_double, ct.c_double, ct.c_int32, ct.c_int32]
+            L.or_tau.restype = ct.c_double
             L.or_gumbel.argtypes = [ct.c_uint64]
             L.or_gumbel.restype = ct.c_float
             L.or_gumbel_argmax.argtypes = [_D, ct.c_int64, ct.c_uint64, ct.c_int32, ct.c_int32,
@@ -250,13 +252,15 @@ def denoise_step(dims, w, x, z, alpha, tau, b, seed, step, block=0, prev_argmax=
     w: dict of float32 numpy arrays E, Wq, Wk, Wv, Wo, W1, W2, Kc, Vc.
     x [B, C] int32, z [B, C, d] float32, alpha [B, C] float32.
     rows: optional list of global rows (b * C + i) for the vocabulary stages.
-    want: names of outputs to return (default: everything except logits).
+    want: names of outputs to return (default: everything except logits).  In rows mode the
+    logits are returned for the listed rows only, in their order ([len(rows), V]).
     """
     B, C, d, V, F = dims.B, dims.C, dims.d, dims.V, dims.F
     M, nq, nkv = B * C, dims.Hq * dims.hd, dims.Hkv * dims.hd
     if want is None:
         want = tuple(n for n in _WANT_ALL if n != "logits")
-    shapes = dict(a=(M, d), q=(M, nq), k=(M, nkv), v=(M, nkv), o=(M, nq), h=(M, d), logits=(M, V),
+    nl = M if rows is None else len(rows)
+    shapes = dict(a=(M, d), q=(M, nq), k=(M, nkv), v=(M, nkv), o=(M, nq), h=(M, d), logits=(nl, V),
                   H=(M,), m=(M,), Z=(M,), top2gap=(M,), argmax=(M,), accept=(M,), cum=(M,),
                   rank=(M,), renoise_tok=(M,), sample_tok=(M,), gumbel_gap=(M,), tokens_out=(M,),
                   u=(M, d), g=(M, F), z_out=(M, d), n_acc=(B,), meanH=(B,), stop=(B,))
@@ -289,6 +293,11 @@ def denoise_step(dims, w, x, z, alpha, tau, b, seed, step, block=0, prev_argmax=
     if "accept" in outs:
         outs["accept"] = outs["accept"].astype(bool)
     return outs
+
+
+def tau_schedule(N=48, tau0=0.8, tau1=0.4):
+    """Temperatures of steps 0..N-1 of the linear anneal (or_tau)."""
+    return np.array([lib().or_tau(float(tau0), float(tau1), int(N), s) for s in range(N)])
 
 
 def denoise_canvas(dims, w, x0, alpha, seed, N=48, tau0=0.8, tau1=0.4, b=0.1, stop_H=0.005,

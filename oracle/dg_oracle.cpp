@@ -334,7 +334,7 @@ typedef struct {
 typedef struct {
   // Every pointer may be NULL (not wanted).  Row-indexed arrays are [B*C].
   double *a, *q, *k, *v, *o, *h;       // [B*C][d], [B*C][Hq*hd], [B*C][Hkv*hd] x2, [B*C][Hq*hd], [B*C][d]
-  double* logits;                      // [B*C][V] (full mode only)
+  double* logits;                      // [B*C][V] in full mode, [nrows][V] (rows order) in rows mode
   double *H, *m, *Z, *top2gap;         // per row
   int32_t* argmax;                     // per row
   uint8_t* accept;                     // per row (full mode)
@@ -480,7 +480,7 @@ int or_denoise_step(const or_dims* D, const or_step_in* in, or_step_out* out, co
       for (int64_t j = 0; j < d; ++j) acc += hr[j] * (double)in->E[vv * d + j];
       lrow[vv] = al * acc * inv_sqrt_d;
     }
-    if (out->logits && full) std::memcpy(&out->logits[r * V], lrow.data(), sizeof(double) * V);
+    if (out->logits) std::memcpy(&out->logits[(full ? r : t) * V], lrow.data(), sizeof(double) * V);
     double Hv, mv, Zv, g2;
     int32_t a_m;
     or_row_stats(lrow.data(), V, in->tau, &Hv, &mv, &Zv, &a_m, &g2);
@@ -569,6 +569,15 @@ int or_denoise_step(const or_dims* D, const or_step_in* in, or_step_out* out, co
 }
 
 // -------------------------------------------------------- the canvas loop ---
+// Temperature of step s of the anneal: linear from tau0 at step 0 to tau1 at
+// step N - 1 ([TR] Table 2: 0.8 -> 0.4 over N = 48 steps; the endpoint is
+// reached at the last step).  Pinned by test_oracle_pins.py::
+// test_loop_matches_manual_steps_with_linear_anneal (the loop equals manual
+// steps at the printed temperatures).
+double or_tau(double tau0, double tau1, int32_t N, int32_t s) {
+  return (N > 1) ? tau0 + (tau1 - tau0) * (double)s / (double)(N - 1) : tau0;
+}
+
 // Up to N denoising steps with the temperature annealed linearly from tau0 at
 // step 0 to tau1 at step N-1 ([TR] step 3 and Table 2: N = 48, 0.8 -> 0.4,
 // b = 0.1, stop threshold 0.005); each canvas stops on its own when the stop
@@ -590,7 +599,7 @@ int or_denoise_canvas(const or_dims* D, const float* E, const float* Wq, const f
   for (int64_t bb = 0; bb < B; ++bb) { steps_taken[bb] = 0; converged[bb] = 0; }
   for (int64_t t = 0; t < B * N; ++t) accepted[t] = -1;
   for (int32_t s = 0; s < N; ++s) {
-    double tau = (N > 1) ? tau0 + (tau1 - tau0) * (double)s / (double)(N - 1) : tau0;
+    double tau = or_tau(tau0, tau1, N, s);
     or_step_in in{};
     in.E = E; in.Wq = Wq; in.Wk = Wk; in.Wv = Wv; in.Wo = Wo; in.W1 = W1; in.W2 = W2;
     in.Kc = Kc; in.Vc = Vc; in.x = x; in.z = z; in.alpha = alpha;

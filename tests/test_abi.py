@@ -145,3 +145,35 @@ def test_small_entry_points_validate(dg):
     assert L.dg_attention_noalloc(f, f, f, 100, 50, f, f, f, 1, 16, 2, 1, 96, None) == dg.DG_ERR_SHAPE
     assert L.dg_attention_noalloc(f, f, f, 100, 200, f, f, f, 1, 16, 2, 1, 32, None) == dg.DG_ERR_ARG
     assert L.dg_attention_noalloc(None, f, f, 100, 50, f, f, f, 1, 16, 2, 1, 32, None) == dg.DG_ERR_ARG
+    # sizes the step rejects are rejected here too, before any CUDA call
+    assert L.dg_attention_noalloc(f, f, f, 100, 50, f, f, f, 1, 2048, 2, 1, 32, None) == dg.DG_ERR_SHAPE
+    assert L.dg_attention_noalloc(f, f, f, 100, 50, f, f, f, 2048, 1024, 2, 1, 32, None) == dg.DG_ERR_SHAPE
+    assert L.dg_attention_noalloc(f, f, f, 100, 50, f, f, f, 2, 16, 32768, 1, 32, None) == dg.DG_ERR_SHAPE
+    big = 2 ** 31 - 1
+    assert L.dg_attention_noalloc(f, f, f, big, big - 8, f, f, f, 1, 16, 2, 1, 32, None) == dg.DG_ERR_SHAPE
+    assert L.dg_attention_noalloc_status(None, None) == dg.DG_ERR_ARG
+
+
+def test_tau_schedule_is_the_linear_anneal(dg):
+    """dg_tau: tau0 at step 0, tau1 at step N-1, linear in between ([TR] Table 2: 0.8 -> 0.4 over
+    48 steps); arguments outside the schedule are rejected."""
+    L = dg.load()
+    t = ct.c_float()
+    sched = dg.dg_sched(0.8, 0.4, 48, 0.1, 0.005)
+    got = []
+    for s in range(48):
+        assert L.dg_tau(ct.byref(sched), s, ct.byref(t)) == dg.DG_OK
+        got.append(t.value)
+    assert got[0] == pytest.approx(0.8, abs=1e-7) and got[-1] == pytest.approx(0.4, abs=1e-7)
+    steps = [got[s + 1] - got[s] for s in range(47)]
+    assert max(steps) == pytest.approx(min(steps), abs=1e-6)
+    assert steps[0] == pytest.approx(-0.4 / 47, abs=1e-6)
+    import oracle
+    assert got == pytest.approx(list(oracle.tau_schedule(48, 0.8, 0.4)), abs=1e-7)
+    one = dg.dg_sched(0.7, 0.4, 1, 0.1, 0.005)
+    assert L.dg_tau(ct.byref(one), 0, ct.byref(t)) == dg.DG_OK and t.value == pytest.approx(0.7)
+    for s in (-1, 48):
+        assert L.dg_tau(ct.byref(sched), s, ct.byref(t)) == dg.DG_ERR_ARG
+    assert L.dg_tau(None, 0, ct.byref(t)) == dg.DG_ERR_ARG
+    assert L.dg_tau(ct.byref(sched), 0, None) == dg.DG_ERR_ARG
+    assert L.dg_tau(ct.byref(dg.dg_sched(0.0, 0.4, 48, 0.1, 0.005)), 0, ct.byref(t)) == dg.DG_ERR_ARG

@@ -13,6 +13,9 @@ from parity import (Collect, bf16_to_np, check_argmax, check_close_bf16, check_e
 
 pytestmark = pytest.mark.gpu
 
+# End-to-end entropy bound of the long d = 128 canvas case (see test_long_canvas_entropy_given_h).
+LONG_CANVAS_H_BOUND = 2e-3
+
 RAGGED = synth.Dims(V=1000, d=128, C=40, B=3, Hq=4, Hkv=2, hd=64, F=192, P=100, cap=160)
 # head dim 128 with a prefix that is a multiple of 128: the tensor-core attention kernel, with a partial
 # canvas key block (C = 100) and a 3-head group whose 300 query rows leave a partial third Q tile and an
@@ -77,8 +80,18 @@ def _run_and_compare(dims, seed, tau=0.8, b=0.1, step=0, alpha=None, z_in=None, 
     ck(check_close_bf16, "h", bf16_to_np(dbg["h"]), ref["h"])
     ck(check_logits, dbg["logits"].cpu().numpy(), ref["logits"])
     if entropy_given_h:
-        ck(check_entropy, out["entropy"].cpu().numpy().reshape(-1),
-           _entropy_given_device_h(dims, synth.to_numpy_f32(w), a.numpy(), bf16_to_np(dbg["h"]), tau))
+        Hg = out["entropy"].cpu().numpy().reshape(-1).astype(np.float64)
+        # end to end: the documented bound of this case, with the rows past 1e-3 counted and printed
+        e2e = np.abs(Hg - ref["H"])
+        print(f"parity-report entropy end to end: max {e2e.max():.3e} nats, "
+              f"{int((e2e > 1e-3).sum())} of {e2e.size} rows above 1e-3")
+
+        def e2e_bound():
+            assert e2e.max() <= LONG_CANVAS_H_BOUND, f"entropy end to end {e2e.max():.3e} > {LONG_CANVAS_H_BOUND}"
+        ck(e2e_bound)
+        # given the device's own h: the LM head and the statistics merge, to the stated 1e-3
+        ck(check_entropy, Hg, _entropy_given_device_h(dims, synth.to_numpy_f32(w), a.numpy(), bf16_to_np(dbg["h"]),
+                                                      tau))
     else:
         ck(check_entropy, out["entropy"].cpu().numpy().reshape(-1), ref["H"])
     scale = np.max(np.abs(ref["logits"]), axis=1)
@@ -133,9 +146,10 @@ def test_ragged_step_tensor_core_attention():
 def test_long_canvas_entropy_given_h():
     # 600 rows of a d = 128 model with sharp alpha: a few q / k / v elements round to the other bf16
     # neighbour than the oracle's (fp32 against exact accumulation), which moves h by an ulp in a few
-    # places and the end-to-end entropy by up to ~1.4e-3 nats; every other quantity is compared end to
-    # end, and the entropy against the oracle's statistics of the device's own h (the LM head and the
-    # statistics merge, to 1e-3)
+    # places and the end-to-end entropy by up to ~1.4e-3 nats (the logit scale alpha / (tau sqrt d)
+    # is 2.4x that of the d = 1024 workload).  Every other quantity is compared end to end; the
+    # entropy end to end against LONG_CANVAS_H_BOUND with the rows above 1e-3 counted, and against
+    # the oracle's statistics of the device's own h (the LM head and the statistics merge) to 1e-3.
     dims = synth.Dims(V=1000, d=128, C=300, B=2, Hq=4, Hkv=2, hd=64, F=192, P=64, cap=64)
     _run_and_compare(dims, 14, tau=0.6, entropy_given_h=True)
 

@@ -363,6 +363,39 @@ def test_step_sampler_invariants():
     assert abs(out["meanH"][0] - H.mean()) < 1e-12
 
 
+def test_step_samples_follow_the_tempered_softmax():
+    """a7 as the step composes it: an accepted position takes argmax_v (l_v / tau + G_v), so over many
+    seeds the sampled token of a row is distributed as softmax(l / tau) (the Gumbel-max law applied to
+    the tempered logits, [TR] step 3 samples from p0).  The same draws reject softmax(l): a step that
+    perturbed l instead of l / tau fails here."""
+    from scipy import special, stats
+    dims = synth.Dims(V=8, d=64, C=16, B=1, Hq=2, Hkv=1, hd=32, F=64, P=4)
+    w, x, z, a = _tiny_inputs(torch.float32, alpha=1.0, seed=11, dims=dims)
+    tau, n = 0.4, 600
+    draws = np.empty((n, dims.C), np.int64)
+    logits = None
+    for k in range(n):
+        o = oracle.denoise_step(dims, w, x, z, a, tau=tau, b=0.1, seed=1000 + k, step=0, mirror_bf16=False,
+                                want=("logits", "sample_tok"), nthreads=1)
+        draws[k] = o["sample_tok"]
+        if logits is None:
+            logits = o["logits"]
+        else:
+            assert np.array_equal(logits, o["logits"])  # the seed moves only the noise
+
+    def pvalue(p):
+        stat = 0.0
+        for i in range(dims.C):
+            e = n * p[i]
+            stat += float((((np.bincount(draws[:, i], minlength=dims.V) - e) ** 2) / e).sum())
+        return stats.chi2.sf(stat, dims.C * (dims.V - 1))
+
+    p_tau, p_one = special.softmax(logits / tau, axis=1), special.softmax(logits, axis=1)
+    assert np.abs(p_tau - p_one).max() > 0.2  # the two laws are far apart: the test has power
+    assert pvalue(p_tau) > 1e-4
+    assert pvalue(p_one) < 1e-12
+
+
 def test_step_uniform_logits_accept_nothing():
     # alpha -> 0 makes every logit row uniform: H = log V > b, nothing accepted.
     w, x, z, a = _tiny_inputs(torch.float32, alpha=1e-12)
@@ -388,10 +421,12 @@ def test_step_one_hot_p0_gives_embedding_row():
 
 def test_rows_mode_agrees_with_full_mode():
     w, x, z, a = _tiny_inputs(torch.bfloat16, seed=3)
-    full = oracle.denoise_step(TINY, w, x, z, a, tau=0.7, b=0.1, seed=1, step=1, nthreads=3)
-    rows = [0, 5, 15]
+    full = oracle.denoise_step(TINY, w, x, z, a, tau=0.7, b=0.1, seed=1, step=1, nthreads=3,
+                               want=oracle._WANT_ALL)
+    rows = [15, 0, 5]
     part = oracle.denoise_step(TINY, w, x, z, a, tau=0.7, b=0.1, seed=1, step=1, rows=rows,
-                               want=("H", "argmax", "sample_tok", "z_out"), nthreads=1)
+                               want=("H", "argmax", "sample_tok", "z_out", "logits"), nthreads=1)
+    assert np.array_equal(part["logits"], full["logits"][rows])  # rows mode: logits in the rows' order
     for r in rows:
         assert part["H"][r] == full["H"][r]
         assert part["argmax"][r] == full["argmax"][r]
@@ -433,6 +468,11 @@ def test_loop_matches_manual_steps_with_linear_anneal(golden_dir):
                                  b=table["entropy_budget"], stop_H=table["stop_mean_entropy"])
     taus = [tau0 + (tau1 - tau0) * s / (N - 1) for s in range(N)]
     assert taus[0] == 0.8 and abs(taus[-1] - 0.4) < 1e-15
+    # the oracle's schedule: the printed endpoints, equal steps in between
+    ot = oracle.tau_schedule(48, tau0, tau1)
+    assert ot[0] == tau0 and abs(ot[-1] - tau1) < 1e-15
+    assert np.ptp(np.diff(ot)) < 1e-15 and abs(np.diff(ot)[0] - (tau1 - tau0) / 47) < 1e-15
+    assert np.array_equal(oracle.tau_schedule(N, tau0, tau1), np.array(taus))
     xx, zz, prev = x.copy(), z.copy(), None
     for s in range(N):
         o = oracle.denoise_step(TINY, w, xx, zz, a, tau=taus[s], b=0.1, seed=8, step=s,
