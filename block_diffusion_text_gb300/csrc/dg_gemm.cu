@@ -208,7 +208,7 @@ struct EpiLM {
     static_assert(BN % kStatCols == 0, "a tile holds whole statistics groups");
     const float al = ok ? __ldg(alpha + row) : 1.0f;
     const float c2 = al * coef2;
-    const int NT = stat_stride(V);
+    const int NT = (V + kStatCols - 1) / kStatCols;
 #pragma unroll 1
     for (int g = 0; g < BN / kStatCols; ++g) {
       const int g0 = n0 + g * kStatCols;
@@ -467,11 +467,6 @@ static int num_sms() {
 
 bool make_tmap_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
                   uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer) {
-  return make_tmap_2d_ex(map, base, inner, outer, row_bytes, box_inner, box_outer, false);
-}
-
-bool make_tmap_2d_ex(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
-                     uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, bool f32_plain) {
   typedef CUresult (*EncodeFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
                                const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
@@ -490,9 +485,8 @@ bool make_tmap_2d_ex(CUtensorMap* map, const void* base, uint64_t inner, uint64_
   cuuint64_t strides[1] = {row_bytes};
   cuuint32_t box[2] = {box_inner, box_outer};
   cuuint32_t es[2] = {1, 1};
-  CUresult r = fn(map, f32_plain ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
-                  const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                  f32_plain ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                  box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }

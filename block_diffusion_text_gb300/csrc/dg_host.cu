@@ -98,13 +98,10 @@ dg_status enqueue_step(const StepCtx& c, float tau, float b, float stop_H, uint6
   float2* rope = at<float2>(ws, L.rope);
   const Prof pf{out ? out->events : nullptr, c.st};
 
-  VocabPlan vp{};
-  const bool fused = vocab_plan(D, &vp);
   DG_TRY(pf.mark(DG_PROF_EMBED, 0));
   DG_TRY(launch_embed_rmsnorm(c.canvas->tokens, c.model->E, c.canvas->z, at<void>(ws, L.a),
                               fill_rope ? rope : nullptr, D, M,
-                              P, ctl, status, c.st, fused ? at<int>(ws, L.vsync) : nullptr,
-                              fused ? (int)vocab_sync_ints(D) : 0));
+                              P, ctl, status, c.st));
   DG_TRY(pf.mark(DG_PROF_EMBED, 1));
   DG_TRY(pf.mark(DG_PROF_QKV, 0));
   DG_TRY(launch_qkv(at<void>(ws, L.a), c.model->Wq, c.model->Wk, c.model->Wv, at<void>(ws, L.q),
@@ -122,50 +119,27 @@ dg_status enqueue_step(const StepCtx& c, float tau, float b, float stop_H, uint6
                           0, M, D.d, D.Hq * D.hd, D.C, ctl, status, at<float>(ws, L.gpart), L.gpart_elems,
                           c.st));
   DG_TRY(pf.mark(DG_PROF_OPROJ, 1));
-  const float coef2 = (float)(1.4426950408889634 / (std::sqrt((double)D.d) * (double)tau));
-  const float inv_sqrt_d = (float)(1.0 / std::sqrt((double)D.d));
-  float* logits = (out && out->debug) ? out->debug->logits : nullptr;
-  DG_TRY(pf.mark(DG_PROF_VOCAB, 0));
-  if (fused) {
-    VocabArgs va{};
-    va.h = at<void>(ws, L.h);
-    va.E = c.model->E;
-    va.alpha = c.canvas->alpha;
-    va.coef2 = coef2;
-    va.inv_sqrt_d = inv_sqrt_d;
-    va.pt = at<void>(ws, L.pt);
-    va.pm = at<float>(ws, L.pm);
-    va.pl = at<float>(ws, L.pl);
-    va.pS = at<float>(ws, L.pS);
-    va.pvmax = at<float>(ws, L.pvmax);
-    va.pidx = at<int>(ws, L.pidx);
-    va.logits = logits;
-    va.upart = at<float>(ws, L.upart);
-    va.rref = at<float>(ws, L.rref);
-    va.sync = at<int>(ws, L.vsync);
-    DG_TRY(launch_vocab(va, vp, ctl, status, c.st));
-  } else {
-    LmArgs lm{};
-    lm.h = at<void>(ws, L.h);
-    lm.E = c.model->E;
-    lm.alpha = c.canvas->alpha;
-    lm.coef2 = coef2;
-    lm.inv_sqrt_d = inv_sqrt_d;
-    lm.pt = at<void>(ws, L.pt);
-    lm.pm = at<float>(ws, L.pm);
-    lm.pl = at<float>(ws, L.pl);
-    lm.pS = at<float>(ws, L.pS);
-    lm.pvmax = at<float>(ws, L.pvmax);
-    lm.pidx = at<int>(ws, L.pidx);
-    lm.logits = logits;
-    lm.M = M;
-    lm.V = D.V;
-    lm.d = D.d;
-    DG_TRY(launch_lmhead(lm, ctl, status, c.st));
-  }
-  DG_TRY(pf.mark(DG_PROF_VOCAB, 1));
+  LmArgs lm{};
+  lm.h = at<void>(ws, L.h);
+  lm.E = c.model->E;
+  lm.alpha = c.canvas->alpha;
+  lm.coef2 = (float)(1.4426950408889634 / (std::sqrt((double)D.d) * (double)tau));
+  lm.inv_sqrt_d = (float)(1.0 / std::sqrt((double)D.d));
+  lm.pt = at<void>(ws, L.pt);
+  lm.pm = at<float>(ws, L.pm);
+  lm.pl = at<float>(ws, L.pl);
+  lm.pS = at<float>(ws, L.pS);
+  lm.pvmax = at<float>(ws, L.pvmax);
+  lm.pidx = at<int>(ws, L.pidx);
+  lm.logits = (out && out->debug) ? out->debug->logits : nullptr;
+  lm.M = M;
+  lm.V = D.V;
+  lm.d = D.d;
+  DG_TRY(pf.mark(DG_PROF_LMHEAD, 0));
+  DG_TRY(launch_lmhead(lm, ctl, status, c.st));
+  DG_TRY(pf.mark(DG_PROF_LMHEAD, 1));
   StatsArgs sa{at<float>(ws, L.pm), at<float>(ws, L.pl), at<float>(ws, L.pS), at<float>(ws, L.pvmax),
-               at<int>(ws, L.pidx), NT, M, stat_stride(D.V), at<double>(ws, L.Hd), at<float>(ws, L.lsum),
+               at<int>(ws, L.pidx), NT, M, at<double>(ws, L.Hd), at<float>(ws, L.lsum),
                at<float>(ws, L.rowmax), at<int>(ws, L.amax), out ? out->entropy : nullptr,
                out ? out->argmax : nullptr};
   DG_TRY(pf.mark(DG_PROF_STATS, 0));
@@ -196,58 +170,37 @@ dg_status enqueue_step(const StepCtx& c, float tau, float b, float stop_H, uint6
   DG_TRY(pf.mark(DG_PROF_SAMPLER, 0));
   DG_TRY(launch_sampler(sp, c.st));
   DG_TRY(pf.mark(DG_PROF_SAMPLER, 1));
-  int nsplit;
-  DG_TRY(pf.mark(DG_PROF_GUMBEL, 0));
-  if (fused) {
-    GumbelArgs ga{};
-    ga.pt = at<void>(ws, L.pt);
-    ga.pm = at<float>(ws, L.pm);
-    ga.rowmax = at<float>(ws, L.rowmax);
-    ga.lsum = at<float>(ws, L.lsum);
-    ga.acc = at<uint8_t>(ws, L.acc);
-    ga.amax = at<int>(ws, L.amax);
-    ga.gbest = at<float>(ws, L.gbest);
-    ga.gidx = at<int>(ws, L.gidx);
-    ga.M = M;
-    ga.V = D.V;
-    ga.C = D.C;
-    ga.seed = seed;
-    ga.block = block;
-    ga.step = step;
-    DG_TRY(launch_gumbel(ga, ctl, c.st));
-    nsplit = vp.Q;
-  } else {
-    P0Args p0{};
-    p0.pt = at<void>(ws, L.pt);
-    p0.pm = at<float>(ws, L.pm);
-    p0.rowmax = at<float>(ws, L.rowmax);
-    p0.lsum = at<float>(ws, L.lsum);
-    p0.acc = at<uint8_t>(ws, L.acc);
-    p0.amax = at<int>(ws, L.amax);
-    p0.gbest = at<float>(ws, L.gbest);
-    p0.gidx = at<int>(ws, L.gidx);
-    p0.M = M;
-    p0.V = D.V;
-    p0.C = D.C;
-    p0.seed = seed;
-    p0.block = block;
-    p0.step = step;
-    DG_TRY(launch_p0_gumbel(p0, ctl, c.st));
-    ScArgs sc{};
-    sc.pt = at<void>(ws, L.pt);
-    sc.E = c.model->E;
-    sc.upart = at<float>(ws, L.upart);
-    sc.M = M;
-    sc.V = D.V;
-    sc.d = D.d;
-    sc.nsplit = selfcond_active_splits(D);
-    DG_TRY(launch_selfcond(sc, ctl, status, c.st));
-    nsplit = sc.nsplit;
-  }
-  DG_TRY(pf.mark(DG_PROF_GUMBEL, 1));
-  ReduceArgs ra{at<float>(ws, L.upart), fused ? at<float>(ws, L.rref) : nullptr, at<float>(ws, L.rowmax),
-                at<float>(ws, L.lsum), at<float>(ws, L.gbest), at<int>(ws, L.gidx), at<uint8_t>(ws, L.acc),
-                at<void>(ws, L.u), c.canvas->tokens, status, M, D.d, D.C, D.V, nsplit,
+  P0Args p0{};
+  p0.pt = at<void>(ws, L.pt);
+  p0.pm = at<float>(ws, L.pm);
+  p0.rowmax = at<float>(ws, L.rowmax);
+  p0.lsum = at<float>(ws, L.lsum);
+  p0.acc = at<uint8_t>(ws, L.acc);
+  p0.amax = at<int>(ws, L.amax);
+  p0.gbest = at<float>(ws, L.gbest);
+  p0.gidx = at<int>(ws, L.gidx);
+  p0.M = M;
+  p0.V = D.V;
+  p0.C = D.C;
+  p0.seed = seed;
+  p0.block = block;
+  p0.step = step;
+  DG_TRY(pf.mark(DG_PROF_P0, 0));
+  DG_TRY(launch_p0_gumbel(p0, ctl, c.st));
+  DG_TRY(pf.mark(DG_PROF_P0, 1));
+  ScArgs sc{};
+  sc.pt = at<void>(ws, L.pt);
+  sc.E = c.model->E;
+  sc.upart = at<float>(ws, L.upart);
+  sc.M = M;
+  sc.V = D.V;
+  sc.d = D.d;
+  sc.nsplit = selfcond_active_splits(D);
+  DG_TRY(pf.mark(DG_PROF_SELFCOND, 0));
+  DG_TRY(launch_selfcond(sc, ctl, status, c.st));
+  DG_TRY(pf.mark(DG_PROF_SELFCOND, 1));
+  ReduceArgs ra{at<float>(ws, L.upart), at<float>(ws, L.gbest), at<int>(ws, L.gidx), at<uint8_t>(ws, L.acc),
+                at<void>(ws, L.u), c.canvas->tokens, status, M, D.d, D.C, D.V, sc.nsplit,
                 cdiv(D.V, kGumbelChunk)};
   DG_TRY(pf.mark(DG_PROF_REDUCE, 0));
   DG_TRY(launch_reduce(ra, ctl, c.st));
@@ -315,7 +268,7 @@ int selfcond_splits(const dg_dims& D) {
 
 bool ws_layout(const dg_dims& D, int32_t cap, WsLayout* L) {
   if (cap < 0) return false;
-  const size_t M = (size_t)D.B * D.C, NT = (size_t)stat_stride(D.V);
+  const size_t M = (size_t)D.B * D.C, NT = (size_t)cdiv(D.V, kStatCols);
   // room for the largest split count any prefix length up to cap can use
   const int ns_attn = attn_max_splits(D, cap + D.C);
   const size_t S = (size_t)selfcond_splits(D);
@@ -347,10 +300,7 @@ bool ws_layout(const dg_dims& D, int32_t cap, WsLayout* L) {
   L->rowmax = take(4 * M);
   L->amax = take(4 * M);
   L->acc = take(M);
-  const size_t Qv = (size_t)vocab_q_bound(D);
-  L->upart = take(4 * (S > Qv ? S : Qv) * M * D.d);
-  L->rref = take(4 * Qv * M);
-  L->vsync = take(4 * vocab_sync_ints(D));
+  L->upart = take(4 * S * M * D.d);
   const size_t NC = (size_t)cdiv(D.V, kGumbelChunk);
   L->gbest = take(4 * NC * M);
   L->gidx = take(4 * NC * M);

@@ -21,10 +21,6 @@ constexpr int kAttnKeys = 64;  // keys per attention block
 constexpr int kMaxAttnSplits = 64;
 
 inline int cdiv(int64_t a, int64_t b) { return (int)((a + b - 1) / b); }
-// Row stride (in groups) of the per-(row, 128-column group) statistics: the
-// group count rounded up to a multiple of 4, so that rows are 16-byte aligned
-// for tensor-memory-access copies.  Only the first cdiv(V, 128) are valid.
-__host__ __device__ inline int stat_stride(int V) { return ((V + 127) / 128 + 3) / 4 * 4; }
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Split of the key sequence [prefix ; canvas] of length T (prefix P) into
@@ -44,7 +40,6 @@ struct WsLayout {
   size_t pm, pl, pS, pvmax, pidx;
   size_t Hd, lsum, rowmax, amax, acc;
   size_t upart, gbest, gidx;
-  size_t rref, vsync;         // fused vocabulary kernel: slice references, sync words
   size_t gpart, gpart_elems;  // split-K partials of the small GEMMs
   size_t u, g;
   size_t total;
@@ -81,12 +76,9 @@ cudaError_t set_smem_once(int bytes) {
   return result;
 }
 
-// cuTensorMapEncodeTiled through the runtime's driver entry point: bf16 with
-// the 128-byte swizzle, or (f32_plain) fp32 without swizzle.
+// cuTensorMapEncodeTiled through the runtime's driver entry point.
 bool make_tmap_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
                   uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer);
-bool make_tmap_2d_ex(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
-                     uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, bool f32_plain);
 
 // ------------------------------------------------------------- launchers --
 struct StopCtl {
@@ -157,61 +149,6 @@ struct P0Args {
 };
 cudaError_t launch_p0_gumbel(const P0Args& a, StopCtl ctl, cudaStream_t st);
 
-// ----------------------------------------------- fused vocabulary kernel --
-// One persistent launch runs the LM head (statistics epilogue) and the
-// self-conditioning contraction over the vocabulary in L2-sized chunks, so
-// that E is read from HBM once per step (see dg_vocab.cu).  The plan is
-// derived from the dims and the number of resident CTA pairs.
-struct VocabPlan {
-  int M, V, d, NT, NTs;   // rows, vocabulary, model width, 128-column groups, their row stride
-  int n_mp, n_nt, kd;     // 256-row pairs, 256-column vocabulary tiles, 64-wide K blocks of d
-  int n_dt;               // 256-column tiles of d (contraction outputs)
-  int CH, TPC, nC;        // chunk length (vocabulary entries), tiles per chunk, chunks
-  int Q, n_slots, n_lm;   // vocabulary slices per (pair, d tile), contraction slots, LM items
-  int ncl;                // clusters (CTA pairs) launched
-};
-// Chunk length and the bound on Q that the workspace is sized for (any device);
-// Q is at most kMaxVocabSlices (the reduce kernel's weight table).
-constexpr int kMaxVocabSlices = 64;
-int vocab_chunk(const dg_dims& D);
-int vocab_q_bound(const dg_dims& D);
-// Int32 synchronisation words the fused kernel needs zeroed before each launch.
-size_t vocab_sync_ints(const dg_dims& D);
-// Plan for the current device; false when the shape needs more contraction
-// slots than CTA pairs fit (the two-kernel path then runs instead).
-bool vocab_plan(const dg_dims& D, VocabPlan* P);
-struct VocabArgs {
-  const void* h;         // bf16 [M][d]
-  const void* E;         // bf16 [V][d]
-  const float* alpha;    // [M]
-  float coef2;           // log2(e) / (sqrt(d) tau)
-  float inv_sqrt_d;
-  void* pt;              // bf16 [M][V]: 2^(t - k_g), t = s log2 e, k_g the group's integer reference
-  float *pm, *pl, *pS, *pvmax;
-  int* pidx;             // [M][NT] group statistics (pm = k_g)
-  float* logits;         // optional fp32 [M][V]
-  float* upart;          // fp32 [Q][M][d]: slice sums of 2^(t - R) E
-  float* rref;           // fp32 [Q][M]: the reference R of each slice sum (log2 units)
-  int* sync;             // vocab_sync_ints zeroed ints
-};
-cudaError_t launch_vocab(const VocabArgs& a, const VocabPlan& P, StopCtl ctl, int* status, cudaStream_t st);
-// Gumbel-max search of the accepted rows over the stored tiles of the fused
-// kernel (p0_v = tile_v 2^(k_g - m) / Z), best per 8192-entry chunk.
-struct GumbelArgs {
-  const void* pt;        // bf16 [M][V]
-  const float* pm;       // [M][NT] group references k_g
-  const float* rowmax;   // [M] row maximum m (log2 units)
-  const float* lsum;     // [M] Z
-  const uint8_t* acc;    // [M]
-  const int* amax;       // [M]
-  float* gbest;          // [NC][M]
-  int* gidx;             // [NC][M]
-  int M, V, C;
-  uint64_t seed;
-  int block, step;
-};
-cudaError_t launch_gumbel(const GumbelArgs& a, StopCtl ctl, cudaStream_t st);
-
 // Attention over [prefix ; canvas].
 struct AttnArgs {
   const void* q;            // bf16 [B][Hq][C][hd]
@@ -230,15 +167,13 @@ void attn_split_mma(const dg_dims& D, int T, int* nsplit, int* keys_per_split);
 
 // Misc kernels.
 // A token outside [0, V) is embedded as token 0 and sets DG_ERR_VALUE in *status.
-// zero / zero_n: int32 words the first CTA clears (the fused vocabulary
-// kernel's synchronisation words for this step), or nullptr / 0.
 cudaError_t launch_embed_rmsnorm(const int32_t* tokens, const void* E, const void* z, void* a,
                                  float2* rope, const dg_dims& D, int rows, int P, StopCtl ctl,
-                                 int* status, cudaStream_t st, int* zero = nullptr, int zero_n = 0);
+                                 int* status, cudaStream_t st);
 struct StatsArgs {
   const float *pm, *pl, *pS, *pvmax;
   const int* pidx;
-  int NT, M, NTs;        // valid groups per row, rows, row stride (stat_stride)
+  int NT, M;
   double* Hd;            // [M]
   float* lsum;           // [M]  Z
   float* rowmax;         // [M]  m (log2 units)
@@ -270,9 +205,6 @@ cudaError_t launch_sampler(const SamplerArgs& a, cudaStream_t st);
 
 struct ReduceArgs {
   const float* upart;    // [S][M][d]
-  const float* rref;     // optional [S][M]: split s is weighted 2^(rref - rowmax) / lsum (fused path)
-  const float* rowmax;   // [M] (with rref)
-  const float* lsum;     // [M] (with rref)
   const float* gbest;    // [NC][M]
   const int* gidx;       // [NC][M]
   const uint8_t* acc;

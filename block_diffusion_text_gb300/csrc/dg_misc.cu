@@ -60,12 +60,10 @@ struct RopeTheta {
 __global__ void __launch_bounds__(kEmbThreads)
     embed_rmsnorm_kernel(const int32_t* tokens, const __nv_bfloat16* E, const __nv_bfloat16* z,
                          __nv_bfloat16* a, float2* rope, int d, int V, float eps, int C, int P, int hd,
-                         RopeTheta theta, StopCtl ctl, int* status, int* zero, int zero_n) {
+                         RopeTheta theta, StopCtl ctl, int* status) {
   pdl_wait();
   if (all_stopped(ctl.stop_at, ctl.B, ctl.step)) return;
   const int row = blockIdx.x;
-  if (row == 0)
-    for (int i = threadIdx.x; i < zero_n; i += kEmbThreads) zero[i] = 0;
   int tok = tokens[row];
   if (tok < 0 || tok >= V) {  // never gather outside E: record the bad token, embed token 0
     if (threadIdx.x == 0) atomicExch(status, kStatusValue);
@@ -154,13 +152,13 @@ __global__ void __launch_bounds__(kEmbThreads)
 
 cudaError_t launch_embed_rmsnorm(const int32_t* tokens, const void* E, const void* z, void* a,
                                  float2* rope, const dg_dims& D, int rows, int P, StopCtl ctl,
-                                 int* status, cudaStream_t st, int* zero, int zero_n) {
+                                 int* status, cudaStream_t st) {
   RopeTheta th{};
   for (int j = 0; j < D.hd / 2 && j < 64; ++j) th.th[j] = std::pow((double)D.rope_base, -2.0 * j / D.hd);
   return launch_pdl(embed_rmsnorm_kernel, dim3(rows), dim3(kEmbThreads), 0, st, tokens,
                     reinterpret_cast<const __nv_bfloat16*>(E), reinterpret_cast<const __nv_bfloat16*>(z),
                     reinterpret_cast<__nv_bfloat16*>(a), rope, D.d, D.V, D.rms_eps, D.C, P, D.hd, th, ctl,
-                    status, zero, zero_n);
+                    status);
 }
 
 // ------------------------------------------------------- tile statistics --
@@ -229,7 +227,7 @@ __global__ void __launch_bounds__(kStatsThreads) stats_kernel(StatsArgs a, int w
   const int row = blockIdx.x * (kStatsWarps / wpr) + warp / wpr;
   const bool ok = row < a.M;
   const int t0 = (warp % wpr) * 32 + threadIdx.x % 32, tstep = wpr * 32;
-  const size_t base = (size_t)(ok ? row : 0) * a.NTs;
+  const size_t base = (size_t)(ok ? row : 0) * a.NT;
   __shared__ float shf[kStatsWarps];
   __shared__ int shi[kStatsWarps];
   __shared__ RowSum shr[kStatsWarps];
@@ -321,7 +319,7 @@ __global__ void __launch_bounds__(kP0Threads) p0_gumbel_kernel(P0Args a, StopCtl
   // (two statistics groups of 128 columns, one scale factor each).
   const int wbase = chunk * kGumbelChunk + (threadIdx.x / 32) * 1024;
   const int lane = threadIdx.x % 32;
-  const size_t fbase = (size_t)row * stat_stride(a.V);
+  const size_t fbase = (size_t)row * ((a.V + kStatCols - 1) / kStatCols);
   uint4 x[4];
   float f[4];
 #pragma unroll
@@ -416,109 +414,6 @@ __global__ void __launch_bounds__(kP0Threads) p0_gumbel_kernel(P0Args a, StopCtl
 cudaError_t launch_p0_gumbel(const P0Args& a, StopCtl ctl, cudaStream_t st) {
   dim3 grid(cdiv(a.V, kGumbelChunk), a.M);
   return launch_pdl(p0_gumbel_kernel, grid, dim3(kP0Threads), 0, st, a, ctl);
-}
-
-// ------------------------------------ Gumbel-max over the fused tiles --
-// The fused vocabulary kernel stores 2^(t - k_g) per entry (k_g the integer
-// reference of the entry's 128-column group), so p0_v = tile_v 2^(k_g - m) / Z
-// with m the row maximum of the references.  The accepted rows search
-// argmax_v (log p0_v + G_v) over the stored tiles (nothing is written back);
-// the threshold pruning is the one of p0_gumbel_kernel, seeded at the argmax
-// token's own perturbed score.  One CTA per (row, 8192-entry chunk); rows
-// that were not accepted return at once.
-__global__ void __launch_bounds__(kP0Threads) gumbel_kernel(GumbelArgs a, StopCtl ctl) {
-  pdl_wait();
-  if (all_stopped(ctl.stop_at, ctl.B, ctl.step)) return;
-  const int row = blockIdx.y;
-  const int chunk = blockIdx.x;
-  if (!a.acc[row] || !canvas_active(ctl.stop_at, row / a.C, ctl.step)) return;
-  const __nv_bfloat16* pt = reinterpret_cast<const __nv_bfloat16*>(a.pt) + (size_t)row * a.V;
-  const int canvas = row / a.C, pos = row % a.C;
-  const float* pmr = a.pm + (size_t)row * stat_stride(a.V);
-  const float mrow = a.rowmax[row], invZ = 1.0f / a.lsum[row];
-  const int wbase = chunk * kGumbelChunk + (threadIdx.x / 32) * 1024;
-  const int lane = threadIdx.x % 32;
-  uint4 x[4];
-  float f[4];
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const int v = wbase + (q * 32 + lane) * 8;
-    if (v < a.V) {  // V is a multiple of 8
-      x[q] = *reinterpret_cast<const uint4*>(pt + v);
-      f[q] = pmr[v / kStatCols];
-    }
-  }
-  // the argmax token's probability from its stored entry, its perturbed
-  // score, and the p0 threshold below which no entry can beat it
-  const int va = a.amax[row];
-  const float pa = __bfloat162float(pt[va]) * exp2f(pmr[va / kStatCols] - mrow) * invZ;
-  uint64_t wa[4];
-  philox_block(wa, a.seed, a.block, a.step, canvas, pos, va >> 2, 0);
-  const float thr = expf(logf(pa) + gumbel_from_word(wa[va & 3]) - kGumbelMaxDraw - 0.02f);
-#pragma unroll
-  for (int q = 0; q < 4; ++q) f[q] = exp2f(f[q] - mrow) * invZ;  // 2^(k_g - m) / Z
-  float best = -FLT_MAX;
-  int bidx = INT_MAX;
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const int vq = wbase + (q * 32 + lane) * 8;
-    if (vq >= a.V) break;
-    const __nv_bfloat16* xb = reinterpret_cast<const __nv_bfloat16*>(&x[q]);
-    float p[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) p[e] = __bfloat162float(xb[e]) * f[q];
-#pragma unroll
-    for (int g4 = 0; g4 < 2; ++g4) {
-      bool any = false;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) any |= p[g4 * 4 + e] >= thr;
-      if (!any) continue;
-      uint64_t w[4];
-      philox_block(w, a.seed, a.block, a.step, canvas, pos, (vq + g4 * 4) >> 2, 0);
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float pv = p[g4 * 4 + e];
-        if (pv >= thr && pv > 0.f) {
-          const float sc = logf(pv) + gumbel_from_word(w[e]);
-          if (sc > best) {
-            best = sc;
-            bidx = vq + g4 * 4 + e;
-          }
-        }
-      }
-    }
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float b2 = __shfl_xor_sync(0xffffffffu, best, o);
-    const int i2 = __shfl_xor_sync(0xffffffffu, bidx, o);
-    if (b2 > best || (b2 == best && i2 < bidx)) {
-      best = b2;
-      bidx = i2;
-    }
-  }
-  __shared__ float sb[kP0Threads / 32];
-  __shared__ int si[kP0Threads / 32];
-  if (threadIdx.x % 32 == 0) {
-    sb[threadIdx.x / 32] = best;
-    si[threadIdx.x / 32] = bidx;
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    for (int k = 1; k < kP0Threads / 32; ++k) {
-      if (sb[k] > best || (sb[k] == best && si[k] < bidx)) {
-        best = sb[k];
-        bidx = si[k];
-      }
-    }
-    a.gbest[(size_t)chunk * a.M + row] = best;
-    a.gidx[(size_t)chunk * a.M + row] = bidx;
-  }
-}
-
-cudaError_t launch_gumbel(const GumbelArgs& a, StopCtl ctl, cudaStream_t st) {
-  dim3 grid(cdiv(a.V, kGumbelChunk), a.M);
-  return launch_pdl(gumbel_kernel, grid, dim3(kP0Threads), 0, st, a, ctl);
 }
 
 // --------------------------------------------------------------- sampler --
@@ -670,16 +565,6 @@ __global__ void __launch_bounds__(256) reduce_kernel(ReduceArgs a, StopCtl ctl) 
   const int n4 = a.d / 4;
   const size_t sstride = (size_t)a.M * a.d;
   const float* src = a.upart + (size_t)row * a.d;
-  // per-split weights: 1, or (fused path) 2^(R_s - m) / Z for a split summed
-  // relative to its own reference R_s
-  __shared__ float wsp[64];
-  if (a.rref) {
-    if (threadIdx.x < a.nsplit) {
-      const float r = a.rref[(size_t)threadIdx.x * a.M + row];
-      wsp[threadIdx.x] = r > -1e29f ? exp2f(r - a.rowmax[row]) / a.lsum[row] : 0.f;
-    }
-    __syncthreads();
-  }
   for (int c = threadIdx.x; c < n4; c += blockDim.x) {
     // four splits at a time: independent loads in flight
     float4 acc[4];
@@ -690,20 +575,18 @@ __global__ void __launch_bounds__(256) reduce_kernel(ReduceArgs a, StopCtl ctl) 
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         const float4 v = *reinterpret_cast<const float4*>(src + (s + k) * sstride + 4 * c);
-        const float w = a.rref ? wsp[s + k] : 1.f;
-        acc[k].x = fmaf(w, v.x, acc[k].x);
-        acc[k].y = fmaf(w, v.y, acc[k].y);
-        acc[k].z = fmaf(w, v.z, acc[k].z);
-        acc[k].w = fmaf(w, v.w, acc[k].w);
+        acc[k].x += v.x;
+        acc[k].y += v.y;
+        acc[k].z += v.z;
+        acc[k].w += v.w;
       }
     }
     for (; s < a.nsplit; ++s) {
       const float4 v = *reinterpret_cast<const float4*>(src + s * sstride + 4 * c);
-      const float w = a.rref ? wsp[s] : 1.f;
-      acc[0].x = fmaf(w, v.x, acc[0].x);
-      acc[0].y = fmaf(w, v.y, acc[0].y);
-      acc[0].z = fmaf(w, v.z, acc[0].z);
-      acc[0].w = fmaf(w, v.w, acc[0].w);
+      acc[0].x += v.x;
+      acc[0].y += v.y;
+      acc[0].z += v.z;
+      acc[0].w += v.w;
     }
     const float x = (acc[0].x + acc[1].x) + (acc[2].x + acc[3].x);
     const float y = (acc[0].y + acc[1].y) + (acc[2].y + acc[3].y);

@@ -26,8 +26,7 @@ DG_OK, DG_ERR_ARG, DG_ERR_SHAPE, DG_ERR_CAPACITY, DG_ERR_WORKSPACE, DG_ERR_CUDA,
 # Every function the C header declares (checked by the tests).
 EXPORTS = ("dg_status_string", "dg_workspace_size", "dg_read_status", "dg_tau", "dg_canvas_init",
            "dg_denoise_step", "dg_denoise_canvas", "dg_commit_block", "dg_debug_gemm",
-           "dg_attention_noalloc", "dg_attention_noalloc_status", "dg_debug_wait_timeout",
-           "dg_vocab_plan_info")
+           "dg_attention_noalloc", "dg_attention_noalloc_status", "dg_debug_wait_timeout")
 
 
 class DgError(RuntimeError):
@@ -65,7 +64,8 @@ class dg_step_out(ct.Structure):
 
 
 # Kernel slots of one step (dg_step_out.events), in launch order.
-PROF_SLOTS = ("embed", "qkv", "attn", "oproj", "vocab", "stats", "sampler", "gumbel", "reduce", "ffw1", "ffw2")
+PROF_SLOTS = ("embed", "qkv", "attn", "oproj", "lmhead", "stats", "sampler", "p0", "selfcond",
+              "reduce", "ffw1", "ffw2")
 
 
 class dg_sched(ct.Structure):
@@ -93,7 +93,6 @@ def load():
             L.dg_read_status.argtypes = [ct.c_void_p, ct.POINTER(ct.c_int32), ct.c_void_p]
             L.dg_tau.argtypes = [ct.POINTER(dg_sched), ct.c_int32, ct.POINTER(ct.c_float)]
             L.dg_attention_noalloc_status.argtypes = [ct.POINTER(ct.c_int32), ct.c_void_p]
-            L.dg_vocab_plan_info.argtypes = [ct.POINTER(dg_dims), ct.POINTER(ct.c_int32)]
             L.dg_canvas_init.argtypes = [ct.c_void_p, ct.c_int32, ct.c_int32, ct.c_int32, ct.c_uint64,
                                          ct.c_int32, ct.c_void_p]
             L.dg_denoise_step.argtypes = [ct.POINTER(dg_model), ct.POINTER(dg_kv_cache),
@@ -341,14 +340,3 @@ def attention_noalloc_status(stream=None) -> int:
     st = ct.c_int32(-1)
     _check(load().dg_attention_noalloc_status(ct.byref(st), _stream(stream)), "dg_attention_noalloc_status")
     return st.value
-
-
-VOCAB_PLAN_KEYS = ("fused", "pairs", "slots", "slices", "chunk", "chunks", "lm_tiles", "row_pairs", "d_tiles",
-                   "k_blocks")
-
-
-def vocab_plan(dims) -> dict:
-    """Work plan of the fused vocabulary kernel on the current device (dg_vocab_plan_info)."""
-    info = (ct.c_int32 * 10)()
-    _check(load().dg_vocab_plan_info(ct.byref(make_dims(dims)), info), "dg_vocab_plan_info")
-    return dict(zip(VOCAB_PLAN_KEYS, list(info)))

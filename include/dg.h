@@ -130,18 +130,15 @@ enum {
   DG_PROF_QKV = 1,       /* q, k, v projections with RoPE             */
   DG_PROF_ATTN = 2,      /* attention over prefix + canvas (+ merge)  */
   DG_PROF_OPROJ = 3,     /* output projection + residual              */
-  DG_PROF_VOCAB = 4,     /* LM head with softmax statistics, fused with
-                            the contraction p0 . E (E read once)      */
+  DG_PROF_LMHEAD = 4,    /* LM head with softmax statistics           */
   DG_PROF_STATS = 5,     /* merge of the statistics: entropy, argmax  */
   DG_PROF_SAMPLER = 6,   /* sort, cumulative entropy, accept, renoise */
-  DG_PROF_GUMBEL = 7,    /* Gumbel-max search of the accepted rows (on
-                            the two-kernel path, for shapes the fused
-                            kernel does not fit: the p0 pass and the
-                            contraction p0 . E)                       */
-  DG_PROF_REDUCE = 8,    /* reduction of p0 . E, sampled tokens        */
-  DG_PROF_FFW1 = 9,      /* GELU(W1 u)                                */
-  DG_PROF_FFW2 = 10,     /* z = W2 g                                  */
-  DG_PROF_NUM = 11
+  DG_PROF_P0 = 7,        /* tiles -> p0 in place; Gumbel-max search   */
+  DG_PROF_SELFCOND = 8,  /* p0 . E on the tensor cores                */
+  DG_PROF_REDUCE = 9,    /* reduction of p0 . E, sampled tokens        */
+  DG_PROF_FFW1 = 10,     /* GELU(W1 u)                                */
+  DG_PROF_FFW2 = 11,     /* z = W2 g                                  */
+  DG_PROF_NUM = 12
 };
 
 /* Per-step outputs (device; any pointer may be NULL except where noted):
@@ -296,13 +293,6 @@ DG_API dg_status dg_attention_noalloc_status(int32_t* status, void* stream);
  * caller sees DG_ERR_TIMEOUT and the context stays usable.  The tests use it
  * to check that path without a device fault.                                  */
 DG_API dg_status dg_debug_wait_timeout(int32_t* status, void* stream);
-
-/* Diagnostics (not a step of the method): the work plan of the fused
- * vocabulary kernel for `dims` on the current device.  info receives 10
- * int32: fused (1) or two-kernel path (0), CTA pairs launched, contraction
- * slots, vocabulary slices per slot tile, chunk length, chunks, LM tiles, row
- * pairs, d tiles, K blocks of d.                                              */
-DG_API dg_status dg_vocab_plan_info(const dg_dims* dims, int32_t* info);
 
 DG_API dg_status dg_debug_gemm(const void* A, const void* Bm, float* D, int32_t M, int32_t N, int32_t K,
                         int32_t b_mn_major, void* stream);
