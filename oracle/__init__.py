@@ -52,7 +52,7 @@ class StepIn(ct.Structure):
     _fields_ = [("E", _F), ("Wq", _F), ("Wk", _F), ("Wv", _F), ("Wo", _F), ("W1", _F), ("W2", _F),
                 ("Kc", _F), ("Vc", _F), ("x", _I), ("z", _F), ("alpha", _F), ("prev_argmax", _I),
                 ("tau", ct.c_double), ("b", ct.c_double), ("stop_H", ct.c_double),
-                ("seed", ct.c_uint64), ("step", ct.c_int32), ("block", ct.c_int32)]
+                ("seed", ct.c_uint64), ("step", ct.c_int32), ("block", ct.c_int32), ("exclude_tok", ct.c_int32)]
 
 
 class StepOut(ct.Structure):
@@ -75,6 +75,8 @@ def lib():
             L.or_philox_word.restype = ct.c_uint64
             L.or_uniform_token.argtypes = [ct.c_uint64, ct.c_int32]
             L.or_uniform_token.restype = ct.c_int32
+            L.or_reveal.argtypes = [_D, _I, _I, ct.c_int32, ct.c_int32, ct.c_int32, ct.c_int32, _U8]
+            L.or_reveal.restype = ct.c_int32
             L.or_tau.argtypes = [ct.c_double, ct.c_double, ct.c_int32, ct.c_int32]
             L.or_tau.restype = ct.c_double
             L.or_gumbel.argtypes = [ct.c_uint64]
@@ -219,6 +221,41 @@ def accept(H, b):
     return dict(n=int(n), accept=acc.astype(bool), cum=cum, rank=rank)
 
 
+def reveal(Z, argmax, tokens, mask_id, step, N):
+    """Masked confidence decoding of one step (or_reveal): returns (new tokens, revealed mask, k)."""
+    Zh = np.ascontiguousarray(np.asarray(Z, dtype=np.float64))
+    am = np.ascontiguousarray(np.asarray(argmax, dtype=np.int32))
+    tok = np.ascontiguousarray(np.asarray(tokens, dtype=np.int32)).copy()
+    rev = np.zeros(Zh.size, dtype=np.uint8)
+    k = lib().or_reveal(_p(Zh, _D), _p(am, _I), _p(tok, _I), Zh.size, int(mask_id), int(step), int(N), _p(rev, _U8))
+    if k < 0:
+        raise ValueError("oracle reveal: bad arguments")
+    return tok, rev.astype(bool), int(k)
+
+
+def denoise_step_masked(dims, w, x, z, alpha, tau, mask_id, step, N, mirror_bf16=True, nthreads=None,
+                        want_extra=()):
+    """One step of masked confidence decoding: the forward and self-conditioning of denoise_step
+    with the [MASK] token excluded from the softmax (not a prediction target), then or_reveal per
+    canvas in place of the uniform-state accept / renoise."""
+    out = denoise_step(dims, w, x, z, alpha, tau=tau, b=0.0, seed=0, step=0, mirror_bf16=mirror_bf16,
+                       want=("H", "Z", "m", "argmax", "top2gap", "z_out", "u") + tuple(want_extra),
+                       nthreads=nthreads, exclude_tok=mask_id)
+    B, C = dims.B, dims.C
+    tok = np.asarray(x, np.int32).reshape(B, C).copy()
+    rev = np.zeros((B, C), bool)
+    ks = []
+    for bb in range(B):
+        t, r, k = reveal(out["Z"][bb * C:(bb + 1) * C], out["argmax"][bb * C:(bb + 1) * C], tok[bb], mask_id,
+                         step, N)
+        tok[bb], rev[bb] = t, r
+        ks.append(k)
+    out["tokens_out"] = tok.reshape(-1)
+    out["revealed"] = rev.reshape(-1)
+    out["n_rev"] = np.array(ks, np.int32)
+    return out
+
+
 def attend_row(q, Kp, Vp, Kc, Vc):
     q = np.ascontiguousarray(np.asarray(q, dtype=np.float64))
     hd = q.size
@@ -245,7 +282,7 @@ _WANT_ALL = ("a", "q", "k", "v", "o", "h", "logits", "H", "m", "Z", "top2gap", "
 
 
 def denoise_step(dims, w, x, z, alpha, tau, b, seed, step, block=0, prev_argmax=None,
-                 stop_H=0.005, mirror_bf16=True, rows=None, want=None, nthreads=None):
+                 stop_H=0.005, mirror_bf16=True, rows=None, want=None, nthreads=None, exclude_tok=-1):
     """Run one oracle denoising step.
 
     dims: an object with V, d, C, B, Hq, Hkv, hd, F, P, cap, rope_base, rms_eps.
@@ -279,7 +316,7 @@ def denoise_step(dims, w, x, z, alpha, tau, b, seed, step, block=0, prev_argmax=
     pa = _i32(prev_argmax) if prev_argmax is not None else None
     si = StepIn(*[_p(a, _F) for a in keep], _p(xx, _I), _p(zz, _F), _p(aa, _F),
                 _p(pa, _I) if pa is not None else None, float(tau), float(b), float(stop_H),
-                int(seed), int(step), int(block))
+                int(seed), int(step), int(block), int(exclude_tok))
     rr = _i32(rows) if rows is not None else None
     nrows = 0 if rr is None else rr.size
     if rr is not None and rr.size == 0:

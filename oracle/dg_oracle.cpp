@@ -238,8 +238,10 @@ void or_row_stats(const double* l, int64_t V, double tau, double* H, double* m_o
   for (int64_t v = 0; v < V; ++v) {
     double t = l[v] / tau - m;
     double e = std::exp(t);
-    Z += e;
-    S += e * t;
+    if (e > 0.0) {  // an excluded entry (l = -inf) has p = 0 and adds nothing
+      Z += e;
+      S += e * t;
+    }
   }
   if (H) *H = std::log(Z) - S / Z;
   if (m_out) *m_out = m;
@@ -329,6 +331,10 @@ typedef struct {
   double tau, b, stop_H;
   uint64_t seed;
   int32_t step, block;
+  // token excluded from the softmax (its logit taken as -inf), or -1: the
+  // [MASK] token of masked confidence decoding, which is not a prediction
+  // target
+  int32_t exclude_tok;
 } or_step_in;
 
 typedef struct {
@@ -481,6 +487,7 @@ int or_denoise_step(const or_dims* D, const or_step_in* in, or_step_out* out, co
       lrow[vv] = al * acc * inv_sqrt_d;
     }
     if (out->logits) std::memcpy(&out->logits[(full ? r : t) * V], lrow.data(), sizeof(double) * V);
+    if (in->exclude_tok >= 0 && in->exclude_tok < V) lrow[in->exclude_tok] = -INFINITY;
     double Hv, mv, Zv, g2;
     int32_t a_m;
     or_row_stats(lrow.data(), V, in->tau, &Hv, &mv, &Zv, &a_m, &g2);
@@ -566,6 +573,42 @@ int or_denoise_step(const or_dims* D, const or_step_in* in, or_step_out* out, co
     if (out->stop) out->stop[bb] = st;
   }
   return 0;
+}
+
+// ------------------------------------------- masked confidence decoding ---
+// The second sampler, masked confidence decoding ([P4] "从零拆开DiffusionGemma",
+// the generate() of its fourth step): the canvas starts as [MASK] everywhere;
+// each of N steps predicts every position, takes the confidence of a position
+// as the largest tempered probability max_v p0_v = 1 / Z (Z = sum_v
+// exp(s_v - max s)) and its candidate as the argmax, and reveals the
+// k = min(ceil(U / (N - step)), U) still-masked positions of highest
+// confidence (U of them still masked), writing their candidates; revealed
+// positions never change again, so after step N - 1 nothing is masked.
+// Readings: ties in confidence go to the lower position; the candidate is the
+// argmax with the lowest index on ties.
+// Z[C], argmax[C], tokens[C] (updated in place), mask_id, step, N.  Fills
+// revealed[i] = 1 for the positions revealed by this step.  Returns k, or -1
+// on bad arguments.  Pinned by test_oracle_pins.py::test_reveal_matches_topk
+// and test_reveal_loop_invariants.
+int32_t or_reveal(const double* Z, const int32_t* argmax, int32_t* tokens, int32_t C, int32_t mask_id,
+                  int32_t step, int32_t N, uint8_t* revealed) {
+  if (C <= 0 || N <= 0 || step < 0 || step >= N) return -1;
+  std::vector<int32_t> idx;
+  for (int32_t i = 0; i < C; ++i) {
+    revealed[i] = 0;
+    if (tokens[i] == mask_id) idx.push_back(i);
+  }
+  const int32_t U = (int32_t)idx.size();
+  const int32_t remaining = N - step;
+  int32_t k = (U + remaining - 1) / remaining;
+  if (k > U) k = U;
+  // highest confidence first: smallest Z (confidence 1 / Z), then lower position
+  std::stable_sort(idx.begin(), idx.end(), [&](int32_t a, int32_t b) { return Z[a] < Z[b]; });
+  for (int32_t t = 0; t < k; ++t) {
+    tokens[idx[t]] = argmax[idx[t]];
+    revealed[idx[t]] = 1;
+  }
+  return k;
 }
 
 // -------------------------------------------------------- the canvas loop ---

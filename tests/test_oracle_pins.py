@@ -505,3 +505,88 @@ def test_commit_appends_reencoded_kv():
             assert np.allclose(Vc[bb, 0, 32 + i], v[bb, i], atol=1e-6)
     with pytest.raises(ValueError):
         oracle.commit(dims, w["E"], w["Wk"], w["Wv"], toks, w["Kc"], w["Vc"], P=60)
+
+
+# ------------------------------------------- masked confidence decoding ---
+def test_reveal_matches_topk():
+    """or_reveal reveals the k = min(ceil(U / (N - step)), U) still-masked positions of highest
+    confidence 1 / Z with their argmax candidates: compared with torch.topk over the confidences
+    (resolved positions at -1, the form of the pages' generate()), on random canvases with distinct
+    confidences."""
+    rng = np.random.default_rng(7)
+    C, V, mask = 64, 1000, 999
+    for trial in range(200):
+        N = int(rng.integers(1, 12))
+        step = int(rng.integers(0, N))
+        tokens = rng.integers(0, V - 1, size=C).astype(np.int32)
+        tokens[rng.random(C) < rng.random()] = mask
+        Z = 1.0 + rng.random(C) * 50.0
+        am = rng.integers(0, V - 1, size=C).astype(np.int32)
+        new, rev, k = oracle.reveal(Z, am, tokens, mask, step, N)
+        unresolved = tokens == mask
+        U = int(unresolved.sum())
+        assert k == min(math.ceil(U / (N - step)), U)
+        conf = torch.from_numpy(np.where(unresolved, 1.0 / Z, -1.0))
+        want = tokens.copy()
+        if k:
+            chosen = conf.topk(k).indices.numpy()
+            want[chosen] = am[chosen]
+        assert np.array_equal(new, want)
+        assert set(np.nonzero(rev)[0]) == (set(chosen.tolist()) if k else set())
+
+
+def test_reveal_ties_and_edges():
+    # equal confidences: the lower position first; nothing masked: nothing changes; the last
+    # step reveals every remaining position
+    Z = np.array([2.0, 1.0, 1.0, 3.0, 1.0])
+    am = np.array([10, 11, 12, 13, 14], np.int32)
+    tok = np.full(5, 99, np.int32)
+    new, rev, k = oracle.reveal(Z, am, tok, 99, 3, 5)  # ceil(5 / 2) = 3
+    assert k == 3 and new.tolist() == [99, 11, 12, 99, 14]
+    new2, rev2, k2 = oracle.reveal(Z, am, new, 99, 4, 5)
+    assert k2 == 2 and (new2 != 99).all()
+    same, rev3, k3 = oracle.reveal(Z, am, new2, 99, 0, 5)
+    assert k3 == 0 and np.array_equal(same, new2) and not rev3.any()
+
+
+def test_reveal_loop_invariants():
+    """The masked loop through the oracle's step: every step reveals ceil(U / (N - step)) positions,
+    revealed positions keep their tokens, nothing is masked after the last step, and each revealed
+    token is the argmax of its position at the step that revealed it."""
+    dims = synth.Dims(V=512, d=64, C=16, B=2, Hq=2, Hkv=1, hd=32, F=128, P=32)
+    w, x, z, a = _tiny_inputs(torch.bfloat16, seed=4, dims=dims)
+    mask = dims.V - 1
+    N = 5
+    tok = np.full((dims.B, dims.C), mask, np.int32)
+    zz = np.zeros_like(z)
+    for s in range(N):
+        o = oracle.denoise_step_masked(dims, w, tok, zz, a, tau=0.8, mask_id=mask, step=s, N=N)
+        new = o["tokens_out"].reshape(dims.B, dims.C)
+        for bb in range(dims.B):
+            U = int((tok[bb] == mask).sum())
+            assert o["n_rev"][bb] == math.ceil(U / (N - s))
+            kept = tok[bb] != mask
+            assert np.array_equal(new[bb][kept], tok[bb][kept])
+            r = o["revealed"].reshape(dims.B, dims.C)[bb]
+            assert np.array_equal(new[bb][r], o["argmax"].reshape(dims.B, dims.C)[bb][r])
+        tok = new
+        zz = o["z_out"].astype(np.float32).reshape(z.shape)
+    assert (tok != mask).all()
+
+
+def test_excluded_token_is_removed_from_the_softmax():
+    """exclude_tok: the row statistics and p0 . E equal those of the softmax over the other tokens
+    (scipy softmax of the logits with that entry removed); the logits output keeps the raw value."""
+    from scipy import special, stats
+    w, x, z, a = _tiny_inputs(torch.float32, seed=5)
+    tau, ex = 0.7, 37
+    out = oracle.denoise_step(TINY, w, x, z, a, tau=tau, b=0.1, seed=1, step=0, mirror_bf16=False,
+                              want=("logits", "H", "Z", "argmax", "u"), exclude_tok=ex)
+    l = out["logits"]
+    keep = np.arange(TINY.V) != ex
+    p = special.softmax(l[:, keep] / tau, axis=1)
+    assert np.allclose(out["H"], stats.entropy(p, axis=1), atol=1e-10)
+    assert np.allclose(out["u"], p @ w["E"].astype(np.float64)[keep], atol=1e-12)
+    am = np.argmax(l[:, keep], axis=1)
+    assert np.array_equal(out["argmax"], np.where(am >= ex, am + 1, am))
+    assert np.allclose(1.0 / out["Z"], p.max(axis=1), rtol=1e-12)
