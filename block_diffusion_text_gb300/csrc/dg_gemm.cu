@@ -201,6 +201,7 @@ struct EpiLM {
   int* pidx;
   float* logits;
   int M, V;
+  int excl;  // vocabulary column left out of the softmax (the [MASK] token), or -1
   // Statistics per group of kStatCols columns, so that a tile may be 128 or
   // 256 columns wide.
   template <int BN, class LD>
@@ -222,7 +223,7 @@ struct EpiLM {
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
           const int col = g0 + c * 32 + j;
-          if (col < N && v[j] > vmax) {
+          if (col < N && col != excl && v[j] > vmax) {
             vmax = v[j];
             imax = col;
           }
@@ -239,8 +240,8 @@ struct EpiLM {
 #pragma unroll
         for (int j = 0; j < 32; j += 2) {
           const float t0 = fmaf(v[j], c2, -m2), t1 = fmaf(v[j + 1], c2, -m2);
-          const float p0 = (col0 + j < N) ? exp2f(t0) : 0.f;
-          const float p1 = (col0 + j + 1 < N) ? exp2f(t1) : 0.f;
+          const float p0 = (col0 + j < N && col0 + j != excl) ? exp2f(t0) : 0.f;
+          const float p1 = (col0 + j + 1 < N && col0 + j + 1 != excl) ? exp2f(t1) : 0.f;
           l += p0 + p1;
           S = fmaf(p0, t0, fmaf(p1, t1, S));
           pk[j / 2] = pack_bf16(p0, p1);
@@ -984,7 +985,7 @@ cudaError_t launch_lmhead(const LmArgs& a, StopCtl ctl, int* status, cudaStream_
       !tmap_kmajor(&mBh, a.E, a.V, a.d, kLmBN / 4))
     return cudaErrorInvalidValue;
   EpiLM epi{a.alpha, a.coef2, a.inv_sqrt_d, reinterpret_cast<__nv_bfloat16*>(a.pt), a.pm, a.pl,
-            a.pS, a.pvmax, a.pidx, a.logits, a.M, a.V};
+            a.pS, a.pvmax, a.pidx, a.logits, a.M, a.V, a.excl};
   return run_gemm_pair<kLmBN, 7, false, EpiLM, true>(mA, mB, mBh, a.M, a.V, a.d, 1, epi, status, ctl, st);
 }
 

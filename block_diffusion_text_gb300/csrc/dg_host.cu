@@ -86,8 +86,12 @@ struct Prof {
 // All kernels of one denoising step, in order, on ctx.st.
 // fill_rope: (re)compute the RoPE table of positions P + i; a canvas loop
 // fills it at its first step only (P is fixed for the loop).
+// mask_id >= 0 selects masked confidence decoding (the [MASK] token left out
+// of the softmax, the reveal kernel in place of the sampler); -1 the
+// uniform-state sampler.
 dg_status enqueue_step(const StepCtx& c, float tau, float b, float stop_H, uint64_t seed, int step,
-                       int block, const dg_step_out* out, int* accepted_log, int N, bool fill_rope) {
+                       int block, const dg_step_out* out, int* accepted_log, int N, bool fill_rope,
+                       int mask_id = -1) {
   const dg_dims& D = c.model->dims;
   const WsLayout& L = c.L;
   void* ws = c.ws;
@@ -135,6 +139,7 @@ dg_status enqueue_step(const StepCtx& c, float tau, float b, float stop_H, uint6
   lm.M = M;
   lm.V = D.V;
   lm.d = D.d;
+  lm.excl = mask_id;
   DG_TRY(pf.mark(DG_PROF_LMHEAD, 0));
   DG_TRY(launch_lmhead(lm, ctl, status, c.st));
   DG_TRY(pf.mark(DG_PROF_LMHEAD, 1));
@@ -168,7 +173,14 @@ dg_status enqueue_step(const StepCtx& c, float tau, float b, float stop_H, uint6
   sp.accepted_log = accepted_log;
   sp.N = N;
   DG_TRY(pf.mark(DG_PROF_SAMPLER, 0));
-  DG_TRY(launch_sampler(sp, c.st));
+  if (mask_id < 0) {
+    DG_TRY(launch_sampler(sp, c.st));
+  } else {
+    RevealArgs rv{at<double>(ws, L.Hd), at<float>(ws, L.lsum), at<int>(ws, L.amax), c.canvas->prev_argmax,
+                  c.canvas->tokens, at<uint8_t>(ws, L.acc), sp.acc_out, sp.n_acc, sp.mean_H, sp.stop,
+                  accepted_log, D.B, D.C, mask_id, step, N};
+    DG_TRY(launch_reveal(rv, c.st));
+  }
   DG_TRY(pf.mark(DG_PROF_SAMPLER, 1));
   P0Args p0{};
   p0.pt = at<void>(ws, L.pt);
@@ -427,6 +439,52 @@ dg_status dg_denoise_canvas(const dg_model* model, const dg_kv_cache* cache, dg_
   }
   return cuda_status(launch_loop_finish(at<int>(ws, c.L.stop_at), D.B, N, result->steps_taken,
                                         result->converged, canvas->prev_argmax, result->xhat0, D.C, c.st));
+}
+
+dg_status dg_canvas_init_masked(int32_t* tokens, int32_t B, int32_t C, int32_t mask_id, void* stream) {
+  if (!tokens || B <= 0 || C <= 0 || mask_id < 0 || (int64_t)B * C > (1 << 30)) return DG_ERR_ARG;
+  return cuda_status(launch_fill_tokens(tokens, B * C, mask_id, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+dg_status dg_denoise_step_masked(const dg_model* model, const dg_kv_cache* cache, dg_canvas* canvas, float tau,
+                                 int32_t mask_id, int32_t step, int32_t N, void* ws, size_t ws_bytes,
+                                 dg_step_out* out, void* stream) {
+  dg_status s = check_model(model);
+  if (s) return s;
+  if ((s = check_cache(model->dims, cache)) || (s = check_canvas(canvas))) return s;
+  if (!(tau > 0.f) || mask_id < 0 || mask_id >= model->dims.V || N <= 0 || step < 0 || step >= N)
+    return DG_ERR_ARG;
+  StepCtx c{model, cache, canvas, ws, {}, reinterpret_cast<cudaStream_t>(stream)};
+  if ((s = check_ws(model->dims, cache->cap, ws, ws_bytes, &c.L))) return s;
+  DG_TRY(cudaMemsetAsync(at<void>(ws, c.L.stop_at), 0x7f, 4 * (size_t)model->dims.B, c.st));
+  return enqueue_step(c, tau, 0.f, 0.f, 0, step, 0, out, nullptr, N, true, mask_id);
+}
+
+dg_status dg_denoise_canvas_masked(const dg_model* model, const dg_kv_cache* cache, dg_canvas* canvas,
+                                   const dg_sched* sched, int32_t mask_id, void* ws, size_t ws_bytes,
+                                   dg_canvas_result* result, void* stream) {
+  dg_status s = check_model(model);
+  if (s) return s;
+  if ((s = check_cache(model->dims, cache)) || (s = check_canvas(canvas))) return s;
+  if (!sched || sched->N <= 0 || sched->N > 4096 || !(sched->tau0 > 0.f) || mask_id < 0 ||
+      mask_id >= model->dims.V)
+    return DG_ERR_ARG;
+  if (!result || !result->steps_taken || !result->converged || !result->accepted || !result->xhat0)
+    return DG_ERR_ARG;
+  StepCtx c{model, cache, canvas, ws, {}, reinterpret_cast<cudaStream_t>(stream)};
+  if ((s = check_ws(model->dims, cache->cap, ws, ws_bytes, &c.L))) return s;
+  const dg_dims& D = model->dims;
+  DG_TRY(cudaMemsetAsync(at<void>(ws, c.L.stop_at), 0x7f, 4 * (size_t)D.B, c.st));
+  const int N = sched->N;
+  for (int step = 0; step < N; ++step) {
+    s = enqueue_step(c, sched->tau0, 0.f, 0.f, 0, step, 0, nullptr, result->accepted, N, step == 0, mask_id);
+    if (s) return s;
+  }
+  // every canvas ran all N steps; its result is the revealed canvas itself
+  DG_TRY(launch_loop_finish(at<int>(ws, c.L.stop_at), D.B, N, result->steps_taken, result->converged, nullptr,
+                            nullptr, D.C, c.st));
+  DG_TRY(cudaMemcpyAsync(result->xhat0, canvas->tokens, 4 * (size_t)D.B * D.C, cudaMemcpyDeviceToDevice, c.st));
+  return DG_OK;
 }
 
 dg_status dg_commit_block(const dg_model* model, dg_kv_cache* cache, const int32_t* tokens, void* ws,

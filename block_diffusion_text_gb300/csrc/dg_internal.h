@@ -116,6 +116,7 @@ struct LmArgs {
   int* pidx;           // [M][NT] (with pm, pl, pS, pvmax)
   float* logits;       // optional fp32 [M][V]
   int M, V, d;
+  int excl;            // column left out of the softmax (masked decoding's [MASK]), or -1
 };
 cudaError_t launch_lmhead(const LmArgs& a, StopCtl ctl, int* status, cudaStream_t st);
 // Self-conditioning contraction u = p0 . E (split over the vocabulary).
@@ -202,6 +203,26 @@ struct SamplerArgs {
   int N;
 };
 cudaError_t launch_sampler(const SamplerArgs& a, cudaStream_t st);
+// Masked confidence decoding of one step: per canvas, the
+// min(ceil(U / (N - step)), U) masked positions of smallest Z (highest
+// confidence 1 / Z) take their argmax; the accept copy is cleared (no
+// Gumbel-max sampling in this mode).
+struct RevealArgs {
+  const double* Hd;      // [B][C] (mean entropy output)
+  const float* lsum;     // [B][C] Z
+  const int* amax;       // [B][C]
+  int* prev_argmax;      // [B][C]
+  int* tokens;           // [B][C]
+  uint8_t* acc;          // [B][C] workspace copy (cleared)
+  uint8_t* acc_out;      // optional: 1 where revealed at this step
+  int* n_acc;            // optional [B]: positions revealed
+  float* mean_H;         // optional [B]
+  int* stop;             // optional [B] (0)
+  int* accepted_log;     // optional [B][N]
+  int B, C, mask_id, step, N;
+};
+cudaError_t launch_reveal(const RevealArgs& a, cudaStream_t st);
+cudaError_t launch_fill_tokens(int32_t* tokens, int n, int value, cudaStream_t st);
 
 struct ReduceArgs {
   const float* upart;    // [S][M][d]

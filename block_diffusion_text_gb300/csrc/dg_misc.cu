@@ -555,6 +555,102 @@ cudaError_t launch_sampler(const SamplerArgs& a, cudaStream_t st) {
   return launch_pdl(sampler_kernel, dim3(a.B), dim3(np), 0, st, a, np);
 }
 
+// ----------------------------------------- masked confidence decoding --
+// The second sampler ("从零拆开DiffusionGemma" news piece, generate() of its
+// fourth step): of the positions of a canvas still holding [MASK], the
+// k = min(ceil(U / (N - step)), U) with the highest confidence take their
+// candidate, the argmax; the others stay masked and revealed positions never
+// change.  The confidence of a position is its largest tempered probability
+// 1 / Z (the [MASK] column is left out of the softmax by the LM head), so the
+// order is ascending Z, ties to the lower position.  One CTA per canvas, one
+// thread per (padded) position, the bitonic network of sampler_kernel.
+DG_DEV uint64_t z_key(float z) {
+  // positive Z: the float's bits order like its value; anything else last
+  return (z > 0.f && z < INFINITY) ? (uint64_t)__float_as_uint(z) : 0xfffffffeull;
+}
+
+__global__ void __launch_bounds__(1024) reveal_kernel(RevealArgs a, int npow2) {
+  pdl_wait();
+  const int b = blockIdx.x, t = threadIdx.x, base = b * a.C;
+  const bool valid = t < a.C;
+  __shared__ uint64_t sk[1024];
+  __shared__ int si[1024];
+  __shared__ long long wsum[32];
+  bool unres = false;
+  long long f = 0;
+  if (valid) {
+    unres = a.tokens[base + t] == a.mask_id;
+    a.acc[base + t] = 0;
+    if (a.acc_out) a.acc_out[base + t] = 0;
+    a.prev_argmax[base + t] = a.amax[base + t];
+    f = fixed_entropy(a.Hd[base + t]);
+  }
+  uint64_t k = unres ? z_key(a.lsum[base + t]) : ~0ull;
+  int ix = t;
+  const int U = __syncthreads_count(unres);
+  for (int size = 2; size <= npow2; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      uint64_t ko;
+      int io;
+      if (stride >= 32) {
+        sk[t] = k;
+        si[t] = ix;
+        __syncthreads();
+        ko = sk[t ^ stride];
+        io = si[t ^ stride];
+        __syncthreads();
+      } else {
+        ko = __shfl_xor_sync(0xffffffffu, k, stride);
+        io = __shfl_xor_sync(0xffffffffu, ix, stride);
+      }
+      const bool keep_min = ((t & stride) == 0) == ((t & size) == 0);
+      const bool other_first = sorts_before(ko, io, k, ix);
+      if (keep_min == other_first) {
+        k = ko;
+        ix = io;
+      }
+    }
+  }
+  const int remaining = a.N - a.step;
+  int kk = (U + remaining - 1) / remaining;
+  if (kk > U) kk = U;
+  __syncthreads();  // every position's own writes above precede the reveal writes
+  if (t < kk) {  // rank t < kk <= U: a masked position
+    a.tokens[base + ix] = a.amax[base + ix];
+    if (a.acc_out) a.acc_out[base + ix] = 1;
+  }
+  // mean entropy (exact fixed-point sum, as in the sampler)
+  const int lane = t & 31, w = t >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) f += __shfl_xor_sync(0xffffffffu, f, o);
+  if (lane == 0) wsum[w] = f;
+  __syncthreads();
+  if (t == 0) {
+    long long tot = 0;
+    for (int i = 0; i < (npow2 + 31) / 32; ++i) tot += wsum[i];
+    if (a.n_acc) a.n_acc[b] = kk;
+    if (a.mean_H) a.mean_H[b] = (float)((double)tot / kFixScale / (double)a.C);
+    if (a.stop) a.stop[b] = 0;
+    if (a.accepted_log) a.accepted_log[(size_t)b * a.N + a.step] = kk;
+  }
+}
+
+cudaError_t launch_reveal(const RevealArgs& a, cudaStream_t st) {
+  int np = 32;
+  while (np < a.C) np <<= 1;
+  return launch_pdl(reveal_kernel, dim3(a.B), dim3(np), 0, st, a, np);
+}
+
+__global__ void fill_tokens_kernel(int32_t* tokens, int n, int value) {
+  pdl_wait();
+  const int t = blockIdx.x * blockDim.x + threadIdx.x;
+  if (t < n) tokens[t] = value;
+}
+
+cudaError_t launch_fill_tokens(int32_t* tokens, int n, int value, cudaStream_t st) {
+  return launch_pdl(fill_tokens_kernel, dim3(cdiv(n, 256)), dim3(256), 0, st, tokens, n, value);
+}
+
 // ------------------------------------------------ self-conditioning reduce --
 // u = sum of the per-split partials of p0 . E (bf16 out), and the Gumbel-max
 // token of accepted positions = the best (score, lowest index) over chunks.
@@ -680,7 +776,7 @@ __global__ void loop_finish_kernel(const int* stop_at, int B, int N, int* steps_
     if (steps_taken) steps_taken[t] = conv ? s + 1 : N;
     if (converged) converged[t] = conv ? 1 : 0;
   }
-  if (t < B * C && xhat0) xhat0[t] = prev_argmax[t];
+  if (t < B * C && xhat0 && prev_argmax) xhat0[t] = prev_argmax[t];
 }
 
 cudaError_t launch_loop_finish(const int* stop_at, int B, int N, int* steps_taken, int* converged,

@@ -26,7 +26,8 @@ DG_OK, DG_ERR_ARG, DG_ERR_SHAPE, DG_ERR_CAPACITY, DG_ERR_WORKSPACE, DG_ERR_CUDA,
 # Every function the C header declares (checked by the tests).
 EXPORTS = ("dg_status_string", "dg_workspace_size", "dg_read_status", "dg_tau", "dg_canvas_init",
            "dg_denoise_step", "dg_denoise_canvas", "dg_commit_block", "dg_debug_gemm",
-           "dg_attention_noalloc", "dg_attention_noalloc_status", "dg_debug_wait_timeout")
+           "dg_attention_noalloc", "dg_attention_noalloc_status", "dg_debug_wait_timeout",
+           "dg_canvas_init_masked", "dg_denoise_step_masked", "dg_denoise_canvas_masked")
 
 
 class DgError(RuntimeError):
@@ -93,6 +94,15 @@ def load():
             L.dg_read_status.argtypes = [ct.c_void_p, ct.POINTER(ct.c_int32), ct.c_void_p]
             L.dg_tau.argtypes = [ct.POINTER(dg_sched), ct.c_int32, ct.POINTER(ct.c_float)]
             L.dg_attention_noalloc_status.argtypes = [ct.POINTER(ct.c_int32), ct.c_void_p]
+            L.dg_canvas_init_masked.argtypes = [ct.c_void_p, ct.c_int32, ct.c_int32, ct.c_int32, ct.c_void_p]
+            L.dg_denoise_step_masked.argtypes = [ct.POINTER(dg_model), ct.POINTER(dg_kv_cache),
+                                                 ct.POINTER(dg_canvas), ct.c_float, ct.c_int32, ct.c_int32,
+                                                 ct.c_int32, ct.c_void_p, ct.c_size_t, ct.POINTER(dg_step_out),
+                                                 ct.c_void_p]
+            L.dg_denoise_canvas_masked.argtypes = [ct.POINTER(dg_model), ct.POINTER(dg_kv_cache),
+                                                   ct.POINTER(dg_canvas), ct.POINTER(dg_sched), ct.c_int32,
+                                                   ct.c_void_p, ct.c_size_t, ct.POINTER(dg_canvas_result),
+                                                   ct.c_void_p]
             L.dg_canvas_init.argtypes = [ct.c_void_p, ct.c_int32, ct.c_int32, ct.c_int32, ct.c_uint64,
                                          ct.c_int32, ct.c_void_p]
             L.dg_denoise_step.argtypes = [ct.POINTER(dg_model), ct.POINTER(dg_kv_cache),
@@ -203,11 +213,13 @@ _STEP_OUT_CACHE: dict = {}
 
 
 def denoise_step(model: Model, canvas: Canvas, tau: float, b: float, seed: int, step: int, block: int = 0,
-                 debug: bool = False, stream=None, events=None, out=None) -> dict:
+                 debug: bool = False, stream=None, events=None, out=None, masked=None) -> dict:
     """One denoising step (dg_denoise_step); updates canvas in place, returns outputs.
 
     events: optional list of 2 * len(PROF_SLOTS) recorded torch.cuda.Event (per-kernel timing).
     out: optional dict of preallocated output tensors (as returned by a previous call).
+    masked: optional (mask_id, N): a step of masked confidence decoding (dg_denoise_step_masked)
+    instead; b, seed and block are then not used.
     """
     d = model.dims
     dev = canvas.tokens.device
@@ -243,6 +255,13 @@ def denoise_step(model: Model, canvas: Canvas, tau: float, b: float, seed: int, 
         out["debug"] = dbg_t
     cs = canvas.struct()
     cache = model.cache()
+    if masked is not None:
+        mask_id, N = masked
+        rc = load().dg_denoise_step_masked(ct.byref(model.s), ct.byref(cache), ct.byref(cs), float(tau),
+                                           int(mask_id), int(step), int(N), model.ws_ptr, model.ws_bytes,
+                                           ct.byref(so), _stream(stream))
+        _check(rc, "dg_denoise_step_masked")
+        return out
     rc = load().dg_denoise_step(ct.byref(model.s), ct.byref(cache), ct.byref(cs), float(tau), float(b),
                                 int(seed), int(step), int(block), model.ws_ptr, model.ws_bytes,
                                 ct.byref(so), _stream(stream))
@@ -279,6 +298,32 @@ def denoise_canvas(model: Model, canvas: Canvas, seed: int, block: int = 0, N: i
                                   int(block), model.ws_ptr, model.ws_bytes, ct.byref(rs), _stream(stream))
     _check(rc, "dg_denoise_canvas")
     return res
+
+
+def denoise_canvas_masked(model: Model, canvas: Canvas, mask_id: int, N: int = 16, tau: float = 1.0,
+                          stream=None) -> dict:
+    """Masked confidence decoding loop (dg_denoise_canvas_masked): N steps at temperature tau."""
+    d = model.dims
+    dev = canvas.tokens.device
+    res = dict(steps_taken=torch.empty(d.B, dtype=torch.int32, device=dev),
+               converged=torch.empty(d.B, dtype=torch.int32, device=dev),
+               accepted=torch.empty(d.B, N, dtype=torch.int32, device=dev),
+               xhat0=torch.empty(d.B, d.C, dtype=torch.int32, device=dev))
+    rs = dg_canvas_result(*[_ptr(res[k]) for k in ("steps_taken", "converged", "accepted", "xhat0")])
+    sched = dg_sched(tau, tau, N, 0.0, 0.0)
+    cs = canvas.struct()
+    cache = model.cache()
+    rc = load().dg_denoise_canvas_masked(ct.byref(model.s), ct.byref(cache), ct.byref(cs), ct.byref(sched),
+                                         int(mask_id), model.ws_ptr, model.ws_bytes, ct.byref(rs), _stream(stream))
+    _check(rc, "dg_denoise_canvas_masked")
+    return res
+
+
+def canvas_init_masked(B, C, mask_id, device="cuda", stream=None) -> torch.Tensor:
+    """A canvas of [MASK] tokens (dg_canvas_init_masked)."""
+    t = torch.empty(B, C, dtype=torch.int32, device=device)
+    _check(load().dg_canvas_init_masked(_ptr(t), B, C, int(mask_id), _stream(stream)), "dg_canvas_init_masked")
+    return t
 
 
 def commit_block(model: Model, tokens: torch.Tensor, stream=None, cache=None) -> int:

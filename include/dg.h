@@ -15,6 +15,8 @@
  *          "Self-conditioning", "Multi-canvas sampling".
  *   [CH12] "DiffusionGemma" chapter of the diffusion docs: the KV-cache timing
  *          list, the attention-mask list and the data-flow pseudocode.
+ *   [P4]   "从零拆开DiffusionGemma" news piece: the masked confidence decoder
+ *          generate() of its fourth step (the second sampler below).
  * The model is a one-layer synthetic stand-in: RMSNorm of embedding plus
  * self-conditioning, one GQA attention layer with RoPE, a tied LM head with a
  * per-position logit sharpness alpha, and a two-matrix FFW for
@@ -246,6 +248,37 @@ DG_API dg_status dg_denoise_canvas(const dg_model* model, const dg_kv_cache* cac
  * DG_ERR_CAPACITY (nothing written) if len + C > cap.                       */
 DG_API dg_status dg_commit_block(const dg_model* model, dg_kv_cache* cache, const int32_t* tokens,
                           void* ws, size_t ws_bytes, void* stream);
+
+/* Masked confidence decoding, the second sampler of the pages ([P4] the
+ * "从零拆开DiffusionGemma" news piece, generate() of its fourth step, given
+ * there as the masked-diffusion contrast to the uniform-state sampler):
+ *
+ * dg_canvas_init_masked: tokens int32 [B][C] all set to mask_id ([MASK]).
+ *
+ * dg_denoise_step_masked: one step of the same denoiser (a, q, k, v, o, h,
+ * l = alpha h E^T / sqrt d, self-conditioning z_{t+1} = W2 GELU(W1 (p0 E)))
+ * with the [MASK] token left out of the tempered softmax p0 = softmax(l / tau)
+ * (it is not a prediction target: its logit counts as -inf).  Per canvas, of
+ * the U positions still holding mask_id, the k = min(ceil(U / (N - step)), U)
+ * with the highest confidence max_v p0_v = 1 / Z (ties to the lower
+ * position) take their candidate argmax_v l_v; every other position keeps its
+ * token, so revealed positions never change and step N - 1 reveals all that
+ * remain.  Outputs as in dg_denoise_step: accept = revealed at this step,
+ * n_acc = k, stop = 0.  mask_id in [0, V); 0 <= step < N.  The cache is read
+ * only; no random draws.
+ *
+ * dg_denoise_canvas_masked: N = sched->N such steps at the fixed temperature
+ * tau0 (the pages' generate() keeps one temperature; tau1, b and stop_H are
+ * not used), enqueued without synchronising.  result: steps_taken = N,
+ * converged = 0 (no adaptive stop in this mode), accepted[b][s] = positions
+ * revealed at step s, xhat0 = the final canvas (every position revealed). */
+DG_API dg_status dg_canvas_init_masked(int32_t* tokens, int32_t B, int32_t C, int32_t mask_id, void* stream);
+DG_API dg_status dg_denoise_step_masked(const dg_model* model, const dg_kv_cache* cache, dg_canvas* canvas,
+                                        float tau, int32_t mask_id, int32_t step, int32_t N, void* ws,
+                                        size_t ws_bytes, dg_step_out* out, void* stream);
+DG_API dg_status dg_denoise_canvas_masked(const dg_model* model, const dg_kv_cache* cache, dg_canvas* canvas,
+                                          const dg_sched* sched, int32_t mask_id, void* ws, size_t ws_bytes,
+                                          dg_canvas_result* result, void* stream);
 
 /* Attention of the denoising step (the bidirectional attention inside
  * dg_denoise_step) for callers that cannot allocate device memory, e.g. a

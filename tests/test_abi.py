@@ -177,3 +177,25 @@ def test_tau_schedule_is_the_linear_anneal(dg):
     assert L.dg_tau(None, 0, ct.byref(t)) == dg.DG_ERR_ARG
     assert L.dg_tau(ct.byref(sched), 0, None) == dg.DG_ERR_ARG
     assert L.dg_tau(ct.byref(dg.dg_sched(0.0, 0.4, 48, 0.1, 0.005)), 0, ct.byref(t)) == dg.DG_ERR_ARG
+
+
+def test_masked_entry_points_validate(dg):
+    L = dg.load()
+    dims = _dims()
+    m, c, cv, wsb = _structs(dg, dims)
+    ws = ct.c_void_p(1 << 30)
+    call = lambda tau, mask, step, N: L.dg_denoise_step_masked(ct.byref(m), ct.byref(c), ct.byref(cv), tau, mask,
+                                                               step, N, ws, wsb, None, None)
+    assert call(0.0, 5, 0, 4) == dg.DG_ERR_ARG
+    assert call(0.8, -1, 0, 4) == dg.DG_ERR_ARG
+    assert call(0.8, dims.V, 0, 4) == dg.DG_ERR_ARG
+    assert call(0.8, 5, 4, 4) == dg.DG_ERR_ARG
+    assert call(0.8, 5, 0, 0) == dg.DG_ERR_ARG
+    res = dg.dg_canvas_result(*[ct.c_void_p(FAKE)] * 4)
+    sched = dg.dg_sched(0.8, 0.8, 16, 0.0, 0.0)
+    assert L.dg_denoise_canvas_masked(ct.byref(m), ct.byref(c), ct.byref(cv), ct.byref(sched), dims.V, ws, wsb,
+                                      ct.byref(res), None) == dg.DG_ERR_ARG
+    assert L.dg_denoise_canvas_masked(ct.byref(m), ct.byref(c), ct.byref(cv), ct.byref(sched), 5, ws, wsb,
+                                      None, None) == dg.DG_ERR_ARG
+    assert L.dg_canvas_init_masked(None, 1, 16, 5, None) == dg.DG_ERR_ARG
+    assert L.dg_canvas_init_masked(ct.c_void_p(FAKE), 1, 16, -1, None) == dg.DG_ERR_ARG
