@@ -34,6 +34,7 @@ class Dims:
     cap: int = 0    # cache capacity in rows (0: equal to P)
     rope_base: float = 10000.0
     rms_eps: float = 1e-6
+    L: int = 1      # attention layers (Wq, Wk, Wv, Wo and the caches stacked [L, ...] when L > 1)
 
     def __post_init__(self):
         if self.cap == 0:
@@ -82,19 +83,21 @@ def make_weights(dims: Dims, seed: int, device="cpu", dtype=torch.bfloat16):
             t.mul_(scale)
         return t.to(dtype)
 
+    L = dims.L
+    lead = () if L == 1 else (L,)
     w = {}
     w["E"] = draw((dims.V, dims.d), sd)
-    w["Wq"] = draw((nq, dims.d), sd)
-    w["Wk"] = draw((nkv, dims.d), sd)
-    w["Wv"] = draw((nkv, dims.d), sd)
-    w["Wo"] = draw((dims.d, nq), sd)
+    w["Wq"] = draw(lead + (nq, dims.d), sd)
+    w["Wk"] = draw(lead + (nkv, dims.d), sd)
+    w["Wv"] = draw(lead + (nkv, dims.d), sd)
+    w["Wo"] = draw(lead + (dims.d, nq), sd)
     w["W1"] = draw((dims.F, dims.d), sd)
     w["W2"] = draw((dims.d, dims.F), sf)
-    Kc = torch.zeros((dims.B, dims.Hkv, dims.cap, dims.hd), device=device, dtype=dtype)
+    Kc = torch.zeros(lead + (dims.B, dims.Hkv, dims.cap, dims.hd), device=device, dtype=dtype)
     Vc = torch.zeros_like(Kc)
     if dims.P > 0:
-        Kc[:, :, : dims.P] = draw((dims.B, dims.Hkv, dims.P, dims.hd), 1.0)
-        Vc[:, :, : dims.P] = draw((dims.B, dims.Hkv, dims.P, dims.hd), 1.0)
+        Kc[..., : dims.P, :] = draw(lead + (dims.B, dims.Hkv, dims.P, dims.hd), 1.0)
+        Vc[..., : dims.P, :] = draw(lead + (dims.B, dims.Hkv, dims.P, dims.hd), 1.0)
     w["Kc"], w["Vc"] = Kc, Vc
     return w
 

@@ -39,7 +39,7 @@ class Dims(ct.Structure):
     _fields_ = [("V", ct.c_int32), ("d", ct.c_int32), ("C", ct.c_int32), ("B", ct.c_int32),
                 ("Hq", ct.c_int32), ("Hkv", ct.c_int32), ("hd", ct.c_int32), ("F", ct.c_int32),
                 ("P", ct.c_int32), ("cap", ct.c_int32), ("rope_base", ct.c_double),
-                ("rms_eps", ct.c_double), ("mirror_bf16", ct.c_int32)]
+                ("rms_eps", ct.c_double), ("mirror_bf16", ct.c_int32), ("L", ct.c_int32)]
 
 
 _F = ct.POINTER(ct.c_float)
@@ -75,6 +75,8 @@ def lib():
             L.or_philox_word.restype = ct.c_uint64
             L.or_uniform_token.argtypes = [ct.c_uint64, ct.c_int32]
             L.or_uniform_token.restype = ct.c_int32
+            L.or_prefill.argtypes = [ct.POINTER(Dims), _F, _F, _F, _F, _F, _I, ct.c_int32, _F, _F, ct.c_int32]
+            L.or_prefill.restype = ct.c_int
             L.or_reveal.argtypes = [_D, _I, _I, ct.c_int32, ct.c_int32, ct.c_int32, ct.c_int32, _U8]
             L.or_reveal.restype = ct.c_int32
             L.or_tau.argtypes = [ct.c_double, ct.c_double, ct.c_int32, ct.c_int32]
@@ -273,7 +275,7 @@ def attend_row(q, Kp, Vp, Kc, Vc):
 def _dims(dims, mirror_bf16: bool, P=None):
     return Dims(V=dims.V, d=dims.d, C=dims.C, B=dims.B, Hq=dims.Hq, Hkv=dims.Hkv, hd=dims.hd,
                 F=dims.F, P=dims.P if P is None else P, cap=dims.cap, rope_base=dims.rope_base,
-                rms_eps=dims.rms_eps, mirror_bf16=1 if mirror_bf16 else 0)
+                rms_eps=dims.rms_eps, mirror_bf16=1 if mirror_bf16 else 0, L=getattr(dims, "L", 1))
 
 
 _WANT_ALL = ("a", "q", "k", "v", "o", "h", "logits", "H", "m", "Z", "top2gap", "argmax", "accept",
@@ -359,7 +361,7 @@ def denoise_canvas(dims, w, x0, alpha, seed, N=48, tau0=0.8, tau1=0.4, b=0.1, st
 
 
 def commit(dims, E, Wk, Wv, tokens, Kc, Vc, P, mirror_bf16=True, nthreads=None):
-    """Append the re-encoded K/V of `tokens` [B, C] at rows P..P+C-1; returns new (Kc, Vc)."""
+    """Append the re-encoded K/V of `tokens` [B, C] at rows P..P+C-1 (one layer); returns new (Kc, Vc)."""
     Kc = _f32(Kc).copy()
     Vc = _f32(Vc).copy()
     D = _dims(dims, mirror_bf16, P=P)
@@ -367,4 +369,20 @@ def commit(dims, E, Wk, Wv, tokens, Kc, Vc, P, mirror_bf16=True, nthreads=None):
                          _p(_i32(tokens), _I), _p(Kc, _F), _p(Vc, _F), nthreads or default_threads())
     if rc != 0:
         raise ValueError("oracle commit: cache capacity exceeded")
+    return Kc, Vc
+
+
+def prefill(dims, w, tokens, P, mirror_bf16=True, nthreads=None):
+    """Causal re-encode of tokens [B, n] appended at rows P..P+n-1 of every layer's cache (or_prefill).
+    w: E, Wq, Wk, Wv, Wo (stacked [L, ...] when L > 1), Kc, Vc ([L, B, Hkv, cap, hd] or [B, Hkv, cap, hd]).
+    Returns the new (Kc, Vc) with the shape of w's."""
+    Kc = _f32(w["Kc"]).copy()
+    Vc = _f32(w["Vc"]).copy()
+    tok = _i32(tokens)
+    n = tok.shape[-1] if tok.ndim > 1 else tok.size // dims.B
+    D = _dims(dims, mirror_bf16, P=P)
+    rc = lib().or_prefill(ct.byref(D), *[_p(_f32(w[k]), _F) for k in ("E", "Wq", "Wk", "Wv", "Wo")],
+                          _p(tok, _I), int(n), _p(Kc, _F), _p(Vc, _F), nthreads or default_threads())
+    if rc != 0:
+        raise ValueError("oracle prefill: cache capacity exceeded")
     return Kc, Vc

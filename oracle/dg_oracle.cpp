@@ -319,11 +319,12 @@ typedef struct {
   int32_t cap;  // cache row capacity per (canvas, kv head)
   double rope_base, rms_eps;
   int32_t mirror_bf16;
+  int32_t L;    // attention layers (>= 1); weights Wq, Wk, Wv, Wo and the caches are stacked [L][...]
 } or_dims;
 
 typedef struct {
-  const float *E, *Wq, *Wk, *Wv, *Wo, *W1, *W2;  // [V][d], [out][in] row-major
-  const float *Kc, *Vc;                          // prefix cache [B][Hkv][cap][hd], keys post-RoPE
+  const float *E, *Wq, *Wk, *Wv, *Wo, *W1, *W2;  // [V][d], [L][out][in] row-major (W1, W2 single)
+  const float *Kc, *Vc;                          // prefix caches [L][B][Hkv][cap][hd], keys post-RoPE
   const int32_t* x;                              // canvas tokens x_t [B][C]
   const float* z;                                // self-conditioning z_t [B][C][d]
   const float* alpha;                            // per-position logit sharpness [B][C]
@@ -393,63 +394,82 @@ int or_denoise_step(const or_dims* D, const or_step_in* in, or_step_out* out, co
     for (int64_t j = 0; j < d; ++j) a[r * d + j] = maybe_bf16(a[r * d + j], mir);
   });
 
-  // a2: projections; RoPE on q and k at absolute position P + i.
-  std::vector<double> q(M * nq), k(M * nkv), v(M * nkv);
-  parallel_rows(M, nthreads, [&](int64_t r) {
-    const double* ar = &a[r * d];
-    double pos = (double)(P + r % C);
-    for (int64_t n = 0; n < nq; ++n) {
-      double acc = 0.0;
-      for (int64_t j = 0; j < d; ++j) acc += ar[j] * (double)in->Wq[n * d + j];
-      q[r * nq + n] = acc;
+  // a2-a4, once per attention layer.  The one-layer stand-in generalises as
+  // pre-norm residual blocks (a reading: the pages' model has 30 layers, the
+  // stand-in's layer is fixed by the problem statement): layer l takes a_l,
+  // h_l = a_l + Attn_l(a_l) Wo_l^T, and a_{l+1} = RMSNorm(h_l); the LM head
+  // reads h_{L-1}.  Layer l attends over its own prefix cache.  With L = 1
+  // this is exactly the single layer.  The debug copies are the last layer's.
+  const int64_t L = D->L < 1 ? 1 : D->L;
+  std::vector<double> q(M * nq), k(M * nkv), v(M * nkv), o(M * nq), hh(M * d);
+  for (int64_t l = 0; l < L; ++l) {
+    const float* Wq = in->Wq + l * nq * d;
+    const float* Wk = in->Wk + l * nkv * d;
+    const float* Wv = in->Wv + l * nkv * d;
+    const float* Wo = in->Wo + l * d * nq;
+    const float* Kcl = in->Kc + l * B * Hkv * cap * hd;
+    const float* Vcl = in->Vc + l * B * Hkv * cap * hd;
+    if (l > 0) {
+      parallel_rows(M, nthreads, [&](int64_t r) {
+        or_rmsnorm(&hh[r * d], (int32_t)d, D->rms_eps, &a[r * d]);
+        for (int64_t j = 0; j < d; ++j) a[r * d + j] = maybe_bf16(a[r * d + j], mir);
+      });
     }
-    for (int64_t n = 0; n < nkv; ++n) {
-      double acc = 0.0, acc2 = 0.0;
-      for (int64_t j = 0; j < d; ++j) {
-        acc += ar[j] * (double)in->Wk[n * d + j];
-        acc2 += ar[j] * (double)in->Wv[n * d + j];
+    // a2: projections; RoPE on q and k at absolute position P + i.
+    parallel_rows(M, nthreads, [&](int64_t r) {
+      const double* ar = &a[r * d];
+      double pos = (double)(P + r % C);
+      for (int64_t n = 0; n < nq; ++n) {
+        double acc = 0.0;
+        for (int64_t j = 0; j < d; ++j) acc += ar[j] * (double)Wq[n * d + j];
+        q[r * nq + n] = acc;
       }
-      k[r * nkv + n] = acc;
-      v[r * nkv + n] = acc2;
-    }
-    for (int64_t h = 0; h < Hq; ++h) or_rope(&q[r * nq + h * hd], (int32_t)hd, pos, D->rope_base);
-    for (int64_t h = 0; h < Hkv; ++h) or_rope(&k[r * nkv + h * hd], (int32_t)hd, pos, D->rope_base);
-    for (int64_t n = 0; n < nq; ++n) q[r * nq + n] = maybe_bf16(q[r * nq + n], mir);
-    for (int64_t n = 0; n < nkv; ++n) {
-      k[r * nkv + n] = maybe_bf16(k[r * nkv + n], mir);
-      v[r * nkv + n] = maybe_bf16(v[r * nkv + n], mir);
-    }
-  });
-
-  // a3: bidirectional GQA attention over [prefix cache ; canvas].  Query head
-  // h reads kv head h / (Hq / Hkv).
-  std::vector<double> o(M * nq);
-  parallel_rows(B * Hq, nthreads, [&](int64_t bh) {
-    int64_t bb = bh / Hq, h = bh % Hq, g = h / (Hq / Hkv);
-    std::vector<double> kc(C * hd), vc(C * hd), qr(hd), orow(hd);
-    for (int64_t i = 0; i < C; ++i)
-      for (int64_t t = 0; t < hd; ++t) {
-        kc[i * hd + t] = k[(bb * C + i) * nkv + g * hd + t];
-        vc[i * hd + t] = v[(bb * C + i) * nkv + g * hd + t];
+      for (int64_t n = 0; n < nkv; ++n) {
+        double acc = 0.0, acc2 = 0.0;
+        for (int64_t j = 0; j < d; ++j) {
+          acc += ar[j] * (double)Wk[n * d + j];
+          acc2 += ar[j] * (double)Wv[n * d + j];
+        }
+        k[r * nkv + n] = acc;
+        v[r * nkv + n] = acc2;
       }
-    const float* Kp = in->Kc + ((bb * Hkv + g) * cap) * hd;
-    const float* Vp = in->Vc + ((bb * Hkv + g) * cap) * hd;
-    for (int64_t i = 0; i < C; ++i) {
-      for (int64_t t = 0; t < hd; ++t) qr[t] = q[(bb * C + i) * nq + h * hd + t];
-      or_attend_row(qr.data(), Kp, Vp, P, kc.data(), vc.data(), C, (int32_t)hd, orow.data());
-      for (int64_t t = 0; t < hd; ++t) o[(bb * C + i) * nq + h * hd + t] = maybe_bf16(orow[t], mir);
-    }
-  });
+      for (int64_t h = 0; h < Hq; ++h) or_rope(&q[r * nq + h * hd], (int32_t)hd, pos, D->rope_base);
+      for (int64_t h = 0; h < Hkv; ++h) or_rope(&k[r * nkv + h * hd], (int32_t)hd, pos, D->rope_base);
+      for (int64_t n = 0; n < nq; ++n) q[r * nq + n] = maybe_bf16(q[r * nq + n], mir);
+      for (int64_t n = 0; n < nkv; ++n) {
+        k[r * nkv + n] = maybe_bf16(k[r * nkv + n], mir);
+        v[r * nkv + n] = maybe_bf16(v[r * nkv + n], mir);
+      }
+    });
 
-  // a4: output projection with the residual from a.
-  std::vector<double> hh(M * d);
-  parallel_rows(M, nthreads, [&](int64_t r) {
-    for (int64_t n = 0; n < d; ++n) {
-      double acc = 0.0;
-      for (int64_t j = 0; j < nq; ++j) acc += o[r * nq + j] * (double)in->Wo[n * nq + j];
-      hh[r * d + n] = maybe_bf16(a[r * d + n] + acc, mir);
-    }
-  });
+    // a3: bidirectional GQA attention over [prefix cache ; canvas].  Query head
+    // h reads kv head h / (Hq / Hkv).
+    parallel_rows(B * Hq, nthreads, [&](int64_t bh) {
+      int64_t bb = bh / Hq, h = bh % Hq, g = h / (Hq / Hkv);
+      std::vector<double> kc(C * hd), vc(C * hd), qr(hd), orow(hd);
+      for (int64_t i = 0; i < C; ++i)
+        for (int64_t t = 0; t < hd; ++t) {
+          kc[i * hd + t] = k[(bb * C + i) * nkv + g * hd + t];
+          vc[i * hd + t] = v[(bb * C + i) * nkv + g * hd + t];
+        }
+      const float* Kp = Kcl + ((bb * Hkv + g) * cap) * hd;
+      const float* Vp = Vcl + ((bb * Hkv + g) * cap) * hd;
+      for (int64_t i = 0; i < C; ++i) {
+        for (int64_t t = 0; t < hd; ++t) qr[t] = q[(bb * C + i) * nq + h * hd + t];
+        or_attend_row(qr.data(), Kp, Vp, P, kc.data(), vc.data(), C, (int32_t)hd, orow.data());
+        for (int64_t t = 0; t < hd; ++t) o[(bb * C + i) * nq + h * hd + t] = maybe_bf16(orow[t], mir);
+      }
+    });
+
+    // a4: output projection with the residual from a.
+    parallel_rows(M, nthreads, [&](int64_t r) {
+      for (int64_t n = 0; n < d; ++n) {
+        double acc = 0.0;
+        for (int64_t j = 0; j < nq; ++j) acc += o[r * nq + j] * (double)Wo[n * nq + j];
+        hh[r * d + n] = maybe_bf16(a[r * d + n] + acc, mir);
+      }
+    });
+  }
 
   if (out->a) std::memcpy(out->a, a.data(), sizeof(double) * M * d);
   if (out->q) std::memcpy(out->q, q.data(), sizeof(double) * M * nq);
@@ -673,43 +693,113 @@ int or_denoise_canvas(const or_dims* D, const float* E, const float* Wq, const f
   return 0;
 }
 
-// ------------------------------------------------------------ the commit ----
-// Commit of a finalized block, [TR] step 5 and [CH12] KV-cache timing: the
-// block's tokens are re-encoded by the encoder path (no self-conditioning,
-// z = 0) and their keys/values appended to the cache at rows P..P+C-1.  With
-// the one-layer stand-in the appended K/V depend only on each token and its
-// position, so the causal mask of the encoder has no effect here.
-// Kc, Vc: [B][Hkv][cap][hd], updated in place.  Returns 1 if P + C > cap.
+// ------------------------------------------------- prefill and commit ----
+// Causal re-encode of n tokens per canvas appended to the caches at rows
+// P..P+n-1: the prompt prefill of [TR] step 1 and [EXP] "Architecture:
+// incremental prefill and denoising", and the commit of a finalized block of
+// [TR] step 5 and [CH12] (the cache comes from re-encoding the finished block,
+// not from the denoiser's states).  The encoder is the denoiser's attention
+// stack with no self-conditioning (z = 0) and a causal mask: token i attends to
+// every cached row and to the block's tokens 0..i.  Per layer l: a_l, k_l and
+// v_l (RoPE at positions P + i) are written to cache l first, then (below the
+// last layer) q_l attends over cache rows 0..P+i, h_l = a_l + o_l Wo_l^T and
+// a_{l+1} = RMSNorm(h_l).  With one layer the appended K/V depend only on each
+// token and its position, so the mask has no effect; with two or more, layer
+// l + 1's K/V depend on the attention of layer l over earlier tokens.
+// Kc, Vc: [L][B][Hkv][cap][hd], updated in place; tokens [B][n].  Returns 1
+// if P + n > cap.  Pinned by test_oracle_pins.py::test_prefill_* (a torch
+// composition with an explicit causal mask, the independence of earlier K/V
+// from later tokens, chunked prefill equal to one piece).
+int or_prefill(const or_dims* D, const float* E, const float* Wq, const float* Wk, const float* Wv,
+               const float* Wo, const int32_t* tokens, int32_t n, float* Kc, float* Vc, int32_t nthreads) {
+  const int64_t d = D->d, B = D->B, Hq = D->Hq, Hkv = D->Hkv, hd = D->hd, P = D->P, cap = D->cap;
+  const int64_t L = D->L < 1 ? 1 : D->L;
+  if (n < 0 || P + n > cap) return 1;
+  const int mir = D->mirror_bf16;
+  const int64_t nq = Hq * hd, nkv = Hkv * hd, Mn = B * (int64_t)n;
+  std::vector<double> a(Mn * d), q(Mn * nq), o(Mn * nq), hh(Mn * d);
+  parallel_rows(Mn, nthreads, [&](int64_t r) {
+    std::vector<double> e(d);
+    for (int64_t j = 0; j < d; ++j) e[j] = (double)E[(int64_t)tokens[r] * d + j];
+    or_rmsnorm(e.data(), (int32_t)d, D->rms_eps, &a[r * d]);
+    for (int64_t j = 0; j < d; ++j) a[r * d + j] = maybe_bf16(a[r * d + j], mir);
+  });
+  for (int64_t l = 0; l < L; ++l) {
+    const float* Wql = Wq + l * nq * d;
+    const float* Wkl = Wk + l * nkv * d;
+    const float* Wvl = Wv + l * nkv * d;
+    const float* Wol = Wo + l * d * nq;
+    float* Kl = Kc + l * B * Hkv * cap * hd;
+    float* Vl = Vc + l * B * Hkv * cap * hd;
+    const bool last = l == L - 1;
+    if (l > 0) {
+      parallel_rows(Mn, nthreads, [&](int64_t r) {
+        or_rmsnorm(&hh[r * d], (int32_t)d, D->rms_eps, &a[r * d]);
+        for (int64_t j = 0; j < d; ++j) a[r * d + j] = maybe_bf16(a[r * d + j], mir);
+      });
+    }
+    parallel_rows(Mn, nthreads, [&](int64_t r) {
+      const int64_t bb = r / n, i = r % n;
+      const double* ar = &a[r * d];
+      std::vector<double> k(nkv), v(nkv);
+      for (int64_t c = 0; c < nkv; ++c) {
+        double acc = 0.0, acc2 = 0.0;
+        for (int64_t j = 0; j < d; ++j) {
+          acc += ar[j] * (double)Wkl[c * d + j];
+          acc2 += ar[j] * (double)Wvl[c * d + j];
+        }
+        k[c] = acc;
+        v[c] = acc2;
+      }
+      for (int64_t g = 0; g < Hkv; ++g) or_rope(&k[g * hd], (int32_t)hd, (double)(P + i), D->rope_base);
+      for (int64_t g = 0; g < Hkv; ++g)
+        for (int64_t t = 0; t < hd; ++t) {
+          const int64_t dst = ((bb * Hkv + g) * cap + P + i) * hd + t;
+          Kl[dst] = (float)maybe_bf16(k[g * hd + t], mir);
+          Vl[dst] = (float)maybe_bf16(v[g * hd + t], mir);
+        }
+      if (!last) {
+        for (int64_t c = 0; c < nq; ++c) {
+          double acc = 0.0;
+          for (int64_t j = 0; j < d; ++j) acc += ar[j] * (double)Wql[c * d + j];
+          q[r * nq + c] = acc;
+        }
+        for (int64_t h = 0; h < Hq; ++h) or_rope(&q[r * nq + h * hd], (int32_t)hd, (double)(P + i), D->rope_base);
+        for (int64_t c = 0; c < nq; ++c) q[r * nq + c] = maybe_bf16(q[r * nq + c], mir);
+      }
+    });
+    if (last) break;
+    // causal attention: token i over cache rows 0..P+i (the block's own rows
+    // were written above)
+    parallel_rows(B * Hq, nthreads, [&](int64_t bh) {
+      const int64_t bb = bh / Hq, h = bh % Hq, g = h / (Hq / Hkv);
+      const float* Kp = Kl + ((bb * Hkv + g) * cap) * hd;
+      const float* Vp = Vl + ((bb * Hkv + g) * cap) * hd;
+      std::vector<double> orow(hd);
+      for (int64_t i = 0; i < n; ++i) {
+        const double* qr = &q[(bb * n + i) * nq + h * hd];
+        or_attend_row(qr, Kp, Vp, P + i + 1, nullptr, nullptr, 0, (int32_t)hd, orow.data());
+        for (int64_t t = 0; t < hd; ++t) o[(bb * n + i) * nq + h * hd + t] = maybe_bf16(orow[t], mir);
+      }
+    });
+    parallel_rows(Mn, nthreads, [&](int64_t r) {
+      for (int64_t c = 0; c < d; ++c) {
+        double acc = 0.0;
+        for (int64_t j = 0; j < nq; ++j) acc += o[r * nq + j] * (double)Wol[c * nq + j];
+        hh[r * d + c] = maybe_bf16(a[r * d + c] + acc, mir);
+      }
+    });
+  }
+  return 0;
+}
+
+// The commit of a finalized block of C tokens per canvas (or_prefill with
+// n = C).  Kept as its own entry for the one-layer callers (Wq, Wo unused
+// when L = 1).
 int or_commit(const or_dims* D, const float* E, const float* Wk, const float* Wv,
               const int32_t* tokens, float* Kc, float* Vc, int32_t nthreads) {
-  const int64_t d = D->d, C = D->C, B = D->B, Hkv = D->Hkv, hd = D->hd, P = D->P, cap = D->cap;
-  if (P + C > cap) return 1;
-  const int mir = D->mirror_bf16;
-  const int64_t nkv = Hkv * hd;
-  parallel_rows(B * C, nthreads, [&](int64_t r) {
-    int64_t bb = r / C, i = r % C;
-    std::vector<double> e(d), a(d), k(nkv), v(nkv);
-    for (int64_t j = 0; j < d; ++j) e[j] = (double)E[(int64_t)tokens[r] * d + j];
-    or_rmsnorm(e.data(), (int32_t)d, D->rms_eps, a.data());
-    for (int64_t j = 0; j < d; ++j) a[j] = maybe_bf16(a[j], mir);
-    for (int64_t n = 0; n < nkv; ++n) {
-      double acc = 0.0, acc2 = 0.0;
-      for (int64_t j = 0; j < d; ++j) {
-        acc += a[j] * (double)Wk[n * d + j];
-        acc2 += a[j] * (double)Wv[n * d + j];
-      }
-      k[n] = acc;
-      v[n] = acc2;
-    }
-    for (int64_t g = 0; g < Hkv; ++g) or_rope(&k[g * hd], (int32_t)hd, (double)(P + i), D->rope_base);
-    for (int64_t g = 0; g < Hkv; ++g)
-      for (int64_t t = 0; t < hd; ++t) {
-        int64_t dst = ((bb * Hkv + g) * cap + P + i) * hd + t;
-        Kc[dst] = (float)maybe_bf16(k[g * hd + t], mir);
-        Vc[dst] = (float)maybe_bf16(v[g * hd + t], mir);
-      }
-  });
-  return 0;
+  if (D->L > 1) return 1;
+  return or_prefill(D, E, nullptr, Wk, Wv, nullptr, tokens, D->C, Kc, Vc, nthreads);
 }
 
 double or_round_bf16(double x) { return round_bf16(x); }

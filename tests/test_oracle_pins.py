@@ -4,6 +4,7 @@ Each test checks the oracle against something other than itself: published
 known answers, closed forms, invariants, library routines that the operation
 reduces to in a special case, or brute force on tiny inputs.
 """
+import dataclasses
 import itertools
 import math
 import os
@@ -590,3 +591,127 @@ def test_excluded_token_is_removed_from_the_softmax():
     am = np.argmax(l[:, keep], axis=1)
     assert np.array_equal(out["argmax"], np.where(am >= ex, am + 1, am))
     assert np.allclose(1.0 / out["Z"], p.max(axis=1), rtol=1e-12)
+
+
+# ---------------------------------------- multi-layer stack and causal prefill ---
+ML = synth.Dims(V=300, d=64, C=12, B=2, Hq=4, Hkv=2, hd=16, F=64, P=10, cap=40, L=3)
+
+
+def _rope_t(t, pos, hd, base):
+    ang = pos[:, None] * base ** (-2.0 * torch.arange(hd // 2, dtype=torch.float64) / hd)
+    rot = torch.polar(torch.ones_like(ang), ang)
+    c = torch.complex(t[..., : hd // 2], t[..., hd // 2:]) * rot
+    return torch.cat([c.real, c.imag], -1)
+
+
+def _torch_layers(dims, w, a, Kc, Vc, P, n, mask=None, write_cache=False):
+    """Float64 composition of the attention stack with library routines (rms_norm, SDPA, complex
+    RoPE): a [B, n, d] into layer 0; per layer q, k, v of a_l, attention over [cache rows 0..P-1 ;
+    the n new rows] with an optional boolean mask, h_l = a_l + o Wo^T, a_{l+1} = rms_norm(h_l).
+    Returns the last h and the new rows' (k, v) of every layer."""
+    f = lambda t: torch.from_numpy(np.asarray(t)).double()
+    B, d, Hq, Hkv, hd = dims.B, dims.d, dims.Hq, dims.Hkv, dims.hd
+    pos = torch.arange(P, P + n, dtype=torch.float64)
+    rep = Hq // Hkv
+    kv = []
+    h = None
+    for l in range(dims.L):
+        if l > 0:
+            a = torch.nn.functional.rms_norm(h, (d,), eps=dims.rms_eps)
+        q = _rope_t((a @ f(w["Wq"][l]).T).view(B, n, Hq, hd).transpose(1, 2), pos, hd, dims.rope_base)
+        k = _rope_t((a @ f(w["Wk"][l]).T).view(B, n, Hkv, hd).transpose(1, 2), pos, hd, dims.rope_base)
+        v = (a @ f(w["Wv"][l]).T).view(B, n, Hkv, hd).transpose(1, 2)
+        kv.append((k, v))
+        Kall = torch.cat([f(Kc[l])[:, :, :P], k], 2)
+        Vall = torch.cat([f(Vc[l])[:, :, :P], v], 2)
+        o = torch.nn.functional.scaled_dot_product_attention(
+            q, Kall.repeat_interleave(rep, 1), Vall.repeat_interleave(rep, 1), attn_mask=mask)
+        h = a + o.transpose(1, 2).reshape(B, n, Hq * hd) @ f(w["Wo"][l]).T
+    return h, kv
+
+
+def test_multilayer_step_matches_library_composition():
+    """L = 3: the oracle step's h (last layer), entropy and u equal a float64 composition of library
+    routines, each layer over its own prefix cache."""
+    from scipy import special, stats
+    w, x, z, al = _tiny_inputs(torch.float32, seed=12, dims=ML)
+    tau = 0.7
+    out = oracle.denoise_step(ML, w, x, z, al, tau=tau, b=0.1, seed=0, step=0, mirror_bf16=False,
+                              want=("h", "logits", "H", "u"), nthreads=2)
+    e = torch.from_numpy(w["E"]).double()[torch.from_numpy(x).long()] + torch.from_numpy(z).double()
+    a0 = torch.nn.functional.rms_norm(e, (ML.d,), eps=ML.rms_eps)
+    h, _ = _torch_layers(ML, w, a0, w["Kc"], w["Vc"], ML.P, ML.C)
+    h = h.reshape(ML.M, ML.d).numpy()
+    assert np.allclose(out["h"], h, rtol=0, atol=1e-10)
+    l = al.reshape(-1, 1) * (h @ w["E"].astype(np.float64).T) / math.sqrt(ML.d)
+    p = special.softmax(l / tau, axis=1)
+    assert np.allclose(out["H"], stats.entropy(p, axis=1), atol=1e-9)
+    assert np.allclose(out["u"], p @ w["E"].astype(np.float64), atol=1e-10)
+    # one layer of the stack: the single-layer step on that layer's weights and cache
+    one = dataclasses.replace(ML, L=1)
+    w1 = {k: (v[0] if k in ("Wq", "Wk", "Wv", "Wo", "Kc", "Vc") else v) for k, v in w.items()}
+    o1 = oracle.denoise_step(one, w1, x, z, al, tau=tau, b=0.1, seed=0, step=0, mirror_bf16=False, want=("h",))
+    h1, _ = _torch_layers(one, {k: (v[None] if k in ("Wq", "Wk", "Wv", "Wo") else v) for k, v in w1.items()},
+                          a0, w["Kc"][:1], w["Vc"][:1], ML.P, ML.C)
+    assert np.allclose(o1["h"], h1.reshape(ML.M, ML.d).numpy(), rtol=0, atol=1e-10)
+
+
+def _prefill_inputs(seed=13, n=7):
+    w, _, _, _ = _tiny_inputs(torch.float32, seed=seed, dims=ML)
+    tok = np.random.default_rng(seed).integers(0, ML.V, size=(ML.B, n)).astype(np.int32)
+    return w, tok
+
+
+def test_prefill_matches_causal_composition():
+    """or_prefill: the appended K/V of every layer equal a float64 composition with an explicit causal
+    mask (token i sees the cached rows and the new tokens 0..i); rows outside the block are untouched."""
+    w, tok = _prefill_inputs()
+    n = tok.shape[1]
+    Kn, Vn = oracle.prefill(ML, w, tok, P=ML.P, mirror_bf16=False)
+    e = torch.from_numpy(w["E"]).double()[torch.from_numpy(tok).long()]
+    a0 = torch.nn.functional.rms_norm(e, (ML.d,), eps=ML.rms_eps)
+    mask = torch.ones(n, ML.P + n, dtype=torch.bool)
+    mask[:, ML.P:] = torch.tril(torch.ones(n, n, dtype=torch.bool))
+    _, kv = _torch_layers(ML, w, a0, w["Kc"], w["Vc"], ML.P, n, mask=mask)
+    # the caches are float32 arrays: the appended rows carry their float32 rounding (~6e-8
+    # relative), which the deeper layers then read back
+    for l, (k, v) in enumerate(kv):
+        assert np.allclose(Kn[l][:, :, ML.P:ML.P + n], k.numpy(), rtol=1e-6, atol=1e-6), l
+        assert np.allclose(Vn[l][:, :, ML.P:ML.P + n], v.numpy(), rtol=1e-6, atol=1e-6), l
+    assert np.array_equal(Kn[:, :, :, :ML.P], w["Kc"][:, :, :, :ML.P])
+    assert np.array_equal(Kn[:, :, :, ML.P + n:], w["Kc"][:, :, :, ML.P + n:])
+
+
+def test_prefill_is_causal_and_chunked_prefill_is_one_piece():
+    """Changing token j leaves every layer's K/V of positions before j unchanged and changes the
+    deeper layers' K/V after j (they attend over it); layer 0's K/V of a position depend on that token
+    only.  Prefill in two pieces equals prefill in one (the second piece attends over the first)."""
+    w, tok = _prefill_inputs(seed=14)
+    n, j = tok.shape[1], 3
+    K1, V1 = oracle.prefill(ML, w, tok, P=ML.P, mirror_bf16=False)
+    t2 = tok.copy()
+    t2[:, j] = (t2[:, j] + 1) % ML.V
+    K2, _ = oracle.prefill(ML, w, t2, P=ML.P, mirror_bf16=False)
+    blk = slice(ML.P, ML.P + n)
+    for l in range(ML.L):
+        d = np.abs(K1[l][:, :, blk] - K2[l][:, :, blk]).max(axis=(1, 3))  # [B, n]
+        assert (d[:, :j] == 0).all(), l
+        assert (d[:, j] > 0).all(), l
+        if l == 0:
+            assert (d[:, j + 1:] == 0).all()
+        else:
+            assert (d[:, j + 1:] > 0).all(), l
+    wa = dict(w)
+    Ka, Va = oracle.prefill(ML, wa, tok[:, :4], P=ML.P, mirror_bf16=False)
+    wa["Kc"], wa["Vc"] = Ka, Va
+    Kb, Vb = oracle.prefill(ML, wa, tok[:, 4:], P=ML.P + 4, mirror_bf16=False)
+    assert np.array_equal(Kb, K1) and np.array_equal(Vb, V1)
+
+
+def test_one_layer_commit_is_the_prefill_of_one_block():
+    one = synth.Dims(V=300, d=64, C=12, B=2, Hq=4, Hkv=2, hd=16, F=64, P=10, cap=40)
+    w, _, _, _ = _tiny_inputs(torch.bfloat16, seed=15, dims=one)
+    tok = np.random.default_rng(15).integers(0, one.V, size=(one.B, one.C)).astype(np.int32)
+    Kc, Vc = oracle.commit(one, w["E"], w["Wk"], w["Wv"], tok, w["Kc"], w["Vc"], P=one.P)
+    Kp, Vp = oracle.prefill(one, w, tok, P=one.P)
+    assert np.array_equal(Kc, Kp) and np.array_equal(Vc, Vp)
