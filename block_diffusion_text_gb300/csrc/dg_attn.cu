@@ -99,7 +99,7 @@ __global__ void __launch_bounds__(128)
   float o[HD / 8][4];
 #pragma unroll
   for (int n = 0; n < HD / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
-  float m_run[2] = {-FLT_MAX, -FLT_MAX}, l_run[2] = {0.f, 0.f};
+  float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
   const int tq = lane % 4;
 
   for (int blk = 0; blk < nblk; ++blk) {
@@ -127,14 +127,17 @@ __global__ void __launch_bounds__(128)
         mma_bf16_16816(s[2 * j + 1], qa[ks], kb[2], kb[3]);
       }
     }
-    // Keys past the chunk end do not exist.
+    // Keys past the chunk end do not exist; with the causal mask (prefill),
+    // canvas query i sees canvas keys 0..i only.
     const int kbase = k_begin + blk * kAttnKeys;
+    const int qrow = q0 + warp * 16 + lane / 4;
 #pragma unroll
     for (int n = 0; n < 8; ++n) {
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int key = kbase + n * 8 + 2 * tq + (e & 1);
-        s[n][e] = key < k_end ? s[n][e] * scale_log2 : -FLT_MAX;
+        const bool seen = key < k_end && (!a.causal || key - a.P <= qrow + (e >> 1) * 8);
+        s[n][e] = seen ? s[n][e] * scale_log2 : -INFINITY;
       }
     }
 #pragma unroll
@@ -145,12 +148,14 @@ __global__ void __launch_bounds__(128)
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
       const float m_new = fmaxf(m_run[hr], mx);
-      const float corr = exp2f(m_run[hr] - m_new);
+      // a row that has seen no key yet (all masked so far) keeps weight 0
+      const float m_sub = m_new == -INFINITY ? 0.f : m_new;
+      const float corr = exp2f(m_run[hr] - m_sub);
       float rs = 0.f;
 #pragma unroll
       for (int n = 0; n < 8; ++n) {
-        s[n][2 * hr] = exp2f(s[n][2 * hr] - m_new);
-        s[n][2 * hr + 1] = exp2f(s[n][2 * hr + 1] - m_new);
+        s[n][2 * hr] = exp2f(s[n][2 * hr] - m_sub);
+        s[n][2 * hr + 1] = exp2f(s[n][2 * hr + 1] - m_sub);
         rs += s[n][2 * hr] + s[n][2 * hr + 1];
       }
       l_run[hr] = l_run[hr] * corr + rs;
@@ -346,7 +351,7 @@ static cudaError_t attn_impl(const AttnArgs& a, StopCtl ctl, cudaStream_t st) {
 cudaError_t launch_attention(const AttnArgs& a, StopCtl ctl, int* status, cudaStream_t st) {
   dg_dims D{};
   D.hd = a.hd;
-  if (attn_use_tc(D, a.P)) return launch_attention_tc(a, ctl, status, st);
+  if (!a.causal && attn_use_tc(D, a.P)) return launch_attention_tc(a, ctl, status, st);
   switch (a.hd) {
     case 32: return attn_impl<32>(a, ctl, st);
     case 64: return attn_impl<64>(a, ctl, st);

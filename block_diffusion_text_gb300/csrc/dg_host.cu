@@ -21,6 +21,7 @@ bool dims_ok(const dg_dims* D) {
     return false;
   if (D->Hq % D->Hkv != 0) return false;
   if (!(D->rope_base > 0.f) || !(D->rms_eps >= 0.f)) return false;
+  if (D->L < 1 || D->L > 64) return false;
   return true;
 }
 
@@ -71,6 +72,12 @@ dg_status check_ws(const dg_dims& D, int32_t cap, void* ws, size_t ws_bytes, WsL
   return DG_OK;
 }
 
+// Layer l of a stacked [L][n] bf16 weight, and a byte offset into a buffer.
+const void* layer_ptr(const void* w, int l, size_t n) {
+  return reinterpret_cast<const uint8_t*>(w) + (size_t)l * n * 2;
+}
+void* byte_ptr(void* p, size_t off) { return reinterpret_cast<uint8_t*>(p) + off; }
+
 struct Prof {
   void* const* ev;
   cudaStream_t st;
@@ -107,22 +114,33 @@ dg_status enqueue_step(const StepCtx& c, float tau, float b, float stop_H, uint6
                               fill_rope ? rope : nullptr, D, M,
                               P, ctl, status, c.st));
   DG_TRY(pf.mark(DG_PROF_EMBED, 1));
-  DG_TRY(pf.mark(DG_PROF_QKV, 0));
-  DG_TRY(launch_qkv(at<void>(ws, L.a), c.model->Wq, c.model->Wk, c.model->Wv, at<void>(ws, L.q),
-                    at<void>(ws, L.kc), at<void>(ws, L.vc), D.C, 0, rope, D, ctl, status,
-                    at<float>(ws, L.gpart), L.gpart_elems, c.st));
-  DG_TRY(pf.mark(DG_PROF_QKV, 1));
-  AttnArgs aa{at<void>(ws, L.q), c.cache->K, c.cache->V, at<void>(ws, L.kc), at<void>(ws, L.vc),
-              at<void>(ws, L.o), at<float>(ws, L.attn_o), at<float>(ws, L.attn_ml), D.B, D.C, D.Hq,
-              D.Hkv, D.hd, P, c.cache->cap};
-  DG_TRY(pf.mark(DG_PROF_ATTN, 0));
-  DG_TRY(launch_attention(aa, ctl, status, c.st));
-  DG_TRY(pf.mark(DG_PROF_ATTN, 1));
-  DG_TRY(pf.mark(DG_PROF_OPROJ, 0));
-  DG_TRY(launch_gemm_bf16(at<void>(ws, L.o), c.model->Wo, at<void>(ws, L.h), D.d, at<void>(ws, L.a), D.d,
-                          0, M, D.d, D.Hq * D.hd, D.C, ctl, status, at<float>(ws, L.gpart), L.gpart_elems,
-                          c.st));
-  DG_TRY(pf.mark(DG_PROF_OPROJ, 1));
+  // a2-a4 per layer; the profiling slots time the first layer's kernels (a
+  // deeper layer's RMSNorm of h goes with its projections)
+  const size_t nq = (size_t)D.Hq * D.hd, nkv = (size_t)D.Hkv * D.hd, dd = D.d;
+  const size_t cache_layer = (size_t)D.B * D.Hkv * c.cache->cap * D.hd * 2;
+  for (int l = 0; l < D.L; ++l) {
+    const Prof pl{l == 0 ? pf.ev : nullptr, c.st};
+    if (l > 0)
+      DG_TRY(launch_embed_rmsnorm(nullptr, nullptr, nullptr, at<void>(ws, L.a), nullptr, D, M, P, ctl, status,
+                                  c.st, at<void>(ws, L.h)));
+    DG_TRY(pl.mark(DG_PROF_QKV, 0));
+    DG_TRY(launch_qkv(at<void>(ws, L.a), layer_ptr(c.model->Wq, l, nq * dd), layer_ptr(c.model->Wk, l, nkv * dd),
+                      layer_ptr(c.model->Wv, l, nkv * dd), at<void>(ws, L.q), at<void>(ws, L.kc),
+                      at<void>(ws, L.vc), D.C, 0, rope, D, ctl, status, at<float>(ws, L.gpart), L.gpart_elems,
+                      c.st));
+    DG_TRY(pl.mark(DG_PROF_QKV, 1));
+    AttnArgs aa{at<void>(ws, L.q), byte_ptr(c.cache->K, l * cache_layer), byte_ptr(c.cache->V, l * cache_layer),
+                at<void>(ws, L.kc), at<void>(ws, L.vc), at<void>(ws, L.o), at<float>(ws, L.attn_o),
+                at<float>(ws, L.attn_ml), D.B, D.C, D.Hq, D.Hkv, D.hd, P, c.cache->cap, 0};
+    DG_TRY(pl.mark(DG_PROF_ATTN, 0));
+    DG_TRY(launch_attention(aa, ctl, status, c.st));
+    DG_TRY(pl.mark(DG_PROF_ATTN, 1));
+    DG_TRY(pl.mark(DG_PROF_OPROJ, 0));
+    DG_TRY(launch_gemm_bf16(at<void>(ws, L.o), layer_ptr(c.model->Wo, l, dd * nq), at<void>(ws, L.h), D.d,
+                            at<void>(ws, L.a), D.d, 0, M, D.d, D.Hq * D.hd, D.C, ctl, status,
+                            at<float>(ws, L.gpart), L.gpart_elems, c.st));
+    DG_TRY(pl.mark(DG_PROF_OPROJ, 1));
+  }
   LmArgs lm{};
   lm.h = at<void>(ws, L.h);
   lm.E = c.model->E;
@@ -487,26 +505,71 @@ dg_status dg_denoise_canvas_masked(const dg_model* model, const dg_kv_cache* cac
   return DG_OK;
 }
 
-dg_status dg_commit_block(const dg_model* model, dg_kv_cache* cache, const int32_t* tokens, void* ws,
-                          size_t ws_bytes, void* stream) {
+dg_status dg_prefill(const dg_model* model, dg_kv_cache* cache, const int32_t* tokens, int32_t n, void* ws,
+                     size_t ws_bytes, void* stream) {
   dg_status s = check_model(model);
   if (s) return s;
   if ((s = check_cache(model->dims, cache))) return s;
-  if (!tokens) return DG_ERR_ARG;
+  if (!tokens || n < 1) return DG_ERR_ARG;
   const dg_dims& D = model->dims;
   WsLayout L;
   if ((s = check_ws(D, cache->cap, ws, ws_bytes, &L))) return s;
-  if ((int64_t)cache->len + D.C > cache->cap) return DG_ERR_CAPACITY;
+  if ((int64_t)cache->len + n > cache->cap) return DG_ERR_CAPACITY;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   StopCtl none{nullptr, 0, 0};
+  int* status = at<int>(ws, L.status);
   float2* rope = at<float2>(ws, L.rope);
-  DG_TRY(launch_embed_rmsnorm(tokens, model->E, nullptr, at<void>(ws, L.a), rope, D, D.B * D.C, cache->len,
-                              none, at<int>(ws, L.status), st));
-  DG_TRY(launch_qkv(at<void>(ws, L.a), nullptr, model->Wk, model->Wv, nullptr, cache->K, cache->V,
-                    cache->cap, cache->len, rope, D, none, at<int>(ws, L.status), at<float>(ws, L.gpart),
-                    L.gpart_elems, st));
-  cache->len += D.C;
+  const size_t nq = (size_t)D.Hq * D.hd, nkv = (size_t)D.Hkv * D.hd, dd = D.d;
+  const size_t cache_layer = (size_t)D.B * D.Hkv * cache->cap * D.hd * 2;
+  // pieces of at most C tokens per canvas: the workspace holds B * C rows
+  for (int32_t done = 0; done < n;) {
+    const int np = n - done < D.C ? n - done : D.C;
+    dg_dims Dn = D;
+    Dn.C = np;
+    const int len = cache->len;
+    // this piece's tokens, [B][np], gathered from [B][n]
+    int32_t* tk = at<int32_t>(ws, L.amax);  // free between steps: the step rewrites it
+    DG_TRY(cudaMemcpy2DAsync(tk, 4 * (size_t)np, tokens + done, 4 * (size_t)n, 4 * (size_t)np, D.B,
+                             cudaMemcpyDeviceToDevice, st));
+    DG_TRY(launch_embed_rmsnorm(tk, model->E, nullptr, at<void>(ws, L.a), rope, Dn, D.B * np, len, none, status,
+                                st));
+    for (int l = 0; l < D.L; ++l) {
+      const bool last = l == D.L - 1;
+      if (l > 0)
+        DG_TRY(launch_embed_rmsnorm(nullptr, nullptr, nullptr, at<void>(ws, L.a), nullptr, Dn, D.B * np, len, none,
+                                    status, st, at<void>(ws, L.h)));
+      // k, v (and below the last layer q) of the piece into the workspace
+      DG_TRY(launch_qkv(at<void>(ws, L.a), last ? nullptr : layer_ptr(model->Wq, l, nq * dd),
+                        layer_ptr(model->Wk, l, nkv * dd), layer_ptr(model->Wv, l, nkv * dd), at<void>(ws, L.q),
+                        at<void>(ws, L.kc), at<void>(ws, L.vc), np, 0, rope, Dn, none, status,
+                        at<float>(ws, L.gpart), L.gpart_elems, st));
+      // ... appended to this layer's cache at rows len..len+np-1
+      const size_t row_bytes = (size_t)D.hd * 2;
+      for (int kv = 0; kv < 2; ++kv)
+        DG_TRY(cudaMemcpy2DAsync(byte_ptr(kv ? cache->V : cache->K, l * cache_layer + (size_t)len * row_bytes),
+                                 cache->cap * row_bytes, at<void>(ws, kv ? L.vc : L.kc), np * row_bytes,
+                                 np * row_bytes, (size_t)D.B * D.Hkv, cudaMemcpyDeviceToDevice, st));
+      if (last) break;
+      // causal attention over the cached rows and the piece, then the output
+      // projection with the residual
+      AttnArgs aa{at<void>(ws, L.q), byte_ptr(cache->K, l * cache_layer), byte_ptr(cache->V, l * cache_layer),
+                  at<void>(ws, L.kc), at<void>(ws, L.vc), at<void>(ws, L.o), at<float>(ws, L.attn_o),
+                  at<float>(ws, L.attn_ml), D.B, np, D.Hq, D.Hkv, D.hd, len, cache->cap, 1};
+      DG_TRY(launch_attention(aa, none, status, st));
+      DG_TRY(launch_gemm_bf16(at<void>(ws, L.o), layer_ptr(model->Wo, l, dd * nq), at<void>(ws, L.h), D.d,
+                              at<void>(ws, L.a), D.d, 0, D.B * np, D.d, D.Hq * D.hd, np, none, status,
+                              at<float>(ws, L.gpart), L.gpart_elems, st));
+    }
+    cache->len += np;
+    done += np;
+  }
   return DG_OK;
+}
+
+dg_status dg_commit_block(const dg_model* model, dg_kv_cache* cache, const int32_t* tokens, void* ws,
+                          size_t ws_bytes, void* stream) {
+  if (!model) return DG_ERR_ARG;
+  return dg_prefill(model, cache, tokens, model->dims.C, ws, ws_bytes, stream);
 }
 
 dg_status dg_debug_gemm(const void* A, const void* Bm, float* D, int32_t M, int32_t N, int32_t K,

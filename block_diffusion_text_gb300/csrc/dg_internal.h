@@ -159,6 +159,7 @@ struct AttnArgs {
   float* opart;             // fp32 [S][B][Hq][C][hd]
   float* ml;                // fp32 [S][B][Hq][C][2]
   int B, C, Hq, Hkv, hd, P, cap;
+  int causal;               // 1: canvas query i sees canvas keys 0..i only (prefill); takes the warp-MMA kernel
 };
 cudaError_t launch_attention(const AttnArgs& a, StopCtl ctl, int* status, cudaStream_t st);
 cudaError_t launch_attention_tc(const AttnArgs& a, StopCtl ctl, int* status, cudaStream_t st);
@@ -168,9 +169,11 @@ void attn_split_mma(const dg_dims& D, int T, int* nsplit, int* keys_per_split);
 
 // Misc kernels.
 // A token outside [0, V) is embedded as token 0 and sets DG_ERR_VALUE in *status.
+// src: optional bf16 [rows][d]; when given, a = RMSNorm(src) (a deeper
+// layer's input) and tokens, E, z are not read.
 cudaError_t launch_embed_rmsnorm(const int32_t* tokens, const void* E, const void* z, void* a,
                                  float2* rope, const dg_dims& D, int rows, int P, StopCtl ctl,
-                                 int* status, cudaStream_t st);
+                                 int* status, cudaStream_t st, const void* src = nullptr);
 struct StatsArgs {
   const float *pm, *pl, *pS, *pvmax;
   const int* pidx;

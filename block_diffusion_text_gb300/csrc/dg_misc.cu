@@ -60,18 +60,25 @@ struct RopeTheta {
 __global__ void __launch_bounds__(kEmbThreads)
     embed_rmsnorm_kernel(const int32_t* tokens, const __nv_bfloat16* E, const __nv_bfloat16* z,
                          __nv_bfloat16* a, float2* rope, int d, int V, float eps, int C, int P, int hd,
-                         RopeTheta theta, StopCtl ctl, int* status) {
+                         RopeTheta theta, StopCtl ctl, int* status, const __nv_bfloat16* src) {
   pdl_wait();
   if (all_stopped(ctl.stop_at, ctl.B, ctl.step)) return;
   const int row = blockIdx.x;
-  int tok = tokens[row];
-  if (tok < 0 || tok >= V) {  // never gather outside E: record the bad token, embed token 0
-    if (threadIdx.x == 0) atomicExch(status, kStatusValue);
-    tok = 0;
-  }
   const int nch = d / 8;
-  const uint4* e4 = reinterpret_cast<const uint4*>(E + (size_t)tok * d);
-  const uint4* z4 = z ? reinterpret_cast<const uint4*>(z + (size_t)row * d) : nullptr;
+  const uint4* e4;
+  const uint4* z4;
+  if (src) {  // a deeper layer: the residual stream h of the layer below
+    e4 = reinterpret_cast<const uint4*>(src + (size_t)row * d);
+    z4 = nullptr;
+  } else {
+    int tok = tokens[row];
+    if (tok < 0 || tok >= V) {  // never gather outside E: record the bad token, embed token 0
+      if (threadIdx.x == 0) atomicExch(status, kStatusValue);
+      tok = 0;
+    }
+    e4 = reinterpret_cast<const uint4*>(E + (size_t)tok * d);
+    z4 = z ? reinterpret_cast<const uint4*>(z + (size_t)row * d) : nullptr;
+  }
   float x[kEmbMaxChunks][8];
   float sh = 0.f, sl = 0.f;  // sum of squares as a float pair
 #pragma unroll
@@ -152,13 +159,13 @@ __global__ void __launch_bounds__(kEmbThreads)
 
 cudaError_t launch_embed_rmsnorm(const int32_t* tokens, const void* E, const void* z, void* a,
                                  float2* rope, const dg_dims& D, int rows, int P, StopCtl ctl,
-                                 int* status, cudaStream_t st) {
+                                 int* status, cudaStream_t st, const void* src) {
   RopeTheta th{};
   for (int j = 0; j < D.hd / 2 && j < 64; ++j) th.th[j] = std::pow((double)D.rope_base, -2.0 * j / D.hd);
   return launch_pdl(embed_rmsnorm_kernel, dim3(rows), dim3(kEmbThreads), 0, st, tokens,
                     reinterpret_cast<const __nv_bfloat16*>(E), reinterpret_cast<const __nv_bfloat16*>(z),
                     reinterpret_cast<__nv_bfloat16*>(a), rope, D.d, D.V, D.rms_eps, D.C, P, D.hd, th, ctl,
-                    status);
+                    status, reinterpret_cast<const __nv_bfloat16*>(src));
 }
 
 // ------------------------------------------------------- tile statistics --

@@ -27,7 +27,7 @@ DG_OK, DG_ERR_ARG, DG_ERR_SHAPE, DG_ERR_CAPACITY, DG_ERR_WORKSPACE, DG_ERR_CUDA,
 EXPORTS = ("dg_status_string", "dg_workspace_size", "dg_read_status", "dg_tau", "dg_canvas_init",
            "dg_denoise_step", "dg_denoise_canvas", "dg_commit_block", "dg_debug_gemm",
            "dg_attention_noalloc", "dg_attention_noalloc_status", "dg_debug_wait_timeout",
-           "dg_canvas_init_masked", "dg_denoise_step_masked", "dg_denoise_canvas_masked")
+           "dg_canvas_init_masked", "dg_denoise_step_masked", "dg_denoise_canvas_masked", "dg_prefill")
 
 
 class DgError(RuntimeError):
@@ -39,7 +39,7 @@ class DgError(RuntimeError):
 class dg_dims(ct.Structure):
     _fields_ = [("V", ct.c_int32), ("d", ct.c_int32), ("C", ct.c_int32), ("B", ct.c_int32),
                 ("Hq", ct.c_int32), ("Hkv", ct.c_int32), ("hd", ct.c_int32), ("F", ct.c_int32),
-                ("rope_base", ct.c_float), ("rms_eps", ct.c_float)]
+                ("rope_base", ct.c_float), ("rms_eps", ct.c_float), ("L", ct.c_int32)]
 
 
 class dg_model(ct.Structure):
@@ -115,6 +115,8 @@ def load():
                                             ct.POINTER(dg_canvas_result), ct.c_void_p]
             L.dg_commit_block.argtypes = [ct.POINTER(dg_model), ct.POINTER(dg_kv_cache), ct.c_void_p,
                                           ct.c_void_p, ct.c_size_t, ct.c_void_p]
+            L.dg_prefill.argtypes = [ct.POINTER(dg_model), ct.POINTER(dg_kv_cache), ct.c_void_p, ct.c_int32,
+                                     ct.c_void_p, ct.c_size_t, ct.c_void_p]
             L.dg_debug_wait_timeout.argtypes = [ct.POINTER(ct.c_int32), ct.c_void_p]
             L.dg_debug_gemm.argtypes = [ct.c_void_p, ct.c_void_p, ct.c_void_p, ct.c_int32, ct.c_int32,
                                         ct.c_int32, ct.c_int32, ct.c_void_p]
@@ -151,7 +153,7 @@ def _stream(stream=None):
 
 def make_dims(d) -> dg_dims:
     return dg_dims(V=d.V, d=d.d, C=d.C, B=d.B, Hq=d.Hq, Hkv=d.Hkv, hd=d.hd, F=d.F,
-                   rope_base=d.rope_base, rms_eps=d.rms_eps)
+                   rope_base=d.rope_base, rms_eps=d.rms_eps, L=getattr(d, "L", 1))
 
 
 def workspace_size(dims, cap: int) -> int:
@@ -167,7 +169,7 @@ class Model:
         self.dims = dims
         self.w = w
         self.K, self.V = w["Kc"], w["Vc"]
-        self.cap = self.K.shape[2]
+        self.cap = self.K.shape[-2]
         self.len = dims.P if cache_len is None else cache_len
         self.s = dg_model(make_dims(dims), *[ct.c_void_p(w[k].data_ptr()) for k in
                                              ("E", "Wq", "Wk", "Wv", "Wo", "W1", "W2")])
@@ -335,13 +337,24 @@ def commit_block(model: Model, tokens: torch.Tensor, stream=None, cache=None) ->
         cs = model.cache()
     else:
         K, V, n = cache
-        cs = dg_kv_cache(ct.c_void_p(K.data_ptr()), ct.c_void_p(V.data_ptr()), K.shape[2], int(n))
+        cs = dg_kv_cache(ct.c_void_p(K.data_ptr()), ct.c_void_p(V.data_ptr()), K.shape[-2], int(n))
     rc = load().dg_commit_block(ct.byref(model.s), ct.byref(cs), _ptr(tokens), model.ws_ptr,
                                 model.ws_bytes, _stream(stream))
     _check(rc, "dg_commit_block")
     if cache is None:
         model.len = cs.len
     return cs.len
+
+
+def prefill(model: Model, tokens: torch.Tensor, stream=None) -> int:
+    """Causal prefill of tokens [B, n] into every layer's cache (dg_prefill); returns the new length."""
+    cache = model.cache()
+    tok = tokens.contiguous()
+    rc = load().dg_prefill(ct.byref(model.s), ct.byref(cache), _ptr(tok), int(tok.shape[-1]), model.ws_ptr,
+                           model.ws_bytes, _stream(stream))
+    _check(rc, "dg_prefill")
+    model.len = cache.len
+    return cache.len
 
 
 def canvas_init(B, C, V, seed, block=0, device="cuda", stream=None) -> torch.Tensor:

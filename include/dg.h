@@ -78,15 +78,21 @@ enum {
  *   Hq   query heads, Hkv key/value heads (Hq % Hkv == 0, grouped-query)
  *   hd   head dim: 32, 64 or 128
  *   F    self-conditioning FFW hidden width (multiple of 64)
- *   rope_base  RoPE base (10000); rms_eps  RMSNorm epsilon (1e-6)          */
+ *   rope_base  RoPE base (10000); rms_eps  RMSNorm epsilon (1e-6)
+ *   L    attention layers (1..64).  The stand-in's layer l takes a_l (a_0 =
+ *        RMSNorm(E[x] + z)), h_l = a_l + Attn_l(a_l) Wo_l^T, a_{l+1} =
+ *        RMSNorm(h_l); the LM head reads h_{L-1}; layer l attends over its own
+ *        prefix cache.  L = 1 is the single-layer model.                       */
 typedef struct dg_dims {
   int32_t V, d, C, B, Hq, Hkv, hd, F;
   float rope_base, rms_eps;
+  int32_t L;
 } dg_dims;
 
 /* Weights (device, bf16):
  *   E  [V][d]        tied token embedding and LM head
- *   Wq [Hq*hd][d], Wk [Hkv*hd][d], Wv [Hkv*hd][d], Wo [d][Hq*hd]
+ *   Wq [L][Hq*hd][d], Wk [L][Hkv*hd][d], Wv [L][Hkv*hd][d], Wo [L][d][Hq*hd]
+ *   (one matrix per layer, stacked)
  *   W1 [F][d], W2 [d][F]                                                    */
 typedef struct dg_model {
   dg_dims dims;
@@ -95,9 +101,10 @@ typedef struct dg_model {
 
 /* Static prefix KV cache ([CH12] "prompt / finished output block -> causal
  * encoder prefill -> written to the KV cache"; [EXP] incremental prefill).
- * K, V: bf16 [B][Hkv][cap][hd]; rows 0..len-1 of every (canvas, head) are
- * valid, keys already rotated by RoPE at their absolute positions.  `len` is
- * a host value: every canvas of the batch has the same prefix length.      */
+ * K, V: bf16 [L][B][Hkv][cap][hd] (one cache per layer); rows 0..len-1 of
+ * every (layer, canvas, head) are valid, keys already rotated by RoPE at their
+ * absolute positions.  `len` is a host value: every canvas of the batch has
+ * the same prefix length.  dg_prefill writes it from a prompt.              */
 typedef struct dg_kv_cache {
   void *K, *V;
   int32_t cap;
@@ -241,10 +248,25 @@ DG_API dg_status dg_denoise_canvas(const dg_model* model, const dg_kv_cache* cac
                             const dg_sched* sched, uint64_t seed, int32_t block, void* ws,
                             size_t ws_bytes, dg_canvas_result* result, void* stream);
 
-/* Commit of a finished block, [TR] step 5 and [CH12] KV-cache timing: the
- * tokens int32 [B][C] are re-encoded by the encoder path (RMSNorm(E[x]), no
- * self-conditioning) and their keys (RoPE at positions len..len+C-1) and
- * values are written to cache rows len..len+C-1; then cache->len += C.
+/* Causal prefill, [TR] step 1 and [EXP] "Architecture: incremental prefill
+ * and denoising": tokens int32 [B][n] (n >= 1, any length) are appended to
+ * every layer's cache at rows len..len+n-1, then cache->len += n.  The
+ * encoder is the denoiser's attention stack with no self-conditioning (a_0 =
+ * RMSNorm(E[x])) and a causal mask: token i attends to every cached row and to
+ * the new tokens 0..i.  Per layer, k and v (RoPE at positions len + i) are
+ * written to the layer's cache; below the last layer q attends (causally)
+ * and h_l = a_l + o_l Wo_l^T, a_{l+1} = RMSNorm(h_l).  Tokens are processed in
+ * pieces of at most C per canvas, each attending over all earlier rows, which
+ * gives the same cache as one pass.  DG_ERR_CAPACITY (nothing written) if
+ * len + n > cap.                                                            */
+DG_API dg_status dg_prefill(const dg_model* model, dg_kv_cache* cache, const int32_t* tokens, int32_t n,
+                            void* ws, size_t ws_bytes, void* stream);
+
+/* Commit of a finished block, [TR] step 5 and [CH12] KV-cache timing (the
+ * cache comes from re-encoding the finished block, not from the denoiser's
+ * states): dg_prefill of the block's tokens int32 [B][C].  With one layer the
+ * appended K/V depend only on each token and its position; with more, the
+ * deeper layers' K/V depend on the causal attention over earlier tokens.
  * DG_ERR_CAPACITY (nothing written) if len + C > cap.                       */
 DG_API dg_status dg_commit_block(const dg_model* model, dg_kv_cache* cache, const int32_t* tokens,
                           void* ws, size_t ws_bytes, void* stream);

@@ -199,3 +199,19 @@ def test_masked_entry_points_validate(dg):
                                       None, None) == dg.DG_ERR_ARG
     assert L.dg_canvas_init_masked(None, 1, 16, 5, None) == dg.DG_ERR_ARG
     assert L.dg_canvas_init_masked(ct.c_void_p(FAKE), 1, 16, -1, None) == dg.DG_ERR_ARG
+
+
+def test_layers_and_prefill_validate(dg):
+    L = dg.load()
+    n = ct.c_size_t()
+    for bad in (0, 65):
+        dd = dg.make_dims(_dims())
+        dd.L = bad
+        assert L.dg_workspace_size(ct.byref(dd), 2048, ct.byref(n)) == dg.DG_ERR_ARG
+    dims = _dims()
+    m, c, cv, wsb = _structs(dg, dims, cap=2100, length=2048)
+    ws = ct.c_void_p(1 << 30)
+    assert L.dg_prefill(ct.byref(m), ct.byref(c), ct.c_void_p(FAKE), 0, ws, wsb, None) == dg.DG_ERR_ARG
+    assert L.dg_prefill(ct.byref(m), ct.byref(c), None, 10, ws, wsb, None) == dg.DG_ERR_ARG
+    assert L.dg_prefill(ct.byref(m), ct.byref(c), ct.c_void_p(FAKE), 53, ws, wsb, None) == dg.DG_ERR_CAPACITY
+    assert c.len == 2048

@@ -8,8 +8,9 @@ import torch
 import oracle
 from block_diffusion_text_gb300 import synth
 
-from parity import (Collect, bf16_to_np, check_argmax, check_close_bf16, check_entropy, check_logits,
-                    check_rel_l2, check_sampler)
+from parity import (Collect, bf16_to_np, check_argmax, check_entropy, check_logits, check_rel_l2,
+                    check_sampler)
+from parity import check_close_bf16 as _close
 
 pytestmark = pytest.mark.gpu
 
@@ -44,7 +45,7 @@ def _entropy_given_device_h(dims, w, alpha, h_dev, tau):
 
 
 def _run_and_compare(dims, seed, tau=0.8, b=0.1, step=0, alpha=None, z_in=None, prev=None,
-                     entropy_given_h=False):
+                     entropy_given_h=False, e2e_bound=None):
     from block_diffusion_text_gb300 import dg
     w, x, z, a, model, canvas = _setup(dims, seed, alpha)
     if z_in is not None:
@@ -65,11 +66,19 @@ def _run_and_compare(dims, seed, tau=0.8, b=0.1, step=0, alpha=None, z_in=None, 
     dbg = out["debug"]
     B, C, Hq, Hkv, hd = dims.B, dims.C, dims.Hq, dims.Hkv, dims.hd
     ck = Collect()
-    # a = RMSNorm(E[x] + z) is the correctly rounded bf16 of its definition on both sides
+    ul = 8 * dims.L  # the last layer's operands carry every earlier layer's rounding
+
+    def check_close_bf16(name, got, ref_):
+        return _close(name, got, ref_, ulps=ul)
+    # a = RMSNorm(E[x] + z) is the correctly rounded bf16 of its definition on both sides; a deeper
+    # layer's input RMSNorm(h) is compared like the other operands (h itself is within tolerance)
     def a_exact():
         n = int((bf16_to_np(dbg["a"]) != ref["a"]).sum())
         assert n == 0, f"a: {n} elements differ from the oracle"
-    ck(a_exact)
+    if dims.L == 1:
+        ck(a_exact)
+    else:
+        ck(check_close_bf16, "a", bf16_to_np(dbg["a"]), ref["a"])
     q = bf16_to_np(dbg["q"]).reshape(B, Hq, C, hd).transpose(0, 2, 1, 3).reshape(B * C, Hq * hd)
     ck(check_close_bf16, "q", q, ref["q"])
     k = bf16_to_np(dbg["k"]).reshape(B, Hkv, C, hd).transpose(0, 2, 1, 3).reshape(B * C, Hkv * hd)
@@ -86,9 +95,11 @@ def _run_and_compare(dims, seed, tau=0.8, b=0.1, step=0, alpha=None, z_in=None, 
         print(f"parity-report entropy end to end: max {e2e.max():.3e} nats, "
               f"{int((e2e > 1e-3).sum())} of {e2e.size} rows above 1e-3")
 
-        def e2e_bound():
-            assert e2e.max() <= LONG_CANVAS_H_BOUND, f"entropy end to end {e2e.max():.3e} > {LONG_CANVAS_H_BOUND}"
-        ck(e2e_bound)
+        bound = LONG_CANVAS_H_BOUND if e2e_bound is None else e2e_bound
+
+        def e2e_within():
+            assert e2e.max() <= bound, f"entropy end to end {e2e.max():.3e} > {bound}"
+        ck(e2e_within)
         # given the device's own h: the LM head and the statistics merge, to the stated 1e-3
         ck(check_entropy, Hg, _entropy_given_device_h(dims, synth.to_numpy_f32(w), a.numpy(), bf16_to_np(dbg["h"]),
                                                       tau))
