@@ -52,7 +52,8 @@ class StepIn(ct.Structure):
     _fields_ = [("E", _F), ("Wq", _F), ("Wk", _F), ("Wv", _F), ("Wo", _F), ("W1", _F), ("W2", _F),
                 ("Kc", _F), ("Vc", _F), ("x", _I), ("z", _F), ("alpha", _F), ("prev_argmax", _I),
                 ("tau", ct.c_double), ("b", ct.c_double), ("stop_H", ct.c_double),
-                ("seed", ct.c_uint64), ("step", ct.c_int32), ("block", ct.c_int32), ("exclude_tok", ct.c_int32)]
+                ("seed", ct.c_uint64), ("step", ct.c_int32), ("block", ct.c_int32), ("exclude_tok", ct.c_int32),
+                ("E8", _U8), ("E8_scale", _F)]
 
 
 class StepOut(ct.Structure):
@@ -79,6 +80,11 @@ def lib():
             L.or_prefill.restype = ct.c_int
             L.or_reveal.argtypes = [_D, _I, _I, ct.c_int32, ct.c_int32, ct.c_int32, ct.c_int32, _U8]
             L.or_reveal.restype = ct.c_int32
+            L.or_round_e4m3.argtypes = [ct.c_double]
+            L.or_round_e4m3.restype = ct.c_double
+            L.or_e4m3_value.argtypes = [ct.c_uint8]
+            L.or_e4m3_value.restype = ct.c_double
+            L.or_quantize_rows_e4m3.argtypes = [_F, ct.c_int64, ct.c_int64, _U8, _F]
             L.or_tau.argtypes = [ct.c_double, ct.c_double, ct.c_int32, ct.c_int32]
             L.or_tau.restype = ct.c_double
             L.or_gumbel.argtypes = [ct.c_uint64]
@@ -174,6 +180,24 @@ def gumbel_many(seed, n):
     out = np.zeros(n, dtype=np.float32)
     lib().or_gumbel_many(seed, n, _p(out, _F))
     return out
+
+
+def round_e4m3(x: float) -> float:
+    return float(lib().or_round_e4m3(float(x)))
+
+
+def e4m3_value(b: int) -> float:
+    return float(lib().or_e4m3_value(int(b)))
+
+
+def quantize_rows_e4m3(X):
+    """Per-row E4M3 codes and scales of a float32 matrix [R, d] (or_quantize_rows_e4m3)."""
+    Xf = _f32(X)
+    R, d = Xf.shape
+    Q = np.zeros((R, d), np.uint8)
+    sc = np.zeros(R, np.float32)
+    lib().or_quantize_rows_e4m3(_p(Xf, _F), R, d, _p(Q, _U8), _p(sc, _F))
+    return Q, sc
 
 
 def round_bf16(x: float) -> float:
@@ -284,13 +308,16 @@ _WANT_ALL = ("a", "q", "k", "v", "o", "h", "logits", "H", "m", "Z", "top2gap", "
 
 
 def denoise_step(dims, w, x, z, alpha, tau, b, seed, step, block=0, prev_argmax=None,
-                 stop_H=0.005, mirror_bf16=True, rows=None, want=None, nthreads=None, exclude_tok=-1):
+                 stop_H=0.005, mirror_bf16=True, rows=None, want=None, nthreads=None, exclude_tok=-1,
+                 fp8_head=None):
     """Run one oracle denoising step.
 
     dims: an object with V, d, C, B, Hq, Hkv, hd, F, P, cap, rope_base, rms_eps.
     w: dict of float32 numpy arrays E, Wq, Wk, Wv, Wo, W1, W2, Kc, Vc.
     x [B, C] int32, z [B, C, d] float32, alpha [B, C] float32.
     rows: optional list of global rows (b * C + i) for the vocabulary stages.
+    fp8_head: optional (E8 uint8 [V, d], scale float32 [V]) from quantize_rows_e4m3(E): the LM head
+    in FP8 (h quantized per row the same way); the embedding and p0 . E keep E.
     want: names of outputs to return (default: everything except logits).  In rows mode the
     logits are returned for the listed rows only, in their order ([len(rows), V]).
     """
@@ -316,9 +343,14 @@ def denoise_step(dims, w, x, z, alpha, tau, b, seed, step, block=0, prev_argmax=
     keep = [_f32(w[k]) for k in ("E", "Wq", "Wk", "Wv", "Wo", "W1", "W2", "Kc", "Vc")]
     xx, zz, aa = _i32(x), _f32(z), _f32(alpha)
     pa = _i32(prev_argmax) if prev_argmax is not None else None
+    e8 = es = None
+    if fp8_head is not None:
+        e8 = np.ascontiguousarray(np.asarray(fp8_head[0], np.uint8))
+        es = _f32(fp8_head[1])
     si = StepIn(*[_p(a, _F) for a in keep], _p(xx, _I), _p(zz, _F), _p(aa, _F),
                 _p(pa, _I) if pa is not None else None, float(tau), float(b), float(stop_H),
-                int(seed), int(step), int(block), int(exclude_tok))
+                int(seed), int(step), int(block), int(exclude_tok),
+                _p(e8, _U8) if e8 is not None else None, _p(es, _F) if es is not None else None)
     rr = _i32(rows) if rows is not None else None
     nrows = 0 if rr is None else rr.size
     if rr is not None and rr.size == 0:

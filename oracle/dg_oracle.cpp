@@ -82,7 +82,52 @@ double round_bf16(double x) {
 
 inline double maybe_bf16(double x, int mirror) { return mirror ? round_bf16(x) : x; }
 
+// ---------------------------------------------------------------- E4M3 ----
+// The 8-bit floating-point format E4M3 of the FP8 LM head: sign, 4 exponent
+// bits biased by 7, 3 mantissa bits; no infinities, the all-ones pattern is
+// NaN, so the largest finite magnitude is 1.75 * 2^8 = 448; subnormals step by
+// 2^-9.  Rounding is to nearest, ties to even, saturating at 448 (values that
+// would round past it become 448).
+double round_e4m3(double x) {
+  if (x == 0.0 || std::isnan(x)) return x;
+  const double a = std::fabs(x);
+  double r;
+  if (a >= 464.0) {
+    r = 448.0;  // 464 is the midpoint between 448 and the first value past the range
+  } else {
+    int e;
+    std::frexp(a, &e);  // a = f 2^e, 0.5 <= f < 1: the leading bit is 2^(e-1)
+    const int lead = e - 1 < -6 ? -6 : e - 1;  // subnormals share the exponent of 2^-6
+    const double q = std::ldexp(1.0, lead - 3);
+    r = std::nearbyint(a / q) * q;  // a / q is exact (a power-of-two scale)
+    if (r > 448.0) r = 448.0;
+  }
+  return std::copysign(r, x);
+}
+
+// The bit pattern of an E4M3 value produced by round_e4m3 (the sign of a zero
+// result is kept).
+uint8_t e4m3_bits(double r, bool negative) {
+  const uint8_t sign = negative ? 0x80 : 0x00;
+  const double a = std::fabs(r);
+  if (a == 0.0) return sign;
+  int e;
+  std::frexp(a, &e);
+  const int E = e - 1;
+  if (E < -6) return sign | (uint8_t)std::lrint(a / std::ldexp(1.0, -9));  // subnormal: m 2^-9
+  const int m = (int)std::lrint((a / std::ldexp(1.0, E) - 1.0) * 8.0);
+  return sign | (uint8_t)((E + 7) << 3) | (uint8_t)m;
+}
+
+double e4m3_value(uint8_t b) {
+  const int sign = b >> 7, E = (b >> 3) & 15, m = b & 7;
+  const double a = E == 0 ? std::ldexp((double)m, -9) : std::ldexp(1.0 + m / 8.0, E - 7);
+  return sign ? -a : a;
+}
+
 }  // namespace
+
+extern "C" void or_quantize_rows_e4m3(const float* X, int64_t R, int64_t d, uint8_t* Q, float* scale);
 
 extern "C" {
 
@@ -336,6 +381,12 @@ typedef struct {
   // [MASK] token of masked confidence decoding, which is not a prediction
   // target
   int32_t exclude_tok;
+  // FP8 LM head, or NULL: E8 [V][d] E4M3 codes of E with per-row scales
+  // E8_scale [V] (or_quantize_rows_e4m3 of E).  The logits then read h
+  // quantized the same way per row: l_v = alpha s_h s_v (q_h . q_v) / sqrt(d).
+  // The embedding and the contraction p0 . E keep the bf16 E.
+  const uint8_t* E8;
+  const float* E8_scale;
 } or_step_in;
 
 typedef struct {
@@ -501,10 +552,26 @@ int or_denoise_step(const or_dims* D, const or_step_in* in, or_step_out* out, co
     std::vector<double> lrow(V);
     const double* hr = &hh[r * d];
     double al = (double)in->alpha[r];
-    for (int64_t vv = 0; vv < V; ++vv) {
-      double acc = 0.0;
-      for (int64_t j = 0; j < d; ++j) acc += hr[j] * (double)in->E[vv * d + j];
-      lrow[vv] = al * acc * inv_sqrt_d;
+    if (in->E8) {
+      // FP8 head: h quantized per row (h is bf16-representable, so float exact)
+      std::vector<float> hf(d);
+      std::vector<uint8_t> hq(d);
+      float hs;
+      for (int64_t j = 0; j < d; ++j) hf[j] = (float)hr[j];
+      or_quantize_rows_e4m3(hf.data(), 1, d, hq.data(), &hs);
+      std::vector<double> hv(d);
+      for (int64_t j = 0; j < d; ++j) hv[j] = e4m3_value(hq[j]);
+      for (int64_t vv = 0; vv < V; ++vv) {
+        double acc = 0.0;
+        for (int64_t j = 0; j < d; ++j) acc += hv[j] * e4m3_value(in->E8[vv * d + j]);
+        lrow[vv] = al * ((double)hs * (double)in->E8_scale[vv] * acc) * inv_sqrt_d;
+      }
+    } else {
+      for (int64_t vv = 0; vv < V; ++vv) {
+        double acc = 0.0;
+        for (int64_t j = 0; j < d; ++j) acc += hr[j] * (double)in->E[vv * d + j];
+        lrow[vv] = al * acc * inv_sqrt_d;
+      }
     }
     if (out->logits) std::memcpy(&out->logits[(full ? r : t) * V], lrow.data(), sizeof(double) * V);
     if (in->exclude_tok >= 0 && in->exclude_tok < V) lrow[in->exclude_tok] = -INFINITY;
@@ -803,5 +870,34 @@ int or_commit(const or_dims* D, const float* E, const float* Wk, const float* Wv
 }
 
 double or_round_bf16(double x) { return round_bf16(x); }
+
+double or_round_e4m3(double x) { return round_e4m3(x); }
+double or_e4m3_value(uint8_t b) { return e4m3_value(b); }
+
+// Per-row quantization to E4M3 with one scale per row (the FP8 LM head's
+// operands: its A rows h and its B rows E): scale = absmax / 448 and
+// q_j = E4M3(x_j * (448 / absmax)), both quotients and the product rounded to
+// float32 (the arithmetic is fixed to float32 so that every implementation of
+// this definition gives the same bytes); x_j ~= q_j * scale.  A zero row has
+// scale 0 and zero codes.  Pinned by test_quantize_rows_e4m3_matches_torch.
+void or_quantize_rows_e4m3(const float* X, int64_t R, int64_t d, uint8_t* Q, float* scale) {
+  for (int64_t r = 0; r < R; ++r) {
+    const float* x = X + r * d;
+    float amax = 0.0f;
+    for (int64_t j = 0; j < d; ++j) amax = std::max(amax, std::fabs(x[j]));
+    if (!(amax > 0.0f)) {
+      scale[r] = 0.0f;
+      for (int64_t j = 0; j < d; ++j) Q[r * d + j] = 0;
+      continue;
+    }
+    const float sc = amax / 448.0f;
+    const float inv = 448.0f / amax;
+    scale[r] = sc;
+    for (int64_t j = 0; j < d; ++j) {
+      const float xs = x[j] * inv;
+      Q[r * d + j] = e4m3_bits(round_e4m3((double)xs), std::signbit(xs));
+    }
+  }
+}
 
 }  // extern "C"

@@ -715,3 +715,64 @@ def test_one_layer_commit_is_the_prefill_of_one_block():
     Kc, Vc = oracle.commit(one, w["E"], w["Wk"], w["Wv"], tok, w["Kc"], w["Vc"], P=one.P)
     Kp, Vp = oracle.prefill(one, w, tok, P=one.P)
     assert np.array_equal(Kc, Kp) and np.array_equal(Vc, Vp)
+
+
+
+# ----------------------------------------------------------------- E4M3 ---
+def test_round_e4m3_matches_torch():
+    """Round to nearest even in E4M3 equals torch's float8_e4m3fn conversion below the saturation
+    point (torch gives NaN past the range; this rounding saturates at 448)."""
+    rng = np.random.default_rng(3)
+    x = np.concatenate([rng.uniform(-463.9, 463.9, 20000), rng.standard_normal(20000) * 1e-2,
+                        rng.standard_normal(5000) * 1e-3, np.arange(-448, 449, 0.5),
+                        (np.arange(1, 64) + 0.5) * 2.0 ** -9])  # subnormal ties
+    x = x.astype(np.float32)
+    want = torch.from_numpy(x).to(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = np.array([oracle.round_e4m3(float(v)) for v in x])
+    assert np.array_equal(got, want)
+    assert oracle.round_e4m3(464.0) == 448.0 and oracle.round_e4m3(-1e9) == -448.0
+    assert oracle.round_e4m3(463.99) == 448.0
+
+
+def test_e4m3_codes_decode_like_torch():
+    codes = np.array([c for c in range(256) if (c & 0x7f) != 0x7f], np.uint8)
+    want = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = np.array([oracle.e4m3_value(int(c)) for c in codes])
+    assert np.array_equal(got, want)
+
+
+def test_quantize_rows_e4m3_matches_torch():
+    """Codes and scales equal the same definition written with torch float32 arithmetic
+    (scale = absmax / 448, codes of x * (448 / absmax)); decoded rows are within E4M3's relative step."""
+    rng = np.random.default_rng(4)
+    X = (rng.standard_normal((64, 200)) * rng.uniform(0.01, 10, (64, 1))).astype(np.float32)
+    X[5] = 0.0
+    Q, sc = oracle.quantize_rows_e4m3(X)
+    t = torch.from_numpy(X)
+    amax = t.abs().amax(dim=1)
+    inv = torch.where(amax > 0, torch.tensor(448.0) / amax, torch.zeros_like(amax))
+    want_q = (t * inv[:, None]).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    want_q[5] = 0
+    assert np.array_equal(Q, want_q)
+    assert np.array_equal(sc, (amax / 448.0).numpy())
+    dq = torch.from_numpy(Q).view(torch.float8_e4m3fn).double().numpy() * sc[:, None]
+    assert np.all(np.abs(dq - X) <= 2.0 ** -4 * np.abs(X) + 2.0 ** -9 * sc[:, None] + 1e-30)
+
+
+def test_fp8_head_logits_are_the_quantized_product():
+    """With an FP8 head the oracle's logits are alpha s_h s_v (q_h . q_v) / sqrt(d) for h quantized per
+    row (recomputed here with numpy from the oracle's h and the quantizer), and the contraction
+    keeps the bf16 E."""
+    from scipy import special
+    w, x, z, a = _tiny_inputs(torch.bfloat16, seed=6)
+    E8, sE = oracle.quantize_rows_e4m3(w["E"])
+    tau = 0.8
+    out = oracle.denoise_step(TINY, w, x, z, a, tau=tau, b=0.1, seed=1, step=0, want=("h", "logits", "u"),
+                              fp8_head=(E8, sE))
+    hq, hs = oracle.quantize_rows_e4m3(out["h"].astype(np.float32))
+    dec = lambda q: torch.from_numpy(q).view(torch.float8_e4m3fn).double().numpy()
+    l = a.reshape(-1, 1) * (hs[:, None].astype(np.float64) * sE[None, :].astype(np.float64) *
+                            (dec(hq) @ dec(E8).T)) / math.sqrt(TINY.d)
+    assert np.allclose(out["logits"], l, rtol=1e-12, atol=1e-12)
+    p = special.softmax(l / tau, axis=1)
+    assert np.allclose(out["u"], np.vectorize(oracle.round_bf16)(p @ w["E"].astype(np.float64)), atol=2e-3)
