@@ -51,6 +51,7 @@ def _args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-loop", action="store_true")
+    ap.add_argument("--no-variants", action="store_true")
     return ap.parse_args()
 
 
@@ -185,6 +186,12 @@ def kernel_work(d: synth.Dims):
     """(FLOPs, algorithmic bytes) per launch of the timed kernel slots."""
     w = stage_work(d)
     return {"lmhead": w["lmhead"], "selfcond": w["selfcond"], "attn": w["attn"]}
+
+
+def fp8_lmhead_work(d: synth.Dims):
+    """The FP8 LM head: the same FLOPs, E4M3 codes of E and h plus their per-row scales."""
+    M, V, D = d.B * d.C, d.V, d.d
+    return (2.0 * M * V * D, 1.0 * V * D + 4.0 * V + 1.0 * M * D + 4.0 * M + 4.0 * M)
 
 
 def step_roofline(d: synth.Dims, peaks):
@@ -453,6 +460,83 @@ def run_ours(args, world, rank, local):
                "note": "sum over stages of max(FLOPs / sustained bf16 peak, algorithmic bytes / HBM peak); "
                        "E read once per step for both vocabulary products"}
 
+    # Variants of the same step, each captured as K' steps in one CUDA graph: the FP8 LM head
+    # (E4M3 E and h on the kind::f8f6f4 tensor cores) and masked confidence decoding (the
+    # second sampler, [MASK] = the last token id)
+    variants = None
+    if rank == 0 and not args.no_variants:
+        variants = {}
+        kv = min(args.steps, 50)
+
+        def time_graph(fn, n):
+            cap = torch.cuda.Stream()
+            cap.wait_stream(stream)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=cap):
+                for s in range(n):
+                    fn(s)
+            torch.cuda.synchronize()
+            g.replay()  # warm replay
+            torch.cuda.synchronize()
+            a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a0.record(stream)
+            g.replay()
+            a1.record(stream)
+            torch.cuda.synchronize()
+            return a0.elapsed_time(a1) / n
+
+        m8 = dg.Model(dims, w, fp8_head=True)
+        c8 = dg.Canvas(x0.clone(), z0.clone(), a)
+        o8 = [None]
+        lm_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * len(slots))] for _ in range(kv)]
+        for row in lm_ev:  # recorded once so that the handles exist before the capture
+            for e in row:
+                e.record(stream)
+
+        def step8(s, events=None):
+            o8[0] = dg.denoise_step(m8, c8, tau=taus[s % 48], b=0.1, seed=seed, step=s % 48, out=o8[0],
+                                    events=events)
+        for s in range(3):
+            step8(s)
+        torch.cuda.synchronize()
+        ms8 = time_graph(step8, kv)
+        time_graph(lambda s: step8(s, events=lm_ev[s]), kv)
+        k = slots.index("lmhead")
+        lm8 = statistics.mean(lm_ev[s][2 * k].elapsed_time(lm_ev[s][2 * k + 1]) for s in range(kv))
+        fl8, by8 = fp8_lmhead_work(dims)
+        pk8 = 2.0 * peaks["tc_sustained"]
+        variants["fp8_lm_head"] = {
+            "value": 1e3 / ms8, "unit": UNIT, "ms_per_step": ms8, "steps": kv, "dtype": "e4m3 x e4m3 -> f32",
+            "lmhead_ms": lm8, "lmhead_bf16_ms": per_kernel.get("lmhead"),
+            "lmhead_roofline": {"bound": "tensor", "achieved": fl8 / (lm8 / 1e3) / 1e12, "peak": pk8,
+                                "unit": "TFLOP/s", "frac": fl8 / (lm8 / 1e3) / 1e12 / pk8,
+                                "hbm_gbs": by8 / (lm8 / 1e3) / 1e9, "algorithmic": {"flop": fl8, "bytes": by8},
+                                "peak_note": "2 x measured sustained bf16 (the nominal fp8 / bf16 ratio)"},
+            "note": "the lmhead slot includes the per-step E4M3 quantization of h"}
+        if m8.status() != 0:
+            raise RuntimeError("device status word set in the FP8 variant")
+        del m8, c8, o8
+
+        mask_id = dims.V - 1
+        cm = dg.Canvas(dg.canvas_init_masked(dims.B, dims.C, mask_id, device=dev), z0.clone(), a)
+        om = [None]
+        tok_m0 = cm.tokens.clone()
+
+        def stepm(s):
+            if s % 16 == 0:
+                cm.tokens.copy_(tok_m0)  # a fresh all-[MASK] canvas every 16 steps
+            om[0] = dg.denoise_step(model, cm, tau=1.0, b=0.0, seed=seed, step=s % 16, out=om[0],
+                                    masked=(mask_id, 16))
+        for s in range(3):
+            stepm(s)
+        torch.cuda.synchronize()
+        msm = time_graph(stepm, 48)
+        variants["masked_confidence"] = {
+            "value": 1e3 / msm, "unit": UNIT, "ms_per_step": msm, "steps": 48,
+            "note": "masked confidence decoding, 16 steps per canvas (reveal ceil(unresolved / steps left))"}
+        if model.status() != 0:
+            raise RuntimeError("device status word set in the masked variant")
+
     # the annealed loop itself (dg_denoise_canvas, up to 48 steps with adaptive stop) from the
     # benchmark's initial canvas, and the commit of its result
     loop = None
@@ -506,6 +590,7 @@ def run_ours(args, world, rank, local):
                          "tensor_frac": dom["tensor_frac"], "hbm_frac": dom["hbm_frac"]},
             "step_roofline": step_rl,
             "loop": loop,
+            "variants": variants,
             "kernels": rl,
             "kernel_ms": {k: round(v, 5) for k, v in per_kernel.items()},
             "timing": "K steps captured in one CUDA graph, CUDA events around its replay; per-kernel "

@@ -254,6 +254,14 @@ __host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool b_mn_major) 
          | ((uint32_t)(M >> 4) << 24);
 }
 
+// Instruction descriptor of tcgen05.mma kind::f8f6f4 with E4M3 A and B (format
+// 0 in both fields), fp32 D, both K-major, shape M x N (K = 32 per instruction).
+__host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N) {
+  return (1u << 4)                                  // D format: f32
+         | ((uint32_t)(N >> 3) << 17)               // N / 8
+         | ((uint32_t)(M >> 4) << 24);              // M / 16
+}
+
 // Instruction descriptor of tcgen05.mma kind::f16: bf16 A and B, fp32 D,
 // A K-major, B K-major or MN-major, shape M x N (K = 16 per instruction).
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool b_mn_major) {
@@ -340,6 +348,15 @@ DG_DEV void umma_bf16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint
   asm volatile(
       "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
       " tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accum)
+      : "memory");
+}
+// The same with E4M3 operands (kind::f8f6f4): 32 bytes of K per instruction,
+// as for bf16, so the shared-memory descriptors advance alike.
+DG_DEV void umma_e4m3_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t accum) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accum)
       : "memory");
 }

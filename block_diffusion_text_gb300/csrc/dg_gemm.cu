@@ -202,12 +202,20 @@ struct EpiLM {
   float* logits;
   int M, V;
   int excl;  // vocabulary column left out of the softmax (the [MASK] token), or -1
+  const float* rowscale;  // FP8 head: per-row scale of h (else null)
+  const float* colscale;  // FP8 head: per-row scale of E, i.e. per column of the tile (else null)
+  // The accumulator of column col, scaled for the FP8 head.
+  DG_DEV void scale_cols(float (&v)[32], int col0, int N) const {
+    if (!colscale) return;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] *= __ldg(colscale + (col0 + j < N ? col0 + j : N - 1));
+  }
   // Statistics per group of kStatCols columns, so that a tile may be 128 or
   // 256 columns wide.
   template <int BN, class LD>
   DG_DEV void tile(int row, bool ok, int n0, int N, LD& ld, int /*split*/) const {
     static_assert(BN % kStatCols == 0, "a tile holds whole statistics groups");
-    const float al = ok ? __ldg(alpha + row) : 1.0f;
+    const float al = (ok ? __ldg(alpha + row) : 1.0f) * (rowscale && ok ? __ldg(rowscale + row) : 1.0f);
     const float c2 = al * coef2;
     const int NT = (V + kStatCols - 1) / kStatCols;
 #pragma unroll 1
@@ -220,6 +228,7 @@ struct EpiLM {
       for (int c = 0; c < kStatCols / 32; ++c) {
         float v[32];
         ld(g * (kStatCols / 32) + c, v);
+        scale_cols(v, g0 + c * 32, N);
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
           const int col = g0 + c * 32 + j;
@@ -236,6 +245,7 @@ struct EpiLM {
         float v[32];
         ld(g * (kStatCols / 32) + c, v);
         const int col0 = g0 + c * 32;
+        scale_cols(v, col0, N);
         uint32_t pk[16];
 #pragma unroll
         for (int j = 0; j < 32; j += 2) {
@@ -467,7 +477,7 @@ static int num_sms() {
 }
 
 bool make_tmap_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
-                  uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer) {
+                  uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, bool u8) {
   typedef CUresult (*EncodeFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
                                const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
@@ -486,7 +496,8 @@ bool make_tmap_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t o
   cuuint64_t strides[1] = {row_bytes};
   cuuint32_t box[2] = {box_inner, box_outer};
   cuuint32_t es[2] = {1, 1};
-  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+  CUresult r = fn(map, u8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                  const_cast<void*>(base), dims, strides,
                   box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
@@ -539,15 +550,19 @@ struct PairLayout {
 // TAIL: when the last round of tiles would leave clusters idle (fewer
 // remaining tiles than clusters), those tiles are cut into two halves of BN / 2
 // columns (loaded through mBh, boxes of BN / 4 rows), so the round is shorter.
-template <int BN, int STAGES, bool B_MN, class Epi, bool TAIL = false>
+// F8: E4M3 operands (tcgen05 kind::f8f6f4): a 128-byte swizzled row then holds
+// 128 elements of K instead of 64, so a stage covers twice the K.
+template <int BN, int STAGES, bool B_MN, class Epi, bool TAIL = false, bool F8 = false>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap mA, const __grid_constant__ CUtensorMap mB,
                      const __grid_constant__ CUtensorMap mBh, int M, int N, int K, int ksplit, Epi epi,
                      int* status, StopCtl ctl) {
   pdl_wait();
   using L = PairLayout<BN, STAGES, B_MN>;
+  constexpr int KBE = F8 ? 2 * kBK : kBK;  // K elements per stage
   static_assert(!B_MN || (BN / 2) % 64 == 0, "MN-major B halves are whole 64-column blocks");
   static_assert(!TAIL || !B_MN, "half tiles are loaded K-major");
+  static_assert(!F8 || !B_MN, "E4M3 operands are loaded K-major");
   if (all_stopped(ctl.stop_at, ctl.B, ctl.step)) return;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
@@ -565,7 +580,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const int num_mp = (M + 2 * kBM - 1) / (2 * kBM), num_n = (N + BN - 1) / BN;
   const int num_mn = num_mp * num_n;
   const int num_full = num_mn * ksplit;  // tile t: split t / num_mn, m-pair and n from t % num_mn
-  const int nk_all = (K + kBK - 1) / kBK;
+  const int nk_all = (K + KBE - 1) / KBE;
   // work items: full tiles, then (TAIL) the last round's tiles as two halves each
   const int n_whole = num_full / ncl * ncl, n_rest = num_full - n_whole;
   const bool halves = TAIL && ksplit == 1 && n_rest > 0 && 2 * n_rest <= ncl;
@@ -626,9 +641,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           uint8_t* sb = sa + L::kA;
           if (leader) mbar_arrive_expect_tx(&full[stage], 2 * (L::kA + (width / 2) * kBK * 2));
           const uint32_t bar = cluster_addr(&full[stage], 0);
-          tma_load_2d_pair(sa, &mA, bar, kb * kBK, arow);
+          tma_load_2d_pair(sa, &mA, bar, kb * KBE, arow);
           if (!B_MN) {
-            tma_load_2d_pair(sb, width == BN ? &mB : &mBh, bar, kb * kBK, bcol);
+            tma_load_2d_pair(sb, width == BN ? &mB : &mBh, bar, kb * KBE, bcol);
           } else {
 #pragma unroll
             for (int j = 0; j < BN / 128; ++j)
@@ -652,8 +667,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
   } else if (warp == 1) {
     if (leader && lane == 0) {  // one thread of the leader waits and issues for the pair
-      constexpr uint32_t idesc_full = idesc_bf16(2 * kBM, BN, B_MN);
-      constexpr uint32_t idesc_half = idesc_bf16(2 * kBM, BN / 2, B_MN);
+      constexpr uint32_t idesc_full = F8 ? idesc_e4m3(2 * kBM, BN) : idesc_bf16(2 * kBM, BN, B_MN);
+      constexpr uint32_t idesc_half = F8 ? idesc_e4m3(2 * kBM, BN / 2) : idesc_bf16(2 * kBM, BN / 2, B_MN);
       int stage = 0;
       uint32_t phase = 0;
       bool alive = true;
@@ -680,7 +695,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             const uint64_t ad = sdesc_sw128(sa + kk * 32, 16, 1024);
             const uint64_t bd = B_MN ? sdesc_sw128(sb + kk * 2048, kBK * 128, 1024)
                                      : sdesc_sw128(sb + kk * 32, 16, 1024);
-            umma_bf16_pair(dt, ad, bd, idesc, (kb != kb_lo || kk != 0) ? 1u : 0u);
+            if constexpr (F8)
+              umma_e4m3_pair(dt, ad, bd, idesc, (kb != kb_lo || kk != 0) ? 1u : 0u);
+            else
+              umma_bf16_pair(dt, ad, bd, idesc, (kb != kb_lo || kk != 0) ? 1u : 0u);
           }
           umma_commit_pair(&empty[stage]);
           if (++stage == STAGES) {
@@ -753,19 +771,19 @@ static int max_pair_clusters(int smem) {
 }
 
 // Clusters a pair GEMM of this many tiles may use (0 if none can launch).
-template <int BN, int STAGES, bool B_MN, class Epi, bool TAIL = false>
+template <int BN, int STAGES, bool B_MN, class Epi, bool TAIL = false, bool F8 = false>
 static int pair_clusters() {
   using L = PairLayout<BN, STAGES, B_MN>;
-  if (set_smem_once<gemm_pair_kernel<BN, STAGES, B_MN, Epi, TAIL>>(L::kSmem) != cudaSuccess) return 0;
-  return max_pair_clusters<gemm_pair_kernel<BN, STAGES, B_MN, Epi, TAIL>>(L::kSmem);
+  if (set_smem_once<gemm_pair_kernel<BN, STAGES, B_MN, Epi, TAIL, F8>>(L::kSmem) != cudaSuccess) return 0;
+  return max_pair_clusters<gemm_pair_kernel<BN, STAGES, B_MN, Epi, TAIL, F8>>(L::kSmem);
 }
 
-template <int BN, int STAGES, bool B_MN, class Epi, bool TAIL = false>
+template <int BN, int STAGES, bool B_MN, class Epi, bool TAIL = false, bool F8 = false>
 static cudaError_t run_gemm_pair(const CUtensorMap& mA, const CUtensorMap& mB, const CUtensorMap& mBh, int M,
                                  int N, int K, int ksplit, const Epi& epi, int* status, StopCtl ctl,
                                  cudaStream_t st) {
   using L = PairLayout<BN, STAGES, B_MN>;
-  const int maxc = pair_clusters<BN, STAGES, B_MN, Epi, TAIL>();
+  const int maxc = pair_clusters<BN, STAGES, B_MN, Epi, TAIL, F8>();
   if (maxc <= 0) return cudaErrorInvalidConfiguration;
   const int tiles = cdiv(M, 2 * kBM) * cdiv(N, BN) * ksplit;
   const int ncl = tiles < maxc ? tiles : maxc;
@@ -783,8 +801,8 @@ static cudaError_t run_gemm_pair(const CUtensorMap& mA, const CUtensorMap& mB, c
   attr[1].val.programmaticStreamSerializationAllowed = kProgrammaticLaunch;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, gemm_pair_kernel<BN, STAGES, B_MN, Epi, TAIL>, mA, mB, mBh, M, N, K, ksplit, epi,
-                            status, ctl);
+  return cudaLaunchKernelEx(&cfg, gemm_pair_kernel<BN, STAGES, B_MN, Epi, TAIL, F8>, mA, mB, mBh, M, N, K, ksplit,
+                            epi, status, ctl);
 }
 
 cudaError_t launch_debug_gemm(const void* A, const void* Bm, float* D, int M, int N, int K,
@@ -981,11 +999,19 @@ cudaError_t launch_qkv(const void* a, const void* Wq, const void* Wk, const void
 
 cudaError_t launch_lmhead(const LmArgs& a, StopCtl ctl, int* status, cudaStream_t st) {
   CUtensorMap mA, mB, mBh;  // B boxes: half a vocabulary tile (one CTA of a pair), or half of a half tile
+  EpiLM epi{a.alpha, a.coef2, a.inv_sqrt_d, reinterpret_cast<__nv_bfloat16*>(a.pt), a.pm, a.pl,
+            a.pS, a.pvmax, a.pidx, a.logits, a.M, a.V, a.excl, a.hscale, a.escale};
+  if (a.E8) {
+    // E4M3 codes: 128 one-byte elements per 128-byte row
+    if (!make_tmap_2d(&mA, a.h8, (uint64_t)a.d, (uint64_t)a.M, (uint64_t)a.d, 2 * kBK, kBM, true) ||
+        !make_tmap_2d(&mB, a.E8, (uint64_t)a.d, (uint64_t)a.V, (uint64_t)a.d, 2 * kBK, kLmBN / 2, true) ||
+        !make_tmap_2d(&mBh, a.E8, (uint64_t)a.d, (uint64_t)a.V, (uint64_t)a.d, 2 * kBK, kLmBN / 4, true))
+      return cudaErrorInvalidValue;
+    return run_gemm_pair<kLmBN, 7, false, EpiLM, true, true>(mA, mB, mBh, a.M, a.V, a.d, 1, epi, status, ctl, st);
+  }
   if (!tmap_kmajor(&mA, a.h, a.M, a.d, kBM) || !tmap_kmajor(&mB, a.E, a.V, a.d, kLmBN / 2) ||
       !tmap_kmajor(&mBh, a.E, a.V, a.d, kLmBN / 4))
     return cudaErrorInvalidValue;
-  EpiLM epi{a.alpha, a.coef2, a.inv_sqrt_d, reinterpret_cast<__nv_bfloat16*>(a.pt), a.pm, a.pl,
-            a.pS, a.pvmax, a.pidx, a.logits, a.M, a.V, a.excl};
   return run_gemm_pair<kLmBN, 7, false, EpiLM, true>(mA, mB, mBh, a.M, a.V, a.d, 1, epi, status, ctl, st);
 }
 

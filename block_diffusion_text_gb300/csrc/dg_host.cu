@@ -61,6 +61,8 @@ dg_status check_model(const dg_model* m) {
   dg_status s = dims_supported(&m->dims);
   if (s) return s;
   if (!m->E || !m->Wq || !m->Wk || !m->Wv || !m->Wo || !m->W1 || !m->W2) return DG_ERR_ARG;
+  if (!m->E8 != !m->E8_scale) return DG_ERR_ARG;  // the FP8 head needs codes and scales
+  if (reinterpret_cast<uintptr_t>(m->E8) % 16 != 0) return DG_ERR_ARG;  // TMA base
   return DG_OK;
 }
 
@@ -159,6 +161,13 @@ dg_status enqueue_step(const StepCtx& c, float tau, float b, float stop_H, uint6
   lm.d = D.d;
   lm.excl = mask_id;
   DG_TRY(pf.mark(DG_PROF_LMHEAD, 0));
+  if (c.model->E8) {
+    lm.h8 = at<void>(ws, L.h8);
+    lm.hscale = at<float>(ws, L.hscale);
+    lm.E8 = c.model->E8;
+    lm.escale = c.model->E8_scale;
+    DG_TRY(launch_quantize_rows_e4m3(lm.h, M, D.d, at<uint8_t>(ws, L.h8), at<float>(ws, L.hscale), c.st));
+  }
   DG_TRY(launch_lmhead(lm, ctl, status, c.st));
   DG_TRY(pf.mark(DG_PROF_LMHEAD, 1));
   StatsArgs sa{at<float>(ws, L.pm), at<float>(ws, L.pl), at<float>(ws, L.pS), at<float>(ws, L.pvmax),
@@ -347,6 +356,8 @@ bool ws_layout(const dg_dims& D, int32_t cap, WsLayout* L) {
   }
   L->u = take(2 * M * D.d);
   L->g = take(2 * M * D.F);
+  L->h8 = take(M * D.d);
+  L->hscale = take(4 * M);
   L->total = off;
   return true;
 }
@@ -378,6 +389,16 @@ dg_status dg_workspace_size(const dg_dims* dims, int32_t cap, size_t* bytes) {
   if (!ws_layout(*dims, cap, &L)) return DG_ERR_SHAPE;
   *bytes = L.total;
   return DG_OK;
+}
+
+dg_status dg_quantize_rows_e4m3(const void* X, int32_t R, int32_t d, void* Q, float* scale, void* stream) {
+  if (!X || !Q || !scale || R < 0) return DG_ERR_ARG;
+  if (reinterpret_cast<uintptr_t>(X) % 16 || reinterpret_cast<uintptr_t>(Q) % 16 ||
+      reinterpret_cast<uintptr_t>(scale) % 4)
+    return DG_ERR_ARG;
+  if (d <= 0 || d % 16 != 0) return DG_ERR_SHAPE;
+  return cuda_status(launch_quantize_rows_e4m3(X, R, d, reinterpret_cast<uint8_t*>(Q), scale,
+                                               reinterpret_cast<cudaStream_t>(stream)));
 }
 
 dg_status dg_tau(const dg_sched* sched, int32_t step, float* tau) {

@@ -42,6 +42,7 @@ struct WsLayout {
   size_t upart, gbest, gidx;
   size_t gpart, gpart_elems;  // split-K partials of the small GEMMs
   size_t u, g;
+  size_t h8, hscale;          // FP8 head: h quantized per row
   size_t total;
 };
 bool ws_layout(const dg_dims& D, int32_t cap, WsLayout* L);
@@ -76,9 +77,10 @@ cudaError_t set_smem_once(int bytes) {
   return result;
 }
 
-// cuTensorMapEncodeTiled through the runtime's driver entry point.
+// cuTensorMapEncodeTiled through the runtime's driver entry point (bf16, or
+// with u8 set 8-bit codes; 128-byte swizzle).
 bool make_tmap_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
-                  uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer);
+                  uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, bool u8 = false);
 
 // ------------------------------------------------------------- launchers --
 struct StopCtl {
@@ -117,6 +119,11 @@ struct LmArgs {
   float* logits;       // optional fp32 [M][V]
   int M, V, d;
   int excl;            // column left out of the softmax (masked decoding's [MASK]), or -1
+  // FP8 head (all null for bf16): h8 [M][d] and E8 [V][d] E4M3 codes with
+  // per-row scales hscale [M] and escale [V]; the product runs on
+  // tcgen05 kind::f8f6f4 and the epilogue applies the scales
+  const void *h8, *E8;
+  const float *hscale, *escale;
 };
 cudaError_t launch_lmhead(const LmArgs& a, StopCtl ctl, int* status, cudaStream_t st);
 // Self-conditioning contraction u = p0 . E (split over the vocabulary).
@@ -206,6 +213,10 @@ struct SamplerArgs {
   int N;
 };
 cudaError_t launch_sampler(const SamplerArgs& a, cudaStream_t st);
+// Per-row E4M3 quantization of a bf16 matrix [R][d]: scale = absmax / 448 and
+// codes of x * (448 / absmax), float32 arithmetic, round to nearest even with
+// saturation; zero rows get scale 0 and zero codes.
+cudaError_t launch_quantize_rows_e4m3(const void* X, int R, int d, uint8_t* Q, float* scale, cudaStream_t st);
 // Masked confidence decoding of one step: per canvas, the
 // min(ceil(U / (N - step)), U) masked positions of smallest Z (highest
 // confidence 1 / Z) take their argmax; the accept copy is cleared (no

@@ -7,6 +7,8 @@
 
 #include <cmath>
 
+#include <cuda_fp8.h>
+
 #include "dg_common.cuh"
 #include "dg_internal.h"
 
@@ -790,6 +792,61 @@ cudaError_t launch_loop_finish(const int* stop_at, int B, int N, int* steps_take
                                const int* prev_argmax, int* xhat0, int C, cudaStream_t st) {
   return launch_pdl(loop_finish_kernel, dim3(cdiv(B * C > B ? B * C : B, 256)), dim3(256), 0, st, stop_at, B, N,
                     steps_taken, converged, prev_argmax, xhat0, C);
+}
+
+// ------------------------------------------------- E4M3 quantization ----
+// One warp per row of X (bf16 [R][d], d a multiple of 8): the row's absmax,
+// then the codes of x * (448 / absmax) through the hardware's saturating
+// round-to-nearest-even conversion.  Scale and its inverse are IEEE float32
+// quotients, the product a float32 multiply, so the bytes are fixed by the
+// definition.  A zero row gets scale 0 and zero codes.
+__global__ void __launch_bounds__(256) quant_rows_e4m3_kernel(const __nv_bfloat16* __restrict__ X, int R, int d,
+                                                              uint8_t* __restrict__ Q, float* __restrict__ scale) {
+  pdl_wait();
+  const int lane = threadIdx.x & 31;
+  const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (row >= R) return;
+  const uint4* x = reinterpret_cast<const uint4*>(X + (size_t)row * d);
+  const int n8 = d / 8;
+  float amax = 0.0f;
+  for (int c = lane; c < n8; c += 32) {
+    const uint4 u = __ldg(x + c);
+    const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float2 f = __bfloat1622float2(b[j]);
+      amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
+    }
+  }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  uint2* q = reinterpret_cast<uint2*>(Q + (size_t)row * d);
+  if (!(amax > 0.0f)) {
+    for (int c = lane; c < n8; c += 32) q[c] = make_uint2(0u, 0u);
+    if (lane == 0) scale[row] = 0.0f;
+    return;
+  }
+  const float inv = __fdiv_rn(448.0f, amax);
+  if (lane == 0) scale[row] = __fdiv_rn(amax, 448.0f);
+  for (int c = lane; c < n8; c += 32) {
+    const uint4 u = __ldg(x + c);
+    const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&u);
+    uint32_t w[2] = {0u, 0u};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float2 f = __bfloat1622float2(b[j]);
+      const uint32_t lo = __nv_cvt_float_to_fp8(__fmul_rn(f.x, inv), __NV_SATFINITE, __NV_E4M3);
+      const uint32_t hi = __nv_cvt_float_to_fp8(__fmul_rn(f.y, inv), __NV_SATFINITE, __NV_E4M3);
+      w[j >> 1] |= (lo | (hi << 8)) << (16 * (j & 1));
+    }
+    q[c] = make_uint2(w[0], w[1]);
+  }
+}
+
+cudaError_t launch_quantize_rows_e4m3(const void* X, int R, int d, uint8_t* Q, float* scale, cudaStream_t st) {
+  if (R <= 0) return cudaSuccess;
+  return launch_pdl(quant_rows_e4m3_kernel, dim3(cdiv(R, 8)), dim3(256), 0, st,
+                    reinterpret_cast<const __nv_bfloat16*>(X), R, d, Q, scale);
 }
 
 }  // namespace dg

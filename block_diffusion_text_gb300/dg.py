@@ -27,7 +27,8 @@ DG_OK, DG_ERR_ARG, DG_ERR_SHAPE, DG_ERR_CAPACITY, DG_ERR_WORKSPACE, DG_ERR_CUDA,
 EXPORTS = ("dg_status_string", "dg_workspace_size", "dg_read_status", "dg_tau", "dg_canvas_init",
            "dg_denoise_step", "dg_denoise_canvas", "dg_commit_block", "dg_debug_gemm",
            "dg_attention_noalloc", "dg_attention_noalloc_status", "dg_debug_wait_timeout",
-           "dg_canvas_init_masked", "dg_denoise_step_masked", "dg_denoise_canvas_masked", "dg_prefill")
+           "dg_canvas_init_masked", "dg_denoise_step_masked", "dg_denoise_canvas_masked", "dg_prefill",
+           "dg_quantize_rows_e4m3")
 
 
 class DgError(RuntimeError):
@@ -43,7 +44,8 @@ class dg_dims(ct.Structure):
 
 
 class dg_model(ct.Structure):
-    _fields_ = [("dims", dg_dims)] + [(n, ct.c_void_p) for n in ("E", "Wq", "Wk", "Wv", "Wo", "W1", "W2")]
+    _fields_ = [("dims", dg_dims)] + [(n, ct.c_void_p) for n in ("E", "Wq", "Wk", "Wv", "Wo", "W1", "W2",
+                                                                 "E8", "E8_scale")]
 
 
 class dg_kv_cache(ct.Structure):
@@ -118,6 +120,8 @@ def load():
             L.dg_prefill.argtypes = [ct.POINTER(dg_model), ct.POINTER(dg_kv_cache), ct.c_void_p, ct.c_int32,
                                      ct.c_void_p, ct.c_size_t, ct.c_void_p]
             L.dg_debug_wait_timeout.argtypes = [ct.POINTER(ct.c_int32), ct.c_void_p]
+            L.dg_quantize_rows_e4m3.argtypes = [ct.c_void_p, ct.c_int32, ct.c_int32, ct.c_void_p, ct.c_void_p,
+                                                ct.c_void_p]
             L.dg_debug_gemm.argtypes = [ct.c_void_p, ct.c_void_p, ct.c_void_p, ct.c_int32, ct.c_int32,
                                         ct.c_int32, ct.c_int32, ct.c_void_p]
             L.dg_attention_noalloc.argtypes = [ct.c_void_p, ct.c_void_p, ct.c_void_p, ct.c_int32, ct.c_int32,
@@ -165,14 +169,22 @@ def workspace_size(dims, cap: int) -> int:
 class Model:
     """Weights (bf16 device tensors, [out][in]) and the prefix cache of a batch of canvases."""
 
-    def __init__(self, dims, w: dict, cache_len: int | None = None):
+    def __init__(self, dims, w: dict, cache_len: int | None = None, fp8_head: bool = False):
+        """fp8_head: quantize E per row to E4M3 (quantize_rows_e4m3) and take the
+        LM head's logits on the FP8 tensor cores; E8 / E8_scale are then kept
+        here as the codes and scales."""
         self.dims = dims
         self.w = w
         self.K, self.V = w["Kc"], w["Vc"]
         self.cap = self.K.shape[-2]
         self.len = dims.P if cache_len is None else cache_len
+        self.E8 = self.E8_scale = None
+        if fp8_head:
+            self.E8, self.E8_scale = quantize_rows_e4m3(w["E"])
         self.s = dg_model(make_dims(dims), *[ct.c_void_p(w[k].data_ptr()) for k in
-                                             ("E", "Wq", "Wk", "Wv", "Wo", "W1", "W2")])
+                                             ("E", "Wq", "Wk", "Wv", "Wo", "W1", "W2")],
+                          ct.c_void_p(self.E8.data_ptr() if fp8_head else None),
+                          ct.c_void_p(self.E8_scale.data_ptr() if fp8_head else None))
         self.ws_bytes = workspace_size(dims, self.cap)
         # zero-initialised: the first word is the device status word
         self.ws = torch.zeros(self.ws_bytes + 256, dtype=torch.uint8, device=self.K.device)
@@ -398,3 +410,14 @@ def attention_noalloc_status(stream=None) -> int:
     st = ct.c_int32(-1)
     _check(load().dg_attention_noalloc_status(ct.byref(st), _stream(stream)), "dg_attention_noalloc_status")
     return st.value
+
+
+def quantize_rows_e4m3(X: torch.Tensor, stream=None):
+    """Per-row E4M3 codes (uint8 [R, d]) and scales (fp32 [R]) of a bf16 matrix X [R, d]."""
+    assert X.dtype == torch.bfloat16 and X.dim() == 2 and X.is_contiguous()
+    R, d = X.shape
+    Q = torch.empty((R, d), dtype=torch.uint8, device=X.device)
+    sc = torch.empty(R, dtype=torch.float32, device=X.device)
+    _check(load().dg_quantize_rows_e4m3(_ptr(X), R, d, _ptr(Q), _ptr(sc), _stream(stream)),
+           "dg_quantize_rows_e4m3")
+    return Q, sc

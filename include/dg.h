@@ -17,9 +17,12 @@
  *          list, the attention-mask list and the data-flow pseudocode.
  *   [P4]   "从零拆开DiffusionGemma" news piece: the masked confidence decoder
  *          generate() of its fourth step (the second sampler below).
- * The model is a one-layer synthetic stand-in: RMSNorm of embedding plus
- * self-conditioning, one GQA attention layer with RoPE, a tied LM head with a
- * per-position logit sharpness alpha, and a two-matrix FFW for
+ *   [SURV] "Text diffusion 2026" survey page, DiffusionGemma sections, and the
+ *          [TR] results paragraph: the throughput figures are quoted for FP8
+ *          (quantized) deployment, the basis of the optional FP8 LM head.
+ * The model is a synthetic stand-in: RMSNorm of embedding plus
+ * self-conditioning, L pre-norm GQA attention layers with RoPE, a tied LM head
+ * with a per-position logit sharpness alpha, and a two-matrix FFW for
  * self-conditioning.
  *
  * Conventions for every entry point:
@@ -93,10 +96,19 @@ typedef struct dg_dims {
  *   E  [V][d]        tied token embedding and LM head
  *   Wq [L][Hq*hd][d], Wk [L][Hkv*hd][d], Wv [L][Hkv*hd][d], Wo [L][d][Hq*hd]
  *   (one matrix per layer, stacked)
- *   W1 [F][d], W2 [d][F]                                                    */
+ *   W1 [F][d], W2 [d][F]
+ * Optional FP8 LM head [SURV] (both NULL = bf16 head):
+ *   E8 [V][d] uint8  E4M3 codes of E, E8_scale [V] float32 its per-row scales
+ *   (dg_quantize_rows_e4m3 of E; E8 16-byte aligned, and both or neither
+ *   given, else DG_ERR_ARG).  Each step then quantizes h per row the same
+ *   way and takes the logits l_v = alpha s_h s_v (q_h . q_v) / sqrt(d) on the
+ *   E4M3 tensor cores (fp32 accumulation); the embedding lookup and the
+ *   self-conditioning contraction p0 . E keep the bf16 E.                    */
 typedef struct dg_model {
   dg_dims dims;
   const void *E, *Wq, *Wk, *Wv, *Wo, *W1, *W2;
+  const void* E8;
+  const float* E8_scale;
 } dg_model;
 
 /* Static prefix KV cache ([CH12] "prompt / finished output block -> causal
@@ -328,6 +340,18 @@ DG_API dg_status dg_denoise_canvas_masked(const dg_model* model, const dg_kv_cac
 DG_API dg_status dg_attention_noalloc(const void* q, const void* K, const void* V, int32_t cap,
                                       int32_t len, const void* k, const void* v, void* o, int32_t B,
                                       int32_t C, int32_t Hq, int32_t Hkv, int32_t hd, void* stream);
+
+/* Per-row E4M3 quantization [SURV] (the FP8 LM head's operands).
+ *   X      bf16 [R][d] device, d a multiple of 16
+ *   Q      uint8 [R][d] device (written): codes of x * (448 / absmax(row))
+ *          rounded to nearest even with saturation at 448
+ *   scale  float32 [R] device (written): absmax(row) / 448; x ~= code * scale.
+ * Both quotients and the product are IEEE float32.  A zero row gets scale 0
+ * and zero codes.  R = 0 is a no-op.  Returns DG_ERR_ARG for NULL pointers,
+ * R < 0 or X / Q not 16-byte aligned, DG_ERR_SHAPE for d not a positive
+ * multiple of 16.                                                            */
+DG_API dg_status dg_quantize_rows_e4m3(const void* X, int32_t R, int32_t d, void* Q, float* scale,
+                                       void* stream);
 
 /* Status word of the last dg_attention_noalloc call on the current device:
  * synchronises `stream` and copies the word to *status (DG_OK, or

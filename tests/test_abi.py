@@ -215,3 +215,24 @@ def test_layers_and_prefill_validate(dg):
     assert L.dg_prefill(ct.byref(m), ct.byref(c), None, 10, ws, wsb, None) == dg.DG_ERR_ARG
     assert L.dg_prefill(ct.byref(m), ct.byref(c), ct.c_void_p(FAKE), 53, ws, wsb, None) == dg.DG_ERR_CAPACITY
     assert c.len == 2048
+
+
+def test_fp8_head_entry_points_validate(dg):
+    """dg_quantize_rows_e4m3 argument checks, and a model whose FP8 head has codes but no scales (or
+    misaligned codes) is rejected before any launch."""
+    L = dg.load()
+    f = ct.c_void_p(FAKE)
+    assert L.dg_quantize_rows_e4m3(None, 4, 64, f, f, None) == dg.DG_ERR_ARG
+    assert L.dg_quantize_rows_e4m3(f, 4, 64, None, f, None) == dg.DG_ERR_ARG
+    assert L.dg_quantize_rows_e4m3(f, 4, 64, f, None, None) == dg.DG_ERR_ARG
+    assert L.dg_quantize_rows_e4m3(f, -1, 64, f, f, None) == dg.DG_ERR_ARG
+    assert L.dg_quantize_rows_e4m3(ct.c_void_p(FAKE + 8), 4, 64, f, f, None) == dg.DG_ERR_ARG
+    assert L.dg_quantize_rows_e4m3(f, 4, 40, f, f, None) == dg.DG_ERR_SHAPE
+    assert L.dg_quantize_rows_e4m3(f, 4, 0, f, f, None) == dg.DG_ERR_SHAPE
+    dims = _dims()
+    m, c, cv, wsb = _structs(dg, dims)
+    ws = ct.c_void_p(1 << 30)
+    for e8, es in ((f, None), (None, f), (ct.c_void_p(FAKE + 8), f)):
+        m.E8, m.E8_scale = e8, es
+        assert L.dg_denoise_step(ct.byref(m), ct.byref(c), ct.byref(cv), 0.8, 0.1, 1, 0, 0, ws, wsb, None,
+                                 None) == dg.DG_ERR_ARG
