@@ -8,6 +8,8 @@ here.  Distributions (the one-layer synthetic stand-in):
 * prefix K/V cache ~ N(0, 1), keys taken as already rotated
 * alpha (per-position logit sharpness) = exp(U(ln 0.5, ln 64))
 * canvas tokens uniform over [0, V); self-conditioning z = 0
+* MoE (optional): router Wr ~ N(0, 1/d) for moe_hot experts and N(0, 1/d) / 64 for
+  the rest; expert We1 ~ N(0, 1/d), We2 ~ N(0, 1/Fe)
 * everything rounded to bf16 (round to nearest even) unless fp32 is asked for
 
 Workloads are named by what they are, with their sizes.
@@ -35,6 +37,10 @@ class Dims:
     rope_base: float = 10000.0
     rms_eps: float = 1e-6
     L: int = 1      # attention layers (Wq, Wk, Wv, Wo and the caches stacked [L, ...] when L > 1)
+    n_exp: int = 0  # routed experts of the per-layer MoE FFN (0: no MoE)
+    top_k: int = 0  # experts per token
+    Fe: int = 0     # expert hidden width (the shared expert has the same shape)
+    moe_hot: int = 0  # experts with full-spread router logits (0: all); the rest near zero
 
     def __post_init__(self):
         if self.cap == 0:
@@ -99,6 +105,20 @@ def make_weights(dims: Dims, seed: int, device="cpu", dtype=torch.bfloat16):
         Kc[..., : dims.P, :] = draw(lead + (dims.B, dims.Hkv, dims.P, dims.hd), 1.0)
         Vc[..., : dims.P, :] = draw(lead + (dims.B, dims.Hkv, dims.P, dims.hd), 1.0)
     w["Kc"], w["Vc"] = Kc, Vc
+    if dims.n_exp > 0:
+        # router rows of the "hot" experts ~ N(0, 1/d) (logits of unit spread), the other
+        # experts' rows scaled by 1/64 (logits near zero, rarely in a top-k): a canvas then
+        # activates about moe_hot experts; experts W1 ~ N(0, 1/d), W2 ~ N(0, 1/Fe), expert
+        # index n_exp being the shared expert
+        NE = dims.n_exp
+        Wr = torch.randn(lead + (NE, dims.d), **kw).mul_(sd)
+        We1 = draw(lead + (NE + 1, dims.Fe, dims.d), sd)
+        We2 = draw(lead + (NE + 1, dims.d, dims.Fe), 1.0 / math.sqrt(dims.Fe))
+        hot = dims.moe_hot if 0 < dims.moe_hot < NE else NE
+        if hot < NE:
+            cold = torch.randperm(NE, generator=g, device=device)[hot:]
+            Wr[..., cold, :] *= 1.0 / 64
+        w["Wr"], w["We1"], w["We2"] = Wr.to(dtype), We1, We2
     return w
 
 

@@ -39,7 +39,8 @@ class Dims(ct.Structure):
     _fields_ = [("V", ct.c_int32), ("d", ct.c_int32), ("C", ct.c_int32), ("B", ct.c_int32),
                 ("Hq", ct.c_int32), ("Hkv", ct.c_int32), ("hd", ct.c_int32), ("F", ct.c_int32),
                 ("P", ct.c_int32), ("cap", ct.c_int32), ("rope_base", ct.c_double),
-                ("rms_eps", ct.c_double), ("mirror_bf16", ct.c_int32), ("L", ct.c_int32)]
+                ("rms_eps", ct.c_double), ("mirror_bf16", ct.c_int32), ("L", ct.c_int32),
+                ("n_exp", ct.c_int32), ("top_k", ct.c_int32), ("Fe", ct.c_int32)]
 
 
 _F = ct.POINTER(ct.c_float)
@@ -53,7 +54,7 @@ class StepIn(ct.Structure):
                 ("Kc", _F), ("Vc", _F), ("x", _I), ("z", _F), ("alpha", _F), ("prev_argmax", _I),
                 ("tau", ct.c_double), ("b", ct.c_double), ("stop_H", ct.c_double),
                 ("seed", ct.c_uint64), ("step", ct.c_int32), ("block", ct.c_int32), ("exclude_tok", ct.c_int32),
-                ("E8", _U8), ("E8_scale", _F)]
+                ("E8", _U8), ("E8_scale", _F), ("Wr", _F), ("We1", _F), ("We2", _F)]
 
 
 class StepOut(ct.Structure):
@@ -61,7 +62,8 @@ class StepOut(ct.Structure):
                 ("H", _D), ("m", _D), ("Z", _D), ("top2gap", _D), ("argmax", _I), ("accept", _U8),
                 ("cum", _D), ("rank", _I), ("renoise_tok", _I), ("sample_tok", _I),
                 ("gumbel_gap", _D), ("tokens_out", _I), ("u", _D), ("g", _D), ("z_out", _D),
-                ("n_acc", _I), ("meanH", _D), ("stop", _I)]
+                ("n_acc", _I), ("meanH", _D), ("stop", _I), ("moe_idx", _I), ("moe_gate", _D),
+                ("moe_logits", _D)]
 
 
 def lib():
@@ -76,7 +78,10 @@ def lib():
             L.or_philox_word.restype = ct.c_uint64
             L.or_uniform_token.argtypes = [ct.c_uint64, ct.c_int32]
             L.or_uniform_token.restype = ct.c_int32
-            L.or_prefill.argtypes = [ct.POINTER(Dims), _F, _F, _F, _F, _F, _I, ct.c_int32, _F, _F, ct.c_int32]
+            L.or_prefill.argtypes = [ct.POINTER(Dims), _F, _F, _F, _F, _F, ct.c_void_p, _I, ct.c_int32, _F, _F,
+                                     ct.c_int32]
+            L.or_moe_ffn.argtypes = [ct.POINTER(Dims), _F, _F, _F, _D, ct.c_int64, _I, _D, _D, ct.c_int32]
+            L.or_moe_ffn.restype = ct.c_int
             L.or_prefill.restype = ct.c_int
             L.or_reveal.argtypes = [_D, _I, _I, ct.c_int32, ct.c_int32, ct.c_int32, ct.c_int32, _U8]
             L.or_reveal.restype = ct.c_int32
@@ -299,7 +304,12 @@ def attend_row(q, Kp, Vp, Kc, Vc):
 def _dims(dims, mirror_bf16: bool, P=None):
     return Dims(V=dims.V, d=dims.d, C=dims.C, B=dims.B, Hq=dims.Hq, Hkv=dims.Hkv, hd=dims.hd,
                 F=dims.F, P=dims.P if P is None else P, cap=dims.cap, rope_base=dims.rope_base,
-                rms_eps=dims.rms_eps, mirror_bf16=1 if mirror_bf16 else 0, L=getattr(dims, "L", 1))
+                rms_eps=dims.rms_eps, mirror_bf16=1 if mirror_bf16 else 0, L=getattr(dims, "L", 1),
+                n_exp=getattr(dims, "n_exp", 0), top_k=getattr(dims, "top_k", 0), Fe=getattr(dims, "Fe", 0))
+
+
+class _MoeW(ct.Structure):
+    _fields_ = [("Wr", _F), ("We1", _F), ("We2", _F)]
 
 
 _WANT_ALL = ("a", "q", "k", "v", "o", "h", "logits", "H", "m", "Z", "top2gap", "argmax", "accept",
@@ -330,8 +340,10 @@ def denoise_step(dims, w, x, z, alpha, tau, b, seed, step, block=0, prev_argmax=
                   H=(M,), m=(M,), Z=(M,), top2gap=(M,), argmax=(M,), accept=(M,), cum=(M,),
                   rank=(M,), renoise_tok=(M,), sample_tok=(M,), gumbel_gap=(M,), tokens_out=(M,),
                   u=(M, d), g=(M, F), z_out=(M, d), n_acc=(B,), meanH=(B,), stop=(B,))
+    ne, tk = getattr(dims, "n_exp", 0), getattr(dims, "top_k", 0)
+    shapes.update(moe_idx=(M, tk), moe_gate=(M, tk), moe_logits=(M, ne))
     types = dict(argmax=np.int32, accept=np.uint8, rank=np.int32, renoise_tok=np.int32,
-                 sample_tok=np.int32, tokens_out=np.int32, n_acc=np.int32, stop=np.int32)
+                 sample_tok=np.int32, tokens_out=np.int32, n_acc=np.int32, stop=np.int32, moe_idx=np.int32)
     outs = {}
     so = StepOut()
     ctmap = {np.float64: _D, np.int32: _I, np.uint8: _U8}
@@ -347,10 +359,12 @@ def denoise_step(dims, w, x, z, alpha, tau, b, seed, step, block=0, prev_argmax=
     if fp8_head is not None:
         e8 = np.ascontiguousarray(np.asarray(fp8_head[0], np.uint8))
         es = _f32(fp8_head[1])
+    mw = [_f32(w[k]) if k in w else None for k in ("Wr", "We1", "We2")] if ne > 0 else [None] * 3
     si = StepIn(*[_p(a, _F) for a in keep], _p(xx, _I), _p(zz, _F), _p(aa, _F),
                 _p(pa, _I) if pa is not None else None, float(tau), float(b), float(stop_H),
                 int(seed), int(step), int(block), int(exclude_tok),
-                _p(e8, _U8) if e8 is not None else None, _p(es, _F) if es is not None else None)
+                _p(e8, _U8) if e8 is not None else None, _p(es, _F) if es is not None else None,
+                *[_p(a, _F) if a is not None else None for a in mw])
     rr = _i32(rows) if rows is not None else None
     nrows = 0 if rr is None else rr.size
     if rr is not None and rr.size == 0:
@@ -364,6 +378,24 @@ def denoise_step(dims, w, x, z, alpha, tau, b, seed, step, block=0, prev_argmax=
     if "accept" in outs:
         outs["accept"] = outs["accept"].astype(bool)
     return outs
+
+
+def moe_ffn(dims, Wr, We1, We2, h, mirror_bf16=True, nthreads=None):
+    """The MoE FFN of one layer on rows h [n, d] (or_moe_ffn).  dims carries d, rms_eps, n_exp,
+    top_k, Fe; Wr [n_exp, d], We1 [n_exp + 1, Fe, d], We2 [n_exp + 1, d, Fe] (index n_exp: the
+    shared expert).  Returns dict(h=h + y, idx [n, top_k], gate [n, top_k], logits [n, n_exp])."""
+    hh = np.ascontiguousarray(np.array(h, dtype=np.float64))
+    n = hh.shape[0]
+    idx = np.zeros((n, dims.top_k), np.int32)
+    gate = np.zeros((n, dims.top_k))
+    logits = np.zeros((n, dims.n_exp))
+    D = _dims(dims, mirror_bf16, P=0)
+    arrs = [_f32(Wr), _f32(We1), _f32(We2)]
+    rc = lib().or_moe_ffn(ct.byref(D), *[_p(a, _F) for a in arrs], _p(hh, _D), n, _p(idx, _I), _p(gate, _D),
+                          _p(logits, _D), nthreads or default_threads())
+    if rc != 0:
+        raise ValueError("oracle moe_ffn: bad arguments")
+    return dict(h=hh, idx=idx, gate=gate, logits=logits)
 
 
 def tau_schedule(N=48, tau0=0.8, tau1=0.4):
@@ -413,7 +445,12 @@ def prefill(dims, w, tokens, P, mirror_bf16=True, nthreads=None):
     tok = _i32(tokens)
     n = tok.shape[-1] if tok.ndim > 1 else tok.size // dims.B
     D = _dims(dims, mirror_bf16, P=P)
+    mw = None
+    if getattr(dims, "n_exp", 0) > 0:
+        arrs = [_f32(w[k]) for k in ("Wr", "We1", "We2")]
+        mw = _MoeW(*[_p(a, _F) for a in arrs])
     rc = lib().or_prefill(ct.byref(D), *[_p(_f32(w[k]), _F) for k in ("E", "Wq", "Wk", "Wv", "Wo")],
+                          ct.byref(mw) if mw is not None else None,
                           _p(tok, _I), int(n), _p(Kc, _F), _p(Vc, _F), nthreads or default_threads())
     if rc != 0:
         raise ValueError("oracle prefill: cache capacity exceeded")

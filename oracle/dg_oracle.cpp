@@ -365,7 +365,18 @@ typedef struct {
   double rope_base, rms_eps;
   int32_t mirror_bf16;
   int32_t L;    // attention layers (>= 1); weights Wq, Wk, Wv, Wo and the caches are stacked [L][...]
+  // Mixture-of-experts FFN after each attention block (n_exp = 0: none):
+  // n_exp routed experts of hidden width Fe, top_k of them per token, plus one
+  // shared expert of the same shape.
+  int32_t n_exp, top_k, Fe;
 } or_dims;
+
+// Weights of the MoE FFN, stacked per layer: router Wr [L][n_exp][d]; expert
+// matrices We1 [L][n_exp + 1][Fe][d] and We2 [L][n_exp + 1][d][Fe], expert
+// index n_exp being the shared expert.
+typedef struct {
+  const float *Wr, *We1, *We2;
+} or_moe_w;
 
 typedef struct {
   const float *E, *Wq, *Wk, *Wv, *Wo, *W1, *W2;  // [V][d], [L][out][in] row-major (W1, W2 single)
@@ -387,6 +398,7 @@ typedef struct {
   // The embedding and the contraction p0 . E keep the bf16 E.
   const uint8_t* E8;
   const float* E8_scale;
+  or_moe_w moe;  // used when n_exp > 0
 } or_step_in;
 
 typedef struct {
@@ -406,7 +418,76 @@ typedef struct {
   int32_t* n_acc;                      // [B]
   double* meanH;                       // [B]
   int32_t* stop;                       // [B]
+  // MoE routing of the last layer (n_exp > 0): expert ids in rank order and
+  // their gates, [B*C][top_k]; the router logits [B*C][n_exp]
+  int32_t* moe_idx;
+  double *moe_gate, *moe_logits;
 } or_step_out;
+
+// ------------------------------------------------------------------ MoE -----
+// The mixture-of-experts FFN of one layer, applied to rows h [n][d] in place
+// (the DiffusionGemma backbone's FFN: "Text diffusion 2026" survey page,
+// DiffusionGemma model section -- 128 experts per layer, 8 routed plus one
+// shared; the technical report summary's MoE paragraph -- each token activates
+// a few experts).  Per row, as a pre-norm residual block:
+//   x   = RMSNorm(h)                          (bf16 when mirroring)
+//   r_e = x . Wr_e                            router logit of routed expert e
+//   S   = the top_k experts by r (ties: lower index first), in rank order
+//   g_j = exp(r_{S_j}) / sum_{e in S} exp(r_e)     softmax over the selected
+//         logits, i.e. the softmax over all experts renormalised on S
+//   y   = sum_j g_j FFN_{S_j}(x) + FFN_shared(x),  FFN_e(x) = We2_e GELU(We1_e x)
+//         (no biases; the hidden GELU output rounded to bf16 when mirroring)
+//   h  <- h + y                               (bf16 when mirroring)
+// The pages give neither the expert width nor the gating formula; the
+// softmax-then-top-k-renormalised gate and the two-matrix GELU expert (the
+// self-conditioning FFW's shape) are the plainest readings.  Optional outputs:
+// idx [n][top_k], gate [n][top_k], logits [n][n_exp].
+void moe_ffn(const or_dims* D, const float* Wr, const float* We1, const float* We2, double* h, int64_t n,
+             int32_t* idx_out, double* gate_out, double* logit_out, int nthreads) {
+  const int64_t d = D->d, NE = D->n_exp, K = D->top_k, Fe = D->Fe;
+  const int mir = D->mirror_bf16;
+  parallel_rows(n, nthreads, [&](int64_t r) {
+    double* hr = &h[r * d];
+    std::vector<double> x(d), rl(NE), hid(Fe), y(d, 0.0);
+    or_rmsnorm(hr, (int32_t)d, D->rms_eps, x.data());
+    for (int64_t j = 0; j < d; ++j) x[j] = maybe_bf16(x[j], mir);
+    for (int64_t e = 0; e < NE; ++e) {
+      double acc = 0.0;
+      for (int64_t j = 0; j < d; ++j) acc += x[j] * (double)Wr[e * d + j];
+      rl[e] = acc;
+    }
+    std::vector<int32_t> order(NE);
+    for (int64_t e = 0; e < NE; ++e) order[e] = (int32_t)e;
+    std::stable_sort(order.begin(), order.end(), [&](int32_t u, int32_t v) { return rl[u] > rl[v]; });
+    const double top = rl[order[0]];
+    double Z = 0.0;
+    for (int64_t j = 0; j < K; ++j) Z += std::exp(rl[order[j]] - top);
+    auto expert = [&](int64_t e, double gate) {
+      const float* W1 = We1 + e * Fe * d;
+      const float* W2 = We2 + e * d * Fe;
+      for (int64_t f = 0; f < Fe; ++f) {
+        double acc = 0.0;
+        for (int64_t j = 0; j < d; ++j) acc += x[j] * (double)W1[f * d + j];
+        hid[f] = maybe_bf16(or_gelu(acc), mir);
+      }
+      for (int64_t c = 0; c < d; ++c) {
+        double acc = 0.0;
+        for (int64_t f = 0; f < Fe; ++f) acc += hid[f] * (double)W2[c * Fe + f];
+        y[c] += gate * acc;
+      }
+    };
+    for (int64_t j = 0; j < K; ++j) {
+      const double g = std::exp(rl[order[j]] - top) / Z;
+      if (idx_out) idx_out[r * K + j] = order[j];
+      if (gate_out) gate_out[r * K + j] = g;
+      expert(order[j], g);
+    }
+    expert(NE, 1.0);  // the shared expert
+    if (logit_out)
+      for (int64_t e = 0; e < NE; ++e) logit_out[r * NE + e] = rl[e];
+    for (int64_t c = 0; c < d; ++c) hr[c] = maybe_bf16(hr[c] + y[c], mir);
+  });
+}
 
 // One denoising step, [TR] step 3 (and the stop test of step 4):
 //   a1  a = RMSNorm(E[x_t] + z_t)                       [CH12] pseudocode, [TR]
@@ -430,6 +511,9 @@ int or_denoise_step(const or_dims* D, const or_step_in* in, or_step_out* out, co
                 F = D->F, P = D->P, cap = D->cap;
   if (V <= 0 || d <= 0 || C <= 0 || B <= 0 || Hq <= 0 || Hkv <= 0 || hd <= 0 || F <= 0 ||
       Hq % Hkv != 0 || hd % 2 != 0 || P < 0 || P > cap)
+    return 1;
+  if (D->n_exp < 0 || (D->n_exp > 0 && (D->top_k < 1 || D->top_k > D->n_exp || D->Fe < 1 || !in->moe.Wr ||
+                                        !in->moe.We1 || !in->moe.We2)))
     return 1;
   const int mir = D->mirror_bf16;
   const int64_t M = B * C, nq = Hq * hd, nkv = Hkv * hd;
@@ -520,6 +604,14 @@ int or_denoise_step(const or_dims* D, const or_step_in* in, or_step_out* out, co
         hh[r * d + n] = maybe_bf16(a[r * d + n] + acc, mir);
       }
     });
+    // the layer's MoE FFN (when configured); the routing outputs are the last layer's
+    if (D->n_exp > 0) {
+      const bool lastl = l == L - 1;
+      moe_ffn(D, in->moe.Wr + l * D->n_exp * d, in->moe.We1 + l * (D->n_exp + 1) * (int64_t)D->Fe * d,
+              in->moe.We2 + l * (D->n_exp + 1) * d * (int64_t)D->Fe, hh.data(), M,
+              lastl ? out->moe_idx : nullptr, lastl ? out->moe_gate : nullptr,
+              lastl ? out->moe_logits : nullptr, nthreads);
+    }
   }
 
   if (out->a) std::memcpy(out->a, a.data(), sizeof(double) * M * d);
@@ -734,7 +826,7 @@ int or_denoise_canvas(const or_dims* D, const float* E, const float* Wq, const f
     in.E = E; in.Wq = Wq; in.Wk = Wk; in.Wv = Wv; in.Wo = Wo; in.W1 = W1; in.W2 = W2;
     in.Kc = Kc; in.Vc = Vc; in.x = x; in.z = z; in.alpha = alpha;
     in.prev_argmax = prev.data(); in.tau = tau; in.b = b; in.stop_H = stop_H;
-    in.seed = seed; in.step = s; in.block = block;
+    in.seed = seed; in.step = s; in.block = block; in.exclude_tok = -1;
     or_step_out out{};
     out.argmax = am.data(); out.tokens_out = tok.data(); out.z_out = zo.data();
     out.n_acc = na.data(); out.stop = st.data();
@@ -778,10 +870,12 @@ int or_denoise_canvas(const or_dims* D, const float* E, const float* Wq, const f
 // composition with an explicit causal mask, the independence of earlier K/V
 // from later tokens, chunked prefill equal to one piece).
 int or_prefill(const or_dims* D, const float* E, const float* Wq, const float* Wk, const float* Wv,
-               const float* Wo, const int32_t* tokens, int32_t n, float* Kc, float* Vc, int32_t nthreads) {
+               const float* Wo, const or_moe_w* moe, const int32_t* tokens, int32_t n, float* Kc, float* Vc,
+               int32_t nthreads) {
   const int64_t d = D->d, B = D->B, Hq = D->Hq, Hkv = D->Hkv, hd = D->hd, P = D->P, cap = D->cap;
   const int64_t L = D->L < 1 ? 1 : D->L;
   if (n < 0 || P + n > cap) return 1;
+  if (D->n_exp > 0 && L > 1 && (!moe || D->top_k < 1 || D->top_k > D->n_exp || D->Fe < 1)) return 1;
   const int mir = D->mirror_bf16;
   const int64_t nq = Hq * hd, nkv = Hkv * hd, Mn = B * (int64_t)n;
   std::vector<double> a(Mn * d), q(Mn * nq), o(Mn * nq), hh(Mn * d);
@@ -856,6 +950,12 @@ int or_prefill(const or_dims* D, const float* E, const float* Wq, const float* W
         hh[r * d + c] = maybe_bf16(a[r * d + c] + acc, mir);
       }
     });
+    // the layer's MoE FFN feeds the next layer's input (the last layer's output
+    // is not needed for the cache)
+    if (D->n_exp > 0)
+      moe_ffn(D, moe->Wr + l * D->n_exp * d, moe->We1 + l * (D->n_exp + 1) * (int64_t)D->Fe * d,
+              moe->We2 + l * (D->n_exp + 1) * d * (int64_t)D->Fe, hh.data(), Mn, nullptr, nullptr, nullptr,
+              nthreads);
   }
   return 0;
 }
@@ -866,7 +966,16 @@ int or_prefill(const or_dims* D, const float* E, const float* Wq, const float* W
 int or_commit(const or_dims* D, const float* E, const float* Wk, const float* Wv,
               const int32_t* tokens, float* Kc, float* Vc, int32_t nthreads) {
   if (D->L > 1) return 1;
-  return or_prefill(D, E, nullptr, Wk, Wv, nullptr, tokens, D->C, Kc, Vc, nthreads);
+  return or_prefill(D, E, nullptr, Wk, Wv, nullptr, nullptr, tokens, D->C, Kc, Vc, nthreads);
+}
+
+// The MoE FFN of one layer on rows h [n][d] (in place), with its routing.
+int or_moe_ffn(const or_dims* D, const float* Wr, const float* We1, const float* We2, double* h, int64_t n,
+               int32_t* idx, double* gate, double* logits, int32_t nthreads) {
+  if (!D || D->n_exp < 1 || D->top_k < 1 || D->top_k > D->n_exp || D->Fe < 1 || !Wr || !We1 || !We2 || n < 0)
+    return 1;
+  moe_ffn(D, Wr, We1, We2, h, n, idx, gate, logits, nthreads);
+  return 0;
 }
 
 double or_round_bf16(double x) { return round_bf16(x); }

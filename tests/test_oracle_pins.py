@@ -776,3 +776,153 @@ def test_fp8_head_logits_are_the_quantized_product():
     assert np.allclose(out["logits"], l, rtol=1e-12, atol=1e-12)
     p = special.softmax(l / tau, axis=1)
     assert np.allclose(out["u"], np.vectorize(oracle.round_bf16)(p @ w["E"].astype(np.float64)), atol=2e-3)
+
+
+# ------------------------------------------------------------------ MoE FFN ----
+# The DiffusionGemma backbone's FFN ("Text diffusion 2026" survey page, DiffusionGemma model
+# section: 128 experts per layer, 8 routed plus one shared).  The pins below fix the routing, the
+# gates, the experts' orientation and the residual against closed forms and library routines.
+MOE = synth.Dims(V=300, d=64, C=12, B=2, Hq=4, Hkv=2, hd=16, F=64, P=10, cap=40, n_exp=16, top_k=4, Fe=32)
+
+
+def _moe_dims(**kw):
+    return dataclasses.replace(MOE, **kw)
+
+
+def _gelu1():
+    return 0.5 * (1.0 + math.erf(1.0 / math.sqrt(2.0)))  # GELU(1)
+
+
+def _probe_experts(dims, logit_of):
+    """Weights whose routed expert e maps x = ones(d) to GELU(1) e_e (unit vector on output column e)
+    and whose router gives expert e the logit logit_of[e]; the shared expert is zero."""
+    NE, d, Fe = dims.n_exp, dims.d, dims.Fe
+    Wr = np.zeros((NE, d), np.float32)
+    for e in range(NE):
+        Wr[e, :] = np.float32(logit_of[e]) / d  # x = ones: r_e = d * (logit / d)
+    We1 = np.zeros((NE + 1, Fe, d), np.float32)
+    We2 = np.zeros((NE + 1, d, Fe), np.float32)
+    for e in range(NE):
+        We1[e, 0, 0] = 1.0   # hidden unit 0 = GELU(x_0) = GELU(1)
+        We2[e, e, 0] = 1.0   # output column e
+    return Wr, We1, We2
+
+
+def test_moe_gates_and_routing_closed_form():
+    """x = RMSNorm(ones) = ones (eps 0); selected logits ln 4, ln 2, 0, 0 among negatives: the gates
+    are 4/8, 2/8, 1/8, 1/8 and y lands on exactly the selected experts' columns."""
+    dims = _moe_dims(rms_eps=0.0)
+    lg = np.full(dims.n_exp, -5.0)
+    lg[[9, 2, 13, 6]] = [math.log(4), math.log(2), 0.0, 0.0]
+    Wr, We1, We2 = _probe_experts(dims, lg)
+    h = np.ones((3, dims.d))
+    out = oracle.moe_ffn(dims, Wr, We1, We2, h, mirror_bf16=False)
+    assert out["idx"].tolist() == [[9, 2, 6, 13]] * 3  # rank order; the tie 0 = 0 in index order
+    np.testing.assert_allclose(out["gate"], [[0.5, 0.25, 0.125, 0.125]] * 3, rtol=1e-6)
+    y = out["h"] - h
+    want = np.zeros(dims.d)
+    want[[9, 2, 6, 13]] = np.array([0.5, 0.25, 0.125, 0.125]) * _gelu1()
+    np.testing.assert_allclose(y, np.tile(want, (3, 1)), rtol=1e-6, atol=1e-12)
+
+
+def test_moe_top1_and_ties():
+    """top_k = 1 gives gate 1 exactly; with top_k = 2 and three equal logits the two lowest indices
+    are taken with gates 1/2 each."""
+    d1 = _moe_dims(rms_eps=0.0, top_k=1)
+    lg = np.linspace(-1, 1, d1.n_exp)
+    Wr, We1, We2 = _probe_experts(d1, lg)
+    out = oracle.moe_ffn(d1, Wr, We1, We2, np.ones((1, d1.d)), mirror_bf16=False)
+    assert out["idx"][0, 0] == d1.n_exp - 1 and out["gate"][0, 0] == 1.0
+    d2 = _moe_dims(rms_eps=0.0, top_k=2)
+    lg = np.full(d2.n_exp, -3.0)
+    lg[[7, 3, 11]] = 1.0
+    Wr, We1, We2 = _probe_experts(d2, lg)
+    out = oracle.moe_ffn(d2, Wr, We1, We2, np.ones((1, d2.d)), mirror_bf16=False)
+    assert out["idx"][0].tolist() == [3, 7]
+    assert out["gate"][0].tolist() == [0.5, 0.5]
+
+
+def test_moe_identical_experts_reduce_to_dense_ffn():
+    """With every routed expert equal, the gates sum to one whatever the router does: the block is
+    h + FFN(x) + FFN_shared(x), x = rms_norm(h), composed here from torch's rms_norm and GELU."""
+    dims = MOE
+    rng = np.random.default_rng(5)
+    d, Fe, NE = dims.d, dims.Fe, dims.n_exp
+    A = (rng.standard_normal((Fe, d)) / math.sqrt(d)).astype(np.float32)
+    Bm = (rng.standard_normal((d, Fe)) / math.sqrt(Fe)).astype(np.float32)
+    S1 = (rng.standard_normal((Fe, d)) / math.sqrt(d)).astype(np.float32)
+    S2 = (rng.standard_normal((d, Fe)) / math.sqrt(Fe)).astype(np.float32)
+    Wr = (rng.standard_normal((NE, d)) / math.sqrt(d)).astype(np.float32)
+    We1 = np.concatenate([np.repeat(A[None], NE, 0), S1[None]])
+    We2 = np.concatenate([np.repeat(Bm[None], NE, 0), S2[None]])
+    h = rng.standard_normal((20, d))
+    out = oracle.moe_ffn(dims, Wr, We1, We2, h, mirror_bf16=False)
+    ht = torch.from_numpy(h)
+    x = torch.nn.functional.rms_norm(ht, (d,), eps=dims.rms_eps)
+    gelu = torch.nn.functional.gelu
+    ffn = lambda W1, W2: gelu(x @ torch.from_numpy(W1).double().T) @ torch.from_numpy(W2).double().T
+    ref = (ht + ffn(A, Bm) + ffn(S1, S2)).numpy()
+    np.testing.assert_allclose(out["h"], ref, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(out["gate"].sum(axis=1), 1.0, rtol=1e-14)
+    # the router logits are x . Wr_e
+    np.testing.assert_allclose(out["logits"], (x @ torch.from_numpy(Wr).double().T).numpy(), rtol=1e-12,
+                               atol=1e-12)
+
+
+def test_moe_expert_permutation_invariance():
+    """Relabelling the routed experts (router rows and expert matrices alike) leaves the output
+    unchanged and relabels the selection."""
+    dims = MOE
+    w = synth.to_numpy_f32(synth.make_weights(dims, 3))
+    rng = np.random.default_rng(9)
+    perm = rng.permutation(dims.n_exp)
+    h = rng.standard_normal((24, dims.d))
+    a = oracle.moe_ffn(dims, w["Wr"], w["We1"], w["We2"], h)
+    ext = np.r_[perm, dims.n_exp]
+    b = oracle.moe_ffn(dims, w["Wr"][perm], w["We1"][ext], w["We2"][ext], h)
+    np.testing.assert_array_equal(a["h"], b["h"])
+    np.testing.assert_array_equal(a["idx"], perm[b["idx"]])
+
+
+def test_moe_hot_experts_bound_the_canvas_activation():
+    """The synthetic router's cold experts (row norm / 64) never reach a top-8 of 84 unit-spread
+    logits: a 256-token canvas activates exactly the hot set (the pages' 84 of 128)."""
+    dims = dataclasses.replace(MOE, d=128, n_exp=128, top_k=8, moe_hot=84)
+    w = synth.to_numpy_f32(synth.make_weights(dims, 4))
+    h = np.random.default_rng(1).standard_normal((256, dims.d))
+    x = torch.nn.functional.rms_norm(torch.from_numpy(h), (dims.d,), eps=dims.rms_eps).numpy()
+    r = x @ w["Wr"].astype(np.float64).T
+    top = np.argsort(-r, axis=1, kind="stable")[:, :8]
+    assert len(np.unique(top)) == 84
+
+
+def test_moe_in_the_step_follows_the_attention_block():
+    """The step with an MoE layer: its h is the MoE block applied to the attention block's h (the
+    same step without MoE), and the routing outputs are that block's."""
+    dims = MOE
+    w = synth.to_numpy_f32(synth.make_weights(dims, 6))
+    x, z, a = synth.make_canvas(dims, 6)
+    base = dataclasses.replace(dims, n_exp=0, top_k=0, Fe=0)
+    r0 = oracle.denoise_step(base, w, x.numpy(), z.float().numpy(), a.numpy(), tau=0.8, b=0.1, seed=1, step=0,
+                             want=("h",))
+    r1 = oracle.denoise_step(dims, w, x.numpy(), z.float().numpy(), a.numpy(), tau=0.8, b=0.1, seed=1, step=0,
+                             want=("h", "moe_idx", "moe_gate", "H"))
+    m = oracle.moe_ffn(dims, w["Wr"], w["We1"], w["We2"], r0["h"])
+    np.testing.assert_array_equal(r1["h"], m["h"])
+    np.testing.assert_array_equal(r1["moe_idx"], m["idx"])
+    np.testing.assert_array_equal(r1["moe_gate"], m["gate"])
+
+
+def test_moe_prefill_feeds_the_next_layer_only():
+    """Prefill with two layers and MoE: layer 0's cache rows do not depend on the MoE weights, layer
+    1's do (the MoE output is the next layer's input)."""
+    dims = dataclasses.replace(MOE, L=2)
+    w = synth.to_numpy_f32(synth.make_weights(dims, 8))
+    toks = np.random.default_rng(2).integers(0, dims.V, (dims.B, 5)).astype(np.int32)
+    K1, V1 = oracle.prefill(dims, w, toks, dims.P)
+    w2 = dict(w)
+    w2["We2"] = w["We2"] * 2
+    K2, V2 = oracle.prefill(dims, w2, toks, dims.P)
+    rows = slice(dims.P, dims.P + 5)
+    np.testing.assert_array_equal(K1[0][..., rows, :], K2[0][..., rows, :])
+    assert np.abs(K1[1][..., rows, :] - K2[1][..., rows, :]).max() > 1e-3
