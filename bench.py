@@ -298,7 +298,7 @@ def run_ours(args, world, rank, local):
     taus = dg.tau_schedule(48)
     outbuf = None
     slots = dg.PROF_SLOTS
-    timed_slots = slots
+    timed_slots = tuple(k for k in slots if k != "moe" or dims.n_exp > 0)
 
     def step(s, events=None):
         nonlocal outbuf

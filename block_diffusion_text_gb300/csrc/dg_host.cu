@@ -22,6 +22,8 @@ bool dims_ok(const dg_dims* D) {
   if (D->Hq % D->Hkv != 0) return false;
   if (!(D->rope_base > 0.f) || !(D->rms_eps >= 0.f)) return false;
   if (D->L < 1 || D->L > 64) return false;
+  if (D->n_exp < 0 || D->n_exp > kMoeMaxExperts) return false;
+  if (D->n_exp > 0 && (D->top_k < 1 || D->top_k > D->n_exp || D->top_k > kMoeMaxTopK || D->Fe <= 0)) return false;
   return true;
 }
 
@@ -31,6 +33,8 @@ dg_status dims_supported(const dg_dims* D) {
   if (D->hd != 32 && D->hd != 64 && D->hd != 128) return DG_ERR_SHAPE;
   if (D->C > 1024) return DG_ERR_SHAPE;
   if ((int64_t)D->B * D->C > (1 << 20) || (int64_t)D->V > (1 << 30)) return DG_ERR_SHAPE;
+  if (D->n_exp > 0 && (D->Fe % 128 != 0 || D->Fe > 16384 || D->d % 128 != 0 || (int64_t)D->B * D->C > kMoeMaxRows))
+    return DG_ERR_SHAPE;
   return DG_OK;
 }
 
@@ -63,6 +67,7 @@ dg_status check_model(const dg_model* m) {
   if (!m->E || !m->Wq || !m->Wk || !m->Wv || !m->Wo || !m->W1 || !m->W2) return DG_ERR_ARG;
   if (!m->E8 != !m->E8_scale) return DG_ERR_ARG;  // the FP8 head needs codes and scales
   if (reinterpret_cast<uintptr_t>(m->E8) % 16 != 0) return DG_ERR_ARG;  // TMA base
+  if (m->dims.n_exp > 0 && (!m->Wr || !m->We1 || !m->We2)) return DG_ERR_ARG;
   return DG_OK;
 }
 
@@ -91,6 +96,35 @@ struct Prof {
                                     cudaEventRecordExternal);
   }
 };
+
+// The MoE block of layer l on the rows h [rows][d] (in place): RMSNorm,
+// router and top-k, plan, gather, the two grouped expert GEMMs, combine.
+// dbg (optional) receives the routing of this layer.
+dg_status enqueue_moe(const dg_model* m, int l, void* ws, const WsLayout& L, int rows, int C, StopCtl ctl,
+                      int* status, const dg_step_debug* dbg, cudaStream_t st) {
+  const dg_dims& D = m->dims;
+  const int NE = D.n_exp, K = D.top_k, R = rows * (K + 1);
+  DG_TRY(launch_embed_rmsnorm(nullptr, nullptr, nullptr, at<void>(ws, L.moe_x), nullptr, D, rows, 0, ctl, status, st,
+                              at<void>(ws, L.h)));
+  MoeRouteArgs ra{at<void>(ws, L.moe_x), layer_ptr(m->Wr, l, (size_t)NE * D.d), at<int>(ws, L.moe_idx),
+                  at<float>(ws, L.moe_gate), dbg ? dbg->moe_idx : nullptr, dbg ? dbg->moe_gate : nullptr,
+                  dbg ? dbg->moe_logits : nullptr, rows, D.d, NE, K};
+  DG_TRY(launch_moe_route(ra, status, ctl, st));
+  const int max_tiles = cdiv(R, 128) + NE + 1;
+  MoePlanArgs pa{at<int>(ws, L.moe_idx), at<float>(ws, L.moe_gate), at<int>(ws, L.moe_ptok),
+                 at<float>(ws, L.moe_pgate), at<int>(ws, L.moe_slot), at<int4>(ws, L.moe_tiles), rows, NE, K,
+                 max_tiles};
+  DG_TRY(launch_moe_plan(pa, status, ctl, st));
+  DG_TRY(launch_moe_gather(at<void>(ws, L.moe_x), at<int>(ws, L.moe_ptok), at<void>(ws, L.moe_xp), R, D.d, rows,
+                           ctl, st));
+  const size_t e1 = (size_t)(NE + 1) * D.Fe * D.d;  // elements of one layer's We1 (and We2)
+  DG_TRY(launch_moe_experts(at<void>(ws, L.moe_xp), layer_ptr(m->We1, l, e1), layer_ptr(m->We2, l, e1),
+                            at<int4>(ws, L.moe_tiles), max_tiles, R, NE + 1, at<float>(ws, L.moe_pgate),
+                            at<void>(ws, L.moe_gp), at<float>(ws, L.moe_yp), D.d, D.Fe, status, ctl, st));
+  DG_TRY(launch_moe_combine(at<void>(ws, L.h), at<float>(ws, L.moe_yp), at<int>(ws, L.moe_slot), rows, D.d, K, C,
+                            ctl, st));
+  return DG_OK;
+}
 
 // All kernels of one denoising step, in order, on ctx.st.
 // fill_rope: (re)compute the RoPE table of positions P + i; a canvas loop
@@ -142,6 +176,13 @@ dg_status enqueue_step(const StepCtx& c, float tau, float b, float stop_H, uint6
                             at<void>(ws, L.a), D.d, 0, M, D.d, D.Hq * D.hd, D.C, ctl, status,
                             at<float>(ws, L.gpart), L.gpart_elems, c.st));
     DG_TRY(pl.mark(DG_PROF_OPROJ, 1));
+    if (D.n_exp > 0) {
+      DG_TRY(pl.mark(DG_PROF_MOE, 0));
+      dg_status ms = enqueue_moe(c.model, l, ws, L, M, D.C, ctl, status,
+                                 (out && out->debug && l == D.L - 1) ? out->debug : nullptr, c.st);
+      if (ms) return ms;
+      DG_TRY(pl.mark(DG_PROF_MOE, 1));
+    }
   }
   LmArgs lm{};
   lm.h = at<void>(ws, L.h);
@@ -268,6 +309,8 @@ dg_status enqueue_step(const StepCtx& c, float tau, float b, float stop_H, uint6
               {g->g, L.g, bf * M * D.F}};
     for (auto& e : cp)
       if (e.dst) DG_TRY(cudaMemcpyAsync(e.dst, at<void>(ws, e.off), e.bytes, cudaMemcpyDeviceToDevice, c.st));
+    if (g->moe_x && D.n_exp > 0)
+      DG_TRY(cudaMemcpyAsync(g->moe_x, at<void>(ws, L.moe_x), bf * M * D.d, cudaMemcpyDeviceToDevice, c.st));
   }
   return DG_OK;
 }
@@ -358,6 +401,20 @@ bool ws_layout(const dg_dims& D, int32_t cap, WsLayout* L) {
   L->g = take(2 * M * D.F);
   L->h8 = take(M * D.d);
   L->hscale = take(4 * M);
+  if (D.n_exp > 0) {
+    const size_t K = D.top_k, R = M * (K + 1);
+    L->moe_max_tiles = cdiv((int64_t)R, 128) + D.n_exp + 1;
+    L->moe_x = take(2 * M * D.d);
+    L->moe_idx = take(4 * M * K);
+    L->moe_gate = take(4 * M * K);
+    L->moe_slot = take(4 * R);
+    L->moe_ptok = take(4 * R);
+    L->moe_pgate = take(4 * R);
+    L->moe_tiles = take(16 * (size_t)(L->moe_max_tiles + 1));
+    L->moe_xp = take(2 * R * D.d);
+    L->moe_gp = take(2 * R * D.Fe);
+    L->moe_yp = take(4 * R * D.d);
+  }
   L->total = off;
   return true;
 }
@@ -580,6 +637,11 @@ dg_status dg_prefill(const dg_model* model, dg_kv_cache* cache, const int32_t* t
       DG_TRY(launch_gemm_bf16(at<void>(ws, L.o), layer_ptr(model->Wo, l, dd * nq), at<void>(ws, L.h), D.d,
                               at<void>(ws, L.a), D.d, 0, D.B * np, D.d, D.Hq * D.hd, np, none, status,
                               at<float>(ws, L.gpart), L.gpart_elems, st));
+      // the layer's MoE block feeds the next layer (the last layer's is not needed)
+      if (D.n_exp > 0) {
+        dg_status ms = enqueue_moe(model, l, ws, L, D.B * np, np, none, status, nullptr, st);
+        if (ms) return ms;
+      }
     }
     cache->len += np;
     done += np;

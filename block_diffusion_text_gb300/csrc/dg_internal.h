@@ -43,6 +43,10 @@ struct WsLayout {
   size_t gpart, gpart_elems;  // split-K partials of the small GEMMs
   size_t u, g;
   size_t h8, hscale;          // FP8 head: h quantized per row
+  // MoE FFN (n_exp > 0): normalised input, routing, permutation, tile table,
+  // gathered rows, expert hidden and gated outputs (R = rows * (top_k + 1))
+  size_t moe_x, moe_idx, moe_gate, moe_slot, moe_ptok, moe_pgate, moe_tiles, moe_xp, moe_gp, moe_yp;
+  int moe_max_tiles;
   size_t total;
 };
 bool ws_layout(const dg_dims& D, int32_t cap, WsLayout* L);
@@ -126,6 +130,54 @@ struct LmArgs {
   const float *hscale, *escale;
 };
 cudaError_t launch_lmhead(const LmArgs& a, StopCtl ctl, int* status, cudaStream_t st);
+
+// ------------------------------------------------------------ MoE FFN ----
+// Router and top-k per row of x (bf16 [M][d]): fp32 logits x . Wr_e, the
+// top_k experts (value descending, lower index on ties) and their gates
+// (softmax over the selected logits).  idx, gate [M][top_k]; the optional
+// debug copies also get the logits [M][n_exp].
+struct MoeRouteArgs {
+  const void* x;
+  const void* Wr;  // bf16 [n_exp][d]
+  int* idx;
+  float* gate;
+  int32_t* dbg_idx;
+  float *dbg_gate, *dbg_logits;
+  int M, d, n_exp, top_k;
+};
+cudaError_t launch_moe_route(const MoeRouteArgs& a, int* status, StopCtl ctl, cudaStream_t st);
+// Expert-sorted permutation of the M * (top_k + 1) assignments (the shared
+// expert, index n_exp, takes every row with gate 1): per expert, rows in
+// increasing row order.  ptok / pgate [R] (source row and gate of permuted
+// row p), slot [M][top_k + 1] (permuted row of each assignment), and the
+// M-tile table of the grouped GEMMs: tiles[0].x = count, then per tile
+// (expert, first permuted row, rows) in tiles[1 + t].
+struct MoePlanArgs {
+  const int* idx;
+  const float* gate;
+  int* ptok;
+  float* pgate;
+  int* slot;
+  int4* tiles;
+  int M, n_exp, top_k, max_tiles;
+};
+cudaError_t launch_moe_plan(const MoePlanArgs& a, int* status, StopCtl ctl, cudaStream_t st);
+// Shared memory of the plan kernel (bytes); bounds of its one-CTA design.
+int moe_plan_smem(int M, int n_exp);
+constexpr int kMoeMaxRows = 4096, kMoeMaxExperts = 256, kMoeMaxTopK = 16;
+// xp[p] = x[ptok[p]] for the R permuted rows (bf16, d columns; x has M rows).
+cudaError_t launch_moe_gather(const void* x, const int* ptok, void* xp, int R, int d, int M, StopCtl ctl,
+                              cudaStream_t st);
+// Grouped expert GEMMs over the tile table: up: gp = GELU(xp We1_e^T) (bf16
+// [R][Fe]); down: yp = pgate * (gp We2_e^T) (fp32 [R][d]).
+// R: rows of xp / gp / yp; groups = n_exp + 1 stacked expert matrices.
+cudaError_t launch_moe_experts(const void* xp, const void* We1, const void* We2, const int4* tiles,
+                               int max_tiles, int R, int groups, const float* pgate, void* gp, float* yp, int d,
+                               int Fe, int* status, StopCtl ctl, cudaStream_t st);
+// h[r] = bf16(h[r] + sum_j yp[slot[r][j]]), j = 0..top_k (rank order, then
+// the shared expert), on the rows of active canvases (C rows per canvas).
+cudaError_t launch_moe_combine(void* h, const float* yp, const int* slot, int M, int d, int top_k, int C,
+                               StopCtl ctl, cudaStream_t st);
 // Self-conditioning contraction u = p0 . E (split over the vocabulary).
 struct ScArgs {
   const void* pt;        // bf16 [M][V]: p0

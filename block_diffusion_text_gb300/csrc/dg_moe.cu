@@ -1,0 +1,289 @@
+// Mixture-of-experts FFN of a layer (the DiffusionGemma backbone's FFN:
+// "Text diffusion 2026" survey page, DiffusionGemma model section -- 128
+// experts per layer, 8 routed plus one shared; "DiffusionGemma Technical
+// Report" summary, MoE paragraph -- expert weight traffic is the bottleneck
+// of a denoising step, a canvas activating far more experts than one token).
+//
+// One layer's block on the rows h [M][d], x = RMSNorm(h) (bf16, computed by
+// the embedding / RMSNorm kernel):
+//   route    fp32 router logits x . Wr_e, top_k experts per row (value
+//            descending, lower index on ties), gates = softmax over the
+//            selected logits
+//   plan     one CTA: the M * (top_k + 1) assignments (the shared expert
+//            takes every row) sorted by expert, rows in increasing order
+//            within an expert, and the table of 128-row tiles per expert
+//   gather   the expert-sorted copy of x
+//   experts  two grouped tcgen05 GEMMs (dg_gemm.cu): GELU(x We1_e^T), then
+//            gate * (. We2_e^T) in fp32
+//   combine  h += sum over the row's assignments in rank order, then the
+//            shared expert (fp32), rounded to bf16
+// Every weight matrix of an active expert is read once per layer and step
+// (the expert's rows share its B tiles), which is the HBM floor of the block.
+#include <cfloat>
+#include <climits>
+
+#include "dg_common.cuh"
+#include "dg_internal.h"
+
+namespace dg {
+
+constexpr int kRouteRows = 4;  // rows per router CTA, one top-k warp each
+
+DG_DEV void bf16x8(const uint4& u, float (&f)[8]) {
+  const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const float2 p = __bfloat1622float2(b[j]);
+    f[2 * j] = p.x;
+    f[2 * j + 1] = p.y;
+  }
+}
+
+// Router logits of kRouteRows rows against every expert (four warps over the
+// experts, lanes over d), then one warp per row picks the top_k.
+__global__ void __launch_bounds__(128) moe_route_kernel(MoeRouteArgs a, int* status, StopCtl ctl) {
+  pdl_wait();
+  if (all_stopped(ctl.stop_at, ctl.B, ctl.step)) return;
+  extern __shared__ uint4 sm_route[];
+  const int r0 = blockIdx.x * kRouteRows;
+  const int nr = min(kRouteRows, a.M - r0);
+  const int d8 = a.d / 8;
+  uint4* xs = sm_route;
+  float* lg = reinterpret_cast<float*>(xs + kRouteRows * d8);
+  const uint4* x = reinterpret_cast<const uint4*>(a.x);
+  for (int i = threadIdx.x; i < kRouteRows * d8; i += blockDim.x) {
+    const int t = i / d8, c = i % d8;
+    xs[i] = t < nr ? __ldg(x + (size_t)(r0 + t) * d8 + c) : make_uint4(0u, 0u, 0u, 0u);
+  }
+  __syncthreads();
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const uint4* wr = reinterpret_cast<const uint4*>(a.Wr);
+  for (int e = warp; e < a.n_exp; e += 4) {
+    float acc[kRouteRows] = {};
+    for (int c = lane; c < d8; c += 32) {
+      float w[8];
+      bf16x8(__ldg(wr + (size_t)e * d8 + c), w);
+#pragma unroll
+      for (int t = 0; t < kRouteRows; ++t) {
+        float xv[8];
+        bf16x8(xs[t * d8 + c], xv);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[t] = fmaf(xv[j], w[j], acc[t]);
+      }
+    }
+#pragma unroll
+    for (int t = 0; t < kRouteRows; ++t) {
+#pragma unroll
+      for (int o = 16; o; o >>= 1) acc[t] += __shfl_xor_sync(0xffffffffu, acc[t], o);
+    }
+    if (lane == 0)
+      for (int t = 0; t < kRouteRows; ++t) lg[t * a.n_exp + e] = acc[t];
+  }
+  __syncthreads();
+  if (a.dbg_logits)
+    for (int i = threadIdx.x; i < nr * a.n_exp; i += blockDim.x) a.dbg_logits[(size_t)r0 * a.n_exp + i] = lg[i];
+  if (warp >= nr) return;
+  // top-k of row r0 + warp: lane holds experts lane, lane + 32, ... (n_exp <= 256)
+  const int row = r0 + warp;
+  const float* l = lg + warp * a.n_exp;
+  uint32_t taken = 0;
+  float top = 0.f, Z = 0.f;
+  float sv[16];
+  int se[16];
+#pragma unroll 1
+  for (int k = 0; k < a.top_k; ++k) {
+    float bv = -FLT_MAX;
+    int be = INT_MAX;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int e = lane + 32 * j;
+      if (e < a.n_exp && !((taken >> j) & 1u)) {
+        const float v = l[e];
+        if (v > bv || (v == bv && e < be)) {
+          bv = v;
+          be = e;
+        }
+      }
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+      if (ov > bv || (ov == bv && oe < be)) {
+        bv = ov;
+        be = oe;
+      }
+    }
+    if (be < 0 || be >= a.n_exp) {  // non-finite logits: record and route to a valid expert
+      if (lane == 0) atomicExch(status, kStatusValue);
+      be = k;
+      bv = -FLT_MAX;
+    }
+    if ((be & 31) == lane) taken |= 1u << (be >> 5);
+    if (k == 0) top = bv;
+    sv[k] = bv;
+    se[k] = be;
+  }
+  for (int k = 0; k < a.top_k; ++k) Z += expf(sv[k] - top);
+  if (lane == 0) {
+    for (int k = 0; k < a.top_k; ++k) {
+      const float g = expf(sv[k] - top) / Z;
+      a.idx[(size_t)row * a.top_k + k] = se[k];
+      a.gate[(size_t)row * a.top_k + k] = g;
+      if (a.dbg_idx) a.dbg_idx[(size_t)row * a.top_k + k] = se[k];
+      if (a.dbg_gate) a.dbg_gate[(size_t)row * a.top_k + k] = g;
+    }
+  }
+}
+
+cudaError_t launch_moe_route(const MoeRouteArgs& a, int* status, StopCtl ctl, cudaStream_t st) {
+  const size_t smem = (size_t)kRouteRows * a.d * 2 + (size_t)kRouteRows * a.n_exp * 4;
+  cudaError_t e = set_smem_once<moe_route_kernel>(kRouteRows * 16384 * 2 + kRouteRows * 256 * 4);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(moe_route_kernel, dim3(cdiv(a.M, kRouteRows)), dim3(128), smem, st, a, status, ctl);
+}
+
+// The expert-sorted permutation and the tile table, in one CTA.  A bitmap per
+// expert over the rows gives, for each assignment, its rank among the
+// expert's rows (a prefix popcount), so the order is fixed by the data alone.
+__global__ void __launch_bounds__(1024) moe_plan_kernel(MoePlanArgs a, int* status, StopCtl ctl) {
+  pdl_wait();
+  if (all_stopped(ctl.stop_at, ctl.B, ctl.step)) return;
+  extern __shared__ uint32_t sm_plan[];
+  const int G = a.n_exp + 1, W = (a.M + 31) / 32, K1 = a.top_k + 1;
+  const int R = a.M * K1;
+  uint32_t* bm = sm_plan;                               // [G][W]
+  int* cnt = reinterpret_cast<int*>(bm + (size_t)G * W);  // [G]
+  int* off = cnt + G;                                   // [G + 1]
+  int* toff = off + G + 1;                              // [G + 1]
+  for (int i = threadIdx.x; i < G * W; i += blockDim.x) bm[i] = 0u;
+  for (int p = threadIdx.x; p < R; p += blockDim.x) {
+    a.ptok[p] = 0;
+    a.pgate[p] = 0.f;
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < a.M * a.top_k; i += blockDim.x) {
+    int e = a.idx[i];
+    if (e < 0 || e >= a.n_exp) {
+      atomicExch(status, kStatusValue);
+      e = 0;
+    }
+    const int t = i / a.top_k;
+    atomicOr(&bm[(size_t)e * W + t / 32], 1u << (t % 32));
+  }
+  for (int w = threadIdx.x; w < W; w += blockDim.x) {
+    const int left = a.M - 32 * w;
+    bm[(size_t)a.n_exp * W + w] = left >= 32 ? 0xffffffffu : ((1u << left) - 1u);
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < G; e += blockDim.x) {
+    int c = 0;
+    for (int w = 0; w < W; ++w) c += __popc(bm[(size_t)e * W + w]);
+    cnt[e] = c;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int o = 0, to = 0;
+    for (int e = 0; e < G; ++e) {
+      off[e] = o;
+      toff[e] = to;
+      o += cnt[e];
+      to += (cnt[e] + 127) / 128;
+    }
+    off[G] = o;
+    toff[G] = to;
+    a.tiles[0] = make_int4(min(to, a.max_tiles), 0, 0, 0);
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < G; e += blockDim.x) {
+    for (int j = 0; j * 128 < cnt[e]; ++j) {
+      const int ti = toff[e] + j;
+      if (ti < a.max_tiles) a.tiles[1 + ti] = make_int4(e, off[e] + 128 * j, min(128, cnt[e] - 128 * j), 0);
+    }
+  }
+  for (int i = threadIdx.x; i < R; i += blockDim.x) {
+    const int t = i / K1, j = i % K1;
+    int e;
+    float g;
+    if (j < a.top_k) {
+      e = a.idx[(size_t)t * a.top_k + j];
+      if (e < 0 || e >= a.n_exp) e = 0;
+      g = a.gate[(size_t)t * a.top_k + j];
+    } else {
+      e = a.n_exp;
+      g = 1.0f;
+    }
+    const uint32_t* row = bm + (size_t)e * W;
+    int rank = __popc(row[t / 32] & ((1u << (t % 32)) - 1u));
+    for (int w = 0; w < t / 32; ++w) rank += __popc(row[w]);
+    const int p = min(off[e] + rank, R - 1);
+    a.slot[i] = p;
+    a.ptok[p] = t;
+    a.pgate[p] = g;
+  }
+}
+
+int moe_plan_smem(int M, int n_exp) {
+  const int G = n_exp + 1, W = (M + 31) / 32;
+  return (G * W + 3 * (G + 1)) * 4;
+}
+
+cudaError_t launch_moe_plan(const MoePlanArgs& a, int* status, StopCtl ctl, cudaStream_t st) {
+  cudaError_t e = set_smem_once<moe_plan_kernel>(moe_plan_smem(kMoeMaxRows, kMoeMaxExperts));
+  if (e != cudaSuccess) return e;
+  return launch_pdl(moe_plan_kernel, dim3(1), dim3(1024), (size_t)moe_plan_smem(a.M, a.n_exp), st, a, status,
+                    ctl);
+}
+
+__global__ void __launch_bounds__(256) moe_gather_kernel(const uint4* __restrict__ x, const int* __restrict__ ptok,
+                                                         uint4* __restrict__ xp, int R, int d8, int M, StopCtl ctl) {
+  pdl_wait();
+  if (all_stopped(ctl.stop_at, ctl.B, ctl.step)) return;
+  const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= (size_t)R * d8) return;
+  const int p = (int)(i / d8), c = (int)(i % d8);
+  const int t = min(max(ptok[p], 0), M - 1);
+  xp[i] = __ldg(x + (size_t)t * d8 + c);
+}
+
+cudaError_t launch_moe_gather(const void* x, const int* ptok, void* xp, int R, int d, int M, StopCtl ctl,
+                              cudaStream_t st) {
+  const size_t n = (size_t)R * (d / 8);
+  return launch_pdl(moe_gather_kernel, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, st,
+                    reinterpret_cast<const uint4*>(x), ptok, reinterpret_cast<uint4*>(xp), R, d / 8, M, ctl);
+}
+
+// One thread per 8 columns of a row: the row's gated expert outputs summed in
+// rank order, then the shared expert, added to h and rounded once.
+__global__ void __launch_bounds__(256) moe_combine_kernel(__nv_bfloat16* h, const float* __restrict__ yp,
+                                                          const int* __restrict__ slot, int M, int d, int K1,
+                                                          int C, StopCtl ctl) {
+  pdl_wait();
+  if (all_stopped(ctl.stop_at, ctl.B, ctl.step)) return;
+  const int row = blockIdx.y;
+  const int c8 = (blockIdx.x * blockDim.x + threadIdx.x) * 8;
+  if (c8 >= d || !canvas_active(ctl.stop_at, row / C, ctl.step)) return;
+  const int R = M * K1;
+  float s[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  for (int j = 0; j < K1; ++j) {
+    const int p = min(max(slot[(size_t)row * K1 + j], 0), R - 1);
+    const float4* src = reinterpret_cast<const float4*>(yp + (size_t)p * d + c8);
+    const float4 u = src[0], v = src[1];
+    s[0] += u.x; s[1] += u.y; s[2] += u.z; s[3] += u.w;
+    s[4] += v.x; s[5] += v.y; s[6] += v.z; s[7] += v.w;
+  }
+  uint4* hp = reinterpret_cast<uint4*>(h + (size_t)row * d + c8);
+  float hv[8];
+  bf16x8(*hp, hv);
+  *hp = make_uint4(pack_bf16(hv[0] + s[0], hv[1] + s[1]), pack_bf16(hv[2] + s[2], hv[3] + s[3]),
+                   pack_bf16(hv[4] + s[4], hv[5] + s[5]), pack_bf16(hv[6] + s[6], hv[7] + s[7]));
+}
+
+cudaError_t launch_moe_combine(void* h, const float* yp, const int* slot, int M, int d, int top_k, int C,
+                               StopCtl ctl, cudaStream_t st) {
+  dim3 grid(cdiv(d / 8, 256), M);
+  return launch_pdl(moe_combine_kernel, grid, dim3(256), 0, st, reinterpret_cast<__nv_bfloat16*>(h), yp, slot, M,
+                    d, top_k + 1, C, ctl);
+}
+
+}  // namespace dg

@@ -40,12 +40,13 @@ class DgError(RuntimeError):
 class dg_dims(ct.Structure):
     _fields_ = [("V", ct.c_int32), ("d", ct.c_int32), ("C", ct.c_int32), ("B", ct.c_int32),
                 ("Hq", ct.c_int32), ("Hkv", ct.c_int32), ("hd", ct.c_int32), ("F", ct.c_int32),
-                ("rope_base", ct.c_float), ("rms_eps", ct.c_float), ("L", ct.c_int32)]
+                ("rope_base", ct.c_float), ("rms_eps", ct.c_float), ("L", ct.c_int32),
+                ("n_exp", ct.c_int32), ("top_k", ct.c_int32), ("Fe", ct.c_int32)]
 
 
 class dg_model(ct.Structure):
     _fields_ = [("dims", dg_dims)] + [(n, ct.c_void_p) for n in ("E", "Wq", "Wk", "Wv", "Wo", "W1", "W2",
-                                                                 "E8", "E8_scale")]
+                                                                 "E8", "E8_scale", "Wr", "We1", "We2")]
 
 
 class dg_kv_cache(ct.Structure):
@@ -58,7 +59,8 @@ class dg_canvas(ct.Structure):
 
 
 class dg_step_debug(ct.Structure):
-    _fields_ = [(n, ct.c_void_p) for n in ("a", "q", "k", "v", "o", "h", "u", "g", "logits")]
+    _fields_ = [(n, ct.c_void_p) for n in ("a", "q", "k", "v", "o", "h", "u", "g", "logits", "moe_idx", "moe_gate",
+                                           "moe_logits", "moe_x")]
 
 
 class dg_step_out(ct.Structure):
@@ -68,7 +70,7 @@ class dg_step_out(ct.Structure):
 
 # Kernel slots of one step (dg_step_out.events), in launch order.
 PROF_SLOTS = ("embed", "qkv", "attn", "oproj", "lmhead", "stats", "sampler", "p0", "selfcond",
-              "reduce", "ffw1", "ffw2")
+              "reduce", "ffw1", "ffw2", "moe")
 
 
 class dg_sched(ct.Structure):
@@ -157,7 +159,8 @@ def _stream(stream=None):
 
 def make_dims(d) -> dg_dims:
     return dg_dims(V=d.V, d=d.d, C=d.C, B=d.B, Hq=d.Hq, Hkv=d.Hkv, hd=d.hd, F=d.F,
-                   rope_base=d.rope_base, rms_eps=d.rms_eps, L=getattr(d, "L", 1))
+                   rope_base=d.rope_base, rms_eps=d.rms_eps, L=getattr(d, "L", 1),
+                   n_exp=getattr(d, "n_exp", 0), top_k=getattr(d, "top_k", 0), Fe=getattr(d, "Fe", 0))
 
 
 def workspace_size(dims, cap: int) -> int:
@@ -184,7 +187,8 @@ class Model:
         self.s = dg_model(make_dims(dims), *[ct.c_void_p(w[k].data_ptr()) for k in
                                              ("E", "Wq", "Wk", "Wv", "Wo", "W1", "W2")],
                           ct.c_void_p(self.E8.data_ptr() if fp8_head else None),
-                          ct.c_void_p(self.E8_scale.data_ptr() if fp8_head else None))
+                          ct.c_void_p(self.E8_scale.data_ptr() if fp8_head else None),
+                          *[ct.c_void_p(w[k].data_ptr() if k in w else None) for k in ("Wr", "We1", "We2")])
         self.ws_bytes = workspace_size(dims, self.cap)
         # zero-initialised: the first word is the device status word
         self.ws = torch.zeros(self.ws_bytes + 256, dtype=torch.uint8, device=self.K.device)
@@ -254,6 +258,8 @@ def denoise_step(model: Model, canvas: Canvas, tau: float, b: float, seed: int, 
             _STEP_OUT_CACHE.clear()  # one entry: the output set of the latest plain call
             _STEP_OUT_CACHE[ptrs] = so
     if events is not None:
+        if len(events) != 2 * len(PROF_SLOTS):
+            raise ValueError(f"events: expected {2 * len(PROF_SLOTS)} entries, got {len(events)}")
         arr = (ct.c_void_p * len(events))(*[ct.c_void_p(e.cuda_event if e is not None else 0) for e in events])
         so.events = ct.cast(arr, ct.POINTER(ct.c_void_p))
     dbg = None
@@ -264,7 +270,14 @@ def denoise_step(model: Model, canvas: Canvas, tau: float, b: float, seed: int, 
                      o=torch.empty(M, d.Hq * d.hd, **bf), h=torch.empty(M, d.d, **bf),
                      u=torch.empty(M, d.d, **bf), g=torch.empty(M, d.F, **bf),
                      logits=torch.empty(M, d.V, dtype=torch.float32, device=dev))
-        dbg = dg_step_debug(*[_ptr(dbg_t[k]) for k in ("a", "q", "k", "v", "o", "h", "u", "g", "logits")])
+        ne, tk = getattr(d, "n_exp", 0), getattr(d, "top_k", 0)
+        if ne > 0:
+            dbg_t.update(moe_idx=torch.empty(M, tk, dtype=torch.int32, device=dev),
+                         moe_gate=torch.empty(M, tk, dtype=torch.float32, device=dev),
+                         moe_logits=torch.empty(M, ne, dtype=torch.float32, device=dev),
+                         moe_x=torch.empty(M, d.d, **bf))
+        dbg = dg_step_debug(*[_ptr(dbg_t.get(k)) for k in ("a", "q", "k", "v", "o", "h", "u", "g", "logits",
+                                                            "moe_idx", "moe_gate", "moe_logits", "moe_x")])
         so.debug = ct.pointer(dbg)
         out["debug"] = dbg_t
     cs = canvas.struct()

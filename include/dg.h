@@ -85,11 +85,21 @@ enum {
  *   L    attention layers (1..64).  The stand-in's layer l takes a_l (a_0 =
  *        RMSNorm(E[x] + z)), h_l = a_l + Attn_l(a_l) Wo_l^T, a_{l+1} =
  *        RMSNorm(h_l); the LM head reads h_{L-1}; layer l attends over its own
- *        prefix cache.  L = 1 is the single-layer model.                       */
+ *        prefix cache.  L = 1 is the single-layer model.
+ *   n_exp, top_k, Fe  optional mixture-of-experts FFN after each attention
+ *        block [SURV] (n_exp = 0: none): n_exp routed experts (1..256) of
+ *        hidden width Fe (multiple of 128), top_k (1..min(16, n_exp)) of them
+ *        per token, plus one shared expert of the same shape.  Layer l then
+ *        takes h_l <- h_l + sum_j g_j FFN_{e_j}(x) + FFN_shared(x) with
+ *        x = RMSNorm(h_l), router logits r = x Wr_l^T (fp32), e_j the top_k
+ *        experts (value descending, lower index on ties), g = softmax of their
+ *        logits, FFN_e(x) = We2_e GELU(We1_e x); a_{l+1} = RMSNorm(h_l).  Needs
+ *        d a multiple of 128 and B*C <= 4096.                                  */
 typedef struct dg_dims {
   int32_t V, d, C, B, Hq, Hkv, hd, F;
   float rope_base, rms_eps;
   int32_t L;
+  int32_t n_exp, top_k, Fe;
 } dg_dims;
 
 /* Weights (device, bf16):
@@ -103,12 +113,16 @@ typedef struct dg_dims {
  *   given, else DG_ERR_ARG).  Each step then quantizes h per row the same
  *   way and takes the logits l_v = alpha s_h s_v (q_h . q_v) / sqrt(d) on the
  *   E4M3 tensor cores (fp32 accumulation); the embedding lookup and the
- *   self-conditioning contraction p0 . E keep the bf16 E.                    */
+ *   self-conditioning contraction p0 . E keep the bf16 E.
+ * MoE FFN (n_exp > 0; bf16, stacked per layer; else ignored):
+ *   Wr [L][n_exp][d] router; We1 [L][n_exp + 1][Fe][d], We2 [L][n_exp + 1][d][Fe]
+ *   expert matrices, index n_exp being the shared expert.                    */
 typedef struct dg_model {
   dg_dims dims;
   const void *E, *Wq, *Wk, *Wv, *Wo, *W1, *W2;
   const void* E8;
   const float* E8_scale;
+  const void *Wr, *We1, *We2;
 } dg_model;
 
 /* Static prefix KV cache ([CH12] "prompt / finished output block -> causal
@@ -139,10 +153,18 @@ typedef struct dg_canvas {
 /* Optional copies of the intermediates of one step, for checking (every
  * pointer may be NULL).  Device buffers:
  *   a, h [B*C][d]; q [B][Hq][C][hd]; k, v [B][Hkv][C][hd]; o [B*C][Hq*hd];
- *   u [B*C][d]; g [B*C][F]  (bf16)      logits fp32 [B*C][V] (l = alpha h.E / sqrt d) */
+ *   u [B*C][d]; g [B*C][F]  (bf16)      logits fp32 [B*C][V] (l = alpha h.E / sqrt d)
+ *   MoE routing of the last layer (n_exp > 0): moe_idx int32 [B*C][top_k]
+ *   (experts in rank order), moe_gate fp32 [B*C][top_k], moe_logits fp32
+ *   [B*C][n_exp] (router logits), moe_x bf16 [B*C][d] (the router's input
+ *   RMSNorm(h)).  h is the last layer's output (after its MoE block when there
+ *   is one).                                                                 */
 typedef struct dg_step_debug {
   void *a, *q, *k, *v, *o, *h, *u, *g;
   float* logits;
+  int32_t* moe_idx;
+  float *moe_gate, *moe_logits;
+  void* moe_x;
 } dg_step_debug;
 
 /* Kernel slots of a step, in launch order, for dg_step_out.events. */
@@ -159,7 +181,8 @@ enum {
   DG_PROF_REDUCE = 9,    /* reduction of p0 . E, sampled tokens        */
   DG_PROF_FFW1 = 10,     /* GELU(W1 u)                                */
   DG_PROF_FFW2 = 11,     /* z = W2 g                                  */
-  DG_PROF_NUM = 12
+  DG_PROF_MOE = 12,      /* MoE FFN of the first layer (n_exp > 0)    */
+  DG_PROF_NUM = 13
 };
 
 /* Per-step outputs (device; any pointer may be NULL except where noted):

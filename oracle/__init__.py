@@ -63,7 +63,7 @@ class StepOut(ct.Structure):
                 ("cum", _D), ("rank", _I), ("renoise_tok", _I), ("sample_tok", _I),
                 ("gumbel_gap", _D), ("tokens_out", _I), ("u", _D), ("g", _D), ("z_out", _D),
                 ("n_acc", _I), ("meanH", _D), ("stop", _I), ("moe_idx", _I), ("moe_gate", _D),
-                ("moe_logits", _D)]
+                ("moe_logits", _D), ("moe_x", _D)]
 
 
 def lib():
@@ -341,7 +341,7 @@ def denoise_step(dims, w, x, z, alpha, tau, b, seed, step, block=0, prev_argmax=
                   rank=(M,), renoise_tok=(M,), sample_tok=(M,), gumbel_gap=(M,), tokens_out=(M,),
                   u=(M, d), g=(M, F), z_out=(M, d), n_acc=(B,), meanH=(B,), stop=(B,))
     ne, tk = getattr(dims, "n_exp", 0), getattr(dims, "top_k", 0)
-    shapes.update(moe_idx=(M, tk), moe_gate=(M, tk), moe_logits=(M, ne))
+    shapes.update(moe_idx=(M, tk), moe_gate=(M, tk), moe_logits=(M, ne), moe_x=(M, d))
     types = dict(argmax=np.int32, accept=np.uint8, rank=np.int32, renoise_tok=np.int32,
                  sample_tok=np.int32, tokens_out=np.int32, n_acc=np.int32, stop=np.int32, moe_idx=np.int32)
     outs = {}

@@ -422,6 +422,7 @@ typedef struct {
   // their gates, [B*C][top_k]; the router logits [B*C][n_exp]
   int32_t* moe_idx;
   double *moe_gate, *moe_logits;
+  double* moe_x;  // the last layer's router input RMSNorm(h) [B*C][d]
 } or_step_out;
 
 // ------------------------------------------------------------------ MoE -----
@@ -441,9 +442,9 @@ typedef struct {
 // The pages give neither the expert width nor the gating formula; the
 // softmax-then-top-k-renormalised gate and the two-matrix GELU expert (the
 // self-conditioning FFW's shape) are the plainest readings.  Optional outputs:
-// idx [n][top_k], gate [n][top_k], logits [n][n_exp].
+// idx [n][top_k], gate [n][top_k], logits [n][n_exp], x [n][d] (the router's input).
 void moe_ffn(const or_dims* D, const float* Wr, const float* We1, const float* We2, double* h, int64_t n,
-             int32_t* idx_out, double* gate_out, double* logit_out, int nthreads) {
+             int32_t* idx_out, double* gate_out, double* logit_out, double* x_out, int nthreads) {
   const int64_t d = D->d, NE = D->n_exp, K = D->top_k, Fe = D->Fe;
   const int mir = D->mirror_bf16;
   parallel_rows(n, nthreads, [&](int64_t r) {
@@ -451,6 +452,8 @@ void moe_ffn(const or_dims* D, const float* Wr, const float* We1, const float* W
     std::vector<double> x(d), rl(NE), hid(Fe), y(d, 0.0);
     or_rmsnorm(hr, (int32_t)d, D->rms_eps, x.data());
     for (int64_t j = 0; j < d; ++j) x[j] = maybe_bf16(x[j], mir);
+    if (x_out)
+      for (int64_t j = 0; j < d; ++j) x_out[r * d + j] = x[j];
     for (int64_t e = 0; e < NE; ++e) {
       double acc = 0.0;
       for (int64_t j = 0; j < d; ++j) acc += x[j] * (double)Wr[e * d + j];
@@ -610,7 +613,7 @@ int or_denoise_step(const or_dims* D, const or_step_in* in, or_step_out* out, co
       moe_ffn(D, in->moe.Wr + l * D->n_exp * d, in->moe.We1 + l * (D->n_exp + 1) * (int64_t)D->Fe * d,
               in->moe.We2 + l * (D->n_exp + 1) * d * (int64_t)D->Fe, hh.data(), M,
               lastl ? out->moe_idx : nullptr, lastl ? out->moe_gate : nullptr,
-              lastl ? out->moe_logits : nullptr, nthreads);
+              lastl ? out->moe_logits : nullptr, lastl ? out->moe_x : nullptr, nthreads);
     }
   }
 
@@ -955,7 +958,7 @@ int or_prefill(const or_dims* D, const float* E, const float* Wq, const float* W
     if (D->n_exp > 0)
       moe_ffn(D, moe->Wr + l * D->n_exp * d, moe->We1 + l * (D->n_exp + 1) * (int64_t)D->Fe * d,
               moe->We2 + l * (D->n_exp + 1) * d * (int64_t)D->Fe, hh.data(), Mn, nullptr, nullptr, nullptr,
-              nthreads);
+              nullptr, nthreads);
   }
   return 0;
 }
@@ -974,7 +977,7 @@ int or_moe_ffn(const or_dims* D, const float* Wr, const float* We1, const float*
                int32_t* idx, double* gate, double* logits, int32_t nthreads) {
   if (!D || D->n_exp < 1 || D->top_k < 1 || D->top_k > D->n_exp || D->Fe < 1 || !Wr || !We1 || !We2 || n < 0)
     return 1;
-  moe_ffn(D, Wr, We1, We2, h, n, idx, gate, logits, nthreads);
+  moe_ffn(D, Wr, We1, We2, h, n, idx, gate, logits, nullptr, nthreads);
   return 0;
 }
 

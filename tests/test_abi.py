@@ -3,6 +3,7 @@ rejects bad arguments with the documented codes before touching the device.
 Device pointers passed here are never dereferenced: every call takes an error
 path that returns before any CUDA call."""
 import ctypes as ct
+import dataclasses
 import os
 import re
 
@@ -236,3 +237,30 @@ def test_fp8_head_entry_points_validate(dg):
         m.E8, m.E8_scale = e8, es
         assert L.dg_denoise_step(ct.byref(m), ct.byref(c), ct.byref(cv), 0.8, 0.1, 1, 0, 0, ws, wsb, None,
                                  None) == dg.DG_ERR_ARG
+
+
+def test_moe_dims_and_weights_validate(dg):
+    L = dg.load()
+    n = ct.c_size_t()
+    base = _dims()
+
+    def ws_rc(**kw):
+        dd = dg.make_dims(base)
+        for k, v in kw.items():
+            setattr(dd, k, v)
+        return L.dg_workspace_size(ct.byref(dd), 2048, ct.byref(n))
+    assert ws_rc(n_exp=128, top_k=8, Fe=768) == dg.DG_OK
+    assert ws_rc(n_exp=128, top_k=0, Fe=768) == dg.DG_ERR_ARG
+    assert ws_rc(n_exp=4, top_k=5, Fe=768) == dg.DG_ERR_ARG
+    assert ws_rc(n_exp=257, top_k=8, Fe=768) == dg.DG_ERR_ARG
+    assert ws_rc(n_exp=128, top_k=17, Fe=768) == dg.DG_ERR_ARG
+    assert ws_rc(n_exp=-1) == dg.DG_ERR_ARG
+    assert ws_rc(n_exp=128, top_k=8, Fe=700) == dg.DG_ERR_SHAPE
+    assert ws_rc(n_exp=128, top_k=8, Fe=768, d=1088) == dg.DG_ERR_SHAPE   # d not a multiple of 128
+    assert ws_rc(n_exp=128, top_k=8, Fe=768, B=17) == dg.DG_ERR_SHAPE    # B * C > 4096
+    dims = dataclasses.replace(base, n_exp=16, top_k=4, Fe=128)
+    m, c, cv, wsb = _structs(dg, dims)
+    ws = ct.c_void_p(1 << 30)
+    m.Wr, m.We1, m.We2 = ct.c_void_p(FAKE), None, ct.c_void_p(FAKE)
+    assert L.dg_denoise_step(ct.byref(m), ct.byref(c), ct.byref(cv), 0.8, 0.1, 1, 0, 0, ws, wsb, None,
+                             None) == dg.DG_ERR_ARG
