@@ -20,6 +20,7 @@ instead (rank 0 only).
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import math
 import os
@@ -516,6 +517,50 @@ def run_ours(args, world, rank, local):
         if m8.status() != 0:
             raise RuntimeError("device status word set in the FP8 variant")
         del m8, c8, o8
+
+        # the MoE FFN after the attention block (128 experts, top 8 + shared, Fe 768, 84 hot experts:
+        # the pages' canvas-level activation), same workload otherwise
+        dmoe = dataclasses.replace(dims, n_exp=128, top_k=8, Fe=768, moe_hot=84)
+        wm = dict(w)
+        wm.update({k: v for k, v in synth.make_weights(dmoe, seed + 1, device=dev).items()
+                   if k in ("Wr", "We1", "We2")})
+        mm = dg.Model(dmoe, wm)
+        cmo = dg.Canvas(x0.clone(), z0.clone(), a)
+        om = [None]
+        dbg_run = dg.denoise_step(mm, cmo, tau=taus[0], b=0.1, seed=seed, step=0, debug=True)
+        n_active = int(torch.unique(dbg_run["debug"]["moe_idx"]).numel()) + 1  # + the shared expert
+        del dbg_run
+        mo_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * len(slots))] for _ in range(kv)]
+        for row in mo_ev:
+            for e in row:
+                e.record(stream)
+
+        def stepmo(s, events=None):
+            om[0] = dg.denoise_step(mm, cmo, tau=taus[s % 48], b=0.1, seed=seed, step=s % 48, out=om[0],
+                                    events=events)
+        for s in range(3):
+            stepmo(s)
+        torch.cuda.synchronize()
+        msmo = time_graph(stepmo, kv)
+        time_graph(lambda s: stepmo(s, events=mo_ev[s]), kv)
+        k = slots.index("moe")
+        moe_ms = statistics.mean(mo_ev[s][2 * k].elapsed_time(mo_ev[s][2 * k + 1]) for s in range(kv))
+        wbytes = 2.0 * n_active * 2 * dmoe.Fe * dmoe.d + 2.0 * dmoe.n_exp * dmoe.d  # active experts + router
+        mflop = 2.0 * dmoe.M * (dmoe.top_k + 1) * 2 * dmoe.Fe * dmoe.d
+        variants["moe_ffn"] = {
+            "value": 1e3 / msmo, "unit": UNIT, "ms_per_step": msmo, "steps": kv,
+            "config": {"n_exp": 128, "top_k": 8, "shared": 1, "Fe": dmoe.Fe, "hot_experts": 84},
+            "experts_active": n_active, "moe_ms": moe_ms,
+            "moe_roofline": {"bound": "hbm", "achieved": wbytes / (moe_ms / 1e3) / 1e9, "peak": peaks["hbm"],
+                             "unit": "GB/s", "frac": wbytes / (moe_ms / 1e3) / 1e9 / peaks["hbm"],
+                             "algorithmic": {"bytes": wbytes, "flop": mflop},
+                             "tflops": mflop / (moe_ms / 1e3) / 1e12,
+                             "note": "bytes: the active experts' two matrices (each read once per step) and the "
+                                     "router; the block's kernels: RMSNorm, router, plan, gather, two grouped "
+                                     "GEMMs, combine"}}
+        if mm.status() != 0:
+            raise RuntimeError("device status word set in the MoE variant")
+        del mm, cmo, om, wm
 
         mask_id = dims.V - 1
         cm = dg.Canvas(dg.canvas_init_masked(dims.B, dims.C, mask_id, device=dev), z0.clone(), a)

@@ -1008,6 +1008,14 @@ cudaError_t launch_debug_gemm(const void* A, const void* Bm, float* D, int M, in
   return run_gemm<256, 4, true>(mA, mB, mB, mB, N, 0, 64, M, N, K, lbo, sbo, epi, status, ctl, st);
 }
 
+cudaError_t launch_gemm_f32_partials(const void* A, const void* W, float* part, int M, int N, int K, int ks,
+                                     StopCtl ctl, int* status, cudaStream_t st) {
+  CUtensorMap mA, mB;
+  if (!tmap_kmajor(&mA, A, M, K, kBM) || !tmap_kmajor(&mB, W, N, K, 128)) return cudaErrorInvalidValue;
+  EpiPartial ep{part, M, N};
+  return run_gemm<128, 4, false>(mA, mB, mB, mB, N, 0, 128, M, N, K, 0, 0, ep, status, ctl, st, ks);
+}
+
 int gemm_ksplit(int M, int N, int K) {
   const int tiles = cdiv(M, kBM) * cdiv(N, 128);
   const int nk = cdiv(K, kBK);

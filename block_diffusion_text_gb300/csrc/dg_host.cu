@@ -109,7 +109,7 @@ dg_status enqueue_moe(const dg_model* m, int l, void* ws, const WsLayout& L, int
   MoeRouteArgs ra{at<void>(ws, L.moe_x), layer_ptr(m->Wr, l, (size_t)NE * D.d), at<int>(ws, L.moe_idx),
                   at<float>(ws, L.moe_gate), dbg ? dbg->moe_idx : nullptr, dbg ? dbg->moe_gate : nullptr,
                   dbg ? dbg->moe_logits : nullptr, rows, D.d, NE, K};
-  DG_TRY(launch_moe_route(ra, status, ctl, st));
+  DG_TRY(launch_moe_route(ra, at<float>(ws, L.moe_rpart), L.moe_rpart_elems, status, ctl, st));
   const int max_tiles = cdiv(R, 128) + NE + 1;
   MoePlanArgs pa{at<int>(ws, L.moe_idx), at<float>(ws, L.moe_gate), at<int>(ws, L.moe_ptok),
                  at<float>(ws, L.moe_pgate), at<int>(ws, L.moe_slot), at<int4>(ws, L.moe_tiles), rows, NE, K,
@@ -414,6 +414,8 @@ bool ws_layout(const dg_dims& D, int32_t cap, WsLayout* L) {
     L->moe_xp = take(2 * R * D.d);
     L->moe_gp = take(2 * R * D.Fe);
     L->moe_yp = take(4 * R * D.d);
+    L->moe_rpart_elems = (size_t)gemm_ksplit((int)M, D.n_exp, D.d) * M * D.n_exp;
+    L->moe_rpart = take(4 * L->moe_rpart_elems);
   }
   L->total = off;
   return true;

@@ -46,6 +46,7 @@ struct WsLayout {
   // MoE FFN (n_exp > 0): normalised input, routing, permutation, tile table,
   // gathered rows, expert hidden and gated outputs (R = rows * (top_k + 1))
   size_t moe_x, moe_idx, moe_gate, moe_slot, moe_ptok, moe_pgate, moe_tiles, moe_xp, moe_gp, moe_yp;
+  size_t moe_rpart, moe_rpart_elems;  // router GEMM partials
   int moe_max_tiles;
   size_t total;
 };
@@ -145,7 +146,14 @@ struct MoeRouteArgs {
   float *dbg_gate, *dbg_logits;
   int M, d, n_exp, top_k;
 };
-cudaError_t launch_moe_route(const MoeRouteArgs& a, int* status, StopCtl ctl, cudaStream_t st);
+// The router logits run as a K-split tcgen05 GEMM into fp32 partials `part`
+// (room for part_elems floats), summed by the top-k kernel.
+cudaError_t launch_moe_route(const MoeRouteArgs& a, float* part, size_t part_elems, int* status, StopCtl ctl,
+                             cudaStream_t st);
+// part [ks][M][N] = the K-split partial products of A [M][K] and W [N][K] (bf16).
+cudaError_t launch_gemm_f32_partials(const void* A, const void* W, float* part, int M, int N, int K, int ks,
+                                     StopCtl ctl, int* status, cudaStream_t st);
+int gemm_ksplit(int M, int N, int K);
 // Expert-sorted permutation of the M * (top_k + 1) assignments (the shared
 // expert, index n_exp, takes every row with gate 1): per expert, rows in
 // increasing row order.  ptok / pgate [R] (source row and gate of permuted

@@ -27,7 +27,7 @@
 
 namespace dg {
 
-constexpr int kRouteRows = 4;  // rows per router CTA, one top-k warp each
+constexpr int kTopkRows = 8;  // rows per top-k CTA, one warp each
 
 DG_DEV void bf16x8(const uint4& u, float (&f)[8]) {
   const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&u);
@@ -39,57 +39,30 @@ DG_DEV void bf16x8(const uint4& u, float (&f)[8]) {
   }
 }
 
-// Router logits of kRouteRows rows against every expert (four warps over the
-// experts, lanes over d), then one warp per row picks the top_k.
-__global__ void __launch_bounds__(128) moe_route_kernel(MoeRouteArgs a, int* status, StopCtl ctl) {
+// Router logits from the K-split partials of the router GEMM x Wr^T (summed in
+// split order), then the row's top_k: one warp per row, lane holding experts
+// lane, lane + 32, ... (n_exp <= 256).
+__global__ void __launch_bounds__(kTopkRows * 32) moe_topk_kernel(MoeRouteArgs a, const float* __restrict__ part,
+                                                                  int ksplit, int* status, StopCtl ctl) {
   pdl_wait();
   if (all_stopped(ctl.stop_at, ctl.B, ctl.step)) return;
-  extern __shared__ uint4 sm_route[];
-  const int r0 = blockIdx.x * kRouteRows;
-  const int nr = min(kRouteRows, a.M - r0);
-  const int d8 = a.d / 8;
-  uint4* xs = sm_route;
-  float* lg = reinterpret_cast<float*>(xs + kRouteRows * d8);
-  const uint4* x = reinterpret_cast<const uint4*>(a.x);
-  for (int i = threadIdx.x; i < kRouteRows * d8; i += blockDim.x) {
-    const int t = i / d8, c = i % d8;
-    xs[i] = t < nr ? __ldg(x + (size_t)(r0 + t) * d8 + c) : make_uint4(0u, 0u, 0u, 0u);
-  }
-  __syncthreads();
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const uint4* wr = reinterpret_cast<const uint4*>(a.Wr);
-  for (int e = warp; e < a.n_exp; e += 4) {
-    float acc[kRouteRows] = {};
-    for (int c = lane; c < d8; c += 32) {
-      float w[8];
-      bf16x8(__ldg(wr + (size_t)e * d8 + c), w);
+  const int row = blockIdx.x * kTopkRows + warp;
+  if (row >= a.M) return;
+  float l[8];
 #pragma unroll
-      for (int t = 0; t < kRouteRows; ++t) {
-        float xv[8];
-        bf16x8(xs[t * d8 + c], xv);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) acc[t] = fmaf(xv[j], w[j], acc[t]);
-      }
-    }
-#pragma unroll
-    for (int t = 0; t < kRouteRows; ++t) {
-#pragma unroll
-      for (int o = 16; o; o >>= 1) acc[t] += __shfl_xor_sync(0xffffffffu, acc[t], o);
-    }
-    if (lane == 0)
-      for (int t = 0; t < kRouteRows; ++t) lg[t * a.n_exp + e] = acc[t];
+  for (int j = 0; j < 8; ++j) {
+    const int e = lane + 32 * j;
+    float v = 0.f;
+    if (e < a.n_exp)
+      for (int sp = 0; sp < ksplit; ++sp) v += part[((size_t)sp * a.M + row) * a.n_exp + e];
+    l[j] = v;
+    if (a.dbg_logits && e < a.n_exp) a.dbg_logits[(size_t)row * a.n_exp + e] = v;
   }
-  __syncthreads();
-  if (a.dbg_logits)
-    for (int i = threadIdx.x; i < nr * a.n_exp; i += blockDim.x) a.dbg_logits[(size_t)r0 * a.n_exp + i] = lg[i];
-  if (warp >= nr) return;
-  // top-k of row r0 + warp: lane holds experts lane, lane + 32, ... (n_exp <= 256)
-  const int row = r0 + warp;
-  const float* l = lg + warp * a.n_exp;
   uint32_t taken = 0;
   float top = 0.f, Z = 0.f;
-  float sv[16];
-  int se[16];
+  float sv[kMoeMaxTopK];
+  int se[kMoeMaxTopK];
 #pragma unroll 1
   for (int k = 0; k < a.top_k; ++k) {
     float bv = -FLT_MAX;
@@ -97,12 +70,9 @@ __global__ void __launch_bounds__(128) moe_route_kernel(MoeRouteArgs a, int* sta
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       const int e = lane + 32 * j;
-      if (e < a.n_exp && !((taken >> j) & 1u)) {
-        const float v = l[e];
-        if (v > bv || (v == bv && e < be)) {
-          bv = v;
-          be = e;
-        }
+      if (e < a.n_exp && !((taken >> j) & 1u) && (l[j] > bv || (l[j] == bv && e < be))) {
+        bv = l[j];
+        be = e;
       }
     }
 #pragma unroll
@@ -125,22 +95,30 @@ __global__ void __launch_bounds__(128) moe_route_kernel(MoeRouteArgs a, int* sta
     se[k] = be;
   }
   for (int k = 0; k < a.top_k; ++k) Z += expf(sv[k] - top);
-  if (lane == 0) {
-    for (int k = 0; k < a.top_k; ++k) {
-      const float g = expf(sv[k] - top) / Z;
-      a.idx[(size_t)row * a.top_k + k] = se[k];
-      a.gate[(size_t)row * a.top_k + k] = g;
-      if (a.dbg_idx) a.dbg_idx[(size_t)row * a.top_k + k] = se[k];
-      if (a.dbg_gate) a.dbg_gate[(size_t)row * a.top_k + k] = g;
-    }
+  if (lane < a.top_k) {
+    float v = sv[0];
+    int e = se[0];
+    for (int k = 1; k < a.top_k; ++k)
+      if (k == lane) {
+        v = sv[k];
+        e = se[k];
+      }
+    const float g = expf(v - top) / Z;
+    a.idx[(size_t)row * a.top_k + lane] = e;
+    a.gate[(size_t)row * a.top_k + lane] = g;
+    if (a.dbg_idx) a.dbg_idx[(size_t)row * a.top_k + lane] = e;
+    if (a.dbg_gate) a.dbg_gate[(size_t)row * a.top_k + lane] = g;
   }
 }
 
-cudaError_t launch_moe_route(const MoeRouteArgs& a, int* status, StopCtl ctl, cudaStream_t st) {
-  const size_t smem = (size_t)kRouteRows * a.d * 2 + (size_t)kRouteRows * a.n_exp * 4;
-  cudaError_t e = set_smem_once<moe_route_kernel>(kRouteRows * 16384 * 2 + kRouteRows * 256 * 4);
+cudaError_t launch_moe_route(const MoeRouteArgs& a, float* part, size_t part_elems, int* status, StopCtl ctl,
+                             cudaStream_t st) {
+  int ks = gemm_ksplit(a.M, a.n_exp, a.d);
+  while (ks > 1 && (size_t)ks * a.M * a.n_exp > part_elems) --ks;
+  cudaError_t e = launch_gemm_f32_partials(a.x, a.Wr, part, a.M, a.n_exp, a.d, ks, ctl, status, st);
   if (e != cudaSuccess) return e;
-  return launch_pdl(moe_route_kernel, dim3(cdiv(a.M, kRouteRows)), dim3(128), smem, st, a, status, ctl);
+  return launch_pdl(moe_topk_kernel, dim3(cdiv(a.M, kTopkRows)), dim3(kTopkRows * 32), 0, st, a,
+                    (const float*)part, ks, status, ctl);
 }
 
 // The expert-sorted permutation and the tile table, in one CTA.  A bitmap per
