@@ -188,10 +188,11 @@ struct EpiQKV {
   }
 };
 
-// LM head: l = alpha h.E / sqrt d, s = l / tau.  Per (row, 256-column tile):
-// m_t = max s (kept in log2 units), exp(s - m_t) stored as bf16 for the
-// self-conditioning pass, l_t = sum exp(s - m_t), S_t = sum exp(s - m_t)
-// (s - m_t) log2 e, and the argmax of h.E (lowest column on ties).
+// LM head: l = alpha h.E / sqrt d, s = l / tau.  Per (row, 128-column group):
+// m_g = max s (kept in log2 units), l_g = sum exp(s - m_g), S_g = sum
+// exp(s - m_g) (s - m_g) log2 e, and the argmax of h.E (lowest column on
+// ties); the tile values are stored as bf16 for the self-conditioning pass,
+// exp(s - R) for the row's reference R (kRefSpan).
 struct EpiLM {
   const float* alpha;
   float coef2;  // log2(e) / (sqrt(d) tau)
@@ -204,6 +205,8 @@ struct EpiLM {
   int excl;  // vocabulary column left out of the softmax (the [MASK] token), or -1
   const float* rowscale;  // FP8 head: per-row scale of h (else null)
   const float* colscale;  // FP8 head: per-row scale of E, i.e. per column of the tile (else null)
+  const float* ref2;      // per-row storage reference R (log2 units)
+  int* rflag;             // set for a row with a group stored against its own maximum
   // The accumulator of column col, scaled for the FP8 head.
   DG_DEV void scale_cols(float (&v)[32], int col0, int N) const {
     if (!colscale) return;
@@ -217,6 +220,7 @@ struct EpiLM {
     static_assert(BN % kStatCols == 0, "a tile holds whole statistics groups");
     const float al = (ok ? __ldg(alpha + row) : 1.0f) * (rowscale && ok ? __ldg(rowscale + row) : 1.0f);
     const float c2 = al * coef2;
+    const float R2 = ok ? __ldg(ref2 + row) : 0.f;
     const int NT = (V + kStatCols - 1) / kStatCols;
 #pragma unroll 1
     for (int g = 0; g < BN / kStatCols; ++g) {
@@ -239,6 +243,11 @@ struct EpiLM {
         }
       }
       const float m2 = vmax * c2;
+      // stored values exp2(t - R2) = p * exp2(m2 - R2), unless they would
+      // overflow (then p itself, row flagged)
+      const bool own = !(m2 - R2 <= kRefSpan);
+      const float F = own ? 1.0f : exp2f(m2 - R2);
+      if (own && ok) atomicOr(rflag + row, 1);
       float l = 0.f, S = 0.f;
 #pragma unroll 1
       for (int c = 0; c < kStatCols / 32; ++c) {
@@ -254,7 +263,7 @@ struct EpiLM {
           const float p1 = (col0 + j + 1 < N && col0 + j + 1 != excl) ? exp2f(t1) : 0.f;
           l += p0 + p1;
           S = fmaf(p0, t0, fmaf(p1, t1, S));
-          pk[j / 2] = pack_bf16(p0, p1);
+          pk[j / 2] = pack_bf16(p0 * F, p1 * F);
         }
         if (ok) {
           if (col0 + 32 <= N) {
@@ -1186,7 +1195,7 @@ cudaError_t launch_qkv(const void* a, const void* Wq, const void* Wk, const void
 cudaError_t launch_lmhead(const LmArgs& a, StopCtl ctl, int* status, cudaStream_t st) {
   CUtensorMap mA, mB, mBh;  // B boxes: half a vocabulary tile (one CTA of a pair), or half of a half tile
   EpiLM epi{a.alpha, a.coef2, a.inv_sqrt_d, reinterpret_cast<__nv_bfloat16*>(a.pt), a.pm, a.pl,
-            a.pS, a.pvmax, a.pidx, a.logits, a.M, a.V, a.excl, a.hscale, a.escale};
+            a.pS, a.pvmax, a.pidx, a.logits, a.M, a.V, a.excl, a.hscale, a.escale, a.ref2, a.rflag};
   if (a.E8) {
     // E4M3 codes: 128 one-byte elements per 128-byte row
     if (!make_tmap_2d(&mA, a.h8, (uint64_t)a.d, (uint64_t)a.M, (uint64_t)a.d, 2 * kBK, kBM, true) ||

@@ -201,7 +201,12 @@ dg_status enqueue_step(const StepCtx& c, float tau, float b, float stop_H, uint6
   lm.V = D.V;
   lm.d = D.d;
   lm.excl = mask_id;
+  lm.ref2 = at<float>(ws, L.ref2);
+  lm.rflag = at<int>(ws, L.rflag);
   DG_TRY(pf.mark(DG_PROF_LMHEAD, 0));
+  RefArgs rf{lm.h, c.model->E, c.canvas->alpha, lm.coef2, c.canvas->tokens, c.canvas->prev_argmax, step, M, D.d,
+             D.V, mask_id, at<float>(ws, L.ref2), lm.rflag};
+  DG_TRY(launch_lm_ref(rf, ctl, c.st));
   if (c.model->E8) {
     lm.h8 = at<void>(ws, L.h8);
     lm.hscale = at<float>(ws, L.hscale);
@@ -265,6 +270,8 @@ dg_status enqueue_step(const StepCtx& c, float tau, float b, float stop_H, uint6
   p0.seed = seed;
   p0.block = block;
   p0.step = step;
+  p0.ref2 = lm.ref2;
+  p0.rflag = lm.rflag;
   DG_TRY(pf.mark(DG_PROF_P0, 0));
   DG_TRY(launch_p0_gumbel(p0, ctl, c.st));
   DG_TRY(pf.mark(DG_PROF_P0, 1));
@@ -281,7 +288,7 @@ dg_status enqueue_step(const StepCtx& c, float tau, float b, float stop_H, uint6
   DG_TRY(pf.mark(DG_PROF_SELFCOND, 1));
   ReduceArgs ra{at<float>(ws, L.upart), at<float>(ws, L.gbest), at<int>(ws, L.gidx), at<uint8_t>(ws, L.acc),
                 at<void>(ws, L.u), c.canvas->tokens, status, M, D.d, D.C, D.V, sc.nsplit,
-                cdiv(D.V, kGumbelChunk)};
+                cdiv(D.V, kGumbelChunk), lm.ref2, at<float>(ws, L.rowmax), at<float>(ws, L.lsum), lm.rflag};
   DG_TRY(pf.mark(DG_PROF_REDUCE, 0));
   DG_TRY(launch_reduce(ra, ctl, c.st));
   DG_TRY(pf.mark(DG_PROF_REDUCE, 1));
@@ -401,6 +408,8 @@ bool ws_layout(const dg_dims& D, int32_t cap, WsLayout* L) {
   L->g = take(2 * M * D.F);
   L->h8 = take(M * D.d);
   L->hscale = take(4 * M);
+  L->ref2 = take(4 * M);
+  L->rflag = take(4 * M);
   if (D.n_exp > 0) {
     const size_t K = D.top_k, R = M * (K + 1);
     L->moe_max_tiles = cdiv((int64_t)R, 128) + D.n_exp + 1;

@@ -43,6 +43,7 @@ struct WsLayout {
   size_t gpart, gpart_elems;  // split-K partials of the small GEMMs
   size_t u, g;
   size_t h8, hscale;          // FP8 head: h quantized per row
+  size_t ref2, rflag;         // tile storage reference per row
   // MoE FFN (n_exp > 0): normalised input, routing, permutation, tile table,
   // gathered rows, expert hidden and gated outputs (R = rows * (top_k + 1))
   size_t moe_x, moe_idx, moe_gate, moe_slot, moe_ptok, moe_pgate, moe_tiles, moe_xp, moe_gp, moe_yp;
@@ -129,8 +130,36 @@ struct LmArgs {
   // tcgen05 kind::f8f6f4 and the epilogue applies the scales
   const void *h8, *E8;
   const float *hscale, *escale;
+  // Tile storage reference (see RefArgs): ref2 [M] in, rflag [M] set to 1 for
+  // a row with a group stored against its own maximum
+  const float* ref2;
+  int* rflag;
 };
 cudaError_t launch_lmhead(const LmArgs& a, StopCtl ctl, int* status, cudaStream_t st);
+// The stored tiles of a row are exp2(t - R) for a per-row reference R (log2
+// units of the LM head's epilogue: the scaled logit of a reference token,
+// alpha (h . E_ref) log2(e) / (sqrt(d) tau)), so the contraction reads them as
+// they are and one per-row factor exp2(R - m) / Z makes p0 of the result.  The
+// reference token is the previous step's argmax (step >= 1 with prev_argmax
+// given), else the current token, and never the excluded column, so R <= m:
+// values of a group far below R underflow only where p0 < 2^-64 relative to
+// the row's largest.  A group whose maximum lies more than kRefSpan above R
+// (its stored values would overflow) is stored against its own maximum and
+// flags the row; the p0 pass rewrites a flagged row as p0 in place.
+constexpr float kRefSpan = 64.0f;
+struct RefArgs {
+  const void* h;               // bf16 [M][d]
+  const void* E;               // bf16 [V][d]
+  const float* alpha;          // [M]
+  float coef2;                 // log2(e) / (sqrt(d) tau)
+  const int32_t* tokens;       // [M]
+  const int32_t* prev_argmax;  // [M] or null
+  int step, M, d, V;
+  int excl;                    // column left out of the softmax, or -1 (never the reference)
+  float* ref2;                 // out [M]
+  int* rflag;                  // out [M], cleared
+};
+cudaError_t launch_lm_ref(const RefArgs& a, StopCtl ctl, cudaStream_t st);
 
 // ------------------------------------------------------------ MoE FFN ----
 // Router and top-k per row of x (bf16 [M][d]): fp32 logits x . Wr_e, the
@@ -214,6 +243,8 @@ struct P0Args {
   int M, V, C;
   uint64_t seed;
   int block, step;
+  const float* ref2;     // [M] storage reference R (log2 units)
+  const int* rflag;      // [M] 1: some group stored against its own maximum
 };
 cudaError_t launch_p0_gumbel(const P0Args& a, StopCtl ctl, cudaStream_t st);
 
@@ -307,6 +338,10 @@ struct ReduceArgs {
   int* tokens;           // [M]
   int* status;           // DG_ERR_VALUE if an accepted row has no finite Gumbel score
   int M, d, C, V, nsplit, nchunks;
+  // per-row factor of the contraction: exp2(ref2 - rowmax) / lsum, or 1 for a
+  // flagged row (its tiles were rewritten as p0)
+  const float *ref2, *rowmax, *lsum;
+  const int* rflag;
 };
 cudaError_t launch_reduce(const ReduceArgs& a, StopCtl ctl, cudaStream_t st);
 cudaError_t launch_wait_timeout(int* status, cudaStream_t st);

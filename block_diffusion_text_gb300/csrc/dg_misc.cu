@@ -297,17 +297,18 @@ cudaError_t launch_stats(const StatsArgs& a, StopCtl ctl, cudaStream_t st) {
 }
 
 // ------------------------------------------- p0 and Gumbel-max sampling --
-// One pass over the stored tiles exp(s - m_t): each becomes p0 =
-// exp(s - m_t) * exp(m_t - m) / Z in place (the A operand of the
-// self-conditioning contraction), and for the accepted rows the sample
-// argmax_v (log p0_v + G_v) is searched, G_v the Gumbel noise of Philox
-// stream 0 keyed by (seed, block, step, canvas, position, v), lowest index on
-// ties (technical report summary, step 3: accepted positions take their
-// predicted token; the Gumbel-max form of that draw is this library's
-// reading).  The argmax token's p0 is exactly 1/Z (its stored value is 2^0
-// and its scale factor 1/Z), so its perturbed score S_a = log(1/Z) + G_a is
-// computed first; the largest draw is 16.64, so entries with
-// log p0 < S_a - 16.64 - 0.02 can never win and skip the draw.
+// The stored tiles of a row hold exp2(t - R) against the row's reference R
+// (kRefSpan), so p0 = stored * exp2(R - m) / Z with one factor per row, which
+// the contraction's reduce applies; a flagged row (some group stored against
+// its own maximum m_g, p0 = stored * exp2(m_g - m) / Z there) is rewritten here
+// as p0 in place.  For the accepted rows the sample argmax_v (log p0_v + G_v)
+// is searched, G_v the Gumbel noise of Philox stream 0 keyed by (seed, block,
+// step, canvas, position, v), lowest index on ties (technical report summary,
+// step 3: accepted positions take their predicted token; the Gumbel-max form
+// of that draw is this library's reading).  The argmax token's p0 is 1/Z, so
+// its perturbed score S_a = log(1/Z) + G_a is computed first; the largest
+// draw is 16.64, so entries with log p0 < S_a - 16.64 - 0.02 can never win and
+// skip the draw.  Rows that are neither flagged nor accepted are not read.
 // One CTA per (row, 8192-entry chunk).
 constexpr int kP0Threads = kGumbelChunk / 32;
 constexpr float kGumbelMaxDraw = 16.6355f;  // -log(-log(1 - 2^-24))
@@ -317,10 +318,12 @@ __global__ void __launch_bounds__(kP0Threads) p0_gumbel_kernel(P0Args a, StopCtl
   if (all_stopped(ctl.stop_at, ctl.B, ctl.step)) return;
   const int row = blockIdx.y;
   const int chunk = blockIdx.x;
-  __nv_bfloat16* pt = reinterpret_cast<__nv_bfloat16*>(a.pt) + (size_t)row * a.V;
   const bool gum = a.acc[row] && canvas_active(ctl.stop_at, row / a.C, ctl.step);
+  const bool own = a.rflag[row] != 0;
+  if (!gum && !own) return;  // uniform over the CTA
+  __nv_bfloat16* pt = reinterpret_cast<__nv_bfloat16*>(a.pt) + (size_t)row * a.V;
   const int canvas = row / a.C, pos = row % a.C;
-  const float mrow = a.rowmax[row], invZ = 1.0f / a.lsum[row];
+  const float mrow = a.rowmax[row], invZ = 1.0f / a.lsum[row], R2 = a.ref2[row];
   float best = -FLT_MAX;
   int bidx = INT_MAX;
   // Each warp takes 1024 contiguous entries (2 KB); load q of lane l is the
@@ -339,12 +342,13 @@ __global__ void __launch_bounds__(kP0Threads) p0_gumbel_kernel(P0Args a, StopCtl
       f[q] = a.pm[fbase + v / kStatCols];
     }
   }
+  // p0 factor per group: exp2(R - m) / Z, or exp2(m_g - m) / Z for a group
+  // stored against its own maximum (the LM head's test, on the same values)
 #pragma unroll
-  for (int q = 0; q < 4; ++q) f[q] = exp2f(f[q] - mrow) * invZ;  // exp(m_g - m) / Z
+  for (int q = 0; q < 4; ++q) f[q] = exp2f((f[q] - R2 <= kRefSpan ? R2 : f[q]) - mrow) * invZ;
   // p0 threshold below which no entry can win the Gumbel-max search: the
-  // argmax token's p0 is exactly 1/Z (its stored tile value is 2^0), so its
-  // perturbed score S_a is known, and an entry beats it only if
-  // log p0 + (largest draw) >= S_a.
+  // argmax token's p0 is 1/Z, so its perturbed score S_a is known, and an
+  // entry beats it only if log p0 + (largest draw) >= S_a.
   float thr = 0.f;
   if (gum) {
     const int va = a.amax[row];
@@ -353,7 +357,6 @@ __global__ void __launch_bounds__(kP0Threads) p0_gumbel_kernel(P0Args a, StopCtl
     const float sa = logf(invZ) + gumbel_from_word(wa[va & 3]);
     thr = expf(sa - kGumbelMaxDraw - 0.02f);
   }
-
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     const int vq = wbase + (q * 32 + lane) * 8;
@@ -362,12 +365,14 @@ __global__ void __launch_bounds__(kP0Threads) p0_gumbel_kernel(P0Args a, StopCtl
     float p[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e) p[e] = __bfloat162float(xb[e]) * f[q];
-    uint4 y;
-    y.x = pack_bf16(p[0], p[1]);
-    y.y = pack_bf16(p[2], p[3]);
-    y.z = pack_bf16(p[4], p[5]);
-    y.w = pack_bf16(p[6], p[7]);
-    *reinterpret_cast<uint4*>(pt + vq) = y;
+    if (own) {
+      uint4 y;
+      y.x = pack_bf16(p[0], p[1]);
+      y.y = pack_bf16(p[2], p[3]);
+      y.z = pack_bf16(p[4], p[5]);
+      y.w = pack_bf16(p[6], p[7]);
+      *reinterpret_cast<uint4*>(pt + vq) = y;
+    }
     if (!gum) continue;
 #pragma unroll
     for (int g4 = 0; g4 < 2; ++g4) {
@@ -669,6 +674,8 @@ __global__ void __launch_bounds__(256) reduce_kernel(ReduceArgs a, StopCtl ctl) 
   const int row = blockIdx.x;
   const int n4 = a.d / 4;
   const size_t sstride = (size_t)a.M * a.d;
+  // the row's p0 factor (the tiles of an unflagged row hold exp2(t - R))
+  const float fr = a.rflag[row] ? 1.0f : exp2f(a.ref2[row] - a.rowmax[row]) / a.lsum[row];
   const float* src = a.upart + (size_t)row * a.d;
   for (int c = threadIdx.x; c < n4; c += blockDim.x) {
     // four splits at a time: independent loads in flight
@@ -698,8 +705,8 @@ __global__ void __launch_bounds__(256) reduce_kernel(ReduceArgs a, StopCtl ctl) 
     const float z = (acc[0].z + acc[1].z) + (acc[2].z + acc[3].z);
     const float t = (acc[0].w + acc[1].w) + (acc[2].w + acc[3].w);
     uint2 w;
-    w.x = pack_bf16(x, y);
-    w.y = pack_bf16(z, t);
+    w.x = pack_bf16(x * fr, y * fr);
+    w.y = pack_bf16(z * fr, t * fr);
     *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(a.u) + (size_t)row * a.d + 4 * c) = w;
   }
   // sampled token of an accepted row: the best (score, lowest index) over the
@@ -847,6 +854,46 @@ cudaError_t launch_quantize_rows_e4m3(const void* X, int R, int d, uint8_t* Q, f
   if (R <= 0) return cudaSuccess;
   return launch_pdl(quant_rows_e4m3_kernel, dim3(cdiv(R, 8)), dim3(256), 0, st,
                     reinterpret_cast<const __nv_bfloat16*>(X), R, d, Q, scale);
+}
+
+// ------------------------------------------------ tile storage reference --
+// R = alpha (h . E_ref) log2(e) / (sqrt(d) tau) per row, E_ref the previous
+// step's argmax token (else the current token; never the excluded column, so
+// that R is at most the row's maximum); clears the row's flag.
+__global__ void __launch_bounds__(128) lm_ref_kernel(RefArgs a, StopCtl ctl) {
+  pdl_wait();
+  if (all_stopped(ctl.stop_at, ctl.B, ctl.step)) return;
+  const int row = blockIdx.x;
+  int tok = (a.step > 0 && a.prev_argmax) ? a.prev_argmax[row] : a.tokens[row];
+  tok = min(max(tok, 0), a.V - 1);       // a reference only: any column but the excluded one
+  if (tok == a.excl) tok = tok == 0 ? 1 : 0;
+  const uint4* h = reinterpret_cast<const uint4*>(a.h) + (size_t)row * (a.d / 8);
+  const uint4* e = reinterpret_cast<const uint4*>(a.E) + (size_t)tok * (a.d / 8);
+  float acc = 0.f;
+  for (int c = threadIdx.x; c < a.d / 8; c += blockDim.x) {
+    const uint4 hv = __ldg(h + c), ev = __ldg(e + c);
+    const __nv_bfloat162* hb = reinterpret_cast<const __nv_bfloat162*>(&hv);
+    const __nv_bfloat162* eb = reinterpret_cast<const __nv_bfloat162*>(&ev);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float2 x = __bfloat1622float2(hb[j]), y = __bfloat1622float2(eb[j]);
+      acc = fmaf(x.x, y.x, fmaf(x.y, y.y, acc));
+    }
+  }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  __shared__ float red[4];
+  if (threadIdx.x % 32 == 0) red[threadIdx.x / 32] = acc;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const float dot = (red[0] + red[1]) + (red[2] + red[3]);
+    a.ref2[row] = a.alpha[row] * a.coef2 * dot;
+    a.rflag[row] = 0;
+  }
+}
+
+cudaError_t launch_lm_ref(const RefArgs& a, StopCtl ctl, cudaStream_t st) {
+  return launch_pdl(lm_ref_kernel, dim3(a.M), dim3(128), 0, st, a, ctl);
 }
 
 }  // namespace dg

@@ -1,8 +1,9 @@
-// Mixture-of-experts FFN of a layer (the DiffusionGemma backbone's FFN:
-// "Text diffusion 2026" survey page, DiffusionGemma model section -- 128
-// experts per layer, 8 routed plus one shared; "DiffusionGemma Technical
-// Report" summary, MoE paragraph -- expert weight traffic is the bottleneck
-// of a denoising step, a canvas activating far more experts than one token).
+// Mixture-of-experts FFN of a layer (the DiffusionGemma backbone's FFN: the
+// "文本 Diffusion 模型" survey page, §11 -- 128 experts per layer, 8 routed
+// plus one shared -- and §13 -- router top-k, expert GEMM, token permutation;
+// the "DiffusionGemma Technical Report" summary, MoE paragraph -- expert
+// weight traffic is the bottleneck of a denoising step, a canvas activating
+// far more experts than one token).
 //
 // One layer's block on the rows h [M][d], x = RMSNorm(h) (bf16, computed by
 // the embedding / RMSNorm kernel):

@@ -17,9 +17,11 @@
  *          list, the attention-mask list and the data-flow pseudocode.
  *   [P4]   "从零拆开DiffusionGemma" news piece: the masked confidence decoder
  *          generate() of its fourth step (the second sampler below).
- *   [SURV] "Text diffusion 2026" survey page, DiffusionGemma sections, and the
- *          [TR] results paragraph: the throughput figures are quoted for FP8
- *          (quantized) deployment, the basis of the optional FP8 LM head.
+ *   [SURV] "文本 Diffusion 模型" survey page: §11 (DiffusionGemma: 128
+ *          experts per layer, 8 routed plus one shared; throughput quoted for
+ *          FP8) and §13 (router top-k, expert GEMM, token permutation); with
+ *          the [TR] results paragraph (FP8 on H100), the basis of the optional
+ *          FP8 LM head and MoE FFN.
  * The model is a synthetic stand-in: RMSNorm of embedding plus
  * self-conditioning, L pre-norm GQA attention layers with RoPE, a tied LM head
  * with a per-position logit sharpness alpha, and a two-matrix FFW for

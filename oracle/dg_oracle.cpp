@@ -427,10 +427,10 @@ typedef struct {
 
 // ------------------------------------------------------------------ MoE -----
 // The mixture-of-experts FFN of one layer, applied to rows h [n][d] in place
-// (the DiffusionGemma backbone's FFN: "Text diffusion 2026" survey page,
-// DiffusionGemma model section -- 128 experts per layer, 8 routed plus one
-// shared; the technical report summary's MoE paragraph -- each token activates
-// a few experts).  Per row, as a pre-norm residual block:
+// (the DiffusionGemma backbone's FFN: the "文本 Diffusion 模型" survey page,
+// §11 -- 128 experts per layer, 8 routed plus one shared -- and §13 -- router
+// top-k, expert GEMM, token permutation; the technical report summary's MoE
+// paragraph -- each token activates a few experts).  Per row, as a pre-norm residual block:
 //   x   = RMSNorm(h)                          (bf16 when mirroring)
 //   r_e = x . Wr_e                            router logit of routed expert e
 //   S   = the top_k experts by r (ties: lower index first), in rank order

@@ -779,8 +779,8 @@ def test_fp8_head_logits_are_the_quantized_product():
 
 
 # ------------------------------------------------------------------ MoE FFN ----
-# The DiffusionGemma backbone's FFN ("Text diffusion 2026" survey page, DiffusionGemma model
-# section: 128 experts per layer, 8 routed plus one shared).  The pins below fix the routing, the
+# The DiffusionGemma backbone's FFN (the "文本 Diffusion 模型" survey page, §11: 128 experts per
+# layer, 8 routed plus one shared; §13: router top-k, expert GEMM, token permutation).  The pins below fix the routing, the
 # gates, the experts' orientation and the residual against closed forms and library routines.
 MOE = synth.Dims(V=300, d=64, C=12, B=2, Hq=4, Hkv=2, hd=16, F=64, P=10, cap=40, n_exp=16, top_k=4, Fe=32)
 
