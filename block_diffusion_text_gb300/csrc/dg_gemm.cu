@@ -210,8 +210,20 @@ struct EpiLM {
   // The accumulator of column col, scaled for the FP8 head.
   DG_DEV void scale_cols(float (&v)[32], int col0, int N) const {
     if (!colscale) return;
+    if (col0 + 32 <= N) {  // 16-byte aligned (col0 is a multiple of 32)
+      const float4* s4 = reinterpret_cast<const float4*>(colscale + col0);
 #pragma unroll
-    for (int j = 0; j < 32; ++j) v[j] *= __ldg(colscale + (col0 + j < N ? col0 + j : N - 1));
+      for (int j = 0; j < 8; ++j) {
+        const float4 sc = __ldg(s4 + j);
+        v[4 * j] *= sc.x;
+        v[4 * j + 1] *= sc.y;
+        v[4 * j + 2] *= sc.z;
+        v[4 * j + 3] *= sc.w;
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v[j] *= __ldg(colscale + (col0 + j < N ? col0 + j : N - 1));
+    }
   }
   // Statistics per group of kStatCols columns, so that a tile may be 128 or
   // 256 columns wide.

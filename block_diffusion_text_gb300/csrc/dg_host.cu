@@ -66,7 +66,8 @@ dg_status check_model(const dg_model* m) {
   if (s) return s;
   if (!m->E || !m->Wq || !m->Wk || !m->Wv || !m->Wo || !m->W1 || !m->W2) return DG_ERR_ARG;
   if (!m->E8 != !m->E8_scale) return DG_ERR_ARG;  // the FP8 head needs codes and scales
-  if (reinterpret_cast<uintptr_t>(m->E8) % 16 != 0) return DG_ERR_ARG;  // TMA base
+  if (reinterpret_cast<uintptr_t>(m->E8) % 16 != 0 || reinterpret_cast<uintptr_t>(m->E8_scale) % 16 != 0)
+    return DG_ERR_ARG;  // TMA base; vector loads of the scales
   if (m->dims.n_exp > 0 && (!m->Wr || !m->We1 || !m->We2)) return DG_ERR_ARG;
   return DG_OK;
 }

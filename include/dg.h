@@ -111,7 +111,7 @@ typedef struct dg_dims {
  *   W1 [F][d], W2 [d][F]
  * Optional FP8 LM head [SURV] (both NULL = bf16 head):
  *   E8 [V][d] uint8  E4M3 codes of E, E8_scale [V] float32 its per-row scales
- *   (dg_quantize_rows_e4m3 of E; E8 16-byte aligned, and both or neither
+ *   (dg_quantize_rows_e4m3 of E; E8 and E8_scale 16-byte aligned, both or neither
  *   given, else DG_ERR_ARG).  Each step then quantizes h per row the same
  *   way and takes the logits l_v = alpha s_h s_v (q_h . q_v) / sqrt(d) on the
  *   E4M3 tensor cores (fp32 accumulation); the embedding lookup and the
