@@ -230,7 +230,7 @@ int selfcond_splits(const dg_dims& D);
 int selfcond_active_splits(const dg_dims& D);
 // The stored tiles become p0 in place, and the Gumbel-max search of the
 // accepted rows runs over vocabulary chunks in the same pass.
-constexpr int kGumbelChunk = 8192;
+constexpr int kGumbelChunk = 4096;
 struct P0Args {
   void* pt;              // bf16 [M][V]: exp(s - m_tile) in, p0 out
   const float* pm;       // [M][NT]  group maxima m_g (log2 units)
