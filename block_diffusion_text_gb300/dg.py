@@ -202,10 +202,27 @@ class Model:
             self._cache_key = key
         return self._cache_s
 
+    def workspace_for(self, cap: int):
+        """(pointer, bytes) of a workspace for a cache of `cap` rows: the model's own when that is
+        large enough, else one allocated once per capacity (a commit into a larger cache)."""
+        if cap <= self.cap:
+            return self.ws_ptr, self.ws_bytes
+        extra = getattr(self, "_ws_extra", {})
+        if cap not in extra:
+            nb = workspace_size(self.dims, cap)
+            t = torch.zeros(nb + 256, dtype=torch.uint8, device=self.K.device)
+            extra[cap] = (t, ct.c_void_p(t.data_ptr() + (-t.data_ptr()) % 256), nb)
+            self._ws_extra = extra
+        return extra[cap][1], extra[cap][2]
+
     def status(self) -> int:
-        st = ct.c_int32()
-        _check(load().dg_read_status(self.ws_ptr, ct.byref(st), _stream()), "dg_read_status")
-        return st.value
+        """The device status word (first non-zero over the model's workspaces)."""
+        for ptr in [self.ws_ptr] + [e[1] for e in getattr(self, "_ws_extra", {}).values()]:
+            st = ct.c_int32()
+            _check(load().dg_read_status(ptr, ct.byref(st), _stream()), "dg_read_status")
+            if st.value:
+                return st.value
+        return 0
 
 
 @dataclass
@@ -363,8 +380,8 @@ def commit_block(model: Model, tokens: torch.Tensor, stream=None, cache=None) ->
     else:
         K, V, n = cache
         cs = dg_kv_cache(ct.c_void_p(K.data_ptr()), ct.c_void_p(V.data_ptr()), K.shape[-2], int(n))
-    rc = load().dg_commit_block(ct.byref(model.s), ct.byref(cs), _ptr(tokens), model.ws_ptr,
-                                model.ws_bytes, _stream(stream))
+    ws, wsb = model.workspace_for(cs.cap)
+    rc = load().dg_commit_block(ct.byref(model.s), ct.byref(cs), _ptr(tokens), ws, wsb, _stream(stream))
     _check(rc, "dg_commit_block")
     if cache is None:
         model.len = cs.len
