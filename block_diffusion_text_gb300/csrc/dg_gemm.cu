@@ -34,6 +34,13 @@ DG_DEV void drain_if_aborted(volatile int* abort) {
   }
 }
 
+// 256-bit global store of w[o .. o+7] (the address 32-byte aligned).
+DG_DEV void st_global_v8(uint32_t* p, const uint32_t (&w)[16], int o) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(w[o]), "r"(w[o + 1]),
+               "r"(w[o + 2]), "r"(w[o + 3]), "r"(w[o + 4]), "r"(w[o + 5]), "r"(w[o + 6]), "r"(w[o + 7])
+               : "memory");
+}
+
 // ================================================================ epilogues
 struct EpiF32 {
   float* out;
@@ -278,7 +285,13 @@ struct EpiLM {
           pk[j / 2] = pack_bf16(p0 * F, p1 * F);
         }
         if (ok) {
-          if (col0 + 32 <= N) {
+          if (col0 + 32 <= N && V % 16 == 0) {
+            // rows 32-byte aligned: two 256-bit stores (half the L1 wavefronts of
+            // four 128-bit ones, each lane of the warp writing another row)
+            uint32_t* dst = reinterpret_cast<uint32_t*>(pt + (size_t)row * V + col0);
+            st_global_v8(dst, pk, 0);
+            st_global_v8(dst + 8, pk, 8);
+          } else if (col0 + 32 <= N) {
             uint4* dst = reinterpret_cast<uint4*>(pt + (size_t)row * V + col0);
 #pragma unroll
             for (int j = 0; j < 4; ++j)
