@@ -265,13 +265,13 @@ def reveal(Z, argmax, tokens, mask_id, step, N):
 
 
 def denoise_step_masked(dims, w, x, z, alpha, tau, mask_id, step, N, mirror_bf16=True, nthreads=None,
-                        want_extra=()):
+                        want_extra=(), fp8_head=None):
     """One step of masked confidence decoding: the forward and self-conditioning of denoise_step
     with the [MASK] token excluded from the softmax (not a prediction target), then or_reveal per
     canvas in place of the uniform-state accept / renoise."""
     out = denoise_step(dims, w, x, z, alpha, tau=tau, b=0.0, seed=0, step=0, mirror_bf16=mirror_bf16,
                        want=("H", "Z", "m", "argmax", "top2gap", "z_out", "u") + tuple(want_extra),
-                       nthreads=nthreads, exclude_tok=mask_id)
+                       nthreads=nthreads, exclude_tok=mask_id, fp8_head=fp8_head)
     B, C = dims.B, dims.C
     tok = np.asarray(x, np.int32).reshape(B, C).copy()
     rev = np.zeros((B, C), bool)
