@@ -140,8 +140,9 @@ cudaError_t launch_lmhead(const LmArgs& a, StopCtl ctl, int* status, cudaStream_
 // units of the LM head's epilogue: the scaled logit of a reference token,
 // alpha (h . E_ref) log2(e) / (sqrt(d) tau)), so the contraction reads them as
 // they are and one per-row factor exp2(R - m) / Z makes p0 of the result.  The
-// reference token is the previous step's argmax (step >= 1 with prev_argmax
-// given), else the current token, and never the excluded column, so R <= m:
+// reference is the larger of the logits of the current token and (step >= 1
+// with prev_argmax given) the previous step's argmax, never of the excluded
+// column, so R <= m:
 // values of a group far below R underflow only where p0 < 2^-64 relative to
 // the row's largest.  A group whose maximum lies more than kRefSpan above R
 // (its stored values would overflow) is stored against its own maximum and

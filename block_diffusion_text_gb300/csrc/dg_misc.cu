@@ -859,37 +859,53 @@ cudaError_t launch_quantize_rows_e4m3(const void* X, int R, int d, uint8_t* Q, f
 }
 
 // ------------------------------------------------ tile storage reference --
-// R = alpha (h . E_ref) log2(e) / (sqrt(d) tau) per row, E_ref the previous
-// step's argmax token (else the current token; never the excluded column, so
-// that R is at most the row's maximum); clears the row's flag.
+// R = alpha (h . E_ref) log2(e) / (sqrt(d) tau) per row, the larger of the
+// values for E_ref = the current token and E_ref = the previous step's argmax
+// (never the excluded column, so that R is at most the row's maximum); clears
+// the row's flag.
 __global__ void __launch_bounds__(128) lm_ref_kernel(RefArgs a, StopCtl ctl) {
   pdl_wait();
   if (all_stopped(ctl.stop_at, ctl.B, ctl.step)) return;
   const int row = blockIdx.x;
-  int tok = (a.step > 0 && a.prev_argmax) ? a.prev_argmax[row] : a.tokens[row];
-  tok = min(max(tok, 0), a.V - 1);       // a reference only: any column but the excluded one
-  if (tok == a.excl) tok = tok == 0 ? 1 : 0;
+  // candidates: the current token and (from step 1) the previous step's argmax;
+  // a reference only, so any column but the excluded one will do
+  int t0 = min(max(a.tokens[row], 0), a.V - 1);
+  int t1 = (a.step > 0 && a.prev_argmax) ? min(max(a.prev_argmax[row], 0), a.V - 1) : t0;
+  if (t0 == a.excl) t0 = t1;
+  if (t1 == a.excl) t1 = t0;
+  if (t0 == a.excl) t0 = t1 = a.excl == 0 ? 1 : 0;
   const uint4* h = reinterpret_cast<const uint4*>(a.h) + (size_t)row * (a.d / 8);
-  const uint4* e = reinterpret_cast<const uint4*>(a.E) + (size_t)tok * (a.d / 8);
-  float acc = 0.f;
+  const uint4* e0 = reinterpret_cast<const uint4*>(a.E) + (size_t)t0 * (a.d / 8);
+  const uint4* e1 = reinterpret_cast<const uint4*>(a.E) + (size_t)t1 * (a.d / 8);
+  float acc0 = 0.f, acc1 = 0.f;
   for (int c = threadIdx.x; c < a.d / 8; c += blockDim.x) {
-    const uint4 hv = __ldg(h + c), ev = __ldg(e + c);
+    const uint4 hv = __ldg(h + c), ev = __ldg(e0 + c), fv = __ldg(e1 + c);
     const __nv_bfloat162* hb = reinterpret_cast<const __nv_bfloat162*>(&hv);
     const __nv_bfloat162* eb = reinterpret_cast<const __nv_bfloat162*>(&ev);
+    const __nv_bfloat162* fb = reinterpret_cast<const __nv_bfloat162*>(&fv);
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const float2 x = __bfloat1622float2(hb[j]), y = __bfloat1622float2(eb[j]);
-      acc = fmaf(x.x, y.x, fmaf(x.y, y.y, acc));
+      const float2 x = __bfloat1622float2(hb[j]), y = __bfloat1622float2(eb[j]), z = __bfloat1622float2(fb[j]);
+      acc0 = fmaf(x.x, y.x, fmaf(x.y, y.y, acc0));
+      acc1 = fmaf(x.x, z.x, fmaf(x.y, z.y, acc1));
     }
   }
 #pragma unroll
-  for (int o = 16; o; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-  __shared__ float red[4];
-  if (threadIdx.x % 32 == 0) red[threadIdx.x / 32] = acc;
+  for (int o = 16; o; o >>= 1) {
+    acc0 += __shfl_xor_sync(0xffffffffu, acc0, o);
+    acc1 += __shfl_xor_sync(0xffffffffu, acc1, o);
+  }
+  __shared__ float red[2][4];
+  if (threadIdx.x % 32 == 0) {
+    red[0][threadIdx.x / 32] = acc0;
+    red[1][threadIdx.x / 32] = acc1;
+  }
   __syncthreads();
   if (threadIdx.x == 0) {
-    const float dot = (red[0] + red[1]) + (red[2] + red[3]);
-    a.ref2[row] = a.alpha[row] * a.coef2 * dot;
+    const float c = a.alpha[row] * a.coef2;
+    const float r0 = c * ((red[0][0] + red[0][1]) + (red[0][2] + red[0][3]));
+    const float r1 = c * ((red[1][0] + red[1][1]) + (red[1][2] + red[1][3]));
+    a.ref2[row] = fmaxf(r0, r1);  // the larger of two logits: still at most the row's maximum
     a.rflag[row] = 0;
   }
 }
