@@ -494,6 +494,13 @@ DG_DEV float gumbel_from_word(uint64_t w) {
 }
 
 // Canvas b is still denoising at `step` unless its stop test fired earlier.
+// Order-preserving unsigned key of a float (unsigned order = numeric order;
+// 0 is below every finite value) and its inverse.
+DG_DEV unsigned float_key(float f) {
+  const unsigned b = __float_as_uint(f);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+DG_DEV float key_float(unsigned k) { return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k); }
 DG_DEV bool canvas_active(const int* stop_at, int b, int step) {
   return stop_at == nullptr || stop_at[b] >= step;
 }

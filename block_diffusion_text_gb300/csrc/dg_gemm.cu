@@ -213,7 +213,7 @@ struct EpiLM {
   const float* rowscale;  // FP8 head: per-row scale of h (else null)
   const float* colscale;  // FP8 head: per-row scale of E, i.e. per column of the tile (else null)
   const float* ref2;      // per-row storage reference R (log2 units)
-  int* rflag;             // set for a row with a group stored against its own maximum
+  unsigned* rkey;         // raised to the key of a group maximum stored against itself
   // The accumulator of column col, scaled for the FP8 head.
   DG_DEV void scale_cols(float (&v)[32], int col0, int N) const {
     if (!colscale) return;
@@ -266,7 +266,7 @@ struct EpiLM {
       // overflow (then p itself, row flagged)
       const bool own = !(m2 - R2 <= kRefSpan);
       const float F = own ? 1.0f : exp2f(m2 - R2);
-      if (own && ok) atomicOr(rflag + row, 1);
+      if (own && ok) atomicMax(rkey + row, float_key(m2));
       float l = 0.f, S = 0.f;
 #pragma unroll 1
       for (int c = 0; c < kStatCols / 32; ++c) {
@@ -1220,7 +1220,7 @@ cudaError_t launch_qkv(const void* a, const void* Wq, const void* Wk, const void
 cudaError_t launch_lmhead(const LmArgs& a, StopCtl ctl, int* status, cudaStream_t st) {
   CUtensorMap mA, mB, mBh;  // B boxes: half a vocabulary tile (one CTA of a pair), or half of a half tile
   EpiLM epi{a.alpha, a.coef2, a.inv_sqrt_d, reinterpret_cast<__nv_bfloat16*>(a.pt), a.pm, a.pl,
-            a.pS, a.pvmax, a.pidx, a.logits, a.M, a.V, a.excl, a.hscale, a.escale, a.ref2, a.rflag};
+            a.pS, a.pvmax, a.pidx, a.logits, a.M, a.V, a.excl, a.hscale, a.escale, a.ref2, a.rkey};
   if (a.E8) {
     // E4M3 codes: 128 one-byte elements per 128-byte row
     if (!make_tmap_2d(&mA, a.h8, (uint64_t)a.d, (uint64_t)a.M, (uint64_t)a.d, 2 * kBK, kBM, true) ||

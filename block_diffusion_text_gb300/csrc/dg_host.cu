@@ -4,6 +4,7 @@
 #include <climits>
 #include <cmath>
 #include <cstring>
+#include <mutex>
 
 #include "dg_internal.h"
 
@@ -127,6 +128,41 @@ dg_status enqueue_moe(const dg_model* m, int l, void* ws, const WsLayout& L, int
   return DG_OK;
 }
 
+// A second stream per device for the work of a step that may overlap the
+// self-conditioning contraction (statistics, sampler, Gumbel search): forked
+// from and joined back into the caller's stream with two events, so a step
+// stays one unit of work on the caller's stream (and one fork/join in a
+// captured graph).  Created once, outside stream capture; the mutex keeps the
+// record/wait pairs of concurrent callers apart.
+struct SideStream {
+  cudaStream_t s = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+std::mutex g_side_mu;
+SideStream g_side[64];
+
+// The device's side stream, or null (no overlap) when it cannot be created
+// now: the first call on a device made under stream capture.
+SideStream* side_stream(cudaStream_t st) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  SideStream& sd = g_side[dev];
+  if (sd.s) return &sd;
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(st, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone) return nullptr;
+  if (cudaStreamCreateWithFlags(&sd.s, cudaStreamNonBlocking) != cudaSuccess) {
+    sd.s = nullptr;
+    return nullptr;
+  }
+  if (cudaEventCreateWithFlags(&sd.fork, cudaEventDisableTiming) != cudaSuccess ||
+      cudaEventCreateWithFlags(&sd.join, cudaEventDisableTiming) != cudaSuccess) {
+    cudaStreamDestroy(sd.s);
+    sd.s = nullptr;
+    return nullptr;
+  }
+  return &sd;
+}
+
 // All kernels of one denoising step, in order, on ctx.st.
 // fill_rope: (re)compute the RoPE table of positions P + i; a canvas loop
 // fills it at its first step only (P is fixed for the loop).
@@ -203,10 +239,11 @@ dg_status enqueue_step(const StepCtx& c, float tau, float b, float stop_H, uint6
   lm.d = D.d;
   lm.excl = mask_id;
   lm.ref2 = at<float>(ws, L.ref2);
-  lm.rflag = at<int>(ws, L.rflag);
+  lm.rkey = at<unsigned>(ws, L.rkey);
+  float* ref2f = at<float>(ws, L.ref2f);
   DG_TRY(pf.mark(DG_PROF_LMHEAD, 0));
   RefArgs rf{lm.h, c.model->E, c.canvas->alpha, lm.coef2, c.canvas->tokens, c.canvas->prev_argmax, step, M, D.d,
-             D.V, mask_id, at<float>(ws, L.ref2), lm.rflag};
+             D.V, mask_id, at<float>(ws, L.ref2), ref2f, lm.rkey};
   DG_TRY(launch_lm_ref(rf, ctl, c.st));
   if (c.model->E8) {
     lm.h8 = at<void>(ws, L.h8);
@@ -216,14 +253,28 @@ dg_status enqueue_step(const StepCtx& c, float tau, float b, float stop_H, uint6
     DG_TRY(launch_quantize_rows_e4m3(lm.h, M, D.d, at<uint8_t>(ws, L.h8), at<float>(ws, L.hscale), c.st));
   }
   DG_TRY(launch_lmhead(lm, ctl, status, c.st));
+  FixArgs fx{at<void>(ws, L.pt), at<float>(ws, L.pm), lm.ref2, lm.rkey, ref2f, M, D.V};
+  DG_TRY(launch_lm_fix(fx, ctl, c.st));
   DG_TRY(pf.mark(DG_PROF_LMHEAD, 1));
+  // fork: statistics, sampler and Gumbel search on the side stream, the
+  // contraction (which reads only the tiles) on the caller's stream
+  SideStream* sd = side_stream(c.st);
+  std::unique_lock<std::mutex> side_lock(g_side_mu, std::defer_lock);
+  cudaStream_t sst = c.st;
+  if (sd) {
+    side_lock.lock();
+    DG_TRY(cudaEventRecord(sd->fork, c.st));
+    DG_TRY(cudaStreamWaitEvent(sd->s, sd->fork, 0));
+    sst = sd->s;
+  }
+  const Prof ps{pf.ev, sst};
   StatsArgs sa{at<float>(ws, L.pm), at<float>(ws, L.pl), at<float>(ws, L.pS), at<float>(ws, L.pvmax),
                at<int>(ws, L.pidx), NT, M, at<double>(ws, L.Hd), at<float>(ws, L.lsum),
                at<float>(ws, L.rowmax), at<int>(ws, L.amax), out ? out->entropy : nullptr,
                out ? out->argmax : nullptr};
-  DG_TRY(pf.mark(DG_PROF_STATS, 0));
-  DG_TRY(launch_stats(sa, ctl, c.st));
-  DG_TRY(pf.mark(DG_PROF_STATS, 1));
+  DG_TRY(ps.mark(DG_PROF_STATS, 0));
+  DG_TRY(launch_stats(sa, ctl, sst));
+  DG_TRY(ps.mark(DG_PROF_STATS, 1));
   SamplerArgs sp{};
   sp.Hd = at<double>(ws, L.Hd);
   sp.amax = at<int>(ws, L.amax);
@@ -246,16 +297,16 @@ dg_status enqueue_step(const StepCtx& c, float tau, float b, float stop_H, uint6
   sp.step = step;
   sp.accepted_log = accepted_log;
   sp.N = N;
-  DG_TRY(pf.mark(DG_PROF_SAMPLER, 0));
+  DG_TRY(ps.mark(DG_PROF_SAMPLER, 0));
   if (mask_id < 0) {
-    DG_TRY(launch_sampler(sp, c.st));
+    DG_TRY(launch_sampler(sp, sst));
   } else {
     RevealArgs rv{at<double>(ws, L.Hd), at<float>(ws, L.lsum), at<int>(ws, L.amax), c.canvas->prev_argmax,
                   c.canvas->tokens, at<uint8_t>(ws, L.acc), sp.acc_out, sp.n_acc, sp.mean_H, sp.stop,
                   accepted_log, D.B, D.C, mask_id, step, N};
-    DG_TRY(launch_reveal(rv, c.st));
+    DG_TRY(launch_reveal(rv, sst));
   }
-  DG_TRY(pf.mark(DG_PROF_SAMPLER, 1));
+  DG_TRY(ps.mark(DG_PROF_SAMPLER, 1));
   P0Args p0{};
   p0.pt = at<void>(ws, L.pt);
   p0.pm = at<float>(ws, L.pm);
@@ -271,11 +322,10 @@ dg_status enqueue_step(const StepCtx& c, float tau, float b, float stop_H, uint6
   p0.seed = seed;
   p0.block = block;
   p0.step = step;
-  p0.ref2 = lm.ref2;
-  p0.rflag = lm.rflag;
-  DG_TRY(pf.mark(DG_PROF_P0, 0));
-  DG_TRY(launch_p0_gumbel(p0, ctl, c.st));
-  DG_TRY(pf.mark(DG_PROF_P0, 1));
+  p0.ref2f = ref2f;
+  DG_TRY(ps.mark(DG_PROF_P0, 0));
+  DG_TRY(launch_p0_gumbel(p0, ctl, sst));
+  DG_TRY(ps.mark(DG_PROF_P0, 1));
   ScArgs sc{};
   sc.pt = at<void>(ws, L.pt);
   sc.E = c.model->E;
@@ -287,9 +337,14 @@ dg_status enqueue_step(const StepCtx& c, float tau, float b, float stop_H, uint6
   DG_TRY(pf.mark(DG_PROF_SELFCOND, 0));
   DG_TRY(launch_selfcond(sc, ctl, status, c.st));
   DG_TRY(pf.mark(DG_PROF_SELFCOND, 1));
+  if (sd) {  // join
+    DG_TRY(cudaEventRecord(sd->join, sd->s));
+    DG_TRY(cudaStreamWaitEvent(c.st, sd->join, 0));
+    side_lock.unlock();
+  }
   ReduceArgs ra{at<float>(ws, L.upart), at<float>(ws, L.gbest), at<int>(ws, L.gidx), at<uint8_t>(ws, L.acc),
                 at<void>(ws, L.u), c.canvas->tokens, status, M, D.d, D.C, D.V, sc.nsplit,
-                cdiv(D.V, kGumbelChunk), lm.ref2, at<float>(ws, L.rowmax), at<float>(ws, L.lsum), lm.rflag};
+                cdiv(D.V, kGumbelChunk), ref2f, at<float>(ws, L.rowmax), at<float>(ws, L.lsum)};
   DG_TRY(pf.mark(DG_PROF_REDUCE, 0));
   DG_TRY(launch_reduce(ra, ctl, c.st));
   DG_TRY(pf.mark(DG_PROF_REDUCE, 1));
@@ -410,7 +465,8 @@ bool ws_layout(const dg_dims& D, int32_t cap, WsLayout* L) {
   L->h8 = take(M * D.d);
   L->hscale = take(4 * M);
   L->ref2 = take(4 * M);
-  L->rflag = take(4 * M);
+  L->ref2f = take(4 * M);
+  L->rkey = take(4 * M);
   if (D.n_exp > 0) {
     const size_t K = D.top_k, R = M * (K + 1);
     L->moe_max_tiles = cdiv((int64_t)R, 128) + D.n_exp + 1;

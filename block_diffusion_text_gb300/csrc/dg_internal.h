@@ -43,7 +43,7 @@ struct WsLayout {
   size_t gpart, gpart_elems;  // split-K partials of the small GEMMs
   size_t u, g;
   size_t h8, hscale;          // FP8 head: h quantized per row
-  size_t ref2, rflag;         // tile storage reference per row
+  size_t ref2, ref2f, rkey;   // tile storage reference per row
   // MoE FFN (n_exp > 0): normalised input, routing, permutation, tile table,
   // gathered rows, expert hidden and gated outputs (R = rows * (top_k + 1))
   size_t moe_x, moe_idx, moe_gate, moe_slot, moe_ptok, moe_pgate, moe_tiles, moe_xp, moe_gp, moe_yp;
@@ -130,10 +130,12 @@ struct LmArgs {
   // tcgen05 kind::f8f6f4 and the epilogue applies the scales
   const void *h8, *E8;
   const float *hscale, *escale;
-  // Tile storage reference (see RefArgs): ref2 [M] in, rflag [M] set to 1 for
-  // a row with a group stored against its own maximum
+  // Tile storage reference (see RefArgs): ref2 [M] in; rkey [M] raised (an
+  // order-preserving key of the group's maximum) for every group stored
+  // against its own maximum, so that a row with rkey != 0 is flagged and
+  // rkey holds its maximum
   const float* ref2;
-  int* rflag;
+  unsigned* rkey;
 };
 cudaError_t launch_lmhead(const LmArgs& a, StopCtl ctl, int* status, cudaStream_t st);
 // The stored tiles of a row are exp2(t - R) for a per-row reference R (log2
@@ -146,7 +148,10 @@ cudaError_t launch_lmhead(const LmArgs& a, StopCtl ctl, int* status, cudaStream_
 // values of a group far below R underflow only where p0 < 2^-64 relative to
 // the row's largest.  A group whose maximum lies more than kRefSpan above R
 // (its stored values would overflow) is stored against its own maximum and
-// flags the row; the p0 pass rewrites a flagged row as p0 in place.
+// flags the row; right after the LM head, lm_fix rewrites a flagged row
+// against the row's maximum R' (the largest such group maximum), which
+// becomes the row's final reference ref2f.  From there on every row's tiles
+// hold exp2(t - ref2f) and p0 = tile * exp2(ref2f - m) / Z.
 constexpr float kRefSpan = 64.0f;
 struct RefArgs {
   const void* h;               // bf16 [M][d]
@@ -158,9 +163,20 @@ struct RefArgs {
   int step, M, d, V;
   int excl;                    // column left out of the softmax, or -1 (never the reference)
   float* ref2;                 // out [M]
-  int* rflag;                  // out [M], cleared
+  float* ref2f;                // out [M], = ref2 (lm_fix updates flagged rows)
+  unsigned* rkey;              // out [M], cleared
 };
 cudaError_t launch_lm_ref(const RefArgs& a, StopCtl ctl, cudaStream_t st);
+// Rewrite of the flagged rows' tiles against their maximum (see kRefSpan).
+struct FixArgs {
+  void* pt;                    // bf16 [M][V] tiles
+  const float* pm;             // [M][NT] group maxima (log2 units)
+  const float* ref2;           // [M] the LM head's reference
+  const unsigned* rkey;        // [M] 0, or the key of the row's maximum
+  float* ref2f;                // [M] final reference (flagged rows: their maximum)
+  int M, V;
+};
+cudaError_t launch_lm_fix(const FixArgs& a, StopCtl ctl, cudaStream_t st);
 
 // ------------------------------------------------------------ MoE FFN ----
 // Router and top-k per row of x (bf16 [M][d]): fp32 logits x . Wr_e, the
@@ -233,7 +249,7 @@ int selfcond_active_splits(const dg_dims& D);
 // accepted rows runs over vocabulary chunks in the same pass.
 constexpr int kGumbelChunk = 4096;
 struct P0Args {
-  void* pt;              // bf16 [M][V]: exp(s - m_tile) in, p0 out
+  const void* pt;        // bf16 [M][V]: the tiles, exp2(t - ref2f)
   const float* pm;       // [M][NT]  group maxima m_g (log2 units)
   const float* rowmax;   // [M]  row maximum m (log2 units)
   const float* lsum;     // [M]  Z
@@ -244,8 +260,7 @@ struct P0Args {
   int M, V, C;
   uint64_t seed;
   int block, step;
-  const float* ref2;     // [M] storage reference R (log2 units)
-  const int* rflag;      // [M] 1: some group stored against its own maximum
+  const float* ref2f;    // [M] final storage reference of the tiles (log2 units)
 };
 cudaError_t launch_p0_gumbel(const P0Args& a, StopCtl ctl, cudaStream_t st);
 
@@ -339,10 +354,8 @@ struct ReduceArgs {
   int* tokens;           // [M]
   int* status;           // DG_ERR_VALUE if an accepted row has no finite Gumbel score
   int M, d, C, V, nsplit, nchunks;
-  // per-row factor of the contraction: exp2(ref2 - rowmax) / lsum, or 1 for a
-  // flagged row (its tiles were rewritten as p0)
-  const float *ref2, *rowmax, *lsum;
-  const int* rflag;
+  // per-row factor of the contraction: exp2(ref2f - rowmax) / lsum
+  const float *ref2f, *rowmax, *lsum;
 };
 cudaError_t launch_reduce(const ReduceArgs& a, StopCtl ctl, cudaStream_t st);
 cudaError_t launch_wait_timeout(int* status, cudaStream_t st);

@@ -297,21 +297,20 @@ cudaError_t launch_stats(const StatsArgs& a, StopCtl ctl, cudaStream_t st) {
 }
 
 // ------------------------------------------- p0 and Gumbel-max sampling --
-// The stored tiles of a row hold exp2(t - R) against the row's reference R
-// (kRefSpan), so p0 = stored * exp2(R - m) / Z with one factor per row, which
-// the contraction's reduce applies; a flagged row (some group stored against
-// its own maximum m_g, p0 = stored * exp2(m_g - m) / Z there) is rewritten here
-// as p0 in place.  For the accepted rows the sample argmax_v (log p0_v + G_v)
-// is searched, G_v the Gumbel noise of Philox stream 0 keyed by (seed, block,
-// step, canvas, position, v), lowest index on ties (technical report summary,
-// step 3: accepted positions take their predicted token; the Gumbel-max form
-// of that draw is this library's reading).  The argmax token's p0 is 1/Z, so
-// its perturbed score S_a = log(1/Z) + G_a is computed first; the largest
-// draw is 16.64, so entries with log p0 < S_a - 16.64 - 0.02 can never win and
-// skip the draw.  Rows that are neither flagged nor accepted are not read.
-// One CTA per (row, 4096-entry chunk): a smaller grid of larger chunks measured
-// slower (16384: +2 us; the CTAs of rows that are neither accepted nor flagged
-// exit at once, and the others finish sooner).
+// The stored tiles of a row hold exp2(t - R) against the row's final reference
+// R (kRefSpan; flagged rows were rewritten by lm_fix), so p0 = tile *
+// exp2(R - m) / Z with one factor per row, which the contraction's reduce
+// applies.  This pass searches, for the accepted rows only, the sample
+// argmax_v (log p0_v + G_v), G_v the Gumbel noise of Philox stream 0 keyed by
+// (seed, block, step, canvas, position, v), lowest index on ties (technical
+// report summary, step 3: accepted positions take their predicted token; the
+// Gumbel-max form of that draw is this library's reading).  The argmax token's
+// p0 is 1/Z, so its perturbed score S_a = log(1/Z) + G_a is computed first; the
+// largest draw is 16.64, so entries with log p0 < S_a - 16.64 - 0.02 can never
+// win and skip the draw.  Rows that are not accepted are not read.
+// One CTA per (row, 4096-entry chunk): larger chunks measured slower (16384:
+// +2 us; 32768 with 16 loads in flight per thread: +22 us): the search wants
+// many CTAs.
 constexpr int kP0Threads = kGumbelChunk / 32;
 constexpr float kGumbelMaxDraw = 16.6355f;  // -log(-log(1 - 2^-24))
 
@@ -321,11 +320,11 @@ __global__ void __launch_bounds__(kP0Threads) p0_gumbel_kernel(P0Args a, StopCtl
   const int row = blockIdx.y;
   const int chunk = blockIdx.x;
   const bool gum = a.acc[row] && canvas_active(ctl.stop_at, row / a.C, ctl.step);
-  const bool own = a.rflag[row] != 0;
-  if (!gum && !own) return;  // uniform over the CTA
-  __nv_bfloat16* pt = reinterpret_cast<__nv_bfloat16*>(a.pt) + (size_t)row * a.V;
+  if (!gum) return;  // uniform over the CTA
+  const __nv_bfloat16* pt = reinterpret_cast<const __nv_bfloat16*>(a.pt) + (size_t)row * a.V;
   const int canvas = row / a.C, pos = row % a.C;
-  const float mrow = a.rowmax[row], invZ = 1.0f / a.lsum[row], R2 = a.ref2[row];
+  const float mrow = a.rowmax[row], invZ = 1.0f / a.lsum[row];
+  const float f = exp2f(a.ref2f[row] - mrow) * invZ;  // p0 = tile * f
   float best = -FLT_MAX;
   int bidx = INT_MAX;
   // Each warp takes 1024 contiguous entries (2 KB); load q of lane l is the
@@ -333,21 +332,12 @@ __global__ void __launch_bounds__(kP0Threads) p0_gumbel_kernel(P0Args a, StopCtl
   // (two statistics groups of 128 columns, one scale factor each).
   const int wbase = chunk * kGumbelChunk + (threadIdx.x / 32) * 1024;
   const int lane = threadIdx.x % 32;
-  const size_t fbase = (size_t)row * ((a.V + kStatCols - 1) / kStatCols);
   uint4 x[4];
-  float f[4];
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     const int v = wbase + (q * 32 + lane) * 8;
-    if (v < a.V) {  // V is a multiple of 8
-      x[q] = *reinterpret_cast<const uint4*>(pt + v);
-      f[q] = a.pm[fbase + v / kStatCols];
-    }
+    if (v < a.V) x[q] = *reinterpret_cast<const uint4*>(pt + v);  // V is a multiple of 8
   }
-  // p0 factor per group: exp2(R - m) / Z, or exp2(m_g - m) / Z for a group
-  // stored against its own maximum (the LM head's test, on the same values)
-#pragma unroll
-  for (int q = 0; q < 4; ++q) f[q] = exp2f((f[q] - R2 <= kRefSpan ? R2 : f[q]) - mrow) * invZ;
   // p0 threshold below which no entry can win the Gumbel-max search: the
   // argmax token's p0 is 1/Z, so its perturbed score S_a is known, and an
   // entry beats it only if log p0 + (largest draw) >= S_a.
@@ -366,16 +356,7 @@ __global__ void __launch_bounds__(kP0Threads) p0_gumbel_kernel(P0Args a, StopCtl
     const __nv_bfloat16* xb = reinterpret_cast<const __nv_bfloat16*>(&x[q]);
     float p[8];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) p[e] = __bfloat162float(xb[e]) * f[q];
-    if (own) {
-      uint4 y;
-      y.x = pack_bf16(p[0], p[1]);
-      y.y = pack_bf16(p[2], p[3]);
-      y.z = pack_bf16(p[4], p[5]);
-      y.w = pack_bf16(p[6], p[7]);
-      *reinterpret_cast<uint4*>(pt + vq) = y;
-    }
-    if (!gum) continue;
+    for (int e = 0; e < 8; ++e) p[e] = __bfloat162float(xb[e]) * f;
 #pragma unroll
     for (int g4 = 0; g4 < 2; ++g4) {
       bool any = false;
@@ -397,7 +378,6 @@ __global__ void __launch_bounds__(kP0Threads) p0_gumbel_kernel(P0Args a, StopCtl
       }
     }
   }
-  if (!gum) return;  // uniform over the CTA
   // (score, lowest index) over the block
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
@@ -676,8 +656,8 @@ __global__ void __launch_bounds__(256) reduce_kernel(ReduceArgs a, StopCtl ctl) 
   const int row = blockIdx.x;
   const int n4 = a.d / 4;
   const size_t sstride = (size_t)a.M * a.d;
-  // the row's p0 factor (the tiles of an unflagged row hold exp2(t - R))
-  const float fr = a.rflag[row] ? 1.0f : exp2f(a.ref2[row] - a.rowmax[row]) / a.lsum[row];
+  // the row's p0 factor (its tiles hold exp2(t - ref2f))
+  const float fr = exp2f(a.ref2f[row] - a.rowmax[row]) / a.lsum[row];
   const float* src = a.upart + (size_t)row * a.d;
   for (int c = threadIdx.x; c < n4; c += blockDim.x) {
     // four splits at a time: independent loads in flight
@@ -905,13 +885,55 @@ __global__ void __launch_bounds__(128) lm_ref_kernel(RefArgs a, StopCtl ctl) {
     const float c = a.alpha[row] * a.coef2;
     const float r0 = c * ((red[0][0] + red[0][1]) + (red[0][2] + red[0][3]));
     const float r1 = c * ((red[1][0] + red[1][1]) + (red[1][2] + red[1][3]));
-    a.ref2[row] = fmaxf(r0, r1);  // the larger of two logits: still at most the row's maximum
-    a.rflag[row] = 0;
+    const float R = fmaxf(r0, r1);  // the larger of two logits: still at most the row's maximum
+    a.ref2[row] = R;
+    a.ref2f[row] = R;
+    a.rkey[row] = 0u;
   }
 }
 
 cudaError_t launch_lm_ref(const RefArgs& a, StopCtl ctl, cudaStream_t st) {
   return launch_pdl(lm_ref_kernel, dim3(a.M), dim3(128), 0, st, a, ctl);
+}
+
+// ------------------------------------------------ flagged-row rewrite --
+// A flagged row (some group stored against its own maximum, kRefSpan) is
+// rewritten against the row's maximum R' (the largest of those group maxima,
+// rkey): a group stored against R scales by exp2(R - R') (< 2^-64: its
+// values were negligible), one stored against its own maximum m_g by
+// exp2(m_g - R'); R' becomes the row's final reference.  Needs only the group
+// maxima, so it runs right after the LM head.  kFixSplit CTAs per row, each
+// reading the row's flag once; those of unflagged rows return at once.
+constexpr int kFixSplit = 4;
+constexpr int kFixThreads = 256;
+__global__ void __launch_bounds__(kFixThreads) lm_fix_kernel(FixArgs a, StopCtl ctl) {
+  pdl_wait();
+  if (all_stopped(ctl.stop_at, ctl.B, ctl.step)) return;
+  const int row = blockIdx.y;
+  const unsigned key = a.rkey[row];
+  if (key == 0u) return;  // uniform over the CTA
+  const float R = a.ref2[row], Rn = key_float(key);
+  if (blockIdx.x == 0 && threadIdx.x == 0) a.ref2f[row] = Rn;
+  const int NT = (a.V + kStatCols - 1) / kStatCols;
+  const int per = ((a.V + kFixSplit - 1) / kFixSplit + 7) / 8 * 8;  // entries of this CTA, a multiple of 8
+  const int v0 = blockIdx.x * per, v1 = min(a.V, v0 + per);
+  __nv_bfloat16* pt = reinterpret_cast<__nv_bfloat16*>(a.pt) + (size_t)row * a.V;
+  for (int v = v0 + threadIdx.x * 8; v < v1; v += kFixThreads * 8) {  // V is a multiple of 8
+    const float mg = a.pm[(size_t)row * NT + v / kStatCols];
+    const float f = exp2f((mg - R <= kRefSpan ? R : mg) - Rn);
+    uint4 x = *reinterpret_cast<const uint4*>(pt + v);
+    const __nv_bfloat16* xb = reinterpret_cast<const __nv_bfloat16*>(&x);
+    uint4 y;
+    y.x = pack_bf16(__bfloat162float(xb[0]) * f, __bfloat162float(xb[1]) * f);
+    y.y = pack_bf16(__bfloat162float(xb[2]) * f, __bfloat162float(xb[3]) * f);
+    y.z = pack_bf16(__bfloat162float(xb[4]) * f, __bfloat162float(xb[5]) * f);
+    y.w = pack_bf16(__bfloat162float(xb[6]) * f, __bfloat162float(xb[7]) * f);
+    *reinterpret_cast<uint4*>(pt + v) = y;
+  }
+}
+
+cudaError_t launch_lm_fix(const FixArgs& a, StopCtl ctl, cudaStream_t st) {
+  return launch_pdl(lm_fix_kernel, dim3(kFixSplit, a.M), dim3(kFixThreads), 0, st, a, ctl);
 }
 
 }  // namespace dg
