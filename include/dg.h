@@ -35,6 +35,12 @@
  *    contiguous), so y = x W^T.
  *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  Every
  *    call only enqueues work on `stream` and returns; the exceptions are said.
+ *    A denoising step also runs part of its work (statistics, sampler, Gumbel
+ *    search) on a library-owned stream of the device, forked from `stream` by
+ *    an event and joined back into it within the step, so the step's work is
+ *    done when `stream`'s is; under stream capture the fork and join are
+ *    captured too.  The library creates that stream and two events once per
+ *    device, at the first step not under capture.
  *  - Arguments are validated before anything is enqueued: on any error code no
  *    device memory has been written.
  *  - The workspace `ws` (size from dg_workspace_size, 256-byte aligned) holds
