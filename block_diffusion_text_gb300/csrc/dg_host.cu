@@ -138,7 +138,8 @@ struct SideStream {
   cudaStream_t s = nullptr;
   cudaEvent_t fork = nullptr, join = nullptr;
 };
-std::mutex g_side_mu;
+std::mutex g_side_mu;       // held from a step's fork record to its join wait
+std::mutex g_side_make_mu;  // creation of the side streams
 SideStream g_side[64];
 
 // The device's side stream, or null (no overlap) when it cannot be created
@@ -147,6 +148,7 @@ SideStream* side_stream(cudaStream_t st) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
   SideStream& sd = g_side[dev];
+  std::lock_guard<std::mutex> lock(g_side_make_mu);
   if (sd.s) return &sd;
   cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
   if (cudaStreamIsCapturing(st, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone) return nullptr;
