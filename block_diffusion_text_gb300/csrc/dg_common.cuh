@@ -51,28 +51,41 @@ DG_DEV void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
 DG_DEV void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
+// kCluster: acquire at cluster scope, for phases completed by arrivals from
+// other CTAs of the cluster that release their remote shared-memory stores.
+template <bool kCluster = false>
 DG_DEV bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-      " selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
+  if (kCluster) {
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+  }
   return ok != 0;
 }
 // Bounded wait for the phase with the given parity.  Returns false (after
 // recording the timeout in *status and raising *abort) if the wait ran out or
 // another role of the CTA already gave up.
+template <bool kCluster = false>
 DG_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, int* status, volatile int* abort) {
 #pragma unroll 1
   for (int i = 0; i < 256; ++i)
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait<kCluster>(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   while (true) {
 #pragma unroll 1
     for (int i = 0; i < 64; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
+      if (mbar_try_wait<kCluster>(bar, parity)) return true;
     if (*abort) return false;
     if (globaltimer() - t0 > kWaitLimitNs) {
       atomicExch(status, kStatusTimeout);
@@ -85,8 +98,9 @@ DG_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, int* status, volatile int*
 // The same wait taken by a whole warp that goes on to warp-collective
 // tcgen05 loads / stores: every lane gets the same answer, so the warp never
 // splits between a lane that gave up and one that carries on.
+template <bool kCluster = false>
 DG_DEV bool mbar_wait_warp(uint64_t* bar, uint32_t parity, int* status, volatile int* abort) {
-  return __all_sync(0xffffffffu, mbar_wait(bar, parity, status, abort));
+  return __all_sync(0xffffffffu, mbar_wait<kCluster>(bar, parity, status, abort));
 }
 
 // ------------------------------------------------------------------ TMA ----
@@ -320,6 +334,17 @@ DG_DEV uint32_t cluster_addr(const void* p, uint32_t rank) {
 // release would add a memory barrier to every call).
 DG_DEV void mbar_arrive_cluster(uint32_t caddr) {
   asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(caddr) : "memory");
+}
+// Store of four floats into the shared memory of a CTA of the cluster
+// (cluster address), and an arrival on an mbarrier there that releases this
+// thread's earlier stores at cluster scope (the waiter acquires them with
+// mbar_wait<true>).
+DG_DEV void st_cluster_v4(uint32_t caddr, float a, float b, float c, float d) {
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(caddr), "f"(a), "f"(b), "f"(c), "f"(d)
+               : "memory");
+}
+DG_DEV void mbar_arrive_cluster_release(uint32_t caddr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(caddr) : "memory");
 }
 // 2-D tiled copy into this CTA's shared memory whose completion is counted on
 // an mbarrier of either CTA of the pair (cluster address).

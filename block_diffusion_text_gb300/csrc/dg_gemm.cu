@@ -6,6 +6,9 @@
 //     double-buffered TMEM accumulator.  Epilogues: fp32 store (diagnostics),
 //     bf16 store with residual / GELU (output projection, FFW), RoPE
 //     projections (q, k, v), and the LM head statistics epilogue.
+//   * gemm_ksum_kernel: the same engine split over K across a cluster of 2 or
+//     4 CTAs, the slices summed in the owning CTA's shared memory before the
+//     epilogue (the q, k, v projections and FFW1 at C = 256).
 //   * gemm_pair_kernel: the same engine on CTA pairs (M = 256 MMAs over two
 //     SMs), for the two vocabulary-sized products: the LM head and the
 //     self-conditioning contraction u = p0 . E (p0 rescaled in place after
@@ -498,6 +501,190 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   }
 }
 
+// ================================================= split-K over a cluster
+// The KS CTAs of a cluster (cluster dims KS x 1 x 1) compute the KS K-slices
+// of one output tile, CTA rank r the slice [r nk / KS, (r + 1) nk / KS) of the
+// nk 64-wide K blocks.  The sum over the slices is taken in shared memory: the
+// 32 rows of epilogue warp quarter q belong to rank q KS / 4, the other ranks
+// store their partial sums of those rows into the owner's receive buffer
+// (remote stores, then one release arrival per lane on the owner's barrier
+// for quarter q), and the owner's warp adds them to its own accumulator and
+// runs the epilogue.  No fp32 partials go through global memory and no
+// second launch reduces them.  One tile per cluster; a cluster barrier at the
+// end keeps every CTA resident until no peer can still store into it.
+template <int BN, int STAGES, int KS>
+struct KsumLayout {
+  static_assert(KS == 2 || KS == 4, "a quarter of the tile's rows per owner warp");
+  static constexpr int kA = kBM * kBK * 2;
+  static constexpr int kB = BN * kBK * 2;
+  static constexpr int kStage = kA + kB;
+  static constexpr int kOwned = kBM / KS;  // rows kept by each rank
+  static constexpr int kLd = BN + 4;       // floats per received row (padded against bank conflicts)
+  static constexpr int kRecv = (KS - 1) * kOwned * kLd * 4;
+  static constexpr int kBar = STAGES * kStage + kRecv;
+  static constexpr int kSmem = kBar + 256 + 1024;
+};
+
+template <int BN, int STAGES, int KS, class Epi>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    gemm_ksum_kernel(const __grid_constant__ CUtensorMap mA, const __grid_constant__ CUtensorMap mB0,
+                     const __grid_constant__ CUtensorMap mB1, const __grid_constant__ CUtensorMap mB2,
+                     int nb0, int nb1, int b_sub, int M, int N, int K, Epi epi, int* status, StopCtl ctl) {
+  pdl_wait();
+  using L = KsumLayout<BN, STAGES, KS>;
+  if (all_stopped(ctl.stop_at, ctl.B, ctl.step)) return;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  float* recv = reinterpret_cast<float*>(smem + STAGES * L::kStage);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kBar);
+  uint64_t* empty = full + STAGES;
+  uint64_t* tfull = empty + STAGES;
+  uint64_t* rbar = tfull + 1;  // [4]: the other slices of quarter q have arrived
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(rbar + 4);
+  volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int rank = (int)cluster_ctarank();
+  const int tmn = (int)cluster_id_x();
+  const int num_m = (M + kBM - 1) / kBM;
+  const int m0 = (tmn % num_m) * kBM, n0 = (tmn / num_m) * BN;
+  const int nk = (K + kBK - 1) / kBK;
+  const int kb_lo = rank * nk / KS, kb_hi = (rank + 1) * nk / KS;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(tfull, 1);
+    for (int q = 0; q < 4; ++q) mbar_init(&rbar[q], (KS - 1) * 32);
+    *abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, BN);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // the peers' barriers are initialised before any remote arrival
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      tma_prefetch(&mA);
+      tma_prefetch(&mB0);
+      int stage = 0;
+      uint32_t phase = 0;
+      for (int kb = kb_lo; kb < kb_hi; ++kb) {
+        if (!mbar_wait(&empty[stage], phase ^ 1, status, abort)) break;
+        uint8_t* sa = smem + stage * L::kStage;
+        uint8_t* sb = sa + L::kA;
+        mbar_arrive_expect_tx(&full[stage], L::kStage);
+        tma_load_2d(sa, &mA, &full[stage], kb * kBK, m0);
+        for (int r = 0; r < BN; r += b_sub) {
+          const int n = n0 + r;
+          const CUtensorMap* mb = &mB0;
+          int nb = n;
+          if (n >= nb0 + nb1) {
+            mb = &mB2;
+            nb = n - nb0 - nb1;
+          } else if (n >= nb0) {
+            mb = &mB1;
+            nb = n - nb0;
+          }
+          tma_load_2d(sb + r * 128, mb, &full[stage], kb * kBK, nb);
+        }
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16(kBM, BN, false);
+      int stage = 0;
+      uint32_t phase = 0;
+      bool alive = true;
+      for (int kb = kb_lo; kb < kb_hi; ++kb) {
+        if (!mbar_wait(&full[stage], phase, status, abort)) {
+          alive = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t sa = smem_u32(smem + stage * L::kStage);
+        const uint32_t sb = sa + L::kA;
+#pragma unroll
+        for (int kk = 0; kk < kBK / 16; ++kk) {
+          const uint64_t ad = sdesc_sw128(sa + kk * 32, 16, 1024);
+          const uint64_t bd = sdesc_sw128(sb + kk * 32, 16, 1024);
+          umma_bf16(tmem, ad, bd, idesc, (kb != kb_lo || kk != 0) ? 1u : 0u);
+        }
+        umma_commit(&empty[stage]);
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+      if (alive) umma_commit(tfull);
+    }
+    __syncwarp();
+  } else {
+    const int q = warp & 3;  // TMEM lane quarter this warp may read
+    const int r_local = q * 32 + lane;
+    const int owner = q * KS / 4;
+    const int lr = r_local - owner * L::kOwned;  // row within the owner's block
+    const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16);
+    if (mbar_wait_warp(tfull, 0, status, abort)) {
+      tc_fence_after();
+      if (owner != rank) {
+        const int slot = rank < owner ? rank : rank - 1;
+        const uint32_t dst = cluster_addr(recv + ((size_t)slot * L::kOwned + lr) * L::kLd, (uint32_t)owner);
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          float v[32];
+          tmem_ld32(tb + c * 32, v);
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            st_cluster_v4(dst + (uint32_t)((c * 32 + 4 * j) * 4), v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+        }
+        mbar_arrive_cluster_release(cluster_addr(&rbar[q], (uint32_t)owner));
+      } else if (mbar_wait_warp<true>(&rbar[q], 0, status, abort)) {
+        const float* own = recv + (size_t)lr * L::kLd;
+        auto ld = [&](int c, float(&v)[32]) {
+          tmem_ld32(tb + c * 32, v);
+#pragma unroll
+          for (int s = 0; s < KS - 1; ++s) {
+            const float4* src = reinterpret_cast<const float4*>(own + (size_t)s * L::kOwned * L::kLd + c * 32);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const float4 x = src[j];
+              v[4 * j] += x.x;
+              v[4 * j + 1] += x.y;
+              v[4 * j + 2] += x.z;
+              v[4 * j + 3] += x.w;
+            }
+          }
+        };
+        const int row = m0 + r_local;
+        epi.template tile<BN>(row, row < M, n0, N, ld, 0);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  __syncwarp();
+  cluster_sync();  // no CTA leaves while a peer may still store into its shared memory
+  drain_if_aborted(abort);
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, BN);
+  }
+}
+
 // ============================================================ grouped GEMM
 // The MoE expert products: A = expert-sorted rows [R][K], B = the experts'
 // matrices stacked [groups * b_rows][K].  The M-tile table (written on the
@@ -737,6 +924,83 @@ static cudaError_t run_gemm(const CUtensorMap& mA, const CUtensorMap& mB0, const
   const int grid = tiles < num_sms() ? tiles : num_sms();
   return launch_pdl(kern, dim3(grid), dim3(kGemmThreads), L::kSmem, st, mA, mB0, mB1, mB2, nb0, nb1, b_sub, M,
                     N, K, ksplit, lbo, sbo, epi, status, ctl);
+}
+
+template <int BN, int STAGES, int KS, class Epi>
+static cudaError_t run_gemm_ksum(const CUtensorMap& mA, const CUtensorMap& mB0, const CUtensorMap& mB1,
+                                 const CUtensorMap& mB2, int nb0, int nb1, int b_sub, int M, int N, int K,
+                                 const Epi& epi, int* status, StopCtl ctl, cudaStream_t st) {
+  using L = KsumLayout<BN, STAGES, KS>;
+  cudaError_t e = set_smem_once<gemm_ksum_kernel<BN, STAGES, KS, Epi>>(L::kSmem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(cdiv(M, kBM) * cdiv(N, BN) * KS, 1, 1);
+  cfg.blockDim = dim3(kGemmThreads, 1, 1);
+  cfg.dynamicSmemBytes = L::kSmem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = KS;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = kProgrammaticLaunch;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, gemm_ksum_kernel<BN, STAGES, KS, Epi>, mA, mB0, mB1, mB2, nb0, nb1, b_sub, M, N,
+                            K, epi, status, ctl);
+}
+
+// Shape of a cluster split-K launch: 128- or 64-column tiles, 2 or 4 K-slices
+// per tile, one wave (tiles x slices <= SMs), each slice at least 4 K blocks;
+// the choice with the fewest operand bytes per CTA, or {0, 0} when none fits
+// or none beats an unsplit 64-column launch by a quarter.  `bn128_only` for
+// epilogues that need whole 128-column tiles.  The launchers take it only
+// where the GEMM would otherwise be split over K with a reduce launch: where
+// unsplit 64-column tiles fit in one wave they measured as fast or faster.
+struct KsumShape {
+  int bn, ks;
+};
+static KsumShape ksum_shape(int M, int N, int K, bool bn128_only) {
+  const int nk = cdiv(K, kBK), mt = cdiv(M, kBM);
+  KsumShape best{0, 0};
+  double best_bytes = 0;
+  for (int bn : {128, 64}) {
+    if (bn == 64 && bn128_only) continue;
+    if (N % bn != 0) continue;
+    for (int ks : {2, 4}) {
+      const int ctas = mt * (N / bn) * ks;
+      if (ctas > num_sms() || nk < 4 * ks) continue;
+      const double bytes = (double)cdiv(nk, ks) * (kBM + bn) * kBK * 2;
+      if (best.ks == 0 || bytes < best_bytes) {
+        best = {bn, ks};
+        best_bytes = bytes;
+      }
+    }
+  }
+  if (best.ks == 0) return best;
+  const double unsplit = (double)nk * (kBM + 64) * kBK * 2;
+  if (best_bytes > 0.75 * unsplit) return KsumShape{0, 0};
+  return best;
+}
+
+// k64: instantiate the 64-column shapes too (not for epilogues that need
+// whole 128-column tiles).
+template <bool k64, class Epi>
+static cudaError_t run_ksum(KsumShape sh, const CUtensorMap& mA, const CUtensorMap& mB0, const CUtensorMap& mB1,
+                            const CUtensorMap& mB2, int nb0, int nb1, int b_sub, int M, int N, int K, const Epi& epi,
+                            int* status, StopCtl ctl, cudaStream_t st) {
+  if (sh.bn == 128 && sh.ks == 2)
+    return run_gemm_ksum<128, 4, 2>(mA, mB0, mB1, mB2, nb0, nb1, b_sub, M, N, K, epi, status, ctl, st);
+  if (sh.bn == 128 && sh.ks == 4)
+    return run_gemm_ksum<128, 4, 4>(mA, mB0, mB1, mB2, nb0, nb1, b_sub, M, N, K, epi, status, ctl, st);
+  if constexpr (k64) {
+    if (sh.bn == 64 && sh.ks == 2)
+      return run_gemm_ksum<64, 6, 2>(mA, mB0, mB1, mB2, nb0, nb1, b_sub, M, N, K, epi, status, ctl, st);
+    if (sh.bn == 64 && sh.ks == 4)
+      return run_gemm_ksum<64, 6, 4>(mA, mB0, mB1, mB2, nb0, nb1, b_sub, M, N, K, epi, status, ctl, st);
+  }
+  return cudaErrorInvalidConfiguration;
 }
 
 // ============================================================ pair GEMM
@@ -1027,6 +1291,11 @@ cudaError_t launch_debug_gemm(const void* A, const void* Bm, float* D, int M, in
     if (!tmap_kmajor(&mB, Bm, N, K, 256)) return cudaErrorInvalidValue;
     return run_gemm<256, 4, false>(mA, mB, mB, mB, N, 0, 256, M, N, K, 0, 0, epi, status, ctl, st);
   }
+  if (b_mn_major >= 5) {  // cluster split-K engine, B [N][K]
+    const KsumShape sh{b_mn_major <= 6 ? 128 : 64, b_mn_major % 2 == 1 ? 2 : 4};
+    if (!tmap_kmajor(&mB, Bm, N, K, sh.bn)) return cudaErrorInvalidValue;
+    return run_ksum<true>(sh, mA, mB, mB, mB, N, 0, sh.bn, M, N, K, epi, status, ctl, st);
+  }
   if (b_mn_major == 3) {  // CTA-pair engine, B [N][K]
     if (!tmap_kmajor(&mB, Bm, N, K, 128)) return cudaErrorInvalidValue;
     return run_gemm_pair<256, 6, false>(mA, mB, mB, M, N, K, 1, epi, status, ctl, st);
@@ -1154,6 +1423,15 @@ cudaError_t launch_gemm_bf16(const void* A, const void* W, void* out, int ldo, c
     return run_gemm<64, 6, false>(mA, mB64, mB64, mB64, N, 0, 64, M, N, K, 0, 0, epi, status, ctl, st);
   }
   const int ks = gemm_ksplit(M, N, K);
+  // Split over K: one wave of clusters that sum their K slices in shared
+  // memory (no partials, no reduce launch) when the shape allows, else fp32
+  // partials and a reduce kernel.
+  const KsumShape sh = ks > 1 ? ksum_shape(M, N, K, false) : KsumShape{0, 0};
+  if (sh.ks > 0) {
+    CUtensorMap mBs;
+    if (!tmap_kmajor(&mBs, W, N, K, sh.bn)) return cudaErrorInvalidValue;
+    return run_ksum<true>(sh, mA, mBs, mBs, mBs, N, 0, sh.bn, M, N, K, epi, status, ctl, st);
+  }
   if (ks > 1 && part && (size_t)ks * M * N <= part_elems && N % 8 == 0) {
     EpiPartial ep{part, M, N};
     cudaError_t e = run_gemm<128, 4, false>(mA, mB, mB, mB, N, 0, 128, M, N, K, 0, 0, ep, status, ctl, st, ks);
@@ -1191,6 +1469,25 @@ cudaError_t launch_qkv(const void* a, const void* Wq, const void* Wk, const void
   const CUtensorMap& m2 = mv;
   const int nb0 = Wq ? nq : nkv, nb1 = Wq ? nkv : nkv;
   const int ks = gemm_ksplit(M, N, D.d);
+  const KsumShape sh = ks > 1 ? ksum_shape(M, N, D.d, D.hd > 64) : KsumShape{0, 0};
+  if (sh.ks > 0) {  // split over K, summed across the cluster (see launch_gemm_bf16)
+    switch (D.hd) {
+      case 32: {
+        EpiQKV<32> e{bf(q), bf(k), bf(v), rope, D.C, D.Hq, D.Hkv, nq, nkv, kv_rows, kv_row0};
+        return run_ksum<true>(sh, mA, m0, m1, m2, nb0, nb1, D.hd, M, N, D.d, e, status, ctl, st);
+      }
+      case 64: {
+        EpiQKV<64> e{bf(q), bf(k), bf(v), rope, D.C, D.Hq, D.Hkv, nq, nkv, kv_rows, kv_row0};
+        return run_ksum<true>(sh, mA, m0, m1, m2, nb0, nb1, D.hd, M, N, D.d, e, status, ctl, st);
+      }
+      case 128: {
+        EpiQKV<128> e{bf(q), bf(k), bf(v), rope, D.C, D.Hq, D.Hkv, nq, nkv, kv_rows, kv_row0};
+        return run_ksum<false>(sh, mA, m0, m1, m2, nb0, nb1, D.hd, M, N, D.d, e, status, ctl, st);
+      }
+      default:
+        return cudaErrorInvalidValue;
+    }
+  }
   if (ks > 1 && part && (size_t)ks * M * N <= part_elems) {
     EpiPartial ep{part, M, N};
     cudaError_t e =

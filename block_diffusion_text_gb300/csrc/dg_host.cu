@@ -727,9 +727,10 @@ dg_status dg_commit_block(const dg_model* model, dg_kv_cache* cache, const int32
 
 dg_status dg_debug_gemm(const void* A, const void* Bm, float* D, int32_t M, int32_t N, int32_t K,
                         int32_t b_mn_major, void* stream) {
-  if (!A || !Bm || !D || M <= 0 || N <= 0 || K <= 0 || b_mn_major < 0 || b_mn_major > 4)
+  if (!A || !Bm || !D || M <= 0 || N <= 0 || K <= 0 || b_mn_major < 0 || b_mn_major > 8)
     return DG_ERR_ARG;
   if (K % 8 != 0 || N % 8 != 0) return DG_ERR_SHAPE;
+  if (b_mn_major >= 5 && cdiv(K, 64) < (b_mn_major == 6 || b_mn_major == 8 ? 4 : 2)) return DG_ERR_SHAPE;
   int* status = nullptr;
   DG_TRY(cudaGetSymbolAddress(reinterpret_cast<void**>(&status), g_debug_status));
   return cuda_status(launch_debug_gemm(A, Bm, D, M, N, K, b_mn_major, status,

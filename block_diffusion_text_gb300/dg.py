@@ -406,10 +406,10 @@ def canvas_init(B, C, V, seed, block=0, device="cuda", stream=None) -> torch.Ten
 
 
 def debug_gemm(A: torch.Tensor, Bm: torch.Tensor, b_mn_major: int = 0, stream=None) -> torch.Tensor:
-    """fp32 A B^T on the tensor-core engine; B is [N][K] (b_mn_major 0, or 3 on CTA pairs) or
-    [K][N] (1 or 2, or 4 on CTA pairs)."""
+    """fp32 A B^T on the tensor-core engine; B is [N][K] (b_mn_major 0, 3 on CTA pairs, 5-8 on
+    the cluster split-K engine) or [K][N] (1 or 2, or 4 on CTA pairs)."""
     M, K = A.shape
-    N = Bm.shape[0] if b_mn_major in (0, 3) else Bm.shape[1]
+    N = Bm.shape[0] if b_mn_major in (0, 3, 5, 6, 7, 8) else Bm.shape[1]
     D = torch.empty(M, N, dtype=torch.float32, device=A.device)
     _check(load().dg_debug_gemm(_ptr(A), _ptr(Bm), _ptr(D), M, N, K, b_mn_major, _stream(stream)),
            "dg_debug_gemm")

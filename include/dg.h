@@ -389,13 +389,6 @@ DG_API dg_status dg_quantize_rows_e4m3(const void* X, int32_t R, int32_t d, void
  * DG_ERR_TIMEOUT if a bounded wait of that call ran out).  Allocates nothing.  */
 DG_API dg_status dg_attention_noalloc_status(int32_t* status, void* stream);
 
-/* Diagnostics of the tensor-core GEMM engine, used by the tests to check it
- * in isolation (not a step of the method).  D fp32 [M][N] = A B^T with
- * A bf16 [M][K], and B bf16 [N][K] when b_mn_major == 0, or B bf16 [K][N]
- * when b_mn_major == 1 (the layout of E in the self-conditioning contraction).
- * b_mn_major == 3 / 4 run the same products (B [N][K] / B [K][N]) on the
- * CTA-pair engine (M = 256 MMAs over two SMs) that the LM head and the
- * self-conditioning contraction use.  K, N multiples of 8.                     */
 /* Diagnostics of the bounded device waits (not a step of the method): runs
  * one kernel whose mbarrier wait is never satisfied.  The wait gives up after
  * its limit (2 s), records DG_ERR_TIMEOUT in a library status word, and the
@@ -404,6 +397,18 @@ DG_API dg_status dg_attention_noalloc_status(int32_t* status, void* stream);
  * to check that path without a device fault.                                  */
 DG_API dg_status dg_debug_wait_timeout(int32_t* status, void* stream);
 
+/* Diagnostics of the tensor-core GEMM engine, used by the tests to check it
+ * in isolation (not a step of the method).  D fp32 [M][N] = A B^T with
+ * A bf16 [M][K], and B bf16 [N][K] when b_mn_major == 0, or B bf16 [K][N]
+ * when b_mn_major == 1 (the layout of E in the self-conditioning contraction).
+ * b_mn_major == 3 / 4 run the same products (B [N][K] / B [K][N]) on the
+ * CTA-pair engine (M = 256 MMAs over two SMs) that the LM head and the
+ * self-conditioning contraction use.  b_mn_major == 5 / 6 / 7 / 8 run
+ * B [N][K] on the cluster split-K engine of the small projections (the K
+ * slices of a tile summed in shared memory across the cluster): 128-column
+ * tiles over 2 / 4 slices, 64-column tiles over 2 / 4 slices; K must then
+ * hold at least one 64-wide block per slice (DG_ERR_SHAPE otherwise).
+ * K, N multiples of 8.                                                        */
 DG_API dg_status dg_debug_gemm(const void* A, const void* Bm, float* D, int32_t M, int32_t N, int32_t K,
                         int32_t b_mn_major, void* stream);
 

@@ -142,6 +142,12 @@ def test_small_entry_points_validate(dg):
     assert L.dg_debug_wait_timeout(None, None) == dg.DG_ERR_ARG
     assert L.dg_debug_gemm(ct.c_void_p(FAKE), ct.c_void_p(FAKE), ct.c_void_p(FAKE), 4, 12, 8, 0, None) == \
         dg.DG_ERR_SHAPE
+    assert L.dg_debug_gemm(ct.c_void_p(FAKE), ct.c_void_p(FAKE), ct.c_void_p(FAKE), 4, 16, 64, 9, None) == \
+        dg.DG_ERR_ARG
+    # the cluster split-K modes need a 64-wide K block per slice
+    for mode, k in ((5, 64), (6, 192), (7, 64), (8, 192)):
+        assert L.dg_debug_gemm(ct.c_void_p(FAKE), ct.c_void_p(FAKE), ct.c_void_p(FAKE), 4, 16, k, mode, None) == \
+            dg.DG_ERR_SHAPE
     f = ct.c_void_p(FAKE)
     assert L.dg_attention_noalloc(f, f, f, 100, 50, f, f, f, 1, 16, 2, 1, 96, None) == dg.DG_ERR_SHAPE
     assert L.dg_attention_noalloc(f, f, f, 100, 200, f, f, f, 1, 16, 2, 1, 32, None) == dg.DG_ERR_ARG
