@@ -1028,8 +1028,12 @@ struct PairLayout {
 // columns (loaded through mBh, boxes of BN / 4 rows), so the round is shorter.
 // F8: E4M3 operands (tcgen05 kind::f8f6f4): a 128-byte swizzled row then holds
 // 128 elements of K instead of 64, so a stage covers twice the K.
-template <int BN, int STAGES, bool B_MN, class Epi, bool TAIL = false, bool F8 = false>
-__global__ void __launch_bounds__(kGemmThreads, 1)
+// EW: epilogue warps per TMEM lane quarter.  With 2, each of the two warps of a
+// quarter takes one half of the tile's columns (BN / 2, one statistics group
+// of the LM head), so two warps per SM sub-partition hide each other's TMEM
+// and exp latency; a half tile (TAIL) goes to the first warp of each quarter.
+template <int BN, int STAGES, bool B_MN, class Epi, bool TAIL = false, bool F8 = false, int EW = 1>
+__global__ void __launch_bounds__(64 + 128 * EW, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap mA, const __grid_constant__ CUtensorMap mB,
                      const __grid_constant__ CUtensorMap mBh, int M, int N, int K, int ksplit, Epi epi,
                      int* status, StopCtl ctl) {
@@ -1083,7 +1087,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], 8);  // four epilogue warps in each CTA
+      mbar_init(&tempty[a], 8 * EW);  // 4 EW epilogue warps in each CTA
     }
     *abort = 0;
     fence_mbar_init();
@@ -1188,6 +1192,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     __syncwarp();
   } else {
     const int q = warp & 3;  // TMEM lane quarter this warp may read
+    const int half = (warp - 2) / 4;  // EW == 2: which half of the tile's columns
     const int r_local = q * 32 + lane;
     int it = 0;
     for (int tile = cid; tile < num_tiles; tile += ncl, ++it) {
@@ -1199,11 +1204,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       coords(tile, m0, n0, kb_lo, kb_hi, width);
       const int row = m0 + (int)rank * kBM + r_local;
       const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
-      auto ld = [&](int c, float(&v)[32]) { tmem_ld32(tb + c * 32, v); };
-      if (!TAIL || width == BN)
-        epi.template tile<BN>(row, row < M, n0, N, ld, tile / num_mn);
-      else
-        epi.template tile<BN / 2>(row, row < M, n0, N, ld, 0);
+      if constexpr (EW == 1) {
+        auto ld = [&](int c, float(&v)[32]) { tmem_ld32(tb + c * 32, v); };
+        if (!TAIL || width == BN)
+          epi.template tile<BN>(row, row < M, n0, N, ld, tile / num_mn);
+        else
+          epi.template tile<BN / 2>(row, row < M, n0, N, ld, 0);
+      } else {
+        static_assert(EW == 2, "one or two epilogue warps per lane quarter");
+        const uint32_t th = tb + (uint32_t)(half * (BN / 2));
+        auto ld = [&](int c, float(&v)[32]) { tmem_ld32(th + c * 32, v); };
+        if (!TAIL || width == BN)
+          epi.template tile<BN / 2>(row, row < M, n0 + half * (BN / 2), N, ld, tile / num_mn);
+        else if (half == 0)
+          epi.template tile<BN / 2>(row, row < M, n0, N, ld, 0);
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(cluster_addr(&tempty[acc], 0));
@@ -1222,12 +1237,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 // Clusters of two that can be resident at once with this kernel's shared
 // memory (SMs per GPC may be odd, so it can be below half the SM count).
 template <auto Kernel>
-static int max_pair_clusters(int smem) {
+static int max_pair_clusters(int smem, int threads) {
   static int n = -1;
   if (n < 0) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * (kTargetCtas / 2), 1, 1);
-    cfg.blockDim = dim3(kGemmThreads, 1, 1);
+    cfg.blockDim = dim3(threads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -1247,25 +1262,25 @@ static int max_pair_clusters(int smem) {
 }
 
 // Clusters a pair GEMM of this many tiles may use (0 if none can launch).
-template <int BN, int STAGES, bool B_MN, class Epi, bool TAIL = false, bool F8 = false>
+template <int BN, int STAGES, bool B_MN, class Epi, bool TAIL = false, bool F8 = false, int EW = 1>
 static int pair_clusters() {
   using L = PairLayout<BN, STAGES, B_MN>;
-  if (set_smem_once<gemm_pair_kernel<BN, STAGES, B_MN, Epi, TAIL, F8>>(L::kSmem) != cudaSuccess) return 0;
-  return max_pair_clusters<gemm_pair_kernel<BN, STAGES, B_MN, Epi, TAIL, F8>>(L::kSmem);
+  if (set_smem_once<gemm_pair_kernel<BN, STAGES, B_MN, Epi, TAIL, F8, EW>>(L::kSmem) != cudaSuccess) return 0;
+  return max_pair_clusters<gemm_pair_kernel<BN, STAGES, B_MN, Epi, TAIL, F8, EW>>(L::kSmem, 64 + 128 * EW);
 }
 
-template <int BN, int STAGES, bool B_MN, class Epi, bool TAIL = false, bool F8 = false>
+template <int BN, int STAGES, bool B_MN, class Epi, bool TAIL = false, bool F8 = false, int EW = 1>
 static cudaError_t run_gemm_pair(const CUtensorMap& mA, const CUtensorMap& mB, const CUtensorMap& mBh, int M,
                                  int N, int K, int ksplit, const Epi& epi, int* status, StopCtl ctl,
                                  cudaStream_t st) {
   using L = PairLayout<BN, STAGES, B_MN>;
-  const int maxc = pair_clusters<BN, STAGES, B_MN, Epi, TAIL, F8>();
+  const int maxc = pair_clusters<BN, STAGES, B_MN, Epi, TAIL, F8, EW>();
   if (maxc <= 0) return cudaErrorInvalidConfiguration;
   const int tiles = cdiv(M, 2 * kBM) * cdiv(N, BN) * ksplit;
   const int ncl = tiles < maxc ? tiles : maxc;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * ncl, 1, 1);
-  cfg.blockDim = dim3(kGemmThreads, 1, 1);
+  cfg.blockDim = dim3(64 + 128 * EW, 1, 1);
   cfg.dynamicSmemBytes = L::kSmem;
   cfg.stream = st;
   cudaLaunchAttribute attr[2];
@@ -1277,8 +1292,8 @@ static cudaError_t run_gemm_pair(const CUtensorMap& mA, const CUtensorMap& mB, c
   attr[1].val.programmaticStreamSerializationAllowed = kProgrammaticLaunch;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, gemm_pair_kernel<BN, STAGES, B_MN, Epi, TAIL, F8>, mA, mB, mBh, M, N, K, ksplit,
-                            epi, status, ctl);
+  return cudaLaunchKernelEx(&cfg, gemm_pair_kernel<BN, STAGES, B_MN, Epi, TAIL, F8, EW>, mA, mB, mBh, M, N, K,
+                            ksplit, epi, status, ctl);
 }
 
 cudaError_t launch_debug_gemm(const void* A, const void* Bm, float* D, int M, int N, int K,
@@ -1514,6 +1529,12 @@ cudaError_t launch_qkv(const void* a, const void* Wq, const void* Wk, const void
   return cudaErrorInvalidValue;
 }
 
+// Epilogue warps per TMEM lane quarter of the LM head.  The FP8 head's main
+// loop is half as long as the bf16 head's, so its epilogue bounds it: two
+// warps per quarter took it from 216 to 180 us at V = 262144, d = 2816, C = 256
+// (same-box A/B), while the bf16 head measured 3.5 us slower with two.
+constexpr int kLmEW = 1, kLmEW8 = 2;
+
 cudaError_t launch_lmhead(const LmArgs& a, StopCtl ctl, int* status, cudaStream_t st) {
   CUtensorMap mA, mB, mBh;  // B boxes: half a vocabulary tile (one CTA of a pair), or half of a half tile
   EpiLM epi{a.alpha, a.coef2, a.inv_sqrt_d, reinterpret_cast<__nv_bfloat16*>(a.pt), a.pm, a.pl,
@@ -1524,12 +1545,14 @@ cudaError_t launch_lmhead(const LmArgs& a, StopCtl ctl, int* status, cudaStream_
         !make_tmap_2d(&mB, a.E8, (uint64_t)a.d, (uint64_t)a.V, (uint64_t)a.d, 2 * kBK, kLmBN / 2, true) ||
         !make_tmap_2d(&mBh, a.E8, (uint64_t)a.d, (uint64_t)a.V, (uint64_t)a.d, 2 * kBK, kLmBN / 4, true))
       return cudaErrorInvalidValue;
-    return run_gemm_pair<kLmBN, 7, false, EpiLM, true, true>(mA, mB, mBh, a.M, a.V, a.d, 1, epi, status, ctl, st);
+    return run_gemm_pair<kLmBN, 7, false, EpiLM, true, true, kLmEW8>(mA, mB, mBh, a.M, a.V, a.d, 1, epi, status, ctl,
+                                                                    st);
   }
   if (!tmap_kmajor(&mA, a.h, a.M, a.d, kBM) || !tmap_kmajor(&mB, a.E, a.V, a.d, kLmBN / 2) ||
       !tmap_kmajor(&mBh, a.E, a.V, a.d, kLmBN / 4))
     return cudaErrorInvalidValue;
-  return run_gemm_pair<kLmBN, 7, false, EpiLM, true>(mA, mB, mBh, a.M, a.V, a.d, 1, epi, status, ctl, st);
+  return run_gemm_pair<kLmBN, 7, false, EpiLM, true, false, kLmEW>(mA, mB, mBh, a.M, a.V, a.d, 1, epi, status, ctl,
+                                                                st);
 }
 
 // ====================================================== self-conditioning
