@@ -650,46 +650,48 @@ cudaError_t launch_fill_tokens(int32_t* tokens, int n, int value, cudaStream_t s
 // ------------------------------------------------ self-conditioning reduce --
 // u = sum of the per-split partials of p0 . E (bf16 out), and the Gumbel-max
 // token of accepted positions = the best (score, lowest index) over chunks.
-__global__ void __launch_bounds__(256) reduce_kernel(ReduceArgs a, StopCtl ctl) {
+// Grid (M, G + 1): CTA (row, y < G) sums 128 float4 columns of the row, each
+// thread one column with the loads of eight splits in flight at once (summed
+// as a fixed tree per group of eight, the groups in order); CTA (row, G) picks
+// the sampled token.
+constexpr int kReduceCols = 128;
+
+__global__ void __launch_bounds__(kReduceCols) reduce_kernel(ReduceArgs a, StopCtl ctl) {
   pdl_wait();
   if (all_stopped(ctl.stop_at, ctl.B, ctl.step)) return;
   const int row = blockIdx.x;
   const int n4 = a.d / 4;
-  const size_t sstride = (size_t)a.M * a.d;
-  // the row's p0 factor (its tiles hold exp2(t - ref2f))
-  const float fr = exp2f(a.ref2f[row] - a.rowmax[row]) / a.lsum[row];
-  const float* src = a.upart + (size_t)row * a.d;
-  for (int c = threadIdx.x; c < n4; c += blockDim.x) {
-    // four splits at a time: independent loads in flight
-    float4 acc[4];
+  if ((int)blockIdx.y * kReduceCols < n4) {
+    const int c = blockIdx.y * kReduceCols + threadIdx.x;
+    if (c >= n4) return;
+    const size_t sstride = (size_t)a.M * a.d;
+    // the row's p0 factor (its tiles hold exp2(t - ref2f))
+    const float fr = exp2f(a.ref2f[row] - a.rowmax[row]) / a.lsum[row];
+    const float* src = a.upart + (size_t)row * a.d + 4 * c;
+    float4 tot = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s0 = 0; s0 < a.nsplit; s0 += 8) {
+      float4 v[8];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-    int s = 0;
-    for (; s + 4 <= a.nsplit; s += 4) {
+      for (int k = 0; k < 8; ++k)
+        v[k] = s0 + k < a.nsplit ? *reinterpret_cast<const float4*>(src + (s0 + k) * sstride)
+                                 : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        const float4 v = *reinterpret_cast<const float4*>(src + (s + k) * sstride + 4 * c);
-        acc[k].x += v.x;
-        acc[k].y += v.y;
-        acc[k].z += v.z;
-        acc[k].w += v.w;
+        v[k].x += v[k + 4].x;
+        v[k].y += v[k + 4].y;
+        v[k].z += v[k + 4].z;
+        v[k].w += v[k + 4].w;
       }
+      tot.x += (v[0].x + v[1].x) + (v[2].x + v[3].x);
+      tot.y += (v[0].y + v[1].y) + (v[2].y + v[3].y);
+      tot.z += (v[0].z + v[1].z) + (v[2].z + v[3].z);
+      tot.w += (v[0].w + v[1].w) + (v[2].w + v[3].w);
     }
-    for (; s < a.nsplit; ++s) {
-      const float4 v = *reinterpret_cast<const float4*>(src + s * sstride + 4 * c);
-      acc[0].x += v.x;
-      acc[0].y += v.y;
-      acc[0].z += v.z;
-      acc[0].w += v.w;
-    }
-    const float x = (acc[0].x + acc[1].x) + (acc[2].x + acc[3].x);
-    const float y = (acc[0].y + acc[1].y) + (acc[2].y + acc[3].y);
-    const float z = (acc[0].z + acc[1].z) + (acc[2].z + acc[3].z);
-    const float t = (acc[0].w + acc[1].w) + (acc[2].w + acc[3].w);
     uint2 w;
-    w.x = pack_bf16(x * fr, y * fr);
-    w.y = pack_bf16(z * fr, t * fr);
+    w.x = pack_bf16(tot.x * fr, tot.y * fr);
+    w.y = pack_bf16(tot.z * fr, tot.w * fr);
     *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(a.u) + (size_t)row * a.d + 4 * c) = w;
+    return;
   }
   // sampled token of an accepted row: the best (score, lowest index) over the
   // chunks, one warp
@@ -724,7 +726,8 @@ __global__ void __launch_bounds__(256) reduce_kernel(ReduceArgs a, StopCtl ctl) 
 }
 
 cudaError_t launch_reduce(const ReduceArgs& a, StopCtl ctl, cudaStream_t st) {
-  return launch_pdl(reduce_kernel, dim3(a.M), dim3(256), 0, st, a, ctl);
+  const int g = cdiv(a.d / 4, kReduceCols);
+  return launch_pdl(reduce_kernel, dim3(a.M, g + 1), dim3(kReduceCols), 0, st, a, ctl);
 }
 
 // ------------------------------------------------- bounded-wait diagnostics --
