@@ -165,6 +165,16 @@ def test_long_canvas_entropy_given_h():
     _run_and_compare(dims, 14, tau=0.6, entropy_given_h=True)
 
 
+@pytest.mark.parametrize("hd", [32, 64])
+def test_split_k_clusters_small_heads(hd):
+    """d = 2048 with 128 canvas rows: the q/k/v projection (64-column tiles, heads of 32 or 64) and
+    FFW1 (GELU) run split over K on clusters of four CTAs that sum their slices in shared memory."""
+    dims = synth.Dims(V=2000, d=2048, C=64, B=2, Hq=4, Hkv=2, hd=hd, F=1024, P=100, cap=160)
+    g = torch.Generator().manual_seed(7)
+    z = (torch.randn(dims.B, dims.C, dims.d, generator=g) * 0.02).to(torch.bfloat16)
+    _run_and_compare(dims, 15 + hd, tau=0.7, step=1, z_in=z)
+
+
 def test_tensor_core_attention_canvas_tail():
     dims = synth.Dims(V=512, d=64, C=40, B=1, Hq=2, Hkv=2, hd=128, F=64, P=128, cap=128)
     _run_and_compare(dims, 13)
