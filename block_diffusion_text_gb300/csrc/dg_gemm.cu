@@ -236,7 +236,11 @@ struct EpiLM {
     }
   }
   // Statistics per group of kStatCols columns, so that a tile may be 128 or
-  // 256 columns wide.
+  // 256 columns wide.  The maximum / argmax scan and the two sums each run as
+  // four independent chains (columns j mod 4, pairs (j / 2) mod 4) merged at
+  // the end of the group, so that one thread's dependent adds and compares
+  // overlap; chunks wholly inside the vocabulary and clear of the excluded
+  // column skip the per-column tests.
   template <int BN, class LD>
   DG_DEV void tile(int row, bool ok, int n0, int N, LD& ld, int /*split*/) const {
     static_assert(BN % kStatCols == 0, "a tile holds whole statistics groups");
@@ -248,43 +252,67 @@ struct EpiLM {
     for (int g = 0; g < BN / kStatCols; ++g) {
       const int g0 = n0 + g * kStatCols;
       if (g0 >= N) break;  // uniform over the warp
-      float vmax = -FLT_MAX;
-      int imax = g0;
-#pragma unroll 1
-      for (int c = 0; c < kStatCols / 32; ++c) {
-        float v[32];
-        ld(g * (kStatCols / 32) + c, v);
-        scale_cols(v, g0 + c * 32, N);
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const int col = g0 + c * 32 + j;
-          if (col < N && col != excl && v[j] > vmax) {
-            vmax = v[j];
-            imax = col;
-          }
-        }
-      }
-      const float m2 = vmax * c2;
-      // stored values exp2(t - R2) = p * exp2(m2 - R2), unless they would
-      // overflow (then p itself, row flagged)
-      const bool own = !(m2 - R2 <= kRefSpan);
-      const float F = own ? 1.0f : exp2f(m2 - R2);
-      if (own && ok) atomicMax(rkey + row, float_key(m2));
-      float l = 0.f, S = 0.f;
+      float vm[4] = {-FLT_MAX, -FLT_MAX, -FLT_MAX, -FLT_MAX};
+      int im[4] = {g0, g0, g0, g0};
 #pragma unroll 1
       for (int c = 0; c < kStatCols / 32; ++c) {
         float v[32];
         ld(g * (kStatCols / 32) + c, v);
         const int col0 = g0 + c * 32;
         scale_cols(v, col0, N);
+        if (col0 + 32 <= N && (excl < col0 || excl >= col0 + 32)) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (v[j] > vm[j & 3]) {
+              vm[j & 3] = v[j];
+              im[j & 3] = col0 + j;
+            }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int col = col0 + j;
+            if (col < N && col != excl && v[j] > vm[j & 3]) {
+              vm[j & 3] = v[j];
+              im[j & 3] = col;
+            }
+          }
+        }
+      }
+      // the chains' first maxima, ties to the lowest column
+      float vmax = vm[0];
+      int imax = im[0];
+#pragma unroll
+      for (int k = 1; k < 4; ++k)
+        if (vm[k] > vmax || (vm[k] == vmax && im[k] < imax)) {
+          vmax = vm[k];
+          imax = im[k];
+        }
+      const float m2 = vmax * c2;
+      // stored values exp2(t - R2) = p * exp2(m2 - R2), unless they would
+      // overflow (then p itself, row flagged)
+      const bool own = !(m2 - R2 <= kRefSpan);
+      const float F = own ? 1.0f : exp2f(m2 - R2);
+      if (own && ok) atomicMax(rkey + row, float_key(m2));
+      float l4[4] = {0.f, 0.f, 0.f, 0.f}, S4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+      for (int c = 0; c < kStatCols / 32; ++c) {
+        float v[32];
+        ld(g * (kStatCols / 32) + c, v);
+        const int col0 = g0 + c * 32;
+        scale_cols(v, col0, N);
+        const bool full = col0 + 32 <= N && (excl < col0 || excl >= col0 + 32);
         uint32_t pk[16];
 #pragma unroll
         for (int j = 0; j < 32; j += 2) {
           const float t0 = fmaf(v[j], c2, -m2), t1 = fmaf(v[j + 1], c2, -m2);
-          const float p0 = (col0 + j < N && col0 + j != excl) ? exp2f(t0) : 0.f;
-          const float p1 = (col0 + j + 1 < N && col0 + j + 1 != excl) ? exp2f(t1) : 0.f;
-          l += p0 + p1;
-          S = fmaf(p0, t0, fmaf(p1, t1, S));
+          float p0 = exp2f(t0), p1 = exp2f(t1);
+          if (!full) {
+            if (col0 + j >= N || col0 + j == excl) p0 = 0.f;
+            if (col0 + j + 1 >= N || col0 + j + 1 == excl) p1 = 0.f;
+          }
+          const int k = (j / 2) & 3;
+          l4[k] += p0 + p1;
+          S4[k] = fmaf(p0, t0, fmaf(p1, t1, S4[k]));
           pk[j / 2] = pack_bf16(p0 * F, p1 * F);
         }
         if (ok) {
@@ -311,6 +339,8 @@ struct EpiLM {
           }
         }
       }
+      const float l = (l4[0] + l4[1]) + (l4[2] + l4[3]);
+      const float S = (S4[0] + S4[1]) + (S4[2] + S4[3]);
       if (ok) {
         const size_t o = (size_t)row * NT + g0 / kStatCols;  // [row][group]
         pm[o] = m2;

@@ -90,12 +90,17 @@ void* byte_ptr(void* p, size_t off) { return reinterpret_cast<uint8_t*>(p) + off
 struct Prof {
   void* const* ev;
   cudaStream_t st;
-  // External record: inside a stream capture it becomes an event-record node of
-  // the graph (timing each replay); outside a capture it is a plain record.
+  // Inside a stream capture an external record, which becomes an event-record
+  // node of the graph (timing each replay); outside a capture a plain record
+  // (the external flag is only accepted under capture).
   cudaError_t mark(int slot, int end) const {
     if (!ev || !ev[2 * slot + end]) return cudaSuccess;
-    return cudaEventRecordWithFlags(reinterpret_cast<cudaEvent_t>(ev[2 * slot + end]), st,
-                                    cudaEventRecordExternal);
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    const cudaError_t e = cudaStreamIsCapturing(st, &cs);
+    if (e != cudaSuccess) return e;
+    const cudaEvent_t evt = reinterpret_cast<cudaEvent_t>(ev[2 * slot + end]);
+    return cs == cudaStreamCaptureStatusActive ? cudaEventRecordWithFlags(evt, st, cudaEventRecordExternal)
+                                               : cudaEventRecord(evt, st);
   }
 };
 

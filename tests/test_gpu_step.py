@@ -165,6 +165,52 @@ def test_long_canvas_entropy_given_h():
     _run_and_compare(dims, 14, tau=0.6, entropy_given_h=True)
 
 
+def test_step_events_eager_and_captured():
+    """Per-kernel events through the ABI: recorded by a host-launched step and by a replayed graph of
+    the same step, every timed slot's pair recorded in order (non-negative elapsed time), and the
+    step's results unchanged by the events."""
+    from block_diffusion_text_gb300 import dg
+    dims, seed = synth.workload("tiny_v512_c16")
+    slots = [k for k in dg.PROF_SLOTS if k != "moe"]
+
+    def events():
+        ev = [None] * (2 * len(dg.PROF_SLOTS))
+        for k in slots:
+            i = dg.PROF_SLOTS.index(k)
+            for e in (0, 1):
+                ev[2 * i + e] = torch.cuda.Event(enable_timing=True)
+                ev[2 * i + e].record()
+        return ev
+
+    outs = []
+    for use_events in (False, True):
+        _, _, _, _, model, canvas = _setup(dims, seed)
+        ev = events() if use_events else None
+        out = dg.denoise_step(model, canvas, tau=0.7, b=0.1, seed=seed, step=0, events=ev)
+        torch.cuda.synchronize()
+        assert model.status() == 0
+        if use_events:
+            for k in slots:
+                i = dg.PROF_SLOTS.index(k)
+                assert ev[2 * i].elapsed_time(ev[2 * i + 1]) >= 0.0, k
+        outs.append((canvas.tokens.cpu(), canvas.z.cpu(), out["entropy"].cpu()))
+        if use_events:  # the same step captured with its events, then replayed
+            ev2 = events()
+            g = torch.cuda.CUDAGraph()
+            s = torch.cuda.Stream()
+            s.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.graph(g, stream=s):
+                dg.denoise_step(model, canvas, tau=0.7, b=0.1, seed=seed, step=1, events=ev2)
+            g.replay()
+            torch.cuda.synchronize()
+            assert model.status() == 0
+            for k in slots:
+                i = dg.PROF_SLOTS.index(k)
+                assert ev2[2 * i].elapsed_time(ev2[2 * i + 1]) >= 0.0, k
+    for x, y in zip(outs[0], outs[1]):
+        assert torch.equal(x, y)
+
+
 @pytest.mark.parametrize("hd", [32, 64])
 def test_split_k_clusters_small_heads(hd):
     """d = 2048 with 128 canvas rows: the q/k/v projection (64-column tiles, heads of 32 or 64) and
