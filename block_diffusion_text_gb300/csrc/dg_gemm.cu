@@ -208,8 +208,7 @@ struct EpiLM {
   float coef2;  // log2(e) / (sqrt(d) tau)
   float inv_sqrt_d;
   __nv_bfloat16* pt;
-  float *pm, *pl, *pS, *pvmax;
-  int* pidx;
+  GroupStat* gst;
   float* logits;
   int M, V;
   int excl;  // vocabulary column left out of the softmax (the [MASK] token), or -1
@@ -341,13 +340,15 @@ struct EpiLM {
       }
       const float l = (l4[0] + l4[1]) + (l4[2] + l4[3]);
       const float S = (S4[0] + S4[1]) + (S4[2] + S4[3]);
-      if (ok) {
-        const size_t o = (size_t)row * NT + g0 / kStatCols;  // [row][group]
-        pm[o] = m2;
-        pl[o] = l;
-        pS[o] = S;
-        pvmax[o] = vmax;
-        pidx[o] = imax;
+      if (ok) {  // one 32-byte record: a whole sector per lane
+        uint32_t rec[16];
+        rec[0] = __float_as_uint(m2);
+        rec[1] = __float_as_uint(l);
+        rec[2] = __float_as_uint(S);
+        rec[3] = __float_as_uint(vmax);
+        rec[4] = (uint32_t)imax;
+        rec[5] = rec[6] = rec[7] = 0u;
+        st_global_v8(reinterpret_cast<uint32_t*>(gst + (size_t)row * NT + g0 / kStatCols), rec, 0);
       }
     }
   }
@@ -1567,8 +1568,8 @@ constexpr int kLmEW = 1, kLmEW8 = 2;
 
 cudaError_t launch_lmhead(const LmArgs& a, StopCtl ctl, int* status, cudaStream_t st) {
   CUtensorMap mA, mB, mBh;  // B boxes: half a vocabulary tile (one CTA of a pair), or half of a half tile
-  EpiLM epi{a.alpha, a.coef2, a.inv_sqrt_d, reinterpret_cast<__nv_bfloat16*>(a.pt), a.pm, a.pl,
-            a.pS, a.pvmax, a.pidx, a.logits, a.M, a.V, a.excl, a.hscale, a.escale, a.ref2, a.rkey};
+  EpiLM epi{a.alpha, a.coef2, a.inv_sqrt_d, reinterpret_cast<__nv_bfloat16*>(a.pt), a.gst, a.logits, a.M, a.V,
+            a.excl, a.hscale, a.escale, a.ref2, a.rkey};
   if (a.E8) {
     // E4M3 codes: 128 one-byte elements per 128-byte row
     if (!make_tmap_2d(&mA, a.h8, (uint64_t)a.d, (uint64_t)a.M, (uint64_t)a.d, 2 * kBK, kBM, true) ||

@@ -235,11 +235,7 @@ dg_status enqueue_step(const StepCtx& c, float tau, float b, float stop_H, uint6
   lm.coef2 = (float)(1.4426950408889634 / (std::sqrt((double)D.d) * (double)tau));
   lm.inv_sqrt_d = (float)(1.0 / std::sqrt((double)D.d));
   lm.pt = at<void>(ws, L.pt);
-  lm.pm = at<float>(ws, L.pm);
-  lm.pl = at<float>(ws, L.pl);
-  lm.pS = at<float>(ws, L.pS);
-  lm.pvmax = at<float>(ws, L.pvmax);
-  lm.pidx = at<int>(ws, L.pidx);
+  lm.gst = at<GroupStat>(ws, L.gst);
   lm.logits = (out && out->debug) ? out->debug->logits : nullptr;
   lm.M = M;
   lm.V = D.V;
@@ -260,7 +256,7 @@ dg_status enqueue_step(const StepCtx& c, float tau, float b, float stop_H, uint6
     DG_TRY(launch_quantize_rows_e4m3(lm.h, M, D.d, at<uint8_t>(ws, L.h8), at<float>(ws, L.hscale), c.st));
   }
   DG_TRY(launch_lmhead(lm, ctl, status, c.st));
-  FixArgs fx{at<void>(ws, L.pt), at<float>(ws, L.pm), lm.ref2, lm.rkey, ref2f, M, D.V};
+  FixArgs fx{at<void>(ws, L.pt), lm.gst, lm.ref2, lm.rkey, ref2f, M, D.V};
   DG_TRY(launch_lm_fix(fx, ctl, c.st));
   DG_TRY(pf.mark(DG_PROF_LMHEAD, 1));
   // fork: statistics, sampler and Gumbel search on the side stream, the
@@ -275,8 +271,7 @@ dg_status enqueue_step(const StepCtx& c, float tau, float b, float stop_H, uint6
     sst = sd->s;
   }
   const Prof ps{pf.ev, sst};
-  StatsArgs sa{at<float>(ws, L.pm), at<float>(ws, L.pl), at<float>(ws, L.pS), at<float>(ws, L.pvmax),
-               at<int>(ws, L.pidx), NT, M, at<double>(ws, L.Hd), at<float>(ws, L.lsum),
+  StatsArgs sa{lm.gst, NT, M, at<double>(ws, L.Hd), at<float>(ws, L.lsum),
                at<float>(ws, L.rowmax), at<int>(ws, L.amax), out ? out->entropy : nullptr,
                out ? out->argmax : nullptr};
   DG_TRY(ps.mark(DG_PROF_STATS, 0));
@@ -316,7 +311,6 @@ dg_status enqueue_step(const StepCtx& c, float tau, float b, float stop_H, uint6
   DG_TRY(ps.mark(DG_PROF_SAMPLER, 1));
   P0Args p0{};
   p0.pt = at<void>(ws, L.pt);
-  p0.pm = at<float>(ws, L.pm);
   p0.rowmax = at<float>(ws, L.rowmax);
   p0.lsum = at<float>(ws, L.lsum);
   p0.acc = at<uint8_t>(ws, L.acc);
@@ -442,11 +436,7 @@ bool ws_layout(const dg_dims& D, int32_t cap, WsLayout* L) {
   L->attn_o = take(4 * (size_t)ns_attn * M * D.Hq * D.hd);
   L->attn_ml = take(8 * (size_t)ns_attn * M * D.Hq);
   L->pt = take(2 * M * (size_t)D.V);
-  L->pm = take(4 * NT * M);
-  L->pl = take(4 * NT * M);
-  L->pS = take(4 * NT * M);
-  L->pvmax = take(4 * NT * M);
-  L->pidx = take(4 * NT * M);
+  L->gst = take(sizeof(GroupStat) * NT * M);
   L->Hd = take(8 * M);
   L->lsum = take(4 * M);
   L->rowmax = take(4 * M);

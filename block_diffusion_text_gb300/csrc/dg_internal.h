@@ -37,7 +37,7 @@ struct WsLayout {
   size_t a, q, kc, vc, o, h;
   size_t attn_o, attn_ml;
   size_t pt;
-  size_t pm, pl, pS, pvmax, pidx;
+  size_t gst;  // per (row, 128-column group) statistics records
   size_t Hd, lsum, rowmax, amax, acc;
   size_t upart, gbest, gidx;
   size_t gpart, gpart_elems;  // split-K partials of the small GEMMs
@@ -112,6 +112,16 @@ cudaError_t launch_qkv(const void* a, const void* Wq, const void* Wk, const void
                        void* k, void* v, int kv_rows, int kv_row0, const float2* rope,
                        const dg_dims& D, StopCtl ctl, int* status, float* part, size_t part_elems,
                        cudaStream_t st);
+// Statistics of one (row, 128-column group) of the LM head, one 32-byte
+// record (a whole sector, written by one 256-bit store): the group maximum m
+// of the tempered logits and l = sum exp2(t - m), S = sum exp2(t - m) (t - m)
+// (log2 units), the largest raw product vmax and its column idx.
+struct GroupStat {
+  float m, l, S, vmax;
+  int idx, pad0, pad1, pad2;
+};
+static_assert(sizeof(GroupStat) == 32, "one sector per record");
+
 // LM head with the statistics epilogue.
 struct LmArgs {
   const void* h;       // bf16 [M][d]
@@ -120,8 +130,7 @@ struct LmArgs {
   float coef2;         // log2(e) / (sqrt(d) tau)
   float inv_sqrt_d;
   void* pt;            // bf16 [M][V]  exp(s - m_tile)
-  float *pm, *pl, *pS, *pvmax;
-  int* pidx;           // [M][NT] (with pm, pl, pS, pvmax)
+  GroupStat* gst;      // [M][NT] statistics of each 128-column group
   float* logits;       // optional fp32 [M][V]
   int M, V, d;
   int excl;            // column left out of the softmax (masked decoding's [MASK]), or -1
@@ -170,7 +179,7 @@ cudaError_t launch_lm_ref(const RefArgs& a, StopCtl ctl, cudaStream_t st);
 // Rewrite of the flagged rows' tiles against their maximum (see kRefSpan).
 struct FixArgs {
   void* pt;                    // bf16 [M][V] tiles
-  const float* pm;             // [M][NT] group maxima (log2 units)
+  const GroupStat* gst;        // [M][NT] group statistics (the maxima m, log2 units)
   const float* ref2;           // [M] the LM head's reference
   const unsigned* rkey;        // [M] 0, or the key of the row's maximum
   float* ref2f;                // [M] final reference (flagged rows: their maximum)
@@ -250,7 +259,6 @@ int selfcond_active_splits(const dg_dims& D);
 constexpr int kGumbelChunk = 4096;
 struct P0Args {
   const void* pt;        // bf16 [M][V]: the tiles, exp2(t - ref2f)
-  const float* pm;       // [M][NT]  group maxima m_g (log2 units)
   const float* rowmax;   // [M]  row maximum m (log2 units)
   const float* lsum;     // [M]  Z
   const uint8_t* acc;    // [M]
@@ -289,8 +297,7 @@ cudaError_t launch_embed_rmsnorm(const int32_t* tokens, const void* E, const voi
                                  float2* rope, const dg_dims& D, int rows, int P, StopCtl ctl,
                                  int* status, cudaStream_t st, const void* src = nullptr);
 struct StatsArgs {
-  const float *pm, *pl, *pS, *pvmax;
-  const int* pidx;
+  const GroupStat* gst;  // [M][NT]
   int NT, M;
   double* Hd;            // [M]
   float* lsum;           // [M]  Z

@@ -248,11 +248,18 @@ __global__ void __launch_bounds__(kStatsThreads) stats_kernel(StatsArgs a, int w
     for (int t = t0; t < a.NT; t += 2 * tstep) {
       const int t2 = t + tstep;
       const bool has2 = t2 < a.NT;
-      const float m1 = a.pm[base + t], l1 = a.pl[base + t], S1 = a.pS[base + t], v1 = a.pvmax[base + t];
-      const int i1 = a.pidx[base + t];
-      const float m2 = has2 ? a.pm[base + t2] : -FLT_MAX, l2 = has2 ? a.pl[base + t2] : 0.f;
-      const float S2 = has2 ? a.pS[base + t2] : 0.f, v2 = has2 ? a.pvmax[base + t2] : -FLT_MAX;
-      const int i2 = has2 ? a.pidx[base + t2] : INT_MAX;
+      const float4* r1 = reinterpret_cast<const float4*>(a.gst + base + t);
+      const float4 x1 = r1[0], y1 = r1[1];
+      float4 x2 = make_float4(-FLT_MAX, 0.f, 0.f, -FLT_MAX), y2 = make_float4(__int_as_float(INT_MAX), 0.f, 0.f, 0.f);
+      if (has2) {
+        const float4* r2 = reinterpret_cast<const float4*>(a.gst + base + t2);
+        x2 = r2[0];
+        y2 = r2[1];
+      }
+      const float m1 = x1.x, l1 = x1.y, S1 = x1.z, v1 = x1.w;
+      const int i1 = __float_as_int(y1.x);
+      const float m2 = x2.x, l2 = x2.y, S2 = x2.z, v2 = x2.w;
+      const int i2 = __float_as_int(y2.x);
       if (v1 > vbest || (v1 == vbest && i1 < ibest)) {
         vbest = v1;
         ibest = i1;
@@ -922,7 +929,7 @@ __global__ void __launch_bounds__(kFixThreads) lm_fix_kernel(FixArgs a, StopCtl 
   const int v0 = blockIdx.x * per, v1 = min(a.V, v0 + per);
   __nv_bfloat16* pt = reinterpret_cast<__nv_bfloat16*>(a.pt) + (size_t)row * a.V;
   for (int v = v0 + threadIdx.x * 8; v < v1; v += kFixThreads * 8) {  // V is a multiple of 8
-    const float mg = a.pm[(size_t)row * NT + v / kStatCols];
+    const float mg = a.gst[(size_t)row * NT + v / kStatCols].m;
     const float f = exp2f((mg - R <= kRefSpan ? R : mg) - Rn);
     uint4 x = *reinterpret_cast<const uint4*>(pt + v);
     const __nv_bfloat16* xb = reinterpret_cast<const __nv_bfloat16*>(&x);
