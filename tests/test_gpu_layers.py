@@ -42,6 +42,16 @@ def test_two_layer_step_tensor_core_attention():
     _run_and_compare(dims, 32, tau=0.7, entropy_given_h=True, e2e_bound=LAYERS_H_BOUND)
 
 
+def test_two_layer_step_split_k_clusters():
+    """d = 2048, 128 canvas rows, two layers: each layer's q/k/v projection runs on clusters of four
+    K slices (128-column tiles, RoPE in the owner's epilogue), FFW1 on 64-column tiles over four
+    slices with GELU; the tensor-core attention reads a 128-row prefix."""
+    dims = synth.Dims(V=1000, d=2048, C=64, B=2, Hq=4, Hkv=2, hd=128, F=1024, P=128, cap=192, L=2)
+    g = torch.Generator().manual_seed(35)
+    z = (torch.randn(dims.B, dims.C, dims.d, generator=g) * 0.02).to(torch.bfloat16)
+    _run_and_compare(dims, 35, tau=0.7, step=1, z_in=z, entropy_given_h=True, e2e_bound=LAYERS_H_BOUND)
+
+
 def _model(dims, seed):
     from block_diffusion_text_gb300 import dg
     w = synth.make_weights(dims, seed, device="cpu")
@@ -55,13 +65,14 @@ def _check_caches(ck, tag, Kd, Vd, Kr, Vr, rows):
         ck(check_close_bf16, f"{tag} V layer {l}", Vd[l][:, :, rows], Vr[l][:, :, rows], ulps=u)
 
 
-@pytest.mark.parametrize("hd", [64, 128])
-def test_prefill_matches_oracle_in_pieces(hd):
+@pytest.mark.parametrize("hd,d", [(64, 128), (128, 128), (128, 2048)])
+def test_prefill_matches_oracle_in_pieces(hd, d):
     """A 100-token prompt into an empty three-layer cache: three pieces of at most C = 40 tokens, each
     attending causally over everything before it; every layer's rows against the oracle's one pass,
-    the rows past the prompt untouched, and the length advanced."""
+    the rows past the prompt untouched, and the length advanced.  At d = 2048 each piece's k/v
+    projection runs on split-K clusters."""
     from block_diffusion_text_gb300 import dg
-    dims = synth.Dims(V=1000, d=128, C=40, B=2, Hq=4, Hkv=2, hd=hd, F=192, P=0, cap=160, L=3)
+    dims = synth.Dims(V=1000, d=d, C=40, B=2, Hq=4, Hkv=2, hd=hd, F=192, P=0, cap=160, L=3)
     w, model = _model(dims, 33)
     tok = torch.randint(0, dims.V, (dims.B, 100), dtype=torch.int32, generator=torch.Generator().manual_seed(3))
     n = dg.prefill(model, tok.cuda())
