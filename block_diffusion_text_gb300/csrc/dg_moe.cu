@@ -50,15 +50,29 @@ __global__ void __launch_bounds__(kTopkRows * 32) moe_topk_kernel(MoeRouteArgs a
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int row = blockIdx.x * kTopkRows + warp;
   if (row >= a.M) return;
+  // the row's logits, summed over the K splits in order; the loads of four
+  // splits of every expert of the lane are in flight at once
   float l[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) l[j] = 0.f;
+  for (int sp0 = 0; sp0 < ksplit; sp0 += 4) {
+    float t[8][4];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int e = lane + 32 * j;
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        t[j][k] = (e < a.n_exp && sp0 + k < ksplit) ? part[((size_t)(sp0 + k) * a.M + row) * a.n_exp + e] : 0.f;
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) l[j] += t[j][k];
+  }
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
     const int e = lane + 32 * j;
-    float v = 0.f;
-    if (e < a.n_exp)
-      for (int sp = 0; sp < ksplit; ++sp) v += part[((size_t)sp * a.M + row) * a.n_exp + e];
-    l[j] = v;
-    if (a.dbg_logits && e < a.n_exp) a.dbg_logits[(size_t)row * a.n_exp + e] = v;
+    if (a.dbg_logits && e < a.n_exp) a.dbg_logits[(size_t)row * a.n_exp + e] = l[j];
   }
   uint32_t taken = 0;
   float top = 0.f, Z = 0.f;
@@ -243,13 +257,32 @@ __global__ void __launch_bounds__(256) moe_combine_kernel(__nv_bfloat16* h, cons
   const int c8 = (blockIdx.x * blockDim.x + threadIdx.x) * 8;
   if (c8 >= d || !canvas_active(ctl.stop_at, row / C, ctl.step)) return;
   const int R = M * K1;
+  // the row's slots first (one round trip), then the loads of up to eight
+  // gated outputs in flight at once, summed in rank order
+  int ps[kMoeMaxTopK + 1];
+#pragma unroll
+  for (int j = 0; j < kMoeMaxTopK + 1; ++j)
+    ps[j] = j < K1 ? min(max(slot[(size_t)row * K1 + j], 0), R - 1) : 0;
   float s[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-  for (int j = 0; j < K1; ++j) {
-    const int p = min(max(slot[(size_t)row * K1 + j], 0), R - 1);
-    const float4* src = reinterpret_cast<const float4*>(yp + (size_t)p * d + c8);
-    const float4 u = src[0], v = src[1];
-    s[0] += u.x; s[1] += u.y; s[2] += u.z; s[3] += u.w;
-    s[4] += v.x; s[5] += v.y; s[6] += v.z; s[7] += v.w;
+#pragma unroll
+  for (int j0 = 0; j0 < kMoeMaxTopK + 1; j0 += 8) {
+    if (j0 >= K1) break;
+    float4 u[8], v[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      if (j0 + k < K1) {
+        const float4* src = reinterpret_cast<const float4*>(yp + (size_t)ps[j0 + k] * d + c8);
+        u[k] = src[0];
+        v[k] = src[1];
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      if (j0 + k < K1) {
+        s[0] += u[k].x; s[1] += u[k].y; s[2] += u[k].z; s[3] += u[k].w;
+        s[4] += v[k].x; s[5] += v[k].y; s[6] += v[k].z; s[7] += v[k].w;
+      }
+    }
   }
   uint4* hp = reinterpret_cast<uint4*>(h + (size_t)row * d + c8);
   float hv[8];
