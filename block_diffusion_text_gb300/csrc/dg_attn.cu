@@ -231,6 +231,7 @@ constexpr int kCombineRows = 8;
 
 template <int HD>
 __global__ void __launch_bounds__(32 * kCombineRows) attn_combine_kernel(AttnArgs a, int nsplit, StopCtl ctl) {
+  pdl_trigger();
   pdl_wait();
   if (all_stopped(ctl.stop_at, ctl.B, ctl.step)) return;
   constexpr int VEC = HD / 32;

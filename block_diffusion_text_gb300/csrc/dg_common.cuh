@@ -33,11 +33,16 @@ DG_DEV uint64_t globaltimer() {
 // ---------------------------------------------- programmatic launches ----
 // Every kernel of the library begins with pdl_wait(): wait until the kernel
 // before it in the stream has completed and its writes are visible (a no-op
-// when launched without programmatic serialisation).  No kernel triggers its
-// dependents early: CTAs of the next kernel parked on the SMs while this one
-// runs cost more than the launch latency they hide (measured), so the next
-// launch begins as this kernel's CTAs retire.
+// when launched without programmatic serialisation).  The short kernels on the
+// step's critical path (embedding, attention merge, tile reference, flagged-row
+// rewrite, reduce) call pdl_trigger() first, so that the GEMM or attention
+// after them is launched while they run and its CTAs wait on the SMs they
+// leave free; the long kernels do not, since CTAs of the next kernel parked
+// beside them cost more than the launch latency they hide (measured).
+// pdl_trigger() only allows the launch: the dependent's pdl_wait() still
+// waits for this kernel's completion.
 DG_DEV void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+DG_DEV void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 // ------------------------------------------------------------- mbarrier ----
 DG_DEV void mbar_init(uint64_t* bar, uint32_t count) {

@@ -63,6 +63,7 @@ __global__ void __launch_bounds__(kEmbThreads)
     embed_rmsnorm_kernel(const int32_t* tokens, const __nv_bfloat16* E, const __nv_bfloat16* z,
                          __nv_bfloat16* a, float2* rope, int d, int V, float eps, int C, int P, int hd,
                          RopeTheta theta, StopCtl ctl, int* status, const __nv_bfloat16* src) {
+  pdl_trigger();
   pdl_wait();
   if (all_stopped(ctl.stop_at, ctl.B, ctl.step)) return;
   const int row = blockIdx.x;
@@ -664,6 +665,7 @@ cudaError_t launch_fill_tokens(int32_t* tokens, int n, int value, cudaStream_t s
 constexpr int kReduceCols = 128;
 
 __global__ void __launch_bounds__(kReduceCols) reduce_kernel(ReduceArgs a, StopCtl ctl) {
+  pdl_trigger();
   pdl_wait();
   if (all_stopped(ctl.stop_at, ctl.B, ctl.step)) return;
   const int row = blockIdx.x;
@@ -854,6 +856,7 @@ cudaError_t launch_quantize_rows_e4m3(const void* X, int R, int d, uint8_t* Q, f
 // (never the excluded column, so that R is at most the row's maximum); clears
 // the row's flag.
 __global__ void __launch_bounds__(128) lm_ref_kernel(RefArgs a, StopCtl ctl) {
+  pdl_trigger();
   pdl_wait();
   if (all_stopped(ctl.stop_at, ctl.B, ctl.step)) return;
   const int row = blockIdx.x;
@@ -917,6 +920,7 @@ cudaError_t launch_lm_ref(const RefArgs& a, StopCtl ctl, cudaStream_t st) {
 constexpr int kFixSplit = 4;
 constexpr int kFixThreads = 256;
 __global__ void __launch_bounds__(kFixThreads) lm_fix_kernel(FixArgs a, StopCtl ctl) {
+  pdl_trigger();
   pdl_wait();
   if (all_stopped(ctl.stop_at, ctl.B, ctl.step)) return;
   const int row = blockIdx.y;
