@@ -40,7 +40,12 @@ DG_DEV uint64_t globaltimer() {
 // leave free; the long kernels do not, since CTAs of the next kernel parked
 // beside them cost more than the launch latency they hide (measured).
 // pdl_trigger() only allows the launch: the dependent's pdl_wait() still
-// waits for this kernel's completion.
+// waits for this kernel's completion.  The tensor-core GEMM kernels call
+// pdl_wait() after their prologue (barrier initialisation, TMEM allocation,
+// cluster synchronisation), which reads nothing the kernel before wrote, so
+// that the prologue of a GEMM launched early overlaps the short kernel
+// before it.  No kernel that holds TMEM triggers early, so such a prologue
+// never waits on TMEM held by a kernel still running.
 DG_DEV void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 DG_DEV void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 

@@ -374,9 +374,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 const __grid_constant__ CUtensorMap mB1, const __grid_constant__ CUtensorMap mB2,
                 int nb0, int nb1, int b_sub, int M, int N, int K, int ksplit, uint32_t b_lbo,
                 uint32_t b_sbo, Epi epi, int* status, StopCtl ctl) {
-  pdl_wait();
   using L = GemmLayout<BN, STAGES, B_MN>;
-  if (all_stopped(ctl.stop_at, ctl.B, ctl.step)) return;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kBar);
@@ -418,110 +416,115 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 0) {
-    if (lane == 0) {
-      tma_prefetch(&mA);
-      tma_prefetch(&mB0);
-      int stage = 0;
-      uint32_t phase = 0;
-      bool alive = true;
-      for (int tile = blockIdx.x; tile < num_tiles && alive; tile += gridDim.x) {
-        const int tmn = tile % num_mn;
-        const int m0 = (tmn % num_m) * kBM, n0 = (tmn / num_m) * BN;
-        int kb_lo, kb_hi;
-        krange(tile, kb_lo, kb_hi);
-        for (int kb = kb_lo; kb < kb_hi; ++kb) {
-          if (!mbar_wait(&empty[stage], phase ^ 1, status, abort)) {
-            alive = false;
-            break;
-          }
-          uint8_t* sa = smem + stage * L::kStage;
-          uint8_t* sb = sa + L::kA;
-          mbar_arrive_expect_tx(&full[stage], L::kStage);
-          tma_load_2d(sa, &mA, &full[stage], kb * kBK, m0);
-          if (!B_MN) {
-            for (int r = 0; r < BN; r += b_sub) {
-              const int n = n0 + r;
-              const CUtensorMap* mb = &mB0;
-              int nb = n;
-              if (n >= nb0 + nb1) {
-                mb = &mB2;
-                nb = n - nb0 - nb1;
-              } else if (n >= nb0) {
-                mb = &mB1;
-                nb = n - nb0;
-              }
-              tma_load_2d(sb + r * 128, mb, &full[stage], kb * kBK, nb);
+  // The prologue above overlaps the kernel before this one when that one
+  // triggers its dependents early; its results are read only from here on.
+  pdl_wait();
+  if (!all_stopped(ctl.stop_at, ctl.B, ctl.step)) {
+    if (warp == 0) {
+      if (lane == 0) {
+        tma_prefetch(&mA);
+        tma_prefetch(&mB0);
+        int stage = 0;
+        uint32_t phase = 0;
+        bool alive = true;
+        for (int tile = blockIdx.x; tile < num_tiles && alive; tile += gridDim.x) {
+          const int tmn = tile % num_mn;
+          const int m0 = (tmn % num_m) * kBM, n0 = (tmn / num_m) * BN;
+          int kb_lo, kb_hi;
+          krange(tile, kb_lo, kb_hi);
+          for (int kb = kb_lo; kb < kb_hi; ++kb) {
+            if (!mbar_wait(&empty[stage], phase ^ 1, status, abort)) {
+              alive = false;
+              break;
             }
-          } else {
-#pragma unroll
-            for (int j = 0; j < BN / 64; ++j)
-              tma_load_2d(sb + j * (kBK * 128), &mB0, &full[stage], n0 + 64 * j, kb * kBK);
-          }
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1;
+            uint8_t* sa = smem + stage * L::kStage;
+            uint8_t* sb = sa + L::kA;
+            mbar_arrive_expect_tx(&full[stage], L::kStage);
+            tma_load_2d(sa, &mA, &full[stage], kb * kBK, m0);
+            if (!B_MN) {
+              for (int r = 0; r < BN; r += b_sub) {
+                const int n = n0 + r;
+                const CUtensorMap* mb = &mB0;
+                int nb = n;
+                if (n >= nb0 + nb1) {
+                  mb = &mB2;
+                  nb = n - nb0 - nb1;
+                } else if (n >= nb0) {
+                  mb = &mB1;
+                  nb = n - nb0;
+                }
+                tma_load_2d(sb + r * 128, mb, &full[stage], kb * kBK, nb);
+              }
+            } else {
+  #pragma unroll
+              for (int j = 0; j < BN / 64; ++j)
+                tma_load_2d(sb + j * (kBK * 128), &mB0, &full[stage], n0 + 64 * j, kb * kBK);
+            }
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1;
+            }
           }
         }
       }
-    }
-  } else if (warp == 1) {
-    if (lane == 0) {  // one thread waits and issues; the MMAs need no other lane
-      constexpr uint32_t idesc = idesc_bf16(kBM, BN, B_MN);
-      int stage = 0;
-      uint32_t phase = 0;
-      bool alive = true;
+    } else if (warp == 1) {
+      if (lane == 0) {  // one thread waits and issues; the MMAs need no other lane
+        constexpr uint32_t idesc = idesc_bf16(kBM, BN, B_MN);
+        int stage = 0;
+        uint32_t phase = 0;
+        bool alive = true;
+        int it = 0;
+        for (int tile = blockIdx.x; tile < num_tiles && alive; tile += gridDim.x, ++it) {
+          const int acc = it & 1;
+          const uint32_t aph = (it >> 1) & 1;
+          if (!mbar_wait(&tempty[acc], aph ^ 1, status, abort)) break;
+          tc_fence_after();
+          const uint32_t dt = tmem + acc * BN;
+          int kb_lo, kb_hi;
+          krange(tile, kb_lo, kb_hi);
+          for (int kb = kb_lo; kb < kb_hi; ++kb) {
+            if (!mbar_wait(&full[stage], phase, status, abort)) {
+              alive = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t sa = smem_u32(smem + stage * L::kStage);
+            const uint32_t sb = sa + L::kA;
+  #pragma unroll
+            for (int kk = 0; kk < kBK / 16; ++kk) {
+              const uint64_t ad = sdesc_sw128(sa + kk * 32, 16, 1024);
+              const uint64_t bd = B_MN ? sdesc_sw128(sb + kk * 2048, b_lbo, b_sbo)
+                                       : sdesc_sw128(sb + kk * 32, 16, 1024);
+              umma_bf16(dt, ad, bd, idesc, (kb != kb_lo || kk != 0) ? 1u : 0u);
+            }
+            umma_commit(&empty[stage]);
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1;
+            }
+          }
+          if (alive) umma_commit(&tfull[acc]);
+        }
+      }
+      __syncwarp();
+    } else {
+      const int q = warp & 3;  // TMEM lane quarter this warp may read
+      const int r_local = q * 32 + lane;
       int it = 0;
-      for (int tile = blockIdx.x; tile < num_tiles && alive; tile += gridDim.x, ++it) {
+      for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++it) {
         const int acc = it & 1;
         const uint32_t aph = (it >> 1) & 1;
-        if (!mbar_wait(&tempty[acc], aph ^ 1, status, abort)) break;
+        if (!mbar_wait_warp(&tfull[acc], aph, status, abort)) break;
         tc_fence_after();
-        const uint32_t dt = tmem + acc * BN;
-        int kb_lo, kb_hi;
-        krange(tile, kb_lo, kb_hi);
-        for (int kb = kb_lo; kb < kb_hi; ++kb) {
-          if (!mbar_wait(&full[stage], phase, status, abort)) {
-            alive = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t sa = smem_u32(smem + stage * L::kStage);
-          const uint32_t sb = sa + L::kA;
-#pragma unroll
-          for (int kk = 0; kk < kBK / 16; ++kk) {
-            const uint64_t ad = sdesc_sw128(sa + kk * 32, 16, 1024);
-            const uint64_t bd = B_MN ? sdesc_sw128(sb + kk * 2048, b_lbo, b_sbo)
-                                     : sdesc_sw128(sb + kk * 32, 16, 1024);
-            umma_bf16(dt, ad, bd, idesc, (kb != kb_lo || kk != 0) ? 1u : 0u);
-          }
-          umma_commit(&empty[stage]);
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1;
-          }
-        }
-        if (alive) umma_commit(&tfull[acc]);
+        const int tmn = tile % num_mn;
+        const int m0 = (tmn % num_m) * kBM, n0 = (tmn / num_m) * BN;
+        const int row = m0 + r_local;
+        const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
+        auto ld = [&](int c, float(&v)[32]) { tmem_ld32(tb + c * 32, v); };
+        epi.template tile<BN>(row, row < M, n0, N, ld, tile / num_mn);
+        tc_fence_before();
+        mbar_arrive(&tempty[acc]);
       }
-    }
-    __syncwarp();
-  } else {
-    const int q = warp & 3;  // TMEM lane quarter this warp may read
-    const int r_local = q * 32 + lane;
-    int it = 0;
-    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++it) {
-      const int acc = it & 1;
-      const uint32_t aph = (it >> 1) & 1;
-      if (!mbar_wait_warp(&tfull[acc], aph, status, abort)) break;
-      tc_fence_after();
-      const int tmn = tile % num_mn;
-      const int m0 = (tmn % num_m) * kBM, n0 = (tmn / num_m) * BN;
-      const int row = m0 + r_local;
-      const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
-      auto ld = [&](int c, float(&v)[32]) { tmem_ld32(tb + c * 32, v); };
-      epi.template tile<BN>(row, row < M, n0, N, ld, tile / num_mn);
-      tc_fence_before();
-      mbar_arrive(&tempty[acc]);
     }
   }
   __syncthreads();
@@ -561,9 +564,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_ksum_kernel(const __grid_constant__ CUtensorMap mA, const __grid_constant__ CUtensorMap mB0,
                      const __grid_constant__ CUtensorMap mB1, const __grid_constant__ CUtensorMap mB2,
                      int nb0, int nb1, int b_sub, int M, int N, int K, Epi epi, int* status, StopCtl ctl) {
-  pdl_wait();
   using L = KsumLayout<BN, STAGES, KS>;
-  if (all_stopped(ctl.stop_at, ctl.B, ctl.step)) return;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   float* recv = reinterpret_cast<float*>(smem + STAGES * L::kStage);
@@ -602,106 +603,111 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 0) {
-    if (lane == 0) {
-      tma_prefetch(&mA);
-      tma_prefetch(&mB0);
-      int stage = 0;
-      uint32_t phase = 0;
-      for (int kb = kb_lo; kb < kb_hi; ++kb) {
-        if (!mbar_wait(&empty[stage], phase ^ 1, status, abort)) break;
-        uint8_t* sa = smem + stage * L::kStage;
-        uint8_t* sb = sa + L::kA;
-        mbar_arrive_expect_tx(&full[stage], L::kStage);
-        tma_load_2d(sa, &mA, &full[stage], kb * kBK, m0);
-        for (int r = 0; r < BN; r += b_sub) {
-          const int n = n0 + r;
-          const CUtensorMap* mb = &mB0;
-          int nb = n;
-          if (n >= nb0 + nb1) {
-            mb = &mB2;
-            nb = n - nb0 - nb1;
-          } else if (n >= nb0) {
-            mb = &mB1;
-            nb = n - nb0;
-          }
-          tma_load_2d(sb + r * 128, mb, &full[stage], kb * kBK, nb);
-        }
-        if (++stage == STAGES) {
-          stage = 0;
-          phase ^= 1;
-        }
-      }
-    }
-    __syncwarp();
-  } else if (warp == 1) {
-    if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16(kBM, BN, false);
-      int stage = 0;
-      uint32_t phase = 0;
-      bool alive = true;
-      for (int kb = kb_lo; kb < kb_hi; ++kb) {
-        if (!mbar_wait(&full[stage], phase, status, abort)) {
-          alive = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t sa = smem_u32(smem + stage * L::kStage);
-        const uint32_t sb = sa + L::kA;
-#pragma unroll
-        for (int kk = 0; kk < kBK / 16; ++kk) {
-          const uint64_t ad = sdesc_sw128(sa + kk * 32, 16, 1024);
-          const uint64_t bd = sdesc_sw128(sb + kk * 32, 16, 1024);
-          umma_bf16(tmem, ad, bd, idesc, (kb != kb_lo || kk != 0) ? 1u : 0u);
-        }
-        umma_commit(&empty[stage]);
-        if (++stage == STAGES) {
-          stage = 0;
-          phase ^= 1;
-        }
-      }
-      if (alive) umma_commit(tfull);
-    }
-    __syncwarp();
-  } else {
-    const int q = warp & 3;  // TMEM lane quarter this warp may read
-    const int r_local = q * 32 + lane;
-    const int owner = q * KS / 4;
-    const int lr = r_local - owner * L::kOwned;  // row within the owner's block
-    const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16);
-    if (mbar_wait_warp(tfull, 0, status, abort)) {
-      tc_fence_after();
-      if (owner != rank) {
-        const int slot = rank < owner ? rank : rank - 1;
-        const uint32_t dst = cluster_addr(recv + ((size_t)slot * L::kOwned + lr) * L::kLd, (uint32_t)owner);
-#pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
-          float v[32];
-          tmem_ld32(tb + c * 32, v);
-#pragma unroll
-          for (int j = 0; j < 8; ++j)
-            st_cluster_v4(dst + (uint32_t)((c * 32 + 4 * j) * 4), v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-        }
-        mbar_arrive_cluster_release(cluster_addr(&rbar[q], (uint32_t)owner));
-      } else if (mbar_wait_warp<true>(&rbar[q], 0, status, abort)) {
-        const float* own = recv + (size_t)lr * L::kLd;
-        auto ld = [&](int c, float(&v)[32]) {
-          tmem_ld32(tb + c * 32, v);
-#pragma unroll
-          for (int s = 0; s < KS - 1; ++s) {
-            const float4* src = reinterpret_cast<const float4*>(own + (size_t)s * L::kOwned * L::kLd + c * 32);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              const float4 x = src[j];
-              v[4 * j] += x.x;
-              v[4 * j + 1] += x.y;
-              v[4 * j + 2] += x.z;
-              v[4 * j + 3] += x.w;
+  // The prologue above overlaps the kernel before this one when that one
+  // triggers its dependents early; its results are read only from here on.
+  pdl_wait();
+  if (!all_stopped(ctl.stop_at, ctl.B, ctl.step)) {
+    if (warp == 0) {
+      if (lane == 0) {
+        tma_prefetch(&mA);
+        tma_prefetch(&mB0);
+        int stage = 0;
+        uint32_t phase = 0;
+        for (int kb = kb_lo; kb < kb_hi; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1, status, abort)) break;
+          uint8_t* sa = smem + stage * L::kStage;
+          uint8_t* sb = sa + L::kA;
+          mbar_arrive_expect_tx(&full[stage], L::kStage);
+          tma_load_2d(sa, &mA, &full[stage], kb * kBK, m0);
+          for (int r = 0; r < BN; r += b_sub) {
+            const int n = n0 + r;
+            const CUtensorMap* mb = &mB0;
+            int nb = n;
+            if (n >= nb0 + nb1) {
+              mb = &mB2;
+              nb = n - nb0 - nb1;
+            } else if (n >= nb0) {
+              mb = &mB1;
+              nb = n - nb0;
             }
+            tma_load_2d(sb + r * 128, mb, &full[stage], kb * kBK, nb);
           }
-        };
-        const int row = m0 + r_local;
-        epi.template tile<BN>(row, row < M, n0, N, ld, 0);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      __syncwarp();
+    } else if (warp == 1) {
+      if (lane == 0) {
+        constexpr uint32_t idesc = idesc_bf16(kBM, BN, false);
+        int stage = 0;
+        uint32_t phase = 0;
+        bool alive = true;
+        for (int kb = kb_lo; kb < kb_hi; ++kb) {
+          if (!mbar_wait(&full[stage], phase, status, abort)) {
+            alive = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + stage * L::kStage);
+          const uint32_t sb = sa + L::kA;
+  #pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk) {
+            const uint64_t ad = sdesc_sw128(sa + kk * 32, 16, 1024);
+            const uint64_t bd = sdesc_sw128(sb + kk * 32, 16, 1024);
+            umma_bf16(tmem, ad, bd, idesc, (kb != kb_lo || kk != 0) ? 1u : 0u);
+          }
+          umma_commit(&empty[stage]);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (alive) umma_commit(tfull);
+      }
+      __syncwarp();
+    } else {
+      const int q = warp & 3;  // TMEM lane quarter this warp may read
+      const int r_local = q * 32 + lane;
+      const int owner = q * KS / 4;
+      const int lr = r_local - owner * L::kOwned;  // row within the owner's block
+      const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16);
+      if (mbar_wait_warp(tfull, 0, status, abort)) {
+        tc_fence_after();
+        if (owner != rank) {
+          const int slot = rank < owner ? rank : rank - 1;
+          const uint32_t dst = cluster_addr(recv + ((size_t)slot * L::kOwned + lr) * L::kLd, (uint32_t)owner);
+  #pragma unroll 1
+          for (int c = 0; c < BN / 32; ++c) {
+            float v[32];
+            tmem_ld32(tb + c * 32, v);
+  #pragma unroll
+            for (int j = 0; j < 8; ++j)
+              st_cluster_v4(dst + (uint32_t)((c * 32 + 4 * j) * 4), v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+          }
+          mbar_arrive_cluster_release(cluster_addr(&rbar[q], (uint32_t)owner));
+        } else if (mbar_wait_warp<true>(&rbar[q], 0, status, abort)) {
+          const float* own = recv + (size_t)lr * L::kLd;
+          auto ld = [&](int c, float(&v)[32]) {
+            tmem_ld32(tb + c * 32, v);
+  #pragma unroll
+            for (int s = 0; s < KS - 1; ++s) {
+              const float4* src = reinterpret_cast<const float4*>(own + (size_t)s * L::kOwned * L::kLd + c * 32);
+  #pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                const float4 x = src[j];
+                v[4 * j] += x.x;
+                v[4 * j + 1] += x.y;
+                v[4 * j + 2] += x.z;
+                v[4 * j + 3] += x.w;
+              }
+            }
+          };
+          const int row = m0 + r_local;
+          epi.template tile<BN>(row, row < M, n0, N, ld, 0);
+        }
       }
     }
   }
@@ -1068,13 +1074,11 @@ __global__ void __launch_bounds__(64 + 128 * EW, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap mA, const __grid_constant__ CUtensorMap mB,
                      const __grid_constant__ CUtensorMap mBh, int M, int N, int K, int ksplit, Epi epi,
                      int* status, StopCtl ctl) {
-  pdl_wait();
   using L = PairLayout<BN, STAGES, B_MN>;
   constexpr int KBE = F8 ? 2 * kBK : kBK;  // K elements per stage
   static_assert(!B_MN || (BN / 2) % 64 == 0, "MN-major B halves are whole 64-column blocks");
   static_assert(!TAIL || !B_MN, "half tiles are loaded K-major");
   static_assert(!F8 || !B_MN, "E4M3 operands are loaded K-major");
-  if (all_stopped(ctl.stop_at, ctl.B, ctl.step)) return;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kBar);
@@ -1132,127 +1136,132 @@ __global__ void __launch_bounds__(64 + 128 * EW, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 0) {
-    if (lane == 0) {
-      tma_prefetch(&mA);
-      tma_prefetch(&mB);
-      int stage = 0;
-      uint32_t phase = 0;
-      bool alive = true;
-      for (int tile = cid; tile < num_tiles && alive; tile += ncl) {
-        int m0, n0, kb_lo, kb_hi, width;
-        coords(tile, m0, n0, kb_lo, kb_hi, width);
-        const int arow = m0 + (int)rank * kBM, bcol = n0 + (int)rank * (width / 2);
-        for (int kb = kb_lo; kb < kb_hi; ++kb) {
-          if (!mbar_wait(&empty[stage], phase ^ 1, status, abort)) {
-            alive = false;
-            break;
+  // The prologue above overlaps the kernel before this one when that one
+  // triggers its dependents early; its results are read only from here on.
+  pdl_wait();
+  if (!all_stopped(ctl.stop_at, ctl.B, ctl.step)) {
+    if (warp == 0) {
+      if (lane == 0) {
+        tma_prefetch(&mA);
+        tma_prefetch(&mB);
+        int stage = 0;
+        uint32_t phase = 0;
+        bool alive = true;
+        for (int tile = cid; tile < num_tiles && alive; tile += ncl) {
+          int m0, n0, kb_lo, kb_hi, width;
+          coords(tile, m0, n0, kb_lo, kb_hi, width);
+          const int arow = m0 + (int)rank * kBM, bcol = n0 + (int)rank * (width / 2);
+          for (int kb = kb_lo; kb < kb_hi; ++kb) {
+            if (!mbar_wait(&empty[stage], phase ^ 1, status, abort)) {
+              alive = false;
+              break;
+            }
+            uint8_t* sa = smem + stage * L::kStage;
+            uint8_t* sb = sa + L::kA;
+            if (leader) mbar_arrive_expect_tx(&full[stage], 2 * (L::kA + (width / 2) * kBK * 2));
+            const uint32_t bar = cluster_addr(&full[stage], 0);
+            tma_load_2d_pair(sa, &mA, bar, kb * KBE, arow);
+            if (!B_MN) {
+              tma_load_2d_pair(sb, width == BN ? &mB : &mBh, bar, kb * KBE, bcol);
+            } else {
+  #pragma unroll
+              for (int j = 0; j < BN / 128; ++j)
+                tma_load_2d_pair(sb + j * (kBK * 128), &mB, bar, bcol + 64 * j, kb * kBK);
+            }
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1;
+            }
           }
-          uint8_t* sa = smem + stage * L::kStage;
-          uint8_t* sb = sa + L::kA;
-          if (leader) mbar_arrive_expect_tx(&full[stage], 2 * (L::kA + (width / 2) * kBK * 2));
-          const uint32_t bar = cluster_addr(&full[stage], 0);
-          tma_load_2d_pair(sa, &mA, bar, kb * KBE, arow);
-          if (!B_MN) {
-            tma_load_2d_pair(sb, width == BN ? &mB : &mBh, bar, kb * KBE, bcol);
-          } else {
-#pragma unroll
-            for (int j = 0; j < BN / 128; ++j)
-              tma_load_2d_pair(sb + j * (kBK * 128), &mB, bar, bcol + 64 * j, kb * kBK);
-          }
+        }
+        // Wait until the leader's MMAs released every stage, so that no commit
+        // is still on its way to this CTA's barriers when it exits.
+        for (int i = 0; i < STAGES && alive; ++i) {
+          if (!mbar_wait(&empty[stage], phase ^ 1, status, abort)) break;
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1;
           }
         }
       }
-      // Wait until the leader's MMAs released every stage, so that no commit
-      // is still on its way to this CTA's barriers when it exits.
-      for (int i = 0; i < STAGES && alive; ++i) {
-        if (!mbar_wait(&empty[stage], phase ^ 1, status, abort)) break;
-        if (++stage == STAGES) {
-          stage = 0;
-          phase ^= 1;
+    } else if (warp == 1) {
+      if (leader && lane == 0) {  // one thread of the leader waits and issues for the pair
+        constexpr uint32_t idesc_full = F8 ? idesc_e4m3(2 * kBM, BN) : idesc_bf16(2 * kBM, BN, B_MN);
+        constexpr uint32_t idesc_half = F8 ? idesc_e4m3(2 * kBM, BN / 2) : idesc_bf16(2 * kBM, BN / 2, B_MN);
+        int stage = 0;
+        uint32_t phase = 0;
+        bool alive = true;
+        int it = 0;
+        for (int tile = cid; tile < num_tiles && alive; tile += ncl, ++it) {
+          const int acc = it & 1;
+          const uint32_t aph = (it >> 1) & 1;
+          if (!mbar_wait(&tempty[acc], aph ^ 1, status, abort)) break;
+          tc_fence_after();
+          const uint32_t dt = tmem + acc * BN;
+          int m0, n0, kb_lo, kb_hi, width;
+          coords(tile, m0, n0, kb_lo, kb_hi, width);
+          const uint32_t idesc = width == BN ? idesc_full : idesc_half;
+          for (int kb = kb_lo; kb < kb_hi; ++kb) {
+            if (!mbar_wait(&full[stage], phase, status, abort)) {
+              alive = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t sa = smem_u32(smem + stage * L::kStage);
+            const uint32_t sb = sa + L::kA;
+  #pragma unroll
+            for (int kk = 0; kk < kBK / 16; ++kk) {
+              const uint64_t ad = sdesc_sw128(sa + kk * 32, 16, 1024);
+              const uint64_t bd = B_MN ? sdesc_sw128(sb + kk * 2048, kBK * 128, 1024)
+                                       : sdesc_sw128(sb + kk * 32, 16, 1024);
+              if constexpr (F8)
+                umma_e4m3_pair(dt, ad, bd, idesc, (kb != kb_lo || kk != 0) ? 1u : 0u);
+              else
+                umma_bf16_pair(dt, ad, bd, idesc, (kb != kb_lo || kk != 0) ? 1u : 0u);
+            }
+            umma_commit_pair(&empty[stage]);
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1;
+            }
+          }
+          if (alive) umma_commit_pair(&tfull[acc]);
         }
       }
-    }
-  } else if (warp == 1) {
-    if (leader && lane == 0) {  // one thread of the leader waits and issues for the pair
-      constexpr uint32_t idesc_full = F8 ? idesc_e4m3(2 * kBM, BN) : idesc_bf16(2 * kBM, BN, B_MN);
-      constexpr uint32_t idesc_half = F8 ? idesc_e4m3(2 * kBM, BN / 2) : idesc_bf16(2 * kBM, BN / 2, B_MN);
-      int stage = 0;
-      uint32_t phase = 0;
-      bool alive = true;
+      __syncwarp();
+    } else {
+      const int q = warp & 3;  // TMEM lane quarter this warp may read
+      const int half = (warp - 2) / 4;  // EW == 2: which half of the tile's columns
+      const int r_local = q * 32 + lane;
       int it = 0;
-      for (int tile = cid; tile < num_tiles && alive; tile += ncl, ++it) {
+      for (int tile = cid; tile < num_tiles; tile += ncl, ++it) {
         const int acc = it & 1;
         const uint32_t aph = (it >> 1) & 1;
-        if (!mbar_wait(&tempty[acc], aph ^ 1, status, abort)) break;
+        if (!mbar_wait_warp(&tfull[acc], aph, status, abort)) break;
         tc_fence_after();
-        const uint32_t dt = tmem + acc * BN;
         int m0, n0, kb_lo, kb_hi, width;
         coords(tile, m0, n0, kb_lo, kb_hi, width);
-        const uint32_t idesc = width == BN ? idesc_full : idesc_half;
-        for (int kb = kb_lo; kb < kb_hi; ++kb) {
-          if (!mbar_wait(&full[stage], phase, status, abort)) {
-            alive = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t sa = smem_u32(smem + stage * L::kStage);
-          const uint32_t sb = sa + L::kA;
-#pragma unroll
-          for (int kk = 0; kk < kBK / 16; ++kk) {
-            const uint64_t ad = sdesc_sw128(sa + kk * 32, 16, 1024);
-            const uint64_t bd = B_MN ? sdesc_sw128(sb + kk * 2048, kBK * 128, 1024)
-                                     : sdesc_sw128(sb + kk * 32, 16, 1024);
-            if constexpr (F8)
-              umma_e4m3_pair(dt, ad, bd, idesc, (kb != kb_lo || kk != 0) ? 1u : 0u);
-            else
-              umma_bf16_pair(dt, ad, bd, idesc, (kb != kb_lo || kk != 0) ? 1u : 0u);
-          }
-          umma_commit_pair(&empty[stage]);
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1;
-          }
+        const int row = m0 + (int)rank * kBM + r_local;
+        const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
+        if constexpr (EW == 1) {
+          auto ld = [&](int c, float(&v)[32]) { tmem_ld32(tb + c * 32, v); };
+          if (!TAIL || width == BN)
+            epi.template tile<BN>(row, row < M, n0, N, ld, tile / num_mn);
+          else
+            epi.template tile<BN / 2>(row, row < M, n0, N, ld, 0);
+        } else {
+          static_assert(EW == 2, "one or two epilogue warps per lane quarter");
+          const uint32_t th = tb + (uint32_t)(half * (BN / 2));
+          auto ld = [&](int c, float(&v)[32]) { tmem_ld32(th + c * 32, v); };
+          if (!TAIL || width == BN)
+            epi.template tile<BN / 2>(row, row < M, n0 + half * (BN / 2), N, ld, tile / num_mn);
+          else if (half == 0)
+            epi.template tile<BN / 2>(row, row < M, n0, N, ld, 0);
         }
-        if (alive) umma_commit_pair(&tfull[acc]);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(cluster_addr(&tempty[acc], 0));
       }
-    }
-    __syncwarp();
-  } else {
-    const int q = warp & 3;  // TMEM lane quarter this warp may read
-    const int half = (warp - 2) / 4;  // EW == 2: which half of the tile's columns
-    const int r_local = q * 32 + lane;
-    int it = 0;
-    for (int tile = cid; tile < num_tiles; tile += ncl, ++it) {
-      const int acc = it & 1;
-      const uint32_t aph = (it >> 1) & 1;
-      if (!mbar_wait_warp(&tfull[acc], aph, status, abort)) break;
-      tc_fence_after();
-      int m0, n0, kb_lo, kb_hi, width;
-      coords(tile, m0, n0, kb_lo, kb_hi, width);
-      const int row = m0 + (int)rank * kBM + r_local;
-      const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
-      if constexpr (EW == 1) {
-        auto ld = [&](int c, float(&v)[32]) { tmem_ld32(tb + c * 32, v); };
-        if (!TAIL || width == BN)
-          epi.template tile<BN>(row, row < M, n0, N, ld, tile / num_mn);
-        else
-          epi.template tile<BN / 2>(row, row < M, n0, N, ld, 0);
-      } else {
-        static_assert(EW == 2, "one or two epilogue warps per lane quarter");
-        const uint32_t th = tb + (uint32_t)(half * (BN / 2));
-        auto ld = [&](int c, float(&v)[32]) { tmem_ld32(th + c * 32, v); };
-        if (!TAIL || width == BN)
-          epi.template tile<BN / 2>(row, row < M, n0 + half * (BN / 2), N, ld, tile / num_mn);
-        else if (half == 0)
-          epi.template tile<BN / 2>(row, row < M, n0, N, ld, 0);
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(cluster_addr(&tempty[acc], 0));
     }
   }
   __syncwarp();
