@@ -311,6 +311,7 @@ dg_status enqueue_step(const StepCtx& c, float tau, float b, float stop_H, uint6
   DG_TRY(ps.mark(DG_PROF_SAMPLER, 1));
   P0Args p0{};
   p0.pt = at<void>(ws, L.pt);
+  p0.gst = lm.gst;
   p0.rowmax = at<float>(ws, L.rowmax);
   p0.lsum = at<float>(ws, L.lsum);
   p0.acc = at<uint8_t>(ws, L.acc);

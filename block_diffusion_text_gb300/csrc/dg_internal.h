@@ -259,6 +259,7 @@ int selfcond_active_splits(const dg_dims& D);
 constexpr int kGumbelChunk = 4096;
 struct P0Args {
   const void* pt;        // bf16 [M][V]: the tiles, exp2(t - ref2f)
+  const GroupStat* gst;  // [M][NT]  group maxima m_g (log2 units)
   const float* rowmax;   // [M]  row maximum m (log2 units)
   const float* lsum;     // [M]  Z
   const uint8_t* acc;    // [M]

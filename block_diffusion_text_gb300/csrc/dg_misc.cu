@@ -315,7 +315,10 @@ cudaError_t launch_stats(const StatsArgs& a, StopCtl ctl, cudaStream_t st) {
 // Gumbel-max form of that draw is this library's reading).  The argmax token's
 // p0 is 1/Z, so its perturbed score S_a = log(1/Z) + G_a is computed first; the
 // largest draw is 16.64, so entries with log p0 < S_a - 16.64 - 0.02 can never
-// win and skip the draw.  Rows that are not accepted are not read.
+// win and skip the draw.  Rows that are not accepted are not read, nor are the
+// tiles of a statistics group whose maximum (from the LM head's records) lies
+// below that threshold: in the low-entropy rows that are accepted most groups
+// are.
 // One CTA per (row, 4096-entry chunk): larger chunks measured slower (16384:
 // +2 us; 32768 with 16 loads in flight per thread: +22 us): the search wants
 // many CTAs.
@@ -340,11 +343,14 @@ __global__ void __launch_bounds__(kP0Threads) p0_gumbel_kernel(P0Args a, StopCtl
   // (two statistics groups of 128 columns, one scale factor each).
   const int wbase = chunk * kGumbelChunk + (threadIdx.x / 32) * 1024;
   const int lane = threadIdx.x % 32;
-  uint4 x[4];
+  // the maxima of the statistics groups of this lane's four 8-entry pieces
+  // (L2-resident records), read while the threshold's draw is computed
+  const int NT = (a.V + kStatCols - 1) / kStatCols;
+  float mg[4];
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     const int v = wbase + (q * 32 + lane) * 8;
-    if (v < a.V) x[q] = *reinterpret_cast<const uint4*>(pt + v);  // V is a multiple of 8
+    mg[q] = v < a.V ? a.gst[(size_t)row * NT + v / kStatCols].m : -FLT_MAX;
   }
   // p0 threshold below which no entry can win the Gumbel-max search: the
   // argmax token's p0 is 1/Z, so its perturbed score S_a is known, and an
@@ -357,10 +363,21 @@ __global__ void __launch_bounds__(kP0Threads) p0_gumbel_kernel(P0Args a, StopCtl
     const float sa = logf(invZ) + gumbel_from_word(wa[va & 3]);
     thr = expf(sa - kGumbelMaxDraw - 0.02f);
   }
+  // A group whose largest p0, exp2(m_g - m) / Z (the tile holds it rounded
+  // to bf16; a margin of 2^-6 covers that), is below the threshold holds no
+  // candidate: its tiles are not read.
+  bool need[4];
+  uint4 x[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int v = wbase + (q * 32 + lane) * 8;
+    need[q] = v < a.V && exp2f(mg[q] - mrow) * invZ * 1.015625f >= thr;
+    if (need[q]) x[q] = *reinterpret_cast<const uint4*>(pt + v);  // V is a multiple of 8
+  }
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     const int vq = wbase + (q * 32 + lane) * 8;
-    if (vq >= a.V) break;
+    if (!need[q]) continue;
     const __nv_bfloat16* xb = reinterpret_cast<const __nv_bfloat16*>(&x[q]);
     float p[8];
 #pragma unroll
