@@ -254,9 +254,8 @@ cudaError_t launch_selfcond(const ScArgs& a, StopCtl ctl, int* status, cudaStrea
 // on the current device uses (at most the bound).
 int selfcond_splits(const dg_dims& D);
 int selfcond_active_splits(const dg_dims& D);
-// The stored tiles become p0 in place, and the Gumbel-max search of the
-// accepted rows runs over vocabulary chunks in the same pass.
-constexpr int kGumbelChunk = 4096;
+// The Gumbel-max search of the accepted rows over the stored tiles (one best
+// (score, index) per row).
 struct P0Args {
   const void* pt;        // bf16 [M][V]: the tiles, exp2(t - ref2f)
   const GroupStat* gst;  // [M][NT]  group maxima m_g (log2 units)
@@ -264,8 +263,8 @@ struct P0Args {
   const float* lsum;     // [M]  Z
   const uint8_t* acc;    // [M]
   const int* amax;       // [M]  argmax of the logits (lowest index on ties)
-  float* gbest;          // [NC][M]
-  int* gidx;             // [NC][M]
+  float* gbest;          // [M]
+  int* gidx;             // [M]
   int M, V, C;
   uint64_t seed;
   int block, step;
@@ -355,8 +354,8 @@ cudaError_t launch_fill_tokens(int32_t* tokens, int n, int value, cudaStream_t s
 
 struct ReduceArgs {
   const float* upart;    // [S][M][d]
-  const float* gbest;    // [NC][M]
-  const int* gidx;       // [NC][M]
+  const float* gbest;    // [nchunks][M]
+  const int* gidx;       // [nchunks][M]
   const uint8_t* acc;
   void* u;               // bf16 [M][d]
   int* tokens;           // [M]
