@@ -165,6 +165,15 @@ def test_long_canvas_entropy_given_h():
     _run_and_compare(dims, 14, tau=0.6, entropy_given_h=True)
 
 
+def test_gumbel_search_flat_rows_every_group():
+    """V = 131072 (1024 statistics groups), near-flat rows and b large enough that every position is
+    accepted: every group of a row can hold the Gumbel-max winner, so the search passes its list of
+    candidate groups and scans all of them; the sampled tokens against the oracle's."""
+    dims = synth.Dims(V=131072, d=64, C=16, B=1, Hq=2, Hkv=1, hd=32, F=64, P=32)
+    out, ref, stats = _run_and_compare(dims, 17, tau=0.8, b=1e9, alpha=0.5)
+    assert stats["accepted"] == dims.C
+
+
 def test_step_events_eager_and_captured():
     """Per-kernel events through the ABI: recorded by a host-launched step and by a replayed graph of
     the same step, every timed slot's pair recorded in order (non-negative elapsed time), and the
