@@ -11,8 +11,9 @@
 //     epilogue (the q, k, v projections and FFW1 at C = 256).
 //   * gemm_pair_kernel: the same engine on CTA pairs (M = 256 MMAs over two
 //     SMs), for the two vocabulary-sized products: the LM head and the
-//     self-conditioning contraction u = p0 . E (p0 rescaled in place after
-//     the LM head, E as the MN-major B operand, split over the vocabulary).
+//     self-conditioning contraction u = p0 . E (the LM head's stored tiles
+//     as A, one p0 factor per row applied in the reduce, E as the MN-major B
+//     operand, split over the vocabulary).
 #include <cfloat>
 
 #include "dg_common.cuh"

@@ -39,7 +39,7 @@ struct WsLayout {
   size_t pt;
   size_t gst;  // per (row, 128-column group) statistics records
   size_t Hd, lsum, rowmax, amax, acc;
-  size_t upart, gbest, gidx;
+  size_t upart, gidx;
   size_t gpart, gpart_elems;  // split-K partials of the small GEMMs
   size_t u, g;
   size_t h8, hscale;          // FP8 head: h quantized per row
@@ -263,8 +263,7 @@ struct P0Args {
   const float* lsum;     // [M]  Z
   const uint8_t* acc;    // [M]
   const int* amax;       // [M]  argmax of the logits (lowest index on ties)
-  float* gbest;          // [M]
-  int* gidx;             // [M]
+  int* gidx;             // [M] the winning token of each accepted row
   int M, V, C;
   uint64_t seed;
   int block, step;
@@ -354,13 +353,12 @@ cudaError_t launch_fill_tokens(int32_t* tokens, int n, int value, cudaStream_t s
 
 struct ReduceArgs {
   const float* upart;    // [S][M][d]
-  const float* gbest;    // [nchunks][M]
-  const int* gidx;       // [nchunks][M]
+  const int* gidx;       // [M] the Gumbel search's winner of each accepted row
   const uint8_t* acc;
   void* u;               // bf16 [M][d]
   int* tokens;           // [M]
   int* status;           // DG_ERR_VALUE if an accepted row has no finite Gumbel score
-  int M, d, C, V, nsplit, nchunks;
+  int M, d, C, V, nsplit;
   // per-row factor of the contraction: exp2(ref2f - rowmax) / lsum
   const float *ref2f, *rowmax, *lsum;
 };

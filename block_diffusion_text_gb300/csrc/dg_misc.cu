@@ -421,7 +421,6 @@ __global__ void __launch_bounds__(kP0Threads) p0_gumbel_kernel(P0Args a, StopCtl
         bidx = si[k];
       }
     }
-    a.gbest[row] = best;
     a.gidx[row] = bidx;
   }
 }
@@ -670,8 +669,8 @@ cudaError_t launch_fill_tokens(int32_t* tokens, int n, int value, cudaStream_t s
 // token of accepted positions = the best (score, lowest index) over chunks.
 // Grid (M, G + 1): CTA (row, y < G) sums 128 float4 columns of the row, each
 // thread one column with the loads of eight splits in flight at once (summed
-// as a fixed tree per group of eight, the groups in order); CTA (row, G) picks
-// the sampled token.
+// as a fixed tree per group of eight, the groups in order); CTA (row, G) sets
+// the sampled token of an accepted row.
 constexpr int kReduceCols = 128;
 
 __global__ void __launch_bounds__(kReduceCols) reduce_kernel(ReduceArgs a, StopCtl ctl) {
@@ -712,35 +711,14 @@ __global__ void __launch_bounds__(kReduceCols) reduce_kernel(ReduceArgs a, StopC
     *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(a.u) + (size_t)row * a.d + 4 * c) = w;
     return;
   }
-  // sampled token of an accepted row: the best (score, lowest index) over the
-  // chunks, one warp
-  if (threadIdx.x < 32 && a.acc[row] && canvas_active(ctl.stop_at, row / a.C, ctl.step)) {
-    float best = -FLT_MAX;
-    int bi = INT_MAX;
-    for (int s = threadIdx.x; s < a.nchunks; s += 32) {
-      const float v = a.gbest[(size_t)s * a.M + row];
-      const int i = a.gidx[(size_t)s * a.M + row];
-      if (v > best || (v == best && i < bi)) {
-        best = v;
-        bi = i;
-      }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float b2 = __shfl_xor_sync(0xffffffffu, best, o);
-      const int i2 = __shfl_xor_sync(0xffffffffu, bi, o);
-      if (b2 > best || (b2 == best && i2 < bi)) {
-        best = b2;
-        bi = i2;
-      }
-    }
-    // no candidate only when the probabilities are not finite: keep the token
-    if (threadIdx.x == 0) {
-      if (bi >= 0 && bi < a.V)
-        a.tokens[row] = bi;
-      else
-        atomicExch(a.status, kStatusValue);
-    }
+  // sampled token of an accepted row: the Gumbel search's winner; it has none
+  // only when the probabilities are not finite: then the token is kept
+  if (threadIdx.x == 0 && a.acc[row] && canvas_active(ctl.stop_at, row / a.C, ctl.step)) {
+    const int bi = a.gidx[row];
+    if (bi >= 0 && bi < a.V)
+      a.tokens[row] = bi;
+    else
+      atomicExch(a.status, kStatusValue);
   }
 }
 

@@ -184,7 +184,7 @@ enum {
   DG_PROF_LMHEAD = 4,    /* LM head with softmax statistics           */
   DG_PROF_STATS = 5,     /* merge of the statistics: entropy, argmax  */
   DG_PROF_SAMPLER = 6,   /* sort, cumulative entropy, accept, renoise */
-  DG_PROF_P0 = 7,        /* tiles -> p0 in place; Gumbel-max search   */
+  DG_PROF_P0 = 7,        /* Gumbel-max search of the accepted rows    */
   DG_PROF_SELFCOND = 8,  /* p0 . E on the tensor cores                */
   DG_PROF_REDUCE = 9,    /* reduction of p0 . E, sampled tokens        */
   DG_PROF_FFW1 = 10,     /* GELU(W1 u)                                */
