@@ -724,31 +724,28 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 }
 
 // ============================================================ grouped GEMM
-// The MoE expert products: A = expert-sorted rows [R][K], B = the experts'
-// matrices stacked [groups * b_rows][K].  The M-tile table (written on the
-// device by the routing plan) holds the count in tiles[0].x and, per tile,
-// (expert, first row, rows) in tiles[1 + t]; output tile (t, n) multiplies
-// A rows [first, first + 128) by B rows [expert * b_rows + n, + BN).  Rows of
-// the A box past the tile's own (the next expert's, or past the end and
-// zero-filled) are computed and not stored.  Tiles run n-major so that the
-// M-tiles of one expert, which share its B tiles, run side by side.
+// The MoE expert products, D^T = W x^T per expert: A = the experts' matrices
+// stacked [groups * b_rows][K] (M = 128 output features of one expert per
+// tile), B = a tile of that expert's rows of the expert-sorted input [R][K]
+// (N = kMoeTileRows rows).  An expert gets few rows at C = 256 (top 8 of 128:
+// ~24 each), so the rows are the narrow side: a 128-row tile of them would be
+// mostly padding in the MMA and in the operand loads.  The tile table
+// (written on the device by the routing plan) holds the count in tiles[0].x
+// and, per tile, (expert, first row, rows) in tiles[1 + t]; output tile
+// (t, n) is rows [first, first + rows) x features [n, n + 128).  Tiles run
+// n-major, so the row tiles of one expert, which share its weight tiles, run
+// side by side.  TMEM lane f of the accumulator holds feature n + f for the
+// tile's rows (its columns); the epilogue stores one row at a time, the lanes
+// of a warp writing consecutive features.
 struct EpiMoeUp {  // expert hidden: bf16(GELU(acc))
   __nv_bfloat16* gp;
   int ldo;
-  template <int BN, class LD>
-  DG_DEV void tile(int row, bool ok, int n0, int /*N*/, LD& ld, int /*group*/) const {
-#pragma unroll 1
-    for (int c = 0; c < BN / 32; ++c) {
-      float v[32];
-      ld(c, v);
-      if (!ok) continue;
+  DG_DEV void store(int feat, int first, int rows, const float (&v)[kMoeTileRows]) const {
 #pragma unroll
-      for (int j = 0; j < 32; ++j) v[j] = 0.5f * v[j] * (1.0f + erff(v[j] * 0.70710678118654752f));
-      uint4* dst = reinterpret_cast<uint4*>(gp + (size_t)row * ldo + n0 + c * 32);
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-        dst[j] = make_uint4(pack_bf16(v[8 * j], v[8 * j + 1]), pack_bf16(v[8 * j + 2], v[8 * j + 3]),
-                            pack_bf16(v[8 * j + 4], v[8 * j + 5]), pack_bf16(v[8 * j + 6], v[8 * j + 7]));
+    for (int j = 0; j < kMoeTileRows; ++j) {
+      if (j >= rows) break;  // uniform over the warp
+      const float x = v[j];
+      gp[(size_t)(first + j) * ldo + feat] = __float2bfloat16_rn(0.5f * x * (1.0f + erff(x * 0.70710678118654752f)));
     }
   }
 };
@@ -756,29 +753,23 @@ struct EpiMoeDown {  // gated expert output, fp32
   float* yp;
   const float* pgate;
   int ldo;
-  template <int BN, class LD>
-  DG_DEV void tile(int row, bool ok, int n0, int /*N*/, LD& ld, int /*group*/) const {
-    const float g = ok ? __ldg(pgate + row) : 0.f;
-#pragma unroll 1
-    for (int c = 0; c < BN / 32; ++c) {
-      float v[32];
-      ld(c, v);
-      if (!ok) continue;
-      float4* dst = reinterpret_cast<float4*>(yp + (size_t)row * ldo + n0 + c * 32);
+  DG_DEV void store(int feat, int first, int rows, const float (&v)[kMoeTileRows]) const {
 #pragma unroll
-      for (int j = 0; j < 8; ++j) dst[j] = make_float4(g * v[4 * j], g * v[4 * j + 1], g * v[4 * j + 2], g * v[4 * j + 3]);
+    for (int j = 0; j < kMoeTileRows; ++j) {
+      if (j >= rows) break;  // uniform over the warp
+      yp[(size_t)(first + j) * ldo + feat] = __ldg(pgate + first + j) * v[j];
     }
   }
 };
 
-template <int BN, int STAGES, class Epi>
+template <int STAGES, class Epi>
 __global__ void __launch_bounds__(kGemmThreads, 1)
-    gemm_grouped_kernel(const __grid_constant__ CUtensorMap mA, const __grid_constant__ CUtensorMap mB,
+    gemm_grouped_kernel(const __grid_constant__ CUtensorMap mW, const __grid_constant__ CUtensorMap mX,
                         const int4* __restrict__ tiles, int max_tiles, int b_rows, int N, int K, Epi epi,
                         int* status, StopCtl ctl) {
-  pdl_wait();
-  using L = GemmLayout<BN, STAGES, false>;
-  if (all_stopped(ctl.stop_at, ctl.B, ctl.step)) return;
+  static_assert(kMoeTileRows == 32, "one 32-column TMEM load per tile");
+  constexpr int BN = kMoeTileRows;
+  using L = GemmLayout<BN, STAGES, false>;  // A: 128 weight rows, B: BN rows of the input
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kBar);
@@ -787,12 +778,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   uint64_t* tempty = tfull + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
   volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
-
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int n_mt = min(tiles[0].x, max_tiles);
-  const int num_n = N / BN;
-  const int num_tiles = n_mt * num_n;
-  const int nk = (K + kBK - 1) / kBK;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -815,82 +801,88 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 0) {
-    if (lane == 0) {
-      tma_prefetch(&mA);
-      tma_prefetch(&mB);
-      int stage = 0;
-      uint32_t phase = 0;
-      bool alive = true;
-      for (int tile = blockIdx.x; tile < num_tiles && alive; tile += gridDim.x) {
-        const int4 te = tiles[1 + tile % n_mt];
-        const int brow = te.x * b_rows + (tile / n_mt) * BN;
-        for (int kb = 0; kb < nk; ++kb) {
-          if (!mbar_wait(&empty[stage], phase ^ 1, status, abort)) {
-            alive = false;
-            break;
-          }
-          uint8_t* sa = smem + stage * L::kStage;
-          mbar_arrive_expect_tx(&full[stage], L::kStage);
-          tma_load_2d(sa, &mA, &full[stage], kb * kBK, te.y);
-          tma_load_2d(sa + L::kA, &mB, &full[stage], kb * kBK, brow);
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1;
+  // The prologue above reads nothing the kernel before wrote (see pdl_trigger).
+  pdl_wait();
+  if (!all_stopped(ctl.stop_at, ctl.B, ctl.step)) {
+    const int n_mt = min(tiles[0].x, max_tiles);
+    const int num_tiles = n_mt * (N / kBM);
+    const int nk = (K + kBK - 1) / kBK;
+    if (warp == 0) {
+      if (lane == 0) {
+        tma_prefetch(&mW);
+        tma_prefetch(&mX);
+        int stage = 0;
+        uint32_t phase = 0;
+        bool alive = true;
+        for (int tile = blockIdx.x; tile < num_tiles && alive; tile += gridDim.x) {
+          const int4 te = tiles[1 + tile % n_mt];
+          const int wrow = te.x * b_rows + (tile / n_mt) * kBM;
+          for (int kb = 0; kb < nk; ++kb) {
+            if (!mbar_wait(&empty[stage], phase ^ 1, status, abort)) {
+              alive = false;
+              break;
+            }
+            uint8_t* sa = smem + stage * L::kStage;
+            mbar_arrive_expect_tx(&full[stage], L::kStage);
+            tma_load_2d(sa, &mW, &full[stage], kb * kBK, wrow);
+            tma_load_2d(sa + L::kA, &mX, &full[stage], kb * kBK, te.y);
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1;
+            }
           }
         }
       }
-    }
-  } else if (warp == 1) {
-    if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16(kBM, BN, false);
-      int stage = 0;
-      uint32_t phase = 0;
-      bool alive = true;
+    } else if (warp == 1) {
+      if (lane == 0) {
+        constexpr uint32_t idesc = idesc_bf16(kBM, BN, false);
+        int stage = 0;
+        uint32_t phase = 0;
+        bool alive = true;
+        int it = 0;
+        for (int tile = blockIdx.x; tile < num_tiles && alive; tile += gridDim.x, ++it) {
+          const int acc = it & 1;
+          const uint32_t aph = (it >> 1) & 1;
+          if (!mbar_wait(&tempty[acc], aph ^ 1, status, abort)) break;
+          tc_fence_after();
+          const uint32_t dt = tmem + acc * BN;
+          for (int kb = 0; kb < nk; ++kb) {
+            if (!mbar_wait(&full[stage], phase, status, abort)) {
+              alive = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t sa = smem_u32(smem + stage * L::kStage);
+            const uint32_t sb = sa + L::kA;
+#pragma unroll
+            for (int kk = 0; kk < kBK / 16; ++kk)
+              umma_bf16(dt, sdesc_sw128(sa + kk * 32, 16, 1024), sdesc_sw128(sb + kk * 32, 16, 1024), idesc,
+                        (kb != 0 || kk != 0) ? 1u : 0u);
+            umma_commit(&empty[stage]);
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1;
+            }
+          }
+          if (alive) umma_commit(&tfull[acc]);
+        }
+      }
+      __syncwarp();
+    } else {
+      const int q = warp & 3;
       int it = 0;
-      for (int tile = blockIdx.x; tile < num_tiles && alive; tile += gridDim.x, ++it) {
+      for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++it) {
         const int acc = it & 1;
         const uint32_t aph = (it >> 1) & 1;
-        if (!mbar_wait(&tempty[acc], aph ^ 1, status, abort)) break;
+        if (!mbar_wait_warp(&tfull[acc], aph, status, abort)) break;
         tc_fence_after();
-        const uint32_t dt = tmem + acc * BN;
-        for (int kb = 0; kb < nk; ++kb) {
-          if (!mbar_wait(&full[stage], phase, status, abort)) {
-            alive = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t sa = smem_u32(smem + stage * L::kStage);
-          const uint32_t sb = sa + L::kA;
-#pragma unroll
-          for (int kk = 0; kk < kBK / 16; ++kk)
-            umma_bf16(dt, sdesc_sw128(sa + kk * 32, 16, 1024), sdesc_sw128(sb + kk * 32, 16, 1024), idesc,
-                      (kb != 0 || kk != 0) ? 1u : 0u);
-          umma_commit(&empty[stage]);
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1;
-          }
-        }
-        if (alive) umma_commit(&tfull[acc]);
+        const int4 te = tiles[1 + tile % n_mt];
+        float v[kMoeTileRows];
+        tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN), v);
+        tc_fence_before();
+        mbar_arrive(&tempty[acc]);  // the accumulator is in registers
+        epi.store((tile / n_mt) * kBM + q * 32 + lane, te.y, te.z, v);
       }
-    }
-    __syncwarp();
-  } else {
-    const int q = warp & 3;
-    const int r_local = q * 32 + lane;
-    int it = 0;
-    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++it) {
-      const int acc = it & 1;
-      const uint32_t aph = (it >> 1) & 1;
-      if (!mbar_wait_warp(&tfull[acc], aph, status, abort)) break;
-      tc_fence_after();
-      const int4 te = tiles[1 + tile % n_mt];
-      const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
-      auto ld = [&](int c, float(&v)[32]) { tmem_ld32(tb + c * 32, v); };
-      epi.template tile<BN>(te.y + r_local, r_local < te.z, (tile / n_mt) * BN, N, ld, te.x);
-      tc_fence_before();
-      mbar_arrive(&tempty[acc]);
     }
   }
   __syncthreads();
@@ -1622,31 +1614,32 @@ cudaError_t launch_selfcond(const ScArgs& a, StopCtl ctl, int* status, cudaStrea
 // The two grouped expert GEMMs of the MoE FFN (128-column tiles; d and Fe are
 // multiples of 128).
 template <class Epi>
-static cudaError_t run_grouped(const CUtensorMap& mA, const CUtensorMap& mB, const int4* tiles, int max_tiles,
+static cudaError_t run_grouped(const CUtensorMap& mW, const CUtensorMap& mX, const int4* tiles, int max_tiles,
                                int b_rows, int N, int K, const Epi& epi, int* status, StopCtl ctl,
                                cudaStream_t st) {
-  constexpr int BN = 128, STAGES = 6;
-  using L = GemmLayout<BN, STAGES, false>;
-  cudaError_t e = set_smem_once<gemm_grouped_kernel<BN, STAGES, Epi>>(L::kSmem);
+  constexpr int STAGES = 8;
+  using L = GemmLayout<kMoeTileRows, STAGES, false>;
+  cudaError_t e = set_smem_once<gemm_grouped_kernel<STAGES, Epi>>(L::kSmem);
   if (e != cudaSuccess) return e;
-  const int bound = max_tiles * (N / BN);
+  const int bound = max_tiles * (N / kBM);
   const int grid = bound < num_sms() ? (bound > 0 ? bound : 1) : num_sms();
-  return launch_pdl(gemm_grouped_kernel<BN, STAGES, Epi>, dim3(grid), dim3(kGemmThreads), L::kSmem, st, mA, mB,
-                    tiles, max_tiles, b_rows, N, K, epi, status, ctl);
+  return launch_pdl(gemm_grouped_kernel<STAGES, Epi>, dim3(grid), dim3(kGemmThreads), L::kSmem, st, mW, mX, tiles,
+                    max_tiles, b_rows, N, K, epi, status, ctl);
 }
 
 cudaError_t launch_moe_experts(const void* xp, const void* We1, const void* We2, const int4* tiles,
                                int max_tiles, int R, int groups, const float* pgate, void* gp, float* yp, int d,
                                int Fe, int* status, StopCtl ctl, cudaStream_t st) {
-  // A boxes reaching past row R read zeros (the tensor maps end there)
+  // row boxes reaching past row R read zeros (the tensor maps end there);
+  // their results are not stored
   CUtensorMap mX, mW1, mG, mW2;
-  if (!tmap_kmajor(&mX, xp, R, d, kBM) || !tmap_kmajor(&mG, gp, R, Fe, kBM) ||
-      !tmap_kmajor(&mW1, We1, groups * Fe, d, 128) || !tmap_kmajor(&mW2, We2, groups * d, Fe, 128))
+  if (!tmap_kmajor(&mX, xp, R, d, kMoeTileRows) || !tmap_kmajor(&mG, gp, R, Fe, kMoeTileRows) ||
+      !tmap_kmajor(&mW1, We1, groups * Fe, d, kBM) || !tmap_kmajor(&mW2, We2, groups * d, Fe, kBM))
     return cudaErrorInvalidValue;
-  cudaError_t e = run_grouped(mX, mW1, tiles, max_tiles, Fe, Fe, d,
+  cudaError_t e = run_grouped(mW1, mX, tiles, max_tiles, Fe, Fe, d,
                               EpiMoeUp{reinterpret_cast<__nv_bfloat16*>(gp), Fe}, status, ctl, st);
   if (e != cudaSuccess) return e;
-  return run_grouped(mG, mW2, tiles, max_tiles, d, d, Fe, EpiMoeDown{yp, pgate, d}, status, ctl, st);
+  return run_grouped(mW2, mG, tiles, max_tiles, d, d, Fe, EpiMoeDown{yp, pgate, d}, status, ctl, st);
 }
 
 }  // namespace dg

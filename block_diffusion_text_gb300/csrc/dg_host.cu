@@ -117,7 +117,7 @@ dg_status enqueue_moe(const dg_model* m, int l, void* ws, const WsLayout& L, int
                   at<float>(ws, L.moe_gate), dbg ? dbg->moe_idx : nullptr, dbg ? dbg->moe_gate : nullptr,
                   dbg ? dbg->moe_logits : nullptr, rows, D.d, NE, K};
   DG_TRY(launch_moe_route(ra, at<float>(ws, L.moe_rpart), L.moe_rpart_elems, status, ctl, st));
-  const int max_tiles = cdiv(R, 128) + NE + 1;
+  const int max_tiles = cdiv(R, kMoeTileRows) + NE + 1;
   MoePlanArgs pa{at<int>(ws, L.moe_idx), at<float>(ws, L.moe_gate), at<int>(ws, L.moe_ptok),
                  at<float>(ws, L.moe_pgate), at<int>(ws, L.moe_slot), at<int4>(ws, L.moe_tiles), rows, NE, K,
                  max_tiles};
@@ -464,7 +464,7 @@ bool ws_layout(const dg_dims& D, int32_t cap, WsLayout* L) {
   L->rkey = take(4 * M);
   if (D.n_exp > 0) {
     const size_t K = D.top_k, R = M * (K + 1);
-    L->moe_max_tiles = cdiv((int64_t)R, 128) + D.n_exp + 1;
+    L->moe_max_tiles = cdiv((int64_t)R, kMoeTileRows) + D.n_exp + 1;
     L->moe_x = take(2 * M * D.d);
     L->moe_idx = take(4 * M * K);
     L->moe_gate = take(4 * M * K);

@@ -228,6 +228,8 @@ cudaError_t launch_moe_plan(const MoePlanArgs& a, int* status, StopCtl ctl, cuda
 // Shared memory of the plan kernel (bytes); bounds of its one-CTA design.
 int moe_plan_smem(int M, int n_exp);
 constexpr int kMoeMaxRows = 4096, kMoeMaxExperts = 256, kMoeMaxTopK = 16;
+// Rows of an expert per tile of the grouped expert GEMMs (their N dimension).
+constexpr int kMoeTileRows = 32;
 // xp[p] = x[ptok[p]] for the R permuted rows (bf16, d columns; x has M rows).
 cudaError_t launch_moe_gather(const void* x, const int* ptok, void* xp, int R, int d, int M, StopCtl ctl,
                               cudaStream_t st);

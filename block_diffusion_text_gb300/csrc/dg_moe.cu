@@ -12,14 +12,17 @@
 //            selected logits
 //   plan     one CTA: the M * (top_k + 1) assignments (the shared expert
 //            takes every row) sorted by expert, rows in increasing order
-//            within an expert, and the table of 128-row tiles per expert
+//            within an expert, and the table of row tiles per expert
+//            (kMoeTileRows rows each)
 //   gather   the expert-sorted copy of x
-//   experts  two grouped tcgen05 GEMMs (dg_gemm.cu): GELU(x We1_e^T), then
-//            gate * (. We2_e^T) in fp32
+//   experts  two grouped tcgen05 GEMMs (dg_gemm.cu), the expert's weights
+//            as the 128-row operand and a tile of its rows as N:
+//            GELU(x We1_e^T), then gate * (. We2_e^T) in fp32
 //   combine  h += sum over the row's assignments in rank order, then the
 //            shared expert (fp32), rounded to bf16
 // Every weight matrix of an active expert is read once per layer and step
-// (the expert's rows share its B tiles), which is the HBM floor of the block.
+// (the tiles of an expert's rows run side by side and share its weight
+// tiles), which is the HBM floor of the block.
 #include <cfloat>
 #include <climits>
 
@@ -181,7 +184,7 @@ __global__ void __launch_bounds__(1024) moe_plan_kernel(MoePlanArgs a, int* stat
       off[e] = o;
       toff[e] = to;
       o += cnt[e];
-      to += (cnt[e] + 127) / 128;
+      to += (cnt[e] + kMoeTileRows - 1) / kMoeTileRows;
     }
     off[G] = o;
     toff[G] = to;
@@ -189,9 +192,10 @@ __global__ void __launch_bounds__(1024) moe_plan_kernel(MoePlanArgs a, int* stat
   }
   __syncthreads();
   for (int e = threadIdx.x; e < G; e += blockDim.x) {
-    for (int j = 0; j * 128 < cnt[e]; ++j) {
+    for (int j = 0; j * kMoeTileRows < cnt[e]; ++j) {
       const int ti = toff[e] + j;
-      if (ti < a.max_tiles) a.tiles[1 + ti] = make_int4(e, off[e] + 128 * j, min(128, cnt[e] - 128 * j), 0);
+      if (ti < a.max_tiles)
+        a.tiles[1 + ti] = make_int4(e, off[e] + kMoeTileRows * j, min(kMoeTileRows, cnt[e] - kMoeTileRows * j), 0);
     }
   }
   for (int i = threadIdx.x; i < R; i += blockDim.x) {
