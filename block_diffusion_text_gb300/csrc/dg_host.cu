@@ -244,10 +244,12 @@ dg_status enqueue_step(const StepCtx& c, float tau, float b, float stop_H, uint6
   lm.ref2 = at<float>(ws, L.ref2);
   lm.rkey = at<unsigned>(ws, L.rkey);
   float* ref2f = at<float>(ws, L.ref2f);
-  DG_TRY(pf.mark(DG_PROF_LMHEAD, 0));
   RefArgs rf{lm.h, c.model->E, c.canvas->alpha, lm.coef2, c.canvas->tokens, c.canvas->prev_argmax, step, M, D.d,
              D.V, mask_id, at<float>(ws, L.ref2), ref2f, lm.rkey};
   DG_TRY(launch_lm_ref(rf, ctl, c.st));
+  // the LM head slot: the product with its statistics (and, for the FP8
+  // head, the quantization of h it needs), without the reference and fix
+  DG_TRY(pf.mark(DG_PROF_LMHEAD, 0));
   if (c.model->E8) {
     lm.h8 = at<void>(ws, L.h8);
     lm.hscale = at<float>(ws, L.hscale);
@@ -256,9 +258,9 @@ dg_status enqueue_step(const StepCtx& c, float tau, float b, float stop_H, uint6
     DG_TRY(launch_quantize_rows_e4m3(lm.h, M, D.d, at<uint8_t>(ws, L.h8), at<float>(ws, L.hscale), c.st));
   }
   DG_TRY(launch_lmhead(lm, ctl, status, c.st));
+  DG_TRY(pf.mark(DG_PROF_LMHEAD, 1));
   FixArgs fx{at<void>(ws, L.pt), lm.gst, lm.ref2, lm.rkey, ref2f, M, D.V};
   DG_TRY(launch_lm_fix(fx, ctl, c.st));
-  DG_TRY(pf.mark(DG_PROF_LMHEAD, 1));
   // fork: statistics, sampler and Gumbel search on the side stream, the
   // contraction (which reads only the tiles) on the caller's stream
   SideStream* sd = side_stream(c.st);

@@ -181,7 +181,7 @@ enum {
   DG_PROF_QKV = 1,       /* q, k, v projections with RoPE             */
   DG_PROF_ATTN = 2,      /* attention over prefix + canvas (+ merge)  */
   DG_PROF_OPROJ = 3,     /* output projection + residual              */
-  DG_PROF_LMHEAD = 4,    /* LM head with softmax statistics           */
+  DG_PROF_LMHEAD = 4,    /* LM head + statistics (FP8: + h's codes)   */
   DG_PROF_STATS = 5,     /* merge of the statistics: entropy, argmax  */
   DG_PROF_SAMPLER = 6,   /* sort, cumulative entropy, accept, renoise */
   DG_PROF_P0 = 7,        /* Gumbel-max search of the accepted rows    */
