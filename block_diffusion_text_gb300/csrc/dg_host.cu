@@ -265,10 +265,29 @@ dg_status enqueue_step(const StepCtx& c, float tau, float b, float stop_H, uint6
   // contraction (which reads only the tiles) on the caller's stream
   SideStream* sd = side_stream(c.st);
   std::unique_lock<std::mutex> side_lock(g_side_mu, std::defer_lock);
+  // Joins the side stream back into the caller's stream on every way out of
+  // this function once the fork is recorded, an error return included, so
+  // that no side-stream kernel still reads the workspace after the caller's
+  // stream has passed the step.  Declared after the lock: it runs first.
+  struct JoinGuard {
+    SideStream* sd = nullptr;
+    cudaStream_t st = nullptr;
+    cudaError_t join() {
+      if (!sd) return cudaSuccess;
+      SideStream* s = sd;
+      sd = nullptr;
+      const cudaError_t e = cudaEventRecord(s->join, s->s);
+      const cudaError_t w = cudaStreamWaitEvent(st, s->join, 0);
+      return e != cudaSuccess ? e : w;
+    }
+    ~JoinGuard() { join(); }
+  } side_join;
   cudaStream_t sst = c.st;
   if (sd) {
     side_lock.lock();
     DG_TRY(cudaEventRecord(sd->fork, c.st));
+    side_join.sd = sd;
+    side_join.st = c.st;
     DG_TRY(cudaStreamWaitEvent(sd->s, sd->fork, 0));
     sst = sd->s;
   }
@@ -341,8 +360,7 @@ dg_status enqueue_step(const StepCtx& c, float tau, float b, float stop_H, uint6
   DG_TRY(launch_selfcond(sc, ctl, status, c.st));
   DG_TRY(pf.mark(DG_PROF_SELFCOND, 1));
   if (sd) {  // join
-    DG_TRY(cudaEventRecord(sd->join, sd->s));
-    DG_TRY(cudaStreamWaitEvent(c.st, sd->join, 0));
+    DG_TRY(side_join.join());
     side_lock.unlock();
   }
   ReduceArgs ra{at<float>(ws, L.upart), at<int>(ws, L.gidx), at<uint8_t>(ws, L.acc), at<void>(ws, L.u),
