@@ -337,6 +337,7 @@ dg_status enqueue_step(const StepCtx& c, float tau, float b, float stop_H, uint6
   p0.lsum = at<float>(ws, L.lsum);
   p0.acc = at<uint8_t>(ws, L.acc);
   p0.amax = at<int>(ws, L.amax);
+  p0.gbest = at<float>(ws, L.gbest);
   p0.gidx = at<int>(ws, L.gidx);
   p0.M = M;
   p0.V = D.V;
@@ -363,9 +364,9 @@ dg_status enqueue_step(const StepCtx& c, float tau, float b, float stop_H, uint6
     DG_TRY(side_join.join());
     side_lock.unlock();
   }
-  ReduceArgs ra{at<float>(ws, L.upart), at<int>(ws, L.gidx), at<uint8_t>(ws, L.acc), at<void>(ws, L.u),
-                c.canvas->tokens, status, M, D.d, D.C, D.V, sc.nsplit, ref2f, at<float>(ws, L.rowmax),
-                at<float>(ws, L.lsum)};
+  ReduceArgs ra{at<float>(ws, L.upart), at<float>(ws, L.gbest), at<int>(ws, L.gidx), at<uint8_t>(ws, L.acc),
+                at<void>(ws, L.u), c.canvas->tokens, status, M, D.d, D.C, D.V, sc.nsplit,
+                cdiv(D.V, kGumbelChunk), ref2f, at<float>(ws, L.rowmax), at<float>(ws, L.lsum)};
   DG_TRY(pf.mark(DG_PROF_REDUCE, 0));
   DG_TRY(launch_reduce(ra, ctl, c.st));
   DG_TRY(pf.mark(DG_PROF_REDUCE, 1));
@@ -463,7 +464,9 @@ bool ws_layout(const dg_dims& D, int32_t cap, WsLayout* L) {
   L->amax = take(4 * M);
   L->acc = take(M);
   L->upart = take(4 * S * M * D.d);
-  L->gidx = take(4 * M);
+  const size_t NC = (size_t)cdiv(D.V, kGumbelChunk);
+  L->gbest = take(4 * NC * M);
+  L->gidx = take(4 * NC * M);
   {
     const int nq = D.Hq * D.hd, nkv = D.Hkv * D.hd;
     const int shapes[5][2] = {{nq + 2 * nkv, D.d}, {D.d, nq}, {D.F, D.d}, {D.d, D.F}, {2 * nkv, D.d}};

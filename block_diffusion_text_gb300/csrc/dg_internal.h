@@ -39,7 +39,7 @@ struct WsLayout {
   size_t pt;
   size_t gst;  // per (row, 128-column group) statistics records
   size_t Hd, lsum, rowmax, amax, acc;
-  size_t upart, gidx;
+  size_t upart, gbest, gidx;
   size_t gpart, gpart_elems;  // split-K partials of the small GEMMs
   size_t u, g;
   size_t h8, hscale;          // FP8 head: h quantized per row
@@ -256,8 +256,10 @@ cudaError_t launch_selfcond(const ScArgs& a, StopCtl ctl, int* status, cudaStrea
 // on the current device uses (at most the bound).
 int selfcond_splits(const dg_dims& D);
 int selfcond_active_splits(const dg_dims& D);
-// The Gumbel-max search of the accepted rows over the stored tiles (one best
-// (score, index) per row).
+// The Gumbel-max search of the accepted rows over the stored tiles, in
+// vocabulary chunks of kGumbelChunk entries (one best (score, index) per row
+// and chunk; the reduce takes the best of a row's chunks).
+constexpr int kGumbelChunk = 4096;
 struct P0Args {
   const void* pt;        // bf16 [M][V]: the tiles, exp2(t - ref2f)
   const GroupStat* gst;  // [M][NT]  group maxima m_g (log2 units)
@@ -265,7 +267,8 @@ struct P0Args {
   const float* lsum;     // [M]  Z
   const uint8_t* acc;    // [M]
   const int* amax;       // [M]  argmax of the logits (lowest index on ties)
-  int* gidx;             // [M] the winning token of each accepted row
+  float* gbest;          // [NC][M]
+  int* gidx;             // [NC][M]
   int M, V, C;
   uint64_t seed;
   int block, step;
@@ -355,12 +358,13 @@ cudaError_t launch_fill_tokens(int32_t* tokens, int n, int value, cudaStream_t s
 
 struct ReduceArgs {
   const float* upart;    // [S][M][d]
-  const int* gidx;       // [M] the Gumbel search's winner of each accepted row
+  const float* gbest;    // [NC][M]
+  const int* gidx;       // [NC][M]
   const uint8_t* acc;
   void* u;               // bf16 [M][d]
   int* tokens;           // [M]
   int* status;           // DG_ERR_VALUE if an accepted row has no finite Gumbel score
-  int M, d, C, V, nsplit;
+  int M, d, C, V, nsplit, nchunks;
   // per-row factor of the contraction: exp2(ref2f - rowmax) / lsum
   const float *ref2f, *rowmax, *lsum;
 };

@@ -319,82 +319,90 @@ cudaError_t launch_stats(const StatsArgs& a, StopCtl ctl, cudaStream_t st) {
 // tiles of a statistics group whose maximum (from the LM head's records) lies
 // below that threshold: in the low-entropy rows that are accepted most groups
 // are.
-// One CTA per row.  Its threads first scan the row's group maxima and list the
-// groups that can hold a candidate; then each warp takes a listed group (four
-// entries per lane, one Philox block) and the CTA reduces (score, lowest
-// index).  An earlier form ran one CTA per (row, 4096 entries), each reading
-// its tiles: 64 CTAs per row, each repeating the argmax's draw.
-constexpr int kP0Threads = 256;
-constexpr int kP0MaxCand = 512;  // listed groups; beyond that every group is searched
+// One CTA per (row, 4096-entry chunk): larger chunks measured slower (16384:
+// +2 us; 32768 with 16 loads in flight per thread: +22 us): the search wants
+// many CTAs.  So did one CTA per row listing its candidate groups: quicker
+// beside the long contraction at V = 262144, but a row whose accepted
+// distribution leaves many groups above the threshold went through them eight
+// warps at a time, and at V = 32768 (a short contraction) that lengthened the
+// step.
+constexpr int kP0Threads = kGumbelChunk / 32;
 constexpr float kGumbelMaxDraw = 16.6355f;  // -log(-log(1 - 2^-24))
 
 __global__ void __launch_bounds__(kP0Threads) p0_gumbel_kernel(P0Args a, StopCtl ctl) {
   pdl_wait();
   if (all_stopped(ctl.stop_at, ctl.B, ctl.step)) return;
-  const int row = blockIdx.x;
+  const int row = blockIdx.y;
+  const int chunk = blockIdx.x;
   const bool gum = a.acc[row] && canvas_active(ctl.stop_at, row / a.C, ctl.step);
   if (!gum) return;  // uniform over the CTA
-  __shared__ int cand[kP0MaxCand];
-  __shared__ int ncand;
-  __shared__ float sb[kP0Threads / 32];
-  __shared__ int si[kP0Threads / 32];
   const __nv_bfloat16* pt = reinterpret_cast<const __nv_bfloat16*>(a.pt) + (size_t)row * a.V;
   const int canvas = row / a.C, pos = row % a.C;
   const float mrow = a.rowmax[row], invZ = 1.0f / a.lsum[row];
   const float f = exp2f(a.ref2f[row] - mrow) * invZ;  // p0 = tile * f
+  float best = -FLT_MAX;
+  int bidx = INT_MAX;
+  // Each warp takes 1024 contiguous entries (2 KB); load q of lane l is the
+  // 16-byte chunk q * 32 + l, so a warp's load covers 512 contiguous bytes
+  // (two statistics groups of 128 columns, one scale factor each).
+  const int wbase = chunk * kGumbelChunk + (threadIdx.x / 32) * 1024;
+  const int lane = threadIdx.x % 32;
+  // the maxima of the statistics groups of this lane's four 8-entry pieces
+  // (L2-resident records), read while the threshold's draw is computed
   const int NT = (a.V + kStatCols - 1) / kStatCols;
-  if (threadIdx.x == 0) ncand = 0;
+  float mg[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int v = wbase + (q * 32 + lane) * 8;
+    mg[q] = v < a.V ? a.gst[(size_t)row * NT + v / kStatCols].m : -FLT_MAX;
+  }
   // p0 threshold below which no entry can win the Gumbel-max search: the
   // argmax token's p0 is 1/Z, so its perturbed score S_a is known, and an
   // entry beats it only if log p0 + (largest draw) >= S_a.
-  float thr;
-  {
+  float thr = 0.f;
+  if (gum) {
     const int va = a.amax[row];
     uint64_t wa[4];
     philox_block(wa, a.seed, a.block, a.step, canvas, pos, va >> 2, 0);
     const float sa = logf(invZ) + gumbel_from_word(wa[va & 3]);
     thr = expf(sa - kGumbelMaxDraw - 0.02f);
   }
-  __syncthreads();
   // A group whose largest p0, exp2(m_g - m) / Z (the tile holds it rounded
   // to bf16; a margin of 2^-6 covers that), is below the threshold holds no
-  // candidate and is not read.
-  for (int g = threadIdx.x; g < NT; g += kP0Threads) {
-    const float mg = a.gst[(size_t)row * NT + g].m;
-    if (exp2f(mg - mrow) * invZ * 1.015625f >= thr) {
-      const int k = atomicAdd(&ncand, 1);
-      if (k < kP0MaxCand) cand[k] = g;
-    }
+  // candidate: its tiles are not read.
+  bool need[4];
+  uint4 x[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int v = wbase + (q * 32 + lane) * 8;
+    need[q] = v < a.V && exp2f(mg[q] - mrow) * invZ * 1.015625f >= thr;
+    if (need[q]) x[q] = *reinterpret_cast<const uint4*>(pt + v);  // V is a multiple of 8
   }
-  __syncthreads();
-  const int nc = ncand;
-  const bool listed = nc <= kP0MaxCand;
-  const int ng = listed ? nc : NT;
-  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  float best = -FLT_MAX;
-  int bidx = INT_MAX;
-  for (int k = warp; k < ng; k += kP0Threads / 32) {
-    const int v0 = (listed ? cand[k] : k) * kStatCols + lane * 4;
-    if (v0 >= a.V) continue;  // V is a multiple of 8: the lane's four entries all exist
-    const uint2 x = *reinterpret_cast<const uint2*>(pt + v0);
-    const __nv_bfloat16* xb = reinterpret_cast<const __nv_bfloat16*>(&x);
-    float p[4];
-    bool any = false;
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      p[e] = __bfloat162float(xb[e]) * f;
-      any |= p[e] >= thr;
-    }
-    if (!any) continue;
-    uint64_t w[4];
-    philox_block(w, a.seed, a.block, a.step, canvas, pos, v0 >> 2, 0);
+  for (int q = 0; q < 4; ++q) {
+    const int vq = wbase + (q * 32 + lane) * 8;
+    if (!need[q]) continue;
+    const __nv_bfloat16* xb = reinterpret_cast<const __nv_bfloat16*>(&x[q]);
+    float p[8];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      if (p[e] >= thr && p[e] > 0.f) {
-        const float sc = logf(p[e]) + gumbel_from_word(w[e]);
-        if (sc > best || (sc == best && v0 + e < bidx)) {
-          best = sc;
-          bidx = v0 + e;
+    for (int e = 0; e < 8; ++e) p[e] = __bfloat162float(xb[e]) * f;
+#pragma unroll
+    for (int g4 = 0; g4 < 2; ++g4) {
+      bool any = false;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) any |= p[g4 * 4 + e] >= thr;
+      if (!any) continue;
+      uint64_t w[4];
+      philox_block(w, a.seed, a.block, a.step, canvas, pos, (vq + g4 * 4) >> 2, 0);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float pv = p[g4 * 4 + e];
+        if (pv >= thr && pv > 0.f) {
+          const float sc = logf(pv) + gumbel_from_word(w[e]);
+          if (sc > best) {
+            best = sc;
+            bidx = vq + g4 * 4 + e;
+          }
         }
       }
     }
@@ -409,9 +417,11 @@ __global__ void __launch_bounds__(kP0Threads) p0_gumbel_kernel(P0Args a, StopCtl
       bidx = i2;
     }
   }
-  if (lane == 0) {
-    sb[warp] = best;
-    si[warp] = bidx;
+  __shared__ float sb[kP0Threads / 32];
+  __shared__ int si[kP0Threads / 32];
+  if (threadIdx.x % 32 == 0) {
+    sb[threadIdx.x / 32] = best;
+    si[threadIdx.x / 32] = bidx;
   }
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -421,12 +431,14 @@ __global__ void __launch_bounds__(kP0Threads) p0_gumbel_kernel(P0Args a, StopCtl
         bidx = si[k];
       }
     }
-    a.gidx[row] = bidx;
+    a.gbest[(size_t)chunk * a.M + row] = best;
+    a.gidx[(size_t)chunk * a.M + row] = bidx;
   }
 }
 
 cudaError_t launch_p0_gumbel(const P0Args& a, StopCtl ctl, cudaStream_t st) {
-  return launch_pdl(p0_gumbel_kernel, dim3(a.M), dim3(kP0Threads), 0, st, a, ctl);
+  dim3 grid(cdiv(a.V, kGumbelChunk), a.M);
+  return launch_pdl(p0_gumbel_kernel, grid, dim3(kP0Threads), 0, st, a, ctl);
 }
 
 // --------------------------------------------------------------- sampler --
@@ -669,8 +681,8 @@ cudaError_t launch_fill_tokens(int32_t* tokens, int n, int value, cudaStream_t s
 // token of accepted positions = the best (score, lowest index) over chunks.
 // Grid (M, G + 1): CTA (row, y < G) sums 128 float4 columns of the row, each
 // thread one column with the loads of eight splits in flight at once (summed
-// as a fixed tree per group of eight, the groups in order); CTA (row, G) sets
-// the sampled token of an accepted row.
+// as a fixed tree per group of eight, the groups in order); CTA (row, G) picks
+// the sampled token.
 constexpr int kReduceCols = 128;
 
 __global__ void __launch_bounds__(kReduceCols) reduce_kernel(ReduceArgs a, StopCtl ctl) {
@@ -711,14 +723,35 @@ __global__ void __launch_bounds__(kReduceCols) reduce_kernel(ReduceArgs a, StopC
     *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(a.u) + (size_t)row * a.d + 4 * c) = w;
     return;
   }
-  // sampled token of an accepted row: the Gumbel search's winner; it has none
-  // only when the probabilities are not finite: then the token is kept
-  if (threadIdx.x == 0 && a.acc[row] && canvas_active(ctl.stop_at, row / a.C, ctl.step)) {
-    const int bi = a.gidx[row];
-    if (bi >= 0 && bi < a.V)
-      a.tokens[row] = bi;
-    else
-      atomicExch(a.status, kStatusValue);
+  // sampled token of an accepted row: the best (score, lowest index) over the
+  // chunks, one warp
+  if (threadIdx.x < 32 && a.acc[row] && canvas_active(ctl.stop_at, row / a.C, ctl.step)) {
+    float best = -FLT_MAX;
+    int bi = INT_MAX;
+    for (int s = threadIdx.x; s < a.nchunks; s += 32) {
+      const float v = a.gbest[(size_t)s * a.M + row];
+      const int i = a.gidx[(size_t)s * a.M + row];
+      if (v > best || (v == best && i < bi)) {
+        best = v;
+        bi = i;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float b2 = __shfl_xor_sync(0xffffffffu, best, o);
+      const int i2 = __shfl_xor_sync(0xffffffffu, bi, o);
+      if (b2 > best || (b2 == best && i2 < bi)) {
+        best = b2;
+        bi = i2;
+      }
+    }
+    // no candidate only when the probabilities are not finite: keep the token
+    if (threadIdx.x == 0) {
+      if (bi >= 0 && bi < a.V)
+        a.tokens[row] = bi;
+      else
+        atomicExch(a.status, kStatusValue);
+    }
   }
 }
 
